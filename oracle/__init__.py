@@ -1,0 +1,167 @@
+"""fp64 CPU oracle for the gated delta rule -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package. The CUDA library never uses it and it never uses the CUDA library:
+the two share no code. Inputs come from the seeded generator module, which both sides use.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, one thread per (b, h, column block)).
+This file only compiles it on first use and marshals numpy arrays in and out.
+
+What each function computes (pages cited by title and section):
+  recurrence      -- the per-token recurrence of "RFC: HyperParallel Linear Attention
+                     Context Parallel", section 2.1: residual_t = beta_t (v_t - k_t @ H),
+                     H <- exp(g_t) H + outer(k_t, residual_t), o_t = q_t @ H.
+  summary         -- the per-segment affine summary H_out = M @ H_in + S (RFC 2.2), built
+                     token by token in rank-1 form from M = I, S = 0.
+  compose / scan  -- M = M1 @ M0, S = M1 @ S0 + S1 (RFC 2.2; "Context Parallelism in ART",
+                     section 08 "Then parallelize across GPUs"), scanned exclusively in
+                     segment order from h0.
+  chunked_fwd / chunked_summary -- the chunk equations of "Context Parallelism in ART",
+                     section 08 "First parallelize within a GPU", restated for the RFC's
+                     un-decayed read; used only to pin chunked == per-token.
+
+Pins: every function here is checked against closed forms, brute force on tiny inputs and
+invariants in tests/test_oracle.py (no function is "parity unpinned").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+
+
+def build(force: bool = False) -> str:
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_recurrence.argtypes = [_I] * 6 + [_P] * 9 + [_I, _I]
+        lib.oracle_summary.argtypes = [_I] * 6 + [_P] * 6 + [_I]
+        lib.oracle_compose.argtypes = [_I, _I] + [_P] * 6
+        lib.oracle_scan.argtypes = [_I] * 4 + [_P] * 4
+        lib.oracle_chunked_fwd.argtypes = [_I] * 6 + [_P] * 8 + [_I]
+        lib.oracle_chunked_summary.argtypes = [_I] * 7 + [_P] * 6 + [_I]
+        lib.oracle_num_threads.argtypes = [_I]
+        lib.oracle_num_threads.restype = _I
+        for fn in ("oracle_recurrence", "oracle_summary", "oracle_compose", "oracle_scan",
+                   "oracle_chunked_fwd", "oracle_chunked_summary"):
+            getattr(lib, fn).restype = None
+        _lib = lib
+    return _lib
+
+
+def _f32(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def num_threads(nthreads: int = 0) -> int:
+    return _load().oracle_num_threads(nthreads)
+
+
+def recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
+               nthreads: int = 0, want_o: bool = True):
+    """Per-token recurrence. Returns (o [B,T,H,V], h_final [B,H,K,V], H_in or None).
+
+    If seg_len > 0, H_in [T//seg_len, B, H, K, V] holds the state entering each segment.
+    """
+    q, k, v, g, beta, h0 = map(_f32, (q, k, v, g, beta, h0))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.empty((B, T, H, V), np.float64) if want_o else None
+    hf = np.empty((B, H, K, V), np.float64)
+    H_in = np.empty((T // seg_len, B, H, K, V), np.float64) if seg_len > 0 else None
+    _load().oracle_recurrence(B, T, H, K, V, seg_len, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                              _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), _ptr(H_in), col_block,
+                              nthreads)
+    return o, hf, H_in
+
+
+def summary(k, v, g, beta, nseg: int, nthreads: int = 0):
+    """Per-segment summaries (M [nseg,B,H,K,K], S [nseg,B,H,K,V]), rank-1 token updates."""
+    k, v, g, beta = map(_f32, (k, v, g, beta))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    assert T % nseg == 0
+    M = np.empty((nseg, B, H, K, K), np.float64)
+    S = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_summary(B, T, H, K, V, nseg, _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(M), _ptr(S), nthreads)
+    return M, S
+
+
+def compose(M1, S1, M0, S0):
+    """(M0,S0) then (M1,S1): returns (M1 @ M0, M1 @ S0 + S1) for one head."""
+    M1, S1, M0, S0 = map(_f64, (M1, S1, M0, S0))
+    K, V = S1.shape
+    M = np.empty((K, K), np.float64)
+    S = np.empty((K, V), np.float64)
+    _load().oracle_compose(K, V, _ptr(M1), _ptr(S1), _ptr(M0), _ptr(S0), _ptr(M), _ptr(S))
+    return M, S
+
+
+def scan(M, S, h0=None):
+    """Exclusive in-order scan: H_in[0] = h0, H_in[s] = M[s-1] @ H_in[s-1] + S[s-1].
+
+    M [nseg, B, H, K, K], S [nseg, B, H, K, V], h0 [B, H, K, V] or None (zero).
+    """
+    M, S, h0 = _f64(M), _f64(S), _f64(h0)
+    nseg, B, H, K, V = S.shape
+    H_in = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_scan(nseg, B * H, K, V, _ptr(M), _ptr(S), _ptr(h0), _ptr(H_in))
+    return H_in
+
+
+def chunked_fwd(q, k, v, g, beta, h0=None, chunk: int = 64, nthreads: int = 0):
+    q, k, v, g, beta, h0 = map(_f32, (q, k, v, g, beta, h0))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    o = np.empty((B, T, H, V), np.float64)
+    hf = np.empty((B, H, K, V), np.float64)
+    _load().oracle_chunked_fwd(B, T, H, K, V, chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), nthreads)
+    return o, hf
+
+
+def chunked_summary(k, v, g, beta, nseg: int, chunk: int = 64, nthreads: int = 0):
+    k, v, g, beta = map(_f32, (k, v, g, beta))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    assert T % nseg == 0
+    M = np.empty((nseg, B, H, K, K), np.float64)
+    S = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_chunked_summary(B, T, H, K, V, chunk, nseg, _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(M), _ptr(S), nthreads)
+    return M, S

@@ -1,0 +1,499 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU reference for the gated delta rule.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark load this file's library. The CUDA library never includes, links or calls
+ * it, and this file uses nothing of the CUDA library: the two share no code.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [RFC]  "RFC: HyperParallel Linear Attention Context Parallel", section 2.1 (the
+ *          per-token recurrence) and section 2.2 (the affine summary H_out = M@H_in + S
+ *          and its compose rule).
+ *   [ART]  "Context Parallelism in ART", section 08 "Gated DeltaNet context
+ *          parallelism", sub-sections "First parallelize within a GPU" (chunk
+ *          equations) and "Then parallelize across GPUs" (summary, compose, scan).
+ *
+ * Conventions. One (b,h) head has a K x V state H. Inputs are float arrays holding the
+ * values exactly as stored (bf16 inputs arrive already rounded); every operation here is
+ * done in double. Layouts (row-major, contiguous):
+ *   q, k : [B, T, H, K]     v, o : [B, T, H, V]     g, beta : [B, T, H]
+ *   states h0, h_final : [B, H, K, V]
+ *   summaries M : [nseg, B, H, K, K],  S : [nseg, B, H, K, V]
+ *
+ * Readings of the pages that this file takes (each listed in the design notes):
+ *   - the recurrence reads the un-decayed state H_{t-1} ([RFC] 2.1), so the per-token
+ *     transition is exp(g_t) I - beta_t k_t k_t^T;
+ *   - g is a natural-log decay (exp(g_t)); no query scale;
+ *   - segments are contiguous, equal length, in token order; segment 0 starts from h0.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------------------ */
+/* a tiny work queue over "units": each thread takes the next unit index atomically      */
+/* ------------------------------------------------------------------------------------ */
+typedef void (*unit_fn)(void* ctx, long unit);
+typedef struct {
+    unit_fn fn;
+    void* ctx;
+    long n_units;
+    long next;
+    pthread_mutex_t lock;
+} pool_t;
+
+static void* pool_worker(void* arg) {
+    pool_t* p = (pool_t*)arg;
+    for (;;) {
+        pthread_mutex_lock(&p->lock);
+        long u = p->next++;
+        pthread_mutex_unlock(&p->lock);
+        if (u >= p->n_units) break;
+        p->fn(p->ctx, u);
+    }
+    return NULL;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static void run_units(unit_fn fn, void* ctx, long n_units, int nthreads) {
+    pool_t p;
+    p.fn = fn;
+    p.ctx = ctx;
+    p.n_units = n_units;
+    p.next = 0;
+    pthread_mutex_init(&p.lock, NULL);
+    int nt = resolve_threads(nthreads);
+    if (nt > n_units) nt = (int)n_units;
+    if (nt <= 1) {
+        pool_worker(&p);
+    } else {
+        pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nt);
+        for (int i = 0; i < nt; ++i) pthread_create(&th[i], NULL, pool_worker, &p);
+        for (int i = 0; i < nt; ++i) pthread_join(th[i], NULL);
+        free(th);
+    }
+    pthread_mutex_destroy(&p.lock);
+}
+
+int oracle_num_threads(int nthreads) { return resolve_threads(nthreads); }
+
+/* ------------------------------------------------------------------------------------ */
+/* 1. Per-token recurrence ([RFC] 2.1), literally:                                        */
+/*      residual_t = beta_t * (v_t - k_t @ H_{t-1})                                      */
+/*      H_t        = exp(g_t) * H_{t-1} + outer(k_t, residual_t)                          */
+/*      o_t        = q_t @ H_t                                                           */
+/* Column v of H only ever meets column v of the value vectors, so the columns are       */
+/* independent recurrences; a work unit is one (b, h, block of columns).                 */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V, seg_len, col_block;
+    const float *q, *k, *v, *g, *beta, *h0;
+    double *o, *h_final, *H_in;
+} rec_ctx;
+
+static void rec_unit(void* vctx, long unit) {
+    const rec_ctx* c = (const rec_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T;
+    const int nblk = (V + c->col_block - 1) / c->col_block;
+    const int blk = (int)(unit % nblk);
+    const long bh = unit / nblk;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const int c0 = blk * c->col_block;
+    const int nc = (c0 + c->col_block <= V) ? c->col_block : V - c0;
+
+    double* S = (double*)malloc(sizeof(double) * (size_t)K * (size_t)nc); /* S[kk][cc] */
+    double* kt = (double*)malloc(sizeof(double) * (size_t)K);
+    double* qt = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int kk = 0; kk < K; ++kk)
+        for (int cc = 0; cc < nc; ++cc)
+            S[(size_t)kk * nc + cc] =
+                c->h0 ? (double)c->h0[(((size_t)b * H + h) * K + kk) * V + c0 + cc] : 0.0;
+
+    for (int t = 0; t < T; ++t) {
+        const size_t row = ((size_t)b * T + t) * H + h;
+        if (c->H_in && c->seg_len > 0 && t % c->seg_len == 0) {
+            const int s = t / c->seg_len;
+            const size_t base = (((size_t)s * c->B + b) * H + h) * (size_t)K * V;
+            for (int kk = 0; kk < K; ++kk)
+                for (int cc = 0; cc < nc; ++cc)
+                    c->H_in[base + (size_t)kk * V + c0 + cc] = S[(size_t)kk * nc + cc];
+        }
+        const double decay = exp((double)c->g[row]);
+        const double bt = (double)c->beta[row];
+        for (int kk = 0; kk < K; ++kk) {
+            kt[kk] = (double)c->k[row * K + kk];
+            qt[kk] = (double)c->q[row * K + kk];
+        }
+        for (int cc = 0; cc < nc; ++cc) {
+            /* k_t @ H_{t-1}, column cc */
+            double read = 0.0;
+            for (int kk = 0; kk < K; ++kk) read += kt[kk] * S[(size_t)kk * nc + cc];
+            const double resid = bt * ((double)c->v[row * V + c0 + cc] - read);
+            /* H_t = exp(g_t) H_{t-1} + k_t residual_t^T, then o_t = q_t @ H_t */
+            double out = 0.0;
+            for (int kk = 0; kk < K; ++kk) {
+                double* s = &S[(size_t)kk * nc + cc];
+                *s = decay * (*s) + kt[kk] * resid;
+                out += qt[kk] * (*s);
+            }
+            if (c->o) c->o[row * V + c0 + cc] = out;
+        }
+    }
+    if (c->h_final)
+        for (int kk = 0; kk < K; ++kk)
+            for (int cc = 0; cc < nc; ++cc)
+                c->h_final[(((size_t)b * H + h) * K + kk) * V + c0 + cc] = S[(size_t)kk * nc + cc];
+    free(S);
+    free(kt);
+    free(qt);
+}
+
+/* seg_len > 0 and H_in != NULL: H_in[s] receives the state entering token s*seg_len.
+ * col_block <= 0 means all V columns in one unit.                                       */
+void oracle_recurrence(int B, int T, int H, int K, int V, int seg_len, const float* q,
+                       const float* k, const float* v, const float* g, const float* beta,
+                       const float* h0, double* o, double* h_final, double* H_in,
+                       int col_block, int nthreads) {
+    rec_ctx c = {B, T, H, K, V, seg_len, col_block > 0 ? col_block : V,
+                 q, k, v, g, beta, h0, o, h_final, H_in};
+    const long nblk = (V + c.col_block - 1) / c.col_block;
+    run_units(rec_unit, &c, (long)B * H * nblk, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 2. Segment summary ([RFC] 2.2): H_out = M @ H_in + S for one contiguous segment.      */
+/* Substituting H_{t-1} = M H_in + S into the recurrence gives the per-token update      */
+/*   x = k^T M,  y = k^T S                                                               */
+/*   M <- exp(g) M - beta k x^T                                                          */
+/*   S <- exp(g) S - beta k y^T + beta k v^T                                             */
+/* starting from M = I, S = 0 (rank-1 form; no K^3 products).                            */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V, nseg;
+    const float *k, *v, *g, *beta;
+    double *M, *S;
+} sum_ctx;
+
+static void sum_unit(void* vctx, long unit) {
+    const sum_ctx* c = (const sum_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T;
+    const int seg_len = T / c->nseg;
+    const int s = (int)(unit % c->nseg);
+    const long bh = unit / c->nseg;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    double* M = c->M + (((size_t)s * c->B + b) * H + h) * (size_t)K * K;
+    double* S = c->S + (((size_t)s * c->B + b) * H + h) * (size_t)K * V;
+    double* x = (double*)malloc(sizeof(double) * (size_t)K);
+    double* y = (double*)malloc(sizeof(double) * (size_t)V);
+    double* kt = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < K; ++j) M[(size_t)i * K + j] = (i == j) ? 1.0 : 0.0;
+    for (size_t i = 0; i < (size_t)K * V; ++i) S[i] = 0.0;
+
+    for (int t = s * seg_len; t < (s + 1) * seg_len; ++t) {
+        const size_t row = ((size_t)b * T + t) * H + h;
+        const double decay = exp((double)c->g[row]);
+        const double bt = (double)c->beta[row];
+        for (int i = 0; i < K; ++i) kt[i] = (double)c->k[row * K + i];
+        for (int j = 0; j < K; ++j) {
+            double a = 0.0;
+            for (int i = 0; i < K; ++i) a += kt[i] * M[(size_t)i * K + j];
+            x[j] = a;
+        }
+        for (int j = 0; j < V; ++j) {
+            double a = 0.0;
+            for (int i = 0; i < K; ++i) a += kt[i] * S[(size_t)i * V + j];
+            y[j] = a;
+        }
+        for (int i = 0; i < K; ++i) {
+            const double bk = bt * kt[i];
+            for (int j = 0; j < K; ++j) M[(size_t)i * K + j] = decay * M[(size_t)i * K + j] - bk * x[j];
+            for (int j = 0; j < V; ++j)
+                S[(size_t)i * V + j] =
+                    decay * S[(size_t)i * V + j] - bk * y[j] + bk * (double)c->v[row * V + j];
+        }
+    }
+    free(x);
+    free(y);
+    free(kt);
+}
+
+void oracle_summary(int B, int T, int H, int K, int V, int nseg, const float* k, const float* v,
+                    const float* g, const float* beta, double* M, double* S, int nthreads) {
+    sum_ctx c = {B, T, H, K, V, nseg, k, v, g, beta, M, S};
+    run_units(sum_unit, &c, (long)B * H * nseg, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 3. Compose ([RFC] 2.2; [ART] "Then parallelize across GPUs"): segment 0 then          */
+/* segment 1 is  M = M1 @ M0,  S = M1 @ S0 + S1.  One (b,h) pair.                         */
+/* ------------------------------------------------------------------------------------ */
+void oracle_compose(int K, int V, const double* M1, const double* S1, const double* M0,
+                    const double* S0, double* M, double* S) {
+    for (int i = 0; i < K; ++i) {
+        for (int j = 0; j < K; ++j) {
+            double a = 0.0;
+            for (int l = 0; l < K; ++l) a += M1[(size_t)i * K + l] * M0[(size_t)l * K + j];
+            M[(size_t)i * K + j] = a;
+        }
+        for (int j = 0; j < V; ++j) {
+            double a = S1[(size_t)i * V + j];
+            for (int l = 0; l < K; ++l) a += M1[(size_t)i * K + l] * S0[(size_t)l * V + j];
+            S[(size_t)i * V + j] = a;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 4. Exclusive in-order scan of segment summaries: H_in[0] = h0 (zero when NULL),        */
+/* H_in[s] = M[s-1] @ H_in[s-1] + S[s-1]. "Every segment starts from the previous         */
+/* segment's final state" ([RFC] 2.1 last paragraph; [ART] prefix scan, made exclusive). */
+/* BH = B*H heads; M [nseg,BH,K,K], S/H_in [nseg,BH,K,V], h0 [BH,K,V].                    */
+/* ------------------------------------------------------------------------------------ */
+void oracle_scan(int nseg, int BH, int K, int V, const double* M, const double* S,
+                 const double* h0, double* H_in) {
+    const size_t kk = (size_t)K * K, kv = (size_t)K * V;
+    for (int bh = 0; bh < BH; ++bh) {
+        double* first = H_in + (size_t)bh * kv;
+        for (size_t i = 0; i < kv; ++i) first[i] = h0 ? h0[(size_t)bh * kv + i] : 0.0;
+        for (int s = 1; s < nseg; ++s) {
+            const double* Mp = M + ((size_t)(s - 1) * BH + bh) * kk;
+            const double* Sp = S + ((size_t)(s - 1) * BH + bh) * kv;
+            const double* Hp = H_in + ((size_t)(s - 1) * BH + bh) * kv;
+            double* Hn = H_in + ((size_t)s * BH + bh) * kv;
+            for (int i = 0; i < K; ++i)
+                for (int j = 0; j < V; ++j) {
+                    double a = Sp[(size_t)i * V + j];
+                    for (int l = 0; l < K; ++l) a += Mp[(size_t)i * K + l] * Hp[(size_t)l * V + j];
+                    Hn[(size_t)i * V + j] = a;
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 5. Chunked form ([ART] 08, "First parallelize within a GPU"), restated for the         */
+/* un-decayed read of [RFC] 2.1. Within one chunk of c tokens, with G_i the inclusive    */
+/* cumulative sum of g inside the chunk and Gx_i = G_i - g_i the exclusive one:          */
+/*   P[i,j] = exp(Gx_i - G_j) (k_i . k_j)  for j < i         (decay-weighted key Gram)    */
+/*   A      = (I + diag(beta) P)^{-1}                         (unit lower triangular)     */
+/*   U      = A diag(beta) V,   W = A diag(beta) Kr,   Kr_i = exp(Gx_i) k_i              */
+/*   R      = U - W H_start                                  (corrected values)           */
+/*   C[i,j] = exp(G_i - G_j) (q_i . k_j)  for j <= i                                     */
+/*   O      = Qd H_start + C R,   Qd_i = exp(G_i) q_i                                     */
+/*   H_end  = exp(G_last) H_start + Kd^T R,   Kd_j = exp(G_last - G_j) k_j               */
+/* and the chunk's own summary  M_n = exp(G_last) I - Kd^T W,  E_n = Kd^T U.              */
+/* This exists to pin "chunked == per-token" and to expose chunk intermediates.         */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V, chunk, nseg;
+    const float *q, *k, *v, *g, *beta, *h0;
+    double *o, *h_final, *M, *S;
+} chk_ctx;
+
+/* forward substitution for A = (I + L)^{-1}, L strictly lower (n x n, row-major) */
+static void unit_lower_inverse(int n, const double* L, double* A) {
+    for (int j = 0; j < n; ++j) {
+        for (int i = 0; i < n; ++i) A[(size_t)i * n + j] = 0.0;
+        A[(size_t)j * n + j] = 1.0;
+        for (int i = j + 1; i < n; ++i) {
+            double a = 0.0;
+            for (int l = j; l < i; ++l) a += L[(size_t)i * n + l] * A[(size_t)l * n + j];
+            A[(size_t)i * n + j] = -a;
+        }
+    }
+}
+
+/* One chunk: reads Hs (K x V), writes O rows (if o != NULL), overwrites Hs with H_end.
+ * If Mn/En are non-NULL, also writes the chunk summary.                                 */
+static void chunk_step(const chk_ctx* c, int b, int h, int t0, int n, double* Hs, double* Mn,
+                       double* En, double* work) {
+    const int K = c->K, V = c->V, H = c->H;
+    double* G = work;                     /* n   */
+    double* Gx = G + n;                   /* n   */
+    double* bt = Gx + n;                  /* n   */
+    double* kd = bt + n;                  /* n*K */
+    double* qd = kd + (size_t)n * K;      /* n*K */
+    double* vd = qd + (size_t)n * K;      /* n*V */
+    double* L = vd + (size_t)n * V;       /* n*n */
+    double* A = L + (size_t)n * n;        /* n*n */
+    double* Cm = A + (size_t)n * n;       /* n*n */
+    double* U = Cm + (size_t)n * n;       /* n*V */
+    double* W = U + (size_t)n * V;        /* n*K */
+    double* R = W + (size_t)n * K;        /* n*V */
+    double acc = 0.0;
+    for (int i = 0; i < n; ++i) {
+        const size_t row = ((size_t)b * c->T + t0 + i) * H + h;
+        const double gi = (double)c->g[row];
+        Gx[i] = acc;
+        acc += gi;
+        G[i] = acc;
+        bt[i] = (double)c->beta[row];
+        for (int j = 0; j < K; ++j) {
+            kd[(size_t)i * K + j] = (double)c->k[row * K + j];
+            qd[(size_t)i * K + j] = c->q ? (double)c->q[row * K + j] : 0.0;
+        }
+        for (int j = 0; j < V; ++j) vd[(size_t)i * V + j] = (double)c->v[row * V + j];
+    }
+    const double Glast = G[n - 1];
+    /* L = diag(beta) P */
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < n; ++j) {
+            double p = 0.0, cq = 0.0;
+            if (j < i) {
+                double d = 0.0;
+                for (int l = 0; l < K; ++l) d += kd[(size_t)i * K + l] * kd[(size_t)j * K + l];
+                p = exp(Gx[i] - G[j]) * d;
+            }
+            if (j <= i) {
+                double d = 0.0;
+                for (int l = 0; l < K; ++l) d += qd[(size_t)i * K + l] * kd[(size_t)j * K + l];
+                cq = exp(G[i] - G[j]) * d;
+            }
+            L[(size_t)i * n + j] = bt[i] * p;
+            Cm[(size_t)i * n + j] = cq;
+        }
+    unit_lower_inverse(n, L, A);
+    /* U = A diag(beta) V ; W = A diag(beta) Kr */
+    for (int i = 0; i < n; ++i) {
+        for (int j = 0; j < V; ++j) {
+            double a = 0.0;
+            for (int l = 0; l <= i; ++l) a += A[(size_t)i * n + l] * bt[l] * vd[(size_t)l * V + j];
+            U[(size_t)i * V + j] = a;
+        }
+        for (int j = 0; j < K; ++j) {
+            double a = 0.0;
+            for (int l = 0; l <= i; ++l)
+                a += A[(size_t)i * n + l] * bt[l] * exp(Gx[l]) * kd[(size_t)l * K + j];
+            W[(size_t)i * K + j] = a;
+        }
+    }
+    /* R = U - W Hs */
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < V; ++j) {
+            double a = U[(size_t)i * V + j];
+            for (int l = 0; l < K; ++l) a -= W[(size_t)i * K + l] * Hs[(size_t)l * V + j];
+            R[(size_t)i * V + j] = a;
+        }
+    /* O = Qd Hs + C R */
+    if (c->o) {
+        for (int i = 0; i < n; ++i) {
+            const size_t row = ((size_t)b * c->T + t0 + i) * H + h;
+            for (int j = 0; j < V; ++j) {
+                double a = 0.0;
+                for (int l = 0; l < K; ++l) a += qd[(size_t)i * K + l] * Hs[(size_t)l * V + j];
+                a *= exp(G[i]);
+                for (int l = 0; l <= i; ++l) a += Cm[(size_t)i * n + l] * R[(size_t)l * V + j];
+                c->o[row * V + j] = a;
+            }
+        }
+    }
+    /* chunk summary, M_n = exp(G_last) I - Kd^T W, E_n = Kd^T U */
+    if (Mn && En) {
+        for (int r = 0; r < K; ++r) {
+            for (int j = 0; j < K; ++j) {
+                double a = (r == j) ? exp(Glast) : 0.0;
+                for (int l = 0; l < n; ++l)
+                    a -= exp(Glast - G[l]) * kd[(size_t)l * K + r] * W[(size_t)l * K + j];
+                Mn[(size_t)r * K + j] = a;
+            }
+            for (int j = 0; j < V; ++j) {
+                double a = 0.0;
+                for (int l = 0; l < n; ++l)
+                    a += exp(Glast - G[l]) * kd[(size_t)l * K + r] * U[(size_t)l * V + j];
+                En[(size_t)r * V + j] = a;
+            }
+        }
+    }
+    /* H_end = exp(G_last) Hs + Kd^T R */
+    for (int r = 0; r < K; ++r)
+        for (int j = 0; j < V; ++j) {
+            double a = exp(Glast) * Hs[(size_t)r * V + j];
+            for (int l = 0; l < n; ++l)
+                a += exp(Glast - G[l]) * kd[(size_t)l * K + r] * R[(size_t)l * V + j];
+            Hs[(size_t)r * V + j] = a;
+        }
+}
+
+static size_t chunk_work_doubles(int n, int K, int V) {
+    return (size_t)3 * n + (size_t)n * K * 3 + (size_t)n * V * 3 + (size_t)n * n * 3;
+}
+
+static void chk_fwd_unit(void* vctx, long unit) {
+    const chk_ctx* c = (const chk_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H;
+    const int b = (int)(unit / H), h = (int)(unit % H);
+    double* Hs = (double*)malloc(sizeof(double) * (size_t)K * V);
+    double* work = (double*)malloc(sizeof(double) * chunk_work_doubles(c->chunk, K, V));
+    for (int kk = 0; kk < K; ++kk)
+        for (int j = 0; j < V; ++j)
+            Hs[(size_t)kk * V + j] = c->h0 ? (double)c->h0[(((size_t)b * H + h) * K + kk) * V + j] : 0.0;
+    for (int t0 = 0; t0 < c->T; t0 += c->chunk) {
+        const int n = (t0 + c->chunk <= c->T) ? c->chunk : c->T - t0;
+        chunk_step(c, b, h, t0, n, Hs, NULL, NULL, work);
+    }
+    if (c->h_final)
+        for (size_t i = 0; i < (size_t)K * V; ++i)
+            c->h_final[((size_t)b * H + h) * (size_t)K * V + i] = Hs[i];
+    free(Hs);
+    free(work);
+}
+
+/* Chunked forward from h0 over all T tokens (the last chunk may be short). */
+void oracle_chunked_fwd(int B, int T, int H, int K, int V, int chunk, const float* q, const float* k,
+                        const float* v, const float* g, const float* beta, const float* h0,
+                        double* o, double* h_final, int nthreads) {
+    chk_ctx c = {B, T, H, K, V, chunk, 1, q, k, v, g, beta, h0, o, h_final, NULL, NULL};
+    run_units(chk_fwd_unit, &c, (long)B * H, nthreads);
+}
+
+static void chk_sum_unit(void* vctx, long unit) {
+    const chk_ctx* c = (const chk_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H;
+    const int seg_len = c->T / c->nseg;
+    const int s = (int)(unit % c->nseg);
+    const long bh = unit / c->nseg;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    double* Mseg = c->M + (((size_t)s * c->B + b) * H + h) * (size_t)K * K;
+    double* Sseg = c->S + (((size_t)s * c->B + b) * H + h) * (size_t)K * V;
+    double* Mn = (double*)malloc(sizeof(double) * (size_t)K * K);
+    double* En = (double*)malloc(sizeof(double) * (size_t)K * V);
+    double* Mt = (double*)malloc(sizeof(double) * (size_t)K * K);
+    double* St = (double*)malloc(sizeof(double) * (size_t)K * V);
+    double* Hs = (double*)malloc(sizeof(double) * (size_t)K * V);
+    double* work = (double*)malloc(sizeof(double) * chunk_work_doubles(c->chunk, K, V));
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < K; ++j) Mseg[(size_t)i * K + j] = (i == j) ? 1.0 : 0.0;
+    for (size_t i = 0; i < (size_t)K * V; ++i) Sseg[i] = 0.0;
+    for (int t0 = s * seg_len; t0 < (s + 1) * seg_len; t0 += c->chunk) {
+        const int n = (t0 + c->chunk <= (s + 1) * seg_len) ? c->chunk : (s + 1) * seg_len - t0;
+        for (size_t i = 0; i < (size_t)K * V; ++i) Hs[i] = 0.0;
+        chunk_step(c, b, h, t0, n, Hs, Mn, En, work);
+        /* segment-so-far (Mseg, Sseg) then this chunk (Mn, En) */
+        oracle_compose(K, V, Mn, En, Mseg, Sseg, Mt, St);
+        memcpy(Mseg, Mt, sizeof(double) * (size_t)K * K);
+        memcpy(Sseg, St, sizeof(double) * (size_t)K * V);
+    }
+    free(Mn);
+    free(En);
+    free(Mt);
+    free(St);
+    free(Hs);
+    free(work);
+}
+
+/* Per-segment summaries built from the chunk summaries (M_n, E_n) composed in order. */
+void oracle_chunked_summary(int B, int T, int H, int K, int V, int chunk, int nseg, const float* k,
+                            const float* v, const float* g, const float* beta, double* M,
+                            double* S, int nthreads) {
+    chk_ctx c = {B, T, H, K, V, chunk, nseg, NULL, k, v, g, beta, NULL, NULL, NULL, M, S};
+    run_units(chk_sum_unit, &c, (long)B * H * nseg, nthreads);
+}
