@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the GDN segmented forward (one JSON line on rank 0).
+
+A step is one whole gdn_segmented_fwd call -- segment summaries, exclusive scan, and every
+segment's chunked forward -- over one batch of the headline workload (B=2, H=32,
+T=32768, K=V=128, 4 segments, bf16 inputs, fp32 state and output), inputs already
+resident in HBM. Inputs (~0.8 GB) and output (1 GB) are larger than the 129 MB L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the method's plain definition) on the host
+cores, a bounded sample of the same workload per step.
+Under torchrun (N > 1) every rank runs its own batch (weak scaling; no data-path
+collective); timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN segmented fwd tokens/s at H32 K=V=128 T=32K bf16; % of roofline"
+DEFAULT_WORKLOAD = "cp4_b2_h32_t32k"
+L2_BYTES = 129 * 1024 * 1024
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (host logic; tested on CPU with gloo)
+# ---------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def reduce_max(x: float, device="cpu") -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[int(str(device).split(":")[1])])
+        else:
+            dist.barrier()
+
+
+def aggregate(tokens_per_rank_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: tokens all ranks processed / the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / max_seconds
+
+
+def rank_seed_offset(rank: int) -> int:
+    return 0x1000 * rank
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic model of the path (bytes and flops per launch)
+# ---------------------------------------------------------------------------------------
+def algorithmic(w, out_bytes: int = 4):
+    """Compulsory HBM bytes and dense-contraction flops of each stage for workload w."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    BH = w.B * w.H
+    tok_heads = w.B * w.T * w.H
+    sum_tok_heads = tok_heads * (w.nseg - 1) // w.nseg
+    chunks = tok_heads // 64
+    sum_chunks = sum_tok_heads // 64
+    K, V = w.K, w.V
+    kv_state = BH * K * V * 4
+    kk_state = BH * K * K * 4
+    stages = {
+        "summary": {
+            "bytes": sum_tok_heads * ((K + V) * isz + 2 * isz) + (w.nseg - 1) * (kk_state + kv_state),
+            # prep (K K^T, U, W) + augmented K x (K+V) state update per chunk
+            "flops": sum_chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K
+                                   + 2 * 2 * 64 * K * (K + V)),
+        },
+        "scan": {
+            "bytes": (w.nseg - 1) * (kk_state + kv_state) + w.nseg * kv_state + kv_state,
+            "flops": (w.nseg - 1) * BH * 2 * K * K * V,
+        },
+        "forward": {
+            "bytes": tok_heads * ((2 * K + V) * isz + 2 * isz + V * out_bytes)
+            + w.nseg * kv_state + kv_state,
+            # prep (K K^T, U, W) + state (W H, Kd^T R) + output (Q K^T, Qd H, C R)
+            "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K
+                               + 2 * 64 * K * V * 2
+                               + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V),
+        },
+    }
+    total = {"bytes": sum(s["bytes"] for s in stages.values()),
+             "flops": sum(s["flops"] for s in stages.values())}
+    return stages, total
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "context_scan_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    if kv.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        rows = list(csv.reader(io.StringIO(text)))
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from context_scan_gb300 import gdn, synth
+
+    world, rank = init_dist("nccl" if args.gpus > 1 else "gloo")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w0 = synth.WORKLOADS[args.workload]
+    w = synth.scaled(w0, seed=w0.seed + rank_seed_offset(rank),
+                     per_sequence_seed=(None if w0.per_sequence_seed is None
+                                        else w0.per_sequence_seed + rank_seed_offset(rank)))
+    x = synth.make_inputs(w)
+    dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    names = ("q", "k", "v", "g", "beta")
+    host = {n: torch.from_numpy(x[n]).to(dt).pin_memory() for n in names}
+    host["h0"] = None if x["h0"] is None else torch.from_numpy(x["h0"]).pin_memory()
+    d = {n: (None if t is None else t.to(dev, non_blocking=False)) for n, t in host.items()}
+    o = torch.empty((w.B, w.T, w.H, w.V), dtype=torch.float32, device=dev)
+    hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    prob = gdn.problem(d["k"], d["v"], o)
+    ws = gdn.alloc_workspace(prob, w.nseg, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        if events is None:
+            gdn.gdn_segmented_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf,
+                                  w.nseg, ws, prob=prob, stream=stream)
+        else:
+            gdn.gdn_segmented_fwd_timed(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o,
+                                        hf, w.nseg, ws, events, prob=prob, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in ev:        # torch creates the CUDA event on first record; the library then
+        for e in e4:     # re-records the same handles inside each step
+            e.record(stream)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dev)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)   # let the sampler start before the timed region
+    t0.record(stream)
+    for i in range(K):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(dev)
+    elapsed = t0.elapsed_time(t1) / 1e3
+    max_elapsed = reduce_max(elapsed, device=dev if world > 1 else "cpu")
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
+
+    stage_ms = {"summary": [], "scan": [], "forward": []}
+    for e in ev:
+        stage_ms["summary"].append(e[0].elapsed_time(e[1]))
+        stage_ms["scan"].append(e[1].elapsed_time(e[2]))
+        stage_ms["forward"].append(e[2].elapsed_time(e[3]))
+    stages, total = algorithmic(w)
+    avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+    dominant = max(avg, key=avg.get)
+    peaks, peaks_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ach = stages[dominant]["bytes"] / (avg[dominant] * 1e-3) / 1e9
+    kernel_name = {"summary": "gdn_summary", "scan": "gdn_scan", "forward": "gdn_forward"}[dominant]
+    roofline = {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": recorded_traffic(kernel_name, w0.name),
+                "kernel": kernel_name, "kernel_ms": round(avg[dominant], 4),
+                "algorithmic_bytes": stages[dominant]["bytes"],
+                "peak_source": f"{peaks_src} hbm_gbs"}
+    t_roof = max(total["bytes"] / (hbm * 1e9),
+                 total["flops"] / (float(peaks["bf16_tflops"]) * 1e12))
+    ms_per_step = max_elapsed / K * 1e3
+    tokens = w.B * w.T
+    value = aggregate(tokens, K, world, max_elapsed)
+
+    # ---- end to end through the public API: pinned host -> device, call, device -> host
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = max(3, min(K, args.e2e_steps))
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hf_host = torch.empty(hf.shape, dtype=hf.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+        d2h = o_host.numel() * 4 + hf_host.numel() * 4
+
+        def e2e_step():
+            for n, t in host.items():
+                if t is not None:
+                    d[n].copy_(t, non_blocking=True)
+            step()
+            o_host.copy_(o, non_blocking=True)
+            hf_host.copy_(hf, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_el = reduce_max(a.elapsed_time(b) / 1e3, device=dev if world > 1 else "cpu")
+        e2e = {"value": round(aggregate(tokens, n_e2e, world, e_el), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, x, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w0.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
+                       "nseg": w.nseg, "chunk": 64, "in_dtype": w.in_dtype, "out_dtype": "f32",
+                       "state_dtype": "f32",
+                       "l2": f"inputs larger than L2 ({total_input_mb(w):.0f} MB in + "
+                             f"{w.B * w.T * w.H * w.V * 4 / 2**20:.0f} MB out > 129 MB); no flush",
+                       "parallelism": f"weak: {world} rank(s) x one batch each"},
+            "roofline": roofline,
+            "path_roofline": {"t_roof_us": round(t_roof * 1e6, 1),
+                              "frac": round(t_roof / (ms_per_step * 1e-3), 4),
+                              "bytes": total["bytes"], "flops": total["flops"],
+                              "peaks": f"{peaks_src}: hbm {hbm} GB/s, bf16 {peaks['bf16_tflops']} TF/s"},
+            "stage_ms": {k: round(v, 4) for k, v in avg.items()},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K if w.nseg > 1 else K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
+def total_input_mb(w):
+    isz = 2 if w.in_dtype == "bf16" else 4
+    return w.B * w.T * w.H * ((2 * w.K + w.V) * isz + 2 * isz) / 2**20
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle timed on the host cores (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------------------
+def oracle_heads(w, x, heads, nthreads=0):
+    """Run the oracle recurrence (o, h_final and the state entering every segment) on the
+    given (b, h) heads; returns seconds."""
+    import oracle
+    t = time.perf_counter()
+    for b, h in heads:
+        xs = {n: x[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+        h0 = None if x["h0"] is None else x["h0"][b:b + 1, h:h + 1]
+        oracle.recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], h0,
+                          seg_len=w.seg_len, col_block=8, nthreads=nthreads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    import oracle
+    cores = oracle.num_threads(0)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, secs = 0, 0.0
+    while done < len(heads) and secs < budget_s:
+        secs += oracle_heads(w, x, [heads[done]])
+        done += 1
+    value = w.B * w.T * done / len(heads) / secs
+    return {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {len(heads)} (b,h) heads of {w.name}, all T={w.T} tokens, "
+                      f"fp64 per-token recurrence with the state entering each of the "
+                      f"{w.nseg} segments; {secs:.1f} s; tokens/s scaled to the whole batch"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from context_scan_gb300 import synth
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    cores = oracle.num_threads(0)
+    for i in range(args.warmup):
+        oracle_heads(w, x, [heads[i % len(heads)]])
+    secs = 0.0
+    for i in range(args.steps):
+        secs += oracle_heads(w, x, [heads[(args.warmup + i) % len(heads)]])
+    # one step = one of the B*H heads; tokens/s scaled to the whole batch
+    value = w.B * w.T * args.steps / len(heads) / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
+                   "nseg": w.nseg, "in_dtype": w.in_dtype},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step: one (b,h) head of {w.name} ({w.T} tokens), "
+                                   f"fp64 per-token recurrence on {cores} host threads"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

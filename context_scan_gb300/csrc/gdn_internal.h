@@ -1,0 +1,56 @@
+// gdn_internal.h -- launch interface shared by the host API and the kernels (not public).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;
+
+// Device error word, at the start of the caller's workspace. The first error a kernel
+// records sticks (atomicCAS from 0); gdn_check_device_error reads and clears it.
+struct DeviceError {
+    unsigned code;    // 0 or a gdn_status value
+    unsigned detail;  // which wait gave up (kernel-specific tag)
+};
+
+// One launch of the chain kernels: every (b, h, segment) is an independent "chain" that
+// walks its segment's chunks in order, carrying the state on chip.
+struct ChainParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    // Initial state of each chain: h_start + seg * h_start_seg_stride + (b*H + h)*K*V,
+    // or zero when h_start == nullptr.
+    const float* h_start;
+    long long h_start_seg_stride;
+    void* o;           // forward: [B,T,H,V] out dtype
+    float* h_final;    // forward: written by chains whose segment is nseg_total-1 (nullable)
+    float* M;          // summary: [nseg_total,B,H,K,K]
+    float* S;          // summary: [nseg_total,B,H,K,V]
+    int B, T, H, K, V;
+    int seg_len;       // tokens per segment (multiple of 64)
+    int nseg_run;      // segments this launch processes: 0..nseg_run-1
+    int nseg_total;    // segments in the whole problem
+    int in_bf16;
+    int out_bf16;
+    DeviceError* err;
+};
+
+// fp32 CUDA-core kernels (any supported K/V, fp32 or bf16 inputs)
+cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s);
+cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
+cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
+                        int BH, int K, int V, cudaStream_t s);
+
+// tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
+bool tc_supported(const ChainParams& p);
+cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
+cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,348 @@
+// gdn_simt.cu -- fp32 CUDA-core kernels: the chunked forward, the segment summary and the
+// exclusive summary scan.
+//
+// These run every problem whose inputs are fp32 (exact fp32 arithmetic, no tensor cores:
+// the tensor cores' fp32 path would round operands to tf32) and bf16 problems with
+// K == V == 64. Each CTA owns one chain (b, h, segment) and a tile of CT state columns;
+// the columns of the state are independent, so tiles of one chain never communicate.
+//
+// Per chunk of 64 tokens (chunk equations of "Context Parallelism in ART", section 08,
+// "First parallelize within a GPU", with the un-decayed read of "RFC: HyperParallel Linear
+// Attention Context Parallel", section 2.1):
+//   G_i  = inclusive cumsum of g inside the chunk, Gx_i = G_i - g_i
+//   L    = diag(beta) P,  P[i,j] = exp(Gx_i - G_j) k_i.k_j  (j < i)
+//   A    = (I + L)^{-1}                 -- blocked: 16x16 diagonal blocks by forward
+//                                          substitution, then block forward substitution
+//   R    = A diag(beta) (V - diag(exp(Gx)) K H)      (= U - W H of the WY form)
+//   O    = diag(exp(G)) Q H + C R,  C[i,j] = exp(G_i - G_j) q_i.k_j  (j <= i)
+//   H   <- exp(G_last) H + sum_j exp(G_last - G_j) k_j R_j
+// The summary runs the same chunk step on the augmented K x (K+V) state [M | S], started
+// from [I | 0] with value vectors [0 | v_t] (RFC section 2.2: S is the state reached from
+// H_in = 0; M the linear part). Exponents are always differences of cumulative gates
+// (never exp(-G)), so wide gate spreads cannot overflow.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float load_in(const void* base, long long idx, int bf16) {
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+    return reinterpret_cast<const float*>(base)[idx];
+}
+
+__device__ __forceinline__ void store_out(void* base, long long idx, float x, int bf16) {
+    if (bf16)
+        reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(x);
+    else
+        reinterpret_cast<float*>(base)[idx] = x;
+}
+
+template <int KD, int CT, bool SUMMARY>
+struct SimtSmem {
+    static constexpr int KP = KD + 1;  // padded row of k / q
+    static constexpr int LP = 65;      // padded row of the 64x64 matrices
+    static constexpr int off_k = 0;
+    static constexpr int off_q = off_k + 64 * KP;
+    static constexpr int off_v = off_q + (SUMMARY ? 0 : 64 * KP);
+    static constexpr int off_h = off_v + 64 * CT;
+    static constexpr int off_l = off_h + KD * CT;
+    static constexpr int off_a = off_l + 64 * LP;
+    static constexpr int off_c = off_a + 64 * LP;
+    static constexpr int off_y = off_c + (SUMMARY ? 0 : 64 * LP);
+    static constexpr int off_r = off_y + 64 * CT;
+    static constexpr int off_s = off_r + 64 * CT;  // scalars: 6 x 64
+    static constexpr int total = off_s + 6 * 64;
+    static constexpr size_t bytes = sizeof(float) * total;
+};
+
+template <int KD, int CT, bool SUMMARY>
+__global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
+    using L = SimtSmem<KD, CT, SUMMARY>;
+    extern __shared__ float sm[];
+    float* ks = sm + L::off_k;
+    float* qs = sm + L::off_q;
+    float* vs = sm + L::off_v;
+    float* Hs = sm + L::off_h;
+    float* Ls = sm + L::off_l;
+    float* As = sm + L::off_a;
+    float* Cs = sm + L::off_c;
+    float* Ys = sm + L::off_y;
+    float* Rs = sm + L::off_r;
+    float* gam = sm + L::off_s;
+    float* gx = gam + 64;
+    float* bet = gx + 64;
+    float* dk = bet + 64;   // exp(G_last - G_j)
+    float* eq = dk + 64;    // exp(G_i)
+    float* ekr = eq + 64;   // exp(Gx_i)
+    constexpr int KP = L::KP, LP = L::LP;
+
+    const int tid = threadIdx.x;
+    const int chain = blockIdx.x;
+    const int seg = chain % p.nseg_run;
+    const int bh = chain / p.nseg_run;
+    const int b = bh / p.H, h = bh % p.H;
+    const int c0 = blockIdx.y * CT;   // first state column of this tile
+    const int V = p.V, H = p.H, T = p.T;
+
+    // ---- initial state tile
+    for (int e = tid; e < KD * CT; e += kThreads) {
+        const int l = e / CT, c = e % CT;
+        float x = 0.f;
+        if (SUMMARY) {
+            x = (c0 + c == l) ? 1.f : 0.f;   // [I | 0]
+        } else if (p.h_start) {
+            x = p.h_start[(long long)seg * p.h_start_seg_stride +
+                          ((long long)bh * KD + l) * V + c0 + c];
+        }
+        Hs[e] = x;
+    }
+
+    const int t_begin = seg * p.seg_len;
+    const int n_chunks = p.seg_len / kChunk;
+    for (int ch = 0; ch < n_chunks; ++ch) {
+        const int t0 = t_begin + ch * kChunk;
+        // ---- (1) load the chunk
+        for (int e = tid; e < 64 * KD; e += kThreads) {
+            const int i = e / KD, l = e % KD;
+            const long long row = ((long long)b * T + t0 + i) * H + h;
+            ks[i * KP + l] = load_in(p.k, row * KD + l, p.in_bf16);
+            if (!SUMMARY) qs[i * KP + l] = load_in(p.q, row * KD + l, p.in_bf16);
+        }
+        for (int e = tid; e < 64 * CT; e += kThreads) {
+            const int i = e / CT, c = e % CT;
+            const long long row = ((long long)b * T + t0 + i) * H + h;
+            const int gc = c0 + c;
+            float x;
+            if (SUMMARY)
+                x = (gc < KD) ? 0.f : load_in(p.v, row * V + (gc - KD), p.in_bf16);
+            else
+                x = load_in(p.v, row * V + gc, p.in_bf16);
+            vs[e] = x;
+        }
+        if (tid < 64) {
+            const long long row = ((long long)b * T + t0 + tid) * H + h;
+            gx[tid] = load_in(p.g, row, p.in_bf16);   // raw gate for now
+            bet[tid] = load_in(p.beta, row, p.in_bf16);
+        }
+        __syncthreads();
+        // ---- (2) gate cumsum inside the chunk (one warp; two gates per lane)
+        if (tid < 32) {
+            const float a0 = gx[2 * tid], a1 = gx[2 * tid + 1];
+            float s = a0 + a1;
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, s, off);
+                if (tid >= off) s += o;
+            }
+            const float excl = s - (a0 + a1);
+            gam[2 * tid] = excl + a0;
+            gam[2 * tid + 1] = excl + a0 + a1;
+            gx[2 * tid] = excl;              // Gx_i = G_i - g_i
+            gx[2 * tid + 1] = excl + a0;
+        }
+        __syncthreads();
+        const float glast = gam[63];
+        if (tid < 64) {
+            dk[tid] = expf(glast - gam[tid]);
+            eq[tid] = expf(gam[tid]);
+            ekr[tid] = expf(gx[tid]);
+        }
+        // ---- (3) L = diag(beta) P and C; clear A
+        for (int e = tid; e < 64 * 64; e += kThreads) {
+            const int i = e / 64, j = e % 64;
+            float lv = 0.f, cv = 0.f;
+            if (j < i) {
+                float d = 0.f;
+#pragma unroll 8
+                for (int l = 0; l < KD; ++l) d = fmaf(ks[i * KP + l], ks[j * KP + l], d);
+                lv = bet[i] * expf(gx[i] - gam[j]) * d;
+            }
+            if (!SUMMARY && j <= i) {
+                float d = 0.f;
+#pragma unroll 8
+                for (int l = 0; l < KD; ++l) d = fmaf(qs[i * KP + l], ks[j * KP + l], d);
+                cv = expf(gam[i] - gam[j]) * d;
+            }
+            Ls[i * LP + j] = lv;
+            if (!SUMMARY) Cs[i * LP + j] = cv;
+            As[i * LP + j] = 0.f;
+        }
+        __syncthreads();
+        // ---- (4a) inverses of the four 16x16 diagonal blocks of I + L
+        if (tid < 64) {
+            const int base = (tid / 16) * 16, c = tid % 16;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 1; r < 16; ++r) {
+                float a = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) a = fmaf(Ls[(base + r) * LP + base + m], x[m], a);
+                if (r > c) x[r] = -a;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) As[(base + r) * LP + base + c] = x[r];
+        }
+        __syncthreads();
+        // ---- (4b) block forward substitution: X_IJ = -inv(T_II) * sum_{m=J}^{I-1} L_Im X_mJ
+        {
+            float* Yb = Ys;   // scratch, 3 blocks of 16x16 (Ys is free until step 5)
+            const int r = tid / 16, c = tid % 16;
+            for (int I = 1; I < 4; ++I) {
+                for (int J = 0; J < I; ++J) {
+                    float a = 0.f;
+                    for (int m = J; m < I; ++m) {
+#pragma unroll
+                        for (int l = 0; l < 16; ++l)
+                            a = fmaf(Ls[(16 * I + r) * LP + 16 * m + l],
+                                     As[(16 * m + l) * LP + 16 * J + c], a);
+                    }
+                    Yb[J * 256 + r * 16 + c] = a;
+                }
+                __syncthreads();
+                for (int J = 0; J < I; ++J) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int l = 0; l < 16; ++l)
+                        a = fmaf(As[(16 * I + r) * LP + 16 * I + l], Yb[J * 256 + l * 16 + c], a);
+                    As[(16 * I + r) * LP + 16 * J + c] = -a;
+                }
+                __syncthreads();
+            }
+        }
+        // ---- (5) Y = diag(beta) (V - diag(exp(Gx)) K H)
+        for (int e = tid; e < 64 * CT; e += kThreads) {
+            const int i = e / CT, c = e % CT;
+            float a = 0.f;
+#pragma unroll 8
+            for (int l = 0; l < KD; ++l) a = fmaf(ks[i * KP + l], Hs[l * CT + c], a);
+            Ys[e] = bet[i] * (vs[e] - ekr[i] * a);
+        }
+        __syncthreads();
+        // ---- (6) R = A Y
+        for (int e = tid; e < 64 * CT; e += kThreads) {
+            const int i = e / CT, c = e % CT;
+            float a = 0.f;
+            for (int j = 0; j <= i; ++j) a = fmaf(As[i * LP + j], Ys[j * CT + c], a);
+            Rs[e] = a;
+        }
+        __syncthreads();
+        // ---- (7) O = diag(exp(G)) Q H + C R
+        if (!SUMMARY) {
+            for (int e = tid; e < 64 * CT; e += kThreads) {
+                const int i = e / CT, c = e % CT;
+                float a = 0.f;
+#pragma unroll 8
+                for (int l = 0; l < KD; ++l) a = fmaf(qs[i * KP + l], Hs[l * CT + c], a);
+                float bsum = 0.f;
+                for (int j = 0; j <= i; ++j) bsum = fmaf(Cs[i * LP + j], Rs[j * CT + c], bsum);
+                const long long row = ((long long)b * T + t0 + i) * H + h;
+                store_out(p.o, row * V + c0 + c, fmaf(eq[i], a, bsum), p.out_bf16);
+            }
+            __syncthreads();
+        }
+        // ---- (8) H <- exp(G_last) H + sum_j exp(G_last - G_j) k_j R_j
+        const float dlast = expf(glast);
+        for (int e = tid; e < KD * CT; e += kThreads) {
+            const int l = e / CT, c = e % CT;
+            float a = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < 64; ++j) a = fmaf(dk[j] * ks[j * KP + l], Rs[j * CT + c], a);
+            Hs[e] = fmaf(dlast, Hs[e], a);
+        }
+        __syncthreads();
+    }
+
+    // ---- write the chain's final state
+    if (SUMMARY) {
+        const long long base = (long long)seg * p.B * H + bh;
+        for (int e = tid; e < KD * CT; e += kThreads) {
+            const int l = e / CT, c = e % CT;
+            const int gc = c0 + c;
+            if (gc < KD)
+                p.M[(base * KD + l) * KD + gc] = Hs[e];
+            else
+                p.S[(base * KD + l) * V + (gc - KD)] = Hs[e];
+        }
+    } else if (p.h_final && seg == p.nseg_total - 1) {
+        for (int e = tid; e < KD * CT; e += kThreads) {
+            const int l = e / CT, c = e % CT;
+            p.h_final[((long long)bh * KD + l) * V + c0 + c] = Hs[e];
+        }
+    }
+}
+
+template <int KD, bool SUMMARY>
+cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
+    constexpr int CT = 32;
+    using L = SimtSmem<KD, CT, SUMMARY>;
+    auto kern = simt_chain_kernel<KD, CT, SUMMARY>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    const int ncols = SUMMARY ? KD + p.V : p.V;
+    dim3 grid((unsigned)(p.B * p.H * p.nseg_run), (unsigned)(ncols / CT));
+    kern<<<grid, kThreads, L::bytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Exclusive scan H_in[0] = h0, H_in[s] = M[s-1] H_in[s-1] + S[s-1], fp32, one CTA per
+// (head, 32-column tile); the serial dependency runs over segments inside the CTA.
+__global__ void __launch_bounds__(kThreads)
+scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
+            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int K,
+            int V) {
+    extern __shared__ float sm[];
+    constexpr int CT = 32;
+    float* Hc = sm;            // K x CT
+    float* Hn = sm + K * CT;   // K x CT
+    const int bh = blockIdx.x, c0 = blockIdx.y * CT, tid = threadIdx.x;
+    for (int e = tid; e < K * CT; e += kThreads) {
+        const int l = e / CT, c = e % CT;
+        Hc[e] = h0 ? h0[((long long)bh * K + l) * V + c0 + c] : 0.f;
+    }
+    __syncthreads();
+    for (int s = 0; s < nseg; ++s) {
+        const long long hb = ((long long)s * BH + bh) * K;
+        for (int e = tid; e < K * CT; e += kThreads) {
+            const int l = e / CT, c = e % CT;
+            H_in[(hb + l) * V + c0 + c] = Hc[e];
+        }
+        if (s == nseg - 1) break;
+        const float* Ms = M + ((long long)s * BH + bh) * K * K;
+        const float* Ss = S + ((long long)s * BH + bh) * K * V;
+        for (int e = tid; e < K * CT; e += kThreads) {
+            const int i = e / CT, c = e % CT;
+            float a = Ss[(long long)i * V + c0 + c];
+            for (int l = 0; l < K; ++l) a = fmaf(__ldg(&Ms[(long long)i * K + l]), Hc[l * CT + c], a);
+            Hn[e] = a;
+        }
+        __syncthreads();
+        for (int e = tid; e < K * CT; e += kThreads) Hc[e] = Hn[e];
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s) {
+    return p.K == 128 ? launch_chain<128, false>(p, s) : launch_chain<64, false>(p, s);
+}
+
+cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s) {
+    return p.K == 128 ? launch_chain<128, true>(p, s) : launch_chain<64, true>(p, s);
+}
+
+cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
+                        int BH, int K, int V, cudaStream_t s) {
+    const size_t smem = sizeof(float) * 2 * K * 32;
+    dim3 grid((unsigned)BH, (unsigned)(V / 32));
+    scan_kernel<<<grid, kThreads, smem, s>>>(M, S, h0, H_in, nseg, BH, K, V);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,164 @@
+"""Thin ctypes binding of the C ABI in include/gdn.h (argument marshalling only).
+
+Every function here takes torch tensors that already live on the GPU, checks nothing
+beyond what marshalling needs, passes raw device pointers plus the current CUDA stream to
+``libgdn.so`` and raises ``GdnError`` on a non-OK status. All validation and all compute
+happen in the library's CUDA kernels; there is no fallback of any kind. If ``libgdn.so``
+has not been built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgdn.so")
+
+GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
+          3: "GDN_ERR_UNSUPPORTED_DTYPE", 4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_WORKSPACE",
+          6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
+EXPORTED = ("gdn_workspace_bytes", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
+            "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_status_string",
+            "gdn_check_device_error")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} "
+                         f"({lib().gdn_status_string(status).decode()})")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("K", ctypes.c_int), ("V", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def lib():
+    """Load libgdn.so (raises OSError if it is missing: build it with __graft_entry__.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"libgdn.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        pp = ctypes.POINTER(Problem)
+        L.gdn_workspace_bytes.argtypes = [pp, ctypes.c_int]
+        L.gdn_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_chunk_fwd.argtypes = [pp] + [_P] * 9 + [ctypes.c_size_t, _P]
+        L.gdn_segment_summary.argtypes = [pp, ctypes.c_int] + [_P] * 7 + [ctypes.c_size_t, _P]
+        L.gdn_summary_scan.argtypes = [pp, ctypes.c_int] + [_P] * 5
+        L.gdn_segmented_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+        L.gdn_segmented_fwd_timed.argtypes = ([pp, ctypes.c_int] + [_P] * 10 +
+                                              [ctypes.c_size_t, _P, _P])
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
+        for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
+                   "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_check_device_error"):
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return GDN_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return GDN_DTYPE_BF16
+    return 99   # the library rejects it with GDN_ERR_UNSUPPORTED_DTYPE
+
+
+def problem(q_or_k, v, o=None, chunk: int = 64) -> Problem:
+    B, T, H, K = q_or_k.shape
+    V = v.shape[-1]
+    out = GDN_DTYPE_F32 if o is None else _dtype_code(o)
+    return Problem(B, T, H, K, V, chunk, _dtype_code(q_or_k), out)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise GdnError(status, where)
+
+
+def workspace_bytes(prob: Problem, nseg: int = 1) -> int:
+    return int(lib().gdn_workspace_bytes(ctypes.byref(prob), nseg))
+
+
+def alloc_workspace(prob: Problem, nseg: int = 1, device="cuda"):
+    """A zeroed workspace tensor of the size the library asks for (torch owns the memory)."""
+    import torch
+    n = workspace_bytes(prob, nseg)
+    if n == 0:
+        raise GdnError(2, "gdn_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, h0, o, h_final, workspace, stream=None, prob=None):
+    prob = prob or problem(k, v, o)
+    _check(lib().gdn_chunk_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final), _ptr(workspace),
+                               workspace.numel() if workspace is not None else 0,
+                               _stream(stream)), "gdn_chunk_fwd")
+
+
+def gdn_segment_summary(k, v, g, beta, M, S, nseg, workspace, stream=None, prob=None):
+    prob = prob or problem(k, v)
+    _check(lib().gdn_segment_summary(ctypes.byref(prob), nseg, _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(beta), _ptr(M), _ptr(S), _ptr(workspace),
+                                     workspace.numel() if workspace is not None else 0,
+                                     _stream(stream)), "gdn_segment_summary")
+
+
+def gdn_summary_scan(M, S, h0, H_in, stream=None, prob=None):
+    nseg, B, H, K, V = H_in.shape
+    prob = prob or Problem(B, 0, H, K, V, 64, GDN_DTYPE_F32, GDN_DTYPE_F32)
+    _check(lib().gdn_summary_scan(ctypes.byref(prob), nseg, _ptr(M), _ptr(S), _ptr(h0),
+                                  _ptr(H_in), _stream(stream)), "gdn_summary_scan")
+
+
+def gdn_segmented_fwd(q, k, v, g, beta, h0, o, h_final, nseg, workspace, H_in=None,
+                      stream=None, prob=None):
+    prob = prob or problem(k, v, o)
+    _check(lib().gdn_segmented_fwd(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
+                                   _ptr(H_in), _ptr(workspace),
+                                   workspace.numel() if workspace is not None else 0,
+                                   _stream(stream)), "gdn_segmented_fwd")
+
+
+def gdn_segmented_fwd_timed(q, k, v, g, beta, h0, o, h_final, nseg, workspace, events,
+                            H_in=None, stream=None, prob=None):
+    """gdn_segmented_fwd recording four torch.cuda.Event (enable_timing=True) around its
+    three stages: before summary, before scan, before forward, after forward."""
+    prob = prob or problem(k, v, o)
+    arr = (_P * 4)(*[e.cuda_event for e in events])
+    _check(lib().gdn_segmented_fwd_timed(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                                         _ptr(h_final), _ptr(H_in), _ptr(workspace),
+                                         workspace.numel() if workspace is not None else 0,
+                                         _stream(stream), arr), "gdn_segmented_fwd_timed")
+
+
+def gdn_check_device_error(workspace, stream=None):
+    """Synchronises, returns (status, detail) from the workspace's device error word."""
+    detail = ctypes.c_uint(0)
+    st = lib().gdn_check_device_error(_ptr(workspace), _stream(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)

@@ -1,0 +1,160 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunkwise Gated DeltaNet forward with per-segment
+ * affine state summaries.
+ *
+ * The operation (per batch b and head h; K x V fp32 state H):
+ *   residual_t = beta_t * (v_t - k_t @ H_{t-1})
+ *   H_t        = exp(g_t) * H_{t-1} + outer(k_t, residual_t)
+ *   o_t        = q_t @ H_t
+ * -- "RFC: HyperParallel Linear Attention Context Parallel", section 2.1. The state reads
+ * the un-decayed H_{t-1}; g is a natural-log decay; there is no query scale.
+ * Computed in chunks of 64 tokens (gate cumsum, chunk K K^T, lower-triangular solve, WY
+ * form, inter-chunk state scan, output) -- "Context Parallelism in ART", section 08,
+ * "First parallelize within a GPU".
+ * A contiguous segment of tokens acts on its incoming state as H_out = M @ H_in + S, with
+ * M [K,K] and S [K,V]; two segments in order compose as M = M1 @ M0, S = M1 @ S0 + S1
+ * (associative, not commutative) -- RFC section 2.2; ART section 08, "Then parallelize
+ * across GPUs". Segments play the role of the pages' context-parallel ranks, here all on
+ * one GPU.
+ *
+ * ---------------------------------------------------------------------------------------
+ * Conventions shared by every call
+ * ---------------------------------------------------------------------------------------
+ * Layouts (row-major, contiguous, no strides):
+ *   q, k     [B, T, H, K]        in_dtype
+ *   v        [B, T, H, V]        in_dtype
+ *   g, beta  [B, T, H]           in_dtype
+ *   o        [B, T, H, V]        out_dtype
+ *   h0, h_final                  [B, H, K, V]           fp32
+ *   M                            [nseg, B, H, K, K]     fp32   ((M@X)[i,v] = sum_j M[i,j] X[j,v])
+ *   S, H_in                      [nseg, B, H, K, V]     fp32
+ * Segment s covers tokens [s*T/nseg, (s+1)*T/nseg) of every sequence.
+ *
+ * Supported set (anything else returns an error and launches nothing):
+ *   chunk == 64; K == V and K in {64, 128}; B, H >= 1; T >= 0; T % (64*nseg) == 0;
+ *   1 <= nseg (and nseg <= T/64 when T > 0); B*T*H*max(K,V) < 2^40.
+ *   in_dtype  in {GDN_DTYPE_F32, GDN_DTYPE_BF16}; out_dtype in {GDN_DTYPE_F32, GDN_DTYPE_BF16}.
+ *   bf16 inputs with K == V == 128 run the tcgen05 tensor-core kernels (fp32 accumulation);
+ *   fp32 inputs, and bf16 inputs with K == V == 64, run the fp32 CUDA-core kernels.
+ *   Every device pointer must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
+ *
+ * Ownership: the caller allocates every buffer (device memory) and keeps it alive until the
+ * stream work completes. The library allocates nothing, keeps no state between calls and
+ * never synchronises the stream, except gdn_check_device_error.
+ *
+ * Workspace: a caller-provided device buffer of at least gdn_workspace_bytes() bytes, whose
+ * first 256 bytes must be zero before the first call that uses it (it holds the device
+ * error word, see gdn_check_device_error). Calls that share a workspace must not overlap.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Every call is
+ * asynchronous on that stream. The returned status covers argument validation and launch
+ * errors only; faults the kernels detect on the device (a bounded wait that ran out) are
+ * recorded in the workspace's error word and reported by gdn_check_device_error.
+ *
+ * There is no CPU fallback: a call either launches its CUDA kernels or returns an error.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,       /* NULL required pointer, bad count, bad nseg */
+    GDN_ERR_UNSUPPORTED_SHAPE = 2, /* K/V/chunk/T outside the supported set */
+    GDN_ERR_UNSUPPORTED_DTYPE = 3, /* dtype code outside the supported set */
+    GDN_ERR_MISALIGNED = 4,        /* a device pointer is not 16-byte aligned */
+    GDN_ERR_WORKSPACE = 5,         /* workspace NULL or smaller than gdn_workspace_bytes() */
+    GDN_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
+    GDN_ERR_TIMEOUT = 7,           /* a kernel's bounded wait ran out (device error word) */
+    GDN_ERR_DEVICE = 8             /* the current device is not an sm_103 GPU */
+} gdn_status;
+
+typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+    int B, T, H, K, V;
+    int chunk;           /* tokens per chunk; must be 64 */
+    gdn_dtype in_dtype;  /* storage type of q, k, v, g, beta */
+    gdn_dtype out_dtype; /* storage type of o */
+} gdn_problem;
+
+/* Bytes of workspace the calls below need for this problem split into nseg segments
+ * (nseg = 1 for gdn_chunk_fwd and gdn_segment_summary). Returns 0 for an invalid problem. */
+GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
+
+/* Chunked forward over all T tokens from the initial state h0.
+ *   RFC section 2.1 (recurrence); ART section 08 "First parallelize within a GPU" (chunks).
+ *   h0       [B,H,K,V] fp32, or NULL for a zero initial state.
+ *   o        [B,T,H,V] out_dtype, written.
+ *   h_final  [B,H,K,V] fp32, the state after token T-1; NULL skips it.
+ * T == 0 writes only h_final (= h0, or zeros). */
+GDN_API gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const float* h0, void* o,
+                         float* h_final, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Affine summary of each of the nseg contiguous segments: H_out = M @ H_in + S.
+ *   RFC section 2.2: S is the state the segment reaches from H_in = 0 and M is its
+ *   linear action on any incoming state. Built chunk by chunk in WY form, so M is the
+ *   ordered product of the per-token factors exp(g_t) I - beta_t k_t k_t^T.
+ *   M [nseg,B,H,K,K] fp32 and S [nseg,B,H,K,V] fp32, written. */
+GDN_API gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const void* k, const void* v,
+                               const void* g, const void* beta, float* M, float* S,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Exclusive in-order prefix scan of segment summaries (RFC section 2.2 compose; ART
+ * section 08 prefix scan, made exclusive):
+ *   H_in[0] = h0 (zeros if h0 == NULL),  H_in[s] = M[s-1] @ H_in[s-1] + S[s-1].
+ *   M [nseg,B,H,K,K], S [nseg,B,H,K,V] fp32 in (M[nseg-1], S[nseg-1] are not read);
+ *   H_in [nseg,B,H,K,V] fp32 out. Computed in fp32 on CUDA cores. Only p->B, p->H, p->K,
+ *   p->V are read from the problem. */
+GDN_API gdn_status gdn_summary_scan(const gdn_problem* p, int nseg, const float* M, const float* S,
+                            const float* h0, float* H_in, void* stream);
+
+/* The segmented forward: summaries of segments 0..nseg-2, the exclusive scan, then every
+ * segment's chunked forward from its scanned H_in (RFC section 6.4.1/6.4.2 forward flow
+ * on one GPU). o and h_final equal gdn_chunk_fwd's up to rounding.
+ *   H_in_out [nseg,B,H,K,V] fp32: if non-NULL receives the scanned states; if NULL they
+ *   live in the workspace. Workspace: gdn_workspace_bytes(p, nseg). */
+GDN_API gdn_status gdn_segmented_fwd(const gdn_problem* p, int nseg, const void* q, const void* k,
+                             const void* v, const void* g, const void* beta, const float* h0,
+                             void* o, float* h_final, float* H_in_out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* gdn_segmented_fwd with stage markers, for timing each kernel from the caller. If
+ * stage_events is non-NULL it points to four cudaEvent_t that are recorded on `stream`
+ * before the summary launch, before the scan, before the forward launch and after it
+ * (for nseg == 1 the first three are recorded back to back). Same results as
+ * gdn_segmented_fwd. */
+GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q,
+                                           const void* k, const void* v, const void* g,
+                                           const void* beta, const float* h0, void* o,
+                                           float* h_final, float* H_in_out, void* workspace,
+                                           size_t workspace_bytes, void* stream,
+                                           void* const* stage_events);
+
+/* Static, NUL-terminated description of a status code. */
+GDN_API const char* gdn_status_string(gdn_status s);
+
+/* Synchronises `stream`, reads the workspace's device error word, clears it, and returns
+ * GDN_OK, GDN_ERR_TIMEOUT (a bounded wait ran out; the results of the affected calls are
+ * invalid) or GDN_ERR_CUDA. If `detail` is non-NULL it receives the recorded detail word
+ * (which wait gave up), or 0. */
+GDN_API gdn_status gdn_check_device_error(void* workspace, void* stream, unsigned* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every entry point include/gdn.h declares, and its host
+validation rejects bad problems before touching a GPU (no compute call runs here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from context_scan_gb300 import _build, gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build_cuda()
+    return gdn.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    declared = declared_symbols()
+    assert {"gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
+            "gdn_segmented_fwd"} <= declared
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    assert declared <= exported, declared - exported
+    for name in declared:
+        assert hasattr(L, name)
+    assert set(gdn.EXPORTED) <= declared
+
+
+def test_binding_arity_matches_header(L):
+    text = "".join(open(os.path.join(ROOT, "include", f)).read()
+                   for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    for m in re.finditer(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(([^)]*)\)", text):
+        name, params = m.group(1), m.group(2)
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        assert len(getattr(L, name).argtypes) == n, (name, n)
+
+
+def test_library_is_sm103a_only():
+    flags = " ".join(_build.NVCC_FLAGS)
+    assert "arch=compute_103a,code=sm_103a" in flags
+    assert flags.count("-gencode") == 1
+
+
+def P(**kw):
+    d = dict(B=1, T=128, H=2, K=128, V=128, chunk=64, in_dtype=1, out_dtype=0)
+    d.update(kw)
+    return gdn.Problem(**{k: d[k] for k in ("B", "T", "H", "K", "V", "chunk", "in_dtype",
+                                             "out_dtype")})
+
+
+def test_workspace_bytes_and_status_strings(L):
+    p = P(B=2, T=32768, H=32)
+    assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256
+    n4 = L.gdn_workspace_bytes(ctypes.byref(p), 4)
+    # M, S and H_in for 4 segments of 64 heads, fp32
+    assert n4 >= 256 + 4 * 64 * 128 * 128 * 4 * 3
+    assert L.gdn_workspace_bytes(ctypes.byref(P(K=96, V=96)), 1) == 0
+    assert L.gdn_workspace_bytes(ctypes.byref(P(T=100)), 1) == 0
+    assert L.gdn_workspace_bytes(ctypes.byref(P(T=128)), 4) == 0   # 128 % (64*4) != 0
+    for code in range(9):
+        assert L.gdn_status_string(code)
+    assert L.gdn_status_string(0) == b"ok"
+
+
+@pytest.mark.parametrize("prob,nseg,expect", [
+    (dict(chunk=32), 1, 2),
+    (dict(K=128, V=64), 1, 2),
+    (dict(K=256, V=256), 1, 2),
+    (dict(T=100), 1, 2),
+    (dict(T=192), 2, 2),
+    (dict(B=0), 1, 1),
+    (dict(T=-64), 1, 1),
+    (dict(in_dtype=7), 1, 3),
+    (dict(out_dtype=5), 1, 3),
+    (dict(), 0, 1),
+])
+def test_validation_rejects_before_launch(L, prob, nseg, expect):
+    p = P(**prob)
+    # all pointers NULL: every rejection here happens before pointers are examined or used
+    st = L.gdn_segmented_fwd(ctypes.byref(p), nseg, *([None] * 10), 0, None)
+    assert st == expect, gdn.STATUS.get(st)
+
+
+def test_null_pointers_and_missing_workspace_rejected(L):
+    p = P()
+    st = L.gdn_chunk_fwd(ctypes.byref(p), *([None] * 9), 0, None)
+    assert st == 1  # q/k/v/g/beta/o missing
+    st = L.gdn_segment_summary(ctypes.byref(p), 1, *([None] * 7), 0, None)
+    assert st == 1  # M/S missing
+    st = L.gdn_summary_scan(ctypes.byref(p), 2, None, None, None, None, None)
+    assert st == 1
+    st = L.gdn_check_device_error(None, None, None)
+    assert st == 5

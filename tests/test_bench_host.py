@@ -1,0 +1,78 @@
+"""Host logic of bench.py: the multi-rank path (gloo, world size 2, on CPU), the
+algorithmic byte/flop model, and the JSON contract of the reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from context_scan_gb300 import synth  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    w, r = bench.init_dist("gloo")
+    bench.barrier()
+    m = bench.reduce_max(1.0 + r)          # rank 1 is "slower"
+    value = bench.aggregate(tokens_per_rank_step=100, steps=4, world=w, max_seconds=m)
+    q.put((r, w, m, value, bench.rank_seed_offset(r)))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_weak_aggregate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    out.sort()
+    for r, w, m, value, off in out:
+        assert w == 2
+        assert m == 2.0                    # max over ranks
+        assert value == 100 * 4 * 2 / 2.0  # all ranks' tokens / slowest rank's time
+    assert out[0][4] != out[1][4]          # every rank draws its own batch
+
+
+def test_algorithmic_model_matches_hand_count():
+    w = synth.WORKLOADS["cp4_b2_h32_t32k"]
+    stages, total = bench.algorithmic(w)
+    tok_heads = 2 * 32768 * 32
+    # forward: q,k,v bf16 (3*128*2) + g,beta bf16 (2*2) in, o fp32 (128*4) out
+    assert stages["forward"]["bytes"] >= tok_heads * (772 + 512)
+    # summary reads k, v, g, beta of 3 of the 4 segments
+    assert stages["summary"]["bytes"] >= tok_heads * 3 // 4 * 516
+    t_roof = total["bytes"] / 6791.4e9
+    assert 520e-6 < t_roof < 540e-6
+
+
+@pytest.mark.parametrize("steps", [3])
+def test_reference_arm_json_line(steps):
+    env = dict(os.environ)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_f32_k64_cp4", "--steps", str(steps), "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
