@@ -19,8 +19,8 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
           3: "GDN_ERR_UNSUPPORTED_DTYPE", 4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_WORKSPACE",
           6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
 EXPORTED = ("gdn_workspace_bytes", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
-            "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_status_string",
-            "gdn_check_device_error")
+            "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
+            "gdn_status_string", "gdn_check_device_error")
 
 
 class GdnError(RuntimeError):
@@ -56,11 +56,13 @@ def lib():
         L.gdn_segmented_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
         L.gdn_segmented_fwd_timed.argtypes = ([pp, ctypes.c_int] + [_P] * 10 +
                                               [ctypes.c_size_t, _P, _P])
+        L.gdn_segmented_fwd_noalloc.argtypes = [pp, ctypes.c_int] + [_P] * 10
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
-                   "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_check_device_error"):
+                   "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
+                   "gdn_check_device_error"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -155,6 +157,18 @@ def gdn_segmented_fwd_timed(q, k, v, g, beta, h0, o, h_final, nseg, workspace, e
                                          _ptr(h_final), _ptr(H_in), _ptr(workspace),
                                          workspace.numel() if workspace is not None else 0,
                                          _stream(stream), arr), "gdn_segmented_fwd_timed")
+
+
+def gdn_segmented_fwd_noalloc(q, k, v, g, beta, h0, o, h_final, nseg, device_error=None,
+                              stream=None, prob=None):
+    """gdn_segmented_fwd with the library's fixed scratch array instead of a workspace.
+    device_error: optional int32/uint32 CUDA tensor of >= 2 elements that receives the
+    call's device error word {code, detail}."""
+    prob = prob or problem(k, v, o)
+    _check(lib().gdn_segmented_fwd_noalloc(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
+                                           _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                                           _ptr(h_final), _ptr(device_error), _stream(stream)),
+           "gdn_segmented_fwd_noalloc")
 
 
 def gdn_check_device_error(workspace, stream=None):

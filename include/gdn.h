@@ -144,6 +144,34 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
                                            size_t workspace_bytes, void* stream,
                                            void* const* stage_events);
 
+/* Size of the fixed scratch array behind gdn_segmented_fwd_noalloc (64 MiB). */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* gdn_segmented_fwd without a workspace, for callers that cannot allocate device memory:
+ * a host framework that owns all device memory through its own pool, a request path that
+ * must not pay an allocation's implicit synchronisation, or a program that only holds
+ * buffers imported from another process. (The pages have no counterpart: this is an
+ * interface choice of this library.)
+ *   Arguments and results are those of gdn_segmented_fwd, minus H_in_out and the
+ *   workspace. The scratch (summaries, scanned states, the device error word) lives in one
+ *   array of GDN_NOALLOC_SCRATCH_BYTES in the library's own device memory; every GPU that
+ *   loads the library holds it until the process exits. The call allocates nothing.
+ *   Limit: problems with gdn_workspace_bytes(p, nseg) > GDN_NOALLOC_SCRATCH_BYTES are
+ *   rejected with GDN_ERR_WORKSPACE (at K = V = 128: B*H*nseg at most 341).
+ *   device_error: optional (NULL to skip) 8-byte-aligned device pointer to two unsigned
+ *   words that receive this call's device error word {code, detail} (see
+ *   gdn_check_device_error for the codes) when the call's stream work completes.
+ *   First call on a device: it looks up that device's copy of the array
+ *   (cudaGetSymbolAddress) with the device current; make it before any stream capture.
+ *   All calls share the one array, which keeps the last call's contents (the call clears
+ *   the error word itself): calls that overlap on the GPU -- on different streams, or from
+ *   different host threads -- race on it and must be serialised by the caller. */
+GDN_API gdn_status gdn_segmented_fwd_noalloc(const gdn_problem* p, int nseg, const void* q,
+                                             const void* k, const void* v, const void* g,
+                                             const void* beta, const float* h0, void* o,
+                                             float* h_final, unsigned* device_error,
+                                             void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 GDN_API const char* gdn_status_string(gdn_status s);
 
