@@ -13,28 +13,30 @@
 //   L  = diag(beta) P,  P[i,j] = 2^(Gx_i - G_j) k_i.k_j (j < i);   A = (I + L)^-1
 //   U  = A diag(beta) V,   W = A diag(beta 2^Gx) K
 //   R  = U - W H
-//   O  = diag(2^G) Q H + C R,   C[i,j] = 2^(G_i - G_j) q_i.k_j (j <= i)
+//   O  = Qd H + C R,   Qd = diag(2^G) Q,   C[i,j] = 2^(G_i - G_j) q_i.k_j (j <= i)
 //   H <- 2^(G_last) H + sum_j 2^(G_last - G_j) k_j R_j
-// Every contraction is issued as an M = 128 tcgen05.mma (kind::f16, bf16 operands, fp32
-// accumulation in tensor memory) by putting a 128-wide dimension on M -- the products are
-// formed transposed:
-//   P1  S^T-free Gram: D[0:128, 0:64]   = [K ; Q] K^T         (rows 0..63 K K^T, 64..127 Q K^T)
-//   P2  U^T          = V^T (A diag(beta))^T
-//   P3  W^T          = K^T (A diag(beta 2^Gx))^T
-//   S1  R^T          = U^T + H^T (-W)^T    (accumulates onto U^T)
-//   S2  (Q H)^T      = H^T Q^T
-//   S3  (C R)^T      = R^T C^T
-//   S4  H^T         += (R^T diag(2^(G_last - G))) K   (state master pre-scaled by 2^G_last)
-// S1-S3 are kind::tf32 with the A operand (H^T, R^T) read straight from tensor memory, so
-// the fp32 state and the corrected values are never rounded to bf16; S4 feeds the decayed
-// R^T as an unevaluated bf16 sum hi + lo (two MMAs). P1-P3 and S4 are kind::f16 (bf16).
-// The triangular inverse, gate exponentials and the output combine run on CUDA cores.
-// Exponents are always differences of cumulative gates, never 2^-G.
+// Every contraction is an M = 128 tcgen05.mma with fp32 accumulation in tensor memory; a
+// 128-wide dimension (v or k) is put on M, so the products are formed transposed:
+//   P1  [K ; Q] K^T        rows 0..63: K K^T, rows 64..127: Q K^T      kind::f16 (bf16)
+//   P2  U^T = V^T (A diag(beta))^T                                      kind::f16
+//   P3  W^T = K^T (A diag(beta 2^Gx))^T                                 kind::f16
+//   S1  R^T = U^T + H^T (-W)^T      A = H^T from tensor memory          kind::tf32
+//   S2  O^T = H^T Qd^T              A = H^T from tensor memory          kind::tf32
+//   S3  O^T += R^T C^T              A = R^T from tensor memory          kind::tf32
+//   S4  H^T += (R^T diag(2^(G_last - G))) K, the decayed R^T held in tensor memory as an
+//       unevaluated bf16 sum hi + lo (two MMAs); the master is pre-scaled by 2^G_last.
+// The fp32 state and the corrected values R never pass through bf16. Exponents are always
+// differences of cumulative gates, never 2^-G. A = (I + L)^-1 is formed on chip: 16x16
+// diagonal blocks by forward substitution (rows in registers, shuffles), then three rounds
+// of block forward substitution on mma.sync (tf32).
 //
-// Warps 0-3 ("math") own tensor-memory lanes 0..127 and run the chunk step; warp 4 is the
-// producer (TMA loads of the q/k/v tiles, 128-byte swizzle, two stages; plain loads of the
-// gates). Every wait on an mbarrier is bounded: on expiry the kernel records
-// GDN_ERR_TIMEOUT in the device error word, drains what it issued and frees tensor memory.
+// Warp roles: warps 0-3 "state" (tensor-memory lanes 0..127; S1-S4, output, final state),
+// warps 4-7 "prep" (P1-P3, gate cumsum, L and C, the inverse, the WY operands), warp 8
+// "producer" (TMA loads of the q/k/v tiles with 128-byte swizzle into two stages; plain
+// loads of the gates). Prep of chunk n+1 runs while the state group works on chunk n. Each
+// group issues its own MMAs (commits track the issuing thread's MMAs). Every wait on an
+// mbarrier is bounded: on expiry the kernel records GDN_ERR_TIMEOUT in the device error
+// word, drains what it issued and frees tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -49,46 +51,49 @@ namespace {
 
 constexpr int kD = 128;        // K == V
 constexpr int kC = 64;         // tokens per chunk
-constexpr int kThreads = 160;  // 4 math warps + 1 producer warp
+constexpr int kThreads = 288;  // 4 state warps + 4 prep warps + 1 producer warp
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// tensor-memory columns (fp32 accumulators, 128 lanes each)
-constexpr uint32_t TM_S = 0;     // [K;Q] K^T, then W^T
-constexpr uint32_t TM_U0 = 64;   // U^T -> R^T (even chunks)
-constexpr uint32_t TM_U1 = 128;  // (odd chunks)
-constexpr uint32_t TM_OI = 192;  // H^T Q^T
-constexpr uint32_t TM_OA = 256;  // R^T C^T
-constexpr uint32_t TM_H = 320;   // state master H^T (128 columns)
+// tensor-memory columns (32-bit cells, 128 lanes)
+constexpr uint32_t TM_S = 0;     // [K;Q] K^T, then W^T                       (prep)
+constexpr uint32_t TM_U = 64;    // U^T -> R^T, two buffers by chunk parity   (64, 128)
+constexpr uint32_t TM_O = 192;   // O^T, two buffers by chunk parity          (192, 256)
+constexpr uint32_t TM_RD = 320;  // decayed R^T as packed bf16: hi 320..351, lo 352..383
+constexpr uint32_t TM_H = 384;   // state master H^T (128 columns)
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t SM_KQ0 = 0;        // stage 0: [khalf][K rows | Q rows] 2 x 16 KB
+constexpr uint32_t SM_KQ0 = 0;        // stage 0: [khalf][K rows | Q rows], 2 x 16 KB
 constexpr uint32_t SM_KQ1 = 32768;    // stage 1
 constexpr uint32_t SM_V = 65536;      // [vhalf][64 rows x 128 B]
-constexpr uint32_t SM_W = 81920;      // -W tf32, K-major: [kblock][64 rows (i) x 32 (k)];
-                                      // inverse scratch before that
-constexpr uint32_t SM_QT = 114688;    // Q tf32, K-major: [kblock][64 rows (i) x 32 (k)]
-constexpr uint32_t SM_RD = 147456;    // R^T diag(2^(G_last - G)) as bf16 hi (+0) and lo (+16 KB);
-                                      // before that, L (+0) and A (+16 KB) of the inverse, fp32
-constexpr uint32_t SM_AB = 180224;    // A diag(beta) bf16: 64 rows (i) x 64 (j)
-constexpr uint32_t SM_ABG = 188416;   // A diag(beta 2^Gx) bf16
-constexpr uint32_t SM_C = 196608;     // C tf32: [kblock][64 rows (i) x 32 (j)]
-constexpr uint32_t SM_SCAL = 212992;  // gates per stage + per-chunk scalars
-constexpr uint32_t SM_BAR = 216064;   // mbarriers, tmem base, abort flag
-constexpr uint32_t SM_END = 216128;
+constexpr uint32_t SM_W = 81920;      // -W tf32 K-major: [kblock 4][64 rows (i) x 32 (k)]
+constexpr uint32_t SM_QT = 114688;    // Qd tf32 K-major: [kblock 4][64 rows (i) x 32 (k)]
+constexpr uint32_t SM_C0 = 147456;    // C tf32 K-major: [kblock 2][64 rows (i) x 32 (j)], x2
+constexpr uint32_t SM_C1 = 163840;
+constexpr uint32_t SM_AB = 180224;    // A diag(beta) bf16 64 x 64; L fp32 (16 KB) before it
+constexpr uint32_t SM_ABG = 188416;   // A diag(beta 2^Gx) bf16 64 x 64
+constexpr uint32_t SM_AS = 196608;    // A fp32 64 x 64 (swizzled)
+constexpr uint32_t SM_YS = 212992;    // per-warp 16 x 8 fp32 scratch of the inverse (4 KB)
+constexpr uint32_t SM_SCAL = 217088;  // per-chunk scalars [parity 2][8][64] + gates [stage 2][2][64]
+constexpr uint32_t SM_BAR = 222208;   // mbarriers and flags
+constexpr uint32_t SM_END = 222336;
 constexpr uint32_t kSmemBytes = SM_END + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// 64 x 64 fp32 matrices of the inverse: row-major with the column XOR-swizzled by the row,
-// so both row-wise and column-wise walks by a warp hit 32 distinct banks
-__device__ __forceinline__ int sw64(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+// per-chunk scalar arrays (offsets in units of 64 floats within a parity block)
+enum { SC_GAM = 0, SC_GX, SC_DD, SC_BET, SC_BEKR, SC_EG, SC_MISC, SC_N = 8 };
 
-// mbarrier slots (8 bytes each) at SM_BAR
+// mbarrier slots and flags at SM_BAR
 constexpr uint32_t B_FULL0 = 0, B_FULL1 = 8, B_EMPTY0 = 16, B_EMPTY1 = 24, B_VEMPTY = 32,
-                   B_MMA = 40, B_TMEM = 48, B_ABORT = 52, B_GO = 56;
+                   B_BARP = 40, B_BARS = 48, B_PREPDONE = 56, B_WFREE = 64, B_UFREE0 = 72,
+                   B_UFREE1 = 80, B_TMEM = 88, B_ABORT = 92, B_GO_S = 96, B_GO_P = 100,
+                   B_VFULL = 104;
 
 // wait tags recorded in the device error word's detail field
-enum : unsigned { TAG_FULL = 1, TAG_MMA = 2, TAG_EMPTY = 3, TAG_VEMPTY = 4 };
+enum : unsigned {
+    TAG_FULL = 1, TAG_BARP = 2, TAG_BARS = 3, TAG_EMPTY = 4, TAG_VEMPTY = 5, TAG_PREPDONE = 6,
+    TAG_WFREE = 7, TAG_UFREE = 8, TAG_VFULL = 9
+};
 
 struct TcParams {
     CUtensorMap tm_q;
@@ -130,6 +135,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the hardware may suspend the waiting warp for up to `hint_ns`
+// nanoseconds until the phase completes, instead of the warp re-polling and taking issue
+// slots from the warps it shares a scheduler with.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void record_error(DeviceError* e, unsigned code, unsigned detail) {
     if (e && atomicCAS(&e->code, 0u, code) == 0u) atomicExch(&e->detail, detail);
 }
@@ -142,7 +163,9 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        // suspended in hardware (up to 20 us per try) rather than re-polling: a polling warp
+        // starves the compute warps on its scheduler
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > limit) {
             record_error(err, GDN_ERR_TIMEOUT, tag);
@@ -158,6 +181,25 @@ __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, long long
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > limit) return;
+}
+
+// The first warp of a warp group waits (when `doit`) -- all of its lanes poll together and
+// see identical values, so the warp stays converged -- and its lane 0 publishes a verdict
+// before the group's named barrier; every thread of the group then reads the same verdict,
+// so a timeout can never split the group between a barrier and a break.
+template <int BAR_ID>
+__device__ __forceinline__ bool group_wait(bool leader_warp, bool lane0, uint32_t bar,
+                                           uint32_t parity, bool doit, volatile int* go,
+                                           volatile int* abort_flag, long long limit,
+                                           DeviceError* err, unsigned tag) {
+    if (leader_warp) {
+        const bool ok = !doit || mbar_wait(bar, parity, abort_flag, limit, err, tag);
+        if (lane0) *go = (ok && !*abort_flag) ? 1 : 0;
+    }
+    if (BAR_ID == 1) asm volatile("barrier.sync 1, 128;" ::: "memory");
+    else asm volatile("barrier.sync 2, 128;" ::: "memory");
+    __syncwarp();   // the leader warp diverged around its poll: reconverge before .aligned work
+    return *go != 0;
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -178,11 +220,23 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void math_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void state_bar() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void prep_bar() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
+template <int ID>
+__device__ __forceinline__ void group_bar() {
+    if (ID == 1) state_bar();
+    else prep_bar();
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
     return y;
 }
 
@@ -196,7 +250,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     d |= (uint64_t)2 << 61;
     return d;
 }
-// K-major operand, rows of 128 bytes packed in 8-row groups of 1024 bytes
+// K-major operand: rows of 128 bytes packed in 8-row groups of 1024 bytes
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return sdesc(saddr, 16, 1024); }
 // MN-major operand: 64-element blocks along M/N `mn_stride` bytes apart, 8-row groups along
 // K 1024 bytes apart
@@ -204,21 +258,20 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t mn_stride) 
     return sdesc(saddr, mn_stride, 1024);
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-constexpr uint32_t idesc(int M, int N, bool a_mn, bool b_mn, bool a_neg) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_neg ? 1u : 0u) << 13) |
-           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptors (dense, fp32 D). kind::f16 with bf16 A and B:
+constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t ID_P1 = idesc(128, 64, false, false, false);
-constexpr uint32_t ID_P23 = idesc(128, 64, true, false, false);
-constexpr uint32_t ID_S4 = idesc(128, 128, false, true, false);
-// kind::tf32, fp32 D, M = 128, N = 64, A from tensor memory, B K-major (S1, S2, S3)
+constexpr uint32_t ID_P1 = idesc_bf16(128, 64, false, false);
+constexpr uint32_t ID_P23 = idesc_bf16(128, 64, true, false);
+constexpr uint32_t ID_S4 = idesc_bf16(128, 128, false, true);   // A from tensor memory
+// kind::tf32, M = 128, N = 64, A from tensor memory, B K-major (S1, S2, S3)
 constexpr uint32_t ID_TF = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                    uint32_t accumulate) {
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                       uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -227,8 +280,7 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
         : "memory");
 }
 
-// D (+)= A B with A read from tensor memory (tf32 operands, fp32 accumulation)
-__device__ __forceinline__ void mma_ta_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                             uint32_t id, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -238,10 +290,14 @@ __device__ __forceinline__ void mma_ta_tf32(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return __uint_as_float(y);
+__device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t id, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -250,41 +306,37 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
+// Tensor-memory accesses of this thread's lane: 16 or 8 consecutive 32-bit columns. The
+// kernel walks wide rows in rolled loops over such groups: each chunk executes its code
+// once, so compact loops (rather than fully unrolled rows) keep it in the instruction cache.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
         : "memory");
 }
 
@@ -300,24 +352,61 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// Write 8*nchunk consecutive values of one 128-byte row of a 128-byte-swizzled tile,
-// starting at 16-byte chunk c0 of the row (rows packed in 8-row groups of 1024 bytes).
-template <int NCHUNK>
-__device__ __forceinline__ void st_row_sw128(uint8_t* tile, int row, int c0, const float* v) {
-    uint8_t* rp = tile + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) {
-        uint4 pk;
-        pk.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
-        pk.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
-        pk.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
-        pk.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
-        *reinterpret_cast<uint4*>(rp + (((c0 + c) ^ (row & 7)) << 4)) = pk;
-    }
+// byte address of 16-byte chunk `c` of row `row` in a 128-byte-swizzled tile of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int row, int c) {
+    return (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
 }
 
 __device__ __forceinline__ float bf16_at(const void* base, long long idx) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
+}
+
+// 64 x 64 fp32 matrices of the inverse: row-major with the column XOR-swizzled by the row,
+// so both row-wise and column-wise walks by a warp hit 32 distinct banks
+__device__ __forceinline__ int sw64(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+
+// D = A B + D on the warp-level tensor path, m16n8k8, tf32 in, fp32 accumulate
+__device__ __forceinline__ void mma_m16n8k8(float* d, const uint32_t* a, const uint32_t* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// m16n8k8 fragments from swizzled fp32 64x64 matrices (rows r0.., cols c0..)
+__device__ __forceinline__ void frag_a(const float* M, int r0, int c0, int lane, uint32_t* a) {
+    const int g = lane >> 2, t = lane & 3;
+    a[0] = tf32_bits(M[sw64(r0 + g, c0 + t)]);
+    a[1] = tf32_bits(M[sw64(r0 + g + 8, c0 + t)]);
+    a[2] = tf32_bits(M[sw64(r0 + g, c0 + t + 4)]);
+    a[3] = tf32_bits(M[sw64(r0 + g + 8, c0 + t + 4)]);
+}
+__device__ __forceinline__ void frag_b(const float* M, int r0, int c0, int lane, uint32_t* b) {
+    const int g = lane >> 2, t = lane & 3;
+    b[0] = tf32_bits(M[sw64(r0 + t, c0 + g)]);
+    b[1] = tf32_bits(M[sw64(r0 + t + 4, c0 + g)]);
+}
+
+// 64 token rows of one output column from a 64-column O^T buffer in tensor memory
+__device__ __forceinline__ void store_o_rows(const ChainParams& c, uint32_t t_col, long long idx0,
+                                             long long tok_stride) {
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+        float ov[16];
+        tmem_ld16(t_col + 16 * g, ov);
+        tmem_wait_ld();
+        const long long base = idx0 + (long long)(16 * g) * tok_stride;
+        if (c.out_bf16) {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(c.o) + base;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[(long long)j * tok_stride] = __float2bfloat16_rn(ov[j]);
+        } else {
+            float* o = reinterpret_cast<float*>(c.o) + base;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[(long long)j * tok_stride] = ov[j];
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -330,17 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
 
-    float* gates = reinterpret_cast<float*>(sm + SM_SCAL);   // [stage][g | beta][64]
-    float* s_gam = gates + 256;   // G (log2 units)
-    float* s_gx = s_gam + 64;     // Gx
-    float* s_eg = s_gx + 64;      // 2^G
-    float* s_dd = s_eg + 64;      // 2^(G_last - G)
-    float* s_bet = s_dd + 64;     // beta
-    float* s_bekr = s_bet + 64;   // beta 2^Gx
-    float* s_misc = s_bekr + 64;  // [0] = 2^G_last
-    float* Ls = reinterpret_cast<float*>(sm + SM_RD);            // inverse only
-    float* As = reinterpret_cast<float*>(sm + SM_RD + 16384);    // inverse only
-    float* Yscr = reinterpret_cast<float*>(sm + SM_W);           // inverse only
+    float* scal = reinterpret_cast<float*>(sm + SM_SCAL);              // [parity][SC_N][64]
+    float* gates = reinterpret_cast<float*>(sm + SM_SCAL + 4096);      // [stage][g | beta][64]
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + SM_BAR + B_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + B_ABORT);
     const uint32_t bar0 = base + SM_BAR;
@@ -366,9 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         mbar_init(bar0 + B_EMPTY0, 1);
         mbar_init(bar0 + B_EMPTY1, 1);
         mbar_init(bar0 + B_VEMPTY, 1);
-        mbar_init(bar0 + B_MMA, 1);
+        mbar_init(bar0 + B_VFULL, 1);
+        mbar_init(bar0 + B_BARP, 1);
+        mbar_init(bar0 + B_BARS, 1);
+        mbar_init(bar0 + B_PREPDONE, 1);
+        mbar_init(bar0 + B_WFREE, 1);
+        mbar_init(bar0 + B_UFREE0, 1);
+        mbar_init(bar0 + B_UFREE1, 1);
         *abort_flag = 0;
-        *reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO) = 1;
+        *reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO_S) = 1;
+        *reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO_P) = 1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
@@ -384,25 +471,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ================================ producer ================================
-        const uint32_t tx = 16384u + (SUMMARY ? 0u : 16384u) + (need_v ? 16384u : 0u);
-        int issued_last[2] = {-1, -1};
+        // K and Q tiles (and the gates) go to a two-stage ring released after S4; the V tile
+        // has its own single buffer released after P2, so a chunk's K and Q are never held
+        // back by the previous chunk's V.
+        const uint32_t tx = 16384u + (SUMMARY ? 0u : 16384u);
+        int issued_last[2] = {-1, -1}, v_issued_last = -1;
+#pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             const uint32_t full = bar0 + (s ? B_FULL1 : B_FULL0);
-            // lane 0 waits; the warp follows its verdict, so the lanes never diverge
-            int ok = 1;
-            if (lane == 0) {
-                if (n >= 2)
-                    ok = mbar_wait(bar0 + (s ? B_EMPTY1 : B_EMPTY0), ((n >> 1) - 1) & 1,
-                                   abort_flag, limit, c.err, TAG_EMPTY);
-                if (ok && need_v && n >= 1)
-                    ok = mbar_wait(bar0 + B_VEMPTY, (n - 1) & 1, abort_flag, limit, c.err,
-                                   TAG_VEMPTY);
-            }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             const int row0 = b * c.T + seg * c.seg_len + n * kC;   // flattened (b, t) row
+            // the whole warp polls together (identical values in every lane), so it stays
+            // converged and never waits on itself
+            if (n >= 2 && !mbar_wait(bar0 + (s ? B_EMPTY1 : B_EMPTY0), ((n >> 1) - 1) & 1,
+                                     abort_flag, limit, c.err, TAG_EMPTY))
+                break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(full, tx);
                 const uint32_t kq = base + (s ? SM_KQ1 : SM_KQ0);
@@ -410,10 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 for (int hf = 0; hf < 2; ++hf) {
                     tma_load_3d(kq + hf * 16384, &p.tm_k, full, hf * 64, h, row0);
                     if (!SUMMARY) tma_load_3d(kq + hf * 16384 + 8192, &p.tm_q, full, hf * 64, h, row0);
-                    if (need_v) tma_load_3d(base + SM_V + hf * 8192, &p.tm_v, full, hf * 64, h, row0);
                 }
             }
-            issued_last[s] = n;
+            if (s) issued_last[1] = n; else issued_last[0] = n;
             float* gs = gates + s * 128;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -424,68 +508,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(full);
+            if (need_v) {
+                if (n >= 1 &&
+                    !mbar_wait(bar0 + B_VEMPTY, (n - 1) & 1, abort_flag, limit, c.err, TAG_VEMPTY))
+                    break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar0 + B_VFULL, 16384u);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(base + SM_V + hf * 8192, &p.tm_v, bar0 + B_VFULL, hf * 64, h, row0);
+                }
+                v_issued_last = n;
+            }
         }
         if (*abort_flag && lane == 0) {
             // let every copy this warp issued land before the CTA's memory is released
-            for (int s = 0; s < 2; ++s)
-                if (issued_last[s] >= 0)
-                    mbar_drain(bar0 + (s ? B_FULL1 : B_FULL0), (issued_last[s] >> 1) & 1, limit);
+            if (issued_last[0] >= 0) mbar_drain(bar0 + B_FULL0, (issued_last[0] >> 1) & 1, limit);
+            if (issued_last[1] >= 0) mbar_drain(bar0 + B_FULL1, (issued_last[1] >> 1) & 1, limit);
+            if (v_issued_last >= 0) mbar_drain(bar0 + B_VFULL, v_issued_last & 1, limit);
         }
-    } else {
-        // ================================== math ==================================
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;   // this warp's TMEM lanes
-        const uint32_t t_row = tmem + lane_off;
-        uint32_t mma_phase = 0;
-        bool mma_pending = false;
-        const long long bhoff = (long long)bh * kD * kD;
+    } else if (warp >= 4) {
+        // ================================== prep ==================================
+        const int pt = tid - 128, pw = warp - 4;
+        const uint32_t t_row = tmem + ((uint32_t)(pw * 32) << 16);   // this warp's TMEM lanes
+        volatile int* go = reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO_P);
+        uint32_t barp_phase = 0;
+        bool barp_pending = false;
+        float* Lm = reinterpret_cast<float*>(sm + SM_AB);   // L, fp32, until the inverse is done
+        float* Am = reinterpret_cast<float*>(sm + SM_AS);
+        float* Ys = reinterpret_cast<float*>(sm + SM_YS) + pw * 128;
 
-        // ---- initial state: row `tid` of H^T (= column tid of H)
-        for (int part = 0; part < 4; ++part) {
-            float x[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int k = part * 32 + j;
-                float v0 = 0.f;
-                if (SUMMARY) {
-                    v0 = (blk == 0 && k == tid) ? 1.f : 0.f;
-                } else if (c.h_start) {
-                    v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + tid];
-                }
-                x[j] = v0;
-            }
-            tmem_st32(t_row + TM_H + part * 32, x);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        math_bar();
+        // the group's first warp waits (optionally) and publishes a verdict that all read
+        // after the named barrier, so a timeout cannot split the group
+#define pwait(bar, parity, tag, doit) \
+    group_wait<2>(pw == 0, lane == 0, (bar), (parity), (doit), go, abort_flag, limit, c.err, (tag))
+#define pmma_wait() \
+    (pwait(bar0 + B_BARP, barp_phase, TAG_BARP, true) ? (barp_phase ^= 1u, barp_pending = false, true) : false)
 
-        // Thread 0 waits and publishes a verdict before the named barrier; every math
-        // thread then reads the same verdict, so a timeout cannot split the warps.
-        volatile int* s_go = reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO);
-        auto math_wait = [&](uint32_t bar, uint32_t parity, unsigned tag) -> bool {
-            if (tid == 0) {
-                const bool ok = mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
-                *s_go = (ok && !*abort_flag) ? 1 : 0;
-            }
-            math_bar();
-            return *s_go != 0;
-        };
-        auto mma_wait = [&]() -> bool {
-            const bool ok = math_wait(bar0 + B_MMA, mma_phase, TAG_MMA);
-            if (ok) {
-                mma_phase ^= 1u;
-                mma_pending = false;
-            }
-            return ok;
-        };
-
+#pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             const uint32_t kq = base + (s ? SM_KQ1 : SM_KQ0);
-            const uint32_t t_u = tmem + ((n & 1) ? TM_U1 : TM_U0);
-            if (!math_wait(bar0 + (s ? B_FULL1 : B_FULL0), (n >> 1) & 1, TAG_FULL)) break;
-            // ---- gate cumsum and per-chunk scalars (warp 0)
-            if (warp == 0) {
+            float* sc = scal + (n & 1) * (SC_N * 64);
+            if (!pwait(bar0 + (s ? B_FULL1 : B_FULL0), (n >> 1) & 1, TAG_FULL, true)) break;
+
+            // ---- gate cumsum and per-chunk scalars (first prep warp)
+            if (pw == 0) {
                 const float* gs = gates + s * 128;
                 const float g0 = gs[2 * lane], g1 = gs[2 * lane + 1];
                 float sum = g0 + g1;
@@ -497,307 +565,381 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 const float excl = sum - (g0 + g1);
                 const float glast = __shfl_sync(0xffffffffu, sum, 31);
                 const float G0 = excl + g0, G1 = excl + g0 + g1;
-                s_gam[2 * lane] = G0;
-                s_gam[2 * lane + 1] = G1;
-                s_gx[2 * lane] = excl;
-                s_gx[2 * lane + 1] = G0;
-                s_eg[2 * lane] = ex2(G0);
-                s_eg[2 * lane + 1] = ex2(G1);
-                s_dd[2 * lane] = ex2(glast - G0);
-                s_dd[2 * lane + 1] = ex2(glast - G1);
                 const float b0 = gs[64 + 2 * lane], b1 = gs[64 + 2 * lane + 1];
-                s_bet[2 * lane] = b0;
-                s_bet[2 * lane + 1] = b1;
-                s_bekr[2 * lane] = b0 * ex2(excl);
-                s_bekr[2 * lane + 1] = b1 * ex2(G0);
-                if (lane == 0) s_misc[0] = ex2(glast);
+                sc[SC_GAM * 64 + 2 * lane] = G0;
+                sc[SC_GAM * 64 + 2 * lane + 1] = G1;
+                sc[SC_GX * 64 + 2 * lane] = excl;
+                sc[SC_GX * 64 + 2 * lane + 1] = G0;
+                sc[SC_DD * 64 + 2 * lane] = ex2(glast - G0);
+                sc[SC_DD * 64 + 2 * lane + 1] = ex2(glast - G1);
+                sc[SC_EG * 64 + 2 * lane] = ex2(G0);
+                sc[SC_EG * 64 + 2 * lane + 1] = ex2(G1);
+                sc[SC_BET * 64 + 2 * lane] = b0;
+                sc[SC_BET * 64 + 2 * lane + 1] = b1;
+                sc[SC_BEKR * 64 + 2 * lane] = b0 * ex2(excl);
+                sc[SC_BEKR * 64 + 2 * lane + 1] = b1 * ex2(G0);
+                if (lane == 0) sc[SC_MISC * 64] = ex2(glast);
             }
-            math_bar();
-
-            // ---- Q tile -> tf32 K-major copy (B operand of S2): thread = (row i, k half)
-            if (!SUMMARY) {
-                const int i = tid >> 1, kh = tid & 1;
-                const uint8_t* src = sm + (s ? SM_KQ1 : SM_KQ0) + kh * 16384 + 8192 +
-                                     (i >> 3) * 1024 + (i & 7) * 128;
-                uint8_t* dst = sm + SM_QT + (i >> 3) * 1024 + (i & 7) * 128;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 u = *reinterpret_cast<const uint4*>(src + ((cc ^ (i & 7)) << 4));
-                    // 8 bf16 -> 8 fp32 (exact); features k = 64 kh + 8 cc .. + 7
-                    const uint4 lo4 = make_uint4(u.x << 16, u.x & 0xFFFF0000u, u.y << 16, u.y & 0xFFFF0000u);
-                    const uint4 hi4 = make_uint4(u.z << 16, u.z & 0xFFFF0000u, u.w << 16, u.w & 0xFFFF0000u);
-                    const int kb = kh * 2 + (cc >> 2);
-                    const int q0 = (2 * cc) & 7, q1 = (2 * cc + 1) & 7;
-                    *reinterpret_cast<uint4*>(dst + kb * 8192 + ((q0 ^ (i & 7)) << 4)) = lo4;
-                    *reinterpret_cast<uint4*>(dst + kb * 8192 + ((q1 ^ (i & 7)) << 4)) = hi4;
-                }
-                fence_proxy_async();
-            }
-
-            // ---- P1: [K ; Q] K^T -> TM_S
-            if (tid == 0) {
+            // ---- P1: [K ; Q] K^T -> TM_S (needs only the loaded tiles)
+            if (pt == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma(tmem + TM_S, desc_k(kq + off), desc_k(kq + off), ID_P1, ks > 0);
+                    mma_ss(tmem + TM_S, desc_k(kq + off), desc_k(kq + off), ID_P1, ks > 0);
                 }
-                mma_commit(bar0 + B_MMA);
+                mma_commit(bar0 + B_BARP);
             }
-            mma_pending = true;
-            if (!mma_wait()) break;
+            __syncwarp();
+            barp_pending = true;
+            if (!pmma_wait()) break;   // its barrier also publishes the scalars
             tc_fence_after();
 
-            // ---- L rows (lanes 0..63) and C rows (lanes 64..127)
+            // ---- L rows (lanes 0..63, fp32) and C rows (lanes 64..127, tf32), 16 columns
+            //      at a time
             {
-                float srow[64];
-                tmem_ld32(t_row + TM_S, srow);
-                tmem_ld32(t_row + TM_S + 32, srow + 32);
-                tmem_wait_ld();
-                if (tid < 64) {
-                    const int i = tid;
-                    const float gxi = s_gx[i], bi = s_bet[i];
+                const float* gam = sc + SC_GAM * 64;
+                const int i = pt & 63;
+                const float gi = (pt < 64) ? sc[SC_GX * 64 + i] : gam[i];
+                const float bi = (pt < 64) ? sc[SC_BET * 64 + i] : 1.f;
+                uint8_t* ctile = sm + ((n & 1) ? SM_C1 : SM_C0);
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    float sv[16];
+                    tmem_ld16(t_row + TM_S + 16 * g, sv);
+                    tmem_wait_ld();
+                    if (pt < 64) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        Ls[sw64(i, j)] = (j < i) ? bi * ex2(gxi - s_gam[j]) * srow[j] : 0.f;
-                } else if (!SUMMARY) {
-                    // C row i as tf32, K-major: two 32-wide blocks of 128-byte rows
-                    const int i = tid - 64;
-                    const float gi = s_gam[i];
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        srow[j] = to_tf32((j <= i) ? ex2(gi - s_gam[j]) * srow[j] : 0.f);
-#pragma unroll
-                    for (int kb = 0; kb < 2; ++kb) {
-                        uint8_t* rp = sm + SM_C + kb * 8192 + (i >> 3) * 1024 + (i & 7) * 128;
-#pragma unroll
-                        for (int cq = 0; cq < 8; ++cq) {
-                            const float* vv = srow + kb * 32 + cq * 4;
-                            *reinterpret_cast<uint4*>(rp + ((cq ^ (i & 7)) << 4)) =
-                                make_uint4(__float_as_uint(vv[0]), __float_as_uint(vv[1]),
-                                           __float_as_uint(vv[2]), __float_as_uint(vv[3]));
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int j = 16 * g + jj;
+                            Lm[sw64(i, j)] = (j < i) ? bi * ex2(gi - gam[j]) * sv[jj] : 0.f;
                         }
+                    } else if (!SUMMARY) {
+                        uint32_t t[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int j = 16 * g + jj;
+                            t[jj] = tf32_bits((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
+                        }
+                        // columns 16g..16g+15: tf32 block g >> 1, 16-byte chunks 4(g&1)..+3
+                        uint8_t* blkp = ctile + (g >> 1) * 8192;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(blkp + sw128(i, 4 * (g & 1) + q)) =
+                                make_uint4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
                     }
                 }
             }
             tc_fence_before();
-            math_bar();
+            prep_bar();
 
-            // ---- A = (I + L)^-1: 16x16 diagonal blocks, then block forward substitution
-            if (tid < 64) {
-                const int bs = (tid >> 4) * 16, cc = tid & 15;
+            // ---- diagonal 16x16 blocks of (I + L)^-1: lane r of a 16-lane group owns row r
+            //      of the block's inverse, X[r] = e_r - sum_{m<r} L[r][m] X[m], with row m
+            //      broadcast by shuffles once it is final. Rows are zero beyond their diagonal,
+            //      so the updates run over all 16 columns with constant bounds.
+            if (pt < 64) {
+                const int bs = (pt >> 4) * 16, r = pt & 15, src0 = lane & 16;
                 float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+                for (int m = 0; m < 16; ++m) x[m] = (m == r) ? 1.f : 0.f;
+#pragma unroll 1
+                for (int m = 0; m < 15; ++m) {
+                    const float f = (r > m) ? Lm[sw64(bs + r, bs + m)] : 0.f;
 #pragma unroll
-                for (int r = 1; r < 16; ++r) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int m = 0; m < r; ++m) a = fmaf(Ls[sw64(bs + r, bs + m)], x[m], a);
-                    if (r > cc) x[r] = -a;
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const float xm = __shfl_sync(0xffffffffu, x[cc], src0 + m);
+                        x[cc] = fmaf(-f, xm, x[cc]);
+                    }
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) As[sw64(bs + r, bs + cc)] = x[r];
+                for (int cc = 0; cc < 16; ++cc) Am[sw64(bs + r, bs + cc)] = x[cc];
             } else {
                 // zero the blocks above the diagonal
-                for (int e = tid - 64; e < 6 * 256; e += 64) {
+#pragma unroll 1
+                for (int e = pt - 64; e < 6 * 256; e += 64) {
                     const int blkid = e >> 8, w = e & 255;
                     const int I = (blkid < 3) ? 0 : (blkid < 5 ? 1 : 2);
                     const int J = (blkid < 3) ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    As[sw64(16 * I + (w >> 4), 16 * J + (w & 15))] = 0.f;
+                    Am[sw64(16 * I + (w >> 4), 16 * J + (w & 15))] = 0.f;
                 }
             }
-            math_bar();
-            {
-                const int r0 = tid >> 4, cc = tid & 15;
-                for (int I = 1; I < 4; ++I) {
-                    for (int J = 0; J < I; ++J) {
+            prep_bar();
+            // ---- block forward substitution: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ
+#pragma unroll 1
+            for (int I = 1; I < 4; ++I) {
+#pragma unroll 1
+                for (int tile = pw; tile < 2 * I; tile += 4) {
+                    const int J = tile >> 1, n0 = 16 * J + 8 * (tile & 1);
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                    for (int m = J; m < I; ++m)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int r = r0 + 8 * e;
-                            float a = 0.f;
-                            for (int m = J; m < I; ++m) {
-#pragma unroll
-                                for (int l = 0; l < 16; ++l)
-                                    a = fmaf(Ls[sw64(16 * I + r, 16 * m + l)],
-                                             As[sw64(16 * m + l, 16 * J + cc)], a);
-                            }
-                            Yscr[J * 256 + r * 16 + cc] = a;
+                        for (int kk = 0; kk < 2; ++kk) {
+                            uint32_t a[4], bb[2];
+                            frag_a(Lm, 16 * I, 16 * m + 8 * kk, lane, a);
+                            frag_b(Am, 16 * m + 8 * kk, n0, lane, bb);
+                            mma_m16n8k8(y, a, bb);
                         }
-                    }
-                    math_bar();
-                    for (int J = 0; J < I; ++J) {
+                    // the Y tile (16 x 8) goes through the warp's scratch, then X = -X_II Y
+                    const int g = lane >> 2, t = lane & 3;
+                    Ys[g * 8 + 2 * t] = y[0];
+                    Ys[g * 8 + 2 * t + 1] = y[1];
+                    Ys[(g + 8) * 8 + 2 * t] = y[2];
+                    Ys[(g + 8) * 8 + 2 * t + 1] = y[3];
+                    __syncwarp();
+                    float xo[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int r = r0 + 8 * e;
-                            float a = 0.f;
-#pragma unroll
-                            for (int l = 0; l < 16; ++l)
-                                a = fmaf(As[sw64(16 * I + r, 16 * I + l)], Yscr[J * 256 + l * 16 + cc], a);
-                            As[sw64(16 * I + r, 16 * J + cc)] = -a;
-                        }
+                    for (int kk = 0; kk < 2; ++kk) {
+                        uint32_t a[4], bb[2];
+                        frag_a(Am, 16 * I, 16 * I + 8 * kk, lane, a);
+                        bb[0] = tf32_bits(Ys[(8 * kk + t) * 8 + g]);
+                        bb[1] = tf32_bits(Ys[(8 * kk + t + 4) * 8 + g]);
+                        mma_m16n8k8(xo, a, bb);
                     }
-                    math_bar();
+                    __syncwarp();
+                    Am[sw64(16 * I + g, n0 + 2 * t)] = -xo[0];
+                    Am[sw64(16 * I + g, n0 + 2 * t + 1)] = -xo[1];
+                    Am[sw64(16 * I + g + 8, n0 + 2 * t)] = -xo[2];
+                    Am[sw64(16 * I + g + 8, n0 + 2 * t + 1)] = -xo[3];
                 }
+                prep_bar();
             }
-            // ---- A diag(beta) and A diag(beta 2^Gx), bf16, K-major rows
+            // ---- A diag(beta) and A diag(beta 2^Gx) as bf16 K-major rows (over L's space;
+            //      the last round's barrier retired every read of L)
             {
-                const int i = tid & 63;
-                const float* scale = (tid < 64) ? s_bet : s_bekr;
-                float arow[64];
+                const int i = pt & 63;
+                const float* scale = sc + ((pt < 64) ? SC_BET : SC_BEKR) * 64;
+                uint8_t* tile = sm + ((pt < 64) ? SM_AB : SM_ABG);
+#pragma unroll 1
+                for (int cq = 0; cq < 8; ++cq) {
+                    float a[8];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) arow[j] = As[sw64(i, j)] * scale[j];
-                st_row_sw128<8>(sm + ((tid < 64) ? SM_AB : SM_ABG), i, 0, arow);
+                    for (int jj = 0; jj < 8; ++jj) a[jj] = Am[sw64(i, 8 * cq + jj)] * scale[8 * cq + jj];
+                    *reinterpret_cast<uint4*>(tile + sw128(i, cq)) =
+                        make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]),
+                                   pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+                }
             }
             fence_proxy_async();
-            math_bar();
-
-            // ---- P2: U^T = V^T (A diag beta)^T -> t_u ;  P3: W^T = K^T (A diag(beta 2^Gx))^T -> TM_S
-            if (tid == 0) {
+            // ---- P2 (U^T into the parity's U buffer, once chunk n-2's R is retired) and P3
+            const uint32_t t_u = tmem + TM_U + (n & 1) * 64;
+            if (!pwait(bar0 + ((n & 1) ? B_UFREE1 : B_UFREE0), ((n >> 1) - 1) & 1, TAG_UFREE,
+                       n >= 2))
+                break;
+            if (!pwait(bar0 + B_VFULL, n & 1, TAG_VFULL, need_v)) break;
+            if (pt == 0) {
                 tc_fence_after();
                 if (need_v) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma(t_u, desc_mn(base + SM_V + ks * 2048, 8192),
-                            desc_k(base + SM_AB + ks * 32), ID_P23, ks > 0);
+                        mma_ss(t_u, desc_mn(base + SM_V + ks * 2048, 8192),
+                               desc_k(base + SM_AB + ks * 32), ID_P23, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma(tmem + TM_S, desc_mn(kq + ks * 2048, 16384), desc_k(base + SM_ABG + ks * 32),
-                        ID_P23, ks > 0);
+                    mma_ss(tmem + TM_S, desc_mn(kq + ks * 2048, 16384),
+                           desc_k(base + SM_ABG + ks * 32), ID_P23, ks > 0);
                 if (need_v) mma_commit(bar0 + B_VEMPTY);
-                mma_commit(bar0 + B_MMA);
+                mma_commit(bar0 + B_BARP);
             }
-            mma_pending = true;
-            if (!mma_wait()) break;
+            __syncwarp();
+            barp_pending = true;
+            if (!pmma_wait()) break;
             tc_fence_after();
-
-            // ---- -W -> tf32, K-major B operand of S1: thread k writes column k of rows i
+            // ---- -W and Qd as tf32 K-major B operands, once chunk n-1's S1/S2 retired
             {
-                float w[64];
-                tmem_ld32(t_row + TM_S, w);
-                tmem_ld32(t_row + TM_S + 32, w + 32);
-                tmem_wait_ld();
-                const int k = tid;
+                if (!pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
+                // thread k holds column k of W^T's rows i: writes element (row i, feature k)
+                const int k = pt;
                 uint8_t* col = sm + SM_W + (k >> 5) * 8192 + (k & 3) * 4;
                 const int qk = (k & 31) >> 2;
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    float w[16];
+                    tmem_ld16(t_row + TM_S + 16 * g, w);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    *reinterpret_cast<float*>(col + (i >> 3) * 1024 + (i & 7) * 128 +
-                                              ((qk ^ (i & 7)) << 4)) = to_tf32(-w[i]);
+                    for (int ii = 0; ii < 16; ++ii)
+                        *reinterpret_cast<uint32_t*>(col + sw128(16 * g + ii, qk)) = tf32_bits(-w[ii]);
+                }
+                if (!SUMMARY) {
+                    // Q tile row i, half kh -> 2^G_i q_i as tf32
+                    const int i = pt >> 1, kh = pt & 1;
+                    const float egi = sc[SC_EG * 64 + i];
+                    const uint8_t* src = sm + (s ? SM_KQ1 : SM_KQ0) + kh * 16384 + 8192;
+#pragma unroll 1
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
+                        const uint4 lo4 = make_uint4(
+                            tf32_bits(__uint_as_float(u.x << 16) * egi),
+                            tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
+                            tf32_bits(__uint_as_float(u.y << 16) * egi),
+                            tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
+                        const uint4 hi4 = make_uint4(
+                            tf32_bits(__uint_as_float(u.z << 16) * egi),
+                            tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
+                            tf32_bits(__uint_as_float(u.w << 16) * egi),
+                            tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
+                        // features 64 kh + 8 cc .. +7: tf32 block 2 kh + cc / 4, chunks 2 (cc % 4) + {0, 1}
+                        uint8_t* dst = sm + SM_QT + (kh * 2 + (cc >> 2)) * 8192;
+                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc) & 7)) = lo4;
+                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc + 1) & 7)) = hi4;
+                    }
+                }
             }
             fence_proxy_async();
             tc_fence_before();
-            math_bar();
+            prep_bar();
+            if (pt == 0) mbar_arrive(bar0 + B_PREPDONE);
+        }
+        if (*go == 0 && barp_pending && pt == 0) mbar_drain(bar0 + B_BARP, barp_phase, limit);
+#undef pmma_wait
+#undef pwait
+    } else {
+        // ================================== state =================================
+        const int st = tid;
+        const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+        volatile int* go = reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO_S);
+        uint32_t bars_phase = 0;
+        bool bars_pending = false;
+        const long long bhoff = (long long)bh * kD * kD;
+        const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
 
-            // ---- S1: R^T = U^T - H^T W^T (onto t_u);  S2: H^T Q^T -> TM_OI
-            if (tid == 0) {
+#define swait(bar, parity, tag) \
+    group_wait<1>(warp == 0, lane == 0, (bar), (parity), true, go, abort_flag, limit, c.err, (tag))
+#define smma_wait() \
+    (swait(bar0 + B_BARS, bars_phase, TAG_BARS) ? (bars_phase ^= 1u, bars_pending = false, true) : false)
+// o rows of chunk m from that chunk's O buffer: thread v writes column v
+#define store_output(m)                                                                          \
+    store_o_rows(c, t_row + TM_O + ((m) & 1) * 64,                                               \
+                 ((long long)(b * c.T + seg * c.seg_len + (m) * kC) * c.H + h) * kD + st, tok_stride)
+
+        // ---- initial state: row `st` of H^T (= column st of H)
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int k = 16 * g + j;
+                float v0 = 0.f;
+                if (SUMMARY)
+                    v0 = (blk == 0 && k == st) ? 1.f : 0.f;
+                else if (c.h_start)
+                    v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + st];
+                x[j] = __float_as_uint(v0);
+            }
+            tmem_st16(t_row + TM_H + 16 * g, x);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        state_bar();
+
+        int done = 0;   // chunks completed
+#pragma unroll 1
+        for (int n = 0; n < nchunks; ++n) {
+            const int s = n & 1;
+            const uint32_t kq = base + (s ? SM_KQ1 : SM_KQ0);
+            const uint32_t t_u = tmem + TM_U + (n & 1) * 64;
+            const uint32_t t_o = tmem + TM_O + (n & 1) * 64;
+            const float* sc = scal + (n & 1) * (SC_N * 64);
+            if (!swait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE)) break;
+            // ---- S1: R^T = U^T + H^T (-W)^T ;  S2: O^T = H^T Qd^T  (A = H^T in TMEM)
+            if (st == 0) {
                 tc_fence_after();
-                // A = H^T straight from tensor memory (fp32 master read as tf32)
 #pragma unroll
                 for (int ks = 0; ks < 16; ++ks)
-                    mma_ta_tf32(t_u, tmem + TM_H + ks * 8,
+                    mma_ts_tf32(t_u, tmem + TM_H + ks * 8,
                                 desc_k(base + SM_W + (ks >> 2) * 8192 + (ks & 3) * 32), ID_TF,
                                 (need_v || ks > 0) ? 1u : 0u);
                 if (!SUMMARY) {
 #pragma unroll
                     for (int ks = 0; ks < 16; ++ks)
-                        mma_ta_tf32(tmem + TM_OI, tmem + TM_H + ks * 8,
+                        mma_ts_tf32(t_o, tmem + TM_H + ks * 8,
                                     desc_k(base + SM_QT + (ks >> 2) * 8192 + (ks & 3) * 32), ID_TF,
                                     ks > 0);
                 }
-                mma_commit(bar0 + B_MMA);
+                mma_commit(bar0 + B_WFREE);
+                mma_commit(bar0 + B_BARS);
             }
-            mma_pending = true;
-            if (!mma_wait()) break;
+            __syncwarp();
+            bars_pending = true;
+            // ---- meanwhile: the previous chunk's output
+            if (!SUMMARY && n >= 1) {
+                tc_fence_after();
+                store_output(n - 1);
+            }
+            if (!smma_wait()) break;
             tc_fence_after();
-
-            // ---- R^T row v = tid -> bf16 (plain and decayed); pre-scale the master by 2^G_last
+            // ---- decayed R^T -> packed bf16 hi/lo in TMEM; pre-scale the master by 2^G_last
             {
-                float r[64];
-                const uint32_t t_ur = lane_off + ((n & 1) ? TM_U1 : TM_U0);
-                tmem_ld32(tmem + t_ur, r);
-                tmem_ld32(tmem + t_ur + 32, r + 32);
-                tmem_wait_ld();
-                // decayed R as an unevaluated bf16 sum hi + lo (R itself stays in TMEM for S3)
-                float lo[64];
+                const float* dd = sc + SC_DD * 64;
+                const uint32_t t_ur = t_row + TM_U + (n & 1) * 64;
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    float r[16];
+                    tmem_ld16(t_ur + 16 * g, r);
+                    tmem_wait_ld();
+                    // packed column q holds the pair (2q, 2q+1) of the 64 tokens j
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float x = r[j] * s_dd[j];
-                    r[j] = __bfloat162float(__float2bfloat16_rn(x));
-                    lo[j] = x - r[j];
+                    for (int j = 0; j < 8; ++j) {
+                        const float x0 = r[2 * j] * dd[16 * g + 2 * j];
+                        const float x1 = r[2 * j + 1] * dd[16 * g + 2 * j + 1];
+                        const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                        const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                        hi[j] = pack_bf16(h0, h1);
+                        lo[j] = pack_bf16(x0 - h0, x1 - h1);
+                    }
+                    tmem_st8(t_row + TM_RD + 8 * g, hi);
+                    tmem_st8(t_row + TM_RD + 32 + 8 * g, lo);
                 }
-                st_row_sw128<8>(sm + SM_RD, tid, 0, r);
-                st_row_sw128<8>(sm + SM_RD + 16384, tid, 0, lo);
-                const float ecl = s_misc[0];
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    float x[32];
-                    tmem_ld32(t_row + TM_H + part * 32, x);
+                const float ecl = sc[SC_MISC * 64];
+#pragma unroll 1
+                for (int g = 0; g < 8; ++g) {
+                    float x[16];
+                    uint32_t y[16];
+                    tmem_ld16(t_row + TM_H + 16 * g, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] *= ecl;
-                    tmem_st32(t_row + TM_H + part * 32, x);
+                    for (int j = 0; j < 16; ++j) y[j] = __float_as_uint(x[j] * ecl);
+                    tmem_st16(t_row + TM_H + 16 * g, y);
                 }
                 tmem_wait_st();
             }
-            fence_proxy_async();
             tc_fence_before();
-            math_bar();
-
-            // ---- S3: R^T C^T -> TM_OA ;  S4: H^T += R^T diag(2^(G_last - G)) K
-            if (tid == 0) {
+            state_bar();
+            // ---- S3: O^T += R^T C^T (A = R^T in TMEM) ; S4: H^T += (R^T D) K (A = hi, lo in TMEM)
+            if (st == 0) {
                 tc_fence_after();
                 if (!SUMMARY) {
-                    // (C R)^T = R^T C^T with R^T read from tensor memory, tf32
+                    const uint32_t cb = base + ((n & 1) ? SM_C1 : SM_C0);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ta_tf32(tmem + TM_OA, t_u + ks * 8,
-                                    desc_k(base + SM_C + (ks >> 2) * 8192 + (ks & 3) * 32), ID_TF,
-                                    ks > 0);
+                        mma_ts_tf32(t_o, t_u + ks * 8, desc_k(cb + (ks >> 2) * 8192 + (ks & 3) * 32),
+                                    ID_TF, 1u);
                 }
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma(tmem + TM_H, desc_k(base + SM_RD + part * 16384 + ks * 32),
-                            desc_mn(kq + ks * 2048, 16384), ID_S4, 1u);
+                        mma_ts_bf16(tmem + TM_H, tmem + TM_RD + part * 32 + ks * 8,
+                                    desc_mn(kq + ks * 2048, 16384), ID_S4, 1u);
                 mma_commit(bar0 + (s ? B_EMPTY1 : B_EMPTY0));
-                mma_commit(bar0 + B_MMA);
+                mma_commit(bar0 + ((n & 1) ? B_UFREE1 : B_UFREE0));
+                mma_commit(bar0 + B_BARS);
             }
-            mma_pending = true;
-            if (!mma_wait()) break;
+            __syncwarp();
+            bars_pending = true;
+            if (!smma_wait()) break;
             tc_fence_after();
-
-            // ---- output: o_i = 2^G_i (H^T Q^T)[:, i] + (R^T C^T)[:, i]
-            if (!SUMMARY) {
-                const int row0 = b * c.T + seg * c.seg_len + n * kC;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float oi[32], oa[32];
-                    tmem_ld32(t_row + TM_OI + half * 32, oi);
-                    tmem_ld32(t_row + TM_OA + half * 32, oa);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = half * 32 + j;
-                        const float val = fmaf(s_eg[i], oi[j], oa[j]);
-                        const long long idx = ((long long)(row0 + i) * c.H + h) * kD + tid;
-                        if (c.out_bf16)
-                            reinterpret_cast<__nv_bfloat16*>(c.o)[idx] = __float2bfloat16_rn(val);
-                        else
-                            reinterpret_cast<float*>(c.o)[idx] = val;
-                    }
-                }
-            }
-            tc_fence_before();
-            math_bar();
+            done = n + 1;
         }
 
-        if (*s_go == 0) {
-            if (mma_pending && tid == 0)   // let an issued MMA group retire before TMEM is freed
-                mbar_drain(bar0 + B_MMA, mma_phase, limit);
+        if (*go == 0) {
+            if (bars_pending && st == 0)   // let an issued MMA group retire before TMEM is freed
+                mbar_drain(bar0 + B_BARS, bars_phase, limit);
         } else {
+            if (!SUMMARY && done >= 1) store_output(done - 1);
             // ---- the chain's final state: thread v writes column v of H (row v of H^T)
             float* dst = nullptr;
             if (SUMMARY) {
@@ -807,16 +949,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 dst = c.h_final + bhoff;
             }
             if (dst) {
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    float x[32];
-                    tmem_ld32(t_row + TM_H + part * 32, x);
+#pragma unroll 1
+                for (int g = 0; g < 8; ++g) {
+                    float x[16];
+                    tmem_ld16(t_row + TM_H + 16 * g, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) dst[(long long)(part * 32 + j) * kD + tid] = x[j];
+                    for (int j = 0; j < 16; ++j) dst[(long long)(16 * g + j) * kD + st] = x[j];
                 }
             }
         }
+#undef store_output
+#undef smma_wait
+#undef swait
     }
 
     tc_fence_before();
