@@ -97,7 +97,15 @@ def algorithmic(w, out_bytes: int = 4):
     K, V = w.K, w.V
     kv_state = BH * K * V * 4
     kk_state = BH * K * K * 4
+    tc = w.in_dtype == "bf16" and K == 128 and V == 128
     stages = {
+        # per-chunk WY factors (tensor-core path only): reads k, g, beta; writes two bf16
+        # 64 x 64 tiles per chunk. An intermediate of this implementation, not of the method,
+        # so it is left out of the path total below.
+        "wy": {
+            "bytes": (tok_heads * (K * isz + 2 * isz) + chunks * 16384) if tc else 0,
+            "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64) if tc else 0,
+        },
         "summary": {
             "bytes": sum_tok_heads * ((K + V) * isz + 2 * isz) + (w.nseg - 1) * (kk_state + kv_state),
             # prep (K K^T, U, W) + augmented K x (K+V) state update per chunk
@@ -117,9 +125,17 @@ def algorithmic(w, out_bytes: int = 4):
                                + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V),
         },
     }
-    total = {"bytes": sum(s["bytes"] for s in stages.values()),
-             "flops": sum(s["flops"] for s in stages.values())}
+    method = [n for n in stages if n != "wy"]
+    total = {"bytes": sum(stages[n]["bytes"] for n in method),
+             "flops": sum(stages[n]["flops"] for n in method)}
     return stages, total
+
+
+def launches_per_step(w):
+    """Kernels one gdn_segmented_fwd call launches: WY factors (tensor-core path), summary,
+    scan, forward; with one segment only WY + forward."""
+    tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128)
+    return tc + (3 if w.nseg > 1 else 1)
 
 
 def load_peaks():
@@ -254,7 +270,7 @@ def run_ours(args):
         raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     for e4 in ev:        # torch creates the CUDA event on first record; the library then
         for e in e4:     # re-records the same handles inside each step
             e.record(stream)
@@ -279,18 +295,18 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
 
-    stage_ms = {"summary": [], "scan": [], "forward": []}
+    stage_ms = {"wy": [], "summary": [], "scan": [], "forward": []}
     for e in ev:
-        stage_ms["summary"].append(e[0].elapsed_time(e[1]))
-        stage_ms["scan"].append(e[1].elapsed_time(e[2]))
-        stage_ms["forward"].append(e[2].elapsed_time(e[3]))
+        for i, name in enumerate(stage_ms):
+            stage_ms[name].append(e[i].elapsed_time(e[i + 1]))
     stages, total = algorithmic(w)
     avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     dominant = max(avg, key=avg.get)
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     ach = stages[dominant]["bytes"] / (avg[dominant] * 1e-3) / 1e9
-    kernel_name = {"summary": "gdn_summary", "scan": "gdn_scan", "forward": "gdn_forward"}[dominant]
+    kernel_name = {"wy": "gdn_wy", "summary": "gdn_summary", "scan": "gdn_scan",
+                   "forward": "gdn_forward"}[dominant]
     roofline = {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "traffic": recorded_traffic(kernel_name, w0.name),
                 "kernel": kernel_name, "kernel_ms": round(avg[dominant], 4),
@@ -357,7 +373,7 @@ def run_ours(args):
             "stage_ms": {k: round(v, 4) for k, v in avg.items()},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * K if w.nseg > 1 else K,
+            "gpu_launches": launches_per_step(w) * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -17,17 +17,25 @@ constexpr size_t kAlign = 256;
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-    size_t off_M, off_S, off_Hin, total;
+    size_t off_wy, off_M, off_S, off_Hin, total;
 };
 
+// Shapes that take the tcgen05 kernels (which also need the per-chunk WY tiles).
+bool tc_shape(const gdn_problem& p) {
+    return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128;
+}
+
+// [header | WY tiles (tcgen05 shapes) | M | S | H_in (nseg > 1)]
 WsLayout layout(const gdn_problem& p, int nseg) {
     WsLayout w{};
     const size_t bh = (size_t)p.B * p.H;
+    w.off_wy = kHeaderBytes;
+    const size_t wy_bytes = tc_shape(p) ? bh * (size_t)(p.T / gdn::kChunk) * 16384u : 0;
+    w.off_M = w.off_wy + round_up(wy_bytes);
     if (nseg <= 1) {
-        w.total = kHeaderBytes;
+        w.total = w.off_M;
         return w;
     }
-    w.off_M = kHeaderBytes;
     w.off_S = w.off_M + round_up(sizeof(float) * nseg * bh * p.K * p.K);
     w.off_Hin = w.off_S + round_up(sizeof(float) * nseg * bh * p.K * p.V);
     w.total = w.off_Hin + round_up(sizeof(float) * nseg * bh * p.K * p.V);
@@ -90,6 +98,13 @@ ChainParams base_params(const gdn_problem* p, void* ws) {
 
 bool use_tc(const ChainParams& c) { return c.T > 0 && gdn::tc_supported(c); }
 
+// The tcgen05 chains read every chunk's WY tiles from the workspace: form them first (one
+// launch for all chunks of the problem). Nothing to do on the CUDA-core path.
+cudaError_t prepare(ChainParams& c, const gdn_problem* p, void* ws, cudaStream_t s) {
+    c.wy = reinterpret_cast<char*>(ws) + layout(*p, 1).off_wy;
+    return use_tc(c) ? gdn::launch_tc_wy(c, s) : cudaSuccess;
+}
+
 cudaError_t run_forward(const ChainParams& c, cudaStream_t s) {
     return use_tc(c) ? gdn::launch_tc_forward(c, s) : gdn::launch_simt_forward(c, s);
 }
@@ -139,6 +154,8 @@ gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, con
         return from_cuda(gdn::launch_scan(nullptr, nullptr, h0, h_final, 1, p->B * p->H, p->K,
                                           p->V, s));
     }
+    cudaError_t e = prepare(c, p, workspace, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
     return from_cuda(run_forward(c, s));
 }
 
@@ -164,6 +181,9 @@ gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const void* k, co
     c.seg_len = p->T / nseg;
     c.nseg_run = nseg;
     c.nseg_total = nseg;
+    if (p->T == 0) return from_cuda(run_summary(c, s));
+    cudaError_t e = prepare(c, p, workspace, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
     return from_cuda(run_summary(c, s));
 }
 
@@ -208,24 +228,35 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
     const int BH = p->B * p->H;
 
     if (nseg == 1) {
-        if (mark(stage_events, 0, s) != cudaSuccess || mark(stage_events, 1, s) != cudaSuccess)
+        if (mark(stage_events, 0, s) != cudaSuccess || mark(stage_events, 1, s) != cudaSuccess ||
+            mark(stage_events, 2, s) != cudaSuccess)
             return GDN_ERR_CUDA;
         if (H_in_out) {
             cudaError_t e = gdn::launch_scan(nullptr, nullptr, h0, H_in_out, 1, BH, p->K, p->V, s);
             if (e != cudaSuccess) return GDN_ERR_CUDA;
         }
-        if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
+        if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
         st = gdn_chunk_fwd(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes,
                            stream);
         if (st != GDN_OK) return st;
-        return from_cuda(mark(stage_events, 3, s));
+        return from_cuda(mark(stage_events, 4, s));
     }
     float* M = reinterpret_cast<float*>(wsb + w.off_M);
     float* S = reinterpret_cast<float*>(wsb + w.off_S);
     float* H_in = H_in_out ? H_in_out : reinterpret_cast<float*>(wsb + w.off_Hin);
 
+    // 0. the WY tiles of every chunk (tcgen05 path only)
+    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ChainParams cw = base_params(p, workspace);
+    cw.k = k;
+    cw.g = g;
+    cw.beta = beta;
+    cw.seg_len = p->T / nseg;
+    cudaError_t e = prepare(cw, p, workspace, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
     // 1. summaries of segments 0..nseg-2 (the last segment's summary feeds nothing)
     ChainParams cs = base_params(p, workspace);
+    cs.wy = cw.wy;
     cs.k = k;
     cs.v = v;
     cs.g = g;
@@ -235,16 +266,17 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
     cs.seg_len = p->T / nseg;
     cs.nseg_run = nseg - 1;
     cs.nseg_total = nseg;
-    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
-    cudaError_t e = run_summary(cs, s);
+    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
+    e = run_summary(cs, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     // 2. exclusive in-order scan of the summaries
-    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
     e = gdn::launch_scan(M, S, h0, H_in, nseg, BH, p->K, p->V, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
-    if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
     // 3. every segment's forward from its scanned state
     ChainParams cf = base_params(p, workspace);
+    cf.wy = cw.wy;
     cf.q = q;
     cf.k = k;
     cf.v = v;
@@ -259,7 +291,7 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
     cf.nseg_total = nseg;
     e = run_forward(cf, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
-    return from_cuda(mark(stage_events, 3, s));
+    return from_cuda(mark(stage_events, 4, s));
 }
 
 const char* gdn_status_string(gdn_status s) {

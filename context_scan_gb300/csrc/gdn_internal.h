@@ -33,6 +33,9 @@ struct ChainParams {
     float* h_final;    // forward: written by chains whose segment is nseg_total-1 (nullable)
     float* M;          // summary: [nseg_total,B,H,K,K]
     float* S;          // summary: [nseg_total,B,H,K,V]
+    // tcgen05 path: per-chunk WY factors, [B*H][T/64][A diag(beta) | A diag(beta 2^Gx)], each
+    // a bf16 64 x 64 tile in the chain kernels' swizzled operand layout (8192 bytes)
+    void* wy;
     int B, T, H, K, V;
     int seg_len;       // tokens per segment (multiple of 64)
     int nseg_run;      // segments this launch processes: 0..nseg_run-1
@@ -50,6 +53,7 @@ cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* 
 
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);
+cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all T/64 chunks of every (b, h)
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);
 

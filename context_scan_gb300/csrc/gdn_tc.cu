@@ -26,25 +26,23 @@
 //   S4  H^T += (R^T diag(2^(G_last - G))) K, the decayed R^T held in tensor memory as an
 //       unevaluated bf16 sum hi + lo (two MMAs); the master is pre-scaled by 2^G_last.
 // The fp32 state and the corrected values R never pass through bf16. Exponents are always
-// differences of cumulative gates, never 2^-G. A = (I + L)^-1 is formed on chip: 16x16
-// diagonal blocks by forward substitution (rows in registers, shuffles), then three rounds
-// of block forward substitution on mma.sync (tf32).
+// differences of cumulative gates, never 2^-G. The factors A diag(beta) and A diag(beta 2^Gx),
+// A = (I + L)^-1, depend only on the chunk's keys and gates: the WY kernel (gdn_wy.cu) forms
+// them for every chunk beforehand, fully parallel, and a chain loads a chunk's pair with one
+// bulk copy next to its k/q tiles.
 //
 // Warp roles: warps 0-3 "state" (tensor-memory lanes 0..127; S1-S4, output, final state),
-// warps 4-7 "prep" (P1-P3, gate cumsum, L and C, the inverse, the WY operands), warp 8
-// "producer" (TMA loads of the q/k/v tiles with 128-byte swizzle into two stages; plain
+// warps 4-7 "prep" (P1-P3, gate cumsum, C, Qd, -W), warp 8 "producer" (TMA loads of the
+// q/k/v tiles with 128-byte swizzle and bulk copies of the WY tiles into two stages; plain
 // loads of the gates). Prep of chunk n+1 runs while the state group works on chunk n. Each
-// group issues its own MMAs (commits track the issuing thread's MMAs). Every wait on an
+// group issues its own MMAs (commits track the issuing thread's MMAs). Named barriers are
+// the non-.aligned form: a group's leader warp diverges around its mbarrier poll, and the
+// .aligned form may count a diverged warp's halves as separate arrivals. Every wait on an
 // mbarrier is bounded: on expiry the kernel records GDN_ERR_TIMEOUT in the device error
 // word, drains what it issued and frees tensor memory.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_bf16.h>
-
 #include <cstring>
-#include <mutex>
 
-#include "gdn_internal.h"
+#include "gdn_tc_common.cuh"
 
 namespace gdn {
 namespace {
@@ -70,18 +68,16 @@ constexpr uint32_t SM_W = 81920;      // -W tf32 K-major: [kblock 4][64 rows (i)
 constexpr uint32_t SM_QT = 114688;    // Qd tf32 K-major: [kblock 4][64 rows (i) x 32 (k)]
 constexpr uint32_t SM_C0 = 147456;    // C tf32 K-major: [kblock 2][64 rows (i) x 32 (j)], x2
 constexpr uint32_t SM_C1 = 163840;
-constexpr uint32_t SM_AB = 180224;    // A diag(beta) bf16 64 x 64; L fp32 (16 KB) before it
-constexpr uint32_t SM_ABG = 188416;   // A diag(beta 2^Gx) bf16 64 x 64
-constexpr uint32_t SM_AS = 196608;    // A fp32 64 x 64 (swizzled)
-constexpr uint32_t SM_YS = 212992;    // per-warp 16 x 8 fp32 scratch of the inverse (4 KB)
-constexpr uint32_t SM_SCAL = 217088;  // per-chunk scalars [parity 2][8][64] + gates [stage 2][2][64]
-constexpr uint32_t SM_BAR = 222208;   // mbarriers and flags
-constexpr uint32_t SM_END = 222336;
+constexpr uint32_t SM_A0 = 180224;    // stage 0 WY tiles: A diag(beta) | A diag(beta 2^Gx), bf16
+constexpr uint32_t SM_A1 = 196608;    // stage 1
+constexpr uint32_t SM_SCAL = 212992;  // per-chunk scalars [parity 2][SC_N][64] + gates [stage 2][64]
+constexpr uint32_t SM_BAR = 215552;   // mbarriers and flags
+constexpr uint32_t SM_END = 215680;
 constexpr uint32_t kSmemBytes = SM_END + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // per-chunk scalar arrays (offsets in units of 64 floats within a parity block)
-enum { SC_GAM = 0, SC_GX, SC_DD, SC_BET, SC_BEKR, SC_EG, SC_MISC, SC_N = 8 };
+enum { SC_GAM = 0, SC_DD, SC_EG, SC_MISC, SC_N = 4 };
 
 // mbarrier slots and flags at SM_BAR
 constexpr uint32_t B_FULL0 = 0, B_FULL1 = 8, B_EMPTY0 = 16, B_EMPTY1 = 24, B_VEMPTY = 32,
@@ -102,291 +98,6 @@ struct TcParams {
     ChainParams c;
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
-
-// ------------------------------------------------------------------------------------
-// PTX wrappers
-// ------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_try_wait, but the hardware may suspend the waiting warp for up to `hint_ns`
-// nanoseconds until the phase completes, instead of the warp re-polling and taking issue
-// slots from the warps it shares a scheduler with.
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
-                                                      uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void record_error(DeviceError* e, unsigned code, unsigned detail) {
-    if (e && atomicCAS(&e->code, 0u, code) == 0u) atomicExch(&e->detail, detail);
-}
-
-// Bounded wait for the completion of the phase with the given parity. Gives up when the
-// CTA's abort flag is raised or after `limit` SM cycles (then records the timeout and
-// raises the flag). Returns false if it gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       long long limit, DeviceError* err, unsigned tag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        // suspended in hardware (up to 20 us per try) rather than re-polling: a polling warp
-        // starves the compute warps on its scheduler
-        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > limit) {
-            record_error(err, GDN_ERR_TIMEOUT, tag);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-// Bounded wait used only while shutting down after an abort: lets copies or MMAs this CTA
-// issued retire before its shared and tensor memory are released.
-__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > limit) return;
-}
-
-// The first warp of a warp group waits (when `doit`) -- all of its lanes poll together and
-// see identical values, so the warp stays converged -- and its lane 0 publishes a verdict
-// before the group's named barrier; every thread of the group then reads the same verdict,
-// so a timeout can never split the group between a barrier and a break.
-template <int BAR_ID>
-__device__ __forceinline__ bool group_wait(bool leader_warp, bool lane0, uint32_t bar,
-                                           uint32_t parity, bool doit, volatile int* go,
-                                           volatile int* abort_flag, long long limit,
-                                           DeviceError* err, unsigned tag) {
-    if (leader_warp) {
-        const bool ok = !doit || mbar_wait(bar, parity, abort_flag, limit, err, tag);
-        if (lane0) *go = (ok && !*abort_flag) ? 1 : 0;
-    }
-    if (BAR_ID == 1) asm volatile("barrier.sync 1, 128;" ::: "memory");
-    else asm volatile("barrier.sync 2, 128;" ::: "memory");
-    __syncwarp();   // the leader warp diverged around its poll: reconverge before .aligned work
-    return *go != 0;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void state_bar() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void prep_bar() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
-template <int ID>
-__device__ __forceinline__ void group_bar() {
-    if (ID == 1) state_bar();
-    else prep_bar();
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return y;
-}
-
-// Shared-memory matrix descriptor (sm_100 format): start, leading/stride byte offsets,
-// version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-// K-major operand: rows of 128 bytes packed in 8-row groups of 1024 bytes
-__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return sdesc(saddr, 16, 1024); }
-// MN-major operand: 64-element blocks along M/N `mn_stride` bytes apart, 8-row groups along
-// K 1024 bytes apart
-__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t mn_stride) {
-    return sdesc(saddr, mn_stride, 1024);
-}
-
-// Instruction descriptors (dense, fp32 D). kind::f16 with bf16 A and B:
-constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-constexpr uint32_t ID_P1 = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_P23 = idesc_bf16(128, 64, true, false);
-constexpr uint32_t ID_S4 = idesc_bf16(128, 128, false, true);   // A from tensor memory
-// kind::tf32, M = 128, N = 64, A from tensor memory, B K-major (S1, S2, S3)
-constexpr uint32_t ID_TF = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
-                           ((uint32_t)(128 >> 4) << 24);
-
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t id, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t id, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// Tensor-memory accesses of this thread's lane: 16 or 8 consecutive 32-bit columns. The
-// kernel walks wide rows in rolled loops over such groups: each chunk executes its code
-// once, so compact loops (rather than fully unrolled rows) keep it in the instruction cache.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&t);
-}
-
-// byte address of 16-byte chunk `c` of row `row` in a 128-byte-swizzled tile of 128-byte rows
-__device__ __forceinline__ uint32_t sw128(int row, int c) {
-    return (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-}
-
-__device__ __forceinline__ float bf16_at(const void* base, long long idx) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
-}
-
-// 64 x 64 fp32 matrices of the inverse: row-major with the column XOR-swizzled by the row,
-// so both row-wise and column-wise walks by a warp hit 32 distinct banks
-__device__ __forceinline__ int sw64(int i, int j) { return i * 64 + (j ^ (i & 31)); }
-
-// D = A B + D on the warp-level tensor path, m16n8k8, tf32 in, fp32 accumulate
-__device__ __forceinline__ void mma_m16n8k8(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// m16n8k8 fragments from swizzled fp32 64x64 matrices (rows r0.., cols c0..)
-__device__ __forceinline__ void frag_a(const float* M, int r0, int c0, int lane, uint32_t* a) {
-    const int g = lane >> 2, t = lane & 3;
-    a[0] = tf32_bits(M[sw64(r0 + g, c0 + t)]);
-    a[1] = tf32_bits(M[sw64(r0 + g + 8, c0 + t)]);
-    a[2] = tf32_bits(M[sw64(r0 + g, c0 + t + 4)]);
-    a[3] = tf32_bits(M[sw64(r0 + g + 8, c0 + t + 4)]);
-}
-__device__ __forceinline__ void frag_b(const float* M, int r0, int c0, int lane, uint32_t* b) {
-    const int g = lane >> 2, t = lane & 3;
-    b[0] = tf32_bits(M[sw64(r0 + t, c0 + g)]);
-    b[1] = tf32_bits(M[sw64(r0 + t + 4, c0 + g)]);
-}
 
 // 64 token rows of one output column from a 64-column O^T buffer in tensor memory
 __device__ __forceinline__ void store_o_rows(const ChainParams& c, uint32_t t_col, long long idx0,
@@ -420,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
     uint8_t* sm = smem_raw + (base - raw);
 
     float* scal = reinterpret_cast<float*>(sm + SM_SCAL);              // [parity][SC_N][64]
-    float* gates = reinterpret_cast<float*>(sm + SM_SCAL + 4096);      // [stage][g | beta][64]
+    float* gates = reinterpret_cast<float*>(sm + SM_SCAL + 2 * SC_N * 256);   // [stage][64]
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + SM_BAR + B_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + B_ABORT);
     const uint32_t bar0 = base + SM_BAR;
@@ -473,10 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
 
     if (warp == 8) {
         // ================================ producer ================================
-        // K and Q tiles (and the gates) go to a two-stage ring released after S4; the V tile
-        // has its own single buffer released after P2, so a chunk's K and Q are never held
-        // back by the previous chunk's V.
-        const uint32_t tx = 16384u + (SUMMARY ? 0u : 16384u);
+        // K and Q tiles, the WY tiles and the gates go to a two-stage ring released after
+        // S4; the V tile has its own single buffer released after P2, so a chunk's K and Q are
+        // never held back by the previous chunk's V. The M part needs only A diag(beta 2^Gx).
+        const uint32_t wy_bytes = need_v ? 16384u : 8192u;
+        const uint32_t wy_skip = 16384u - wy_bytes;
+        const uint32_t tx = 16384u + (SUMMARY ? 0u : 16384u) + wy_bytes;
+        const uint8_t* wy_chain = reinterpret_cast<const uint8_t*>(c.wy) +
+                                  (((long long)bh * (c.T / kC) + (long long)seg * nchunks) << 14);
         int issued_last[2] = {-1, -1}, v_issued_last = -1;
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
@@ -496,15 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                     tma_load_3d(kq + hf * 16384, &p.tm_k, full, hf * 64, h, row0);
                     if (!SUMMARY) tma_load_3d(kq + hf * 16384 + 8192, &p.tm_q, full, hf * 64, h, row0);
                 }
+                bulk_load(base + (s ? SM_A1 : SM_A0) + wy_skip,
+                          wy_chain + ((long long)n << 14) + wy_skip, wy_bytes, full);
             }
             if (s) issued_last[1] = n; else issued_last[0] = n;
-            float* gs = gates + s * 128;
+            float* gs = gates + s * 64;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int i = lane + 32 * e;
-                const long long idx = (long long)(row0 + i) * c.H + h;
-                gs[i] = bf16_at(c.g, idx) * kLog2e;
-                gs[64 + i] = bf16_at(c.beta, idx);
+                gs[i] = bf16_at(c.g, (long long)(row0 + i) * c.H + h) * kLog2e;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(full);
@@ -534,9 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         volatile int* go = reinterpret_cast<volatile int*>(sm + SM_BAR + B_GO_P);
         uint32_t barp_phase = 0;
         bool barp_pending = false;
-        float* Lm = reinterpret_cast<float*>(sm + SM_AB);   // L, fp32, until the inverse is done
-        float* Am = reinterpret_cast<float*>(sm + SM_AS);
-        float* Ys = reinterpret_cast<float*>(sm + SM_YS) + pw * 128;
 
         // the group's first warp waits (optionally) and publishes a verdict that all read
         // after the named barrier, so a timeout cannot split the group
@@ -549,12 +261,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             const uint32_t kq = base + (s ? SM_KQ1 : SM_KQ0);
+            const uint32_t wyt = base + (s ? SM_A1 : SM_A0);
             float* sc = scal + (n & 1) * (SC_N * 64);
             if (!pwait(bar0 + (s ? B_FULL1 : B_FULL0), (n >> 1) & 1, TAG_FULL, true)) break;
 
+            // ---- P1: [K ; Q] K^T -> TM_S; rows 64..127 (Q K^T) give C
+            if (!SUMMARY && pt == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    mma_ss(tmem + TM_S, desc_k(kq + off), desc_k(kq + off), ID_P1, ks > 0);
+                }
+                mma_commit(bar0 + B_BARP);
+            }
             // ---- gate cumsum and per-chunk scalars (first prep warp)
             if (pw == 0) {
-                const float* gs = gates + s * 128;
+                const float* gs = gates + s * 64;
                 const float g0 = gs[2 * lane], g1 = gs[2 * lane + 1];
                 float sum = g0 + g1;
 #pragma unroll
@@ -565,56 +288,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 const float excl = sum - (g0 + g1);
                 const float glast = __shfl_sync(0xffffffffu, sum, 31);
                 const float G0 = excl + g0, G1 = excl + g0 + g1;
-                const float b0 = gs[64 + 2 * lane], b1 = gs[64 + 2 * lane + 1];
                 sc[SC_GAM * 64 + 2 * lane] = G0;
                 sc[SC_GAM * 64 + 2 * lane + 1] = G1;
-                sc[SC_GX * 64 + 2 * lane] = excl;
-                sc[SC_GX * 64 + 2 * lane + 1] = G0;
                 sc[SC_DD * 64 + 2 * lane] = ex2(glast - G0);
                 sc[SC_DD * 64 + 2 * lane + 1] = ex2(glast - G1);
                 sc[SC_EG * 64 + 2 * lane] = ex2(G0);
                 sc[SC_EG * 64 + 2 * lane + 1] = ex2(G1);
-                sc[SC_BET * 64 + 2 * lane] = b0;
-                sc[SC_BET * 64 + 2 * lane + 1] = b1;
-                sc[SC_BEKR * 64 + 2 * lane] = b0 * ex2(excl);
-                sc[SC_BEKR * 64 + 2 * lane + 1] = b1 * ex2(G0);
                 if (lane == 0) sc[SC_MISC * 64] = ex2(glast);
             }
-            // ---- P1: [K ; Q] K^T -> TM_S (needs only the loaded tiles)
-            if (pt == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    mma_ss(tmem + TM_S, desc_k(kq + off), desc_k(kq + off), ID_P1, ks > 0);
-                }
-                mma_commit(bar0 + B_BARP);
-            }
             __syncwarp();
-            barp_pending = true;
-            if (!pmma_wait()) break;   // its barrier also publishes the scalars
-            tc_fence_after();
-
-            // ---- L rows (lanes 0..63, fp32) and C rows (lanes 64..127, tf32), 16 columns
-            //      at a time
-            {
-                const float* gam = sc + SC_GAM * 64;
-                const int i = pt & 63;
-                const float gi = (pt < 64) ? sc[SC_GX * 64 + i] : gam[i];
-                const float bi = (pt < 64) ? sc[SC_BET * 64 + i] : 1.f;
-                uint8_t* ctile = sm + ((n & 1) ? SM_C1 : SM_C0);
+            if (!SUMMARY) {
+                barp_pending = true;
+                if (!pmma_wait()) break;   // its barrier also publishes the scalars
+                tc_fence_after();
+                // C and Qd overwrite what chunk n-2's S3 and chunk n-1's S2 read
+                if (!pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
+                if (pt >= 64) {
+                    // ---- C rows (lanes 64..127), tf32 K-major, 16 columns at a time
+                    const float* gam = sc + SC_GAM * 64;
+                    const int i = pt & 63;
+                    const float gi = gam[i];
+                    uint8_t* ctile = sm + ((n & 1) ? SM_C1 : SM_C0);
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    float sv[16];
-                    tmem_ld16(t_row + TM_S + 16 * g, sv);
-                    tmem_wait_ld();
-                    if (pt < 64) {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int j = 16 * g + jj;
-                            Lm[sw64(i, j)] = (j < i) ? bi * ex2(gi - gam[j]) * sv[jj] : 0.f;
-                        }
-                    } else if (!SUMMARY) {
+                    for (int g = 0; g < 4; ++g) {
+                        float sv[16];
+                        tmem_ld16(t_row + TM_S + 16 * g, sv);
+                        tmem_wait_ld();
                         uint32_t t[16];
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
@@ -628,99 +327,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                             *reinterpret_cast<uint4*>(blkp + sw128(i, 4 * (g & 1) + q)) =
                                 make_uint4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
                     }
-                }
-            }
-            tc_fence_before();
-            prep_bar();
-
-            // ---- diagonal 16x16 blocks of (I + L)^-1: lane r of a 16-lane group owns row r
-            //      of the block's inverse, X[r] = e_r - sum_{m<r} L[r][m] X[m], with row m
-            //      broadcast by shuffles once it is final. Rows are zero beyond their diagonal,
-            //      so the updates run over all 16 columns with constant bounds.
-            if (pt < 64) {
-                const int bs = (pt >> 4) * 16, r = pt & 15, src0 = lane & 16;
-                float x[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) x[m] = (m == r) ? 1.f : 0.f;
+                } else {
+                    // ---- Qd = 2^G_i q_i as tf32 K-major (threads 0..63: row i = pt)
+                    const int i = pt;
+                    const float egi = sc[SC_EG * 64 + i];
 #pragma unroll 1
-                for (int m = 0; m < 15; ++m) {
-                    const float f = (r > m) ? Lm[sw64(bs + r, bs + m)] : 0.f;
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        const float xm = __shfl_sync(0xffffffffu, x[cc], src0 + m);
-                        x[cc] = fmaf(-f, xm, x[cc]);
-                    }
-                }
-#pragma unroll
-                for (int cc = 0; cc < 16; ++cc) Am[sw64(bs + r, bs + cc)] = x[cc];
-            } else {
-                // zero the blocks above the diagonal
-#pragma unroll 1
-                for (int e = pt - 64; e < 6 * 256; e += 64) {
-                    const int blkid = e >> 8, w = e & 255;
-                    const int I = (blkid < 3) ? 0 : (blkid < 5 ? 1 : 2);
-                    const int J = (blkid < 3) ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-                    Am[sw64(16 * I + (w >> 4), 16 * J + (w & 15))] = 0.f;
-                }
-            }
-            prep_bar();
-            // ---- block forward substitution: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ
-#pragma unroll 1
-            for (int I = 1; I < 4; ++I) {
-#pragma unroll 1
-                for (int tile = pw; tile < 2 * I; tile += 4) {
-                    const int J = tile >> 1, n0 = 16 * J + 8 * (tile & 1);
-                    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                    for (int m = J; m < I; ++m)
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            uint32_t a[4], bb[2];
-                            frag_a(Lm, 16 * I, 16 * m + 8 * kk, lane, a);
-                            frag_b(Am, 16 * m + 8 * kk, n0, lane, bb);
-                            mma_m16n8k8(y, a, bb);
+                    for (int kh = 0; kh < 2; ++kh) {
+                        const uint8_t* src = sm + (s ? SM_KQ1 : SM_KQ0) + kh * 16384 + 8192;
+#pragma unroll 2
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
+                            const uint4 lo4 = make_uint4(
+                                tf32_bits(__uint_as_float(u.x << 16) * egi),
+                                tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
+                                tf32_bits(__uint_as_float(u.y << 16) * egi),
+                                tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
+                            const uint4 hi4 = make_uint4(
+                                tf32_bits(__uint_as_float(u.z << 16) * egi),
+                                tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
+                                tf32_bits(__uint_as_float(u.w << 16) * egi),
+                                tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
+                            // features 64 kh + 8 cc .. +7: tf32 block 2 kh + cc / 4, chunks
+                            // 2 (cc % 4) + {0, 1}
+                            uint8_t* dst = sm + SM_QT + (kh * 2 + (cc >> 2)) * 8192;
+                            *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc) & 7)) = lo4;
+                            *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc + 1) & 7)) = hi4;
                         }
-                    // the Y tile (16 x 8) goes through the warp's scratch, then X = -X_II Y
-                    const int g = lane >> 2, t = lane & 3;
-                    Ys[g * 8 + 2 * t] = y[0];
-                    Ys[g * 8 + 2 * t + 1] = y[1];
-                    Ys[(g + 8) * 8 + 2 * t] = y[2];
-                    Ys[(g + 8) * 8 + 2 * t + 1] = y[3];
-                    __syncwarp();
-                    float xo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        uint32_t a[4], bb[2];
-                        frag_a(Am, 16 * I, 16 * I + 8 * kk, lane, a);
-                        bb[0] = tf32_bits(Ys[(8 * kk + t) * 8 + g]);
-                        bb[1] = tf32_bits(Ys[(8 * kk + t + 4) * 8 + g]);
-                        mma_m16n8k8(xo, a, bb);
                     }
-                    __syncwarp();
-                    Am[sw64(16 * I + g, n0 + 2 * t)] = -xo[0];
-                    Am[sw64(16 * I + g, n0 + 2 * t + 1)] = -xo[1];
-                    Am[sw64(16 * I + g + 8, n0 + 2 * t)] = -xo[2];
-                    Am[sw64(16 * I + g + 8, n0 + 2 * t + 1)] = -xo[3];
                 }
-                prep_bar();
+                fence_proxy_async();
+                tc_fence_before();
+                prep_bar();   // TM_S has been read: P3 may overwrite it
             }
-            // ---- A diag(beta) and A diag(beta 2^Gx) as bf16 K-major rows (over L's space;
-            //      the last round's barrier retired every read of L)
-            {
-                const int i = pt & 63;
-                const float* scale = sc + ((pt < 64) ? SC_BET : SC_BEKR) * 64;
-                uint8_t* tile = sm + ((pt < 64) ? SM_AB : SM_ABG);
-#pragma unroll 1
-                for (int cq = 0; cq < 8; ++cq) {
-                    float a[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) a[jj] = Am[sw64(i, 8 * cq + jj)] * scale[8 * cq + jj];
-                    *reinterpret_cast<uint4*>(tile + sw128(i, cq)) =
-                        make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]),
-                                   pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
-                }
-            }
-            fence_proxy_async();
             // ---- P2 (U^T into the parity's U buffer, once chunk n-2's R is retired) and P3
             const uint32_t t_u = tmem + TM_U + (n & 1) * 64;
             if (!pwait(bar0 + ((n & 1) ? B_UFREE1 : B_UFREE0), ((n >> 1) - 1) & 1, TAG_UFREE,
@@ -732,13 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
                 if (need_v) {
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_ss(t_u, desc_mn(base + SM_V + ks * 2048, 8192),
-                               desc_k(base + SM_AB + ks * 32), ID_P23, ks > 0);
+                        mma_ss(t_u, desc_mn(base + SM_V + ks * 2048, 8192), desc_k(wyt + ks * 32),
+                               ID_P23, ks > 0);
                 }
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_ss(tmem + TM_S, desc_mn(kq + ks * 2048, 16384),
-                           desc_k(base + SM_ABG + ks * 32), ID_P23, ks > 0);
+                           desc_k(wyt + 8192 + ks * 32), ID_P23, ks > 0);
                 if (need_v) mma_commit(bar0 + B_VEMPTY);
                 mma_commit(bar0 + B_BARP);
             }
@@ -746,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
             barp_pending = true;
             if (!pmma_wait()) break;
             tc_fence_after();
-            // ---- -W and Qd as tf32 K-major B operands, once chunk n-1's S1/S2 retired
+            // ---- -W as a tf32 K-major B operand, once chunk n-1's S1 retired
             {
-                if (!pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
+                if (SUMMARY && !pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
                 // thread k holds column k of W^T's rows i: writes element (row i, feature k)
                 const int k = pt;
                 uint8_t* col = sm + SM_W + (k >> 5) * 8192 + (k & 3) * 4;
@@ -761,30 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
 #pragma unroll
                     for (int ii = 0; ii < 16; ++ii)
                         *reinterpret_cast<uint32_t*>(col + sw128(16 * g + ii, qk)) = tf32_bits(-w[ii]);
-                }
-                if (!SUMMARY) {
-                    // Q tile row i, half kh -> 2^G_i q_i as tf32
-                    const int i = pt >> 1, kh = pt & 1;
-                    const float egi = sc[SC_EG * 64 + i];
-                    const uint8_t* src = sm + (s ? SM_KQ1 : SM_KQ0) + kh * 16384 + 8192;
-#pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
-                        const uint4 lo4 = make_uint4(
-                            tf32_bits(__uint_as_float(u.x << 16) * egi),
-                            tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
-                            tf32_bits(__uint_as_float(u.y << 16) * egi),
-                            tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
-                        const uint4 hi4 = make_uint4(
-                            tf32_bits(__uint_as_float(u.z << 16) * egi),
-                            tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
-                            tf32_bits(__uint_as_float(u.w << 16) * egi),
-                            tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
-                        // features 64 kh + 8 cc .. +7: tf32 block 2 kh + cc / 4, chunks 2 (cc % 4) + {0, 1}
-                        uint8_t* dst = sm + SM_QT + (kh * 2 + (cc >> 2)) * 8192;
-                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc) & 7)) = lo4;
-                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc + 1) & 7)) = hi4;
-                    }
                 }
             }
             fence_proxy_async();
@@ -976,35 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chain_kernel(const __grid_cons
 // ------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// [B*T, H, 128] bf16 viewed as a 3-d tensor; box = 64 features x 1 head x 64 tokens
-bool make_map(CUtensorMap* m, const void* ptr, const ChainParams& c) {
-    auto fn = encode_fn();
-    if (!fn || !ptr) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)c.H, (cuuint64_t)c.B * (cuuint64_t)c.T};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)c.H * kD * 2};
-    cuuint32_t box[3] = {64, 1, 64};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool SUMMARY>
 cudaError_t launch(const ChainParams& c, cudaStream_t s) {
+    if (!c.wy) return cudaErrorInvalidValue;
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.c = c;

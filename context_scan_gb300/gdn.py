@@ -148,10 +148,13 @@ def gdn_segmented_fwd(q, k, v, g, beta, h0, o, h_final, nseg, workspace, H_in=No
 
 def gdn_segmented_fwd_timed(q, k, v, g, beta, h0, o, h_final, nseg, workspace, events,
                             H_in=None, stream=None, prob=None):
-    """gdn_segmented_fwd recording four torch.cuda.Event (enable_timing=True) around its
-    three stages: before summary, before scan, before forward, after forward."""
+    """gdn_segmented_fwd recording five torch.cuda.Event (enable_timing=True) around its
+    four stages: before the WY factors, before summary, before scan, before forward, after
+    forward."""
     prob = prob or problem(k, v, o)
-    arr = (_P * 4)(*[e.cuda_event for e in events])
+    if len(events) != 5:
+        raise ValueError("gdn_segmented_fwd_timed takes five events")
+    arr = (_P * 5)(*[e.cuda_event for e in events])
     _check(lib().gdn_segmented_fwd_timed(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
                                          _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
                                          _ptr(h_final), _ptr(H_in), _ptr(workspace),

@@ -90,7 +90,11 @@ typedef struct {
 } gdn_problem;
 
 /* Bytes of workspace the calls below need for this problem split into nseg segments
- * (nseg = 1 for gdn_chunk_fwd and gdn_segment_summary). Returns 0 for an invalid problem. */
+ * (nseg = 1 for gdn_chunk_fwd and gdn_segment_summary). Returns 0 for an invalid problem.
+ * It holds the error word; for the tensor-core shapes (bf16 in, K == V == 128) the
+ * per-chunk WY factors A diag(beta) and A diag(beta exp-decay), A = (I + L)^-1, as two bf16
+ * 64 x 64 tiles per chunk (16 KiB per chunk and head, formed by one launch before the
+ * chains); for nseg > 1 the segment summaries and scanned states. */
 GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
 
 /* Chunked forward over all T tokens from the initial state h0.
@@ -133,10 +137,11 @@ GDN_API gdn_status gdn_segmented_fwd(const gdn_problem* p, int nseg, const void*
                              size_t workspace_bytes, void* stream);
 
 /* gdn_segmented_fwd with stage markers, for timing each kernel from the caller. If
- * stage_events is non-NULL it points to four cudaEvent_t that are recorded on `stream`
- * before the summary launch, before the scan, before the forward launch and after it
- * (for nseg == 1 the first three are recorded back to back). Same results as
- * gdn_segmented_fwd. */
+ * stage_events is non-NULL it points to five cudaEvent_t that are recorded on `stream`
+ * before the WY-factor launch, before the summary launch, before the scan, before the
+ * forward launch and after it (the WY launch is skipped on the CUDA-core path; for
+ * nseg == 1 the first four are recorded back to back and the forward stage includes the
+ * WY launch). Same results as gdn_segmented_fwd. */
 GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q,
                                            const void* k, const void* v, const void* g,
                                            const void* beta, const float* h0, void* o,
@@ -153,11 +158,13 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
  * buffers imported from another process. (The pages have no counterpart: this is an
  * interface choice of this library.)
  *   Arguments and results are those of gdn_segmented_fwd, minus H_in_out and the
- *   workspace. The scratch (summaries, scanned states, the device error word) lives in one
+ *   workspace. The scratch (WY tiles, summaries, scanned states, the error word) lives in one
  *   array of GDN_NOALLOC_SCRATCH_BYTES in the library's own device memory; every GPU that
  *   loads the library holds it until the process exits. The call allocates nothing.
  *   Limit: problems with gdn_workspace_bytes(p, nseg) > GDN_NOALLOC_SCRATCH_BYTES are
- *   rejected with GDN_ERR_WORKSPACE (at K = V = 128: B*H*nseg at most 341).
+ *   rejected with GDN_ERR_WORKSPACE (at bf16, K = V = 128 that is
+ *   B*H*(T/64*16 KiB + nseg*192 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
+ *   T = 2048 in 4 segments take 40 MiB).
  *   device_error: optional (NULL to skip) 8-byte-aligned device pointer to two unsigned
  *   words that receive this call's device error word {code, detail} (see
  *   gdn_check_device_error for the codes) when the call's stream work completes.

@@ -64,10 +64,15 @@ def P(**kw):
 
 def test_workspace_bytes_and_status_strings(L):
     p = P(B=2, T=32768, H=32)
-    assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256
+    # bf16, K = V = 128: the error word and two 8 KiB WY tiles per chunk of each head
+    wy = 64 * (32768 // 64) * 16384
+    assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256 + wy
     n4 = L.gdn_workspace_bytes(ctypes.byref(p), 4)
-    # M, S and H_in for 4 segments of 64 heads, fp32
-    assert n4 >= 256 + 4 * 64 * 128 * 128 * 4 * 3
+    # plus M, S and H_in for 4 segments of 64 heads, fp32
+    assert n4 == 256 + wy + 4 * 64 * 128 * 128 * 4 * 3
+    # the CUDA-core shapes need no WY tiles
+    assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, in_dtype=0)), 1) == 256
+    assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, K=64, V=64)), 1) == 256
     assert L.gdn_workspace_bytes(ctypes.byref(P(K=96, V=96)), 1) == 0
     assert L.gdn_workspace_bytes(ctypes.byref(P(T=100)), 1) == 0
     assert L.gdn_workspace_bytes(ctypes.byref(P(T=128)), 4) == 0   # 128 % (64*4) != 0

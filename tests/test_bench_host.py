@@ -64,6 +64,11 @@ def test_algorithmic_model_matches_hand_count():
     assert stages["summary"]["bytes"] >= tok_heads * 3 // 4 * 516
     t_roof = total["bytes"] / 6791.4e9
     assert 520e-6 < t_roof < 540e-6
+    # the WY stage: k, g, beta in, two 8 KiB tiles per chunk out; not part of the path total
+    assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 16384
+    assert total["bytes"] == sum(stages[n]["bytes"] for n in ("summary", "scan", "forward"))
+    assert bench.launches_per_step(w) == 4
+    assert bench.launches_per_step(synth.WORKLOADS["tiny_f32_k64_cp4"]) == 3
 
 
 @pytest.mark.parametrize("steps", [3])
