@@ -241,7 +241,8 @@ def run_ours(args):
     w0 = synth.WORKLOADS[args.workload]
     w = synth.scaled(w0, seed=w0.seed + rank_seed_offset(rank),
                      per_sequence_seed=(None if w0.per_sequence_seed is None
-                                        else w0.per_sequence_seed + rank_seed_offset(rank)))
+                                        else w0.per_sequence_seed + rank_seed_offset(rank)),
+                     **({} if args.T is None else {"T": args.T}))
     x = synth.make_inputs(w)
     dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
     names = ("q", "k", "v", "g", "beta")
@@ -463,6 +464,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--T", type=int, default=None,
+                    help="run the workload at this sequence length instead (a smaller case of "
+                         "the same kernels for profiler captures; not a bench line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

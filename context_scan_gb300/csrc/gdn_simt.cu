@@ -291,42 +291,91 @@ cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
 }
 
 // Exclusive scan H_in[0] = h0, H_in[s] = M[s-1] H_in[s-1] + S[s-1], fp32, one CTA per
-// (head, 32-column tile); the serial dependency runs over segments inside the CTA.
-__global__ void __launch_bounds__(kThreads)
+// (head, 32-column tile); the serial dependency runs over segments inside the CTA. Each
+// step stages M[s-1] in shared memory (rows padded to KD + 4 floats) and every thread
+// accumulates a 4 x 4 block of the product in registers, four terms of the sum at a time.
+template <int KD>
+__global__ void __launch_bounds__(KD * 2)
 scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
-            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int K,
-            int V) {
-    extern __shared__ float sm[];
-    constexpr int CT = 32;
-    float* Hc = sm;            // K x CT
-    float* Hn = sm + K * CT;   // K x CT
+            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int V) {
+    constexpr int CT = 32, NT = KD * 2, MP = KD + 4;
+    extern __shared__ float4 sm4[];
+    float* Ms = reinterpret_cast<float*>(sm4);   // KD x MP
+    float* Hc = Ms + KD * MP;                    // KD x CT, the current state's column tile
     const int bh = blockIdx.x, c0 = blockIdx.y * CT, tid = threadIdx.x;
-    for (int e = tid; e < K * CT; e += kThreads) {
-        const int l = e / CT, c = e % CT;
-        Hc[e] = h0 ? h0[((long long)bh * K + l) * V + c0 + c] : 0.f;
+    const int ri = tid >> 3, ci = tid & 7;       // rows 4ri..4ri+3, columns 4ci..4ci+3
+    for (int e = tid; e < KD * CT / 4; e += NT) {
+        const int l = e / (CT / 4), c4 = e % (CT / 4);
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (h0) x = *reinterpret_cast<const float4*>(h0 + ((long long)bh * KD + l) * V + c0 + 4 * c4);
+        *reinterpret_cast<float4*>(Hc + l * CT + 4 * c4) = x;
     }
     __syncthreads();
     for (int s = 0; s < nseg; ++s) {
-        const long long hb = ((long long)s * BH + bh) * K;
-        for (int e = tid; e < K * CT; e += kThreads) {
-            const int l = e / CT, c = e % CT;
-            H_in[(hb + l) * V + c0 + c] = Hc[e];
+        const long long hb = ((long long)s * BH + bh) * KD;
+        for (int e = tid; e < KD * CT / 4; e += NT) {
+            const int l = e / (CT / 4), c4 = e % (CT / 4);
+            *reinterpret_cast<float4*>(H_in + (hb + l) * V + c0 + 4 * c4) =
+                *reinterpret_cast<const float4*>(Hc + l * CT + 4 * c4);
         }
         if (s == nseg - 1) break;
-        const float* Ms = M + ((long long)s * BH + bh) * K * K;
-        const float* Ss = S + ((long long)s * BH + bh) * K * V;
-        for (int e = tid; e < K * CT; e += kThreads) {
-            const int i = e / CT, c = e % CT;
-            float a = Ss[(long long)i * V + c0 + c];
-            for (int l = 0; l < K; ++l) a = fmaf(__ldg(&Ms[(long long)i * K + l]), Hc[l * CT + c], a);
-            Hn[e] = a;
+        const float* Mg = M + ((long long)s * BH + bh) * KD * KD;
+        const float* Sg = S + ((long long)s * BH + bh) * KD * V;
+        for (int e = tid; e < KD * KD / 4; e += NT) {
+            const int i = e / (KD / 4), l4 = e % (KD / 4);
+            *reinterpret_cast<float4*>(Ms + i * MP + 4 * l4) =
+                __ldg(reinterpret_cast<const float4*>(Mg + (long long)i * KD + 4 * l4));
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(
+                Sg + (long long)(4 * ri + r) * V + c0 + 4 * ci));
+            acc[r][0] = x.x;
+            acc[r][1] = x.y;
+            acc[r][2] = x.z;
+            acc[r][3] = x.w;
         }
         __syncthreads();
-        for (int e = tid; e < K * CT; e += kThreads) Hc[e] = Hn[e];
+#pragma unroll 2
+        for (int l = 0; l < KD; l += 4) {
+            float4 m[4], hv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) m[r] = *reinterpret_cast<const float4*>(Ms + (4 * ri + r) * MP + l);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hv[q] = *reinterpret_cast<const float4*>(Hc + (l + q) * CT + 4 * ci);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float mr[4] = {m[r].x, m[r].y, m[r].z, m[r].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[r][0] = fmaf(mr[q], hv[q].x, acc[r][0]);
+                    acc[r][1] = fmaf(mr[q], hv[q].y, acc[r][1]);
+                    acc[r][2] = fmaf(mr[q], hv[q].z, acc[r][2]);
+                    acc[r][3] = fmaf(mr[q], hv[q].w, acc[r][3]);
+                }
+            }
+        }
+        __syncthreads();   // every read of Hc and Ms is done
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(Hc + (4 * ri + r) * CT + 4 * ci) =
+                make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         __syncthreads();
     }
 }
 
+template <int KD>
+cudaError_t launch_scan_k(const float* M, const float* S, const float* h0, float* H_in, int nseg,
+                          int BH, int V, cudaStream_t s) {
+    const size_t smem = sizeof(float) * ((size_t)KD * (KD + 4) + (size_t)KD * 32);
+    cudaError_t e = cudaFuncSetAttribute(scan_kernel<KD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)BH, (unsigned)(V / 32));
+    scan_kernel<KD><<<grid, KD * 2, smem, s>>>(M, S, h0, H_in, nseg, BH, V);
+    return cudaGetLastError();
+}
 }  // namespace
 
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s) {
@@ -339,10 +388,9 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s) {
 
 cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
                         int BH, int K, int V, cudaStream_t s) {
-    const size_t smem = sizeof(float) * 2 * K * 32;
-    dim3 grid((unsigned)BH, (unsigned)(V / 32));
-    scan_kernel<<<grid, kThreads, smem, s>>>(M, S, h0, H_in, nseg, BH, K, V);
-    return cudaGetLastError();
+    if (K == 128) return launch_scan_k<128>(M, S, h0, H_in, nseg, BH, V, s);
+    if (K == 64) return launch_scan_k<64>(M, S, h0, H_in, nseg, BH, V, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gdn

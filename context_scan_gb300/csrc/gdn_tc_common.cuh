@@ -96,11 +96,18 @@ __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, long long
         if (clock64() - t0 > limit) return;
 }
 
+// Named barrier over `N` threads (non-.aligned form: the threads of a warp may arrive
+// diverged, e.g. after a leader warp's lane-0 work).
+template <int ID, int N>
+__device__ __forceinline__ void named_bar() {
+    asm volatile("barrier.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+
 // The first warp of a warp group waits (when `doit`) -- all of its lanes poll together and
 // see identical values, so the warp stays converged -- and its lane 0 publishes a verdict
 // before the group's named barrier; every thread of the group then reads the same verdict,
 // so a timeout can never split the group between a barrier and a break.
-template <int BAR_ID>
+template <int ID, int N>
 __device__ __forceinline__ bool group_wait(bool leader_warp, bool lane0, uint32_t bar,
                                            uint32_t parity, bool doit, volatile int* go,
                                            volatile int* abort_flag, long long limit,
@@ -109,8 +116,7 @@ __device__ __forceinline__ bool group_wait(bool leader_warp, bool lane0, uint32_
         const bool ok = !doit || mbar_wait(bar, parity, abort_flag, limit, err, tag);
         if (lane0) *go = (ok && !*abort_flag) ? 1 : 0;
     }
-    if (BAR_ID == 1) asm volatile("barrier.sync 1, 128;" ::: "memory");
-    else asm volatile("barrier.sync 2, 128;" ::: "memory");
+    named_bar<ID, N>();
     __syncwarp();   // the leader warp diverged around its poll: reconverge before .aligned work
     return *go != 0;
 }
@@ -143,14 +149,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void state_bar() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void prep_bar() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
-template <int ID>
-__device__ __forceinline__ void group_bar() {
-    if (ID == 1) state_bar();
-    else prep_bar();
-}
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -192,34 +190,42 @@ constexpr uint32_t ID_S4 = idesc_bf16(128, 128, false, true);   // A from tensor
 // kind::tf32, M = 128, N = 64, A from tensor memory, B K-major (S1, S2, S3)
 constexpr uint32_t ID_TF = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
                            ((uint32_t)(128 >> 4) << 24);
+// kind::tf32, M = 128, N = 128 (the forward's fused R^T | O^T product)
+constexpr uint32_t ID_TF128 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                              ((uint32_t)(128 >> 4) << 24);
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                       uint32_t accumulate) {
+// The instruction descriptor is an immediate (template argument): the issuing thread then
+// spends no instructions moving it into place, which keeps back-to-back MMAs from being
+// issue-bound.
+template <uint32_t ID>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        "l"(a), "l"(b), "n"(ID), "r"(accumulate)
         : "memory");
 }
 
+template <uint32_t ID>
 __device__ __forceinline__ void mma_ts_tf32(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t id, uint32_t accumulate) {
+                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        "r"(a_tmem), "l"(b), "n"(ID), "r"(accumulate)
         : "memory");
 }
 
+template <uint32_t ID>
 __device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                            uint32_t id, uint32_t accumulate) {
+                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        "r"(a_tmem), "l"(b), "n"(ID), "r"(accumulate)
         : "memory");
 }
 
