@@ -60,18 +60,35 @@ namespace {
 
 constexpr int kD = 128;         // K == V
 constexpr int kC = 64;          // tokens per chunk
-constexpr int kThreads = 416;   // 4 state warps + 8 prep warps + 1 producer warp
-constexpr int kPrepThreads = 256;
-constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRenorm = -64.f;   // log2 of the smallest sigma kept without folding
 
-// tensor-memory columns (32-bit cells, 128 lanes)
-constexpr uint32_t TM_S = 0;     // Q K^T, then W^T                           (prep)
-constexpr uint32_t TM_U = 64;    // two buffers by chunk parity: U^T -> R^T, and in the
-                                 // forward O^T right after it (64 + 128 p: R^T | O^T)
-constexpr uint32_t TM_RD = 320;  // scaled R^T as packed bf16: hi 320..351, lo 352..383
-constexpr uint32_t TM_H = 384;   // state master H_s^T (128 columns)
+// Warps and tensor memory (32-bit cells, 128 lanes); one CTA per SM. The forward has one
+// state warp group and two prep warp groups; a summary CTA carries both blocks of the
+// augmented state -- the M part (from I, values 0) and the S part (from 0, values v) -- in
+// two state warp groups fed by one prep group, which forms the shared W once per chunk.
+template <bool SUMMARY>
+struct Cfg {
+    static constexpr int NSG = SUMMARY ? 2 : 1;              // state warp groups
+    static constexpr int NGRP = SUMMARY ? 1 : 2;             // prep warp groups
+    static constexpr int PREP_WARP0 = 4 * NSG;
+    static constexpr int PREP_THREADS = 128 * NGRP;
+    static constexpr int PRODUCER_WARP = 4 * NSG + 4 * NGRP;
+    static constexpr int THREADS = 32 * PRODUCER_WARP + 32;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TM_S = 0;    // Q K^T, then W^T (prep)
+    static constexpr uint32_t TM_U = 64;   // U^T -> R^T, two buffers by chunk parity; the
+                                           // forward keeps O^T right after each (64 + 128 p)
+    static constexpr int NUB = 2;                            // U buffers
+    static constexpr uint32_t TU_STRIDE = SUMMARY ? 64 : 128;
+    // scaled R^T packed as bf16 pairs, 16 tokens per 16 columns: hi in the first 8, lo in
+    // the next 8. The forward keeps R^T for S3 and packs into its own 64 columns (TM_RD);
+    // the summary (no S3) packs in place over R^T.
+    static constexpr uint32_t TM_RD = 320;
+    static constexpr uint32_t TM_RM = 192;   // summary: R^T of the M part (one buffer)
+    // state master H_s^T (128 columns) of state group sg: forward 384; summary M 256, S 384
+    __host__ __device__ static constexpr uint32_t tm_h(int sg) { return SUMMARY ? 256u + 128u * (uint32_t)sg : 384u; }
+};
 
 // Shared-memory map (bytes from a 1024-aligned base). A k, q or v tile is two 64-feature
 // halves of 64 rows x 128 bytes (8 KB each, 128-byte swizzle); a WY stage is the tile pair
@@ -96,7 +113,7 @@ struct Smem {
     static constexpr uint32_t BAR = GATES + KST * 256;           // gates [k stage][64]
     static constexpr uint32_t END = BAR + 256;
     static constexpr uint32_t BYTES = END + 1024;                // + alignment slack
-    static_assert(BYTES <= 232448, "shared memory budget");
+    static_assert(BYTES <= 232448u, "shared memory budget");
 };
 
 // per-chunk scalar arrays (offsets in units of 64 floats within a parity block)
@@ -108,7 +125,7 @@ enum { SC_GAM = 0, SC_DD, SC_EG, SC_MISC, SC_N = 4 };
 constexpr uint32_t B_KFULL = 0, B_KEMPTY = 32, B_QFULL = 64, B_QEMPTY = 80, B_AFULL = 96,
                    B_AEMPTY = 112, B_VFULL = 128, B_VEMPTY = 136, B_BARP = 144, B_BARS = 152,
                    B_PREPDONE = 160, B_WFREE = 168, B_UFREE = 176, B_TMEM = 192, B_ABORT = 196,
-                   B_GO_S = 200, B_GO_P = 204;
+                   B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216;
 
 // wait tags recorded in the device error word's detail field
 enum : unsigned {
@@ -128,11 +145,13 @@ struct TcParams {
 // 32 token rows of one output column from a 64-column O^T buffer in tensor memory
 __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_col, long long idx0,
                                                long long tok_stride) {
-#pragma unroll 1
+    float ov2[2][16];
+    tmem_ld16(t_col, ov2[0]);
+    tmem_ld16(t_col + 16, ov2[1]);
+    tmem_wait_ld();
+#pragma unroll
     for (int g = 0; g < 2; ++g) {
-        float ov[16];
-        tmem_ld16(t_col + 16 * g, ov);
-        tmem_wait_ld();
+        const float* ov = ov2[g];
         const long long base = idx0 + (long long)(16 * g) * tok_stride;
         if (c.out_bf16) {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(c.o) + base;
@@ -149,11 +168,15 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
 // ------------------------------------------------------------------------------------
 // the chain kernel
 // ------------------------------------------------------------------------------------
-// 13 warps are allocated registers as 16: bound them at 65536 / 512 per thread
+// Registers are allocated to warps in groups of four: 13 warps count as 16, so at most 128
+// registers per thread.
 template <bool SUMMARY>
 __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant__ TcParams p) {
     using L = Smem<SUMMARY>;
-    constexpr int KST = L::KST, AST = L::AST;
+    using F = Cfg<SUMMARY>;
+    constexpr int KST = L::KST, AST = L::AST, NUB = F::NUB, NSG = F::NSG;
+    constexpr uint32_t TM_S = F::TM_S, TM_U = F::TM_U, TM_RD = F::TM_RD;
+    constexpr int kPrepThreads = F::PREP_THREADS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -167,17 +190,12 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 
     const ChainParams& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    int blk = 1;                    // 1: values are v (forward, or the S part); 0: M part
-    int chain = blockIdx.x;
-    if (SUMMARY) {
-        blk = chain & 1;
-        chain >>= 1;
-    }
+    const int chain = blockIdx.x;
     const int seg = chain % c.nseg_run;
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
     const int nchunks = c.seg_len / kC;
-    const bool need_v = !SUMMARY || blk == 1;
+    constexpr bool need_v = true;   // every CTA forms U (the forward, or the summary's S part)
     const long long limit = p.wait_limit;
     const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
     const long long row_seg = (long long)b * c.T + (long long)seg * c.seg_len;   // flattened (b, t)
@@ -185,23 +203,25 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     if (tid == 0) {
         for (int i = 0; i < KST; ++i) {
             mbar_init(bar0 + B_KFULL + 8 * i, 2);
-            mbar_init(bar0 + B_KEMPTY + 8 * i, 1);
+            mbar_init(bar0 + B_KEMPTY + 8 * i, NSG);   // each state group's S4 reads the k tile
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar0 + B_QFULL + 8 * i, 1);
             mbar_init(bar0 + B_QEMPTY + 8 * i, 1);
             mbar_init(bar0 + B_AFULL + 8 * i, 1);
             mbar_init(bar0 + B_AEMPTY + 8 * i, 1);
-            mbar_init(bar0 + B_UFREE + 8 * i, 1);
+            mbar_init(bar0 + B_UFREE + 8 * i, NSG);
         }
         mbar_init(bar0 + B_VFULL, 1);
         mbar_init(bar0 + B_VEMPTY, 1);
         mbar_init(bar0 + B_BARP, 1);
         mbar_init(bar0 + B_BARS, 1);
+        mbar_init(bar0 + B_BARS1, 1);
         mbar_init(bar0 + B_PREPDONE, 1);
-        mbar_init(bar0 + B_WFREE, 1);
+        mbar_init(bar0 + B_WFREE, NSG);   // each state group's S1 reads -sigma W
         *abort_flag = 0;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S) = 1;
+        *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S1) = 1;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_P) = 1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          bar0 + B_TMEM),
-                     "r"(kTmemCols)
+                     "r"(F::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -218,7 +238,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 12) {
+    if (warp == F::PRODUCER_WARP) {
         // ================================ producer ================================
         // The whole warp runs the loop (its lanes poll together and stay converged); lane 0
         // issues the copies, every lane loads two gates. The gates of chunk n+1 are loaded
@@ -312,15 +332,16 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             if (v_last >= 0) mbar_drain(bar0 + B_VFULL, v_last & 1, limit);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= F::PREP_WARP0) {
         // ================================== prep ==================================
-        const int pt = tid - 128, pw = warp - 4;
-        const int grp = pw >> 2, lq = pw & 3;   // warp group (0, 1); tensor-memory lane quarter
+        const int pt = tid - 32 * F::PREP_WARP0, pw = warp - F::PREP_WARP0;
+        const int grp = pw >> 2, lq = pw & 3;   // warp group; tensor-memory lane quarter
+        constexpr int ECOLS = 64 / F::NGRP;      // W^T / O^T columns per warp group
         const uint32_t t_row = tmem + ((uint32_t)(lq * 32) << 16);   // this warp's TMEM lanes
         volatile int* go = reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_P);
         uint32_t barp_phase = 0;
         bool barp_pending = false;
-        float lam = 0.f;   // log2 sigma before the current chunk (first prep warp)
+        float lam = 0.f;   // log2 sigma before the current chunk (prep warp pw 2)
 
         // the group's first warp waits (optionally) and publishes a verdict that all read
         // after the named barrier, so a timeout cannot split the group
@@ -329,6 +350,14 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                                 limit, c.err, (tag))
 #define pmma_wait() \
     (pwait(bar0 + B_BARP, barp_phase, TAG_BARP, true) ? (barp_phase ^= 1u, barp_pending = false, true) : false)
+// A warp waits on its own (all lanes poll together; lane 0's verdict is broadcast, so the
+// warp stays uniform). If it gives up, the abort flag is up and the group stops at its next
+// group wait.
+#define warp_wait(bar, parity, abort_flag_, limit_, err_, tag, lane_, ...)                       \
+    (__shfl_sync(0xffffffffu,                                                                 \
+                 (int)(!(true __VA_OPT__(&& (__VA_ARGS__))) ||                                 \
+                       mbar_wait((bar), (parity), (abort_flag_), (limit_), (err_), (tag))),    \
+                 0) != 0)
 // output rows of chunk m from its O^T buffer: lanes v, this warp group's 32 token columns
 #define store_output(m)                                                                       \
     store_o_rows32(c, t_row + TM_U + ((m) & 1) * 128 + 64 + 32 * grp,                          \
@@ -337,9 +366,15 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 
 // P1: [Q ; -] K^T -> TM_S for chunk m (k stage m % KST, q stage m & 1); lanes 0..63 hold
 // Q K^T. Rows 64..127 of the A operand run into the next buffer and are never read.
+// Only the issuing thread waits for the tiles (bounded); if it gives up it raises the abort
+// flag, issues nothing, and the group learns of it at its next group wait.
 #define issue_p1(m)                                                                           \
     do {                                                                                      \
-        if (pt == 0) {                                                                        \
+        if (pt == 0 &&                                                                        \
+            mbar_wait(bar0 + B_KFULL + 8 * ((m) % KST), ((m) / KST) & 1, abort_flag, limit,   \
+                      c.err, TAG_KFULL) &&                                                    \
+            mbar_wait(bar0 + B_QFULL + 8 * ((m) & 1), ((m) >> 1) & 1, abort_flag, limit,      \
+                      c.err, TAG_QFULL)) {                                                    \
             const uint32_t kst1 = base + L::K0 + ((m) % KST) * 16384;                          \
             const uint32_t qst1 = base + L::Q0 + ((m) & 1) * 16384;                            \
             tc_fence_after();                                                                 \
@@ -353,24 +388,53 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         barp_pending = true;                                                                  \
     } while (0)
 
-        bool run = true;
-        if (!SUMMARY && nchunks > 0) {
-            run = pwait(bar0 + B_KFULL, 0, TAG_KFULL, true) && pwait(bar0 + B_QFULL, 0, TAG_QFULL, true);
-            if (run) issue_p1(0);
-        }
+// this warp's lane quarter of the output rows of chunk n-2 (its group's 32 token columns),
+// then zero those cells of the parity's O^T buffer
+#define epilogue()                                                                            \
+    do {                                                                                      \
+        tc_fence_after();                                                                     \
+        if (n >= 2) store_output(n - 2);                                                      \
+        const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,                            \
+                                   0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};                           \
+        tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp, zero);                        \
+        tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp + 16, zero);                   \
+        tmem_wait_st();                                                                       \
+    } while (0)
+
+        if (!SUMMARY && nchunks > 0) issue_p1(0);
 #pragma unroll 1
-        for (int n = 0; run && n < nchunks; ++n) {
+        for (int n = 0; n < nchunks; ++n) {
             const int ks = n % KST, qs = n & 1, as = n % AST;
             const uint32_t kst = base + L::K0 + ks * 16384;
             const uint32_t ast = base + L::A0 + as * 16384;
-            const uint32_t t_u = tmem + TM_U + (n & 1) * L::TU_STRIDE;
+            const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
             float* sc = scal + (n & 1) * (SC_N * 64);
-            // chunk n-2 is retired: its scalars, U/R, O and C buffers may be reused
-            if (!pwait(bar0 + B_UFREE + 8 * (n & 1), ((n >> 1) - 1) & 1, TAG_UFREE, n >= 2)) break;
-            if (SUMMARY && !pwait(bar0 + B_KFULL + 8 * ks, (n / KST) & 1, TAG_KFULL, true)) break;
+            // chunk n-NUB is retired: its U/R (and in the forward O, C and scalar) buffers may
+            // be reused
+            if (!pwait(bar0 + B_UFREE + 8 * (n % NUB), ((n / NUB) - 1) & 1, TAG_UFREE, n >= NUB))
+                break;
+            // ---- forward: P2 (U^T into the parity's U buffer) right away; only the issuing
+            //      thread waits for the WY and v tiles. Its completion is covered by the commit
+            //      after P3 below.
+            if (!SUMMARY && pt == 0 &&
+                mbar_wait(bar0 + B_AFULL + 8 * as, (n / AST) & 1, abort_flag, limit, c.err, TAG_AFULL) &&
+                mbar_wait(bar0 + B_VFULL, n & 1, abort_flag, limit, c.err, TAG_VFULL)) {
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
+                                   desc_k(ast + k16 * 32), k16 > 0);
+                mma_commit(bar0 + B_VEMPTY);
+            }
 
-            // ---- gate cumsum, sigma bookkeeping and per-chunk scalars (first prep warp)
-            if (pw == 0) {
+            // ---- gate cumsum, sigma bookkeeping and per-chunk scalars (first prep warp; the
+            //      gates arrive with the chunk's k tile)
+            // (warp pw 2: warp pw 0 may be busy issuing P2)
+            const bool gates_ok =
+                pw == 2 && __shfl_sync(0xffffffffu,
+                                       (int)mbar_wait(bar0 + B_KFULL + 8 * ks, (n / KST) & 1,
+                                                      abort_flag, limit, c.err, TAG_KFULL), 0);
+            if (gates_ok) {
                 const float* gs = gates + ks * 64;
                 const float g0 = gs[2 * lane], g1 = gs[2 * lane + 1];
                 float sum = g0 + g1;
@@ -400,99 +464,118 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             __syncwarp();
             if (!SUMMARY) {
-                if (!pmma_wait()) break;   // P1 of this chunk; its barrier also publishes the scalars
-                tc_fence_after();
-                // C and sigma Qd overwrite what chunk n-1's S12 read
-                if (!pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
+                named_bar<2, kPrepThreads>();   // publishes the scalars
                 if (lq < 2) {
-                    // ---- C rows i = lanes 0..63, this group's 32 columns j, tf32 K-major
-                    const float* gam = sc + SC_GAM * 64;
-                    const int i = 32 * lq + lane;
-                    const float gi = gam[i];
-                    uint8_t* ctile = sm + L::C0 + (n & 1) * 16384 + grp * 8192;
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float sv[16];
-                        tmem_ld16(t_row + TM_S + 32 * grp + 16 * hh, sv);
+                    // ---- C rows i = lanes 0..63 (warps of lane quarters 0, 1), this group's 32
+                    //      columns j, tf32 K-major; then (one thread) P3, once every C warp has
+                    //      read Q K^T out of TM_S
+                    if (warp_wait(bar0 + B_BARP, barp_phase, abort_flag, limit, c.err, TAG_BARP, lane)) {
+                        tc_fence_after();
+                        const float* gam = sc + SC_GAM * 64;
+                        const int i = 32 * lq + lane;
+                        const float gi = gam[i];
+                        uint8_t* ctile = sm + L::C0 + (n & 1) * 16384 + grp * 8192;
+                        float sv2[2][16];
+                        tmem_ld16(t_row + TM_S + 32 * grp, sv2[0]);
+                        tmem_ld16(t_row + TM_S + 32 * grp + 16, sv2[1]);
                         tmem_wait_ld();
-                        uint32_t t[16];
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int j = 32 * grp + 16 * hh + jj;
-                            t[jj] = tf32_bits((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const float* sv = sv2[hh];
+                            uint32_t t[16];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int j = 32 * grp + 16 * hh + jj;
+                                t[jj] = tf32_bits((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
+                            }
+                            // columns 32 grp + 16 hh ..: tf32 block grp, 16-byte chunks 4 hh ..
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<uint4*>(ctile + sw128(i, 4 * hh + q)) =
+                                    make_uint4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
                         }
-                        // columns 32 grp + 16 hh ..: tf32 block grp, 16-byte chunks 4 hh ..
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4*>(ctile + sw128(i, 4 * hh + q)) =
-                                make_uint4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
                     }
+                    fence_proxy_async();
+                    tc_fence_before();
+                    named_bar<3, 128>();   // the C warps only
+                    if (pt == 0 && !*abort_flag) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
+                                           desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                        mma_commit(bar0 + B_AEMPTY + 8 * as);
+                        mma_commit(bar0 + B_BARP);
+                    }
+                    __syncwarp();
+                    // ---- while P3 runs: this warp's share of the output rows of chunk n-2
+                    //      (retired above), then zero it in its O^T buffer, which S12 of this
+                    //      chunk accumulates into
+                    epilogue();
                 } else {
-                    // ---- sigma Qd = sigma 2^G_i q_i as tf32 K-major: row i, feature half kh
-                    const int qt = (grp * 2 + (lq - 2)) * 32 + lane;
-                    const int i = qt >> 1, kh = qt & 1;
-                    const float egi = sc[SC_EG * 64 + i];
-                    const uint8_t* src = sm + L::Q0 + qs * 16384 + kh * 8192;
+                    // ---- output rows first (chunk n-1's S12 is still reading the sigma Qd
+                    //      buffer), then sigma Qd = sigma 2^G_i q_i as tf32 K-major: row i,
+                    //      feature half kh
+                    epilogue();
+                    if (warp_wait(bar0 + B_WFREE, (n - 1) & 1, abort_flag, limit, c.err, TAG_WFREE,
+                                  lane, n >= 1)) {
+                        const int qt = (grp * 2 + (lq - 2)) * 32 + lane;
+                        const int i = qt >> 1, kh = qt & 1;
+                        const float egi = sc[SC_EG * 64 + i];
+                        const uint8_t* src = sm + L::Q0 + qs * 16384 + kh * 8192;
 #pragma unroll 2
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
-                        const uint4 lo4 = make_uint4(
-                            tf32_bits(__uint_as_float(u.x << 16) * egi),
-                            tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
-                            tf32_bits(__uint_as_float(u.y << 16) * egi),
-                            tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
-                        const uint4 hi4 = make_uint4(
-                            tf32_bits(__uint_as_float(u.z << 16) * egi),
-                            tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
-                            tf32_bits(__uint_as_float(u.w << 16) * egi),
-                            tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
-                        // features 64 kh + 8 cc .. +7: kblock 2 kh + cc / 4 (rows 64.. of the
-                        // S12 operand), chunks 2 (cc % 4) + {0, 1}
-                        uint8_t* dst = sm + L::W + (kh * 2 + (cc >> 2)) * L::WQ_KB + 8192;
-                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc) & 7)) = lo4;
-                        *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc + 1) & 7)) = hi4;
+                        for (int cc = 0; cc < 8; ++cc) {
+                            const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
+                            const uint4 lo4 = make_uint4(
+                                tf32_bits(__uint_as_float(u.x << 16) * egi),
+                                tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
+                                tf32_bits(__uint_as_float(u.y << 16) * egi),
+                                tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
+                            const uint4 hi4 = make_uint4(
+                                tf32_bits(__uint_as_float(u.z << 16) * egi),
+                                tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
+                                tf32_bits(__uint_as_float(u.w << 16) * egi),
+                                tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
+                            // features 64 kh + 8 cc .. +7: kblock 2 kh + cc / 4 (rows 64.. of the
+                            // S12 operand), chunks 2 (cc % 4) + {0, 1}
+                            uint8_t* dst = sm + L::W + (kh * 2 + (cc >> 2)) * L::WQ_KB + 8192;
+                            *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc) & 7)) = lo4;
+                            *reinterpret_cast<uint4*>(dst + sw128(i, (2 * cc + 1) & 7)) = hi4;
+                        }
                     }
                 }
-                fence_proxy_async();
-                tc_fence_before();
-                named_bar<2, kPrepThreads>();   // TM_S has been read; the q tile is consumed
-                if (pt == 0) mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
-            }
-            // ---- P2 (U^T into the parity's U buffer) and P3 (W^T into TM_S)
-            if (!pwait(bar0 + B_AFULL + 8 * as, (n / AST) & 1, TAG_AFULL, true)) break;
-            if (!pwait(bar0 + B_VFULL, n & 1, TAG_VFULL, need_v)) break;
-            if (pt == 0) {
-                tc_fence_after();
-                if (need_v) {
+                barp_phase ^= 1u;   // P1's phase, consumed by the C warps
+                fence_proxy_async();   // sigma Qd and C are read by the state group's MMAs
+                barp_pending = true;
+            } else {
+                // ---- summary: P2 (U^T, S part only) and P3 (W^T into TM_S); only the issuing
+                //      thread waits for the k, WY and v tiles
+                if (pt == 0 &&
+                    mbar_wait(bar0 + B_KFULL + 8 * ks, (n / KST) & 1, abort_flag, limit, c.err, TAG_KFULL) &&
+                    mbar_wait(bar0 + B_AFULL + 8 * as, (n / AST) & 1, abort_flag, limit, c.err, TAG_AFULL) &&
+                    (!need_v || mbar_wait(bar0 + B_VFULL, n & 1, abort_flag, limit, c.err, TAG_VFULL))) {
+                    tc_fence_after();
+                    if (need_v) {
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
+                                           desc_k(ast + k16 * 32), k16 > 0);
+                    }
 #pragma unroll
                     for (int k16 = 0; k16 < 4; ++k16)
-                        mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                       desc_k(ast + k16 * 32), k16 > 0);
+                        mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
+                                       desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                    if (need_v) mma_commit(bar0 + B_VEMPTY);
+                    mma_commit(bar0 + B_AEMPTY + 8 * as);
+                    mma_commit(bar0 + B_BARP);
                 }
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
-                                   desc_k(ast + 8192 + k16 * 32), k16 > 0);
-                if (need_v) mma_commit(bar0 + B_VEMPTY);
-                mma_commit(bar0 + B_AEMPTY + 8 * as);
-                mma_commit(bar0 + B_BARP);
+                __syncwarp();
+                barp_pending = true;
             }
-            __syncwarp();
-            barp_pending = true;
-            if (!SUMMARY) {
-                // ---- while P2/P3 run: output rows of chunk n-2 (retired above), then zero its
-                //      O^T buffer, which S12 of this chunk accumulates into
-                tc_fence_after();
-                if (n >= 2) store_output(n - 2);
-                const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
-                                           0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp, zero);
-                tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp + 16, zero);
-                tmem_wait_st();
-            }
-            if (!pmma_wait()) break;
+            if (!pmma_wait()) break;   // P3 (and P2) done; for the forward also every C and Qd
             tc_fence_after();
             // ---- -sigma W as rows 0..63 of the S12 B operand, once chunk n-1's S12 retired
+            //      (the forward's Qd warps waited for that before the barrier above)
             {
                 if (SUMMARY && !pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
                 const float nsig = -sc[SC_MISC * 64 + 2];
@@ -501,28 +584,34 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 uint8_t* col = sm + L::W + lq * L::WQ_KB + (k & 3) * 4;
                 const int qk = (k & 31) >> 2;
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float w[16];
-                    tmem_ld16(t_row + TM_S + 32 * grp + 16 * hh, w);
+                for (int hb = 0; hb < ECOLS; hb += 32) {
+                    float w2[2][16];
+                    tmem_ld16(t_row + TM_S + ECOLS * grp + hb, w2[0]);
+                    tmem_ld16(t_row + TM_S + ECOLS * grp + hb + 16, w2[1]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii)
-                        *reinterpret_cast<uint32_t*>(col + sw128(32 * grp + 16 * hh + ii, qk)) =
-                            tf32_bits(nsig * w[ii]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float* w = w2[hh];
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii)
+                            *reinterpret_cast<uint32_t*>(
+                                col + sw128(ECOLS * grp + hb + 16 * hh + ii, qk)) =
+                                tf32_bits(nsig * w[ii]);
+                    }
                 }
             }
             fence_proxy_async();
             tc_fence_before();
             named_bar<2, kPrepThreads>();
-            // ---- TM_S is free again: P1 of the next chunk goes to the tensor pipe now
-            if (!SUMMARY && n + 1 < nchunks) {
-                const int n1 = n + 1;
-                if (!pwait(bar0 + B_KFULL + 8 * (n1 % KST), (n1 / KST) & 1, TAG_KFULL, true)) break;
-                if (!pwait(bar0 + B_QFULL + 8 * (n1 & 1), (n1 >> 1) & 1, TAG_QFULL, true)) break;
-                issue_p1(n1);
+            // ---- the q tile is consumed (P1 and sigma Qd); TM_S is free again: P1 of the next
+            //      chunk goes to the tensor pipe now
+            if (!SUMMARY) {
+                if (pt == 0) mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
+                if (n + 1 < nchunks) issue_p1(n + 1);
             }
             if (pt == 0) mbar_arrive(bar0 + B_PREPDONE);
         }
+#undef epilogue
 #undef issue_p1
         if (*go == 0) {
             if (barp_pending && pt == 0) mbar_drain(bar0 + B_BARP, barp_phase, limit);
@@ -536,23 +625,37 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
         }
 #undef store_output
+#undef warp_wait
 #undef pmma_wait
 #undef pwait
     } else {
         // ================================== state =================================
-        const int st = tid;
-        const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-        volatile int* go = reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S);
+        // state group sg: the forward's only group, or the summary's M part (0) / S part (1)
+        const int sg = SUMMARY ? (warp >> 2) : 0;
+        const int st = tid & 127;                      // = column of H this thread owns
+        const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t tm_h = F::tm_h(sg);
+        const uint32_t bar_s = bar0 + (sg == 0 ? B_BARS : B_BARS1);
+        volatile int* go = reinterpret_cast<volatile int*>(sm + L::BAR + (sg == 0 ? B_GO_S : B_GO_S1));
+        const bool m_part = SUMMARY && sg == 0;       // starts from I, no values
         uint32_t bars_phase = 0;
         bool bars_pending = false;
         const long long bhoff = (long long)bh * kD * kD;
         float sig_next = 1.f;   // sigma after the last completed chunk
 
-#define swait(bar, parity, tag)                                                              \
-    group_wait<1, 128>(warp == 0, lane == 0, (bar), (parity), true, go, abort_flag, limit, \
-                       c.err, (tag))
+// each state group synchronises on its own named barrier (1 or 4)
+#define sbar()                                   \
+    do {                                         \
+        if (sg == 0) named_bar<1, 128>();        \
+        else named_bar<4, 128>();                \
+    } while (0)
+#define swait(bar, parity, tag)                                                                  \
+    (sg == 0 ? group_wait<1, 128>(warp == 0, lane == 0, (bar), (parity), true, go, abort_flag,   \
+                                  limit, c.err, (tag))                                           \
+             : group_wait<4, 128>(warp == 4, lane == 0, (bar), (parity), true, go, abort_flag,   \
+                                  limit, c.err, (tag)))
 #define smma_wait() \
-    (swait(bar0 + B_BARS, bars_phase, TAG_BARS) ? (bars_phase ^= 1u, bars_pending = false, true) : false)
+    (swait(bar_s, bars_phase, TAG_BARS) ? (bars_phase ^= 1u, bars_pending = false, true) : false)
 
         // ---- initial state: row `st` of H^T (= column st of H), sigma = 1
 #pragma unroll 1
@@ -563,45 +666,47 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 const int k = 16 * g + j;
                 float v0 = 0.f;
                 if (SUMMARY)
-                    v0 = (blk == 0 && k == st) ? 1.f : 0.f;
+                    v0 = (m_part && k == st) ? 1.f : 0.f;
                 else if (c.h_start)
                     v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + st];
                 x[j] = __float_as_uint(v0);
             }
-            tmem_st16(t_row + TM_H + 16 * g, x);
+            tmem_st16(t_row + tm_h + 16 * g, x);
         }
         tmem_wait_st();
         tc_fence_before();
-        named_bar<1, 128>();
+        sbar();
 
         int done = 0;   // chunks completed
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
             const int ks = n % KST;
             const uint32_t kst = base + L::K0 + ks * 16384;
-            const uint32_t t_u = tmem + TM_U + (n & 1) * L::TU_STRIDE;
+            // R^T buffer: the summary's M part has its own; otherwise the parity's U buffer
+            const uint32_t tu_col = m_part ? F::TM_RM : TM_U + (n % NUB) * F::TU_STRIDE;
+            const uint32_t t_u = tmem + tu_col;
             const uint32_t t_o = t_u + 64;   // forward only
             const float* sc = scal + (n & 1) * (SC_N * 64);
             if (!swait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE)) break;
             // ---- S12: [R^T | O^T] = [U^T | 0] + H_s^T [-sigma W ; sigma Qd]^T (forward);
-            //      the summary forms only R^T = U^T + H_s^T (-sigma W)^T
+            //      the summary forms only R^T = U^T + H_s^T (-sigma W)^T (no U in the M part)
             if (st == 0) {
                 tc_fence_after();
                 if (!SUMMARY) {
 #pragma unroll
                     for (int k8 = 0; k8 < 16; ++k8)
-                        mma_ts_tf32<ID_TF128>(t_u, tmem + TM_H + k8 * 8,
+                        mma_ts_tf32<ID_TF128>(t_u, tmem + tm_h + k8 * 8,
                                               desc_k(base + L::W + (k8 >> 2) * L::WQ_KB + (k8 & 3) * 32),
                                               1u);
                 } else {
 #pragma unroll
                     for (int k8 = 0; k8 < 16; ++k8)
-                        mma_ts_tf32<ID_TF>(t_u, tmem + TM_H + k8 * 8,
+                        mma_ts_tf32<ID_TF>(t_u, tmem + tm_h + k8 * 8,
                                            desc_k(base + L::W + (k8 >> 2) * L::WQ_KB + (k8 & 3) * 32),
-                                           (need_v || k8 > 0) ? 1u : 0u);
+                                           (!m_part || k8 > 0) ? 1u : 0u);
                 }
                 mma_commit(bar0 + B_WFREE);
-                mma_commit(bar0 + B_BARS);
+                mma_commit(bar_s);
             }
             __syncwarp();
             bars_pending = true;
@@ -609,15 +714,31 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             sig_next = sc[SC_MISC * 64 + 1];
             if (!smma_wait()) break;
             tc_fence_after();
+            // ---- forward: S3 O^T += R^T C^T (A = R^T in TMEM) goes to the tensor pipe now and
+            //      runs during the packing below (both only read R^T)
+            if (!SUMMARY && st == 0) {
+                const uint32_t cb = base + L::C0 + (n & 1) * 16384;
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8)
+                    mma_ts_tf32<ID_TF>(t_o, t_u + k8 * 8,
+                                       desc_k(cb + (k8 >> 2) * 8192 + (k8 & 3) * 32), 1u);
+            }
+            __syncwarp();
             // ---- scaled R^T -> packed bf16 hi/lo in TMEM (and, rarely, fold sigma into H_s)
+            const uint32_t rd_col = SUMMARY ? tu_col : TM_RD;
             {
                 const float* dd = sc + SC_DD * 64;
-                const uint32_t t_ur = t_row + TM_U + (n & 1) * L::TU_STRIDE;
+                const uint32_t t_ur = t_row + tu_col;
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    float r[16];
-                    tmem_ld16(t_ur + 16 * g, r);
-                    tmem_wait_ld();
+                for (int g2 = 0; g2 < 4; g2 += 2) {
+                  float r2[2][16];
+                  tmem_ld16(t_ur + 16 * g2, r2[0]);
+                  tmem_ld16(t_ur + 16 * g2 + 16, r2[1]);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int gg = 0; gg < 2; ++gg) {
+                    const int g = g2 + gg;
+                    const float* r = r2[gg];
                     // packed column q holds the pair (2q, 2q+1) of the 64 tokens j
                     uint32_t hi[8], lo[8];
 #pragma unroll
@@ -629,44 +750,39 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                         hi[j] = pack_bf16(h0, h1);
                         lo[j] = pack_bf16(x0 - h0, x1 - h1);
                     }
-                    tmem_st8(t_row + TM_RD + 8 * g, hi);
-                    tmem_st8(t_row + TM_RD + 32 + 8 * g, lo);
+                    // (in the summary this overwrites the 16 columns just read)
+                    tmem_st8(t_row + rd_col + 16 * g, hi);
+                    tmem_st8(t_row + rd_col + 16 * g + 8, lo);
+                  }
                 }
                 if (fold != 1.f) {
 #pragma unroll 1
                     for (int g = 0; g < 8; ++g) {
                         float x[16];
                         uint32_t y[16];
-                        tmem_ld16(t_row + TM_H + 16 * g, x);
+                        tmem_ld16(t_row + tm_h + 16 * g, x);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) y[j] = __float_as_uint(x[j] * fold);
-                        tmem_st16(t_row + TM_H + 16 * g, y);
+                        tmem_st16(t_row + tm_h + 16 * g, y);
                     }
                 }
                 tmem_wait_st();
             }
             tc_fence_before();
-            named_bar<1, 128>();
-            // ---- S3: O^T += R^T C^T (A = R^T in TMEM) ; S4: H_s^T += (R^T D) K (A = hi, lo)
+            sbar();
+            // ---- S4: H_s^T += (R^T D) K (A = hi, lo in TMEM); its commits also cover S3
             if (st == 0) {
                 tc_fence_after();
-                if (!SUMMARY) {
-                    const uint32_t cb = base + L::C0 + (n & 1) * 16384;
-#pragma unroll
-                    for (int k8 = 0; k8 < 8; ++k8)
-                        mma_ts_tf32<ID_TF>(t_o, t_u + k8 * 8,
-                                           desc_k(cb + (k8 >> 2) * 8192 + (k8 & 3) * 32), 1u);
-                }
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int k16 = 0; k16 < 4; ++k16)
-                        mma_ts_bf16<ID_S4>(tmem + TM_H, tmem + TM_RD + part * 32 + k16 * 8,
+                        mma_ts_bf16<ID_S4>(tmem + tm_h, tmem + rd_col + 16 * k16 + 8 * part,
                                            desc_mn(kst + k16 * 2048, 8192), 1u);
                 mma_commit(bar0 + B_KEMPTY + 8 * ks);
-                mma_commit(bar0 + B_UFREE + 8 * (n & 1));
-                mma_commit(bar0 + B_BARS);
+                mma_commit(bar0 + B_UFREE + 8 * (n % NUB));
+                mma_commit(bar_s);
             }
             __syncwarp();
             bars_pending = true;
@@ -677,28 +793,29 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 
         if (*go == 0) {
             if (bars_pending && st == 0)   // let an issued MMA group retire before TMEM is freed
-                mbar_drain(bar0 + B_BARS, bars_phase, limit);
+                mbar_drain(bar_s, bars_phase, limit);
         } else {
             // ---- the chain's final state H = sigma H_s: thread v writes column v of H
             float* dst = nullptr;
             if (SUMMARY) {
                 const long long sb = ((long long)seg * c.B * c.H + bh) * kD * kD;
-                dst = (blk == 0 ? c.M : c.S) + sb;
+                dst = (m_part ? c.M : c.S) + sb;
             } else if (c.h_final && seg == c.nseg_total - 1) {
                 dst = c.h_final + bhoff;
             }
             if (dst) {
-                const float sg = done > 0 ? sig_next : 1.f;
+                const float sgm = done > 0 ? sig_next : 1.f;
 #pragma unroll 1
                 for (int g = 0; g < 8; ++g) {
                     float x[16];
-                    tmem_ld16(t_row + TM_H + 16 * g, x);
+                    tmem_ld16(t_row + tm_h + 16 * g, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(long long)(16 * g + j) * kD + st] = sg * x[j];
+                    for (int j = 0; j < 16; ++j) dst[(long long)(16 * g + j) * kD + st] = sgm * x[j];
                 }
             }
         }
+#undef sbar
 #undef smma_wait
 #undef swait
     }
@@ -708,7 +825,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     tc_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols)
+                     "r"(F::TMEM_COLS)
                      : "memory");
 }
 
@@ -730,8 +847,8 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
     if (e != cudaSuccess) return e;
-    const long long chains = (long long)c.B * c.H * c.nseg_run * (SUMMARY ? 2 : 1);
-    kern<<<(unsigned)chains, kThreads, bytes, s>>>(tp);
+    const long long chains = (long long)c.B * c.H * c.nseg_run;
+    kern<<<(unsigned)chains, Cfg<SUMMARY>::THREADS, bytes, s>>>(tp);
     return cudaGetLastError();
 }
 

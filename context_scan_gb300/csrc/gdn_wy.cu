@@ -12,11 +12,13 @@
 // a chunk's pair with one bulk copy instead of inverting on its critical path, and the
 // inverse is computed once per chunk rather than once per chain that walks the chunk.
 //
-// One CTA of four warps per chunk: K K^T on mma.sync (bf16, fp32 accumulate), L in
-// registers, 16 x 16 diagonal blocks of the inverse by forward substitution (rows in
-// registers, shuffles), three rounds of block forward substitution on mma.sync (tf32), then
-// the scaled bf16 tiles leave through one bulk store. Several CTAs share an SM, so the
-// latency of each step is hidden by the other chunks in flight; the kernel has no waits.
+// One CTA of four warps per chunk: K K^T on mma.sync (bf16, fp32 accumulate), L from the
+// accumulators, the four 16 x 16 diagonal blocks of the inverse by forward substitution
+// (one block per warp; rows in registers, shuffles), three rounds of block forward
+// substitution on mma.sync (tf32), then the scaled bf16 tiles leave through one bulk store.
+// The k tile, L and the output tiles share one 16 KB buffer (each is dead before the next
+// is written), so six CTAs fit on an SM and hide each other's latencies; the kernel has no
+// waits.
 #include "gdn_tc_common.cuh"
 
 namespace gdn {
@@ -28,12 +30,12 @@ constexpr float kWyLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t WY_K = 0;        // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle;
-                                    // reused for the two output tiles once K K^T is done
-constexpr uint32_t WY_L = 16384;    // L fp32 64 x 64 (sw64)
-constexpr uint32_t WY_A = 32768;    // A fp32 64 x 64 (sw64)
-constexpr uint32_t WY_Y = 49152;    // per-warp 16 x 8 fp32 scratch of the block rounds
-constexpr uint32_t WY_SC = 51200;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
-constexpr uint32_t WY_END = 52224;
+constexpr uint32_t WY_L = 0;        // then L fp32 64 x 64 (sw64) once K K^T is in registers;
+constexpr uint32_t WY_OUT = 0;      // then the two bf16 output tiles once the rounds are done
+constexpr uint32_t WY_A = 16384;    // A fp32 64 x 64 (sw64)
+constexpr uint32_t WY_Y = 32768;    // per-warp 16 x 8 fp32 scratch of the block rounds
+constexpr uint32_t WY_SC = 34816;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
+constexpr uint32_t WY_END = 35840;
 constexpr uint32_t kWySmem = WY_END + 1024;
 
 struct WyParams {
@@ -59,7 +61,7 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float* d, const uint32_t* a, c
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__global__ void __launch_bounds__(kWyThreads, 4) wy_kernel(const WyParams p) {
+__global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -139,6 +141,7 @@ __global__ void __launch_bounds__(kWyThreads, 4) wy_kernel(const WyParams p) {
                 mma_m16n8k16_bf16(d[2 * np + 1], a, bb + 2);
             }
         }
+        __syncthreads();   // every warp's reads of the k tile are done: L goes over it
         const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -152,33 +155,27 @@ __global__ void __launch_bounds__(kWyThreads, 4) wy_kernel(const WyParams p) {
     }
     __syncthreads();
 
-    // ---- diagonal 16 x 16 blocks of (I + L)^-1: lane r of a 16-lane group owns row r,
-    //      X[r] = e_r - sum_{m<r} L[r][m] X[m], row m broadcast by shuffles once final
-    if (tid < 64) {
-        const int bs = (tid >> 4) * 16, r = tid & 15, src0 = lane & 16;
-        float x[16];
+    // ---- diagonal 16 x 16 blocks of (I + L)^-1, block w by warp w: lane (r, half) owns
+    //      columns 8 half .. 8 half + 7 of row r, X[r] = e_r - sum_{m<r} L[r][m] X[m], with
+    //      row m broadcast by shuffles once it is final. Rows are zero beyond their diagonal,
+    //      so the updates run over all columns with constant bounds. The blocks above the
+    //      diagonal are never written: the rounds never read them and the packing masks them.
+    {
+        const int bs = 16 * warp, r = lane & 15, half = lane >> 4, src0 = lane & 16;
+        float x[8];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) x[m] = (m == r) ? 1.f : 0.f;
+        for (int cc = 0; cc < 8; ++cc) x[cc] = (8 * half + cc == r) ? 1.f : 0.f;
 #pragma unroll 1
         for (int m = 0; m < 15; ++m) {
             const float f = (r > m) ? Lm[sw64(bs + r, bs + m)] : 0.f;
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) {
+            for (int cc = 0; cc < 8; ++cc) {
                 const float xm = __shfl_sync(0xffffffffu, x[cc], src0 + m);
                 x[cc] = fmaf(-f, xm, x[cc]);
             }
         }
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) Am[sw64(bs + r, bs + cc)] = x[cc];
-    } else {
-        // the blocks above the diagonal are zero
-#pragma unroll 1
-        for (int e = tid - 64; e < 6 * 256; e += 64) {
-            const int blkid = e >> 8, w = e & 255;
-            const int I = (blkid < 3) ? 0 : (blkid < 5 ? 1 : 2);
-            const int J = (blkid < 3) ? blkid + 1 : (blkid < 5 ? blkid - 1 : 3);
-            Am[sw64(16 * I + (w >> 4), 16 * J + (w & 15))] = 0.f;
-        }
+        for (int cc = 0; cc < 8; ++cc) Am[sw64(bs + r, bs + 8 * half + cc)] = x[cc];
     }
     __syncthreads();
 
@@ -224,16 +221,19 @@ __global__ void __launch_bounds__(kWyThreads, 4) wy_kernel(const WyParams p) {
     }
 
     // ---- A diag(beta) (threads 0..63) and A diag(beta 2^Gx) (64..127) as bf16 K-major rows,
-    //      over the K tile's space, then one bulk store of both tiles
+    //      over L's space (the last round's barrier retired every read of L), zero above the
+    //      row's diagonal block, then one bulk store of both tiles
     {
         const int i = tid & 63;
+        const int jend = (i & ~15) + 16;   // columns of the blocks up to the diagonal one
         const float* scale = (tid < 64) ? bet : bekr;
-        uint8_t* tile = sm + WY_K + ((tid < 64) ? 0 : 8192);
+        uint8_t* tile = sm + WY_OUT + ((tid < 64) ? 0 : 8192);
 #pragma unroll 1
         for (int cq = 0; cq < 8; ++cq) {
             float a[8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) a[jj] = Am[sw64(i, 8 * cq + jj)] * scale[8 * cq + jj];
+            for (int jj = 0; jj < 8; ++jj)
+                a[jj] = (8 * cq + jj < jend) ? Am[sw64(i, 8 * cq + jj)] * scale[8 * cq + jj] : 0.f;
             *reinterpret_cast<uint4*>(tile + sw128(i, cq)) =
                 make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
                            pack_bf16(a[6], a[7]));
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kWyThreads, 4) wy_kernel(const WyParams p) {
     if (tid == 0) {
         uint8_t* dst = p.wy + ch * 16384;
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                     "r"(base + WY_K), "r"(16384u)
+                     "r"(base + WY_OUT), "r"(16384u)
                      : "memory");
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         // the shared source must stay valid until the copy has read it
