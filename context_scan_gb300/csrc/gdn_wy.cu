@@ -12,13 +12,17 @@
 // a chunk's pair with one bulk copy instead of inverting on its critical path, and the
 // inverse is computed once per chunk rather than once per chain that walks the chunk.
 //
-// One CTA of four warps per chunk: K K^T on mma.sync (bf16, fp32 accumulate), L from the
-// accumulators, the four 16 x 16 diagonal blocks of the inverse by forward substitution
-// (one block per warp; rows in registers, shuffles), three rounds of block forward
-// substitution on mma.sync (tf32), then the scaled bf16 tiles leave through one bulk store.
-// The k tile, L and the output tiles share one 16 KB buffer (each is dead before the next
-// is written), so six CTAs fit on an SM and hide each other's latencies; the kernel has no
-// waits.
+// One CTA of four warps per chunk: K K^T on mma.sync (bf16, fp32 accumulate; the ten lower
+// 16 x 16 blocks dealt round-robin to the warps), L from the accumulators, the four 16 x 16
+// diagonal blocks of the inverse by forward substitution (one block per warp; rows in
+// registers, shuffles), then block forward substitution on mma.sync (tf32), one column of
+// blocks per warp with no barrier between the block rows. The blocks of L that feed the
+// tensor cores and the inverse itself are kept as tf32 bit patterns in row-padded layouts
+// (68 and 72 words per row), so a fragment is two or four shared loads at constant offsets
+// without bank conflicts; the diagonal blocks of L stay fp32 for the substitution. Each
+// block of the inverse is scaled and written to global memory as bf16 as soon as it is
+// final (blocks above the diagonal as zeros). Five CTAs share an SM and hide each other's
+// latencies; the kernel has no waits.
 #include "gdn_tc_common.cuh"
 
 namespace gdn {
@@ -28,15 +32,20 @@ constexpr int kWyThreads = 128;
 constexpr int kWyD = 128;          // K
 constexpr float kWyLog2e = 1.4426950408889634f;
 
-// shared-memory map (bytes from a 1024-aligned base)
+constexpr int LS = 68;   // row pitch (words) of the tf32 off-diagonal blocks of L
+constexpr int XS = 72;   // row pitch (words) of the tf32 inverse X
+constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
+
+// shared-memory map (bytes from a 128-aligned base)
 constexpr uint32_t WY_K = 0;        // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle;
-constexpr uint32_t WY_L = 0;        // then L fp32 64 x 64 (sw64) once K K^T is in registers;
-constexpr uint32_t WY_OUT = 0;      // then the two bf16 output tiles once the rounds are done
-constexpr uint32_t WY_A = 16384;    // A fp32 64 x 64 (sw64)
-constexpr uint32_t WY_Y = 32768;    // per-warp 16 x 8 fp32 scratch of the block rounds
-constexpr uint32_t WY_SC = 34816;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
-constexpr uint32_t WY_END = 35840;
-constexpr uint32_t kWySmem = WY_END + 1024;
+constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS) once K K^T is in registers
+constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
+constexpr uint32_t WY_LD = WY_X;    // diagonal blocks of L (fp32, 4 x 16 x DS), dead before X
+constexpr uint32_t WY_Y = 35840;    // per-warp 16 x 8 fp32 scratch of the block rounds
+constexpr uint32_t WY_SC = 37888;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
+constexpr uint32_t WY_END = 38912;
+constexpr uint32_t kWySmem = WY_END + 128;
+static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_Y - WY_X, "layout");
 
 struct WyParams {
     const void* k;
@@ -61,13 +70,19 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float* d, const uint32_t* a, c
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
+// 16-byte output chunk `c` (8 bf16 columns) of row `row` of one 64 x 64 output tile
+__device__ __forceinline__ uint4* out_chunk(uint8_t* tile, int row, int c) {
+    return reinterpret_cast<uint4*>(tile + sw128(row, c));
+}
+
+__global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const WyParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t base = (raw + 127u) & ~127u;
     uint8_t* sm = smem_raw + (base - raw);
-    float* Lm = reinterpret_cast<float*>(sm + WY_L);
-    float* Am = reinterpret_cast<float*>(sm + WY_A);
+    uint32_t* Lt = reinterpret_cast<uint32_t*>(sm + WY_LT);
+    uint32_t* X = reinterpret_cast<uint32_t*>(sm + WY_X);
+    float* Ld = reinterpret_cast<float*>(sm + WY_LD);
     float* sc = reinterpret_cast<float*>(sm + WY_SC);
     const float* Gx = sc;
     const float* G = sc + 64;
@@ -81,6 +96,8 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
     const long long bh = ch / nchunks;
     const int b = (int)(bh / p.H), h = (int)(bh % p.H);
     const long long row0 = (long long)b * p.T + (long long)n * 64;   // flattened (b, t)
+    uint8_t* out_b = p.wy + ch * 16384;   // A diag(beta)
+    uint8_t* out_g = out_b + 8192;        // A diag(beta 2^Gx)
 
     // ---- K tile: 64 rows of 256 bytes, half a row per 16 lanes (coalesced), stored in two
     //      64-feature halves with the 128-byte swizzle
@@ -116,41 +133,58 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
     }
     __syncthreads();
 
-    // ---- K K^T for rows 16w..16w+15 (warp w), column tiles of 8 up to the diagonal block,
-    //      then L = diag(beta) (2^(Gx_i - G_j) k_i.k_j) below the diagonal, straight from the
-    //      accumulators
+    // ---- K K^T on the ten 16 x 16 blocks (I, J), J <= I, dealt round-robin to the warps
+    //      (3, 3, 2, 2 blocks), then L = diag(beta) (2^(Gx_i - G_j) k_i.k_j) below the
+    //      diagonal straight from the accumulators: fp32 for the diagonal blocks, tf32 for
+    //      the rest
     {
-        float d[8][4];
+        float d[3][2][4];
+        int bI[3], bJ[3];
+        const int nb = warp < 2 ? 3 : 2;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+        for (int q = 0; q < 3; ++q) {
+            // block index warp + 4 q in the order (0,0) (1,0) (1,1) (2,0) (2,1) (2,2) (3,0) ...
+            const int idx = warp + 4 * q;
+            const int I = idx < 1 ? 0 : idx < 3 ? 1 : idx < 6 ? 2 : 3;
+            bI[q] = I;
+            bJ[q] = idx - I * (I + 1) / 2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) d[q][h][0] = d[q][h][1] = d[q][h][2] = d[q][h][3] = 0.f;
+        }
         const int lrow = lane & 7, lsel = lane >> 3;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t kt = base + WY_K + (ks >> 2) * 8192;
             const int c0 = (ks & 3) * 2;
-            uint32_t a[4];
-            // matrices: rows 0-7 / 8-15 of the block at k 0-7, then the same rows at k 8-15
-            ldsm_x4(kt + sw128(16 * warp + lrow + 8 * (lsel & 1), c0 + (lsel >> 1)), a);
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                if (np > warp) continue;   // both column tiles lie above the diagonal block
-                uint32_t bb[4];
-                // column tile 2np: key rows 16np..+7 at k 0-7 and 8-15; tile 2np+1: rows +8
-                ldsm_x4(kt + sw128(16 * np + lrow + 8 * (lsel >> 1), c0 + (lsel & 1)), bb);
-                mma_m16n8k16_bf16(d[2 * np], a, bb);
-                mma_m16n8k16_bf16(d[2 * np + 1], a, bb + 2);
+            for (int q = 0; q < 3; ++q) {
+                if (q >= nb) break;
+                uint32_t a[4], bb[4];
+                // A: rows 16I + 0-7 / 8-15 at k 0-7, then the same rows at k 8-15
+                ldsm_x4(kt + sw128(16 * bI[q] + lrow + 8 * (lsel & 1), c0 + (lsel >> 1)), a);
+                // B: key rows 16J..+7 at k 0-7 and 8-15 (column tile 0), rows +8 (tile 1)
+                ldsm_x4(kt + sw128(16 * bJ[q] + lrow + 8 * (lsel >> 1), c0 + (lsel & 1)), bb);
+                mma_m16n8k16_bf16(d[q][0], a, bb);
+                mma_m16n8k16_bf16(d[q][1], a, bb + 2);
             }
         }
         __syncthreads();   // every warp's reads of the k tile are done: L goes over it
         const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            if ((nt >> 1) > warp) continue;
+        for (int q = 0; q < 3; ++q) {
+            if (q >= nb) break;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = 16 * warp + gq + 8 * (e >> 1), j = 8 * nt + 2 * tq + (e & 1);
-                Lm[sw64(i, j)] = (j < i) ? bet[i] * ex2(Gx[i] - G[j]) * d[nt][e] : 0.f;
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 16 * bI[q] + gq + 8 * (e >> 1);
+                    const int j = 16 * bJ[q] + 8 * h + 2 * tq + (e & 1);
+                    const float v = (j < i) ? bet[i] * ex2(Gx[i] - G[j]) * d[q][h][e] : 0.f;
+                    if (bI[q] == bJ[q])
+                        Ld[bI[q] * 16 * DS + (i & 15) * DS + (j & 15)] = v;   // fp32
+                    else
+                        Lt[i * LS + j] = tf32_bits(v);                        // tensor cores
+                }
         }
     }
     __syncthreads();
@@ -158,45 +192,73 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
     // ---- diagonal 16 x 16 blocks of (I + L)^-1, block w by warp w: lane (r, half) owns
     //      columns 8 half .. 8 half + 7 of row r, X[r] = e_r - sum_{m<r} L[r][m] X[m], with
     //      row m broadcast by shuffles once it is final. Rows are zero beyond their diagonal,
-    //      so the updates run over all columns with constant bounds. The blocks above the
-    //      diagonal are never written: the rounds never read them and the packing masks them.
+    //      so the updates run over all columns with constant bounds.
     {
         const int bs = 16 * warp, r = lane & 15, half = lane >> 4, src0 = lane & 16;
+        const float* ld = Ld + warp * 16 * DS + r * DS;
         float x[8];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) x[cc] = (8 * half + cc == r) ? 1.f : 0.f;
 #pragma unroll 1
         for (int m = 0; m < 15; ++m) {
-            const float f = (r > m) ? Lm[sw64(bs + r, bs + m)] : 0.f;
+            const float f = (r > m) ? ld[m] : 0.f;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 const float xm = __shfl_sync(0xffffffffu, x[cc], src0 + m);
                 x[cc] = fmaf(-f, xm, x[cc]);
             }
         }
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) Am[sw64(bs + r, bs + 8 * half + cc)] = x[cc];
+        __syncthreads();   // every warp is done with Ld, which X overwrites
+        const int row = bs + r, c0 = bs + 8 * half;
+        uint4* xs = reinterpret_cast<uint4*>(X + row * XS + c0);
+        xs[0] = make_uint4(tf32_bits(x[0]), tf32_bits(x[1]), tf32_bits(x[2]), tf32_bits(x[3]));
+        xs[1] = make_uint4(tf32_bits(x[4]), tf32_bits(x[5]), tf32_bits(x[6]), tf32_bits(x[7]));
+        // output: this row's 8 columns of the diagonal block, scaled, as one 16-byte chunk per
+        // tile; and the row's chunks above the diagonal block as zeros (split between halves)
+        *out_chunk(out_b, row, c0 >> 3) =
+            make_uint4(pack_bf16(x[0] * bet[c0], x[1] * bet[c0 + 1]),
+                       pack_bf16(x[2] * bet[c0 + 2], x[3] * bet[c0 + 3]),
+                       pack_bf16(x[4] * bet[c0 + 4], x[5] * bet[c0 + 5]),
+                       pack_bf16(x[6] * bet[c0 + 6], x[7] * bet[c0 + 7]));
+        *out_chunk(out_g, row, c0 >> 3) =
+            make_uint4(pack_bf16(x[0] * bekr[c0], x[1] * bekr[c0 + 1]),
+                       pack_bf16(x[2] * bekr[c0 + 2], x[3] * bekr[c0 + 3]),
+                       pack_bf16(x[4] * bekr[c0 + 4], x[5] * bekr[c0 + 5]),
+                       pack_bf16(x[6] * bekr[c0 + 6], x[7] * bekr[c0 + 7]));
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+        for (int cz = 2 * warp + 2 + half; cz < 8; cz += 2) {
+            *out_chunk(out_b, row, cz) = z;
+            *out_chunk(out_g, row, cz) = z;
+        }
     }
     __syncthreads();
 
-    // ---- block forward substitution: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ
+    // ---- block forward substitution: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ. A column of
+    //      blocks depends only on itself above, the diagonal inverses and L, so each warp
+    //      walks one 8-wide half of block columns down on its own: warps 0, 1 column 0;
+    //      warps 2, 3 columns 1 and then 2. Each 16 x 8 tile goes back to X (tf32) and,
+    //      scaled, to the outputs (bf16 pairs).
     float* Ys = reinterpret_cast<float*>(sm + WY_Y) + warp * 128;
+    const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll 1
-    for (int I = 1; I < 4; ++I) {
+    for (int J = (warp < 2 ? 0 : 1); J < (warp < 2 ? 1 : 3); ++J) {
+        const int n0 = 16 * J + 8 * (warp & 1);
 #pragma unroll 1
-        for (int tile = warp; tile < 2 * I; tile += 4) {
-            const int J = tile >> 1, n0 = 16 * J + 8 * (tile & 1);
+        for (int I = J + 1; I < 4; ++I) {
             float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
             for (int m = J; m < I; ++m)
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
-                    uint32_t a[4], bb[2];
-                    frag_a(Lm, 16 * I, 16 * m + 8 * kk, lane, a);
-                    frag_b(Am, 16 * m + 8 * kk, n0, lane, bb);
+                    // A = L rows 16I + g (+8), columns 16m + 8kk + t (+4); B = X rows
+                    // 16m + 8kk + t (+4), column n0 + g
+                    const uint32_t* la = Lt + (16 * I + gq) * LS + 16 * m + 8 * kk + tq;
+                    const uint32_t* xb = X + (16 * m + 8 * kk + tq) * XS + n0 + gq;
+                    const uint32_t a[4] = {la[0], la[8 * LS], la[4], la[8 * LS + 4]};
+                    const uint32_t bb[2] = {xb[0], xb[4 * XS]};
                     mma_m16n8k8(y, a, bb);
                 }
-            const int gq = lane >> 2, tq = lane & 3;
             Ys[gq * 8 + 2 * tq] = y[0];
             Ys[gq * 8 + 2 * tq + 1] = y[1];
             Ys[(gq + 8) * 8 + 2 * tq] = y[2];
@@ -205,50 +267,24 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const WyParams p) {
             float xo[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-                uint32_t a[4], bb[2];
-                frag_a(Am, 16 * I, 16 * I + 8 * kk, lane, a);
-                bb[0] = tf32_bits(Ys[(8 * kk + tq) * 8 + gq]);
-                bb[1] = tf32_bits(Ys[(8 * kk + tq + 4) * 8 + gq]);
+                const uint32_t* xa = X + (16 * I + gq) * XS + 16 * I + 8 * kk + tq;
+                const uint32_t a[4] = {xa[0], xa[8 * XS], xa[4], xa[8 * XS + 4]};
+                const uint32_t bb[2] = {tf32_bits(Ys[(8 * kk + tq) * 8 + gq]),
+                                        tf32_bits(Ys[(8 * kk + tq + 4) * 8 + gq])};
                 mma_m16n8k8(xo, a, bb);
             }
-            __syncwarp();
-            Am[sw64(16 * I + gq, n0 + 2 * tq)] = -xo[0];
-            Am[sw64(16 * I + gq, n0 + 2 * tq + 1)] = -xo[1];
-            Am[sw64(16 * I + gq + 8, n0 + 2 * tq)] = -xo[2];
-            Am[sw64(16 * I + gq + 8, n0 + 2 * tq + 1)] = -xo[3];
+            const int r0 = 16 * I + gq, c0 = n0 + 2 * tq;
+            *reinterpret_cast<uint2*>(X + r0 * XS + c0) = make_uint2(tf32_bits(-xo[0]), tf32_bits(-xo[1]));
+            *reinterpret_cast<uint2*>(X + (r0 + 8) * XS + c0) =
+                make_uint2(tf32_bits(-xo[2]), tf32_bits(-xo[3]));
+            __syncwarp();   // the next block down reads this one (and Ys is reused)
+            // bf16 pairs (columns c0, c0 + 1) of rows r0 and r0 + 8: byte 4 tq of chunk n0 / 8
+            const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = bekr[c0], e1 = bekr[c0 + 1];
+            *reinterpret_cast<uint32_t*>(out_b + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-xo[0] * b0, -xo[1] * b1);
+            *reinterpret_cast<uint32_t*>(out_b + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-xo[2] * b0, -xo[3] * b1);
+            *reinterpret_cast<uint32_t*>(out_g + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-xo[0] * e0, -xo[1] * e1);
+            *reinterpret_cast<uint32_t*>(out_g + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-xo[2] * e0, -xo[3] * e1);
         }
-        __syncthreads();
-    }
-
-    // ---- A diag(beta) (threads 0..63) and A diag(beta 2^Gx) (64..127) as bf16 K-major rows,
-    //      over L's space (the last round's barrier retired every read of L), zero above the
-    //      row's diagonal block, then one bulk store of both tiles
-    {
-        const int i = tid & 63;
-        const int jend = (i & ~15) + 16;   // columns of the blocks up to the diagonal one
-        const float* scale = (tid < 64) ? bet : bekr;
-        uint8_t* tile = sm + WY_OUT + ((tid < 64) ? 0 : 8192);
-#pragma unroll 1
-        for (int cq = 0; cq < 8; ++cq) {
-            float a[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                a[jj] = (8 * cq + jj < jend) ? Am[sw64(i, 8 * cq + jj)] * scale[8 * cq + jj] : 0.f;
-            *reinterpret_cast<uint4*>(tile + sw128(i, cq)) =
-                make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
-                           pack_bf16(a[6], a[7]));
-        }
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        uint8_t* dst = p.wy + ch * 16384;
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                     "r"(base + WY_OUT), "r"(16384u)
-                     : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        // the shared source must stay valid until the copy has read it
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
 }
 
