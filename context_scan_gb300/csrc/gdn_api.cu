@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "gdn.h"
 #include "gdn_internal.h"
 
@@ -13,6 +15,7 @@ using gdn::ChainParams;
 
 constexpr size_t kHeaderBytes = 256;   // device error word lives here
 constexpr size_t kAlign = 256;
+constexpr int kMaxSub = 2;             // summary sub-segments per segment (segmented forward)
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -25,7 +28,8 @@ bool tc_shape(const gdn_problem& p) {
     return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128;
 }
 
-// [header | WY tiles (tcgen05 shapes) | M | S | H_in (nseg > 1)]
+// [header | WY tiles (tcgen05 shapes) | M | S | H_in (nseg > 1)]; M and S hold up to
+// kMaxSub sub-segment summaries per segment
 WsLayout layout(const gdn_problem& p, int nseg) {
     WsLayout w{};
     const size_t bh = (size_t)p.B * p.H;
@@ -36,8 +40,8 @@ WsLayout layout(const gdn_problem& p, int nseg) {
         w.total = w.off_M;
         return w;
     }
-    w.off_S = w.off_M + round_up(sizeof(float) * nseg * bh * p.K * p.K);
-    w.off_Hin = w.off_S + round_up(sizeof(float) * nseg * bh * p.K * p.V);
+    w.off_S = w.off_M + round_up(sizeof(float) * kMaxSub * nseg * bh * p.K * p.K);
+    w.off_Hin = w.off_S + round_up(sizeof(float) * kMaxSub * nseg * bh * p.K * p.V);
     w.total = w.off_Hin + round_up(sizeof(float) * nseg * bh * p.K * p.V);
     return w;
 }
@@ -97,6 +101,23 @@ ChainParams base_params(const gdn_problem* p, void* ws) {
 }
 
 bool use_tc(const ChainParams& c) { return c.T > 0 && gdn::tc_supported(c); }
+
+// Sub-segments per segment for the segmented forward's summaries. The summary launch has
+// one CTA per (b, h, segment) and a CTA per SM; when B*H*(nseg-1) CTAs fill the last wave
+// poorly, splitting every segment in two (composed again by the scan) balances the waves.
+// Kept at 1 unless the split raises the wave efficiency and the halves keep >= 16 chunks.
+int summary_split(const ChainParams& c, int nseg) {
+    if (!use_tc(c) || nseg < 2) return 1;
+    const int chunks = c.T / nseg / gdn::kChunk;
+    if (chunks % 2 != 0 || chunks / 2 < 16) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return 1;
+    const double units = (double)c.B * c.H * (nseg - 1);
+    auto eff = [&](double u) { return u / (std::ceil(u / sms) * sms); };
+    return eff(2.0 * units) > eff(units) + 0.05 ? 2 : 1;
+}
 
 // The tcgen05 chains read every chunk's WY tiles from the workspace: form them first (one
 // launch for all chunks of the problem). Nothing to do on the CUDA-core path.
@@ -254,7 +275,9 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
     cw.seg_len = p->T / nseg;
     cudaError_t e = prepare(cw, p, workspace, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
-    // 1. summaries of segments 0..nseg-2 (the last segment's summary feeds nothing)
+    // 1. summaries of segments 0..nseg-2 (the last segment's summary feeds nothing), each
+    //    as nsub sub-segment summaries
+    const int nsub = summary_split(cw, nseg);
     ChainParams cs = base_params(p, workspace);
     cs.wy = cw.wy;
     cs.k = k;
@@ -263,15 +286,15 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
     cs.beta = beta;
     cs.M = M;
     cs.S = S;
-    cs.seg_len = p->T / nseg;
-    cs.nseg_run = nseg - 1;
-    cs.nseg_total = nseg;
+    cs.seg_len = p->T / nseg / nsub;
+    cs.nseg_run = (nseg - 1) * nsub;
+    cs.nseg_total = nseg * nsub;
     if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
     e = run_summary(cs, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     // 2. exclusive in-order scan of the summaries
     if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
-    e = gdn::launch_scan(M, S, h0, H_in, nseg, BH, p->K, p->V, s);
+    e = gdn::launch_scan(M, S, h0, H_in, nseg, BH, p->K, p->V, s, nsub);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
     // 3. every segment's forward from its scanned state

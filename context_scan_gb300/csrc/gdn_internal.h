@@ -48,8 +48,9 @@ struct ChainParams {
 // fp32 CUDA-core kernels (any supported K/V, fp32 or bf16 inputs)
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
+// nsub: sub-segment summaries per segment (M, S indexed by sub-segment); H_in at segment starts
 cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                        int BH, int K, int V, cudaStream_t s);
+                        int BH, int K, int V, cudaStream_t s, int nsub = 1);
 
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);

@@ -294,10 +294,14 @@ cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
 // (head, 32-column tile); the serial dependency runs over segments inside the CTA. Each
 // step stages M[s-1] in shared memory (rows padded to KD + 4 floats) and every thread
 // accumulates a 4 x 4 block of the product in registers, four terms of the sum at a time.
+// With nsub > 1 each segment's summary is given as nsub consecutive sub-segment summaries
+// (M, S indexed by sub-segment); they are applied in order, and H_in is written at segment
+// starts only.
 template <int KD>
 __global__ void __launch_bounds__(KD * 2)
 scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
-            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int V) {
+            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int V,
+            int nsub) {
     constexpr int CT = 32, NT = KD * 2, MP = KD + 4;
     extern __shared__ float4 sm4[];
     float* Ms = reinterpret_cast<float*>(sm4);   // KD x MP
@@ -311,16 +315,18 @@ scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
         *reinterpret_cast<float4*>(Hc + l * CT + 4 * c4) = x;
     }
     __syncthreads();
-    for (int s = 0; s < nseg; ++s) {
-        const long long hb = ((long long)s * BH + bh) * KD;
-        for (int e = tid; e < KD * CT / 4; e += NT) {
-            const int l = e / (CT / 4), c4 = e % (CT / 4);
-            *reinterpret_cast<float4*>(H_in + (hb + l) * V + c0 + 4 * c4) =
-                *reinterpret_cast<const float4*>(Hc + l * CT + 4 * c4);
+    for (int ss = 0; ss < nseg * nsub; ++ss) {
+        if (ss % nsub == 0) {
+            const long long hb = ((long long)(ss / nsub) * BH + bh) * KD;
+            for (int e = tid; e < KD * CT / 4; e += NT) {
+                const int l = e / (CT / 4), c4 = e % (CT / 4);
+                *reinterpret_cast<float4*>(H_in + (hb + l) * V + c0 + 4 * c4) =
+                    *reinterpret_cast<const float4*>(Hc + l * CT + 4 * c4);
+            }
+            if (ss / nsub == nseg - 1) break;
         }
-        if (s == nseg - 1) break;
-        const float* Mg = M + ((long long)s * BH + bh) * KD * KD;
-        const float* Sg = S + ((long long)s * BH + bh) * KD * V;
+        const float* Mg = M + ((long long)ss * BH + bh) * KD * KD;
+        const float* Sg = S + ((long long)ss * BH + bh) * KD * V;
         for (int e = tid; e < KD * KD / 4; e += NT) {
             const int i = e / (KD / 4), l4 = e % (KD / 4);
             *reinterpret_cast<float4*>(Ms + i * MP + 4 * l4) =
@@ -367,13 +373,13 @@ scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
 
 template <int KD>
 cudaError_t launch_scan_k(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                          int BH, int V, cudaStream_t s) {
+                          int BH, int V, int nsub, cudaStream_t s) {
     const size_t smem = sizeof(float) * ((size_t)KD * (KD + 4) + (size_t)KD * 32);
     cudaError_t e = cudaFuncSetAttribute(scan_kernel<KD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)BH, (unsigned)(V / 32));
-    scan_kernel<KD><<<grid, KD * 2, smem, s>>>(M, S, h0, H_in, nseg, BH, V);
+    scan_kernel<KD><<<grid, KD * 2, smem, s>>>(M, S, h0, H_in, nseg, BH, V, nsub);
     return cudaGetLastError();
 }
 }  // namespace
@@ -387,9 +393,10 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                        int BH, int K, int V, cudaStream_t s) {
-    if (K == 128) return launch_scan_k<128>(M, S, h0, H_in, nseg, BH, V, s);
-    if (K == 64) return launch_scan_k<64>(M, S, h0, H_in, nseg, BH, V, s);
+                        int BH, int K, int V, cudaStream_t s, int nsub) {
+    if (nsub < 1) return cudaErrorInvalidValue;
+    if (K == 128) return launch_scan_k<128>(M, S, h0, H_in, nseg, BH, V, nsub, s);
+    if (K == 64) return launch_scan_k<64>(M, S, h0, H_in, nseg, BH, V, nsub, s);
     return cudaErrorInvalidValue;
 }
 

@@ -94,7 +94,8 @@ typedef struct {
  * It holds the error word; for the tensor-core shapes (bf16 in, K == V == 128) the
  * per-chunk WY factors A diag(beta) and A diag(beta exp-decay), A = (I + L)^-1, as two bf16
  * 64 x 64 tiles per chunk (16 KiB per chunk and head, formed by one launch before the
- * chains); for nseg > 1 the segment summaries and scanned states. */
+ * chains); for nseg > 1 the segment summaries (up to two sub-segment summaries per segment)
+ * and scanned states. */
 GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
 
 /* Chunked forward over all T tokens from the initial state h0.
@@ -163,8 +164,8 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
  *   loads the library holds it until the process exits. The call allocates nothing.
  *   Limit: problems with gdn_workspace_bytes(p, nseg) > GDN_NOALLOC_SCRATCH_BYTES are
  *   rejected with GDN_ERR_WORKSPACE (at bf16, K = V = 128 that is
- *   B*H*(T/64*16 KiB + nseg*192 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
- *   T = 2048 in 4 segments take 40 MiB).
+ *   B*H*(T/64*16 KiB + nseg*320 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
+ *   T = 2048 in 4 segments take 56 MiB).
  *   device_error: optional (NULL to skip) 8-byte-aligned device pointer to two unsigned
  *   words that receive this call's device error word {code, detail} (see
  *   gdn_check_device_error for the codes) when the call's stream work completes.

@@ -68,8 +68,9 @@ def test_workspace_bytes_and_status_strings(L):
     wy = 64 * (32768 // 64) * 16384
     assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256 + wy
     n4 = L.gdn_workspace_bytes(ctypes.byref(p), 4)
-    # plus M, S and H_in for 4 segments of 64 heads, fp32
-    assert n4 == 256 + wy + 4 * 64 * 128 * 128 * 4 * 3
+    # plus M and S for up to 2 sub-segments of each of 4 segments, and H_in for 4 segments,
+    # of 64 heads, fp32
+    assert n4 == 256 + wy + 4 * 64 * 128 * 128 * 4 * (2 + 2 + 1)
     # the CUDA-core shapes need no WY tiles
     assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, in_dtype=0)), 1) == 256
     assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, K=64, V=64)), 1) == 256
