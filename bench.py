@@ -150,7 +150,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "context_scan_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".h")):
+        if fn.endswith((".cu", ".cuh", ".h")):
             h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
