@@ -86,18 +86,27 @@ def rank_seed_offset(rank: int) -> int:
 # ---------------------------------------------------------------------------------------
 # algorithmic model of the path (bytes and flops per launch)
 # ---------------------------------------------------------------------------------------
-def algorithmic(w, out_bytes: int = 4):
-    """Compulsory HBM bytes and dense-contraction flops of each stage for workload w."""
+def algorithmic(w, pieces=None, out_bytes: int = 4):
+    """Compulsory HBM bytes and dense-contraction flops of each stage for workload w, when the
+    library cuts every sequence into `pieces` pieces (default: one per segment), and of the
+    method itself (the pages' flow: summaries of nseg-1 segments, the scan, the forward)."""
+    P = pieces or w.nseg
     isz = 2 if w.in_dtype == "bf16" else 4
     BH = w.B * w.H
     tok_heads = w.B * w.T * w.H
-    sum_tok_heads = tok_heads * (w.nseg - 1) // w.nseg
     chunks = tok_heads // 64
-    sum_chunks = sum_tok_heads // 64
     K, V = w.K, w.V
     kv_state = BH * K * V * 4
     kk_state = BH * K * K * 4
     tc = w.in_dtype == "bf16" and K == 128 and V == 128
+    fwd_tok = (2 * K + V) * isz + 2 * isz + V * out_bytes      # q, k, v, g, beta in; o out
+    sum_tok = (K + V) * isz + 2 * isz                          # k, v, g, beta in
+    # prep (K K^T, U, W) + state (W H, Kd^T R) + output (Q K^T, Qd H, C R), per chunk
+    fwd_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 64 * K * V * 2
+                 + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
+    # prep (K K^T, U, W) + augmented K x (K+V) state update, per chunk
+    sum_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 2 * 64 * K * (K + V))
+    ps = max(P - 2, 0)   # pieces with a summary
     stages = {
         # per-chunk WY factors (tensor-core path only): reads k, g, beta; writes two bf16
         # 64 x 64 tiles per chunk. An intermediate of this implementation, not of the method,
@@ -106,36 +115,42 @@ def algorithmic(w, out_bytes: int = 4):
             "bytes": (tok_heads * (K * isz + 2 * isz) + chunks * 16384) if tc else 0,
             "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64) if tc else 0,
         },
-        "summary": {
-            "bytes": sum_tok_heads * ((K + V) * isz + 2 * isz) + (w.nseg - 1) * (kk_state + kv_state),
-            # prep (K K^T, U, W) + augmented K x (K+V) state update per chunk
-            "flops": sum_chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K
-                                   + 2 * 2 * 64 * K * (K + V)),
+        # piece 0's forward from h0 (handing its final state on) and the summaries of pieces
+        # 1..P-2
+        "phase1": {
+            "bytes": tok_heads // P * fwd_tok + 2 * kv_state
+            + tok_heads * ps // P * sum_tok + ps * (kk_state + kv_state),
+            "flops": chunks // P * fwd_flops + chunks * ps // P * sum_flops,
         },
         "scan": {
-            "bytes": (w.nseg - 1) * (kk_state + kv_state) + w.nseg * kv_state + kv_state,
-            "flops": (w.nseg - 1) * BH * 2 * K * K * V,
+            "bytes": (ps * (kk_state + kv_state) + kv_state + ps * kv_state + w.nseg * kv_state
+                      if P > 1 else w.nseg * kv_state),
+            "flops": ps * BH * 2 * K * K * V,
         },
-        "forward": {
-            "bytes": tok_heads * ((2 * K + V) * isz + 2 * isz + V * out_bytes)
-            + w.nseg * kv_state + kv_state,
-            # prep (K K^T, U, W) + state (W H, Kd^T R) + output (Q K^T, Qd H, C R)
-            "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K
-                               + 2 * 64 * K * V * 2
-                               + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V),
+        # the forward of pieces 1..P-1 from their scanned states
+        "phase2": {
+            "bytes": (tok_heads * (P - 1) // P * fwd_tok + P * kv_state) if P > 1 else 0,
+            "flops": chunks * (P - 1) // P * fwd_flops,
         },
     }
-    method = [n for n in stages if n != "wy"]
-    total = {"bytes": sum(stages[n]["bytes"] for n in method),
-             "flops": sum(stages[n]["flops"] for n in method)}
-    return stages, total
+    nseg = w.nseg
+    method = {
+        "bytes": tok_heads * (nseg - 1) // nseg * sum_tok + (nseg - 1) * (kk_state + kv_state)
+        + (nseg - 1) * (kk_state + kv_state) + nseg * kv_state + kv_state
+        + tok_heads * fwd_tok + nseg * kv_state + kv_state,
+        "flops": chunks * (nseg - 1) // nseg * sum_flops + (nseg - 1) * BH * 2 * K * K * V
+        + chunks * fwd_flops,
+    }
+    return stages, method
 
 
-def launches_per_step(w):
-    """Kernels one gdn_segmented_fwd call launches: WY factors (tensor-core path), summary,
-    scan, forward; with one segment only WY + forward."""
+def launches_per_step(w, pieces=None):
+    """Kernels one gdn_segmented_fwd call launches: WY factors (tensor-core path), piece 0's
+    forward, the piece summaries (3 pieces or more), the scan and the second forward (2 pieces
+    or more)."""
+    P = pieces or w.nseg
     tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128)
-    return tc + (3 if w.nseg > 1 else 1)
+    return tc + 1 + (1 if P >= 3 else 0) + (2 if P >= 2 else 0)
 
 
 def load_peaks():
@@ -252,6 +267,7 @@ def run_ours(args):
     o = torch.empty((w.B, w.T, w.H, w.V), dtype=torch.float32, device=dev)
     hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
     prob = gdn.problem(d["k"], d["v"], o)
+    pieces = gdn.segmented_pieces(prob, w.nseg)
     ws = gdn.alloc_workspace(prob, w.nseg, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -296,18 +312,18 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
 
-    stage_ms = {"wy": [], "summary": [], "scan": [], "forward": []}
+    stage_ms = {"wy": [], "phase1": [], "scan": [], "phase2": []}
     for e in ev:
         for i, name in enumerate(stage_ms):
             stage_ms[name].append(e[i].elapsed_time(e[i + 1]))
-    stages, total = algorithmic(w)
+    stages, total = algorithmic(w, pieces)
     avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
     dominant = max(avg, key=avg.get)
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     ach = stages[dominant]["bytes"] / (avg[dominant] * 1e-3) / 1e9
-    kernel_name = {"wy": "gdn_wy", "summary": "gdn_summary", "scan": "gdn_scan",
-                   "forward": "gdn_forward"}[dominant]
+    kernel_name = {"wy": "gdn_wy", "phase1": "gdn_phase1", "scan": "gdn_scan",
+                   "phase2": "gdn_forward"}[dominant]
     roofline = {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "traffic": recorded_traffic(kernel_name, w0.name),
                 "kernel": kernel_name, "kernel_ms": round(avg[dominant], 4),
@@ -361,8 +377,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w0.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
-                       "nseg": w.nseg, "chunk": 64, "in_dtype": w.in_dtype, "out_dtype": "f32",
-                       "state_dtype": "f32",
+                       "nseg": w.nseg, "pieces": pieces, "chunk": 64, "in_dtype": w.in_dtype,
+                       "out_dtype": "f32", "state_dtype": "f32",
                        "l2": f"inputs larger than L2 ({total_input_mb(w):.0f} MB in + "
                              f"{w.B * w.T * w.H * w.V * 4 / 2**20:.0f} MB out > 129 MB); no flush",
                        "parallelism": f"weak: {world} rank(s) x one batch each"},
@@ -374,7 +390,7 @@ def run_ours(args):
             "stage_ms": {k: round(v, 4) for k, v in avg.items()},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(w) * K,
+            "gpu_launches": launches_per_step(w, pieces) * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -15,12 +15,14 @@ using gdn::ChainParams;
 
 constexpr size_t kHeaderBytes = 256;   // device error word lives here
 constexpr size_t kAlign = 256;
-constexpr int kMaxSub = 2;             // summary sub-segments per segment (segmented forward)
+constexpr int kMaxSub = 8;             // pieces per segment (segmented forward)
+constexpr int kMinPieceChunks = 8;     // shortest piece, in chunks
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-    size_t off_wy, off_M, off_S, off_Hin, total;
+    size_t off_wy, off_M, off_S, off_Hp, total;
+    int pieces;
 };
 
 // Shapes that take the tcgen05 kernels (which also need the per-chunk WY tiles).
@@ -28,21 +30,58 @@ bool tc_shape(const gdn_problem& p) {
     return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128;
 }
 
-// [header | WY tiles (tcgen05 shapes) | M | S | H_in (nseg > 1)]; M and S hold up to
-// kMaxSub sub-segment summaries per segment
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+// Pieces P per sequence for the segmented forward (a multiple of nseg: segment starts are
+// piece starts). Piece 0's forward runs from h0 beside the summaries of pieces 1..P-2; an
+// in-order scan gives the state entering every piece; pieces 1..P-1 then run their forward.
+// Each phase launches B*H*(P-1) chains of T/P tokens, one per SM at a time, so more pieces
+// mean more parallel chains (and fuller waves) but shorter ones and one more scan step each.
+// P minimises 2 * waves(B*H*(P-1)) * chunks / P + 3 * (P - 2) (in chunk times; a scan step
+// costs about three), over P = nseg * {1, 2, 4, 8} with pieces of at least 8 chunks. Without a
+// device to size the waves it stays at nseg.
+int plan_pieces(const gdn_problem& p, int nseg) {
+    if (p.T <= 0) return nseg;
+    const int chunks = p.T / gdn::kChunk;   // a multiple of nseg (checked)
+    const int sms = sm_count();
+    if (sms < 1) return nseg;
+    const double bh = (double)p.B * p.H;
+    auto cost = [&](int P) {
+        const double waves = std::ceil(bh * (P > 1 ? P - 1 : 1) / sms);
+        const double phases = P > 1 ? 2.0 : 1.0;
+        return phases * waves * ((double)chunks / P) + 3.0 * (P > 2 ? P - 2 : 0);
+    };
+    int best = nseg;
+    for (int nsub = 2; nsub <= kMaxSub; nsub *= 2) {
+        const int P = nseg * nsub;
+        if ((chunks / nseg) % nsub != 0 || chunks / P < kMinPieceChunks) break;
+        if (cost(P) < cost(best)) best = P;
+    }
+    return best;
+}
+
+// [header | WY tiles (tcgen05 shapes) | M | S | Hp], each region 256-byte aligned: M, S hold
+// the summaries of pieces 1..P-2 and Hp the state entering each piece (indexed by piece)
 WsLayout layout(const gdn_problem& p, int nseg) {
     WsLayout w{};
     const size_t bh = (size_t)p.B * p.H;
+    w.pieces = plan_pieces(p, nseg);
     w.off_wy = kHeaderBytes;
     const size_t wy_bytes = tc_shape(p) ? bh * (size_t)(p.T / gdn::kChunk) * 16384u : 0;
     w.off_M = w.off_wy + round_up(wy_bytes);
-    if (nseg <= 1) {
-        w.total = w.off_M;
-        return w;
-    }
-    w.off_S = w.off_M + round_up(sizeof(float) * kMaxSub * nseg * bh * p.K * p.K);
-    w.off_Hin = w.off_S + round_up(sizeof(float) * kMaxSub * nseg * bh * p.K * p.V);
-    w.total = w.off_Hin + round_up(sizeof(float) * nseg * bh * p.K * p.V);
+    const size_t P = (size_t)w.pieces;
+    const size_t m_bytes = P >= 3 ? round_up(sizeof(float) * P * bh * p.K * p.K) : 0;
+    const size_t s_bytes = P >= 3 ? round_up(sizeof(float) * P * bh * p.K * p.V) : 0;
+    const size_t h_bytes = P >= 2 ? round_up(sizeof(float) * P * bh * p.K * p.V) : 0;
+    w.off_S = w.off_M + m_bytes;
+    w.off_Hp = w.off_S + s_bytes;
+    w.total = w.off_Hp + h_bytes;
     return w;
 }
 
@@ -102,23 +141,6 @@ ChainParams base_params(const gdn_problem* p, void* ws) {
 
 bool use_tc(const ChainParams& c) { return c.T > 0 && gdn::tc_supported(c); }
 
-// Sub-segments per segment for the segmented forward's summaries. The summary launch has
-// one CTA per (b, h, segment) and a CTA per SM; when B*H*(nseg-1) CTAs fill the last wave
-// poorly, splitting every segment in two (composed again by the scan) balances the waves.
-// Kept at 1 unless the split raises the wave efficiency and the halves keep >= 16 chunks.
-int summary_split(const ChainParams& c, int nseg) {
-    if (!use_tc(c) || nseg < 2) return 1;
-    const int chunks = c.T / nseg / gdn::kChunk;
-    if (chunks % 2 != 0 || chunks / 2 < 16) return 1;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-        return 1;
-    const double units = (double)c.B * c.H * (nseg - 1);
-    auto eff = [&](double u) { return u / (std::ceil(u / sms) * sms); };
-    return eff(2.0 * units) > eff(units) + 0.05 ? 2 : 1;
-}
-
 // The tcgen05 chains read every chunk's WY tiles from the workspace: form them first (one
 // launch for all chunks of the problem). Nothing to do on the CUDA-core path.
 cudaError_t prepare(ChainParams& c, const gdn_problem* p, void* ws, cudaStream_t s) {
@@ -134,6 +156,97 @@ cudaError_t run_summary(const ChainParams& c, cudaStream_t s) {
     return use_tc(c) ? gdn::launch_tc_summary(c, s) : gdn::launch_simt_summary(c, s);
 }
 
+// The segmented forward on validated arguments (also gdn_chunk_fwd, nseg = 1): each sequence
+// is cut into P pieces (plan_pieces). Stage events: 0 before the WY tiles, 1 before the first
+// phase, 2 before the scan, 3 before the second phase, 4 at the end.
+gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0, void* o,
+                         float* h_final, float* H_in_out, void* workspace, cudaStream_t s,
+                         void* const* events) {
+    const WsLayout w = layout(*p, nseg);
+    const int P = w.pieces, nsub = P / nseg;
+    const int BH = p->B * p->H;
+    char* wsb = reinterpret_cast<char*>(workspace);
+    if (mark(events, 0, s) != cudaSuccess || mark(events, 1, s) != cudaSuccess ||
+        mark(events, 2, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (p->T == 0) {
+        // nothing to process: every segment starts from h0 and h_final = h0 (or zeros)
+        if (H_in_out && gdn::launch_scan(nullptr, nullptr, h0, nullptr, H_in_out, nullptr, 0, nseg,
+                                         1, BH, p->K, p->V, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if (mark(events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
+        if (h_final && gdn::launch_scan(nullptr, nullptr, h0, nullptr, h_final, nullptr, 0, 1, 1, BH,
+                                        p->K, p->V, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        return from_cuda(mark(events, 4, s));
+    }
+    float* M = reinterpret_cast<float*>(wsb + w.off_M);
+    float* S = reinterpret_cast<float*>(wsb + w.off_S);
+    float* Hp = reinterpret_cast<float*>(wsb + w.off_Hp);
+    const long long hstride = (long long)BH * p->K * p->V;
+    auto chain = [&]() {
+        ChainParams c = base_params(p, workspace);
+        c.q = q;
+        c.k = k;
+        c.v = v;
+        c.g = g;
+        c.beta = beta;
+        c.o = o;
+        c.seg_len = p->T / P;
+        c.nseg_total = P;
+        return c;
+    };
+    // 0. the WY tiles of every chunk (tcgen05 path only)
+    if (mark(events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ChainParams cw = chain();
+    cudaError_t e = prepare(cw, p, workspace, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    // 1. piece 0's forward from h0, which hands its final state to piece 1, beside the
+    //    summaries of pieces 1..P-2 (launched as its programmatic dependent, so they start
+    //    at once on the SMs it leaves free)
+    if (mark(events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ChainParams f0 = chain();
+    f0.wy = cw.wy;
+    f0.h_start = h0;
+    f0.seg_first = 0;
+    f0.nseg_run = 1;
+    f0.h_final = P == 1 ? h_final : nullptr;
+    f0.h_out = P > 1 ? Hp : nullptr;
+    f0.h_out_seg_stride = hstride;
+    if ((e = run_forward(f0, s)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (P >= 3) {
+        ChainParams cs = chain();
+        cs.wy = cw.wy;
+        cs.M = M;
+        cs.S = S;
+        cs.seg_first = 1;
+        cs.nseg_run = P - 2;
+        cs.launch_dependent = 1;
+        if ((e = run_summary(cs, s)) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    // 2. the state entering every piece (and every segment)
+    if (mark(events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (P >= 2)
+        e = gdn::launch_scan(M, S, Hp + hstride, Hp, H_in_out, h0, 1, P, nsub, BH, p->K, p->V, s);
+    else if (H_in_out)
+        e = gdn::launch_scan(nullptr, nullptr, h0, nullptr, H_in_out, nullptr, 0, 1, 1, BH, p->K, p->V, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    // 3. pieces 1..P-1 from the scanned states
+    if (mark(events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (P >= 2) {
+        ChainParams cf = chain();
+        cf.wy = cw.wy;
+        cf.h_start = Hp;
+        cf.h_start_seg_stride = hstride;
+        cf.h_final = h_final;
+        cf.seg_first = 1;
+        cf.nseg_run = P - 1;
+        if ((e = run_forward(cf, s)) != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return from_cuda(mark(events, 4, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -141,6 +254,11 @@ extern "C" {
 size_t gdn_workspace_bytes(const gdn_problem* p, int nseg) {
     if (check_problem(p, nseg) != GDN_OK) return 0;
     return layout(*p, nseg).total;
+}
+
+int gdn_segmented_pieces(const gdn_problem* p, int nseg) {
+    if (check_problem(p, nseg) != GDN_OK) return 0;
+    return plan_pieces(*p, nseg);
 }
 
 gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -155,29 +273,8 @@ gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, con
                             (const void*)h_final})
         if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
     if ((st = check_device()) != GDN_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    ChainParams c = base_params(p, workspace);
-    c.q = q;
-    c.k = k;
-    c.v = v;
-    c.g = g;
-    c.beta = beta;
-    c.h_start = h0;
-    c.h_start_seg_stride = 0;
-    c.o = o;
-    c.h_final = h_final;
-    c.seg_len = p->T;
-    c.nseg_run = 1;
-    c.nseg_total = 1;
-    if (p->T == 0) {
-        // nothing to process: h_final = h0 (or zeros)
-        if (!h_final) return GDN_OK;
-        return from_cuda(gdn::launch_scan(nullptr, nullptr, h0, h_final, 1, p->B * p->H, p->K,
-                                          p->V, s));
-    }
-    cudaError_t e = prepare(c, p, workspace, s);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    return from_cuda(run_forward(c, s));
+    return run_segmented(p, 1, q, k, v, g, beta, h0, o, h_final, nullptr, workspace,
+                         reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const void* k, const void* v,
@@ -218,7 +315,8 @@ gdn_status gdn_summary_scan(const gdn_problem* p, int nseg, const float* M, cons
         if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
     gdn_status st = check_device();
     if (st != GDN_OK) return st;
-    return from_cuda(gdn::launch_scan(M, S, h0, H_in, nseg, p->B * p->H, p->K, p->V,
+    return from_cuda(gdn::launch_scan(nseg > 1 ? M : nullptr, nseg > 1 ? S : nullptr, h0, nullptr,
+                                      H_in, nullptr, 0, nseg, 1, p->B * p->H, p->K, p->V,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -243,78 +341,8 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
                             (const void*)h_final, (const void*)H_in_out})
         if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
     if ((st = check_device()) != GDN_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const WsLayout w = layout(*p, nseg);
-    char* wsb = reinterpret_cast<char*>(workspace);
-    const int BH = p->B * p->H;
-
-    if (nseg == 1) {
-        if (mark(stage_events, 0, s) != cudaSuccess || mark(stage_events, 1, s) != cudaSuccess ||
-            mark(stage_events, 2, s) != cudaSuccess)
-            return GDN_ERR_CUDA;
-        if (H_in_out) {
-            cudaError_t e = gdn::launch_scan(nullptr, nullptr, h0, H_in_out, 1, BH, p->K, p->V, s);
-            if (e != cudaSuccess) return GDN_ERR_CUDA;
-        }
-        if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
-        st = gdn_chunk_fwd(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes,
-                           stream);
-        if (st != GDN_OK) return st;
-        return from_cuda(mark(stage_events, 4, s));
-    }
-    float* M = reinterpret_cast<float*>(wsb + w.off_M);
-    float* S = reinterpret_cast<float*>(wsb + w.off_S);
-    float* H_in = H_in_out ? H_in_out : reinterpret_cast<float*>(wsb + w.off_Hin);
-
-    // 0. the WY tiles of every chunk (tcgen05 path only)
-    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
-    ChainParams cw = base_params(p, workspace);
-    cw.k = k;
-    cw.g = g;
-    cw.beta = beta;
-    cw.seg_len = p->T / nseg;
-    cudaError_t e = prepare(cw, p, workspace, s);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    // 1. summaries of segments 0..nseg-2 (the last segment's summary feeds nothing), each
-    //    as nsub sub-segment summaries
-    const int nsub = summary_split(cw, nseg);
-    ChainParams cs = base_params(p, workspace);
-    cs.wy = cw.wy;
-    cs.k = k;
-    cs.v = v;
-    cs.g = g;
-    cs.beta = beta;
-    cs.M = M;
-    cs.S = S;
-    cs.seg_len = p->T / nseg / nsub;
-    cs.nseg_run = (nseg - 1) * nsub;
-    cs.nseg_total = nseg * nsub;
-    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
-    e = run_summary(cs, s);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    // 2. exclusive in-order scan of the summaries
-    if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
-    e = gdn::launch_scan(M, S, h0, H_in, nseg, BH, p->K, p->V, s, nsub);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
-    // 3. every segment's forward from its scanned state
-    ChainParams cf = base_params(p, workspace);
-    cf.wy = cw.wy;
-    cf.q = q;
-    cf.k = k;
-    cf.v = v;
-    cf.g = g;
-    cf.beta = beta;
-    cf.h_start = H_in;
-    cf.h_start_seg_stride = (long long)BH * p->K * p->V;
-    cf.o = o;
-    cf.h_final = h_final;
-    cf.seg_len = p->T / nseg;
-    cf.nseg_run = nseg;
-    cf.nseg_total = nseg;
-    e = run_forward(cf, s);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    return from_cuda(mark(stage_events, 4, s));
+    return run_segmented(p, nseg, q, k, v, g, beta, h0, o, h_final, H_in_out, workspace,
+                         reinterpret_cast<cudaStream_t>(stream), stage_events);
 }
 
 const char* gdn_status_string(gdn_status s) {

@@ -38,19 +38,33 @@ struct ChainParams {
     void* wy;
     int B, T, H, K, V;
     int seg_len;       // tokens per segment (multiple of 64)
-    int nseg_run;      // segments this launch processes: 0..nseg_run-1
+    int seg_first;     // first segment this launch processes
+    int nseg_run;      // segments this launch processes: seg_first .. seg_first+nseg_run-1
     int nseg_total;    // segments in the whole problem
+    // forward: when non-null, the final state of segment s is also written to
+    // h_out + (s + 1) * h_out_seg_stride + (b*H + h)*K*V (the state entering segment s + 1)
+    float* h_out;
+    long long h_out_seg_stride;
     int in_bf16;
     int out_bf16;
+    // launch as the programmatic dependent of the preceding grid in the stream (the kernel
+    // then finishes only after that grid has)
+    int launch_dependent;
     DeviceError* err;
 };
 
 // fp32 CUDA-core kernels (any supported K/V, fp32 or bf16 inputs)
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
-// nsub: sub-segment summaries per segment (M, S indexed by sub-segment); H_in at segment starts
-cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                        int BH, int K, int V, cudaStream_t s, int nsub = 1);
+// In-order scan over consecutive pieces p_first .. P-1 of every (b, h): the state entering
+// piece p_first is h_first ([BH][K][V], or zero when null); entering piece p+1 it is
+// M[p] H + S[p] (M, S indexed by piece, [piece][BH][K][K|V]). The state entering every piece
+// p > p_first is written to Hp[p] ([P][BH][K][V]) when Hp is non-null, and the state entering
+// every piece p with p % nsub == 0 to H_seg[p / nsub] ([P/nsub][BH][K][V]) when H_seg is
+// non-null; H_seg[0] is h_seg0 (or zero) when p_first > 0.
+cudaError_t launch_scan(const float* M, const float* S, const float* h_first, float* Hp,
+                        float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
+                        int K, int V, cudaStream_t s);
 
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);

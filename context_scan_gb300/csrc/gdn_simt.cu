@@ -61,6 +61,8 @@ struct SimtSmem {
 
 template <int KD, int CT, bool SUMMARY>
 __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
+    // a forward grid lets a grid launched as its programmatic dependent start right away
+    if (!SUMMARY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     using L = SimtSmem<KD, CT, SUMMARY>;
     extern __shared__ float sm[];
     float* ks = sm + L::off_k;
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
 
     const int tid = threadIdx.x;
     const int chain = blockIdx.x;
-    const int seg = chain % p.nseg_run;
+    const int seg = p.seg_first + chain % p.nseg_run;
     const int bh = chain / p.nseg_run;
     const int b = bh / p.H, h = bh % p.H;
     const int c0 = blockIdx.y * CT;   // first state column of this tile
@@ -268,12 +270,20 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
             else
                 p.S[(base * KD + l) * V + (gc - KD)] = Hs[e];
         }
-    } else if (p.h_final && seg == p.nseg_total - 1) {
-        for (int e = tid; e < KD * CT; e += kThreads) {
-            const int l = e / CT, c = e % CT;
-            p.h_final[((long long)bh * KD + l) * V + c0 + c] = Hs[e];
-        }
+    } else {
+        if (p.h_final && seg == p.nseg_total - 1)
+            for (int e = tid; e < KD * CT; e += kThreads) {
+                const int l = e / CT, c = e % CT;
+                p.h_final[((long long)bh * KD + l) * V + c0 + c] = Hs[e];
+            }
+        if (p.h_out)   // the state entering the next segment
+            for (int e = tid; e < KD * CT; e += kThreads) {
+                const int l = e / CT, c = e % CT;
+                p.h_out[(seg + 1) * p.h_out_seg_stride + ((long long)bh * KD + l) * V + c0 + c] = Hs[e];
+            }
     }
+    // a summary grid launched as a programmatic dependent completes after its primary grid
+    if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int KD, bool SUMMARY>
@@ -286,47 +296,71 @@ cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int ncols = SUMMARY ? KD + p.V : p.V;
     dim3 grid((unsigned)(p.B * p.H * p.nseg_run), (unsigned)(ncols / CT));
-    kern<<<grid, kThreads, L::bytes, s>>>(p);
-    return cudaGetLastError();
+    if (!p.launch_dependent) {
+        kern<<<grid, kThreads, L::bytes, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-// Exclusive scan H_in[0] = h0, H_in[s] = M[s-1] H_in[s-1] + S[s-1], fp32, one CTA per
-// (head, 32-column tile); the serial dependency runs over segments inside the CTA. Each
-// step stages M[s-1] in shared memory (rows padded to KD + 4 floats) and every thread
-// accumulates a 4 x 4 block of the product in registers, four terms of the sum at a time.
-// With nsub > 1 each segment's summary is given as nsub consecutive sub-segment summaries
-// (M, S indexed by sub-segment); they are applied in order, and H_in is written at segment
-// starts only.
+// In-order scan over consecutive pieces of each sequence, fp32, one CTA per (head, 32-column
+// tile); the serial dependency runs over pieces inside the CTA: the state entering piece
+// p_first is given (h_first, or zero), and the state entering piece p+1 is M[p] H + S[p]
+// (the affine summary of piece p applied to the state entering it). Each step stages M[p] in
+// shared memory (rows padded to KD + 4 floats) and every thread accumulates a 4 x 4 block of
+// the product in registers, four terms of the sum at a time. The states entering pieces
+// p_first+1 .. P-1 go to Hp, those entering every nsub-th piece (segment starts) to H_seg.
 template <int KD>
 __global__ void __launch_bounds__(KD * 2)
 scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
-            const float* __restrict__ h0, float* __restrict__ H_in, int nseg, int BH, int V,
-            int nsub) {
+            const float* __restrict__ h_first, float* __restrict__ Hp, float* __restrict__ H_seg,
+            const float* __restrict__ h_seg0, int p_first, int P, int nsub, int BH, int V) {
     constexpr int CT = 32, NT = KD * 2, MP = KD + 4;
     extern __shared__ float4 sm4[];
     float* Ms = reinterpret_cast<float*>(sm4);   // KD x MP
     float* Hc = Ms + KD * MP;                    // KD x CT, the current state's column tile
     const int bh = blockIdx.x, c0 = blockIdx.y * CT, tid = threadIdx.x;
     const int ri = tid >> 3, ci = tid & 7;       // rows 4ri..4ri+3, columns 4ci..4ci+3
+    // state tile <-> global [.][BH][KD][V]
+    auto put = [&](float* dst, long long slot) {
+        const long long hb = (slot * BH + bh) * KD;
+        for (int e = tid; e < KD * CT / 4; e += NT) {
+            const int l = e / (CT / 4), c4 = e % (CT / 4);
+            *reinterpret_cast<float4*>(dst + (hb + l) * V + c0 + 4 * c4) =
+                *reinterpret_cast<const float4*>(Hc + l * CT + 4 * c4);
+        }
+    };
+    if (H_seg && p_first > 0)   // the state entering the first segment
+        for (int e = tid; e < KD * CT / 4; e += NT) {
+            const int l = e / (CT / 4), c4 = e % (CT / 4);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h_seg0) x = *reinterpret_cast<const float4*>(h_seg0 + ((long long)bh * KD + l) * V + c0 + 4 * c4);
+            *reinterpret_cast<float4*>(H_seg + ((long long)bh * KD + l) * V + c0 + 4 * c4) = x;
+        }
     for (int e = tid; e < KD * CT / 4; e += NT) {
         const int l = e / (CT / 4), c4 = e % (CT / 4);
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (h0) x = *reinterpret_cast<const float4*>(h0 + ((long long)bh * KD + l) * V + c0 + 4 * c4);
+        if (h_first) x = *reinterpret_cast<const float4*>(h_first + ((long long)bh * KD + l) * V + c0 + 4 * c4);
         *reinterpret_cast<float4*>(Hc + l * CT + 4 * c4) = x;
     }
     __syncthreads();
-    for (int ss = 0; ss < nseg * nsub; ++ss) {
-        if (ss % nsub == 0) {
-            const long long hb = ((long long)(ss / nsub) * BH + bh) * KD;
-            for (int e = tid; e < KD * CT / 4; e += NT) {
-                const int l = e / (CT / 4), c4 = e % (CT / 4);
-                *reinterpret_cast<float4*>(H_in + (hb + l) * V + c0 + 4 * c4) =
-                    *reinterpret_cast<const float4*>(Hc + l * CT + 4 * c4);
-            }
-            if (ss / nsub == nseg - 1) break;
-        }
-        const float* Mg = M + ((long long)ss * BH + bh) * KD * KD;
-        const float* Sg = S + ((long long)ss * BH + bh) * KD * V;
+    for (int p = p_first; p < P; ++p) {
+        // Hc holds the state entering piece p
+        if (Hp && p > p_first) put(Hp, p);
+        if (H_seg && p % nsub == 0) put(H_seg, p / nsub);
+        if (p == P - 1 || !M) continue;   // no summaries: every piece starts from the same state
+        const float* Mg = M + ((long long)p * BH + bh) * KD * KD;
+        const float* Sg = S + ((long long)p * BH + bh) * KD * V;
         for (int e = tid; e < KD * KD / 4; e += NT) {
             const int i = e / (KD / 4), l4 = e % (KD / 4);
             *reinterpret_cast<float4*>(Ms + i * MP + 4 * l4) =
@@ -372,14 +406,16 @@ scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
 }
 
 template <int KD>
-cudaError_t launch_scan_k(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                          int BH, int V, int nsub, cudaStream_t s) {
+cudaError_t launch_scan_k(const float* M, const float* S, const float* h_first, float* Hp,
+                          float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
+                          int V, cudaStream_t s) {
     const size_t smem = sizeof(float) * ((size_t)KD * (KD + 4) + (size_t)KD * 32);
     cudaError_t e = cudaFuncSetAttribute(scan_kernel<KD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)BH, (unsigned)(V / 32));
-    scan_kernel<KD><<<grid, KD * 2, smem, s>>>(M, S, h0, H_in, nseg, BH, V, nsub);
+    scan_kernel<KD><<<grid, KD * 2, smem, s>>>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub,
+                                                BH, V);
     return cudaGetLastError();
 }
 }  // namespace
@@ -392,11 +428,12 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s) {
     return p.K == 128 ? launch_chain<128, true>(p, s) : launch_chain<64, true>(p, s);
 }
 
-cudaError_t launch_scan(const float* M, const float* S, const float* h0, float* H_in, int nseg,
-                        int BH, int K, int V, cudaStream_t s, int nsub) {
-    if (nsub < 1) return cudaErrorInvalidValue;
-    if (K == 128) return launch_scan_k<128>(M, S, h0, H_in, nseg, BH, V, nsub, s);
-    if (K == 64) return launch_scan_k<64>(M, S, h0, H_in, nseg, BH, V, nsub, s);
+cudaError_t launch_scan(const float* M, const float* S, const float* h_first, float* Hp,
+                        float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
+                        int K, int V, cudaStream_t s) {
+    if (nsub < 1 || p_first < 0 || P <= p_first) return cudaErrorInvalidValue;
+    if (K == 128) return launch_scan_k<128>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
+    if (K == 64) return launch_scan_k<64>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     return cudaErrorInvalidValue;
 }
 

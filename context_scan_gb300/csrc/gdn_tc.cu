@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     const ChainParams& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int chain = blockIdx.x;
-    const int seg = chain % c.nseg_run;
+    const int seg = c.seg_first + chain % c.nseg_run;
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
     const int nchunks = c.seg_len / kC;
@@ -200,6 +200,10 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
     const long long row_seg = (long long)b * c.T + (long long)seg * c.seg_len;   // flattened (b, t)
 
+    // A forward grid lets a grid launched after it as its programmatic dependent start right
+    // away (the summaries that run beside the first piece's forward); a summary grid so
+    // launched finishes only after its primary has (see the end of the kernel).
+    if (!SUMMARY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         for (int i = 0; i < KST; ++i) {
             mbar_init(bar0 + B_KFULL + 8 * i, 2);
@@ -803,7 +807,9 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             } else if (c.h_final && seg == c.nseg_total - 1) {
                 dst = c.h_final + bhoff;
             }
-            if (dst) {
+            // the forward may also hand its final state to the next segment
+            float* dst2 = (!SUMMARY && c.h_out) ? c.h_out + (seg + 1) * c.h_out_seg_stride + bhoff : nullptr;
+            if (dst || dst2) {
                 const float sgm = done > 0 ? sig_next : 1.f;
 #pragma unroll 1
                 for (int g = 0; g < 8; ++g) {
@@ -811,7 +817,11 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     tmem_ld16(t_row + tm_h + 16 * g, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) dst[(long long)(16 * g + j) * kD + st] = sgm * x[j];
+                    for (int j = 0; j < 16; ++j) {
+                        const long long idx = (long long)(16 * g + j) * kD + st;
+                        if (dst) dst[idx] = sgm * x[j];
+                        if (dst2) dst2[idx] = sgm * x[j];
+                    }
                 }
             }
         }
@@ -827,6 +837,9 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(F::TMEM_COLS)
                      : "memory");
+    // a summary grid launched as a programmatic dependent completes after its primary grid
+    // (a no-op otherwise), so the launches that follow it in the stream see both finished
+    if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------
@@ -848,8 +861,21 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
                                          (int)bytes);
     if (e != cudaSuccess) return e;
     const long long chains = (long long)c.B * c.H * c.nseg_run;
-    kern<<<(unsigned)chains, Cfg<SUMMARY>::THREADS, bytes, s>>>(tp);
-    return cudaGetLastError();
+    if (!c.launch_dependent) {
+        kern<<<(unsigned)chains, Cfg<SUMMARY>::THREADS, bytes, s>>>(tp);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)chains);
+    cfg.blockDim = dim3(Cfg<SUMMARY>::THREADS);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tp);
 }
 
 }  // namespace

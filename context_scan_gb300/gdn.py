@@ -18,7 +18,7 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
           3: "GDN_ERR_UNSUPPORTED_DTYPE", 4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_WORKSPACE",
           6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
-EXPORTED = ("gdn_workspace_bytes", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
+EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
             "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_status_string", "gdn_check_device_error")
 
@@ -50,6 +50,8 @@ def lib():
         pp = ctypes.POINTER(Problem)
         L.gdn_workspace_bytes.argtypes = [pp, ctypes.c_int]
         L.gdn_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_segmented_pieces.argtypes = [pp, ctypes.c_int]
+        L.gdn_segmented_pieces.restype = ctypes.c_int
         L.gdn_chunk_fwd.argtypes = [pp] + [_P] * 9 + [ctypes.c_size_t, _P]
         L.gdn_segment_summary.argtypes = [pp, ctypes.c_int] + [_P] * 7 + [ctypes.c_size_t, _P]
         L.gdn_summary_scan.argtypes = [pp, ctypes.c_int] + [_P] * 5
@@ -102,6 +104,11 @@ def _check(status: int, where: str):
 
 def workspace_bytes(prob: Problem, nseg: int = 1) -> int:
     return int(lib().gdn_workspace_bytes(ctypes.byref(prob), nseg))
+
+
+def segmented_pieces(prob: Problem, nseg: int = 1) -> int:
+    """Pieces per sequence the segmented forward uses on the current device (0: invalid)."""
+    return int(lib().gdn_segmented_pieces(ctypes.byref(prob), nseg))
 
 
 def alloc_workspace(prob: Problem, nseg: int = 1, device="cuda"):

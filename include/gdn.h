@@ -94,12 +94,25 @@ typedef struct {
  * It holds the error word; for the tensor-core shapes (bf16 in, K == V == 128) the
  * per-chunk WY factors A diag(beta) and A diag(beta exp-decay), A = (I + L)^-1, as two bf16
  * 64 x 64 tiles per chunk (16 KiB per chunk and head, formed by one launch before the
- * chains); for nseg > 1 the segment summaries (up to two sub-segment summaries per segment)
- * and scanned states. */
+ * chains); and, with P = gdn_segmented_pieces(p, nseg) pieces per sequence, fp32 [P,B,H,K,K]
+ * and [P,B,H,K,V] arrays for the piece summaries (P >= 3) and one [P,B,H,K,V] for the state
+ * entering each piece (P >= 2). P depends on the current device's SM count: size and run on
+ * the same device. */
 GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
+
+/* Pieces per sequence that gdn_segmented_fwd (and gdn_chunk_fwd, nseg = 1) cuts the tokens
+ * into on the current device: a multiple of nseg, so segment starts are piece starts. The
+ * forward of piece 0 runs from h0 beside the affine summaries of pieces 1..P-2 (RFC section
+ * 2.2), an in-order scan gives the state entering every piece, and pieces 1..P-1 then run
+ * their chunked forward from those states: each phase has B*H*(P-1) independent chains, so
+ * the GPU stays busy when B*H alone would not fill it. Chosen to balance wave fill, chain
+ * length and scan steps (nseg when no device is current). Returns 0 for an invalid problem. */
+GDN_API int gdn_segmented_pieces(const gdn_problem* p, int nseg);
 
 /* Chunked forward over all T tokens from the initial state h0.
  *   RFC section 2.1 (recurrence); ART section 08 "First parallelize within a GPU" (chunks).
+ *   Runs as gdn_segmented_fwd with one segment (cut into gdn_segmented_pieces(p, 1) pieces);
+ *   workspace: gdn_workspace_bytes(p, 1).
  *   h0       [B,H,K,V] fp32, or NULL for a zero initial state.
  *   o        [B,T,H,V] out_dtype, written.
  *   h_final  [B,H,K,V] fp32, the state after token T-1; NULL skips it.
@@ -127,9 +140,12 @@ GDN_API gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const voi
 GDN_API gdn_status gdn_summary_scan(const gdn_problem* p, int nseg, const float* M, const float* S,
                             const float* h0, float* H_in, void* stream);
 
-/* The segmented forward: summaries of segments 0..nseg-2, the exclusive scan, then every
- * segment's chunked forward from its scanned H_in (RFC section 6.4.1/6.4.2 forward flow
- * on one GPU). o and h_final equal gdn_chunk_fwd's up to rounding.
+/* The segmented forward (RFC section 6.4.1/6.4.2 forward flow on one GPU): with P =
+ * gdn_segmented_pieces(p, nseg) pieces per sequence, piece 0's forward from h0 beside the
+ * summaries of pieces 1..P-2, the in-order scan of those summaries from the state piece 0
+ * ends in, then the chunked forward of pieces 1..P-1 from their scanned states. The state
+ * entering segment s is the state entering piece s * P / nseg. o and h_final equal
+ * gdn_chunk_fwd's up to rounding.
  *   H_in_out [nseg,B,H,K,V] fp32: if non-NULL receives the scanned states; if NULL they
  *   live in the workspace. Workspace: gdn_workspace_bytes(p, nseg). */
 GDN_API gdn_status gdn_segmented_fwd(const gdn_problem* p, int nseg, const void* q, const void* k,
@@ -139,10 +155,10 @@ GDN_API gdn_status gdn_segmented_fwd(const gdn_problem* p, int nseg, const void*
 
 /* gdn_segmented_fwd with stage markers, for timing each kernel from the caller. If
  * stage_events is non-NULL it points to five cudaEvent_t that are recorded on `stream`
- * before the WY-factor launch, before the summary launch, before the scan, before the
- * forward launch and after it (the WY launch is skipped on the CUDA-core path; for
- * nseg == 1 the first four are recorded back to back and the forward stage includes the
- * WY launch). Same results as gdn_segmented_fwd. */
+ * before the WY-factor launch, before the first phase (piece 0's forward and the piece
+ * summaries), before the scan, before the second phase (the forward of pieces 1..P-1) and
+ * after it (the WY launch is skipped on the CUDA-core path; with one piece the scan and the
+ * second phase are empty). Same results as gdn_segmented_fwd. */
 GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q,
                                            const void* k, const void* v, const void* g,
                                            const void* beta, const float* h0, void* o,
@@ -163,9 +179,9 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
  *   array of GDN_NOALLOC_SCRATCH_BYTES in the library's own device memory; every GPU that
  *   loads the library holds it until the process exits. The call allocates nothing.
  *   Limit: problems with gdn_workspace_bytes(p, nseg) > GDN_NOALLOC_SCRATCH_BYTES are
- *   rejected with GDN_ERR_WORKSPACE (at bf16, K = V = 128 that is
- *   B*H*(T/64*16 KiB + nseg*320 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
- *   T = 2048 in 4 segments take 56 MiB).
+ *   rejected with GDN_ERR_WORKSPACE (at bf16, K = V = 128 and P >= 3 pieces that is
+ *   B*H*(T/64*16 KiB + P*192 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
+ *   T = 2048 in 4 segments (4 pieces) take 40 MiB).
  *   device_error: optional (NULL to skip) 8-byte-aligned device pointer to two unsigned
  *   words that receive this call's device error word {code, detail} (see
  *   gdn_check_device_error for the codes) when the call's stream work completes.

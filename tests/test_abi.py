@@ -67,10 +67,17 @@ def test_workspace_bytes_and_status_strings(L):
     # bf16, K = V = 128: the error word and two 8 KiB WY tiles per chunk of each head
     wy = 64 * (32768 // 64) * 16384
     assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256 + wy
+    # without a current device the planner keeps one piece per segment
+    assert L.gdn_segmented_pieces(ctypes.byref(p), 1) == 1
+    assert L.gdn_segmented_pieces(ctypes.byref(p), 4) == 4
+    assert L.gdn_segmented_pieces(ctypes.byref(P(T=100)), 1) == 0
     n4 = L.gdn_workspace_bytes(ctypes.byref(p), 4)
-    # plus M and S for up to 2 sub-segments of each of 4 segments, and H_in for 4 segments,
-    # of 64 heads, fp32
-    assert n4 == 256 + wy + 4 * 64 * 128 * 128 * 4 * (2 + 2 + 1)
+    # plus, for P = 4 pieces of 64 heads in fp32: M and S of the piece summaries and the state
+    # entering each piece
+    assert n4 == 256 + wy + 4 * 64 * 128 * 128 * 4 * (1 + 1 + 1)
+    # two pieces need no summaries, only the state entering each piece
+    n2 = L.gdn_workspace_bytes(ctypes.byref(p), 2)
+    assert n2 == 256 + wy + 2 * 64 * 128 * 128 * 4
     # the CUDA-core shapes need no WY tiles
     assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, in_dtype=0)), 1) == 256
     assert L.gdn_workspace_bytes(ctypes.byref(P(B=2, T=32768, H=32, K=64, V=64)), 1) == 256

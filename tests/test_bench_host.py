@@ -56,19 +56,27 @@ def test_two_rank_max_and_weak_aggregate():
 
 def test_algorithmic_model_matches_hand_count():
     w = synth.WORKLOADS["cp4_b2_h32_t32k"]
-    stages, total = bench.algorithmic(w)
     tok_heads = 2 * 32768 * 32
-    # forward: q,k,v bf16 (3*128*2) + g,beta bf16 (2*2) in, o fp32 (128*4) out
-    assert stages["forward"]["bytes"] >= tok_heads * (772 + 512)
-    # summary reads k, v, g, beta of 3 of the 4 segments
-    assert stages["summary"]["bytes"] >= tok_heads * 3 // 4 * 516
-    t_roof = total["bytes"] / 6791.4e9
-    assert 520e-6 < t_roof < 540e-6
-    # the WY stage: k, g, beta in, two 8 KiB tiles per chunk out; not part of the path total
-    assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 16384
-    assert total["bytes"] == sum(stages[n]["bytes"] for n in ("summary", "scan", "forward"))
-    assert bench.launches_per_step(w) == 4
-    assert bench.launches_per_step(synth.WORKLOADS["tiny_f32_k64_cp4"]) == 3
+    for pieces in (4, 8):
+        stages, total = bench.algorithmic(w, pieces)
+        # every token passes the forward once: piece 0 in phase 1, the rest in phase 2; q,k,v
+        # bf16 (3*128*2) + g,beta bf16 (2*2) in, o fp32 (128*4) out
+        fwd = stages["phase1"]["bytes"] + stages["phase2"]["bytes"]
+        assert fwd >= tok_heads * (772 + 512) + tok_heads * (pieces - 2) // pieces * 516
+        assert stages["phase2"]["bytes"] >= tok_heads * (pieces - 1) // pieces * (772 + 512)
+        # the method's path total does not depend on how the library cuts the sequence:
+        # summaries of 3 of the 4 segments (k, v, g, beta), the scan, the forward
+        t_roof = total["bytes"] / 6791.4e9
+        assert 520e-6 < t_roof < 540e-6
+        assert total["bytes"] >= tok_heads * 3 // 4 * 516 + tok_heads * (772 + 512)
+        # the WY stage: k, g, beta in, two 8 KiB tiles per chunk out
+        assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 16384
+    assert bench.algorithmic(w, 8)[1] == bench.algorithmic(w, 4)[1]
+    # WY, piece 0's forward, the summaries, the scan, the second forward
+    assert bench.launches_per_step(w, 8) == 5
+    # CUDA-core shapes have no WY launch; one piece is a single forward
+    assert bench.launches_per_step(synth.WORKLOADS["tiny_f32_k64_cp4"], 4) == 4
+    assert bench.launches_per_step(synth.WORKLOADS["single_seg_h16_t8k"], 1) == 2
 
 
 @pytest.mark.parametrize("steps", [3])
