@@ -12,73 +12,69 @@
 // a chunk's pair with one bulk copy instead of inverting on its critical path, and the
 // inverse is computed once per chunk rather than once per chain that walks the chunk.
 //
-// One CTA of four warps per chunk: K K^T on mma.sync (bf16, fp32 accumulate; the ten lower
-// 16 x 16 blocks dealt round-robin to the warps), L from the accumulators, the four 16 x 16
-// diagonal blocks of the inverse by forward substitution (one block per warp; rows in
-// registers, shuffles), then block forward substitution on mma.sync (tf32), one column of
-// blocks per warp with no barrier between the block rows. The blocks of L that feed the
-// tensor cores and the inverse itself are kept as tf32 bit patterns in row-padded layouts
+// One CTA of four warps per chunk: the k tile arrives by TMA in the chain kernels' swizzled
+// layout; K K^T goes to tensor memory as two tcgen05 groups (bf16, fp32 accumulate) whose A
+// operand starts at the tile for columns 0..31 (rows in lanes 0..63) and 64 rows before it for
+// columns 32..63 (rows in lanes 64..127), so each warp reads out its own quarter and forms L;
+// then the four 16 x 16 diagonal blocks of the inverse by forward substitution (one block per
+// warp; rows in registers, shuffles), and block forward substitution on mma.sync (tf32), one
+// column of blocks per warp with no barrier between the block rows. The blocks of L that feed
+// the tensor cores and the inverse itself are kept as tf32 bit patterns in row-padded layouts
 // (68 and 72 words per row), so a fragment is two or four shared loads at constant offsets
-// without bank conflicts; the diagonal blocks of L stay fp32 for the substitution. Each
-// block of the inverse is scaled and written to global memory as bf16 as soon as it is
-// final (blocks above the diagonal as zeros). Five CTAs share an SM and hide each other's
-// latencies; the kernel has no waits.
+// without bank conflicts; the diagonal blocks of L stay fp32 for the substitution. Each block
+// of the inverse is scaled and written to global memory as bf16 as soon as it is final (blocks
+// above the diagonal as zeros). Five CTAs share an SM (64 tensor-memory columns each) and hide
+// each other's latencies; the two waits (the tile, K K^T) are bounded.
+#include <cstring>
+
 #include "gdn_tc_common.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kWyThreads = 128;
-constexpr int kWyD = 128;          // K
 constexpr float kWyLog2e = 1.4426950408889634f;
 
 constexpr int LS = 68;   // row pitch (words) of the tf32 off-diagonal blocks of L
 constexpr int XS = 72;   // row pitch (words) of the tf32 inverse X
 constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
 
-// shared-memory map (bytes from a 128-aligned base)
-constexpr uint32_t WY_K = 0;        // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle;
-constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS) once K K^T is in registers
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t WY_K = 8192;     // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle
+constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS) once K K^T is in tensor memory
 constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
 constexpr uint32_t WY_LD = WY_X;    // diagonal blocks of L (fp32, 4 x 16 x DS), dead before X
 constexpr uint32_t WY_Y = 35840;    // per-warp 16 x 8 fp32 scratch of the block rounds
 constexpr uint32_t WY_SC = 37888;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
-constexpr uint32_t WY_END = 38912;
-constexpr uint32_t kWySmem = WY_END + 128;
+constexpr uint32_t WY_BAR = 38912;  // mbarriers (tile, K K^T), tensor-memory address
+constexpr uint32_t WY_END = 38976;
+constexpr uint32_t kWySmem = WY_END + 1024;   // + alignment slack
+constexpr uint32_t kWyTmemCols = 64;
+constexpr uint32_t ID_KK = idesc_bf16(128, 32, false, false);   // K K^T, 32 columns per group
 static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_Y - WY_X, "layout");
 
 struct WyParams {
-    const void* k;
+    CUtensorMap tm_k;
     const void* g;
     const void* beta;
     uint8_t* wy;        // [B*H][T/64][2][8192 B]
     int T, H;
+    DeviceError* err;
+    long long wait_limit;   // SM clock cycles before a wait gives up
 };
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-// D = A B + D, m16n8k16, bf16 in, fp32 accumulate
-__device__ __forceinline__ void mma_m16n8k16_bf16(float* d, const uint32_t* a, const uint32_t* b) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 // 16-byte output chunk `c` (8 bf16 columns) of row `row` of one 64 x 64 output tile
 __device__ __forceinline__ uint4* out_chunk(uint8_t* tile, int row, int c) {
     return reinterpret_cast<uint4*>(tile + sw128(row, c));
 }
 
-__global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const WyParams p) {
+// wait tags recorded in the device error word's detail field
+enum : unsigned { WTAG_TILE = 101, WTAG_KK = 102 };
+
+__global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant__ WyParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 127u) & ~127u;
+    const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     uint32_t* Lt = reinterpret_cast<uint32_t*>(sm + WY_LT);
     uint32_t* X = reinterpret_cast<uint32_t*>(sm + WY_X);
@@ -88,6 +84,9 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const WyParams p) {
     const float* G = sc + 64;
     const float* bet = sc + 128;
     const float* bekr = sc + 192;
+    const uint32_t bar_tile = base + WY_BAR, bar_kk = base + WY_BAR + 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + WY_BAR + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + WY_BAR + 20);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nchunks = p.T / 64;
@@ -99,19 +98,28 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const WyParams p) {
     uint8_t* out_b = p.wy + ch * 16384;   // A diag(beta)
     uint8_t* out_g = out_b + 8192;        // A diag(beta 2^Gx)
 
-    // ---- K tile: 64 rows of 256 bytes, half a row per 16 lanes (coalesced), stored in two
-    //      64-feature halves with the 128-byte swizzle
-    {
-        const uint4* kg = reinterpret_cast<const uint4*>(p.k);
+    // ---- the k tile (two 64-feature halves, 128-byte swizzle) by TMA; 64 columns of tensor
+    //      memory for K K^T
+    if (tid == 0) {
+        mbar_init(bar_tile, 1);
+        mbar_init(bar_kk, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar_tile, 16384u);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int e = tid + kWyThreads * r, row = e >> 4, c16 = e & 15;
-            const uint4 x = __ldg(kg + ((row0 + row) * p.H + h) * (kWyD / 8) + c16);
-            *reinterpret_cast<uint4*>(sm + WY_K + (c16 >> 3) * 8192 + sw128(row, c16 & 7)) = x;
-        }
+        for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(base + WY_K + hf * 8192, &p.tm_k, bar_tile, hf * 64, h, (int)row0);
     }
-    // ---- gates: cumulative sums in log2 units (first warp, two tokens per lane)
     if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         base + WY_BAR + 16),
+                     "r"(kWyTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // ---- gates: cumulative sums in log2 units (two tokens per lane)
+    if (warp == 1) {
         const long long i0 = (row0 + 2 * lane) * p.H + h;
         const float g0 = bf16_at(p.g, i0) * kWyLog2e, g1 = bf16_at(p.g, i0 + p.H) * kWyLog2e;
         const float b0 = bf16_at(p.beta, i0), b1 = bf16_at(p.beta, i0 + p.H);
@@ -131,63 +139,81 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const WyParams p) {
         sc[192 + 2 * lane] = b0 * ex2(excl);        // beta 2^Gx
         sc[192 + 2 * lane + 1] = b1 * ex2(excl + g0);
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    // ---- K K^T on the ten 16 x 16 blocks (I, J), J <= I, dealt round-robin to the warps
-    //      (3, 3, 2, 2 blocks), then L = diag(beta) (2^(Gx_i - G_j) k_i.k_j) below the
-    //      diagonal straight from the accumulators: fp32 for the diagonal blocks, tf32 for
-    //      the rest
-    {
-        float d[3][2][4];
-        int bI[3], bJ[3];
-        const int nb = warp < 2 ? 3 : 2;
+    // ---- K K^T (M = 128, N = 32 per group, bf16, fp32 accumulate): columns 0..31 with A
+    //      starting at the tile (rows in lanes 0..63; lanes 64..127 unused), columns 32..63
+    //      with A starting 64 rows before it (rows in lanes 64..127; lanes 0..63 unused), so
+    //      each of the four warps reads its own quarter out of tensor memory
+    bool issued = false;
+    if (tid == 0 && mbar_wait(bar_tile, 0, abort_flag, p.wait_limit, p.err, WTAG_TILE)) {
+        tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            // block index warp + 4 q in the order (0,0) (1,0) (1,1) (2,0) (2,1) (2,2) (3,0) ...
-            const int idx = warp + 4 * q;
-            const int I = idx < 1 ? 0 : idx < 3 ? 1 : idx < 6 ? 2 : 3;
-            bI[q] = I;
-            bJ[q] = idx - I * (I + 1) / 2;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) d[q][h][0] = d[q][h][1] = d[q][h][2] = d[q][h][3] = 0.f;
+        for (int k16 = 0; k16 < 8; ++k16) {
+            const uint32_t off = (k16 >> 2) * 8192 + (k16 & 3) * 32;
+            mma_ss<ID_KK>(tmem, desc_k(base + WY_K + off), desc_k(base + WY_K + off), k16 > 0);
+            mma_ss<ID_KK>(tmem + 32, desc_k(base + WY_K - 8192 + off),
+                          desc_k(base + WY_K + 4096 + off), k16 > 0);
         }
-        const int lrow = lane & 7, lsel = lane >> 3;
+        mma_commit(bar_kk);
+        issued = true;
+    }
+    __syncwarp();
+
+    // ---- L = diag(beta) (2^(Gx_i - G_j) k_i.k_j) below the diagonal: warp w has rows
+    //      i = 32 (w & 1) + lane and columns 32 (w >> 1) .. + 31 (warp 2's quarter lies above
+    //      the diagonal). fp32 for the diagonal 16 x 16 blocks, tf32 for the rest.
+    {
+        const int i = 32 * (warp & 1) + lane, jb = 32 * (warp >> 1);
+        const bool ok = __shfl_sync(0xffffffffu,
+                                    (int)mbar_wait(bar_kk, 0, abort_flag, p.wait_limit, p.err, WTAG_KK), 0) != 0;
+        if (ok && warp != 2) {
+            tc_fence_after();
+            float kk[32];
+            const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)jb;
+            tmem_ld16(t_row, kk);
+            tmem_ld16(t_row + 16, kk + 16);
+            tmem_wait_ld();
+            const float bi = bet[i], gxi = Gx[i];
+            const int I = i >> 4;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t kt = base + WY_K + (ks >> 2) * 8192;
-            const int c0 = (ks & 3) * 2;
+            for (int j4 = 0; j4 < 32; j4 += 4) {
+                const int j = jb + j4;
+                float v[4];
 #pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                if (q >= nb) break;
-                uint32_t a[4], bb[4];
-                // A: rows 16I + 0-7 / 8-15 at k 0-7, then the same rows at k 8-15
-                ldsm_x4(kt + sw128(16 * bI[q] + lrow + 8 * (lsel & 1), c0 + (lsel >> 1)), a);
-                // B: key rows 16J..+7 at k 0-7 and 8-15 (column tile 0), rows +8 (tile 1)
-                ldsm_x4(kt + sw128(16 * bJ[q] + lrow + 8 * (lsel >> 1), c0 + (lsel & 1)), bb);
-                mma_m16n8k16_bf16(d[q][0], a, bb);
-                mma_m16n8k16_bf16(d[q][1], a, bb + 2);
+                for (int e = 0; e < 4; ++e)
+                    v[e] = (j + e < i) ? bi * ex2(gxi - G[j + e]) * kk[j4 + e] : 0.f;
+                if ((j >> 4) < I) {
+                    *reinterpret_cast<uint4*>(Lt + i * LS + j) =
+                        make_uint4(tf32_bits(v[0]), tf32_bits(v[1]), tf32_bits(v[2]), tf32_bits(v[3]));
+                } else if ((j >> 4) == I) {
+                    float* ld = Ld + I * 16 * DS + (i & 15) * DS + (j & 15);
+                    ld[0] = v[0];
+                    ld[1] = v[1];
+                    ld[2] = v[2];
+                    ld[3] = v[3];
+                }
             }
         }
-        __syncthreads();   // every warp's reads of the k tile are done: L goes over it
-        const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            if (q >= nb) break;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 16 * bI[q] + gq + 8 * (e >> 1);
-                    const int j = 16 * bJ[q] + 8 * h + 2 * tq + (e & 1);
-                    const float v = (j < i) ? bet[i] * ex2(Gx[i] - G[j]) * d[q][h][e] : 0.f;
-                    if (bI[q] == bJ[q])
-                        Ld[bI[q] * 16 * DS + (i & 15) * DS + (j & 15)] = v;   // fp32
-                    else
-                        Lt[i * LS + j] = tf32_bits(v);                        // tensor cores
-                }
-        }
+        tc_fence_before();
     }
     __syncthreads();
+    // tensor memory is read out: release it (after K K^T has retired, should a wait have given
+    // up) and let the tile's copy land before its memory is reused
+    if (tid == 0) {
+        if (issued) mbar_drain(bar_kk, 0, p.wait_limit);
+        if (*abort_flag) mbar_drain(bar_tile, 0, p.wait_limit);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kWyTmemCols)
+                     : "memory");
+    }
 
     // ---- diagonal 16 x 16 blocks of (I + L)^-1, block w by warp w: lane (r, half) owns
     //      columns 8 half .. 8 half + 7 of row r, X[r] = e_r - sum_{m<r} L[r][m] X[m], with
@@ -295,7 +321,16 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     const long long nblk = (long long)c.B * c.H * (c.T / kChunk);
     if (nblk == 0) return cudaSuccess;
     if (nblk >= (1LL << 31)) return cudaErrorInvalidValue;
-    WyParams p{c.k, c.g, c.beta, reinterpret_cast<uint8_t*>(c.wy), c.T, c.H};
+    WyParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_k, c.k, c)) return cudaErrorInvalidValue;
+    p.g = c.g;
+    p.beta = c.beta;
+    p.wy = reinterpret_cast<uint8_t*>(c.wy);
+    p.T = c.T;
+    p.H = c.H;
+    p.err = c.err;
+    p.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
     cudaError_t e = cudaFuncSetAttribute(wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kWySmem);
     if (e != cudaSuccess) return e;
