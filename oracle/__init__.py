@@ -56,12 +56,12 @@ def _load():
     global _lib
     if _lib is None:
         lib = ctypes.CDLL(build())
-        lib.oracle_recurrence.argtypes = [_I] * 6 + [_P] * 9 + [_I, _I]
-        lib.oracle_summary.argtypes = [_I] * 6 + [_P] * 6 + [_I]
+        lib.oracle_recurrence.argtypes = [_I] * 6 + [_P] * 9 + [_I, _I, _I]
+        lib.oracle_summary.argtypes = [_I] * 6 + [_P] * 6 + [_I, _I]
         lib.oracle_compose.argtypes = [_I, _I] + [_P] * 6
         lib.oracle_scan.argtypes = [_I] * 4 + [_P] * 4
-        lib.oracle_chunked_fwd.argtypes = [_I] * 6 + [_P] * 8 + [_I]
-        lib.oracle_chunked_summary.argtypes = [_I] * 7 + [_P] * 6 + [_I]
+        lib.oracle_chunked_fwd.argtypes = [_I] * 6 + [_P] * 8 + [_I, _I]
+        lib.oracle_chunked_summary.argtypes = [_I] * 7 + [_P] * 6 + [_I, _I]
         lib.oracle_num_threads.argtypes = [_I]
         lib.oracle_num_threads.restype = _I
         for fn in ("oracle_recurrence", "oracle_summary", "oracle_compose", "oracle_scan",
@@ -92,10 +92,11 @@ def num_threads(nthreads: int = 0) -> int:
 
 
 def recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
-               nthreads: int = 0, want_o: bool = True):
+               nthreads: int = 0, want_o: bool = True, decay_first: bool = False):
     """Per-token recurrence. Returns (o [B,T,H,V], h_final [B,H,K,V], H_in or None).
 
     If seg_len > 0, H_in [T//seg_len, B, H, K, V] holds the state entering each segment.
+    decay_first reads exp(g_t) H_{t-1} (the other reading) instead of H_{t-1}.
     """
     q, k, v, g, beta, h0 = map(_f32, (q, k, v, g, beta, h0))
     B, T, H, K = k.shape
@@ -105,11 +106,11 @@ def recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
     H_in = np.empty((T // seg_len, B, H, K, V), np.float64) if seg_len > 0 else None
     _load().oracle_recurrence(B, T, H, K, V, seg_len, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), _ptr(H_in), col_block,
-                              nthreads)
+                              nthreads, int(decay_first))
     return o, hf, H_in
 
 
-def summary(k, v, g, beta, nseg: int, nthreads: int = 0):
+def summary(k, v, g, beta, nseg: int, nthreads: int = 0, decay_first: bool = False):
     """Per-segment summaries (M [nseg,B,H,K,K], S [nseg,B,H,K,V]), rank-1 token updates."""
     k, v, g, beta = map(_f32, (k, v, g, beta))
     B, T, H, K = k.shape
@@ -118,7 +119,7 @@ def summary(k, v, g, beta, nseg: int, nthreads: int = 0):
     M = np.empty((nseg, B, H, K, K), np.float64)
     S = np.empty((nseg, B, H, K, V), np.float64)
     _load().oracle_summary(B, T, H, K, V, nseg, _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                           _ptr(M), _ptr(S), nthreads)
+                           _ptr(M), _ptr(S), nthreads, int(decay_first))
     return M, S
 
 
@@ -144,18 +145,21 @@ def scan(M, S, h0=None):
     return H_in
 
 
-def chunked_fwd(q, k, v, g, beta, h0=None, chunk: int = 64, nthreads: int = 0):
+def chunked_fwd(q, k, v, g, beta, h0=None, chunk: int = 64, nthreads: int = 0,
+                decay_first: bool = False):
     q, k, v, g, beta, h0 = map(_f32, (q, k, v, g, beta, h0))
     B, T, H, K = k.shape
     V = v.shape[-1]
     o = np.empty((B, T, H, V), np.float64)
     hf = np.empty((B, H, K, V), np.float64)
     _load().oracle_chunked_fwd(B, T, H, K, V, chunk, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), nthreads)
+                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), nthreads,
+                               int(decay_first))
     return o, hf
 
 
-def chunked_summary(k, v, g, beta, nseg: int, chunk: int = 64, nthreads: int = 0):
+def chunked_summary(k, v, g, beta, nseg: int, chunk: int = 64, nthreads: int = 0,
+                    decay_first: bool = False):
     k, v, g, beta = map(_f32, (k, v, g, beta))
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -163,5 +167,5 @@ def chunked_summary(k, v, g, beta, nseg: int, chunk: int = 64, nthreads: int = 0
     M = np.empty((nseg, B, H, K, K), np.float64)
     S = np.empty((nseg, B, H, K, V), np.float64)
     _load().oracle_chunked_summary(B, T, H, K, V, chunk, nseg, _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(M), _ptr(S), nthreads)
+                                   _ptr(beta), _ptr(M), _ptr(S), nthreads, int(decay_first))
     return M, S

@@ -22,7 +22,11 @@
  *
  * Readings of the pages that this file takes (each listed in the design notes):
  *   - the recurrence reads the un-decayed state H_{t-1} ([RFC] 2.1), so the per-token
- *     transition is exp(g_t) I - beta_t k_t k_t^T;
+ *     transition is exp(g_t) I - beta_t k_t k_t^T; with decay_first set, every function
+ *     takes the other reading ([ART] 08 "What a GDN token does to the state"; [KDA] "KDA
+ *     Chunk Backward -- TPU/Pallas Kernel Design" 1.2): the read sees exp(g_t) H_{t-1}, the
+ *     transition is exp(g_t) (I - beta_t k_t k_t^T), and the chunk form uses the inclusive
+ *     cumulative gate G_i where the default uses the exclusive Gx_i (in P and Kr);
  *   - g is a natural-log decay (exp(g_t)); no query scale;
  *   - segments are contiguous, equal length, in token order; segment 0 starts from h0.
  */
@@ -97,6 +101,7 @@ typedef struct {
     int B, T, H, K, V, seg_len, col_block;
     const float *q, *k, *v, *g, *beta, *h0;
     double *o, *h_final, *H_in;
+    int decay_first;   /* read exp(g_t) H_{t-1} instead of H_{t-1} (the other reading) */
 } rec_ctx;
 
 static void rec_unit(void* vctx, long unit) {
@@ -136,6 +141,7 @@ static void rec_unit(void* vctx, long unit) {
             /* k_t @ H_{t-1}, column cc */
             double read = 0.0;
             for (int kk = 0; kk < K; ++kk) read += kt[kk] * S[(size_t)kk * nc + cc];
+            if (c->decay_first) read *= decay;   /* k_t @ (exp(g_t) H_{t-1}) */
             const double resid = bt * ((double)c->v[row * V + c0 + cc] - read);
             /* H_t = exp(g_t) H_{t-1} + k_t residual_t^T, then o_t = q_t @ H_t */
             double out = 0.0;
@@ -161,9 +167,9 @@ static void rec_unit(void* vctx, long unit) {
 void oracle_recurrence(int B, int T, int H, int K, int V, int seg_len, const float* q,
                        const float* k, const float* v, const float* g, const float* beta,
                        const float* h0, double* o, double* h_final, double* H_in,
-                       int col_block, int nthreads) {
+                       int col_block, int nthreads, int decay_first) {
     rec_ctx c = {B, T, H, K, V, seg_len, col_block > 0 ? col_block : V,
-                 q, k, v, g, beta, h0, o, h_final, H_in};
+                 q, k, v, g, beta, h0, o, h_final, H_in, decay_first};
     const long nblk = (V + c.col_block - 1) / c.col_block;
     run_units(rec_unit, &c, (long)B * H * nblk, nthreads);
 }
@@ -180,6 +186,7 @@ typedef struct {
     int B, T, H, K, V, nseg;
     const float *k, *v, *g, *beta;
     double *M, *S;
+    int decay_first;
 } sum_ctx;
 
 static void sum_unit(void* vctx, long unit) {
@@ -215,10 +222,12 @@ static void sum_unit(void* vctx, long unit) {
         }
         for (int i = 0; i < K; ++i) {
             const double bk = bt * kt[i];
-            for (int j = 0; j < K; ++j) M[(size_t)i * K + j] = decay * M[(size_t)i * K + j] - bk * x[j];
+            /* the read's correction is decayed too when the decayed state is read */
+            const double rk = c->decay_first ? decay * bk : bk;
+            for (int j = 0; j < K; ++j) M[(size_t)i * K + j] = decay * M[(size_t)i * K + j] - rk * x[j];
             for (int j = 0; j < V; ++j)
                 S[(size_t)i * V + j] =
-                    decay * S[(size_t)i * V + j] - bk * y[j] + bk * (double)c->v[row * V + j];
+                    decay * S[(size_t)i * V + j] - rk * y[j] + bk * (double)c->v[row * V + j];
         }
     }
     free(x);
@@ -227,8 +236,9 @@ static void sum_unit(void* vctx, long unit) {
 }
 
 void oracle_summary(int B, int T, int H, int K, int V, int nseg, const float* k, const float* v,
-                    const float* g, const float* beta, double* M, double* S, int nthreads) {
-    sum_ctx c = {B, T, H, K, V, nseg, k, v, g, beta, M, S};
+                    const float* g, const float* beta, double* M, double* S, int nthreads,
+                    int decay_first) {
+    sum_ctx c = {B, T, H, K, V, nseg, k, v, g, beta, M, S, decay_first};
     run_units(sum_unit, &c, (long)B * H * nseg, nthreads);
 }
 
@@ -297,6 +307,7 @@ typedef struct {
     int B, T, H, K, V, chunk, nseg;
     const float *q, *k, *v, *g, *beta, *h0;
     double *o, *h_final, *M, *S;
+    int decay_first;   /* the read sees exp(g_i) times the state: G_i in P and Kr, not Gx_i */
 } chk_ctx;
 
 /* forward substitution for A = (I + L)^{-1}, L strictly lower (n x n, row-major) */
@@ -344,6 +355,7 @@ static void chunk_step(const chk_ctx* c, int b, int h, int t0, int n, double* Hs
         for (int j = 0; j < V; ++j) vd[(size_t)i * V + j] = (double)c->v[row * V + j];
     }
     const double Glast = G[n - 1];
+    const double* Gr = c->decay_first ? G : Gx;   /* cumulative gate of the read side */
     /* L = diag(beta) P */
     for (int i = 0; i < n; ++i)
         for (int j = 0; j < n; ++j) {
@@ -351,7 +363,7 @@ static void chunk_step(const chk_ctx* c, int b, int h, int t0, int n, double* Hs
             if (j < i) {
                 double d = 0.0;
                 for (int l = 0; l < K; ++l) d += kd[(size_t)i * K + l] * kd[(size_t)j * K + l];
-                p = exp(Gx[i] - G[j]) * d;
+                p = exp(Gr[i] - G[j]) * d;
             }
             if (j <= i) {
                 double d = 0.0;
@@ -372,7 +384,7 @@ static void chunk_step(const chk_ctx* c, int b, int h, int t0, int n, double* Hs
         for (int j = 0; j < K; ++j) {
             double a = 0.0;
             for (int l = 0; l <= i; ++l)
-                a += A[(size_t)i * n + l] * bt[l] * exp(Gx[l]) * kd[(size_t)l * K + j];
+                a += A[(size_t)i * n + l] * bt[l] * exp(Gr[l]) * kd[(size_t)l * K + j];
             W[(size_t)i * K + j] = a;
         }
     }
@@ -450,8 +462,8 @@ static void chk_fwd_unit(void* vctx, long unit) {
 /* Chunked forward from h0 over all T tokens (the last chunk may be short). */
 void oracle_chunked_fwd(int B, int T, int H, int K, int V, int chunk, const float* q, const float* k,
                         const float* v, const float* g, const float* beta, const float* h0,
-                        double* o, double* h_final, int nthreads) {
-    chk_ctx c = {B, T, H, K, V, chunk, 1, q, k, v, g, beta, h0, o, h_final, NULL, NULL};
+                        double* o, double* h_final, int nthreads, int decay_first) {
+    chk_ctx c = {B, T, H, K, V, chunk, 1, q, k, v, g, beta, h0, o, h_final, NULL, NULL, decay_first};
     run_units(chk_fwd_unit, &c, (long)B * H, nthreads);
 }
 
@@ -493,7 +505,7 @@ static void chk_sum_unit(void* vctx, long unit) {
 /* Per-segment summaries built from the chunk summaries (M_n, E_n) composed in order. */
 void oracle_chunked_summary(int B, int T, int H, int K, int V, int chunk, int nseg, const float* k,
                             const float* v, const float* g, const float* beta, double* M,
-                            double* S, int nthreads) {
-    chk_ctx c = {B, T, H, K, V, chunk, nseg, NULL, k, v, g, beta, NULL, NULL, NULL, M, S};
+                            double* S, int nthreads, int decay_first) {
+    chk_ctx c = {B, T, H, K, V, chunk, nseg, NULL, k, v, g, beta, NULL, NULL, NULL, M, S, decay_first};
     run_units(chk_sum_unit, &c, (long)B * H * nseg, nthreads);
 }

@@ -37,10 +37,11 @@ def rand_inputs(B, T, H, K, V, seed, g_mu=2.0, g_sd=1.0, beta_mu=0.0, beta_sd=1.
 # hand-worked example (tests/golden): pins orientation (k@H, q@H), the un-decayed read,
 # and the summary's M and S
 # --------------------------------------------------------------------------------------
-@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("case", [0, 1, 2])
 def test_hand_worked_example(case):
     d = json.load(open(GOLDEN))
     c = d["cases"][case]
+    df = c.get("reading") == "decay_first"
     tok = d["tokens"]
     q = np.array(tok["q"], np.float32).reshape(1, 3, 1, 2)
     k = np.array(tok["k"], np.float32).reshape(1, 3, 1, 2)
@@ -49,17 +50,17 @@ def test_hand_worked_example(case):
     g = np.array(c["g"], np.float32).reshape(1, 3, 1)
     h0 = np.array(c["h0"], np.float32).reshape(1, 1, 2, 2)
     tol = c["tol"]
-    o, hf, _ = oracle.recurrence(q, k, v, g, beta, h0)
+    o, hf, _ = oracle.recurrence(q, k, v, g, beta, h0, decay_first=df)
     assert np.max(np.abs(o[0, :, 0] - np.array(c["o"]))) <= tol
     assert np.max(np.abs(hf[0, 0] - np.array(c["h_final"]))) <= tol
-    M, S = oracle.summary(k, v, g, beta, nseg=1)
+    M, S = oracle.summary(k, v, g, beta, nseg=1, decay_first=df)
     assert np.max(np.abs(M[0, 0, 0] - np.array(c["M"]))) <= tol
     assert np.max(np.abs(S[0, 0, 0] - np.array(c["S"]))) <= tol
     for chunk in (1, 2, 3):
-        oc, hc = oracle.chunked_fwd(q, k, v, g, beta, h0, chunk=chunk)
+        oc, hc = oracle.chunked_fwd(q, k, v, g, beta, h0, chunk=chunk, decay_first=df)
         assert np.max(np.abs(oc[0, :, 0] - np.array(c["o"]))) <= 10 * tol
         assert np.max(np.abs(hc[0, 0] - np.array(c["h_final"]))) <= 10 * tol
-        Mc, Sc = oracle.chunked_summary(k, v, g, beta, nseg=1, chunk=chunk)
+        Mc, Sc = oracle.chunked_summary(k, v, g, beta, nseg=1, chunk=chunk, decay_first=df)
         assert np.max(np.abs(Mc[0, 0, 0] - np.array(c["M"]))) <= 10 * tol
         assert np.max(np.abs(Sc[0, 0, 0] - np.array(c["S"]))) <= 10 * tol
 
@@ -75,6 +76,22 @@ def test_chunked_equals_per_token(K, V, chunk, T):
     oc, hc = oracle.chunked_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], chunk=chunk)
     assert rel_err(oc, o) <= 1e-12
     assert rel_err(hc, hf) <= 1e-12
+
+
+@pytest.mark.parametrize("K,V,chunk,T", [(4, 4, 1, 32), (8, 4, 4, 64), (16, 8, 64, 100),
+                                         (64, 64, 64, 256)])
+def test_chunked_equals_per_token_decayed_read(K, V, chunk, T):
+    # the other reading of the token update: G_i replaces Gx_i in P and Kr
+    x = rand_inputs(2, T, 2, K, V, seed=2000 + K * 7 + V + chunk, g_mu=0.5)
+    o, hf, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                 decay_first=True)
+    oc, hc = oracle.chunked_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], chunk=chunk,
+                                decay_first=True)
+    assert rel_err(oc, o) <= 1e-12
+    assert rel_err(hc, hf) <= 1e-12
+    # and the two readings really differ on these inputs
+    o0, _, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    assert rel_err(o0, o) > 1e-3
 
 
 def test_chunked_equals_per_token_wide_gates():
@@ -93,11 +110,15 @@ def test_chunked_equals_per_token_wide_gates():
 #     M = T_L ... T_1,  T_t = exp(g_t) I - beta_t k_t k_t^T
 #     S = sum_t (T_L ... T_{t+1}) beta_t k_t v_t^T
 # --------------------------------------------------------------------------------------
-def brute_summary(k, v, g, beta):
-    """k [L,K], v [L,V], g [L], beta [L] (float64) -> (M, S) by explicit matrices."""
+def brute_summary(k, v, g, beta, decay_first=False):
+    """k [L,K], v [L,V], g [L], beta [L] (float64) -> (M, S) by explicit matrices. With
+    decay_first the transitions are exp(g_t) (I - beta_t k_t k_t^T)."""
     L, K = k.shape
     V = v.shape[1]
-    Ts = [np.exp(g[t]) * np.eye(K) - beta[t] * np.outer(k[t], k[t]) for t in range(L)]
+    if decay_first:
+        Ts = [np.exp(g[t]) * (np.eye(K) - beta[t] * np.outer(k[t], k[t])) for t in range(L)]
+    else:
+        Ts = [np.exp(g[t]) * np.eye(K) - beta[t] * np.outer(k[t], k[t]) for t in range(L)]
     M = np.eye(K)
     for t in range(L):
         M = Ts[t] @ M
@@ -110,17 +131,19 @@ def brute_summary(k, v, g, beta):
     return M, S
 
 
+@pytest.mark.parametrize("decay_first", [False, True])
 @pytest.mark.parametrize("K,V,L", [(3, 2, 5), (8, 8, 16), (5, 7, 12), (8, 3, 1)])
-def test_summary_brute_force(K, V, L):
+def test_summary_brute_force(K, V, L, decay_first):
     x = rand_inputs(1, L, 1, K, V, seed=300 + K + V + L, g_mu=1.0)
     k, v = x["k"][0, :, 0].astype(np.float64), x["v"][0, :, 0].astype(np.float64)
     g, beta = x["g"][0, :, 0].astype(np.float64), x["beta"][0, :, 0].astype(np.float64)
-    Mb, Sb = brute_summary(k, v, g, beta)
-    M, S = oracle.summary(x["k"], x["v"], x["g"], x["beta"], nseg=1)
+    Mb, Sb = brute_summary(k, v, g, beta, decay_first)
+    M, S = oracle.summary(x["k"], x["v"], x["g"], x["beta"], nseg=1, decay_first=decay_first)
     assert np.max(np.abs(M[0, 0, 0] - Mb)) <= 1e-13
     assert np.max(np.abs(S[0, 0, 0] - Sb)) <= 1e-13 * max(1.0, np.max(np.abs(Sb)))
     for chunk in (1, 4, 64):
-        Mc, Sc = oracle.chunked_summary(x["k"], x["v"], x["g"], x["beta"], nseg=1, chunk=chunk)
+        Mc, Sc = oracle.chunked_summary(x["k"], x["v"], x["g"], x["beta"], nseg=1, chunk=chunk,
+                                        decay_first=decay_first)
         assert np.max(np.abs(Mc[0, 0, 0] - Mb)) <= 1e-12
         assert np.max(np.abs(Sc[0, 0, 0] - Sb)) <= 1e-12 * max(1.0, np.max(np.abs(Sb)))
 
