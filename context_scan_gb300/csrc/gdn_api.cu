@@ -92,6 +92,7 @@ gdn_status check_problem(const gdn_problem* p, int nseg) {
     if (p->B < 1 || p->H < 1 || p->T < 0) return GDN_ERR_INVALID_ARG;
     if (nseg < 1) return GDN_ERR_INVALID_ARG;
     if (p->chunk != gdn::kChunk) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (p->decay_first != 0 && p->decay_first != 1) return GDN_ERR_INVALID_ARG;
     if (p->K != p->V || (p->K != 64 && p->K != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
     if ((p->in_dtype != GDN_DTYPE_F32 && p->in_dtype != GDN_DTYPE_BF16) ||
         (p->out_dtype != GDN_DTYPE_F32 && p->out_dtype != GDN_DTYPE_BF16))
@@ -135,6 +136,7 @@ ChainParams base_params(const gdn_problem* p, void* ws) {
     c.V = p->V;
     c.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
     c.out_bf16 = p->out_dtype == GDN_DTYPE_BF16;
+    c.decay_first = p->decay_first;
     c.err = reinterpret_cast<gdn::DeviceError*>(ws);
     return c;
 }

@@ -47,6 +47,7 @@ struct ChainParams {
     long long h_out_seg_stride;
     int in_bf16;
     int out_bf16;
+    int decay_first;   // the read sees the decayed state (inclusive gate on the read side)
     // launch as the programmatic dependent of the preceding grid in the stream (the kernel
     // then finishes only after that grid has)
     int launch_dependent;

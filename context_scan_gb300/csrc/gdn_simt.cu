@@ -142,8 +142,9 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
             const float excl = s - (a0 + a1);
             gam[2 * tid] = excl + a0;
             gam[2 * tid + 1] = excl + a0 + a1;
-            gx[2 * tid] = excl;              // Gx_i = G_i - g_i
-            gx[2 * tid + 1] = excl + a0;
+            // read-side gate: Gx_i = G_i - g_i, or G_i when the read sees the decayed state
+            gx[2 * tid] = p.decay_first ? excl + a0 : excl;
+            gx[2 * tid + 1] = p.decay_first ? excl + a0 + a1 : excl + a0;
         }
         __syncthreads();
         const float glast = gam[63];

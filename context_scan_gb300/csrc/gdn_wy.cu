@@ -59,6 +59,7 @@ struct WyParams {
     const void* beta;
     uint8_t* wy;        // [B*H][T/64][2][8192 B]
     int T, H;
+    int decay_first;   // read-side gate G (decayed read) instead of Gx
     DeviceError* err;
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
@@ -136,8 +137,9 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
         sc[64 + 2 * lane + 1] = excl + g0 + g1;
         sc[128 + 2 * lane] = b0;           // beta
         sc[128 + 2 * lane + 1] = b1;
-        sc[192 + 2 * lane] = b0 * ex2(excl);        // beta 2^Gx
-        sc[192 + 2 * lane + 1] = b1 * ex2(excl + g0);
+        // beta 2^Gx (beta 2^G when the read sees the decayed state)
+        sc[192 + 2 * lane] = b0 * ex2(p.decay_first ? excl + g0 : excl);
+        sc[192 + 2 * lane + 1] = b1 * ex2(p.decay_first ? excl + g0 + g1 : excl + g0);
     }
     tc_fence_before();
     __syncthreads();
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
             tmem_ld16(t_row, kk);
             tmem_ld16(t_row + 16, kk + 16);
             tmem_wait_ld();
-            const float bi = bet[i], gxi = Gx[i];
+            const float bi = bet[i], gxi = p.decay_first ? G[i] : Gx[i];   // read-side gate
             const int I = i >> 4;
 #pragma unroll
             for (int j4 = 0; j4 < 32; j4 += 4) {
@@ -329,6 +331,7 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     p.wy = reinterpret_cast<uint8_t*>(c.wy);
     p.T = c.T;
     p.H = c.H;
+    p.decay_first = c.decay_first;
     p.err = c.err;
     p.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
     cudaError_t e = cudaFuncSetAttribute(wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

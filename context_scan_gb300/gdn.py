@@ -33,7 +33,8 @@ class GdnError(RuntimeError):
 class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("K", ctypes.c_int), ("V", ctypes.c_int), ("chunk", ctypes.c_int),
-                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("decay_first", ctypes.c_int)]
 
 
 _lib = None
@@ -79,11 +80,11 @@ def _dtype_code(t) -> int:
     return 99   # the library rejects it with GDN_ERR_UNSUPPORTED_DTYPE
 
 
-def problem(q_or_k, v, o=None, chunk: int = 64) -> Problem:
+def problem(q_or_k, v, o=None, chunk: int = 64, decay_first: bool = False) -> Problem:
     B, T, H, K = q_or_k.shape
     V = v.shape[-1]
     out = GDN_DTYPE_F32 if o is None else _dtype_code(o)
-    return Problem(B, T, H, K, V, chunk, _dtype_code(q_or_k), out)
+    return Problem(B, T, H, K, V, chunk, _dtype_code(q_or_k), out, int(decay_first))
 
 
 def _ptr(t):

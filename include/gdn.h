@@ -87,6 +87,12 @@ typedef struct {
     int chunk;           /* tokens per chunk; must be 64 */
     gdn_dtype in_dtype;  /* storage type of q, k, v, g, beta */
     gdn_dtype out_dtype; /* storage type of o */
+    /* 0: the read sees the state before this token's decay, r_t = beta_t (v_t - k_t@H_{t-1})
+     *    (RFC section 2.1; transition exp(g_t) I - beta_t k_t k_t^T).
+     * 1: the read sees the decayed state, r_t = beta_t (v_t - k_t@(exp(g_t) H_{t-1})) (ART
+     *    section 08 "What a GDN token does to the state"; KDA design section 1.2; transition
+     *    exp(g_t) (I - beta_t k_t k_t^T)). Every call below follows the flag. */
+    int decay_first;
 } gdn_problem;
 
 /* Bytes of workspace the calls below need for this problem split into nseg segments

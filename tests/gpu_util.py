@@ -36,14 +36,14 @@ def upload(x, w, device="cuda"):
     return d
 
 
-def run_segmented(w, d, nseg=None, out_dtype=torch.float32, want_hin=True):
+def run_segmented(w, d, nseg=None, out_dtype=torch.float32, want_hin=True, decay_first=False):
     nseg = nseg or w.nseg
     B, T, H, K = d["k"].shape
     V = d["v"].shape[-1]
     o = torch.empty((B, T, H, V), dtype=out_dtype, device="cuda")
     hf = torch.empty((B, H, K, V), dtype=torch.float32, device="cuda")
     hin = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device="cuda") if want_hin else None
-    prob = gdn.problem(d["k"], d["v"], o)
+    prob = gdn.problem(d["k"], d["v"], o, decay_first=decay_first)
     ws = gdn.alloc_workspace(prob, nseg)
     gdn.gdn_segmented_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf, nseg, ws,
                           H_in=hin, prob=prob)
@@ -53,13 +53,13 @@ def run_segmented(w, d, nseg=None, out_dtype=torch.float32, want_hin=True):
     return o, hf, hin
 
 
-def run_summary(w, d, nseg=None):
+def run_summary(w, d, nseg=None, decay_first=False):
     nseg = nseg or w.nseg
     B, T, H, K = d["k"].shape
     V = d["v"].shape[-1]
     M = torch.empty((nseg, B, H, K, K), dtype=torch.float32, device="cuda")
     S = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device="cuda")
-    prob = gdn.problem(d["k"], d["v"])
+    prob = gdn.problem(d["k"], d["v"], decay_first=decay_first)
     ws = gdn.alloc_workspace(prob, 1)
     gdn.gdn_segment_summary(d["k"], d["v"], d["g"], d["beta"], M, S, nseg, ws, prob=prob)
     torch.cuda.synchronize()
@@ -82,6 +82,7 @@ def head_slice(x, b, h):
     return out
 
 
-def oracle_ref(x, seg_len, nthreads=0, col_block=0):
+def oracle_ref(x, seg_len, nthreads=0, col_block=0, decay_first=False):
     return oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
-                             seg_len=seg_len, nthreads=nthreads, col_block=col_block)
+                             seg_len=seg_len, nthreads=nthreads, col_block=col_block,
+                             decay_first=decay_first)

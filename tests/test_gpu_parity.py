@@ -51,6 +51,32 @@ def test_segmented_matches_oracle(name):
     assert e_in <= tol, (name, "H_in", e_in)
 
 
+@pytest.mark.parametrize("name", ["tiny_f32_k64_cp4", "cp4_small", "single_seg_small",
+                                  "slow_decay_h4_t1k_cp16", "bf16_k64_cp4"])
+def test_decayed_read_matches_oracle(name):
+    # the other reading of the token update (the read sees the decayed state): through the
+    # WY tiles on the tensor-core path and the in-chain solve on the CUDA-core path
+    w = SMALL[name]
+    x = synth.make_inputs(w)
+    o_ref, hf_ref, hin_ref = oracle_ref(x, w.seg_len, decay_first=True)
+    d = upload(x, w)
+    o, hf, hin = run_segmented(w, d, decay_first=True)
+    tol = tol_for(w)
+    assert rel_err(np64(o), o_ref) <= tol, ("o", rel_err(np64(o), o_ref))
+    assert rel_err(np64(hf), hf_ref) <= tol, ("h_final", rel_err(np64(hf), hf_ref))
+    assert rel_err(np64(hin), hin_ref) <= tol, ("H_in", rel_err(np64(hin), hin_ref))
+    # the flag is honoured: the result is much closer to this reading than to the default one
+    o_def, _, _ = oracle_ref(x, w.seg_len)
+    assert rel_err(np64(o), o_def) > 2 * rel_err(np64(o), o_ref)
+    if w.nseg > 1:
+        M_ref, S_ref = oracle.summary(x["k"], x["v"], x["g"], x["beta"], w.nseg, decay_first=True)
+        M, S = run_summary(w, d, decay_first=True)
+        M, S = np64(M), np64(S)
+        m_scale = max(float(np.sqrt(np.mean(M_ref ** 2))), 1e-12)
+        assert float(np.max(np.abs(M - M_ref))) / m_scale <= tol
+        assert rel_err(S, S_ref) <= tol
+
+
 @pytest.mark.parametrize("name", ["tiny_f32_k64_cp4", "cp4_small", "slow_decay_h4_t1k_cp16",
                                   "bf16_k64_cp4"])
 def test_summary_matches_oracle(name):
