@@ -249,6 +249,43 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
     return from_cuda(mark(events, 4, s));
 }
 
+
+// ---- varlen: [header | WY tiles (tcgen05 shapes), [H][T/64 + nseq] | checked cu_seqlens |
+//      cu_chunks], each region 256-byte aligned. T/64 + nseq bounds the chunks of any split of
+//      T tokens into nseq sequences, so the layout needs no host copy of the lengths.
+struct VarlenLayout {
+    size_t off_wy, off_cu, off_cc, total;
+    int chunk_bound;
+};
+
+VarlenLayout varlen_layout(const gdn_problem& p, int nseq) {
+    VarlenLayout w{};
+    w.chunk_bound = p.T / gdn::kChunk + nseq;
+    w.off_wy = kHeaderBytes;
+    const size_t wy_bytes = tc_shape(p) ? (size_t)p.H * (size_t)w.chunk_bound * 16384u : 0;
+    w.off_cu = w.off_wy + round_up(wy_bytes);
+    w.off_cc = w.off_cu + round_up(sizeof(int) * ((size_t)nseq + 1));
+    w.total = w.off_cc + round_up(sizeof(int) * ((size_t)nseq + 1));
+    return w;
+}
+
+gdn_status check_varlen(const gdn_problem* p, int nseq) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    if (p->B != 1 || p->H < 1 || p->T < 0 || nseq < 1) return GDN_ERR_INVALID_ARG;
+    if (p->chunk != gdn::kChunk) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (p->decay_first != 0 && p->decay_first != 1) return GDN_ERR_INVALID_ARG;
+    if (p->K != p->V || (p->K != 64 && p->K != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if ((p->in_dtype != GDN_DTYPE_F32 && p->in_dtype != GDN_DTYPE_BF16) ||
+        (p->out_dtype != GDN_DTYPE_F32 && p->out_dtype != GDN_DTYPE_BF16))
+        return GDN_ERR_UNSUPPORTED_DTYPE;
+    if ((long long)p->T * p->H * p->K >= (1LL << 40)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)p->T + 64LL * ((long long)nseq + 1) >= (1LL << 31)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)nseq * p->H >= (1LL << 31) ||
+        (long long)p->H * (p->T / gdn::kChunk + nseq) >= (1LL << 31))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -347,6 +384,57 @@ gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const void* q
                          reinterpret_cast<cudaStream_t>(stream), stage_events);
 }
 
+size_t gdn_varlen_workspace_bytes(const gdn_problem* p, int nseq) {
+    if (check_varlen(p, nseq) != GDN_OK) return 0;
+    return varlen_layout(*p, nseq).total;
+}
+
+gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_seqlens, const void* q,
+                          const void* k, const void* v, const void* g, const void* beta,
+                          const float* h0, void* o, float* h_final, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    gdn_status st = check_varlen(p, nseq);
+    if (st != GDN_OK) return st;
+    if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (p->T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    const VarlenLayout w = varlen_layout(*p, nseq);
+    if (!workspace || workspace_bytes < w.total) return GDN_ERR_WORKSPACE;
+    for (const void* ptr : {(const void*)workspace, (const void*)cu_seqlens, q, k, v, g, beta,
+                            (const void*)h0, (const void*)o, (const void*)h_final})
+        if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
+    if ((st = check_device()) != GDN_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* wsb = reinterpret_cast<char*>(workspace);
+    int* cu = reinterpret_cast<int*>(wsb + w.off_cu);
+    int* cc = reinterpret_cast<int*>(wsb + w.off_cc);
+    // the chains read the checked copy of the lengths, never the caller's array
+    if (gdn::launch_varlen_meta(cu_seqlens, nseq, p->T, cu, cc,
+                                reinterpret_cast<gdn::DeviceError*>(workspace), s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    ChainParams c = base_params(p, workspace);
+    c.B = nseq;   // one chain per (sequence, head)
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.g = g;
+    c.beta = beta;
+    c.o = o;
+    c.h_start = h0;
+    c.h_final = h_final;
+    c.seg_first = 0;
+    c.nseg_run = 1;
+    c.nseg_total = 1;
+    c.cu_seqlens = cu;
+    c.cu_chunks = cc;
+    c.total_chunks = w.chunk_bound;
+    c.wy = wsb + w.off_wy;
+    if (use_tc(c) && p->T >= gdn::kChunk) {   // (a tensor map box holds 64 tokens)
+        if (gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
+        return from_cuda(gdn::launch_tc_forward(c, s));
+    }
+    return from_cuda(gdn::launch_simt_forward(c, s));
+}
+
 const char* gdn_status_string(gdn_status s) {
     switch (s) {
         case GDN_OK: return "ok";
@@ -376,7 +464,9 @@ gdn_status gdn_check_device_error(void* workspace, void* stream, unsigned* detai
     if (cudaMemsetAsync(workspace, 0, sizeof(host), s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    return host.code == GDN_ERR_TIMEOUT ? GDN_ERR_TIMEOUT : GDN_ERR_CUDA;
+    if (host.code == GDN_ERR_TIMEOUT || host.code == GDN_ERR_INVALID_ARG)
+        return static_cast<gdn_status>(host.code);
+    return GDN_ERR_CUDA;
 }
 
 }  // extern "C"

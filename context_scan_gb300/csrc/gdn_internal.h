@@ -45,6 +45,13 @@ struct ChainParams {
     // h_out + (s + 1) * h_out_seg_stride + (b*H + h)*K*V (the state entering segment s + 1)
     float* h_out;
     long long h_out_seg_stride;
+    // varlen (null otherwise): the batch is packed, sequence b holds tokens cu_seqlens[b] ..
+    // cu_seqlens[b+1]-1 (B = number of sequences, T = total tokens, one segment); its chunks
+    // are numbered from cu_chunks[b] (the last one may be partial) and the WY tiles are
+    // [H][total_chunks], total_chunks = T/64 + B bounding the chunks of any split
+    const int* cu_seqlens;
+    const int* cu_chunks;
+    int total_chunks;
     int in_bf16;
     int out_bf16;
     int decay_first;   // the read sees the decayed state (inclusive gate on the read side)
@@ -67,9 +74,17 @@ cudaError_t launch_scan(const float* M, const float* S, const float* h_first, fl
                         float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
                         int K, int V, cudaStream_t s);
 
+// varlen metadata: checks the caller's cu_seqlens [nseq+1] (0 first, T last, non-decreasing)
+// and writes a checked copy to cu_out and cu_chunks[s] = sum over sequences before s of
+// ceil(length / 64) (s = 0..nseq). A bad array is recorded in the error word
+// (GDN_ERR_INVALID_ARG) and both outputs become all zeros (every sequence empty), so the
+// kernels that read them stay inside the buffers.
+cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
+                               DeviceError* err, cudaStream_t s);
+
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);
-cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all T/64 chunks of every (b, h)
+cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all chunks of every (b, h)
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);
 

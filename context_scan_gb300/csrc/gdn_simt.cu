@@ -103,32 +103,41 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
         Hs[e] = x;
     }
 
-    const int t_begin = seg * p.seg_len;
-    const int n_chunks = p.seg_len / kChunk;
+    // tokens of this chain: a segment of the fixed-length batch, or a whole varlen sequence
+    // whose last chunk may be partial (its padding tokens load as zeros with g = beta = 0,
+    // which leaves the state untouched, and their outputs are not stored)
+    const long long row_base = p.cu_seqlens ? (long long)p.cu_seqlens[b]
+                                            : (long long)b * T + (long long)seg * p.seg_len;
+    const int seq_tokens = p.cu_seqlens ? p.cu_seqlens[b + 1] - p.cu_seqlens[b] : p.seg_len;
+    const int n_chunks = (seq_tokens + kChunk - 1) / kChunk;
     for (int ch = 0; ch < n_chunks; ++ch) {
-        const int t0 = t_begin + ch * kChunk;
+        const int t0 = ch * kChunk;   // first token of the chunk inside the chain
         // ---- (1) load the chunk
         for (int e = tid; e < 64 * KD; e += kThreads) {
             const int i = e / KD, l = e % KD;
-            const long long row = ((long long)b * T + t0 + i) * H + h;
-            ks[i * KP + l] = load_in(p.k, row * KD + l, p.in_bf16);
-            if (!SUMMARY) qs[i * KP + l] = load_in(p.q, row * KD + l, p.in_bf16);
+            const long long row = (row_base + t0 + i) * H + h;
+            const bool in = t0 + i < seq_tokens;
+            ks[i * KP + l] = in ? load_in(p.k, row * KD + l, p.in_bf16) : 0.f;
+            if (!SUMMARY) qs[i * KP + l] = in ? load_in(p.q, row * KD + l, p.in_bf16) : 0.f;
         }
         for (int e = tid; e < 64 * CT; e += kThreads) {
             const int i = e / CT, c = e % CT;
-            const long long row = ((long long)b * T + t0 + i) * H + h;
+            const long long row = (row_base + t0 + i) * H + h;
             const int gc = c0 + c;
-            float x;
-            if (SUMMARY)
-                x = (gc < KD) ? 0.f : load_in(p.v, row * V + (gc - KD), p.in_bf16);
-            else
-                x = load_in(p.v, row * V + gc, p.in_bf16);
+            float x = 0.f;
+            if (t0 + i < seq_tokens) {
+                if (SUMMARY)
+                    x = (gc < KD) ? 0.f : load_in(p.v, row * V + (gc - KD), p.in_bf16);
+                else
+                    x = load_in(p.v, row * V + gc, p.in_bf16);
+            }
             vs[e] = x;
         }
         if (tid < 64) {
-            const long long row = ((long long)b * T + t0 + tid) * H + h;
-            gx[tid] = load_in(p.g, row, p.in_bf16);   // raw gate for now
-            bet[tid] = load_in(p.beta, row, p.in_bf16);
+            const long long row = (row_base + t0 + tid) * H + h;
+            const bool in = t0 + tid < seq_tokens;
+            gx[tid] = in ? load_in(p.g, row, p.in_bf16) : 0.f;   // raw gate for now
+            bet[tid] = in ? load_in(p.beta, row, p.in_bf16) : 0.f;
         }
         __syncthreads();
         // ---- (2) gate cumsum inside the chunk (one warp; two gates per lane)
@@ -243,8 +252,8 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
                 for (int l = 0; l < KD; ++l) a = fmaf(qs[i * KP + l], Hs[l * CT + c], a);
                 float bsum = 0.f;
                 for (int j = 0; j <= i; ++j) bsum = fmaf(Cs[i * LP + j], Rs[j * CT + c], bsum);
-                const long long row = ((long long)b * T + t0 + i) * H + h;
-                store_out(p.o, row * V + c0 + c, fmaf(eq[i], a, bsum), p.out_bf16);
+                const long long row = (row_base + t0 + i) * H + h;
+                if (t0 + i < seq_tokens) store_out(p.o, row * V + c0 + c, fmaf(eq[i], a, bsum), p.out_bf16);
             }
             __syncthreads();
         }
@@ -419,6 +428,48 @@ cudaError_t launch_scan_k(const float* M, const float* S, const float* h_first, 
                                                 BH, V);
     return cudaGetLastError();
 }
+
+// Varlen metadata in one block: each thread checks and sums a contiguous run of sequences,
+// a block scan turns the per-thread chunk counts into the run's first chunk index.
+constexpr int kMetaThreads = 256;
+constexpr unsigned kTagVarlen = 201;   // detail word of a rejected cu_seqlens
+
+__global__ void __launch_bounds__(kMetaThreads) varlen_meta_kernel(
+    const int* __restrict__ cu_in, int nseq, int T, int* __restrict__ cu_out,
+    int* __restrict__ cu_chunks, DeviceError* err) {
+    __shared__ long long part[kMetaThreads];
+    const int t = threadIdx.x;
+    const int per = (nseq + kMetaThreads - 1) / kMetaThreads;
+    const int s0 = min(nseq, t * per), s1 = min(nseq, s0 + per);
+    bool bad = t == 0 && (cu_in[0] != 0 || cu_in[nseq] != T);
+    long long acc = 0;
+    for (int s = s0; s < s1; ++s) {
+        const long long len = (long long)cu_in[s + 1] - cu_in[s];
+        bad |= len < 0;
+        acc += (len + kChunk - 1) / kChunk;
+    }
+    bad = __syncthreads_or(bad);
+    part[t] = acc;
+    __syncthreads();
+    for (int off = 1; off < kMetaThreads; off <<= 1) {   // inclusive scan
+        const long long x = t >= off ? part[t - off] : 0;
+        __syncthreads();
+        part[t] += x;
+        __syncthreads();
+    }
+    long long run = part[t] - acc;
+    for (int s = s0; s < s1; ++s) {
+        cu_out[s] = bad ? 0 : cu_in[s];
+        cu_chunks[s] = bad ? 0 : (int)run;
+        run += ((long long)cu_in[s + 1] - cu_in[s] + kChunk - 1) / kChunk;
+    }
+    if (t == 0) {
+        cu_out[nseq] = bad ? 0 : T;
+        cu_chunks[nseq] = bad ? 0 : (int)part[kMetaThreads - 1];
+        if (bad && err && atomicCAS(&err->code, 0u, (unsigned)GDN_ERR_INVALID_ARG) == 0u)
+            atomicExch(&err->detail, kTagVarlen);
+    }
+}
 }  // namespace
 
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s) {
@@ -436,6 +487,13 @@ cudaError_t launch_scan(const float* M, const float* S, const float* h_first, fl
     if (K == 128) return launch_scan_k<128>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     if (K == 64) return launch_scan_k<64>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
+                               DeviceError* err, cudaStream_t s) {
+    if (!cu_in || !cu_out || !cu_chunks || nseq < 1) return cudaErrorInvalidValue;
+    varlen_meta_kernel<<<1, kMetaThreads, 0, s>>>(cu_in, nseq, T, cu_out, cu_chunks, err);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -334,12 +334,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [B*T, H, 128] bf16 viewed as a 3-d tensor; box = 64 features x 1 head x 64 tokens
+// [B*T, H, 128] bf16 (a packed varlen batch: [T, H, 128]) viewed as a 3-d tensor; box = 64
+// features x 1 head x 64 tokens
 bool make_map(CUtensorMap* m, const void* ptr, const ChainParams& c) {
     constexpr int kD = 128;
     auto fn = encode_fn();
     if (!fn || !ptr) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)c.H, (cuuint64_t)c.B * (cuuint64_t)c.T};
+    const cuuint64_t rows = c.cu_seqlens ? (cuuint64_t)c.T : (cuuint64_t)c.B * (cuuint64_t)c.T;
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)c.H, rows};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)c.H * kD * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};

@@ -60,6 +60,9 @@ struct WyParams {
     uint8_t* wy;        // [B*H][T/64][2][8192 B]
     int T, H;
     int decay_first;   // read-side gate G (decayed read) instead of Gx
+    const int* cu_seqlens;   // varlen: packed sequences (null for the fixed-length batch)
+    const int* cu_chunks;
+    int nseq, total_chunks;   // varlen: total_chunks bounds the chunks (T/64 + nseq)
     DeviceError* err;
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
@@ -90,12 +93,29 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + WY_BAR + 20);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nchunks = p.T / 64;
-    const long long ch = blockIdx.x;                  // (b*H + h) * nchunks + n
-    const int n = (int)(ch % nchunks);
-    const long long bh = ch / nchunks;
-    const int b = (int)(bh / p.H), h = (int)(bh % p.H);
-    const long long row0 = (long long)b * p.T + (long long)n * 64;   // flattened (b, t)
+    const long long ch = blockIdx.x;   // (b*H + h) * (T/64) + n, or h * total_chunks + c (varlen)
+    int h, valid = 64;                  // valid: tokens of the chunk inside its sequence
+    long long row0;                     // flattened (b, t) of the chunk's first token
+    if (!p.cu_seqlens) {
+        const int nchunks = p.T / 64;
+        const int n = (int)(ch % nchunks);
+        const long long bh = ch / nchunks;
+        h = (int)(bh % p.H);
+        row0 = (bh / p.H) * p.T + (long long)n * 64;
+    } else {
+        h = (int)(ch / p.total_chunks);
+        const int c = (int)(ch % p.total_chunks);
+        if (c >= __ldg(p.cu_chunks + p.nseq)) return;   // past the last chunk (the grid holds a bound)
+        int lo = 0, hi = p.nseq;   // the sequence s with cu_chunks[s] <= c < cu_chunks[s+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(p.cu_chunks + mid) <= c) lo = mid; else hi = mid;
+        }
+        const int n = c - __ldg(p.cu_chunks + lo);
+        const int t0 = __ldg(p.cu_seqlens + lo) + 64 * n;
+        row0 = t0;
+        valid = min(64, __ldg(p.cu_seqlens + lo + 1) - t0);
+    }
     uint8_t* out_b = p.wy + ch * 16384;   // A diag(beta)
     uint8_t* out_g = out_b + 8192;        // A diag(beta 2^Gx)
 
@@ -119,11 +139,14 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // ---- gates: cumulative sums in log2 units (two tokens per lane)
+    // ---- gates: cumulative sums in log2 units (two tokens per lane); tokens past the end of a
+    //      varlen sequence get g = 0 and beta = 0, which makes them no-ops on the state
     if (warp == 1) {
         const long long i0 = (row0 + 2 * lane) * p.H + h;
-        const float g0 = bf16_at(p.g, i0) * kWyLog2e, g1 = bf16_at(p.g, i0 + p.H) * kWyLog2e;
-        const float b0 = bf16_at(p.beta, i0), b1 = bf16_at(p.beta, i0 + p.H);
+        const bool v0 = 2 * lane < valid, v1 = 2 * lane + 1 < valid;
+        const float g0 = v0 ? bf16_at(p.g, i0) * kWyLog2e : 0.f;
+        const float g1 = v1 ? bf16_at(p.g, i0 + p.H) * kWyLog2e : 0.f;
+        const float b0 = v0 ? bf16_at(p.beta, i0) : 0.f, b1 = v1 ? bf16_at(p.beta, i0 + p.H) : 0.f;
         float sum = g0 + g1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -316,11 +339,14 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
     }
 }
 
+// varlen: chunk numbering of the packed sequences (a prefix sum over at most a few thousand
+// lengths, one thread)
 }  // namespace
 
 cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     if (!c.wy) return cudaErrorInvalidValue;
-    const long long nblk = (long long)c.B * c.H * (c.T / kChunk);
+    const long long nblk = c.cu_seqlens ? (long long)c.H * c.total_chunks
+                                        : (long long)c.B * c.H * (c.T / kChunk);
     if (nblk == 0) return cudaSuccess;
     if (nblk >= (1LL << 31)) return cudaErrorInvalidValue;
     WyParams p;
@@ -332,6 +358,10 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     p.T = c.T;
     p.H = c.H;
     p.decay_first = c.decay_first;
+    p.cu_seqlens = c.cu_seqlens;
+    p.cu_chunks = c.cu_chunks;
+    p.nseq = c.B;
+    p.total_chunks = c.total_chunks;
     p.err = c.err;
     p.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
     cudaError_t e = cudaFuncSetAttribute(wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -20,6 +20,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
           6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
 EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
             "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
+            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd",
             "gdn_status_string", "gdn_check_device_error")
 
 
@@ -60,12 +61,15 @@ def lib():
         L.gdn_segmented_fwd_timed.argtypes = ([pp, ctypes.c_int] + [_P] * 10 +
                                               [ctypes.c_size_t, _P, _P])
         L.gdn_segmented_fwd_noalloc.argtypes = [pp, ctypes.c_int] + [_P] * 10
+        L.gdn_varlen_workspace_bytes.argtypes = [pp, ctypes.c_int]
+        L.gdn_varlen_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_varlen_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
-                   "gdn_check_device_error"):
+                   "gdn_varlen_fwd", "gdn_check_device_error"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -157,8 +161,9 @@ def gdn_segmented_fwd(q, k, v, g, beta, h0, o, h_final, nseg, workspace, H_in=No
 def gdn_segmented_fwd_timed(q, k, v, g, beta, h0, o, h_final, nseg, workspace, events,
                             H_in=None, stream=None, prob=None):
     """gdn_segmented_fwd recording five torch.cuda.Event (enable_timing=True) around its
-    four stages: before the WY factors, before summary, before scan, before forward, after
-    forward."""
+    four stages: before the WY factors, before the first phase (piece 0's forward beside the
+    piece summaries), before the scan, before the second phase (the forward of pieces
+    1..P-1), after it."""
     prob = prob or problem(k, v, o)
     if len(events) != 5:
         raise ValueError("gdn_segmented_fwd_timed takes five events")
@@ -180,6 +185,32 @@ def gdn_segmented_fwd_noalloc(q, k, v, g, beta, h0, o, h_final, nseg, device_err
                                            _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
                                            _ptr(h_final), _ptr(device_error), _stream(stream)),
            "gdn_segmented_fwd_noalloc")
+
+
+def varlen_workspace_bytes(prob: Problem, nseq: int) -> int:
+    return int(lib().gdn_varlen_workspace_bytes(ctypes.byref(prob), nseq))
+
+
+def alloc_varlen_workspace(prob: Problem, nseq: int, device="cuda"):
+    """A zeroed workspace tensor for gdn_varlen_fwd (torch owns the memory)."""
+    import torch
+    n = varlen_workspace_bytes(prob, nseq)
+    if n == 0:
+        raise GdnError(2, "gdn_varlen_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def gdn_varlen_fwd(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, stream=None,
+                   prob=None):
+    """Packed variable-length forward: q, k, v, g, beta, o hold [1, T, H, *] tokens of
+    nseq = len(cu_seqlens) - 1 sequences; cu_seqlens is an int32 CUDA tensor; h0 and h_final
+    are [nseq, H, K, V] fp32 (or None)."""
+    prob = prob or problem(k, v, o)
+    nseq = int(cu_seqlens.numel()) - 1
+    _check(lib().gdn_varlen_fwd(ctypes.byref(prob), nseq, _ptr(cu_seqlens), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
+                                _ptr(workspace), workspace.numel() if workspace is not None else 0,
+                                _stream(stream)), "gdn_varlen_fwd")
 
 
 def gdn_check_device_error(workspace, stream=None):

@@ -61,6 +61,8 @@ def fill(seed: int, name: str, shape, kind: int, mu: float = 0.0, sd: float = 1.
     """Draw one tensor. Row = product of all dims but the last two for 4-d tensors
     ([B,T,H,K] -> rows of H*K); for [B,T,H] and [B,H,K,V] see the callers."""
     out = np.empty(shape, dtype=np.float32)
+    if out.size == 0:
+        return out
     n_rows = int(np.prod(shape[:2])) if len(shape) >= 2 else 1
     row_len = int(out.size // max(n_rows, 1))
     rc = _load().synth_fill(ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), TENSOR_IDS[name], n_rows,
@@ -89,6 +91,9 @@ class Workload:
     h0_sd: float | None        # None: h0 = 0 (no initial state passed)
     seed: int
     per_sequence_seed: int | None = None   # if set, batch b uses seed per_sequence_seed + b
+    # packed variable-length sequences: B == 1, T == sum(seq_lens), one initial state per
+    # sequence (h0 is [len(seq_lens), H, K, V])
+    seq_lens: tuple | None = None
     chunk: int = 64
     notes: str = field(default="", compare=False)
 
@@ -120,8 +125,19 @@ WORKLOADS = {
                  in_dtype="bf16", g_mu=6, g_sd=1, beta_mu=-2, beta_sd=1, h0_sd=0.1,
                  seed=0x6D6E0005,
                  notes="summary M stays O(0.1-1): exercises the compose path numerically"),
+        Workload("varlen5_h16_t7300", B=1, H=16, T=7300, K=128, V=128, nseg=1, in_dtype="bf16",
+                 g_mu=2, g_sd=1, beta_mu=0, beta_sd=1, h0_sd=0.1, seed=0x6D6E0006,
+                 seq_lens=(1800, 1500, 2000, 1200, 800),
+                 notes="five packed sequences of the lengths the KDA design page measures"),
     ]
 }
+
+
+def cu_seqlens(w: Workload) -> np.ndarray:
+    """Sequence starts of a packed workload: [0, l0, l0+l1, ..., T] as int32."""
+    if w.seq_lens is None:
+        raise ValueError(f"{w.name} is not a packed variable-length workload")
+    return np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32)
 
 
 def scaled(w: Workload, **changes) -> Workload:
@@ -138,6 +154,9 @@ def make_inputs(w: Workload, nthreads: int = 0) -> dict:
     the arrays to bf16 loses nothing. h0 is always fp32 (the state is fp32).
     """
     bf16 = w.in_dtype == "bf16"
+    if w.seq_lens is not None and (w.B != 1 or sum(w.seq_lens) != w.T or min(w.seq_lens) < 0):
+        raise ValueError(f"{w.name}: packed sequences need B == 1 and T == sum(seq_lens)")
+    n_states = len(w.seq_lens) if w.seq_lens is not None else None
     seeds = ([w.per_sequence_seed + b for b in range(w.B)] if w.per_sequence_seed is not None
              else [w.seed])
     per_b = w.per_sequence_seed is not None
@@ -155,8 +174,8 @@ def make_inputs(w: Workload, nthreads: int = 0) -> dict:
         parts["beta"].append(fill(s, "beta", (Bd, w.T, w.H), KIND_SIGMOID, w.beta_mu, w.beta_sd,
                                   bf16=bf16, nthreads=nthreads))
         if w.h0_sd is not None:
-            parts["h0"].append(fill(s, "h0", (Bd, w.H, w.K, w.V), KIND_NORMAL, 0.0, w.h0_sd,
-                                    bf16=False, nthreads=nthreads))
+            parts["h0"].append(fill(s, "h0", (n_states or Bd, w.H, w.K, w.V), KIND_NORMAL, 0.0,
+                                    w.h0_sd, bf16=False, nthreads=nthreads))
     out = {n: (np.concatenate(p, axis=0) if len(p) > 1 else p[0]) for n, p in parts.items() if p}
     if w.h0_sd is None:
         out["h0"] = None

@@ -202,12 +202,48 @@ GDN_API gdn_status gdn_segmented_fwd_noalloc(const gdn_problem* p, int nseg, con
                                              float* h_final, unsigned* device_error,
                                              void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Packed variable-length sequences
+ * ---------------------------------------------------------------------------------------
+ * nseq sequences of different lengths share one token axis: sequence s holds tokens
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1 of q, k, v, g, beta and o, which are laid out as for
+ * B = 1 ([1, T, H, *], T = cu_seqlens[nseq] the total). Each sequence runs the recurrence
+ * from its own initial state and is cut into chunks of 64 tokens counted from its own first
+ * token (its last chunk may be shorter), so no state crosses from one sequence into the
+ * next -- "KDA Chunk Backward -- TPU/Pallas Kernel Design", section 3.8 "Fixed Shapes
+ * Supporting varlen" (cu_seqlens; every sequence aligned to the chunk size). The tokens stay
+ * packed in memory: the alignment is in the chunk numbering, not a padded copy.
+ * Supported set: p->B == 1, T >= 0 (any length), nseq >= 1, the K/V/dtype set above;
+ * bf16 inputs with K == V == 128 and T >= 64 run the tcgen05 kernels, the rest the CUDA-core
+ * kernels. */
+
+/* Workspace bytes for gdn_varlen_fwd: the error word, the WY tiles of at most T/64 + nseq
+ * chunks per head (tensor-core shapes) and two int arrays of nseq + 1. Depends on T, H, K,
+ * V, the dtypes and nseq only, not on the lengths. Returns 0 for an invalid problem. */
+GDN_API size_t gdn_varlen_workspace_bytes(const gdn_problem* p, int nseq);
+
+/* Chunked forward of every packed sequence (RFC section 2.1 per sequence).
+ *   cu_seqlens  [nseq + 1] int32 DEVICE array: 0 first, T last, non-decreasing (empty
+ *               sequences allowed). It is checked on the device: a bad array is recorded in
+ *               the workspace's error word as GDN_ERR_INVALID_ARG (gdn_check_device_error)
+ *               and the call then treats every sequence as empty (o is not written and
+ *               h_final = h0).
+ *   h0       [nseq, H, K, V] fp32, or NULL for zero initial states.
+ *   o        [1, T, H, V] out_dtype, written.
+ *   h_final  [nseq, H, K, V] fp32, the state after each sequence's last token; NULL skips it.
+ *   Workspace: gdn_varlen_workspace_bytes(p, nseq). Nothing is read back to the host: the
+ *   call can be captured in a CUDA graph. */
+GDN_API gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_seqlens,
+                                  const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const float* h0, void* o, float* h_final,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 GDN_API const char* gdn_status_string(gdn_status s);
 
 /* Synchronises `stream`, reads the workspace's device error word, clears it, and returns
  * GDN_OK, GDN_ERR_TIMEOUT (a bounded wait ran out; the results of the affected calls are
- * invalid) or GDN_ERR_CUDA. If `detail` is non-NULL it receives the recorded detail word
+ * invalid), GDN_ERR_INVALID_ARG (gdn_varlen_fwd got a bad cu_seqlens) or GDN_ERR_CUDA. If `detail` is non-NULL it receives the recorded detail word
  * (which wait gave up), or 0. */
 GDN_API gdn_status gdn_check_device_error(void* workspace, void* stream, unsigned* detail);
 

@@ -16,6 +16,9 @@ What each function computes (pages cited by title and section):
   compose / scan  -- M = M1 @ M0, S = M1 @ S0 + S1 (RFC 2.2; "Context Parallelism in ART",
                      section 08 "Then parallelize across GPUs"), scanned exclusively in
                      segment order from h0.
+  varlen_recurrence -- packed variable-length sequences ("KDA Chunk Backward -- TPU/Pallas
+                     Kernel Design", section 3.8): each sequence of the packed token axis
+                     runs the recurrence alone from its own initial state.
   chunked_fwd / chunked_summary -- the chunk equations of "Context Parallelism in ART",
                      section 08 "First parallelize within a GPU", restated for the RFC's
                      un-decayed read; used only to pin chunked == per-token.
@@ -108,6 +111,28 @@ def recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
                               _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), _ptr(H_in), col_block,
                               nthreads, int(decay_first))
     return o, hf, H_in
+
+
+def varlen_recurrence(q, k, v, g, beta, cu_seqlens, h0=None, nthreads: int = 0,
+                      decay_first: bool = False):
+    """Packed sequences: q, k, v, g, beta hold [1, T, H, *]; sequence s is tokens
+    cu_seqlens[s] .. cu_seqlens[s+1]-1 and starts from h0[s] (zero when h0 is None); no state
+    passes between sequences. Returns (o [1,T,H,V], h_final [nseq,H,K,V])."""
+    cu = [int(c) for c in cu_seqlens]
+    nseq = len(cu) - 1
+    B, T, H, K = np.shape(k)
+    V = np.shape(v)[-1]
+    assert B == 1 and cu[0] == 0 and cu[-1] == T and all(a <= b for a, b in zip(cu, cu[1:]))
+    o = np.zeros((1, T, H, V), np.float64)
+    hf = np.empty((nseq, H, K, V), np.float64)
+    for s in range(nseq):
+        a, b = cu[s], cu[s + 1]
+        h0_s = None if h0 is None else np.asarray(h0)[s:s + 1]
+        o_s, hf_s, _ = recurrence(*(np.asarray(x)[:, a:b] for x in (q, k, v, g, beta)), h0_s,
+                                  nthreads=nthreads, decay_first=decay_first)
+        o[:, a:b] = o_s
+        hf[s] = hf_s[0]
+    return o, hf
 
 
 def summary(k, v, g, beta, nseg: int, nthreads: int = 0, decay_first: bool = False):

@@ -118,3 +118,20 @@ def test_null_pointers_and_missing_workspace_rejected(L):
     assert st == 1
     st = L.gdn_check_device_error(None, None, None)
     assert st == 5
+
+
+def test_varlen_workspace_and_validation(L):
+    # packed sequences: B == 1, any T; the WY tiles of at most T/64 + nseq chunks per head,
+    # then two int32 arrays of nseq + 1 (each region 256-byte aligned)
+    p = P(B=1, T=7300, H=16)
+    wy = 16 * (7300 // 64 + 5) * 16384
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 5) == 256 + wy + 256 + 256
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=7300, H=16, in_dtype=0)), 5) == 768
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=0)), 1) == 256 + 2 * 16384 + 512
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=2, T=7300)), 5) == 0   # B must be 1
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 0) == 0
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, K=96, V=96)), 1) == 0
+    # rejections before any pointer is used
+    assert L.gdn_varlen_fwd(ctypes.byref(P(B=2)), 1, *([None] * 10), 0, None) == 1
+    assert L.gdn_varlen_fwd(ctypes.byref(P(B=1, chunk=32)), 1, *([None] * 10), 0, None) == 2
+    assert L.gdn_varlen_fwd(ctypes.byref(P(B=1)), 1, *([None] * 10), 0, None) == 1   # no cu_seqlens

@@ -1,0 +1,162 @@
+"""GPU parity of the packed variable-length forward ("KDA Chunk Backward -- TPU/Pallas Kernel
+Design", section 3.8): gdn_varlen_fwd through the C ABI against the fp64 oracle's
+per-sequence recurrence on the same seeded inputs, element by element.
+
+Bars (per tensor, max|err| / RMS(ref)): 1e-4 for fp32 inputs, 2e-2 for bf16 inputs.
+Lengths cover sequences shorter than a chunk, exactly one chunk, one token over, empty
+sequences first, inside and last, starts that are not multiples of 64, and a total below one
+chunk (which runs the CUDA-core kernels).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from context_scan_gb300 import gdn, synth
+from gpu_util import TOL_BF16, TOL_F32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+BASE = synth.WORKLOADS["varlen5_h16_t7300"]
+
+
+def packed(lens, H=2, K=128, in_dtype="bf16", h0=True, seed=None, **kw):
+    lens = tuple(int(n) for n in lens)
+    return synth.scaled(BASE, H=H, K=K, V=K, T=sum(lens), seq_lens=lens, in_dtype=in_dtype,
+                        h0_sd=0.1 if h0 else None, seed=seed or BASE.seed + sum(lens), **kw)
+
+
+CASES = {
+    "five_scaled": packed((180, 150, 200, 120, 80)),
+    "edge_lengths": packed((1, 63, 64, 65, 0, 130, 0, 127)),
+    "empty_first_and_last": packed((0, 100, 0, 257, 0)),
+    "one_sequence": packed((640,)),
+    "below_one_chunk": packed((10, 20, 0, 3)),
+    "f32_k64": packed((70, 0, 129, 5), K=64, in_dtype="f32"),
+    "bf16_k64": packed((70, 200, 1), K=64),
+    "no_initial_state": packed((65, 190), h0=False),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from context_scan_gb300 import _build
+    _build.build_cuda()
+    gdn.lib()
+
+
+def run_varlen(w, x, decay_first=False, out_dtype=torch.float32, cu=None):
+    dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    d = {n: torch.from_numpy(x[n]).cuda().to(dt).contiguous() for n in ("q", "k", "v", "g", "beta")}
+    h0 = None if x["h0"] is None else torch.from_numpy(x["h0"]).cuda().contiguous()
+    cu = synth.cu_seqlens(w) if cu is None else np.asarray(cu, np.int32)
+    nseq = len(cu) - 1
+    # NaN-filled outputs: a token or state the call fails to write shows up
+    o = torch.full((1, w.T, w.H, w.V), float("nan"), dtype=out_dtype, device="cuda")
+    hf = torch.full((nseq, w.H, w.K, w.V), float("nan"), device="cuda")
+    cu_d = torch.from_numpy(cu).cuda()
+    prob = gdn.problem(d["k"], d["v"], o, decay_first=decay_first)
+    ws = gdn.alloc_varlen_workspace(prob, nseq)
+    gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0, o, hf, cu_d, ws, prob=prob)
+    torch.cuda.synchronize()
+    st, detail = gdn.gdn_check_device_error(ws)
+    return o, hf, st, detail
+
+
+def reference(w, x, decay_first=False):
+    return oracle.varlen_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                    synth.cu_seqlens(w), x["h0"], decay_first=decay_first)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_varlen_matches_oracle(name):
+    w = CASES[name]
+    x = synth.make_inputs(w)
+    o, hf, st, detail = run_varlen(w, x)
+    assert st == 0, (st, detail)
+    o_ref, hf_ref = reference(w, x)
+    tol = TOL_F32 if w.in_dtype == "f32" else TOL_BF16
+    assert torch.isfinite(o).all() and torch.isfinite(hf).all()
+    assert rel_err(np64(o), o_ref) <= tol
+    assert rel_err(np64(hf), hf_ref) <= tol
+    # every sequence on its own scale too (a short one drowns in the others' RMS)
+    cu = synth.cu_seqlens(w)
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b > a:
+            assert rel_err(np64(o[:, a:b]), o_ref[:, a:b]) <= tol, s
+        if x["h0"] is not None or b > a:
+            assert rel_err(np64(hf[s]), hf_ref[s]) <= tol, s
+        else:
+            assert not hf[s].any(), s   # empty sequence from a zero state
+
+
+@pytest.mark.parametrize("name", ["five_scaled", "edge_lengths", "f32_k64"])
+def test_varlen_decayed_read(name):
+    w = CASES[name]
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x, decay_first=True)
+    assert st == 0
+    o_ref, hf_ref = reference(w, x, decay_first=True)
+    tol = TOL_F32 if w.in_dtype == "f32" else TOL_BF16
+    assert rel_err(np64(o), o_ref) <= tol
+    assert rel_err(np64(hf), hf_ref) <= tol
+
+
+def test_varlen_bf16_output():
+    w = CASES["five_scaled"]
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x, out_dtype=torch.bfloat16)
+    assert st == 0 and o.dtype == torch.bfloat16
+    o_ref, hf_ref = reference(w, x)
+    # bf16 storage of o alone costs up to 2^-9 |o|, a few 1e-3 of RMS: bar 3e-2
+    assert rel_err(np64(o), o_ref) <= 3e-2
+    assert rel_err(np64(hf), hf_ref) <= TOL_BF16
+
+
+def test_varlen_all_empty():
+    w = packed((0, 0, 0))
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x)
+    assert st == 0 and o.numel() == 0
+    assert torch.equal(hf.cpu(), torch.from_numpy(x["h0"]))
+
+
+@pytest.mark.parametrize("cu", [[0, 100, 60, 257], [0, 100, 200, 250], [5, 100, 200, 257]])
+def test_varlen_bad_lengths_are_reported(cu):
+    # a device array that is not 0 .. T non-decreasing is caught on the device before any
+    # chain reads it: the error word says GDN_ERR_INVALID_ARG, every sequence is treated as
+    # empty (h_final = h0) and o is left as it was
+    w = packed((100, 100, 57))
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x, cu=cu)
+    assert st == 1
+    assert torch.isnan(o).all()
+    assert torch.equal(hf.cpu(), torch.from_numpy(x["h0"]))
+    # and a call with the right lengths works
+    o, hf, st, _ = run_varlen(w, x)
+    assert st == 0 and torch.isfinite(o).all()
+
+
+def test_varlen_deterministic():
+    w = CASES["edge_lengths"]
+    x = synth.make_inputs(w)
+    o1, hf1, _, _ = run_varlen(w, x)
+    o2, hf2, _, _ = run_varlen(w, x)
+    assert torch.equal(o1, o2) and torch.equal(hf1, hf2)
+
+
+def test_varlen_full_size_sampled_heads():
+    # the KDA design page's packed lengths at H = 16, K = V = 128, checked on sampled heads
+    w = BASE
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x)
+    assert st == 0
+    assert torch.isfinite(o).all() and torch.isfinite(hf).all()
+    cu = synth.cu_seqlens(w)
+    for h in (0, 7, 15):
+        xs = {n: x[n][:, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+        o_ref, hf_ref = oracle.varlen_recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"],
+                                                 cu, x["h0"][:, h:h + 1])
+        assert rel_err(np64(o[:, :, h:h + 1]), o_ref) <= TOL_BF16, h
+        assert rel_err(np64(hf[:, h:h + 1]), hf_ref) <= TOL_BF16, h

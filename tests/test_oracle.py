@@ -337,3 +337,64 @@ def test_column_blocks_and_threads_do_not_change_results():
     o2, h2, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
                                   col_block=5, nthreads=4)
     assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
+
+
+# --------------------------------------------------------------------------------------
+# packed variable-length sequences ("KDA Chunk Backward -- TPU/Pallas Kernel Design",
+# section 3.8): every sequence runs alone from its own initial state
+# --------------------------------------------------------------------------------------
+def _golden_tokens(d, c):
+    tok = d["tokens"]
+    arr = {n: np.array(tok[n], np.float32) for n in ("q", "k", "v", "beta")}
+    arr["g"] = np.array(c["g"], np.float32)
+    return arr
+
+
+def test_varlen_hand_worked_packed():
+    # the two default-reading hand-worked cases packed one after the other, with an empty
+    # sequence between them: outputs and final states are the hand-worked values, and the
+    # empty sequence hands back its initial state
+    d = json.load(open(GOLDEN))
+    c0, c1 = d["cases"][0], d["cases"][1]
+    a0, a1 = _golden_tokens(d, c0), _golden_tokens(d, c1)
+    pack = {n: np.concatenate([a0[n], a1[n]]) for n in a0}
+    q, k, v = (pack[n].reshape(1, 6, 1, 2) for n in ("q", "k", "v"))
+    g, beta = pack["g"].reshape(1, 6, 1), pack["beta"].reshape(1, 6, 1)
+    h_mid = np.array([[7.0, -1.0], [0.5, 3.0]], np.float32)
+    h0 = np.stack([np.array(c0["h0"], np.float32), h_mid,
+                   np.array(c1["h0"], np.float32)]).reshape(3, 1, 2, 2)
+    o, hf = oracle.varlen_recurrence(q, k, v, g, beta, [0, 3, 3, 6], h0)
+    tol = max(c0["tol"], c1["tol"])
+    assert np.max(np.abs(o[0, :3, 0] - np.array(c0["o"]))) <= tol
+    assert np.max(np.abs(o[0, 3:, 0] - np.array(c1["o"]))) <= tol
+    assert np.max(np.abs(hf[0, 0] - np.array(c0["h_final"]))) <= tol
+    assert np.array_equal(hf[1, 0], h_mid.astype(np.float64))
+    assert np.max(np.abs(hf[2, 0] - np.array(c1["h_final"]))) <= tol
+
+
+def test_varlen_split_is_a_continuation():
+    # one sequence cut in two at an unaligned token, the second part started from the
+    # first part's final state, equals the unsplit sequence
+    x = rand_inputs(1, 300, 2, 8, 4, seed=4242)
+    o, hf, _ = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    h0 = np.concatenate([x["h0"], np.zeros_like(x["h0"])])
+    _, hf1 = oracle.varlen_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], [0, 97, 300], h0)
+    h0[1] = hf1[0]
+    o2, hf2 = oracle.varlen_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], [0, 97, 300], h0)
+    assert np.array_equal(o2[:, :97], o[:, :97])
+    # the handed-over state is rounded to fp32 (initial states are fp32 inputs)
+    assert rel_err(o2, o) <= 1e-6
+    assert rel_err(hf2[1], hf[0]) <= 1e-6
+
+
+def test_varlen_sequences_are_independent():
+    x = rand_inputs(1, 200, 2, 8, 8, seed=4343, h0=False)
+    cu = [0, 64, 129, 200]
+    o, hf = oracle.varlen_recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], cu)
+    y = {n: x[n].copy() for n in ("q", "k", "v", "g", "beta")}
+    for n in y:
+        y[n][:, 64:129] = y[n][:, 64:129][:, ::-1]   # change only the middle sequence
+    o2, hf2 = oracle.varlen_recurrence(y["q"], y["k"], y["v"], y["g"], y["beta"], cu)
+    assert np.array_equal(o2[:, :64], o[:, :64]) and np.array_equal(o2[:, 129:], o[:, 129:])
+    assert np.array_equal(hf2[[0, 2]], hf[[0, 2]])
+    assert not np.allclose(o2[:, 64:129], o[:, 64:129])
