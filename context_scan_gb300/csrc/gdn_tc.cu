@@ -73,7 +73,9 @@ struct Cfg {
     static constexpr int NGRP = SUMMARY ? 1 : 2;             // prep warp groups
     static constexpr int PREP_WARP0 = 4 * NSG;
     static constexpr int PREP_THREADS = 128 * NGRP;
-    static constexpr int PRODUCER_WARP = 4 * NSG + 4 * NGRP;
+    // forward: one more warp issues the prep group's MMAs (P1, P2, P3)
+    static constexpr int MMA_WARP = SUMMARY ? -1 : 4 * NSG + 4 * NGRP;
+    static constexpr int PRODUCER_WARP = 4 * NSG + 4 * NGRP + (SUMMARY ? 0 : 1);
     static constexpr int THREADS = 32 * PRODUCER_WARP + 32;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_S = 0;    // Q K^T, then W^T (prep)
@@ -125,13 +127,14 @@ enum { SC_GAM = 0, SC_DD, SC_EG, SC_MISC, SC_N = 4 };
 constexpr uint32_t B_KFULL = 0, B_KEMPTY = 32, B_QFULL = 64, B_QEMPTY = 80, B_AFULL = 96,
                    B_AEMPTY = 112, B_VFULL = 128, B_VEMPTY = 136, B_BARP = 144, B_BARS = 152,
                    B_PREPDONE = 160, B_WFREE = 168, B_UFREE = 176, B_TMEM = 192, B_ABORT = 196,
-                   B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216;
+                   B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216, B_CDONE = 224,
+                   B_WREAD = 232, B_MDRAIN = 240;
 
 // wait tags recorded in the device error word's detail field
 enum : unsigned {
     TAG_KFULL = 1, TAG_BARP = 2, TAG_BARS = 3, TAG_KEMPTY = 4, TAG_VEMPTY = 5, TAG_PREPDONE = 6,
     TAG_WFREE = 7, TAG_UFREE = 8, TAG_VFULL = 9, TAG_QFULL = 10, TAG_QEMPTY = 11,
-    TAG_AFULL = 12, TAG_AEMPTY = 13
+    TAG_AFULL = 12, TAG_AEMPTY = 13, TAG_CDONE = 14, TAG_WREAD = 15
 };
 
 struct TcParams {
@@ -142,9 +145,10 @@ struct TcParams {
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
 
-// 32 token rows of one output column from a 64-column O^T buffer in tensor memory
+// 32 token rows of one output column from a 64-column O^T buffer in tensor memory; rows from
+// `valid` on (past the end of a varlen sequence) are not stored
 __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_col, long long idx0,
-                                               long long tok_stride) {
+                                               long long tok_stride, int valid) {
     float ov2[2][16];
     tmem_ld16(t_col, ov2[0]);
     tmem_ld16(t_col + 16, ov2[1]);
@@ -156,11 +160,13 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
         if (c.out_bf16) {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(c.o) + base;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[(long long)j * tok_stride] = __float2bfloat16_rn(ov[j]);
+            for (int j = 0; j < 16; ++j)
+                if (16 * g + j < valid) o[(long long)j * tok_stride] = __float2bfloat16_rn(ov[j]);
         } else {
             float* o = reinterpret_cast<float*>(c.o) + base;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[(long long)j * tok_stride] = ov[j];
+            for (int j = 0; j < 16; ++j)
+                if (16 * g + j < valid) o[(long long)j * tok_stride] = ov[j];
         }
     }
 }
@@ -170,7 +176,9 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
 // ------------------------------------------------------------------------------------
 // Registers are allocated to warps in groups of four: 13 warps count as 16, so at most 128
 // registers per thread.
-template <bool SUMMARY>
+// VARLEN: the chains are the packed sequences of c.cu_seqlens (forward only); the
+// fixed-length instance has none of the end-of-sequence checks.
+template <bool SUMMARY, bool VARLEN>
 __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant__ TcParams p) {
     using L = Smem<SUMMARY>;
     using F = Cfg<SUMMARY>;
@@ -194,11 +202,16 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     const int seg = c.seg_first + chain % c.nseg_run;
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
-    const int nchunks = c.seg_len / kC;
+    // tokens of this chain: a segment of the fixed-length batch, or a whole varlen sequence
+    // (whose last chunk may be partial: its padding tokens get g = 0 here and beta = 0 in the
+    // WY tiles, which leaves the state untouched, and their outputs are not stored)
+    const int seq_tokens = VARLEN ? c.cu_seqlens[b + 1] - c.cu_seqlens[b] : c.seg_len;
+    const int nchunks = VARLEN ? (seq_tokens + kC - 1) / kC : c.seg_len / kC;
     constexpr bool need_v = true;   // every CTA forms U (the forward, or the summary's S part)
     const long long limit = p.wait_limit;
     const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
-    const long long row_seg = (long long)b * c.T + (long long)seg * c.seg_len;   // flattened (b, t)
+    const long long row_seg = VARLEN ? (long long)c.cu_seqlens[b]   // flattened (b, t)
+                                           : (long long)b * c.T + (long long)seg * c.seg_len;
 
     // A forward grid lets a grid launched after it as its programmatic dependent start right
     // away (the summaries that run beside the first piece's forward); a summary grid so
@@ -223,6 +236,9 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         mbar_init(bar0 + B_BARS1, 1);
         mbar_init(bar0 + B_PREPDONE, 1);
         mbar_init(bar0 + B_WFREE, NSG);   // each state group's S1 reads -sigma W
+        mbar_init(bar0 + B_CDONE, 1);
+        mbar_init(bar0 + B_WREAD, 1);
+        mbar_init(bar0 + B_MDRAIN, 1);
         *abort_flag = 0;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S) = 1;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S1) = 1;
@@ -250,14 +266,16 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         const uint32_t wy_bytes = need_v ? 16384u : 8192u;
         const uint32_t wy_skip = 16384u - wy_bytes;
         const uint8_t* wy_chain = reinterpret_cast<const uint8_t*>(c.wy) +
-                                  (((long long)bh * (c.T / kC) + (long long)seg * nchunks) << 14);
+                                  ((VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[b]
+                                                 : (long long)bh * (c.T / kC) + (long long)seg * nchunks)
+                                   << 14);
         int k_last[KST], q_last[2] = {-1, -1}, a_last[2] = {-1, -1}, v_last = -1;
 #pragma unroll
         for (int i = 0; i < KST; ++i) k_last[i] = -1;
         float gpre0 = 0.f, gpre1 = 0.f;
         if (nchunks > 0) {
-            gpre0 = bf16_at(c.g, (row_seg + lane) * c.H + h) * kLog2e;
-            gpre1 = bf16_at(c.g, (row_seg + lane + 32) * c.H + h) * kLog2e;
+            gpre0 = (!VARLEN || lane < seq_tokens) ? bf16_at(c.g, (row_seg + lane) * c.H + h) * kLog2e : 0.f;
+            gpre1 = (!VARLEN || lane + 32 < seq_tokens) ? bf16_at(c.g, (row_seg + lane + 32) * c.H + h) * kLog2e : 0.f;
         }
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
@@ -280,8 +298,9 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(bar0 + B_KFULL + 8 * ks);
             if (n + 1 < nchunks) {
-                gpre0 = bf16_at(c.g, (row0 + kC + lane) * c.H + h) * kLog2e;
-                gpre1 = bf16_at(c.g, (row0 + kC + lane + 32) * c.H + h) * kLog2e;
+                const int t1 = (n + 1) * kC + lane;   // token index inside the chain
+                gpre0 = (!VARLEN || t1 < seq_tokens) ? bf16_at(c.g, (row0 + kC + lane) * c.H + h) * kLog2e : 0.f;
+                gpre1 = (!VARLEN || t1 + 32 < seq_tokens) ? bf16_at(c.g, (row0 + kC + lane + 32) * c.H + h) * kLog2e : 0.f;
             }
             if (!SUMMARY) {
                 const int qs = n & 1;
@@ -336,6 +355,69 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             if (v_last >= 0) mbar_drain(bar0 + B_VFULL, v_last & 1, limit);
         }
+    } else if (!SUMMARY && warp == F::MMA_WARP) {
+        // ============================== prep MMA issue ============================
+        // The forward prep group's tensor-core work, issued from here so that no prep thread
+        // stalls behind an MMA issue. Per chunk n: P2 (U^T into the parity's U buffer, once
+        // chunk n-2 has retired it), P3 (W^T into TM_S, once the C warps have read Q K^T out of
+        // it) and P1 of chunk n+1 ([Q ; -] K^T into TM_S, once the prep group has read W^T out
+        // of it). Lane 0 issues; every wait is bounded.
+        if (lane == 0 && nchunks > 0) {
+            auto ok = [&](uint32_t bar, uint32_t parity, unsigned tag) {
+                return mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
+            };
+            // P1: [Q ; -] K^T -> TM_S for chunk m; lanes 0..63 hold Q K^T (rows 64..127 of the
+            // A operand run into the next buffer and are never read)
+            auto p1 = [&](int m) {
+                const uint32_t kst1 = base + L::K0 + (m % KST) * 16384;
+                const uint32_t qst1 = base + L::Q0 + (m & 1) * 16384;
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 8; ++k16) {
+                    const uint32_t off = (k16 >> 2) * 8192 + (k16 & 3) * 32;
+                    mma_ss<ID_P1>(tmem + TM_S, desc_k(qst1 + off), desc_k(kst1 + off), k16 > 0);
+                }
+                mma_commit(bar0 + B_BARP);
+            };
+            bool run = ok(bar0 + B_KFULL, 0, TAG_KFULL) && ok(bar0 + B_QFULL, 0, TAG_QFULL);
+            if (run) p1(0);
+#pragma unroll 1
+            for (int n = 0; run && n < nchunks; ++n) {
+                const int as = n % AST;
+                const uint32_t kst = base + L::K0 + (n % KST) * 16384;
+                const uint32_t ast = base + L::A0 + as * 16384;
+                const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
+                run = (n < NUB || ok(bar0 + B_UFREE + 8 * (n % NUB), ((n / NUB) - 1) & 1, TAG_UFREE)) &&
+                      ok(bar0 + B_AFULL + 8 * as, (n / AST) & 1, TAG_AFULL) &&
+                      ok(bar0 + B_VFULL, n & 1, TAG_VFULL);
+                if (!run) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
+                                   desc_k(ast + k16 * 32), k16 > 0);
+                mma_commit(bar0 + B_VEMPTY);
+                if (!(run = ok(bar0 + B_CDONE, n & 1, TAG_CDONE))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
+                                   desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                mma_commit(bar0 + B_AEMPTY + 8 * as);
+                mma_commit(bar0 + B_BARP);   // covers P2 as well
+                if (n + 1 < nchunks) {
+                    const int m = n + 1;
+                    run = ok(bar0 + B_WREAD, n & 1, TAG_WREAD) &&
+                          ok(bar0 + B_KFULL + 8 * (m % KST), (m / KST) & 1, TAG_KFULL) &&
+                          ok(bar0 + B_QFULL + 8 * (m & 1), (m >> 1) & 1, TAG_QFULL);
+                    if (run) p1(m);
+                }
+            }
+            // everything issued here retires before tensor memory is released
+            mma_commit(bar0 + B_MDRAIN);
+            mbar_drain(bar0 + B_MDRAIN, 0, limit);
+        }
+        __syncwarp();
     } else if (warp >= F::PREP_WARP0) {
         // ================================== prep ==================================
         const int pt = tid - 32 * F::PREP_WARP0, pw = warp - F::PREP_WARP0;
@@ -366,31 +448,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #define store_output(m)                                                                       \
     store_o_rows32(c, t_row + TM_U + ((m) & 1) * 128 + 64 + 32 * grp,                          \
                    ((row_seg + (long long)(m) * kC + 32 * grp) * c.H + h) * kD + 32 * lq + lane, \
-                   tok_stride)
-
-// P1: [Q ; -] K^T -> TM_S for chunk m (k stage m % KST, q stage m & 1); lanes 0..63 hold
-// Q K^T. Rows 64..127 of the A operand run into the next buffer and are never read.
-// Only the issuing thread waits for the tiles (bounded); if it gives up it raises the abort
-// flag, issues nothing, and the group learns of it at its next group wait.
-#define issue_p1(m)                                                                           \
-    do {                                                                                      \
-        if (pt == 0 &&                                                                        \
-            mbar_wait(bar0 + B_KFULL + 8 * ((m) % KST), ((m) / KST) & 1, abort_flag, limit,   \
-                      c.err, TAG_KFULL) &&                                                    \
-            mbar_wait(bar0 + B_QFULL + 8 * ((m) & 1), ((m) >> 1) & 1, abort_flag, limit,      \
-                      c.err, TAG_QFULL)) {                                                    \
-            const uint32_t kst1 = base + L::K0 + ((m) % KST) * 16384;                          \
-            const uint32_t qst1 = base + L::Q0 + ((m) & 1) * 16384;                            \
-            tc_fence_after();                                                                 \
-            _Pragma("unroll") for (int k16 = 0; k16 < 8; ++k16) {                             \
-                const uint32_t off = (k16 >> 2) * 8192 + (k16 & 3) * 32;                      \
-                mma_ss<ID_P1>(tmem + TM_S, desc_k(qst1 + off), desc_k(kst1 + off), k16 > 0); \
-            }                                                                                 \
-            mma_commit(bar0 + B_BARP);                                                        \
-        }                                                                                     \
-        __syncwarp();                                                                         \
-        barp_pending = true;                                                                  \
-    } while (0)
+                   tok_stride, VARLEN ? seq_tokens - ((m) * kC + 32 * grp) : 32)
 
 // this warp's lane quarter of the output rows of chunk n-2 (its group's 32 token columns),
 // then zero those cells of the parity's O^T buffer
@@ -405,7 +463,6 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         tmem_wait_st();                                                                       \
     } while (0)
 
-        if (!SUMMARY && nchunks > 0) issue_p1(0);
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
             const int ks = n % KST, qs = n & 1, as = n % AST;
@@ -417,20 +474,6 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             // be reused
             if (!pwait(bar0 + B_UFREE + 8 * (n % NUB), ((n / NUB) - 1) & 1, TAG_UFREE, n >= NUB))
                 break;
-            // ---- forward: P2 (U^T into the parity's U buffer) right away; only the issuing
-            //      thread waits for the WY and v tiles. Its completion is covered by the commit
-            //      after P3 below.
-            if (!SUMMARY && pt == 0 &&
-                mbar_wait(bar0 + B_AFULL + 8 * as, (n / AST) & 1, abort_flag, limit, c.err, TAG_AFULL) &&
-                mbar_wait(bar0 + B_VFULL, n & 1, abort_flag, limit, c.err, TAG_VFULL)) {
-                tc_fence_after();
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                   desc_k(ast + k16 * 32), k16 > 0);
-                mma_commit(bar0 + B_VEMPTY);
-            }
-
             // ---- gate cumsum, sigma bookkeeping and per-chunk scalars (first prep warp; the
             //      gates arrive with the chunk's k tile)
             // (warp pw 2: warp pw 0 may be busy issuing P2)
@@ -471,8 +514,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 named_bar<2, kPrepThreads>();   // publishes the scalars
                 if (lq < 2) {
                     // ---- C rows i = lanes 0..63 (warps of lane quarters 0, 1), this group's 32
-                    //      columns j, tf32 K-major; then (one thread) P3, once every C warp has
-                    //      read Q K^T out of TM_S
+                    //      columns j, tf32 K-major; once every C warp has read Q K^T out of TM_S,
+                    //      the MMA warp issues P3 into it
                     if (warp_wait(bar0 + B_BARP, barp_phase, abort_flag, limit, c.err, TAG_BARP, lane)) {
                         tc_fence_after();
                         const float* gam = sc + SC_GAM * 64;
@@ -502,15 +545,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     fence_proxy_async();
                     tc_fence_before();
                     named_bar<3, 128>();   // the C warps only
-                    if (pt == 0 && !*abort_flag) {
-                        tc_fence_after();
-#pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16)
-                            mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
-                                           desc_k(ast + 8192 + k16 * 32), k16 > 0);
-                        mma_commit(bar0 + B_AEMPTY + 8 * as);
-                        mma_commit(bar0 + B_BARP);
-                    }
+                    if (pt == 0) mbar_arrive(bar0 + B_CDONE);
                     __syncwarp();
                     // ---- while P3 runs: this warp's share of the output rows of chunk n-2
                     //      (retired above), then zero it in its O^T buffer, which S12 of this
@@ -521,8 +556,11 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     //      buffer), then sigma Qd = sigma 2^G_i q_i as tf32 K-major: row i,
                     //      feature half kh
                     epilogue();
+                    // (the q tile's arrival is waited for here: P1 is the MMA warp's)
                     if (warp_wait(bar0 + B_WFREE, (n - 1) & 1, abort_flag, limit, c.err, TAG_WFREE,
-                                  lane, n >= 1)) {
+                                  lane, n >= 1) &&
+                        warp_wait(bar0 + B_QFULL + 8 * qs, (n >> 1) & 1, abort_flag, limit, c.err,
+                                  TAG_QFULL, lane)) {
                         const int qt = (grp * 2 + (lq - 2)) * 32 + lane;
                         const int i = qt >> 1, kh = qt & 1;
                         const float egi = sc[SC_EG * 64 + i];
@@ -607,18 +645,20 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             fence_proxy_async();
             tc_fence_before();
             named_bar<2, kPrepThreads>();
-            // ---- the q tile is consumed (P1 and sigma Qd); TM_S is free again: P1 of the next
-            //      chunk goes to the tensor pipe now
-            if (!SUMMARY) {
-                if (pt == 0) mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
-                if (n + 1 < nchunks) issue_p1(n + 1);
+            // ---- the chunk is ready for the state group; in the forward the q tile is consumed
+            //      (P1 and sigma Qd) and TM_S is free again for the MMA warp's next P1
+            if (pt == 0) {
+                mbar_arrive(bar0 + B_PREPDONE);
+                if (!SUMMARY) {
+                    mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
+                    mbar_arrive(bar0 + B_WREAD);
+                }
             }
-            if (pt == 0) mbar_arrive(bar0 + B_PREPDONE);
         }
 #undef epilogue
-#undef issue_p1
         if (*go == 0) {
-            if (barp_pending && pt == 0) mbar_drain(bar0 + B_BARP, barp_phase, limit);
+            // (the forward's prep MMAs are the MMA warp's, which lets them retire itself)
+            if (SUMMARY && barp_pending && pt == 0) mbar_drain(bar0 + B_BARP, barp_phase, limit);
         } else if (!SUMMARY) {
             // ---- output rows of the last two chunks
 #pragma unroll 1
@@ -847,7 +887,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 // ------------------------------------------------------------------------------------
 template <bool SUMMARY>
 cudaError_t launch(const ChainParams& c, cudaStream_t s) {
-    if (!c.wy) return cudaErrorInvalidValue;
+    if (!c.wy || (SUMMARY && c.cu_seqlens)) return cudaErrorInvalidValue;
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.c = c;
@@ -855,7 +895,7 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
     if (!make_map(&tp.tm_k, c.k, c)) return cudaErrorInvalidValue;
     if (!SUMMARY && !make_map(&tp.tm_q, c.q, c)) return cudaErrorInvalidValue;
     if (!make_map(&tp.tm_v, c.v, c)) return cudaErrorInvalidValue;
-    auto kern = tc_chain_kernel<SUMMARY>;
+    auto kern = c.cu_seqlens ? tc_chain_kernel<SUMMARY, !SUMMARY> : tc_chain_kernel<SUMMARY, false>;
     constexpr uint32_t bytes = Smem<SUMMARY>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
@@ -881,8 +921,8 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
 }  // namespace
 
 bool tc_supported(const ChainParams& p) {
-    return p.in_bf16 && p.K == kD && p.V == kD && p.seg_len > 0 && p.seg_len % kC == 0 &&
-           encode_fn() != nullptr;
+    return p.in_bf16 && p.K == kD && p.V == kD &&
+           (p.cu_seqlens || (p.seg_len > 0 && p.seg_len % kC == 0)) && encode_fn() != nullptr;
 }
 
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s) { return launch<false>(p, s); }
