@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN segmented fwd tokens/s at H32 K=V=128 T=32K bf16; % of roofline"
+VARLEN_METRIC = "GDN packed-sequence fwd tokens/s (lengths 1800,1500,2000,1200,800) at H16 K=V=128 bf16"
 DEFAULT_WORKLOAD = "cp4_b2_h32_t32k"
 L2_BYTES = 129 * 1024 * 1024
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -243,11 +244,178 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------
+def varlen_algorithmic(w, out_bytes: int = 4):
+    """Compulsory HBM bytes and dense-contraction flops of the packed-sequence forward: the WY
+    factors (an intermediate of this implementation) and the chunked forward of every sequence
+    (its partial last chunk counted as a whole chunk of work, its bytes by tokens)."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    K, V, H = w.K, w.V, w.H
+    tok_heads = w.T * H
+    chunks = H * sum((n + 63) // 64 for n in w.seq_lens)
+    states = len(w.seq_lens) * H * K * V * 4
+    fwd_tok = (2 * K + V) * isz + 2 * isz + V * out_bytes
+    fwd_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 64 * K * V * 2
+                 + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
+    return {
+        "wy": {"bytes": tok_heads * (K * isz + 2 * isz) + chunks * 16384,
+               "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64)},
+        "forward": {"bytes": tok_heads * fwd_tok + 2 * states, "flops": chunks * fwd_flops},
+    }
+
+
+def run_varlen(args):
+    """The packed-sequence forward (gdn_varlen_fwd) on a seq_lens workload; one step is one call
+    over the whole packed batch. Its inputs fit in L2, so a buffer larger than L2 is written
+    between timed steps and each step is timed by its own events."""
+    import torch
+
+    from context_scan_gb300 import gdn, synth
+
+    world, rank = init_dist("nccl" if args.gpus > 1 else "gloo")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w0 = synth.WORKLOADS[args.workload]
+    w = synth.scaled(w0, seed=w0.seed + rank_seed_offset(rank))
+    x = synth.make_inputs(w)
+    dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    names = ("q", "k", "v", "g", "beta")
+    host = {n: torch.from_numpy(x[n]).to(dt).pin_memory() for n in names}
+    host["h0"] = None if x["h0"] is None else torch.from_numpy(x["h0"]).pin_memory()
+    d = {n: (None if t is None else t.to(dev)) for n, t in host.items()}
+    cu = torch.from_numpy(synth.cu_seqlens(w)).to(dev)
+    nseq = len(w.seq_lens)
+    o = torch.empty((1, w.T, w.H, w.V), dtype=torch.float32, device=dev)
+    hf = torch.empty((nseq, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+    prob = gdn.problem(d["k"], d["v"], o)
+    ws = gdn.alloc_varlen_workspace(prob, nseq, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(events=None):
+        if events is None:
+            gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf, cu, ws,
+                               prob=prob, stream=stream)
+        else:
+            gdn.gdn_varlen_fwd_timed(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf,
+                                     cu, ws, events, prob=prob, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for e3 in ev:
+        for e in e3:
+            e.record(stream)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dev)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for i in range(K):
+        flush.fill_(1.0)   # outside the step's own events
+        step(ev[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
+    wy_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_s = sum(a + b for a, b in zip(wy_ms, fwd_ms)) / 1e3
+    max_s = reduce_max(step_s, device=dev if world > 1 else "cpu")
+    barrier(dev)
+    stages = varlen_algorithmic(w)
+    avg = {"wy": sum(wy_ms) / K, "forward": sum(fwd_ms) / K}
+    peaks, peaks_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ach = stages["forward"]["bytes"] / (avg["forward"] * 1e-3) / 1e9
+    t_roof = max(stages["forward"]["bytes"] / (hbm * 1e9),
+                 stages["forward"]["flops"] / (float(peaks["bf16_tflops"]) * 1e12))
+    ms_per_step = max_s / K * 1e3
+    value = aggregate(w.T, K, world, max_s)
+
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = max(3, min(K, args.e2e_steps))
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hf_host = torch.empty(hf.shape, dtype=hf.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+        d2h = o_host.numel() * 4 + hf_host.numel() * 4
+
+        def e2e_step():
+            for n, t in host.items():
+                if t is not None:
+                    d[n].copy_(t, non_blocking=True)
+            step()
+            o_host.copy_(o, non_blocking=True)
+            hf_host.copy_(hf, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_el = reduce_max(a.elapsed_time(b) / 1e3, device=dev if world > 1 else "cpu")
+        e2e = {"value": round(aggregate(w.T, n_e2e, world, e_el), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_varlen(w, x, budget_s=args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": VARLEN_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w0.name, "seq_lens": list(w.seq_lens), "B": 1, "H": w.H,
+                       "T": w.T, "K": w.K, "V": w.V, "chunk": 64, "in_dtype": w.in_dtype,
+                       "out_dtype": "f32", "state_dtype": "f32",
+                       "l2": "inputs fit in L2: a 258 MB buffer is written before every step, "
+                             "outside the step's events",
+                       "parallelism": f"weak: {world} rank(s) x one batch each"},
+            "roofline": {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(ach / hbm, 4),
+                         "traffic": recorded_traffic("gdn_varlen_forward", w0.name),
+                         "kernel": "gdn_varlen_forward", "kernel_ms": round(avg["forward"], 4),
+                         "algorithmic_bytes": stages["forward"]["bytes"],
+                         "peak_source": f"{peaks_src} hbm_gbs"},
+            "path_roofline": {"t_roof_us": round(t_roof * 1e6, 1),
+                              "frac": round(t_roof / (ms_per_step * 1e-3), 4),
+                              "bytes": stages["forward"]["bytes"],
+                              "flops": stages["forward"]["flops"],
+                              "peaks": f"{peaks_src}: hbm {hbm} GB/s, bf16 {peaks['bf16_tflops']} TF/s"},
+            "stage_ms": {k: round(v, 4) for k, v in avg.items()},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import numpy as np
     import torch
 
     from context_scan_gb300 import gdn, synth
+
+    if synth.WORKLOADS[args.workload].seq_lens is not None:
+        return run_varlen(args)
 
     world, rank = init_dist("nccl" if args.gpus > 1 else "gloo")
     _, _, local = dist_env()
@@ -435,6 +603,60 @@ def cpu_baseline(w, x, budget_s=12.0):
                       f"{w.nseg} segments; {secs:.1f} s; tokens/s scaled to the whole batch"}
 
 
+def cpu_baseline_varlen(w, x, budget_s=12.0):
+    import oracle
+    from context_scan_gb300 import synth
+    cores = oracle.num_threads(0)
+    cu = synth.cu_seqlens(w)
+    done, secs = 0, 0.0
+    while done < w.H and secs < budget_s:
+        h = done
+        xs = {n: x[n][:, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+        h0 = None if x["h0"] is None else x["h0"][:, h:h + 1]
+        t = time.perf_counter()
+        oracle.varlen_recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], cu, h0)
+        secs += time.perf_counter() - t
+        done += 1
+    value = w.T * done / w.H / secs
+    return {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {w.H} heads of {w.name}, every packed sequence, fp64 per-token "
+                      f"recurrence; {secs:.1f} s; tokens/s scaled to all heads"}
+
+
+def run_reference_varlen(args, w, x):
+    import oracle
+    from context_scan_gb300 import synth
+    cores = oracle.num_threads(0)
+    cu = synth.cu_seqlens(w)
+
+    def head(h):
+        xs = {n: x[n][:, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+        h0 = None if x["h0"] is None else x["h0"][:, h:h + 1]
+        t = time.perf_counter()
+        oracle.varlen_recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], cu, h0)
+        return time.perf_counter() - t
+
+    for i in range(args.warmup):
+        head(i % w.H)
+    secs = sum(head((args.warmup + i) % w.H) for i in range(args.steps))
+    value = w.T * args.steps / w.H / secs   # one step = one head of the packed batch
+    line = {
+        "impl": "reference", "metric": VARLEN_METRIC, "value": round(value, 1),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "seq_lens": list(w.seq_lens), "B": 1, "H": w.H,
+                   "T": w.T, "K": w.K, "V": w.V, "in_dtype": w.in_dtype},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step: one head of {w.name} (every packed sequence), "
+                                   f"fp64 per-token recurrence on {cores} host threads"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -443,6 +665,8 @@ def run_reference(args):
     import oracle
     w = synth.WORKLOADS[args.workload]
     x = synth.make_inputs(w)
+    if w.seq_lens is not None:
+        return run_reference_varlen(args, w, x)
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     cores = oracle.num_threads(0)
     for i in range(args.warmup):

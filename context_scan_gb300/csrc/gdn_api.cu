@@ -393,6 +393,15 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_seqlens,
                           const void* k, const void* v, const void* g, const void* beta,
                           const float* h0, void* o, float* h_final, void* workspace,
                           size_t workspace_bytes, void* stream) {
+    return gdn_varlen_fwd_timed(p, nseq, cu_seqlens, q, k, v, g, beta, h0, o, h_final, workspace,
+                                workspace_bytes, stream, nullptr);
+}
+
+gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_seqlens,
+                                const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, const float* h0, void* o, float* h_final,
+                                void* workspace, size_t workspace_bytes, void* stream,
+                                void* const* stage_events) {
     gdn_status st = check_varlen(p, nseq);
     if (st != GDN_OK) return st;
     if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
@@ -408,6 +417,7 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_seqlens,
     int* cu = reinterpret_cast<int*>(wsb + w.off_cu);
     int* cc = reinterpret_cast<int*>(wsb + w.off_cc);
     // the chains read the checked copy of the lengths, never the caller's array
+    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (gdn::launch_varlen_meta(cu_seqlens, nseq, p->T, cu, cc,
                                 reinterpret_cast<gdn::DeviceError*>(workspace), s) != cudaSuccess)
         return GDN_ERR_CUDA;
@@ -428,11 +438,12 @@ gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_seqlens,
     c.cu_chunks = cc;
     c.total_chunks = w.chunk_bound;
     c.wy = wsb + w.off_wy;
-    if (use_tc(c) && p->T >= gdn::kChunk) {   // (a tensor map box holds 64 tokens)
-        if (gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
-        return from_cuda(gdn::launch_tc_forward(c, s));
-    }
-    return from_cuda(gdn::launch_simt_forward(c, s));
+    const bool tc = use_tc(c) && p->T >= gdn::kChunk;   // (a tensor map box holds 64 tokens)
+    if (tc && gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if ((tc ? gdn::launch_tc_forward(c, s) : gdn::launch_simt_forward(c, s)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return from_cuda(mark(stage_events, 2, s));
 }
 
 const char* gdn_status_string(gdn_status s) {

@@ -20,7 +20,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
           6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
 EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
             "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
-            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd",
+            "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
             "gdn_status_string", "gdn_check_device_error")
 
 
@@ -64,12 +64,14 @@ def lib():
         L.gdn_varlen_workspace_bytes.argtypes = [pp, ctypes.c_int]
         L.gdn_varlen_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_varlen_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
+        L.gdn_varlen_fwd_timed.argtypes = ([pp, ctypes.c_int] + [_P] * 10 +
+                                           [ctypes.c_size_t, _P, _P])
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
-                   "gdn_varlen_fwd", "gdn_check_device_error"):
+                   "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -211,6 +213,22 @@ def gdn_varlen_fwd(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, stre
                                 _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
                                 _ptr(workspace), workspace.numel() if workspace is not None else 0,
                                 _stream(stream)), "gdn_varlen_fwd")
+
+
+def gdn_varlen_fwd_timed(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, events,
+                         stream=None, prob=None):
+    """gdn_varlen_fwd recording three torch.cuda.Event (enable_timing=True): before the length
+    check and the WY factors, before the chunked forward, after it."""
+    prob = prob or problem(k, v, o)
+    if len(events) != 3:
+        raise ValueError("gdn_varlen_fwd_timed takes three events")
+    arr = (_P * 3)(*[e.cuda_event for e in events])
+    nseq = int(cu_seqlens.numel()) - 1
+    _check(lib().gdn_varlen_fwd_timed(ctypes.byref(prob), nseq, _ptr(cu_seqlens), _ptr(q),
+                                      _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                                      _ptr(h_final), _ptr(workspace),
+                                      workspace.numel() if workspace is not None else 0,
+                                      _stream(stream), arr), "gdn_varlen_fwd_timed")
 
 
 def gdn_check_device_error(workspace, stream=None):

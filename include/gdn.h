@@ -238,6 +238,16 @@ GDN_API gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_
                                   const void* beta, const float* h0, void* o, float* h_final,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* gdn_varlen_fwd with stage markers: if stage_events is non-NULL it points to three
+ * cudaEvent_t recorded on `stream` before the length check and WY-factor launches, before
+ * the chunked forward, and after it. Same results as gdn_varlen_fwd. */
+GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_seqlens,
+                                        const void* q, const void* k, const void* v,
+                                        const void* g, const void* beta, const float* h0,
+                                        void* o, float* h_final, void* workspace,
+                                        size_t workspace_bytes, void* stream,
+                                        void* const* stage_events);
+
 /* Static, NUL-terminated description of a status code. */
 GDN_API const char* gdn_status_string(gdn_status s);
 
