@@ -73,9 +73,9 @@ struct Cfg {
     static constexpr int NGRP = SUMMARY ? 1 : 2;             // prep warp groups
     static constexpr int PREP_WARP0 = 4 * NSG;
     static constexpr int PREP_THREADS = 128 * NGRP;
-    // forward: one more warp issues the prep group's MMAs (P1, P2, P3)
-    static constexpr int MMA_WARP = SUMMARY ? -1 : 4 * NSG + 4 * NGRP;
-    static constexpr int PRODUCER_WARP = 4 * NSG + 4 * NGRP + (SUMMARY ? 0 : 1);
+    // one more warp issues the prep group's MMAs (P1 in the forward, P2, P3)
+    static constexpr int MMA_WARP = 4 * NSG + 4 * NGRP;
+    static constexpr int PRODUCER_WARP = MMA_WARP + 1;
     static constexpr int THREADS = 32 * PRODUCER_WARP + 32;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_S = 0;    // Q K^T, then W^T (prep)
@@ -355,14 +355,48 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             if (v_last >= 0) mbar_drain(bar0 + B_VFULL, v_last & 1, limit);
         }
-    } else if (!SUMMARY && warp == F::MMA_WARP) {
+    } else if (warp == F::MMA_WARP) {
         // ============================== prep MMA issue ============================
-        // The forward prep group's tensor-core work, issued from here so that no prep thread
-        // stalls behind an MMA issue. Per chunk n: P2 (U^T into the parity's U buffer, once
+        // The prep group's tensor-core work, issued from here so that no prep thread stalls
+        // behind an MMA issue. Forward, per chunk n: P2 (U^T into the parity's U buffer, once
         // chunk n-2 has retired it), P3 (W^T into TM_S, once the C warps have read Q K^T out of
         // it) and P1 of chunk n+1 ([Q ; -] K^T into TM_S, once the prep group has read W^T out
-        // of it). Lane 0 issues; every wait is bounded.
-        if (lane == 0 && nchunks > 0) {
+        // of it). Summary, per chunk n: P2 and P3 once the U buffer is retired and W^T of chunk
+        // n-1 has been read out. Lane 0 issues; every wait is bounded.
+        if (SUMMARY && lane == 0 && nchunks > 0) {
+            auto ok = [&](uint32_t bar, uint32_t parity, unsigned tag) {
+                return mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
+            };
+#pragma unroll 1
+            for (int n = 0; n < nchunks; ++n) {
+                const int as = n % AST;
+                const uint32_t kst = base + L::K0 + (n % KST) * 16384;
+                const uint32_t ast = base + L::A0 + as * 16384;
+                const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
+                const bool run =
+                    (n < NUB || ok(bar0 + B_UFREE + 8 * (n % NUB), ((n / NUB) - 1) & 1, TAG_UFREE)) &&
+                    (n == 0 || ok(bar0 + B_WREAD, (n - 1) & 1, TAG_WREAD)) &&
+                    ok(bar0 + B_KFULL + 8 * (n % KST), (n / KST) & 1, TAG_KFULL) &&
+                    ok(bar0 + B_AFULL + 8 * as, (n / AST) & 1, TAG_AFULL) &&
+                    ok(bar0 + B_VFULL, n & 1, TAG_VFULL);
+                if (!run) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
+                                   desc_k(ast + k16 * 32), k16 > 0);
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
+                                   desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                mma_commit(bar0 + B_VEMPTY);
+                mma_commit(bar0 + B_AEMPTY + 8 * as);
+                mma_commit(bar0 + B_BARP);
+            }
+            mma_commit(bar0 + B_MDRAIN);
+            mbar_drain(bar0 + B_MDRAIN, 0, limit);
+        }
+        if (!SUMMARY && lane == 0 && nchunks > 0) {
             auto ok = [&](uint32_t bar, uint32_t parity, unsigned tag) {
                 return mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
             };
@@ -589,31 +623,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 barp_phase ^= 1u;   // P1's phase, consumed by the C warps
                 fence_proxy_async();   // sigma Qd and C are read by the state group's MMAs
                 barp_pending = true;
-            } else {
-                // ---- summary: P2 (U^T, S part only) and P3 (W^T into TM_S); only the issuing
-                //      thread waits for the k, WY and v tiles
-                if (pt == 0 &&
-                    mbar_wait(bar0 + B_KFULL + 8 * ks, (n / KST) & 1, abort_flag, limit, c.err, TAG_KFULL) &&
-                    mbar_wait(bar0 + B_AFULL + 8 * as, (n / AST) & 1, abort_flag, limit, c.err, TAG_AFULL) &&
-                    (!need_v || mbar_wait(bar0 + B_VFULL, n & 1, abort_flag, limit, c.err, TAG_VFULL))) {
-                    tc_fence_after();
-                    if (need_v) {
-#pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16)
-                            mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                           desc_k(ast + k16 * 32), k16 > 0);
-                    }
-#pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16)
-                        mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
-                                       desc_k(ast + 8192 + k16 * 32), k16 > 0);
-                    if (need_v) mma_commit(bar0 + B_VEMPTY);
-                    mma_commit(bar0 + B_AEMPTY + 8 * as);
-                    mma_commit(bar0 + B_BARP);
-                }
-                __syncwarp();
-                barp_pending = true;
             }
+            // (the summary's P2 and P3 are the MMA warp's)
             if (!pmma_wait()) break;   // P3 (and P2) done; for the forward also every C and Qd
             tc_fence_after();
             // ---- -sigma W as rows 0..63 of the S12 B operand, once chunk n-1's S12 retired
@@ -649,16 +660,13 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             //      (P1 and sigma Qd) and TM_S is free again for the MMA warp's next P1
             if (pt == 0) {
                 mbar_arrive(bar0 + B_PREPDONE);
-                if (!SUMMARY) {
-                    mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
-                    mbar_arrive(bar0 + B_WREAD);
-                }
+                if (!SUMMARY) mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
+                mbar_arrive(bar0 + B_WREAD);
             }
         }
 #undef epilogue
         if (*go == 0) {
-            // (the forward's prep MMAs are the MMA warp's, which lets them retire itself)
-            if (SUMMARY && barp_pending && pt == 0) mbar_drain(bar0 + B_BARP, barp_phase, limit);
+            // (the prep MMAs are the MMA warp's, which lets them retire itself)
         } else if (!SUMMARY) {
             // ---- output rows of the last two chunks
 #pragma unroll 1
