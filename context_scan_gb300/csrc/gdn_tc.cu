@@ -795,11 +795,13 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     uint32_t hi[8], lo[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float x0 = r[2 * j] * dd[16 * g + 2 * j];
-                        const float x1 = r[2 * j + 1] * dd[16 * g + 2 * j + 1];
-                        const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-                        const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-                        hi[j] = pack_bf16(h0, h1);
+                        const float2 d2 = *reinterpret_cast<const float2*>(dd + 16 * g + 2 * j);
+                        const float x0 = r[2 * j] * d2.x;
+                        const float x1 = r[2 * j + 1] * d2.y;
+                        // both halves rounded in one conversion, then unpacked exactly
+                        hi[j] = pack_bf16(x0, x1);
+                        const float h0 = __uint_as_float(hi[j] << 16);
+                        const float h1 = __uint_as_float(hi[j] & 0xFFFF0000u);
                         lo[j] = pack_bf16(x0 - h0, x1 - h1);
                     }
                     // (in the summary this overwrites the 16 columns just read)
