@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj) {
                                 const int j = 32 * grp + 16 * hh + jj;
-                                t[jj] = tf32_bits((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
+                                t[jj] = tf32_operand((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
                             }
                             // columns 32 grp + 16 hh ..: tf32 block grp, 16-byte chunks 4 hh ..
 #pragma unroll
@@ -603,15 +603,15 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                         for (int cc = 0; cc < 8; ++cc) {
                             const uint4 u = *reinterpret_cast<const uint4*>(src + sw128(i, cc));
                             const uint4 lo4 = make_uint4(
-                                tf32_bits(__uint_as_float(u.x << 16) * egi),
-                                tf32_bits(__uint_as_float(u.x & 0xFFFF0000u) * egi),
-                                tf32_bits(__uint_as_float(u.y << 16) * egi),
-                                tf32_bits(__uint_as_float(u.y & 0xFFFF0000u) * egi));
+                                tf32_operand(__uint_as_float(u.x << 16) * egi),
+                                tf32_operand(__uint_as_float(u.x & 0xFFFF0000u) * egi),
+                                tf32_operand(__uint_as_float(u.y << 16) * egi),
+                                tf32_operand(__uint_as_float(u.y & 0xFFFF0000u) * egi));
                             const uint4 hi4 = make_uint4(
-                                tf32_bits(__uint_as_float(u.z << 16) * egi),
-                                tf32_bits(__uint_as_float(u.z & 0xFFFF0000u) * egi),
-                                tf32_bits(__uint_as_float(u.w << 16) * egi),
-                                tf32_bits(__uint_as_float(u.w & 0xFFFF0000u) * egi));
+                                tf32_operand(__uint_as_float(u.z << 16) * egi),
+                                tf32_operand(__uint_as_float(u.z & 0xFFFF0000u) * egi),
+                                tf32_operand(__uint_as_float(u.w << 16) * egi),
+                                tf32_operand(__uint_as_float(u.w & 0xFFFF0000u) * egi));
                             // features 64 kh + 8 cc .. +7: kblock 2 kh + cc / 4 (rows 64.. of the
                             // S12 operand), chunks 2 (cc % 4) + {0, 1}
                             uint8_t* dst = sm + L::W + (kh * 2 + (cc >> 2)) * L::WQ_KB + 8192;
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                         for (int ii = 0; ii < 16; ++ii)
                             *reinterpret_cast<uint32_t*>(
                                 col + sw128(ECOLS * grp + hb + 16 * hh + ii, qk)) =
-                                tf32_bits(nsig * w[ii]);
+                                tf32_operand(nsig * w[ii]);
                     }
                 }
             }

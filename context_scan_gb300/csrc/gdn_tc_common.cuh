@@ -161,6 +161,12 @@ __device__ __forceinline__ uint32_t tf32_bits(float x) {
     return y;
 }
 
+// A tf32 MMA operand rounded to nearest (ties away from zero) with one integer add: adding
+// half a tf32 unit (bit 12) to the sign-magnitude fp32 pattern carries into the 19 bits the
+// MMA reads, and the MMA ignores the low 13 bits, so they need no clearing. Same rounding as
+// cvt.rna.tf32.f32, on the integer pipe instead of the conversion pipe.
+__device__ __forceinline__ uint32_t tf32_operand(float x) { return __float_as_uint(x) + 0x1000u; }
+
 // Shared-memory matrix descriptor (sm_100 format): start, leading/stride byte offsets,
 // version 1, 128-byte swizzle.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
