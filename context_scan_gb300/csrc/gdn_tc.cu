@@ -798,11 +798,14 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                         const float2 d2 = *reinterpret_cast<const float2*>(dd + 16 * g + 2 * j);
                         const float x0 = r[2 * j] * d2.x;
                         const float x1 = r[2 * j + 1] * d2.y;
-                        // both halves rounded in one conversion, then unpacked exactly
-                        hi[j] = pack_bf16(x0, x1);
-                        const float h0 = __uint_as_float(hi[j] << 16);
-                        const float h1 = __uint_as_float(hi[j] & 0xFFFF0000u);
-                        lo[j] = pack_bf16(x0 - h0, x1 - h1);
+                        // hi = x truncated to bf16 (its top 16 bits), lo = the exact remainder
+                        // truncated to bf16: hi + lo is within 2^-16 |x| of x. Integer and
+                        // byte-permute operations only, no conversions.
+                        const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+                        hi[j] = __byte_perm(b0, b1, 0x7632);
+                        const float l0 = x0 - __uint_as_float(b0 & 0xFFFF0000u);
+                        const float l1 = x1 - __uint_as_float(b1 & 0xFFFF0000u);
+                        lo[j] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
                     }
                     // (in the summary this overwrites the 16 columns just read)
                     tmem_st8(t_row + rd_col + 16 * g, hi);
