@@ -147,6 +147,7 @@ struct TcParams {
 
 // 32 token rows of one output column from a 64-column O^T buffer in tensor memory; rows from
 // `valid` on (past the end of a varlen sequence) are not stored
+template <bool OUT_BF16>
 __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_col, long long idx0,
                                                long long tok_stride, int valid) {
     float ov2[2][16];
@@ -157,7 +158,7 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
     for (int g = 0; g < 2; ++g) {
         const float* ov = ov2[g];
         const long long base = idx0 + (long long)(16 * g) * tok_stride;
-        if (c.out_bf16) {
+        if (OUT_BF16) {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(c.o) + base;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -178,7 +179,7 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
 // registers per thread.
 // VARLEN: the chains are the packed sequences of c.cu_seqlens (forward only); the
 // fixed-length instance has none of the end-of-sequence checks.
-template <bool SUMMARY, bool VARLEN>
+template <bool SUMMARY, bool VARLEN, bool OUT_BF16>
 __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant__ TcParams p) {
     using L = Smem<SUMMARY>;
     using F = Cfg<SUMMARY>;
@@ -480,7 +481,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                  0) != 0)
 // output rows of chunk m from its O^T buffer: lanes v, this warp group's 32 token columns
 #define store_output(m)                                                                       \
-    store_o_rows32(c, t_row + TM_U + ((m) & 1) * 128 + 64 + 32 * grp,                          \
+    store_o_rows32<OUT_BF16>(c, t_row + TM_U + ((m) & 1) * 128 + 64 + 32 * grp,                \
                    ((row_seg + (long long)(m) * kC + 32 * grp) * c.H + h) * kD + 32 * lq + lane, \
                    tok_stride, VARLEN ? seq_tokens - ((m) * kC + 32 * grp) : 32)
 
@@ -908,7 +909,14 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
     if (!make_map(&tp.tm_k, c.k, c)) return cudaErrorInvalidValue;
     if (!SUMMARY && !make_map(&tp.tm_q, c.q, c)) return cudaErrorInvalidValue;
     if (!make_map(&tp.tm_v, c.v, c)) return cudaErrorInvalidValue;
-    auto kern = c.cu_seqlens ? tc_chain_kernel<SUMMARY, !SUMMARY> : tc_chain_kernel<SUMMARY, false>;
+    // one instance per output type and packing, so that each carries only its own store path
+    void (*kern)(TcParams) = tc_chain_kernel<SUMMARY, false, false>;
+    if constexpr (!SUMMARY) {
+        if (c.cu_seqlens)
+            kern = c.out_bf16 ? tc_chain_kernel<false, true, true> : tc_chain_kernel<false, true, false>;
+        else if (c.out_bf16)
+            kern = tc_chain_kernel<false, false, true>;
+    }
     constexpr uint32_t bytes = Smem<SUMMARY>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
