@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
                     v[e] = (j + e < i) ? bi * ex2(gxi - G[j + e]) * kk[j4 + e] : 0.f;
                 if ((j >> 4) < I) {
                     *reinterpret_cast<uint4*>(Lt + i * LS + j) =
-                        make_uint4(tf32_bits(v[0]), tf32_bits(v[1]), tf32_bits(v[2]), tf32_bits(v[3]));
+                        make_uint4(tf32_operand(v[0]), tf32_operand(v[1]), tf32_operand(v[2]), tf32_operand(v[3]));
                 } else if ((j >> 4) == I) {
                     float* ld = Ld + I * 16 * DS + (i & 15) * DS + (j & 15);
                     ld[0] = v[0];
@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
         __syncthreads();   // every warp is done with Ld, which X overwrites
         const int row = bs + r, c0 = bs + 8 * half;
         uint4* xs = reinterpret_cast<uint4*>(X + row * XS + c0);
-        xs[0] = make_uint4(tf32_bits(x[0]), tf32_bits(x[1]), tf32_bits(x[2]), tf32_bits(x[3]));
-        xs[1] = make_uint4(tf32_bits(x[4]), tf32_bits(x[5]), tf32_bits(x[6]), tf32_bits(x[7]));
+        xs[0] = make_uint4(tf32_operand(x[0]), tf32_operand(x[1]), tf32_operand(x[2]), tf32_operand(x[3]));
+        xs[1] = make_uint4(tf32_operand(x[4]), tf32_operand(x[5]), tf32_operand(x[6]), tf32_operand(x[7]));
         // output: this row's 8 columns of the diagonal block, scaled, as one 16-byte chunk per
         // tile; and the row's chunks above the diagonal block as zeros (split between halves)
         *out_chunk(out_b, row, c0 >> 3) =
@@ -320,14 +320,14 @@ __global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant
             for (int kk = 0; kk < 2; ++kk) {
                 const uint32_t* xa = X + (16 * I + gq) * XS + 16 * I + 8 * kk + tq;
                 const uint32_t a[4] = {xa[0], xa[8 * XS], xa[4], xa[8 * XS + 4]};
-                const uint32_t bb[2] = {tf32_bits(Ys[(8 * kk + tq) * 8 + gq]),
-                                        tf32_bits(Ys[(8 * kk + tq + 4) * 8 + gq])};
+                const uint32_t bb[2] = {tf32_operand(Ys[(8 * kk + tq) * 8 + gq]),
+                                        tf32_operand(Ys[(8 * kk + tq + 4) * 8 + gq])};
                 mma_m16n8k8(xo, a, bb);
             }
             const int r0 = 16 * I + gq, c0 = n0 + 2 * tq;
-            *reinterpret_cast<uint2*>(X + r0 * XS + c0) = make_uint2(tf32_bits(-xo[0]), tf32_bits(-xo[1]));
+            *reinterpret_cast<uint2*>(X + r0 * XS + c0) = make_uint2(tf32_operand(-xo[0]), tf32_operand(-xo[1]));
             *reinterpret_cast<uint2*>(X + (r0 + 8) * XS + c0) =
-                make_uint2(tf32_bits(-xo[2]), tf32_bits(-xo[3]));
+                make_uint2(tf32_operand(-xo[2]), tf32_operand(-xo[3]));
             __syncwarp();   // the next block down reads this one (and Ys is reused)
             // bf16 pairs (columns c0, c0 + 1) of rows r0 and r0 + 8: byte 4 tq of chunk n0 / 8
             const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = bekr[c0], e1 = bekr[c0 + 1];
