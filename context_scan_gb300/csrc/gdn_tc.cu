@@ -128,7 +128,7 @@ constexpr uint32_t B_KFULL = 0, B_KEMPTY = 32, B_QFULL = 64, B_QEMPTY = 80, B_AF
                    B_AEMPTY = 112, B_VFULL = 128, B_VEMPTY = 136, B_BARP = 144, B_BARS = 152,
                    B_PREPDONE = 160, B_WFREE = 168, B_UFREE = 176, B_TMEM = 192, B_ABORT = 196,
                    B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216, B_CDONE = 224,
-                   B_WREAD = 232, B_MDRAIN = 240;
+                   B_WREAD = 232, B_MDRAIN = 240, B_SDRAIN = 248;
 
 // wait tags recorded in the device error word's detail field
 enum : unsigned {
@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         mbar_init(bar0 + B_CDONE, 1);
         mbar_init(bar0 + B_WREAD, 1);
         mbar_init(bar0 + B_MDRAIN, 1);
+        mbar_init(bar0 + B_SDRAIN, NSG);   // each state group's last MMAs
         *abort_flag = 0;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S) = 1;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S1) = 1;
@@ -693,6 +694,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         const bool m_part = SUMMARY && sg == 0;       // starts from I, no values
         uint32_t bars_phase = 0;
         bool bars_pending = false;
+        uint32_t s4_parity = 0;    // bar_s phase of the last S4 (issuing thread)
+        bool s4_pending = false;
         const long long bhoff = (long long)bh * kD * kD;
         float sig_next = 1.f;   // sigma after the last completed chunk
 
@@ -741,9 +744,14 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             const uint32_t t_o = t_u + 64;   // forward only
             const float* sc = scal + (n & 1) * (SC_N * 64);
             if (!swait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE)) break;
+            // the previous chunk's S4 has updated H_s (the issuing thread waits; if it gives up
+            // it raises the abort flag, issues nothing, and the group stops at its next wait)
+            const bool s4_ok = st != 0 || !s4_pending ||
+                               mbar_wait(bar_s, s4_parity, abort_flag, limit, c.err, TAG_BARS);
+            s4_pending = false;
             // ---- S12: [R^T | O^T] = [U^T | 0] + H_s^T [-sigma W ; sigma Qd]^T (forward);
             //      the summary forms only R^T = U^T + H_s^T (-sigma W)^T (no U in the M part)
-            if (st == 0) {
+            if (st == 0 && s4_ok) {
                 tc_fence_after();
                 if (!SUMMARY) {
 #pragma unroll
@@ -829,7 +837,9 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             tc_fence_before();
             sbar();
-            // ---- S4: H_s^T += (R^T D) K (A = hi, lo in TMEM); its commits also cover S3
+            // ---- S4: H_s^T += (R^T D) K (A = hi, lo in TMEM); its commits also cover S3. Only
+            //      the issuing thread waits for it, just before it issues the next chunk's S12
+            //      (which reads H_s); the rest of the group goes on to the next chunk.
             if (st == 0) {
                 tc_fence_after();
 #pragma unroll
@@ -843,16 +853,21 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 mma_commit(bar_s);
             }
             __syncwarp();
-            bars_pending = true;
-            if (!smma_wait()) break;
-            tc_fence_after();
+            s4_parity = bars_phase;   // the phase S4 completes
+            s4_pending = true;
+            bars_phase ^= 1u;
             done = n + 1;
         }
 
-        if (*go == 0) {
-            if (bars_pending && st == 0)   // let an issued MMA group retire before TMEM is freed
-                mbar_drain(bar_s, bars_phase, limit);
+        // every MMA this group issued (the last S4) completes before the final state is read
+        // out or tensor memory is released
+        if (st == 0) mma_commit(bar0 + B_SDRAIN);
+        __syncwarp();
+        const bool drained = *go != 0 && swait(bar0 + B_SDRAIN, 0, TAG_BARS);
+        if (!drained) {
+            if (st == 0) mbar_drain(bar0 + B_SDRAIN, 0, limit);
         } else {
+            tc_fence_after();
             // ---- the chain's final state H = sigma H_s: thread v writes column v of H
             float* dst = nullptr;
             if (SUMMARY) {
