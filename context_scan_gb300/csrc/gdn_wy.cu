@@ -23,7 +23,7 @@
 // (68 and 72 words per row), so a fragment is two or four shared loads at constant offsets
 // without bank conflicts; the diagonal blocks of L stay fp32 for the substitution. Each block
 // of the inverse is scaled and written to global memory as bf16 as soon as it is final (blocks
-// above the diagonal as zeros). Five CTAs share an SM (64 tensor-memory columns each) and hide
+// above the diagonal as zeros). Six CTAs share an SM (64 tensor-memory columns each) and hide
 // each other's latencies; the two waits (the tile, K K^T) are bounded.
 #include <cstring>
 
@@ -39,19 +39,22 @@ constexpr int LS = 68;   // row pitch (words) of the tf32 off-diagonal blocks of
 constexpr int XS = 72;   // row pitch (words) of the tf32 inverse X
 constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
 
-// shared-memory map (bytes from a 1024-aligned base)
+// shared-memory map (bytes from a 1024-aligned base). Rows 0..15 of L are never used (the
+// first block row has nothing below the diagonal), so the scratch, the scalars and the
+// barriers live there; 36 KB per CTA lets six CTAs share an SM.
 constexpr uint32_t WY_K = 8192;     // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle
-constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS) once K K^T is in tensor memory
+constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS, rows 16..63) once K K^T is in TMEM
 constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
 constexpr uint32_t WY_LD = WY_X;    // diagonal blocks of L (fp32, 4 x 16 x DS), dead before X
-constexpr uint32_t WY_Y = 35840;    // per-warp 16 x 8 fp32 scratch of the block rounds
-constexpr uint32_t WY_SC = 37888;   // Gx, G, beta, beta 2^Gx: [4][64] fp32
-constexpr uint32_t WY_BAR = 38912;  // mbarriers (tile, K K^T), tensor-memory address
-constexpr uint32_t WY_END = 38976;
+constexpr uint32_t WY_Y = 0;        // per-warp 16 x 8 fp32 scratch of the block rounds
+constexpr uint32_t WY_SC = 2048;    // Gx, G, beta, beta 2^Gx: [4][64] fp32
+constexpr uint32_t WY_BAR = 3072;   // mbarriers (tile, K K^T), tensor-memory address
+constexpr uint32_t WY_END = 35840;
 constexpr uint32_t kWySmem = WY_END + 1024;   // + alignment slack
 constexpr uint32_t kWyTmemCols = 64;
 constexpr uint32_t ID_KK = idesc_bf16(128, 32, false, false);   // K K^T, 32 columns per group
-static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_Y - WY_X, "layout");
+static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_END - WY_X, "layout");
+static_assert(WY_BAR + 64 <= 16 * LS * 4, "scratch, scalars and barriers fit in L's unused rows");
 
 struct WyParams {
     CUtensorMap tm_k;
@@ -75,7 +78,7 @@ __device__ __forceinline__ uint4* out_chunk(uint8_t* tile, int row, int c) {
 // wait tags recorded in the device error word's detail field
 enum : unsigned { WTAG_TILE = 101, WTAG_KK = 102 };
 
-__global__ void __launch_bounds__(kWyThreads, 5) wy_kernel(const __grid_constant__ WyParams p) {
+__global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant__ WyParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
