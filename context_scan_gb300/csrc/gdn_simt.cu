@@ -371,6 +371,8 @@ scan_kernel(const float* __restrict__ M, const float* __restrict__ S,
         if (p == P - 1 || !M) continue;   // no summaries: every piece starts from the same state
         const float* Mg = M + ((long long)p * BH + bh) * KD * KD;
         const float* Sg = S + ((long long)p * BH + bh) * KD * V;
+        // all of this thread's loads of M in flight at once (the trip count is a constant)
+#pragma unroll
         for (int e = tid; e < KD * KD / 4; e += NT) {
             const int i = e / (KD / 4), l4 = e % (KD / 4);
             *reinterpret_cast<float4*>(Ms + i * MP + 4 * l4) =
