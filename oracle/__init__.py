@@ -19,6 +19,10 @@ What each function computes (pages cited by title and section):
   varlen_recurrence -- packed variable-length sequences ("KDA Chunk Backward -- TPU/Pallas
                      Kernel Design", section 3.8): each sequence of the packed token axis
                      runs the recurrence alone from its own initial state.
+  kda_recurrence / kda_summary -- per-channel gates ("KDA Chunk Backward -- TPU/Pallas Kernel
+                     Design", section 1.2): g is [B,T,H,K] and the state decays row by row,
+                     diag(exp(g_t)); written apart from the scalar-gate functions, which
+                     it must reproduce when every channel carries the same gate.
   chunked_fwd / chunked_summary -- the chunk equations of "Context Parallelism in ART",
                      section 08 "First parallelize within a GPU", restated for the RFC's
                      un-decayed read; used only to pin chunked == per-token.
@@ -65,10 +69,13 @@ def _load():
         lib.oracle_scan.argtypes = [_I] * 4 + [_P] * 4
         lib.oracle_chunked_fwd.argtypes = [_I] * 6 + [_P] * 8 + [_I, _I]
         lib.oracle_chunked_summary.argtypes = [_I] * 7 + [_P] * 6 + [_I, _I]
+        lib.oracle_kda_recurrence.argtypes = [_I] * 6 + [_P] * 9 + [_I, _I, _I]
+        lib.oracle_kda_summary.argtypes = [_I] * 6 + [_P] * 6 + [_I, _I]
         lib.oracle_num_threads.argtypes = [_I]
         lib.oracle_num_threads.restype = _I
         for fn in ("oracle_recurrence", "oracle_summary", "oracle_compose", "oracle_scan",
-                   "oracle_chunked_fwd", "oracle_chunked_summary"):
+                   "oracle_chunked_fwd", "oracle_chunked_summary", "oracle_kda_recurrence",
+                   "oracle_kda_summary"):
             getattr(lib, fn).restype = None
         _lib = lib
     return _lib
@@ -113,6 +120,36 @@ def recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
     return o, hf, H_in
 
 
+def kda_recurrence(q, k, v, g, beta, h0=None, seg_len: int = 0, col_block: int = 0,
+                   nthreads: int = 0, want_o: bool = True, decay_first: bool = False):
+    """Per-token recurrence with per-channel gates g [B,T,H,K]. Returns (o [B,T,H,V],
+    h_final [B,H,K,V], H_in [T//seg_len,B,H,K,V] or None)."""
+    q, k, v, g, beta, h0 = map(_f32, (q, k, v, g, beta, h0))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    assert g.shape == (B, T, H, K)
+    o = np.empty((B, T, H, V), np.float64) if want_o else None
+    hf = np.empty((B, H, K, V), np.float64)
+    H_in = np.empty((T // seg_len, B, H, K, V), np.float64) if seg_len > 0 else None
+    _load().oracle_kda_recurrence(B, T, H, K, V, seg_len, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                  _ptr(beta), _ptr(h0), _ptr(o), _ptr(hf), _ptr(H_in),
+                                  col_block, nthreads, int(decay_first))
+    return o, hf, H_in
+
+
+def kda_summary(k, v, g, beta, nseg: int, nthreads: int = 0, decay_first: bool = False):
+    """Per-segment summaries (M [nseg,B,H,K,K], S [nseg,B,H,K,V]) with per-channel gates."""
+    k, v, g, beta = map(_f32, (k, v, g, beta))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    assert g.shape == (B, T, H, K) and T % nseg == 0
+    M = np.empty((nseg, B, H, K, K), np.float64)
+    S = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_kda_summary(B, T, H, K, V, nseg, _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(M), _ptr(S), nthreads, int(decay_first))
+    return M, S
+
+
 def varlen_recurrence(q, k, v, g, beta, cu_seqlens, h0=None, nthreads: int = 0,
                       decay_first: bool = False):
     """Packed sequences: q, k, v, g, beta hold [1, T, H, *]; sequence s is tokens
@@ -128,8 +165,9 @@ def varlen_recurrence(q, k, v, g, beta, cu_seqlens, h0=None, nthreads: int = 0,
     for s in range(nseq):
         a, b = cu[s], cu[s + 1]
         h0_s = None if h0 is None else np.asarray(h0)[s:s + 1]
-        o_s, hf_s, _ = recurrence(*(np.asarray(x)[:, a:b] for x in (q, k, v, g, beta)), h0_s,
-                                  nthreads=nthreads, decay_first=decay_first)
+        rec = kda_recurrence if np.ndim(g) == 4 else recurrence
+        o_s, hf_s, _ = rec(*(np.asarray(x)[:, a:b] for x in (q, k, v, g, beta)), h0_s,
+                           nthreads=nthreads, decay_first=decay_first)
         o[:, a:b] = o_s
         hf[s] = hf_s[0]
     return o, hf

@@ -509,3 +509,152 @@ void oracle_chunked_summary(int B, int T, int H, int K, int V, int chunk, int ns
     chk_ctx c = {B, T, H, K, V, chunk, nseg, NULL, k, v, g, beta, NULL, NULL, NULL, M, S, decay_first};
     run_units(chk_sum_unit, &c, (long)B * H * nseg, nthreads);
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* 5. Per-channel gates ([KDA] "KDA Chunk Backward -- TPU/Pallas Kernel Design", section */
+/* 1.2: the state decays row by row, 2^(g) with g in R^K per token). With a = exp(g_t)   */
+/* per key channel, one token does                                                        */
+/*   read before the decay:  r = beta (v - H^T k),    H <- diag(a) H + k r^T             */
+/*   decayed read (flag):    H' = diag(a) H, r = beta (v - H'^T k),  H <- H' + k r^T    */
+/* and o_t = H_t^T q_t. Written on its own, not through the scalar-gate code above: with */
+/* equal channels it must reproduce that code (a pin), so it may not share it.            */
+/* Gate layout: g [B, T, H, K].                                                           */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V, seg_len, col_block;
+    const float *q, *k, *v, *g, *beta, *h0;
+    double *o, *h_final, *H_in;
+    int decay_first;
+} kda_ctx;
+
+static void kda_rec_unit(void* vctx, long unit) {
+    const kda_ctx* c = (const kda_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T, cb = c->col_block;
+    const long nblk = (V + cb - 1) / cb;
+    const int blk = (int)(unit % nblk);
+    const long bh = unit / nblk;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const int v0 = blk * cb, v1 = (v0 + cb < V) ? v0 + cb : V, w = v1 - v0;
+    double* St = (double*)malloc(sizeof(double) * (size_t)K * w);   /* state columns v0..v1 */
+    double* r = (double*)malloc(sizeof(double) * (size_t)w);
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < w; ++j)
+            St[(size_t)i * w + j] =
+                c->h0 ? (double)c->h0[(((size_t)b * H + h) * K + i) * V + v0 + j] : 0.0;
+    for (int t = 0; t < T; ++t) {
+        if (c->H_in && c->seg_len > 0 && t % c->seg_len == 0) {
+            const int s = t / c->seg_len;
+            for (int i = 0; i < K; ++i)
+                for (int j = 0; j < w; ++j)
+                    c->H_in[((((size_t)s * c->B + b) * H + h) * K + i) * V + v0 + j] =
+                        St[(size_t)i * w + j];
+        }
+        const size_t row = ((size_t)b * T + t) * H + h;
+        const float* kt = c->k + row * K;
+        const float* gt = c->g + row * K;
+        const double bt = (double)c->beta[row];
+        if (c->decay_first)   /* decay every row of the state before the read */
+            for (int i = 0; i < K; ++i) {
+                const double a = exp((double)gt[i]);
+                for (int j = 0; j < w; ++j) St[(size_t)i * w + j] *= a;
+            }
+        for (int j = 0; j < w; ++j) {   /* r = beta (v - H^T k) */
+            double acc = 0.0;
+            for (int i = 0; i < K; ++i) acc += (double)kt[i] * St[(size_t)i * w + j];
+            r[j] = bt * ((double)c->v[row * V + v0 + j] - acc);
+        }
+        for (int i = 0; i < K; ++i) {
+            const double a = c->decay_first ? 1.0 : exp((double)gt[i]);
+            for (int j = 0; j < w; ++j)
+                St[(size_t)i * w + j] = a * St[(size_t)i * w + j] + (double)kt[i] * r[j];
+        }
+        if (c->o)
+            for (int j = 0; j < w; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < K; ++i) acc += (double)c->q[row * K + i] * St[(size_t)i * w + j];
+                c->o[row * V + v0 + j] = acc;
+            }
+    }
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < w; ++j)
+            c->h_final[(((size_t)b * H + h) * K + i) * V + v0 + j] = St[(size_t)i * w + j];
+    free(St);
+    free(r);
+}
+
+void oracle_kda_recurrence(int B, int T, int H, int K, int V, int seg_len, const float* q,
+                           const float* k, const float* v, const float* g, const float* beta,
+                           const float* h0, double* o, double* h_final, double* H_in,
+                           int col_block, int nthreads, int decay_first) {
+    kda_ctx c = {B, T, H, K, V, seg_len, col_block > 0 ? col_block : V,
+                 q, k, v, g, beta, h0, o, h_final, H_in, decay_first};
+    const long nblk = (V + c.col_block - 1) / c.col_block;
+    run_units(kda_rec_unit, &c, (long)B * H * nblk, nthreads);
+}
+
+/* Per-segment summaries with per-channel gates: H_out = M H_in + S over a segment. One   */
+/* token maps H to T_t H + beta k v^T with T_t = diag(a) - beta k k^T (read before the    */
+/* decay) or (I - beta k k^T) diag(a) (decayed read); M is the product of the T_t from I, */
+/* S the state reached from 0.                                                             */
+typedef struct {
+    int B, T, H, K, V, nseg;
+    const float *k, *v, *g, *beta;
+    double *M, *S;
+    int decay_first;
+} kda_sum_ctx;
+
+/* X (K x n) <- T_t X + beta k u^T for one token, u = v (S) or 0 (M) */
+static void kda_apply(int K, int n, double* X, const double* a, const double* kt, double bt,
+                      const float* vrow, int decay_first, double* y) {
+    if (decay_first)
+        for (int i = 0; i < K; ++i)
+            for (int j = 0; j < n; ++j) X[(size_t)i * n + j] *= a[i];
+    for (int j = 0; j < n; ++j) {   /* y = k^T X (X already decayed when the read is) */
+        double acc = 0.0;
+        for (int i = 0; i < K; ++i) acc += kt[i] * X[(size_t)i * n + j];
+        y[j] = acc;
+    }
+    for (int i = 0; i < K; ++i) {
+        const double ai = decay_first ? 1.0 : a[i];
+        for (int j = 0; j < n; ++j)
+            X[(size_t)i * n + j] = ai * X[(size_t)i * n + j] - bt * kt[i] * y[j] +
+                                   (vrow ? bt * kt[i] * (double)vrow[j] : 0.0);
+    }
+}
+
+static void kda_sum_unit(void* vctx, long unit) {
+    const kda_sum_ctx* c = (const kda_sum_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T;
+    const int seg_len = T / c->nseg;
+    const int s = (int)(unit % c->nseg);
+    const long bh = unit / c->nseg;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    double* M = c->M + (((size_t)s * c->B + b) * H + h) * (size_t)K * K;
+    double* S = c->S + (((size_t)s * c->B + b) * H + h) * (size_t)K * V;
+    double* a = (double*)malloc(sizeof(double) * (size_t)K);
+    double* kt = (double*)malloc(sizeof(double) * (size_t)K);
+    double* y = (double*)malloc(sizeof(double) * (size_t)(K > V ? K : V));
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < K; ++j) M[(size_t)i * K + j] = (i == j) ? 1.0 : 0.0;
+    for (size_t i = 0; i < (size_t)K * V; ++i) S[i] = 0.0;
+    for (int t = s * seg_len; t < (s + 1) * seg_len; ++t) {
+        const size_t row = ((size_t)b * T + t) * H + h;
+        for (int i = 0; i < K; ++i) {
+            a[i] = exp((double)c->g[row * K + i]);
+            kt[i] = (double)c->k[row * K + i];
+        }
+        const double bt = (double)c->beta[row];
+        kda_apply(K, K, M, a, kt, bt, NULL, c->decay_first, y);
+        kda_apply(K, V, S, a, kt, bt, c->v + row * V, c->decay_first, y);
+    }
+    free(a);
+    free(kt);
+    free(y);
+}
+
+void oracle_kda_summary(int B, int T, int H, int K, int V, int nseg, const float* k,
+                        const float* v, const float* g, const float* beta, double* M, double* S,
+                        int nthreads, int decay_first) {
+    kda_sum_ctx c = {B, T, H, K, V, nseg, k, v, g, beta, M, S, decay_first};
+    run_units(kda_sum_unit, &c, (long)B * H * nseg, nthreads);
+}

@@ -398,3 +398,82 @@ def test_varlen_sequences_are_independent():
     assert np.array_equal(o2[:, :64], o[:, :64]) and np.array_equal(o2[:, 129:], o[:, 129:])
     assert np.array_equal(hf2[[0, 2]], hf[[0, 2]])
     assert not np.allclose(o2[:, 64:129], o[:, 64:129])
+
+
+# --------------------------------------------------------------------------------------
+# per-channel gates ("KDA Chunk Backward -- TPU/Pallas Kernel Design", section 1.2): the
+# state decays row by row by exp(g_t), g_t in R^K
+# --------------------------------------------------------------------------------------
+GOLDEN_KDA = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_kda_k2v2.json")
+
+
+def kda_inputs(B, T, H, K, V, seed, g_mu=2.0, g_sd=1.0, h0=True):
+    x = rand_inputs(B, T, H, K, V, seed, g_mu=g_mu, g_sd=g_sd, h0=h0)
+    gk = synth.fill(seed + 77, "g", (B, T, H, K), synth.KIND_LOGSIGMOID, g_mu, g_sd)
+    return x, gk
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_kda_hand_worked(case):
+    d = json.load(open(GOLDEN_KDA))
+    c = d["cases"][case]
+    tok = d["tokens"]
+    q, k, v = (np.array(tok[n], np.float32).reshape(1, 2, 1, 2) for n in ("q", "k", "v"))
+    beta = np.array(tok["beta"], np.float32).reshape(1, 2, 1)
+    g = np.array(tok["g"], np.float32).reshape(1, 2, 1, 2)
+    h0 = np.array(d["h0"], np.float32).reshape(1, 1, 2, 2)
+    df = c["decay_first"]
+    o, hf, _ = oracle.kda_recurrence(q, k, v, g, beta, h0, decay_first=df)
+    assert np.max(np.abs(o[0, :, 0] - np.array(c["o"]))) <= c["tol"]
+    assert np.max(np.abs(hf[0, 0] - np.array(c["h_final"]))) <= c["tol"]
+    M, S = oracle.kda_summary(k, v, g, beta, nseg=1, decay_first=df)
+    assert np.max(np.abs(M[0, 0, 0] - np.array(c["M"]))) <= c["tol"]
+    assert np.max(np.abs(S[0, 0, 0] - np.array(c["S"]))) <= c["tol"]
+
+
+@pytest.mark.parametrize("decay_first", [False, True])
+def test_kda_equal_channels_is_the_scalar_gate(decay_first):
+    # every channel carrying the token's scalar gate reproduces the scalar-gate oracle,
+    # which is separate code
+    x = rand_inputs(2, 96, 2, 8, 4, seed=5151, g_mu=0.5)
+    gk = np.repeat(x["g"][..., None], 8, axis=-1)
+    o, hf, hin = oracle.recurrence(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], seg_len=32,
+                                   decay_first=decay_first)
+    ok, hk, hink = oracle.kda_recurrence(x["q"], x["k"], x["v"], gk, x["beta"], x["h0"],
+                                         seg_len=32, decay_first=decay_first)
+    assert rel_err(ok, o) <= 1e-12 and rel_err(hk, hf) <= 1e-12 and rel_err(hink, hin) <= 1e-12
+    M, S = oracle.summary(x["k"], x["v"], x["g"], x["beta"], nseg=3, decay_first=decay_first)
+    Mk, Sk = oracle.kda_summary(x["k"], x["v"], gk, x["beta"], nseg=3, decay_first=decay_first)
+    assert rel_err(Mk, M) <= 1e-12 and rel_err(Sk, S) <= 1e-12
+
+
+@pytest.mark.parametrize("decay_first", [False, True])
+def test_kda_summary_is_the_product_of_token_transitions(decay_first):
+    # brute force on a tiny head: M = T_L ... T_1 with T_t = diag(a_t) - beta_t k_t k_t^T
+    # (read before the decay) or (I - beta_t k_t k_t^T) diag(a_t) (decayed read); S is the
+    # state reached from zero; and H_out = M H_in + S for a random H_in
+    x, gk = kda_inputs(1, 7, 1, 3, 2, seed=5252, g_mu=0.0, g_sd=1.5)
+    M, S = oracle.kda_summary(x["k"], x["v"], gk, x["beta"], nseg=1, decay_first=decay_first)
+    k, v, b, a = (x["k"][0, :, 0].astype(np.float64), x["v"][0, :, 0].astype(np.float64),
+                  x["beta"][0, :, 0].astype(np.float64), np.exp(gk[0, :, 0].astype(np.float64)))
+    Mb, Sb = np.eye(3), np.zeros((3, 2))
+    for t in range(7):
+        P = np.eye(3) - b[t] * np.outer(k[t], k[t])
+        Tt = P @ np.diag(a[t]) if decay_first else np.diag(a[t]) - b[t] * np.outer(k[t], k[t])
+        Mb = Tt @ Mb
+        Sb = Tt @ Sb + b[t] * np.outer(k[t], v[t])
+    assert rel_err(M[0, 0, 0], Mb) <= 1e-12 and rel_err(S[0, 0, 0], Sb) <= 1e-12
+    _, hf, _ = oracle.kda_recurrence(x["q"], x["k"], x["v"], gk, x["beta"], x["h0"],
+                                     decay_first=decay_first)
+    assert rel_err(hf[0, 0], Mb @ x["h0"][0, 0].astype(np.float64) + Sb) <= 1e-12
+
+
+def test_kda_segment_states_are_the_scan_of_the_summaries():
+    x, gk = kda_inputs(2, 128, 2, 8, 8, seed=5353, g_mu=1.0)
+    _, hf, hin = oracle.kda_recurrence(x["q"], x["k"], x["v"], gk, x["beta"], x["h0"], seg_len=32)
+    M, S = oracle.kda_summary(x["k"], x["v"], gk, x["beta"], nseg=4)
+    H_in = oracle.scan(M, S, x["h0"])
+    assert rel_err(H_in, hin) <= 1e-10
+    Mall, Sall = oracle.kda_summary(x["k"], x["v"], gk, x["beta"], nseg=1)
+    h_end = np.einsum("bhij,bhjv->bhiv", Mall[0], x["h0"].astype(np.float64)) + Sall[0]
+    assert rel_err(h_end, hf) <= 1e-10
