@@ -27,7 +27,7 @@ struct WsLayout {
 
 // Shapes that take the tcgen05 kernels (which also need the per-chunk WY tiles).
 bool tc_shape(const gdn_problem& p) {
-    return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128;
+    return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128 && !p.gate_k;
 }
 
 int sm_count() {
@@ -93,6 +93,7 @@ gdn_status check_problem(const gdn_problem* p, int nseg) {
     if (nseg < 1) return GDN_ERR_INVALID_ARG;
     if (p->chunk != gdn::kChunk) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (p->decay_first != 0 && p->decay_first != 1) return GDN_ERR_INVALID_ARG;
+    if (p->gate_k != 0 && p->gate_k != 1) return GDN_ERR_INVALID_ARG;
     if (p->K != p->V || (p->K != 64 && p->K != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
     if ((p->in_dtype != GDN_DTYPE_F32 && p->in_dtype != GDN_DTYPE_BF16) ||
         (p->out_dtype != GDN_DTYPE_F32 && p->out_dtype != GDN_DTYPE_BF16))
@@ -137,6 +138,7 @@ ChainParams base_params(const gdn_problem* p, void* ws) {
     c.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
     c.out_bf16 = p->out_dtype == GDN_DTYPE_BF16;
     c.decay_first = p->decay_first;
+    c.gate_k = p->gate_k;
     c.err = reinterpret_cast<gdn::DeviceError*>(ws);
     return c;
 }
@@ -274,6 +276,7 @@ gdn_status check_varlen(const gdn_problem* p, int nseq) {
     if (p->B != 1 || p->H < 1 || p->T < 0 || nseq < 1) return GDN_ERR_INVALID_ARG;
     if (p->chunk != gdn::kChunk) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (p->decay_first != 0 && p->decay_first != 1) return GDN_ERR_INVALID_ARG;
+    if (p->gate_k != 0 && p->gate_k != 1) return GDN_ERR_INVALID_ARG;
     if (p->K != p->V || (p->K != 64 && p->K != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
     if ((p->in_dtype != GDN_DTYPE_F32 && p->in_dtype != GDN_DTYPE_BF16) ||
         (p->out_dtype != GDN_DTYPE_F32 && p->out_dtype != GDN_DTYPE_BF16))

@@ -55,6 +55,7 @@ struct ChainParams {
     int in_bf16;
     int out_bf16;
     int decay_first;   // the read sees the decayed state (inclusive gate on the read side)
+    int gate_k;        // g holds one gate per key channel, [B,T,H,K] (CUDA-core kernels only)
     // launch as the programmatic dependent of the preceding grid in the stream (the kernel
     // then finishes only after that grid has)
     int launch_dependent;

@@ -41,7 +41,7 @@ __device__ __forceinline__ void store_out(void* base, long long idx, float x, in
         reinterpret_cast<float*>(base)[idx] = x;
 }
 
-template <int KD, int CT, bool SUMMARY>
+template <int KD, int CT, bool SUMMARY, bool GATEK>
 struct SimtSmem {
     static constexpr int KP = KD + 1;  // padded row of k / q
     static constexpr int LP = 65;      // padded row of the 64x64 matrices
@@ -55,15 +55,21 @@ struct SimtSmem {
     static constexpr int off_y = off_c + (SUMMARY ? 0 : 64 * LP);
     static constexpr int off_r = off_y + 64 * CT;
     static constexpr int off_s = off_r + 64 * CT;  // scalars: 6 x 64
-    static constexpr int total = off_s + 6 * 64;
+    // per-channel gates: the chunk's cumulative gates G [64][KP] and a [64][KP] scratch
+    static constexpr int off_gk = off_s + 6 * 64;
+    static constexpr int off_ek = off_gk + (GATEK ? 64 * KP : 0);
+    static constexpr int total = off_ek + (GATEK ? 64 * KP : 0);
     static constexpr size_t bytes = sizeof(float) * total;
 };
 
-template <int KD, int CT, bool SUMMARY>
+// GATEK: per-channel gates ("KDA Chunk Backward -- TPU/Pallas Kernel Design", section 1.2):
+// g is [B,T,H,K] and every quantity above takes the channel's own cumulative gate, e.g.
+// P[i,j] = sum_l k_il k_jl exp(Gx_il - G_jl), the state rows decay by exp(G_last,l).
+template <int KD, int CT, bool SUMMARY, bool GATEK>
 __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
     // a forward grid lets a grid launched as its programmatic dependent start right away
     if (!SUMMARY) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    using L = SimtSmem<KD, CT, SUMMARY>;
+    using L = SimtSmem<KD, CT, SUMMARY, GATEK>;
     extern __shared__ float sm[];
     float* ks = sm + L::off_k;
     float* qs = sm + L::off_q;
@@ -80,6 +86,8 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
     float* dk = bet + 64;   // exp(G_last - G_j)
     float* eq = dk + 64;    // exp(G_i)
     float* ekr = eq + 64;   // exp(Gx_i)
+    float* Gk = sm + L::off_gk;   // per-channel cumulative gates [i][l] (GATEK)
+    float* Ek = sm + L::off_ek;   // per-channel scaled keys [i][l] (GATEK)
     constexpr int KP = L::KP, LP = L::LP;
 
     const int tid = threadIdx.x;
@@ -136,12 +144,62 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
         if (tid < 64) {
             const long long row = (row_base + t0 + tid) * H + h;
             const bool in = t0 + tid < seq_tokens;
-            gx[tid] = in ? load_in(p.g, row, p.in_bf16) : 0.f;   // raw gate for now
+            if (!GATEK) gx[tid] = in ? load_in(p.g, row, p.in_bf16) : 0.f;   // raw gate for now
             bet[tid] = in ? load_in(p.beta, row, p.in_bf16) : 0.f;
         }
+        if (GATEK)
+            for (int e = tid; e < 64 * KD; e += kThreads) {
+                const int i = e / KD, l = e % KD;
+                const long long row = (row_base + t0 + i) * H + h;
+                Gk[i * KP + l] = (t0 + i < seq_tokens) ? load_in(p.g, row * KD + l, p.in_bf16) : 0.f;
+            }
         __syncthreads();
+        if (GATEK) {
+            // ---- (2') per-channel inclusive cumsum down the chunk (one thread per channel)
+            if (tid < KD) {
+                float acc = 0.f;
+                for (int i = 0; i < 64; ++i) {
+                    acc += Gk[i * KP + tid];
+                    Gk[i * KP + tid] = acc;
+                }
+            }
+            __syncthreads();
+            // read-side gate of token i, channel l: G_il, or the exclusive G_(i-1)l
+            auto gread = [&](int i, int l) {
+                return p.decay_first ? Gk[i * KP + l] : (i > 0 ? Gk[(i - 1) * KP + l] : 0.f);
+            };
+            // ---- (3') L = diag(beta) P and C with per-channel decays; clear A. Every
+            //      exponent is a difference G_i - G_j with j <= i, so it is never positive.
+            for (int e = tid; e < 64 * 64; e += kThreads) {
+                const int i = e / 64, j = e % 64;
+                float lv = 0.f, cv = 0.f;
+                if (j < i) {
+                    float d = 0.f;
+#pragma unroll 4
+                    for (int l = 0; l < KD; ++l)
+                        d = fmaf(ks[i * KP + l] * ks[j * KP + l], __expf(gread(i, l) - Gk[j * KP + l]), d);
+                    lv = bet[i] * d;
+                }
+                if (!SUMMARY && j <= i) {
+                    float d = 0.f;
+#pragma unroll 4
+                    for (int l = 0; l < KD; ++l)
+                        d = fmaf(qs[i * KP + l] * ks[j * KP + l], __expf(Gk[i * KP + l] - Gk[j * KP + l]), d);
+                    cv = d;
+                }
+                Ls[i * LP + j] = lv;
+                if (!SUMMARY) Cs[i * LP + j] = cv;
+                As[i * LP + j] = 0.f;
+            }
+            // scaled keys of the read, k_il exp(Gread_il)
+            for (int e = tid; e < 64 * KD; e += kThreads) {
+                const int i = e / KD, l = e % KD;
+                Ek[i * KP + l] = ks[i * KP + l] * __expf(gread(i, l));
+            }
+            __syncthreads();
+        }
         // ---- (2) gate cumsum inside the chunk (one warp; two gates per lane)
-        if (tid < 32) {
+        if (!GATEK && tid < 32) {
             const float a0 = gx[2 * tid], a1 = gx[2 * tid + 1];
             float s = a0 + a1;
             for (int off = 1; off < 32; off <<= 1) {
@@ -156,14 +214,14 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
             gx[2 * tid + 1] = p.decay_first ? excl + a0 + a1 : excl + a0;
         }
         __syncthreads();
-        const float glast = gam[63];
-        if (tid < 64) {
+        const float glast = GATEK ? 0.f : gam[63];
+        if (!GATEK && tid < 64) {
             dk[tid] = expf(glast - gam[tid]);
             eq[tid] = expf(gam[tid]);
             ekr[tid] = expf(gx[tid]);
         }
         // ---- (3) L = diag(beta) P and C; clear A
-        for (int e = tid; e < 64 * 64; e += kThreads) {
+        for (int e = tid; e < (GATEK ? 0 : 64 * 64); e += kThreads) {
             const int i = e / 64, j = e % 64;
             float lv = 0.f, cv = 0.f;
             if (j < i) {
@@ -231,8 +289,8 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
             const int i = e / CT, c = e % CT;
             float a = 0.f;
 #pragma unroll 8
-            for (int l = 0; l < KD; ++l) a = fmaf(ks[i * KP + l], Hs[l * CT + c], a);
-            Ys[e] = bet[i] * (vs[e] - ekr[i] * a);
+            for (int l = 0; l < KD; ++l) a = fmaf(GATEK ? Ek[i * KP + l] : ks[i * KP + l], Hs[l * CT + c], a);
+            Ys[e] = bet[i] * (vs[e] - (GATEK ? a : ekr[i] * a));
         }
         __syncthreads();
         // ---- (6) R = A Y
@@ -243,7 +301,14 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
             Rs[e] = a;
         }
         __syncthreads();
-        // ---- (7) O = diag(exp(G)) Q H + C R
+        // ---- (7) O = diag(exp(G)) Q H + C R (per channel: Q scaled by exp(G_il) in place)
+        if (!SUMMARY && GATEK) {
+            for (int e = tid; e < 64 * KD; e += kThreads) {
+                const int i = e / KD, l = e % KD;
+                qs[i * KP + l] *= __expf(Gk[i * KP + l]);
+            }
+            __syncthreads();
+        }
         if (!SUMMARY) {
             for (int e = tid; e < 64 * CT; e += kThreads) {
                 const int i = e / CT, c = e % CT;
@@ -253,18 +318,28 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
                 float bsum = 0.f;
                 for (int j = 0; j <= i; ++j) bsum = fmaf(Cs[i * LP + j], Rs[j * CT + c], bsum);
                 const long long row = (row_base + t0 + i) * H + h;
-                if (t0 + i < seq_tokens) store_out(p.o, row * V + c0 + c, fmaf(eq[i], a, bsum), p.out_bf16);
+                if (t0 + i < seq_tokens)
+                    store_out(p.o, row * V + c0 + c, GATEK ? a + bsum : fmaf(eq[i], a, bsum), p.out_bf16);
             }
             __syncthreads();
         }
-        // ---- (8) H <- exp(G_last) H + sum_j exp(G_last - G_j) k_j R_j
+        // ---- (8) H <- exp(G_last) H + sum_j exp(G_last - G_j) k_j R_j (per channel: row l
+        //      decays by exp(G_last,l), the keys by exp(G_last,l - G_jl))
+        if (GATEK) {
+            for (int e = tid; e < 64 * KD; e += kThreads) {
+                const int j = e / KD, l = e % KD;
+                Ek[j * KP + l] = ks[j * KP + l] * __expf(Gk[63 * KP + l] - Gk[j * KP + l]);
+            }
+            __syncthreads();
+        }
         const float dlast = expf(glast);
         for (int e = tid; e < KD * CT; e += kThreads) {
             const int l = e / CT, c = e % CT;
             float a = 0.f;
 #pragma unroll 8
-            for (int j = 0; j < 64; ++j) a = fmaf(dk[j] * ks[j * KP + l], Rs[j * CT + c], a);
-            Hs[e] = fmaf(dlast, Hs[e], a);
+            for (int j = 0; j < 64; ++j)
+                a = fmaf(GATEK ? Ek[j * KP + l] : dk[j] * ks[j * KP + l], Rs[j * CT + c], a);
+            Hs[e] = fmaf(GATEK ? __expf(Gk[63 * KP + l]) : dlast, Hs[e], a);
         }
         __syncthreads();
     }
@@ -296,11 +371,11 @@ __global__ void __launch_bounds__(kThreads) simt_chain_kernel(ChainParams p) {
     if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int KD, bool SUMMARY>
-cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
+template <int KD, bool SUMMARY, bool GATEK>
+cudaError_t launch_chain_g(const ChainParams& p, cudaStream_t s) {
     constexpr int CT = 32;
-    using L = SimtSmem<KD, CT, SUMMARY>;
-    auto kern = simt_chain_kernel<KD, CT, SUMMARY>;
+    using L = SimtSmem<KD, CT, SUMMARY, GATEK>;
+    auto kern = simt_chain_kernel<KD, CT, SUMMARY, GATEK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L::bytes);
     if (e != cudaSuccess) return e;
@@ -321,6 +396,11 @@ cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int KD, bool SUMMARY>
+cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
+    return p.gate_k ? launch_chain_g<KD, SUMMARY, true>(p, s) : launch_chain_g<KD, SUMMARY, false>(p, s);
 }
 
 // In-order scan over consecutive pieces of each sequence, fp32, one CTA per (head, 32-column

@@ -957,7 +957,7 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
 }  // namespace
 
 bool tc_supported(const ChainParams& p) {
-    return p.in_bf16 && p.K == kD && p.V == kD &&
+    return p.in_bf16 && p.K == kD && p.V == kD && !p.gate_k &&
            (p.cu_seqlens || (p.seg_len > 0 && p.seg_len % kC == 0)) && encode_fn() != nullptr;
 }
 

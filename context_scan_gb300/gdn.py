@@ -35,7 +35,7 @@ class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("K", ctypes.c_int), ("V", ctypes.c_int), ("chunk", ctypes.c_int),
                 ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("decay_first", ctypes.c_int)]
+                ("decay_first", ctypes.c_int), ("gate_k", ctypes.c_int)]
 
 
 _lib = None
@@ -86,11 +86,14 @@ def _dtype_code(t) -> int:
     return 99   # the library rejects it with GDN_ERR_UNSUPPORTED_DTYPE
 
 
-def problem(q_or_k, v, o=None, chunk: int = 64, decay_first: bool = False) -> Problem:
+def problem(q_or_k, v, o=None, chunk: int = 64, decay_first: bool = False, g=None) -> Problem:
+    """The problem description of these tensors; g (optional) sets gate_k when it carries
+    one gate per key channel ([B, T, H, K])."""
     B, T, H, K = q_or_k.shape
     V = v.shape[-1]
     out = GDN_DTYPE_F32 if o is None else _dtype_code(o)
-    return Problem(B, T, H, K, V, chunk, _dtype_code(q_or_k), out, int(decay_first))
+    gate_k = int(g is not None and g.dim() == 4)
+    return Problem(B, T, H, K, V, chunk, _dtype_code(q_or_k), out, int(decay_first), gate_k)
 
 
 def _ptr(t):
@@ -128,7 +131,7 @@ def alloc_workspace(prob: Problem, nseg: int = 1, device="cuda"):
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, h0, o, h_final, workspace, stream=None, prob=None):
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     _check(lib().gdn_chunk_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final), _ptr(workspace),
                                workspace.numel() if workspace is not None else 0,
@@ -136,7 +139,7 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0, o, h_final, workspace, stream=None, prob
 
 
 def gdn_segment_summary(k, v, g, beta, M, S, nseg, workspace, stream=None, prob=None):
-    prob = prob or problem(k, v)
+    prob = prob or problem(k, v, g=g)
     _check(lib().gdn_segment_summary(ctypes.byref(prob), nseg, _ptr(k), _ptr(v), _ptr(g),
                                      _ptr(beta), _ptr(M), _ptr(S), _ptr(workspace),
                                      workspace.numel() if workspace is not None else 0,
@@ -152,7 +155,7 @@ def gdn_summary_scan(M, S, h0, H_in, stream=None, prob=None):
 
 def gdn_segmented_fwd(q, k, v, g, beta, h0, o, h_final, nseg, workspace, H_in=None,
                       stream=None, prob=None):
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     _check(lib().gdn_segmented_fwd(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
                                    _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
                                    _ptr(H_in), _ptr(workspace),
@@ -166,7 +169,7 @@ def gdn_segmented_fwd_timed(q, k, v, g, beta, h0, o, h_final, nseg, workspace, e
     four stages: before the WY factors, before the first phase (piece 0's forward beside the
     piece summaries), before the scan, before the second phase (the forward of pieces
     1..P-1), after it."""
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     if len(events) != 5:
         raise ValueError("gdn_segmented_fwd_timed takes five events")
     arr = (_P * 5)(*[e.cuda_event for e in events])
@@ -182,7 +185,7 @@ def gdn_segmented_fwd_noalloc(q, k, v, g, beta, h0, o, h_final, nseg, device_err
     """gdn_segmented_fwd with the library's fixed scratch array instead of a workspace.
     device_error: optional int32/uint32 CUDA tensor of >= 2 elements that receives the
     call's device error word {code, detail}."""
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     _check(lib().gdn_segmented_fwd_noalloc(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
                                            _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
                                            _ptr(h_final), _ptr(device_error), _stream(stream)),
@@ -207,7 +210,7 @@ def gdn_varlen_fwd(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, stre
     """Packed variable-length forward: q, k, v, g, beta, o hold [1, T, H, *] tokens of
     nseq = len(cu_seqlens) - 1 sequences; cu_seqlens is an int32 CUDA tensor; h0 and h_final
     are [nseq, H, K, V] fp32 (or None)."""
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     nseq = int(cu_seqlens.numel()) - 1
     _check(lib().gdn_varlen_fwd(ctypes.byref(prob), nseq, _ptr(cu_seqlens), _ptr(q), _ptr(k),
                                 _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
@@ -219,7 +222,7 @@ def gdn_varlen_fwd_timed(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace
                          stream=None, prob=None):
     """gdn_varlen_fwd recording three torch.cuda.Event (enable_timing=True): before the length
     check and the WY factors, before the chunked forward, after it."""
-    prob = prob or problem(k, v, o)
+    prob = prob or problem(k, v, o, g=g)
     if len(events) != 3:
         raise ValueError("gdn_varlen_fwd_timed takes three events")
     arr = (_P * 3)(*[e.cuda_event for e in events])

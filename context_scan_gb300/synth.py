@@ -94,6 +94,8 @@ class Workload:
     # packed variable-length sequences: B == 1, T == sum(seq_lens), one initial state per
     # sequence (h0 is [len(seq_lens), H, K, V])
     seq_lens: tuple | None = None
+    # one gate per key channel (g is [B, T, H, K], each entry log(sigmoid(N(g_mu, g_sd))))
+    gate_k: bool = False
     chunk: int = 64
     notes: str = field(default="", compare=False)
 
@@ -125,6 +127,9 @@ WORKLOADS = {
                  in_dtype="bf16", g_mu=6, g_sd=1, beta_mu=-2, beta_sd=1, h0_sd=0.1,
                  seed=0x6D6E0005,
                  notes="summary M stays O(0.1-1): exercises the compose path numerically"),
+        Workload("kda_h16_t8k", B=1, H=16, T=8192, K=128, V=128, nseg=1, in_dtype="bf16",
+                 g_mu=3, g_sd=1, beta_mu=0, beta_sd=1, h0_sd=0.1, seed=0x6D6E0007, gate_k=True,
+                 notes="per-channel gates at the shape of the KDA design page's measurements"),
         Workload("varlen5_h16_t7300", B=1, H=16, T=7300, K=128, V=128, nseg=1, in_dtype="bf16",
                  g_mu=2, g_sd=1, beta_mu=0, beta_sd=1, h0_sd=0.1, seed=0x6D6E0006,
                  seq_lens=(1800, 1500, 2000, 1200, 800),
@@ -169,7 +174,8 @@ def make_inputs(w: Workload, nthreads: int = 0) -> dict:
                                nthreads=nthreads))
         parts["v"].append(fill(s, "v", (Bd, w.T, w.H, w.V), KIND_NORMAL, 0.0, 1.0, bf16=bf16,
                                nthreads=nthreads))
-        parts["g"].append(fill(s, "g", (Bd, w.T, w.H), KIND_LOGSIGMOID, w.g_mu, w.g_sd,
+        gshape = (Bd, w.T, w.H, w.K) if w.gate_k else (Bd, w.T, w.H)
+        parts["g"].append(fill(s, "g", gshape, KIND_LOGSIGMOID, w.g_mu, w.g_sd,
                                bf16=bf16, nthreads=nthreads))
         parts["beta"].append(fill(s, "beta", (Bd, w.T, w.H), KIND_SIGMOID, w.beta_mu, w.beta_sd,
                                   bf16=bf16, nthreads=nthreads))

@@ -23,7 +23,7 @@
  * Layouts (row-major, contiguous, no strides):
  *   q, k     [B, T, H, K]        in_dtype
  *   v        [B, T, H, V]        in_dtype
- *   g, beta  [B, T, H]           in_dtype
+ *   g, beta  [B, T, H]           in_dtype   (g: [B, T, H, K] when gate_k is set)
  *   o        [B, T, H, V]        out_dtype
  *   h0, h_final                  [B, H, K, V]           fp32
  *   M                            [nseg, B, H, K, K]     fp32   ((M@X)[i,v] = sum_j M[i,j] X[j,v])
@@ -93,6 +93,11 @@ typedef struct {
      *    section 08 "What a GDN token does to the state"; KDA design section 1.2; transition
      *    exp(g_t) (I - beta_t k_t k_t^T)). Every call below follows the flag. */
     int decay_first;
+    /* 0: one gate per token and head, g is [B, T, H] (Gated DeltaNet).
+     * 1: one gate per key channel, g is [B, T, H, K], and the state decays row by row,
+     *    diag(exp(g_t)) H ("KDA Chunk Backward -- TPU/Pallas Kernel Design", section 1.2;
+     *    with either reading above). Runs the fp32 CUDA-core kernels for every dtype. */
+    int gate_k;
 } gdn_problem;
 
 /* Bytes of workspace the calls below need for this problem split into nseg segments
