@@ -32,6 +32,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN segmented fwd tokens/s at H32 K=V=128 T=32K bf16; % of roofline"
 VARLEN_METRIC = "GDN packed-sequence fwd tokens/s (lengths 1800,1500,2000,1200,800) at H16 K=V=128 bf16"
+KDA_METRIC = "GDN per-channel-gate (KDA) fwd tokens/s at H16 K=V=128 T=8K bf16"
+
+
+def metric_of(w) -> str:
+    return KDA_METRIC if w.gate_k else METRIC
 DEFAULT_WORKLOAD = "cp4_b2_h32_t32k"
 L2_BYTES = 129 * 1024 * 1024
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -99,9 +104,10 @@ def algorithmic(w, pieces=None, out_bytes: int = 4):
     K, V = w.K, w.V
     kv_state = BH * K * V * 4
     kk_state = BH * K * K * 4
-    tc = w.in_dtype == "bf16" and K == 128 and V == 128
-    fwd_tok = (2 * K + V) * isz + 2 * isz + V * out_bytes      # q, k, v, g, beta in; o out
-    sum_tok = (K + V) * isz + 2 * isz                          # k, v, g, beta in
+    tc = w.in_dtype == "bf16" and K == 128 and V == 128 and not w.gate_k
+    g_tok = (K if w.gate_k else 1) * isz                       # one gate, or one per channel
+    fwd_tok = (2 * K + V) * isz + g_tok + isz + V * out_bytes  # q, k, v, g, beta in; o out
+    sum_tok = (K + V) * isz + g_tok + isz                      # k, v, g, beta in
     # prep (K K^T, U, W) + state (W H, Kd^T R) + output (Q K^T, Qd H, C R), per chunk
     fwd_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 64 * K * V * 2
                  + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
@@ -150,7 +156,7 @@ def launches_per_step(w, pieces=None):
     forward, the piece summaries (3 pieces or more), the scan and the second forward (2 pieces
     or more)."""
     P = pieces or w.nseg
-    tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128)
+    tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128 and not w.gate_k)
     return tc + 1 + (1 if P >= 3 else 0) + (2 if P >= 2 else 0)
 
 
@@ -287,7 +293,7 @@ def run_varlen(args):
     nseq = len(w.seq_lens)
     o = torch.empty((1, w.T, w.H, w.V), dtype=torch.float32, device=dev)
     hf = torch.empty((nseq, w.H, w.K, w.V), dtype=torch.float32, device=dev)
-    prob = gdn.problem(d["k"], d["v"], o)
+    prob = gdn.problem(d["k"], d["v"], o, g=d["g"])
     ws = gdn.alloc_varlen_workspace(prob, nseq, device=dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -434,7 +440,9 @@ def run_ours(args):
     d = {n: (None if t is None else t.to(dev, non_blocking=False)) for n, t in host.items()}
     o = torch.empty((w.B, w.T, w.H, w.V), dtype=torch.float32, device=dev)
     hf = torch.empty((w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
-    prob = gdn.problem(d["k"], d["v"], o)
+    prob = gdn.problem(d["k"], d["v"], o, g=d["g"])
+    if prob.gate_k != int(w.gate_k):
+        raise RuntimeError("the problem's gate layout does not match the workload")
     pieces = gdn.segmented_pieces(prob, w.nseg)
     ws = gdn.alloc_workspace(prob, w.nseg, device=dev)
     stream = torch.cuda.current_stream()
@@ -540,12 +548,13 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "metric": metric_of(w), "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w0.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
                        "nseg": w.nseg, "pieces": pieces, "chunk": 64, "in_dtype": w.in_dtype,
+                       "gates": "per key channel" if w.gate_k else "per token",
                        "out_dtype": "f32", "state_dtype": "f32",
                        "l2": f"inputs larger than L2 ({total_input_mb(w):.0f} MB in + "
                              f"{w.B * w.T * w.H * w.V * 4 / 2**20:.0f} MB out > 129 MB); no flush",
@@ -569,7 +578,8 @@ def run_ours(args):
 
 def total_input_mb(w):
     isz = 2 if w.in_dtype == "bf16" else 4
-    return w.B * w.T * w.H * ((2 * w.K + w.V) * isz + 2 * isz) / 2**20
+    g = w.K if w.gate_k else 1
+    return w.B * w.T * w.H * ((2 * w.K + w.V) * isz + (g + 1) * isz) / 2**20
 
 
 # ---------------------------------------------------------------------------------------
@@ -583,8 +593,9 @@ def oracle_heads(w, x, heads, nthreads=0):
     for b, h in heads:
         xs = {n: x[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
         h0 = None if x["h0"] is None else x["h0"][b:b + 1, h:h + 1]
-        oracle.recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], h0,
-                          seg_len=w.seg_len, col_block=8, nthreads=nthreads)
+        rec = oracle.kda_recurrence if w.gate_k else oracle.recurrence
+        rec(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], h0,
+            seg_len=w.seg_len, col_block=8, nthreads=nthreads)
     return time.perf_counter() - t
 
 
@@ -677,7 +688,7 @@ def run_reference(args):
     # one step = one of the B*H heads; tokens/s scaled to the whole batch
     value = w.B * w.T * args.steps / len(heads) / secs
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "impl": "reference", "metric": metric_of(w), "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",

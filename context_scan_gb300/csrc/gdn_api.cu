@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "gdn.h"
@@ -30,11 +31,19 @@ bool tc_shape(const gdn_problem& p) {
     return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128 && !p.gate_k;
 }
 
+// Device properties asked on every call, looked up once per device (a call on a short
+// problem would otherwise spend a visible part of its time in these queries).
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_cc[kMaxDevices];   // 10 * major + minor, 0 until known
+
 int sm_count() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int sms = (dev >= 0 && dev < kMaxDevices) ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+    if (sms > 0) return sms;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < kMaxDevices) g_sms[dev].store(sms, std::memory_order_relaxed);
     return sms;
 }
 
@@ -108,11 +117,15 @@ gdn_status check_problem(const gdn_problem* p, int nseg) {
 gdn_status check_device() {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (major != 10 || minor != 3) return GDN_ERR_DEVICE;
-    return GDN_OK;
+    int cc = (dev >= 0 && dev < kMaxDevices) ? g_cc[dev].load(std::memory_order_relaxed) : 0;
+    if (cc == 0) {
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        cc = 10 * major + minor;
+        if (dev >= 0 && dev < kMaxDevices) g_cc[dev].store(cc, std::memory_order_relaxed);
+    }
+    return cc == 103 ? GDN_OK : GDN_ERR_DEVICE;
 }
 
 gdn_status check_workspace(const gdn_problem* p, int nseg, const void* ws, size_t ws_bytes) {

@@ -43,7 +43,7 @@ def run_segmented(w, d, nseg=None, out_dtype=torch.float32, want_hin=True, decay
     o = torch.empty((B, T, H, V), dtype=out_dtype, device="cuda")
     hf = torch.empty((B, H, K, V), dtype=torch.float32, device="cuda")
     hin = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device="cuda") if want_hin else None
-    prob = gdn.problem(d["k"], d["v"], o, decay_first=decay_first)
+    prob = gdn.problem(d["k"], d["v"], o, decay_first=decay_first, g=d["g"])
     ws = gdn.alloc_workspace(prob, nseg)
     gdn.gdn_segmented_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf, nseg, ws,
                           H_in=hin, prob=prob)
@@ -59,7 +59,7 @@ def run_summary(w, d, nseg=None, decay_first=False):
     V = d["v"].shape[-1]
     M = torch.empty((nseg, B, H, K, K), dtype=torch.float32, device="cuda")
     S = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device="cuda")
-    prob = gdn.problem(d["k"], d["v"], decay_first=decay_first)
+    prob = gdn.problem(d["k"], d["v"], decay_first=decay_first, g=d["g"])
     ws = gdn.alloc_workspace(prob, 1)
     gdn.gdn_segment_summary(d["k"], d["v"], d["g"], d["beta"], M, S, nseg, ws, prob=prob)
     torch.cuda.synchronize()
