@@ -41,7 +41,10 @@ constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
 
 // shared-memory map (bytes from a 1024-aligned base). Rows 0..15 of L are never used (the
 // first block row has nothing below the diagonal), so the scratch, the scalars and the
-// barriers live there; 36 KB per CTA lets six CTAs share an SM.
+// barriers live there; 36 KB per CTA lets six CTAs share an SM. The allocation must also hold
+// the K K^T operand windows: an M = 128 MMA reads 128 rows (16 KB) of its A operand per
+// feature half, so the first group reads up to 8 KB past the tile's end and the second group
+// from 8 KB before its start -- bytes 0 .. 32 KB + 96 in all, whatever else lives there.
 constexpr uint32_t WY_K = 8192;     // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle
 constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS, rows 16..63) once K K^T is in TMEM
 constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
@@ -55,6 +58,7 @@ constexpr uint32_t kWyTmemCols = 64;
 constexpr uint32_t ID_KK = idesc_bf16(128, 32, false, false);   // K K^T, 32 columns per group
 static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_END - WY_X, "layout");
 static_assert(WY_BAR + 64 <= 16 * LS * 4, "scratch, scalars and barriers fit in L's unused rows");
+static_assert(WY_K + 3 * 8192 + 128 <= WY_END, "the K K^T operand windows stay inside the allocation");
 
 struct WyParams {
     CUtensorMap tm_k;
