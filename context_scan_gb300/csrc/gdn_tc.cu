@@ -73,10 +73,12 @@ struct Cfg {
     static constexpr int NGRP = SUMMARY ? 1 : 2;             // prep warp groups
     static constexpr int PREP_WARP0 = 4 * NSG;
     static constexpr int PREP_THREADS = 128 * NGRP;
-    // one more warp issues the prep group's MMAs (P1 in the forward, P2, P3)
+    // one more warp issues the prep group's MMAs (P1 in the forward, P2, P3); in the summary
+    // one warp per state group issues that group's MMAs (S12, S4)
     static constexpr int MMA_WARP = 4 * NSG + 4 * NGRP;
     static constexpr int PRODUCER_WARP = MMA_WARP + 1;
-    static constexpr int THREADS = 32 * PRODUCER_WARP + 32;
+    static constexpr int ISSUE_WARP0 = PRODUCER_WARP + 1;
+    static constexpr int THREADS = 32 * (ISSUE_WARP0 + (SUMMARY ? NSG : 0));
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TM_S = 0;    // Q K^T, then W^T (prep)
     static constexpr uint32_t TM_U = 64;   // U^T -> R^T, two buffers by chunk parity; the
@@ -110,10 +112,9 @@ struct Smem {
     static constexpr uint32_t W = V + 16384;
     static constexpr uint32_t C0 = W + 4 * WQ_KB;   // C tf32: [kblock 2][64 (i) x 32 (j)], x2
     static constexpr uint32_t SCAL = C0 + (SUMMARY ? 0 : 32768);
-    static constexpr uint32_t TU_STRIDE = SUMMARY ? 64 : 128;   // tensor-memory U(+O) buffer pitch
     static constexpr uint32_t GATES = SCAL + 2 * 4 * 256;        // after scalars [parity 2][SC_N][64]
     static constexpr uint32_t BAR = GATES + KST * 256;           // gates [k stage][64]
-    static constexpr uint32_t END = BAR + 256;
+    static constexpr uint32_t END = BAR + 512;
     static constexpr uint32_t BYTES = END + 1024;                // + alignment slack
     static_assert(BYTES <= 232448u, "shared memory budget");
 };
@@ -128,7 +129,7 @@ constexpr uint32_t B_KFULL = 0, B_KEMPTY = 32, B_QFULL = 64, B_QEMPTY = 80, B_AF
                    B_AEMPTY = 112, B_VFULL = 128, B_VEMPTY = 136, B_BARP = 144, B_BARS = 152,
                    B_PREPDONE = 160, B_WFREE = 168, B_UFREE = 176, B_TMEM = 192, B_ABORT = 196,
                    B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216, B_CDONE = 224,
-                   B_WREAD = 232, B_MDRAIN = 240, B_SDRAIN = 248;
+                   B_WREAD = 232, B_MDRAIN = 240, B_SDRAIN = 248, B_S4 = 256, B_S4B = 264;
 
 // wait tags recorded in the device error word's detail field
 enum : unsigned {
@@ -172,11 +173,18 @@ __device__ __forceinline__ void store_o_rows32(const ChainParams& c, uint32_t t_
     }
 }
 
+// a state group (128 threads) and its issuer warp meet here once per chunk (named barriers 5
+// and 6)
+__device__ __forceinline__ void pack_bar(int sg) {
+    if (sg == 0) named_bar<5, 160>();
+    else named_bar<6, 160>();
+}
+
 // ------------------------------------------------------------------------------------
 // the chain kernel
 // ------------------------------------------------------------------------------------
-// Registers are allocated to warps in groups of four: 13 warps count as 16, so at most 128
-// registers per thread.
+// Registers are allocated to warps in groups of four: 15 or 16 warps count as 16, so at most
+// 128 registers per thread.
 // VARLEN: the chains are the packed sequences of c.cu_seqlens (forward only); the
 // fixed-length instance has none of the end-of-sequence checks.
 template <bool SUMMARY, bool VARLEN, bool OUT_BF16>
@@ -241,6 +249,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         mbar_init(bar0 + B_WREAD, 1);
         mbar_init(bar0 + B_MDRAIN, 1);
         mbar_init(bar0 + B_SDRAIN, NSG);   // each state group's last MMAs
+        mbar_init(bar0 + B_S4, 1);         // S4 retired (state group 0's issuer)
+        mbar_init(bar0 + B_S4B, 1);        // S4 retired (state group 1's issuer)
         *abort_flag = 0;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S) = 1;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S1) = 1;
@@ -454,7 +464,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             mbar_drain(bar0 + B_MDRAIN, 0, limit);
         }
         __syncwarp();
-    } else if (warp >= F::PREP_WARP0) {
+    } else if (warp >= F::PREP_WARP0 && warp < F::MMA_WARP) {
         // ================================== prep ==================================
         const int pt = tid - 32 * F::PREP_WARP0, pw = warp - F::PREP_WARP0;
         const int grp = pw >> 2, lq = pw & 3;   // warp group; tensor-memory lane quarter
@@ -501,10 +511,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
-            const int ks = n % KST, qs = n & 1, as = n % AST;
-            const uint32_t kst = base + L::K0 + ks * 16384;
-            const uint32_t ast = base + L::A0 + as * 16384;
-            const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
+            const int ks = n % KST, qs = n & 1;
             float* sc = scal + (n & 1) * (SC_N * 64);
             // chunk n-NUB is retired: its U/R (and in the forward O, C and scalar) buffers may
             // be reused
@@ -682,6 +689,220 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #undef warp_wait
 #undef pmma_wait
 #undef pwait
+    } else if (SUMMARY && warp >= F::ISSUE_WARP0) {
+        if constexpr (SUMMARY) {
+        // ========================= state MMA issue (summary) =========================
+        // One warp per state group issues that group's tensor-core work, so that no thread
+        // that packs R^T stalls behind an MMA issue: per chunk n, S12 once the prep group's
+        // operands are in place and S4 of chunk n-1 has updated H_s, then S4 once the group
+        // has packed R^T (a named barrier with the group). Both sides pass that barrier
+        // exactly once per chunk (and once for the initial state) whatever happens, so a
+        // wait that gives up cannot strand the other side; after one, nothing more is
+        // issued. Lane 0 issues; the warp polls together. (The forward's state group issues
+        // its own MMAs: there the prep group, not the state group, sets the pace.)
+        const int sg = warp - F::ISSUE_WARP0;
+        const bool m_part = SUMMARY && sg == 0;
+        const uint32_t tm_h = F::tm_h(sg);
+        const uint32_t bar_s = bar0 + (sg == 0 ? B_BARS : B_BARS1);
+        const uint32_t bar_4 = bar0 + (sg == 0 ? B_S4 : B_S4B);
+        auto wwait = [&](uint32_t bar, uint32_t parity, unsigned tag) {
+            const bool r = mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
+            return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+        };
+        tc_fence_before();
+        pack_bar(sg);   // the initial state is in tensor memory
+        bool ok = true;
+#pragma unroll 1
+        for (int n = 0; n < nchunks; ++n) {
+            const int ks = n % KST;
+            const uint32_t kst = base + L::K0 + ks * 16384;
+            const uint32_t tu_col = m_part ? F::TM_RM : TM_U + (n % NUB) * F::TU_STRIDE;
+            const uint32_t t_u = tmem + tu_col;
+            ok = ok && wwait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE) &&
+                 (n == 0 || wwait(bar_4, (n - 1) & 1, TAG_BARS));
+            // ---- S12: R^T = U^T + H_s^T (-sigma W)^T (no U in the M part)
+            if (ok && lane == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int k8 = 0; k8 < 16; ++k8)
+                    mma_ts_tf32<ID_TF>(t_u, tmem + tm_h + k8 * 8,
+                                       desc_k(base + L::W + (k8 >> 2) * L::WQ_KB + (k8 & 3) * 32),
+                                       (!m_part || k8 > 0) ? 1u : 0u);
+                mma_commit(bar0 + B_WFREE);
+                mma_commit(bar_s);
+            }
+            __syncwarp();
+            pack_bar(sg);   // the group has packed the scaled R^T (in place)
+            // ---- S4: H_s^T += (R^T D) K (A = hi, lo in TMEM)
+            if (ok && lane == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        mma_ts_bf16<ID_S4>(tmem + tm_h, tmem + tu_col + 16 * k16 + 8 * part,
+                                           desc_mn(kst + k16 * 2048, 8192), 1u);
+                mma_commit(bar0 + B_KEMPTY + 8 * ks);
+                mma_commit(bar0 + B_UFREE + 8 * (n % NUB));
+                mma_commit(bar_4);
+            }
+            __syncwarp();
+        }
+        // every MMA issued here retires before the final state is read out or tensor memory
+        // is released (the state group waits for this, or drains it)
+        if (lane == 0) mma_commit(bar0 + B_SDRAIN);
+        __syncwarp();
+        }
+    } else if constexpr (SUMMARY) {
+        // ================================== state =================================
+        // summary state group sg: the M part (0) or the S part (1). Per chunk: wait for S12,
+        // pack the scaled R^T in place, hand it to the group's issuer warp.
+        const int sg = SUMMARY ? (warp >> 2) : 0;
+        const int st = tid & 127;                      // = column of H this thread owns
+        const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t tm_h = F::tm_h(sg);
+        const uint32_t bar_s = bar0 + (sg == 0 ? B_BARS : B_BARS1);
+        volatile int* go = reinterpret_cast<volatile int*>(sm + L::BAR + (sg == 0 ? B_GO_S : B_GO_S1));
+        const bool m_part = SUMMARY && sg == 0;       // starts from I, no values
+        uint32_t bars_phase = 0;
+        const long long bhoff = (long long)bh * kD * kD;
+        float sig_next = 1.f;   // sigma after the last completed chunk
+
+// each state group synchronises its waits on its own named barrier (1 or 4)
+#define swait(bar, parity, tag)                                                                  \
+    (sg == 0 ? group_wait<1, 128>(warp == 0, lane == 0, (bar), (parity), true, go, abort_flag,   \
+                                  limit, c.err, (tag))                                           \
+             : group_wait<4, 128>(warp == 4, lane == 0, (bar), (parity), true, go, abort_flag,   \
+                                  limit, c.err, (tag)))
+
+        // ---- initial state: row `st` of H^T (= column st of H), sigma = 1
+#pragma unroll 1
+        for (int g = 0; g < 8; ++g) {
+            uint32_t x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int k = 16 * g + j;
+                float v0 = 0.f;
+                if (SUMMARY)
+                    v0 = (m_part && k == st) ? 1.f : 0.f;
+                else if (c.h_start)
+                    v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + st];
+                x[j] = __float_as_uint(v0);
+            }
+            tmem_st16(t_row + tm_h + 16 * g, x);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        pack_bar(sg);
+
+        bool live = true;   // uniform over the group
+        int done = 0;       // chunks completed
+#pragma unroll 1
+        for (int n = 0; n < nchunks; ++n) {
+            // R^T buffer: the summary's M part has its own; otherwise the parity's U buffer
+            const uint32_t tu_col = m_part ? F::TM_RM : TM_U + (n % NUB) * F::TU_STRIDE;
+            const float* sc = scal + (n & 1) * (SC_N * 64);
+            // the chunk's scalars are published with PREPDONE; S12 retires after it
+            live = live && swait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE);
+            float fold = 1.f;
+            if (live) {
+                fold = sc[SC_MISC * 64];
+                sig_next = sc[SC_MISC * 64 + 1];
+            }
+            live = live && swait(bar_s, bars_phase, TAG_BARS);
+            bars_phase ^= 1u;
+            if (live) {
+                tc_fence_after();
+                // ---- scaled R^T -> packed bf16 hi/lo in TMEM (and, rarely, fold sigma into H_s)
+                const uint32_t rd_col = tu_col;   // packed in place
+                {
+                    const float* dd = sc + SC_DD * 64;
+                    const uint32_t t_ur = t_row + tu_col;
+#pragma unroll 1
+                    for (int g2 = 0; g2 < 4; g2 += 2) {
+                      float r2[2][16];
+                      tmem_ld16(t_ur + 16 * g2, r2[0]);
+                      tmem_ld16(t_ur + 16 * g2 + 16, r2[1]);
+                      tmem_wait_ld();
+#pragma unroll
+                      for (int gg = 0; gg < 2; ++gg) {
+                        const int g = g2 + gg;
+                        const float* r = r2[gg];
+                        // packed column q holds the pair (2q, 2q+1) of the 64 tokens j
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float2 d2 = *reinterpret_cast<const float2*>(dd + 16 * g + 2 * j);
+                            const float x0 = r[2 * j] * d2.x;
+                            const float x1 = r[2 * j + 1] * d2.y;
+                            // hi = x truncated to bf16 (its top 16 bits), lo = the exact remainder
+                            // truncated to bf16: hi + lo is within 2^-16 |x| of x. Integer and
+                            // byte-permute operations only, no conversions.
+                            const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+                            hi[j] = __byte_perm(b0, b1, 0x7632);
+                            const float l0 = x0 - __uint_as_float(b0 & 0xFFFF0000u);
+                            const float l1 = x1 - __uint_as_float(b1 & 0xFFFF0000u);
+                            lo[j] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
+                        }
+                        // (in the summary this overwrites the 16 columns just read)
+                        tmem_st8(t_row + rd_col + 16 * g, hi);
+                        tmem_st8(t_row + rd_col + 16 * g + 8, lo);
+                      }
+                    }
+                    if (fold != 1.f) {
+#pragma unroll 1
+                        for (int g = 0; g < 8; ++g) {
+                            float x[16];
+                            uint32_t y[16];
+                            tmem_ld16(t_row + tm_h + 16 * g, x);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) y[j] = __float_as_uint(x[j] * fold);
+                            tmem_st16(t_row + tm_h + 16 * g, y);
+                        }
+                    }
+                    tmem_wait_st();
+                }
+                done = n + 1;
+            }
+            tc_fence_before();
+            pack_bar(sg);   // the issuer's S4 reads the packed R^T
+        }
+
+        // every MMA the group's issuer issued (the last S4) completes before the final state
+        // is read out or tensor memory is released
+        const bool drained = live && swait(bar0 + B_SDRAIN, 0, TAG_BARS);
+        if (!drained) {
+            if (st == 0) mbar_drain(bar0 + B_SDRAIN, 0, limit);
+        } else {
+            tc_fence_after();
+            // ---- the chain's final state H = sigma H_s: thread v writes column v of H
+            float* dst = nullptr;
+            if (SUMMARY) {
+                const long long sb = ((long long)seg * c.B * c.H + bh) * kD * kD;
+                dst = (m_part ? c.M : c.S) + sb;
+            } else if (c.h_final && seg == c.nseg_total - 1) {
+                dst = c.h_final + bhoff;
+            }
+            // the forward may also hand its final state to the next segment
+            float* dst2 = (!SUMMARY && c.h_out) ? c.h_out + (seg + 1) * c.h_out_seg_stride + bhoff : nullptr;
+            if (dst || dst2) {
+                const float sgm = done > 0 ? sig_next : 1.f;
+#pragma unroll 1
+                for (int g = 0; g < 8; ++g) {
+                    float x[16];
+                    tmem_ld16(t_row + tm_h + 16 * g, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const long long idx = (long long)(16 * g + j) * kD + st;
+                        if (dst) dst[idx] = sgm * x[j];
+                        if (dst2) dst2[idx] = sgm * x[j];
+                    }
+                }
+            }
+        }
+#undef swait
     } else {
         // ================================== state =================================
         // state group sg: the forward's only group, or the summary's M part (0) / S part (1)
