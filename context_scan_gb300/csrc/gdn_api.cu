@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 
@@ -18,12 +19,20 @@ constexpr size_t kHeaderBytes = 256;   // device error word lives here
 constexpr size_t kAlign = 256;
 constexpr int kMaxSub = 8;             // pieces per segment (segmented forward)
 constexpr int kMinPieceChunks = 8;     // shortest piece, in chunks
+constexpr int kMaxUnevenPieces = 16;   // unequal pieces (one wave per phase): at most this many
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// How the segmented forward cuts each sequence: P pieces; piece 0 has `first` chunks and the
+// others `rest` each (first == rest: equal pieces, whose starts include every segment start).
+struct PiecePlan {
+    int P, first, rest;
+};
 
 struct WsLayout {
     size_t off_wy, off_M, off_S, off_Hp, total;
     int pieces;
+    PiecePlan plan;
 };
 
 // Shapes that take the tcgen05 kernels (which also need the per-chunk WY tiles).
@@ -47,30 +56,54 @@ int sm_count() {
     return sms;
 }
 
-// Pieces P per sequence for the segmented forward (a multiple of nseg: segment starts are
-// piece starts). Piece 0's forward runs from h0 beside the summaries of pieces 1..P-2; an
-// in-order scan gives the state entering every piece; pieces 1..P-1 then run their forward.
-// Each phase launches B*H*(P-1) chains of T/P tokens, one per SM at a time, so more pieces
-// mean more parallel chains (and fuller waves) but shorter ones and one more scan step each.
-// P minimises 2 * waves(B*H*(P-1)) * chunks / P + 3 * (P - 2) (in chunk times; a scan step
-// costs about three), over P = nseg * {1, 2, 4, 8} with pieces of at least 8 chunks. Without a
-// device to size the waves it stays at nseg.
-int plan_pieces(const gdn_problem& p, int nseg) {
-    if (p.T <= 0) return nseg;
+// Pieces per sequence for the segmented forward. Piece 0's forward runs from h0 beside the
+// summaries of pieces 1..P-2; an in-order scan gives the state entering every piece; pieces
+// 1..P-1 then run their forward. Each phase launches B*H*(P-1) chains, one per SM at a time.
+// Costs in chunk times (a summary chunk costs kSumRatio of a forward chunk, a scan step about
+// three):
+//  - equal pieces, P = nseg * {1, 2, 4, 8} (segment starts are piece starts, pieces of at
+//    least 8 chunks): 2 * waves(B*H*(P-1)) * chunks / P + 3 * (P - 2);
+//  - tcgen05 path only, when both phases fit in one wave (B*H*(P-1) <= SMs): piece 0 of L0
+//    chunks and pieces 1..P-1 of x chunks, x = chunks / (P - 1 + kSumRatio), so that piece 0's
+//    forward and the summaries end together: max(L0, kSumRatio x) + x + 3 * (P - 2). The
+//    forward kernels then write the states entering the segments as they pass them.
+// Without a device to size the waves it stays at nseg equal pieces.
+constexpr double kSumRatio = 0.8;
+
+PiecePlan plan_pieces(const gdn_problem& p, int nseg) {
     const int chunks = p.T / gdn::kChunk;   // a multiple of nseg (checked)
+    PiecePlan best{nseg, chunks / nseg, chunks / nseg};
+    if (p.T <= 0) return best;
     const int sms = sm_count();
-    if (sms < 1) return nseg;
+    if (sms < 1) return best;
     const double bh = (double)p.B * p.H;
-    auto cost = [&](int P) {
+    auto cost_equal = [&](int P) {
         const double waves = std::ceil(bh * (P > 1 ? P - 1 : 1) / sms);
         const double phases = P > 1 ? 2.0 : 1.0;
         return phases * waves * ((double)chunks / P) + 3.0 * (P > 2 ? P - 2 : 0);
     };
-    int best = nseg;
+    double best_cost = cost_equal(nseg);
     for (int nsub = 2; nsub <= kMaxSub; nsub *= 2) {
         const int P = nseg * nsub;
         if ((chunks / nseg) % nsub != 0 || chunks / P < kMinPieceChunks) break;
-        if (cost(P) < cost(best)) best = P;
+        const double c = cost_equal(P);
+        if (c < best_cost) {
+            best_cost = c;
+            best = PiecePlan{P, chunks / P, chunks / P};
+        }
+    }
+    if (tc_shape(p) && gdn::tc_runtime_ok()) {
+        for (int P = 3; P <= kMaxUnevenPieces && bh * (P - 1) <= sms; ++P) {
+            int x = (int)std::ceil(chunks / (P - 1 + kSumRatio));
+            if (chunks - (P - 1) * x < 1) x = (chunks - 1) / (P - 1);
+            const int first = chunks - (P - 1) * x;
+            if (x < kMinPieceChunks || first < 1) break;
+            const double c = std::max((double)first, kSumRatio * x) + x + 3.0 * (P - 2);
+            if (c < best_cost) {
+                best_cost = c;
+                best = PiecePlan{P, first, x};
+            }
+        }
     }
     return best;
 }
@@ -80,7 +113,8 @@ int plan_pieces(const gdn_problem& p, int nseg) {
 WsLayout layout(const gdn_problem& p, int nseg) {
     WsLayout w{};
     const size_t bh = (size_t)p.B * p.H;
-    w.pieces = plan_pieces(p, nseg);
+    w.plan = plan_pieces(p, nseg);
+    w.pieces = w.plan.P;
     w.off_wy = kHeaderBytes;
     const size_t wy_bytes = tc_shape(p) ? bh * (size_t)(p.T / gdn::kChunk) * 16384u : 0;
     w.off_M = w.off_wy + round_up(wy_bytes);
@@ -182,6 +216,7 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
                          void* const* events) {
     const WsLayout w = layout(*p, nseg);
     const int P = w.pieces, nsub = P / nseg;
+    const bool equal = w.plan.first == w.plan.rest;   // else the forwards write H_in_out
     const int BH = p->B * p->H;
     char* wsb = reinterpret_cast<char*>(workspace);
     if (mark(events, 0, s) != cudaSuccess || mark(events, 1, s) != cudaSuccess ||
@@ -210,8 +245,13 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
         c.g = g;
         c.beta = beta;
         c.o = o;
-        c.seg_len = p->T / P;
+        c.seg_len = w.plan.rest * gdn::kChunk;
+        c.first_chunks = w.plan.first;
         c.nseg_total = P;
+        if (!equal) {
+            c.H_seg = H_in_out;
+            c.seg_chunks = p->T / gdn::kChunk / nseg;
+        }
         return c;
     };
     // 0. the WY tiles of every chunk (tcgen05 path only)
@@ -245,7 +285,8 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
     // 2. the state entering every piece (and every segment)
     if (mark(events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (P >= 2)
-        e = gdn::launch_scan(M, S, Hp + hstride, Hp, H_in_out, h0, 1, P, nsub, BH, p->K, p->V, s);
+        e = gdn::launch_scan(M, S, Hp + hstride, Hp, equal ? H_in_out : nullptr, h0, 1, P,
+                             equal ? nsub : 1, BH, p->K, p->V, s);
     else if (H_in_out)
         e = gdn::launch_scan(nullptr, nullptr, h0, nullptr, H_in_out, nullptr, 0, 1, 1, BH, p->K, p->V, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -313,7 +354,7 @@ size_t gdn_workspace_bytes(const gdn_problem* p, int nseg) {
 
 int gdn_segmented_pieces(const gdn_problem* p, int nseg) {
     if (check_problem(p, nseg) != GDN_OK) return 0;
-    return plan_pieces(*p, nseg);
+    return plan_pieces(*p, nseg).P;
 }
 
 gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,

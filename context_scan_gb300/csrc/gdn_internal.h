@@ -38,6 +38,9 @@ struct ChainParams {
     void* wy;
     int B, T, H, K, V;
     int seg_len;       // tokens per segment (multiple of 64)
+    // tcgen05 path: chunks of segment 0 when it differs from the others (0 = the same):
+    // segment s > 0 then starts at chunk first_chunks + (s - 1) * seg_len / 64
+    int first_chunks;
     int seg_first;     // first segment this launch processes
     int nseg_run;      // segments this launch processes: seg_first .. seg_first+nseg_run-1
     int nseg_total;    // segments in the whole problem
@@ -45,6 +48,12 @@ struct ChainParams {
     // h_out + (s + 1) * h_out_seg_stride + (b*H + h)*K*V (the state entering segment s + 1)
     float* h_out;
     long long h_out_seg_stride;
+    // forward, tcgen05 path: when non-null, the state entering every chunk g (counted from
+    // the start of the sequence) with g % seg_chunks == 0 that the chain walks is written to
+    // H_seg + (g / seg_chunks)*B*H*K*V + (b*H + h)*K*V (the states entering the API's
+    // segments when pieces and segments do not coincide)
+    float* H_seg;
+    int seg_chunks;
     // varlen (null otherwise): the batch is packed, sequence b holds tokens cu_seqlens[b] ..
     // cu_seqlens[b+1]-1 (B = number of sequences, T = total tokens, one segment); its chunks
     // are numbered from cu_chunks[b] (the last one may be partial) and the WY tiles are
@@ -85,6 +94,7 @@ cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, i
 
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);
+bool tc_runtime_ok();   // the driver entry point that encodes tensor maps is available
 cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all chunks of every (b, h)
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);

@@ -214,13 +214,17 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     // tokens of this chain: a segment of the fixed-length batch, or a whole varlen sequence
     // (whose last chunk may be partial: its padding tokens get g = 0 here and beta = 0 in the
     // WY tiles, which leaves the state untouched, and their outputs are not stored)
-    const int seq_tokens = VARLEN ? c.cu_seqlens[b + 1] - c.cu_seqlens[b] : c.seg_len;
-    const int nchunks = VARLEN ? (seq_tokens + kC - 1) / kC : c.seg_len / kC;
+    // (fixed length: segment 0 may be longer or shorter than the others, see first_chunks)
+    const int seg_chunks0 = c.first_chunks > 0 ? c.first_chunks : c.seg_len / kC;
+    const int chunk0 = VARLEN || seg == 0 ? 0 : seg_chunks0 + (seg - 1) * (c.seg_len / kC);
+    const int seq_tokens =
+        VARLEN ? c.cu_seqlens[b + 1] - c.cu_seqlens[b] : (seg == 0 ? seg_chunks0 * kC : c.seg_len);
+    const int nchunks = (seq_tokens + kC - 1) / kC;
     constexpr bool need_v = true;   // every CTA forms U (the forward, or the summary's S part)
     const long long limit = p.wait_limit;
     const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
     const long long row_seg = VARLEN ? (long long)c.cu_seqlens[b]   // flattened (b, t)
-                                           : (long long)b * c.T + (long long)seg * c.seg_len;
+                                           : (long long)b * c.T + (long long)chunk0 * kC;
 
     // A forward grid lets a grid launched after it as its programmatic dependent start right
     // away (the summaries that run beside the first piece's forward); a summary grid so
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         const uint32_t wy_skip = 16384u - wy_bytes;
         const uint8_t* wy_chain = reinterpret_cast<const uint8_t*>(c.wy) +
                                   ((VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[b]
-                                                 : (long long)bh * (c.T / kC) + (long long)seg * nchunks)
+                                                 : (long long)bh * (c.T / kC) + chunk0)
                                    << 14);
         int k_last[KST], q_last[2] = {-1, -1}, a_last[2] = {-1, -1}, v_last = -1;
 #pragma unroll
@@ -964,6 +968,23 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             const uint32_t t_u = tmem + tu_col;
             const uint32_t t_o = t_u + 64;   // forward only
             const float* sc = scal + (n & 1) * (SC_N * 64);
+            // ---- the state entering this chunk, when an API segment starts here (the pieces
+            //      a sequence is cut into need not start at segment starts): H = sigma H_s
+            //      once the previous chunk's S4 has retired; thread v writes column v
+            if (!VARLEN && c.H_seg && (chunk0 + n) % c.seg_chunks == 0) {
+                if (s4_pending && !swait(bar_s, s4_parity, TAG_BARS)) break;
+                s4_pending = false;
+                tc_fence_after();
+                float* dst = c.H_seg + (long long)((chunk0 + n) / c.seg_chunks) * c.B * c.H * kD * kD + bhoff;
+#pragma unroll 1
+                for (int g = 0; g < 8; ++g) {
+                    float x[16];
+                    tmem_ld16(t_row + tm_h + 16 * g, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[(long long)(16 * g + j) * kD + st] = sig_next * x[j];
+                }
+            }
             if (!swait(bar0 + B_PREPDONE, n & 1, TAG_PREPDONE)) break;
             // the previous chunk's S4 has updated H_s (the issuing thread waits; if it gives up
             // it raises the abort flag, issues nothing, and the group stops at its next wait)
@@ -1181,6 +1202,8 @@ bool tc_supported(const ChainParams& p) {
     return p.in_bf16 && p.K == kD && p.V == kD && !p.gate_k &&
            (p.cu_seqlens || (p.seg_len > 0 && p.seg_len % kC == 0)) && encode_fn() != nullptr;
 }
+
+bool tc_runtime_ok() { return encode_fn() != nullptr; }
 
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s) { return launch<false>(p, s); }
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s) { return launch<true>(p, s); }

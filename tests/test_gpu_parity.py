@@ -27,6 +27,9 @@ SMALL = {
     "slow_decay_h4_t1k_cp16": W["slow_decay_h4_t1k_cp16"],
     "bf16_k64_cp4": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=3, T=512, K=64, V=64),
     "one_chunk_segments": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=512, nseg=8),
+    # few chains on many SMs: unequal pieces whose starts are not segment starts, so the
+    # forwards write the states entering the segments as they pass them
+    "uneven_pieces_cp4": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=4096),
 }
 
 
