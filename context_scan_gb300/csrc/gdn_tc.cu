@@ -129,13 +129,15 @@ constexpr uint32_t B_KFULL = 0, B_KEMPTY = 32, B_QFULL = 64, B_QEMPTY = 80, B_AF
                    B_AEMPTY = 112, B_VFULL = 128, B_VEMPTY = 136, B_BARP = 144, B_BARS = 152,
                    B_PREPDONE = 160, B_WFREE = 168, B_UFREE = 176, B_TMEM = 192, B_ABORT = 196,
                    B_GO_S = 200, B_GO_P = 204, B_BARS1 = 208, B_GO_S1 = 216, B_CDONE = 224,
-                   B_WREAD = 232, B_MDRAIN = 240, B_SDRAIN = 248, B_S4 = 256, B_S4B = 264;
+                   B_WREAD = 232, B_MDRAIN = 240, B_SDRAIN = 248, B_S4 = 256, B_S4B = 264,
+                   B_EPIDONE = 272, B_P1DONE = 280;
 
 // wait tags recorded in the device error word's detail field
 enum : unsigned {
     TAG_KFULL = 1, TAG_BARP = 2, TAG_BARS = 3, TAG_KEMPTY = 4, TAG_VEMPTY = 5, TAG_PREPDONE = 6,
     TAG_WFREE = 7, TAG_UFREE = 8, TAG_VFULL = 9, TAG_QFULL = 10, TAG_QEMPTY = 11,
-    TAG_AFULL = 12, TAG_AEMPTY = 13, TAG_CDONE = 14, TAG_WREAD = 15
+    TAG_AFULL = 12, TAG_AEMPTY = 13, TAG_CDONE = 14, TAG_WREAD = 15, TAG_EPIDONE = 16,
+    TAG_P1DONE = 17
 };
 
 struct TcParams {
@@ -255,6 +257,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         mbar_init(bar0 + B_SDRAIN, NSG);   // each state group's last MMAs
         mbar_init(bar0 + B_S4, 1);         // S4 retired (state group 0's issuer)
         mbar_init(bar0 + B_S4B, 1);        // S4 retired (state group 1's issuer)
+        mbar_init(bar0 + B_EPIDONE, 1);    // forward: the parity's O^T buffer has been read out
+        mbar_init(bar0 + B_P1DONE, 1);     // forward: Q K^T is in TM_S
         *abort_flag = 0;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S) = 1;
         *reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_S1) = 1;
@@ -416,27 +420,28 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             auto ok = [&](uint32_t bar, uint32_t parity, unsigned tag) {
                 return mbar_wait(bar, parity, abort_flag, limit, c.err, tag);
             };
-            // P1: [Q ; -] K^T -> TM_S for chunk m; lanes 0..63 hold Q K^T (rows 64..127 of the
-            // A operand run into the next buffer and are never read)
-            auto p1 = [&](int m) {
-                const uint32_t kst1 = base + L::K0 + (m % KST) * 16384;
-                const uint32_t qst1 = base + L::Q0 + (m & 1) * 16384;
+#pragma unroll 1
+            for (int n = 0; n < nchunks; ++n) {
+                const int as = n % AST;
+                const uint32_t kst = base + L::K0 + (n % KST) * 16384;
+                const uint32_t qst = base + L::Q0 + (n & 1) * 16384;
+                const uint32_t ast = base + L::A0 + as * 16384;
+                const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
+                // P1: [Q ; -] K^T -> TM_S once the C warps have read chunk n-1's Q K^T out of
+                // it; lanes 0..63 hold Q K^T (rows 64..127 of the A operand run into the next
+                // buffer and are never read)
+                bool run = (n == 0 || ok(bar0 + B_CDONE, (n - 1) & 1, TAG_CDONE)) &&
+                           ok(bar0 + B_KFULL + 8 * (n % KST), (n / KST) & 1, TAG_KFULL) &&
+                           ok(bar0 + B_QFULL + 8 * (n & 1), (n >> 1) & 1, TAG_QFULL);
+                if (!run) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k16 = 0; k16 < 8; ++k16) {
                     const uint32_t off = (k16 >> 2) * 8192 + (k16 & 3) * 32;
-                    mma_ss<ID_P1>(tmem + TM_S, desc_k(qst1 + off), desc_k(kst1 + off), k16 > 0);
+                    mma_ss<ID_P1>(tmem + TM_S, desc_k(qst + off), desc_k(kst + off), k16 > 0);
                 }
-                mma_commit(bar0 + B_BARP);
-            };
-            bool run = ok(bar0 + B_KFULL, 0, TAG_KFULL) && ok(bar0 + B_QFULL, 0, TAG_QFULL);
-            if (run) p1(0);
-#pragma unroll 1
-            for (int n = 0; run && n < nchunks; ++n) {
-                const int as = n % AST;
-                const uint32_t kst = base + L::K0 + (n % KST) * 16384;
-                const uint32_t ast = base + L::A0 + as * 16384;
-                const uint32_t t_u = tmem + TM_U + (n % NUB) * F::TU_STRIDE;
+                mma_commit(bar0 + B_P1DONE);
+                // P2: U^T into the parity's U buffer once chunk n-2 has retired it
                 run = (n < NUB || ok(bar0 + B_UFREE + 8 * (n % NUB), ((n / NUB) - 1) & 1, TAG_UFREE)) &&
                       ok(bar0 + B_AFULL + 8 * as, (n / AST) & 1, TAG_AFULL) &&
                       ok(bar0 + B_VFULL, n & 1, TAG_VFULL);
@@ -447,21 +452,16 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
                                    desc_k(ast + k16 * 32), k16 > 0);
                 mma_commit(bar0 + B_VEMPTY);
-                if (!(run = ok(bar0 + B_CDONE, n & 1, TAG_CDONE))) break;
+                // P3: W^T into the parity's O^T buffer once the prep group has stored chunk
+                // n-2's output rows from it (S12 of chunk n then accumulates O^T there)
+                if (!(run = ok(bar0 + B_EPIDONE, n & 1, TAG_EPIDONE))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
+                    mma_ss<ID_P23>(tmem + TM_U + (n & 1) * 128 + 64, desc_mn(kst + k16 * 2048, 8192),
                                    desc_k(ast + 8192 + k16 * 32), k16 > 0);
                 mma_commit(bar0 + B_AEMPTY + 8 * as);
                 mma_commit(bar0 + B_BARP);   // covers P2 as well
-                if (n + 1 < nchunks) {
-                    const int m = n + 1;
-                    run = ok(bar0 + B_WREAD, n & 1, TAG_WREAD) &&
-                          ok(bar0 + B_KFULL + 8 * (m % KST), (m / KST) & 1, TAG_KFULL) &&
-                          ok(bar0 + B_QFULL + 8 * (m & 1), (m >> 1) & 1, TAG_QFULL);
-                    if (run) p1(m);
-                }
             }
             // everything issued here retires before tensor memory is released
             mma_commit(bar0 + B_MDRAIN);
@@ -475,8 +475,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
         constexpr int ECOLS = 64 / F::NGRP;      // W^T / O^T columns per warp group
         const uint32_t t_row = tmem + ((uint32_t)(lq * 32) << 16);   // this warp's TMEM lanes
         volatile int* go = reinterpret_cast<volatile int*>(sm + L::BAR + B_GO_P);
-        uint32_t barp_phase = 0;
-        bool barp_pending = false;
+        uint32_t barp_phase = 0;   // one phase of B_BARP per chunk (P3 and P2 retired)
         float lam = 0.f;   // log2 sigma before the current chunk (prep warp pw 2)
 
         // the group's first warp waits (optionally) and publishes a verdict that all read
@@ -485,7 +484,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     group_wait<2, kPrepThreads>(pw == 0, lane == 0, (bar), (parity), (doit), go, abort_flag, \
                                 limit, c.err, (tag))
 #define pmma_wait() \
-    (pwait(bar0 + B_BARP, barp_phase, TAG_BARP, true) ? (barp_phase ^= 1u, barp_pending = false, true) : false)
+    (pwait(bar0 + B_BARP, barp_phase, TAG_BARP, true) ? (barp_phase ^= 1u, true) : false)
 // A warp waits on its own (all lanes poll together; lane 0's verdict is broadcast, so the
 // warp stays uniform). If it gives up, the abort flag is up and the group stops at its next
 // group wait.
@@ -500,18 +499,6 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                    ((row_seg + (long long)(m) * kC + 32 * grp) * c.H + h) * kD + 32 * lq + lane, \
                    tok_stride, VARLEN ? seq_tokens - ((m) * kC + 32 * grp) : 32)
 
-// this warp's lane quarter of the output rows of chunk n-2 (its group's 32 token columns),
-// then zero those cells of the parity's O^T buffer
-#define epilogue()                                                                            \
-    do {                                                                                      \
-        tc_fence_after();                                                                     \
-        if (n >= 2) store_output(n - 2);                                                      \
-        const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,                            \
-                                   0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};                           \
-        tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp, zero);                        \
-        tmem_st16(t_row + TM_U + (n & 1) * 128 + 64 + 32 * grp + 16, zero);                   \
-        tmem_wait_st();                                                                       \
-    } while (0)
 
 #pragma unroll 1
         for (int n = 0; n < nchunks; ++n) {
@@ -558,12 +545,18 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             }
             __syncwarp();
             if (!SUMMARY) {
-                named_bar<2, kPrepThreads>();   // publishes the scalars
+                // ---- every warp: its share of the output rows of chunk n-2 (retired above) from
+                //      the parity's O^T buffer, which the MMA warp's P3 then reuses for W^T
+                tc_fence_after();
+                if (n >= 2) store_output(n - 2);
+                tc_fence_before();
+                named_bar<2, kPrepThreads>();   // the scalars are published, the O^T buffer read
+                if (pt == 0) mbar_arrive(bar0 + B_EPIDONE);
                 if (lq < 2) {
                     // ---- C rows i = lanes 0..63 (warps of lane quarters 0, 1), this group's 32
                     //      columns j, tf32 K-major; once every C warp has read Q K^T out of TM_S,
-                    //      the MMA warp issues P3 into it
-                    if (warp_wait(bar0 + B_BARP, barp_phase, abort_flag, limit, c.err, TAG_BARP, lane)) {
+                    //      the MMA warp issues the next chunk's P1 into it
+                    if (warp_wait(bar0 + B_P1DONE, n & 1, abort_flag, limit, c.err, TAG_P1DONE, lane)) {
                         tc_fence_after();
                         const float* gam = sc + SC_GAM * 64;
                         const int i = 32 * lq + lane;
@@ -594,15 +587,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                     named_bar<3, 128>();   // the C warps only
                     if (pt == 0) mbar_arrive(bar0 + B_CDONE);
                     __syncwarp();
-                    // ---- while P3 runs: this warp's share of the output rows of chunk n-2
-                    //      (retired above), then zero it in its O^T buffer, which S12 of this
-                    //      chunk accumulates into
-                    epilogue();
                 } else {
-                    // ---- output rows first (chunk n-1's S12 is still reading the sigma Qd
-                    //      buffer), then sigma Qd = sigma 2^G_i q_i as tf32 K-major: row i,
-                    //      feature half kh
-                    epilogue();
+                    // ---- sigma Qd = sigma 2^G_i q_i as tf32 K-major: row i, feature half kh
                     // (the q tile's arrival is waited for here: P1 is the MMA warp's)
                     if (warp_wait(bar0 + B_WFREE, (n - 1) & 1, abort_flag, limit, c.err, TAG_WFREE,
                                   lane, n >= 1) &&
@@ -633,13 +619,13 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                         }
                     }
                 }
-                barp_phase ^= 1u;   // P1's phase, consumed by the C warps
                 fence_proxy_async();   // sigma Qd and C are read by the state group's MMAs
-                barp_pending = true;
             }
             // (the summary's P2 and P3 are the MMA warp's)
             if (!pmma_wait()) break;   // P3 (and P2) done; for the forward also every C and Qd
             tc_fence_after();
+            // W^T: in TM_S (summary) or in the parity's O^T buffer (forward)
+            const uint32_t t_w = t_row + (SUMMARY ? TM_S : TM_U + (n & 1) * 128 + 64) + ECOLS * grp;
             // ---- -sigma W as rows 0..63 of the S12 B operand, once chunk n-1's S12 retired
             //      (the forward's Qd warps waited for that before the barrier above)
             {
@@ -652,8 +638,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #pragma unroll 1
                 for (int hb = 0; hb < ECOLS; hb += 32) {
                     float w2[2][16];
-                    tmem_ld16(t_row + TM_S + ECOLS * grp + hb, w2[0]);
-                    tmem_ld16(t_row + TM_S + ECOLS * grp + hb + 16, w2[1]);
+                    tmem_ld16(t_w + hb, w2[0]);
+                    tmem_ld16(t_w + hb + 16, w2[1]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
@@ -665,19 +651,26 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                                 tf32_operand(nsig * w[ii]);
                     }
                 }
+                if (!SUMMARY) {
+                    // the forward's S12 accumulates this chunk's O^T from zero here
+                    const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
+                                               0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    tmem_st16(t_w, zero);
+                    tmem_st16(t_w + 16, zero);
+                    tmem_wait_st();
+                }
             }
             fence_proxy_async();
             tc_fence_before();
             named_bar<2, kPrepThreads>();
             // ---- the chunk is ready for the state group; in the forward the q tile is consumed
-            //      (P1 and sigma Qd) and TM_S is free again for the MMA warp's next P1
+            //      (P1 and sigma Qd); in the summary TM_S is free again for the next P3
             if (pt == 0) {
                 mbar_arrive(bar0 + B_PREPDONE);
                 if (!SUMMARY) mbar_arrive(bar0 + B_QEMPTY + 8 * qs);
-                mbar_arrive(bar0 + B_WREAD);
+                else mbar_arrive(bar0 + B_WREAD);
             }
         }
-#undef epilogue
         if (*go == 0) {
             // (the prep MMAs are the MMA warp's, which lets them retire itself)
         } else if (!SUMMARY) {
@@ -1017,16 +1010,6 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             sig_next = sc[SC_MISC * 64 + 1];
             if (!smma_wait()) break;
             tc_fence_after();
-            // ---- forward: S3 O^T += R^T C^T (A = R^T in TMEM) goes to the tensor pipe now and
-            //      runs during the packing below (both only read R^T)
-            if (!SUMMARY && st == 0) {
-                const uint32_t cb = base + L::C0 + (n & 1) * 16384;
-#pragma unroll
-                for (int k8 = 0; k8 < 8; ++k8)
-                    mma_ts_tf32<ID_TF>(t_o, t_u + k8 * 8,
-                                       desc_k(cb + (k8 >> 2) * 8192 + (k8 & 3) * 32), 1u);
-            }
-            __syncwarp();
             // ---- scaled R^T -> packed bf16 hi/lo in TMEM (and, rarely, fold sigma into H_s)
             const uint32_t rd_col = SUMMARY ? tu_col : TM_RD;
             {
@@ -1077,6 +1060,17 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                 }
                 tmem_wait_st();
             }
+            // ---- S3 O^T += R^T C^T (A = R^T in TMEM), issued once this warp has packed (the
+            //      issuing thread stalls while the tensor pipe takes the MMAs; before the pack
+            //      that stall would hold back the pack and with it S4)
+            if (st == 0) {
+                const uint32_t cb = base + L::C0 + (n & 1) * 16384;
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8)
+                    mma_ts_tf32<ID_TF>(t_o, t_u + k8 * 8,
+                                       desc_k(cb + (k8 >> 2) * 8192 + (k8 & 3) * 32), 1u);
+            }
+            __syncwarp();
             tc_fence_before();
             sbar();
             // ---- S4: H_s^T += (R^T D) K (A = hi, lo in TMEM); its commits also cover S3. Only
