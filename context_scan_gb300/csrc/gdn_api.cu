@@ -68,7 +68,7 @@ int sm_count() {
 //    forward and the summaries end together: max(L0, kSumRatio x) + x + 3 * (P - 2). The
 //    forward kernels then write the states entering the segments as they pass them.
 // Without a device to size the waves it stays at nseg equal pieces.
-constexpr double kSumRatio = 0.8;
+constexpr double kSumRatio = 0.87;
 
 PiecePlan plan_pieces(const gdn_problem& p, int nseg) {
     const int chunks = p.T / gdn::kChunk;   // a multiple of nseg (checked)
