@@ -31,6 +31,7 @@
 //   P1  [Q ; -] K^T        rows 0..63: Q K^T (rows 64..127 unused)      kind::f16 (bf16)
 //   P2  U^T = V^T (A diag(beta))^T                                      kind::f16
 //   P3  W^T = K^T (A diag(beta 2^Gx))^T                                 kind::f16
+//       (forward: into the parity's O^T buffer, read out and zeroed before S12 runs there)
 //   S12 [R^T | O^T] = [U^T | 0] + H_s^T [-sigma W ; sigma Qd]^T       kind::tf32, N = 128
 //       (A = H_s^T from tensor memory; the summary has no O and runs the R^T half, N = 64)
 //   S3  O^T += R^T C^T                     A = R^T from tensor memory   kind::tf32
@@ -39,18 +40,22 @@
 // The fp32 state and the corrected values R never pass through bf16. Exponents are always
 // differences of cumulative gates or bounded by the renormalisation.
 //
-// Warp roles: warps 0-3 "state" (tensor-memory lanes 0..127; S1-S4, final state), warps
-// 4-11 "prep" (two warp groups, each covering lanes 0..127: P1-P3, gate cumsum and the
-// sigma bookkeeping, C, sigma Qd, -sigma W, and the output rows of chunk n-2; P1 of chunk
-// n+1 is issued as soon as chunk n's W^T has been read out of tensor memory), warp 12
-// "producer" (TMA loads of the q/k/v tiles with 128-byte swizzle, bulk copies of the WY
-// tiles, gates). Rings: k in KST stages (released by S4), q in two (released by prep), WY
-// tiles in AST (released by P3), v in one (released by P2). Prep of chunk n+1 runs while the
-// state group works on chunk n. Each group issues its own MMAs (commits track the issuing
-// thread's MMAs). Named barriers are the non-.aligned form: a group's leader warp diverges
-// around its mbarrier poll. Every wait on an mbarrier is bounded: on expiry the kernel
-// records GDN_ERR_TIMEOUT in the device error word, drains what it issued and frees tensor
-// memory.
+// Warp roles (forward, 14 warps): warps 0-3 "state" (tensor-memory lanes 0..127: S12, S3,
+// S4 issued by thread 0, the pack of R^T, final state); warps 4-11 "prep" (two warp groups,
+// each covering lanes 0..127: gate cumsum and the sigma bookkeeping, the output rows of chunk
+// n-2, C from Q K^T (the warps of lanes 0..63), sigma Qd, -sigma W); warp 12 issues the prep
+// MMAs: P1 of chunk n once the C warps have read chunk n-1's Q K^T out of TM_S, P2 once chunk
+// n-2 has retired its U buffer, P3 once the prep warps have stored chunk n-2's output rows
+// from the O^T buffer P3 writes; warp 13 "producer" (TMA loads of the q/k/v tiles with
+// 128-byte swizzle, bulk copies of the WY tiles, gates). The summary (16 warps) has two
+// state groups (M part, S part), one prep group, the MMA warp for P2/P3, the producer, and
+// one warp per state group that issues that group's S12 and S4 while the group only packs.
+// Rings: k in KST stages (released by S4), q in two (released by prep), WY tiles in AST
+// (released by P3), v in one (released by P2). Prep of chunk n+1 runs while the state group
+// works on chunk n. Commits track the issuing thread's MMAs. Named barriers are the
+// non-.aligned form: a group's leader warp diverges around its mbarrier poll. Every wait on
+// an mbarrier is bounded: on expiry the kernel records GDN_ERR_TIMEOUT in the device error
+// word, drains what it issued and frees tensor memory.
 #include <cstring>
 
 #include "gdn_tc_common.cuh"
@@ -80,9 +85,10 @@ struct Cfg {
     static constexpr int ISSUE_WARP0 = PRODUCER_WARP + 1;
     static constexpr int THREADS = 32 * (ISSUE_WARP0 + (SUMMARY ? NSG : 0));
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TM_S = 0;    // Q K^T, then W^T (prep)
+    static constexpr uint32_t TM_S = 0;    // forward: Q K^T; summary: W^T
     static constexpr uint32_t TM_U = 64;   // U^T -> R^T, two buffers by chunk parity; the
-                                           // forward keeps O^T right after each (64 + 128 p)
+                                           // forward keeps W^T, then O^T right after each
+                                           // (64 + 128 p)
     static constexpr int NUB = 2;                            // U buffers
     static constexpr uint32_t TU_STRIDE = SUMMARY ? 64 : 128;
     // scaled R^T packed as bf16 pairs, 16 tokens per 16 columns: hi in the first 8, lo in
