@@ -247,25 +247,33 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
                      : "memory");
     }
 
-    // ---- diagonal 16 x 16 blocks of (I + L)^-1, block w by warp w: lane (r, half) owns
-    //      columns 8 half .. 8 half + 7 of row r, X[r] = e_r - sum_{m<r} L[r][m] X[m], with
-    //      row m broadcast by shuffles once it is final. Rows are zero beyond their diagonal,
-    //      so the updates run over all columns with constant bounds.
+    // ---- diagonal 16 x 16 blocks of (I + L)^-1 by forward substitution down the columns:
+    //      warps 0 and 1 take two blocks each, lane (block, c) computes column c of its block,
+    //      X[i][c] = [i == c] - sum_{j<i} L[i][j] X[j][c] with the sum in increasing j, the
+    //      whole column in registers and L's rows read as broadcasts (no shuffles). The columns
+    //      go back over the block's L (fp32); every warp then reads its block row by row.
+    if (warp < 2) {
+        const int blk = 2 * warp + (lane >> 4), c = lane & 15;
+        float* lb = Ld + blk * 16 * DS;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float acc = (i == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < i; ++j) acc = fmaf(-lb[i * DS + j], x[j], acc);
+            x[i] = acc;
+        }
+        __syncwarp();   // every lane of the warp has read its blocks of L
+#pragma unroll
+        for (int i = 0; i < 16; ++i) lb[i * DS + c] = x[i];
+    }
+    __syncthreads();
     {
-        const int bs = 16 * warp, r = lane & 15, half = lane >> 4, src0 = lane & 16;
-        const float* ld = Ld + warp * 16 * DS + r * DS;
+        const int bs = 16 * warp, r = lane & 15, half = lane >> 4;
+        const float* lr = Ld + warp * 16 * DS + r * DS + 8 * half;
         float x[8];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) x[cc] = (8 * half + cc == r) ? 1.f : 0.f;
-#pragma unroll 1
-        for (int m = 0; m < 15; ++m) {
-            const float f = (r > m) ? ld[m] : 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const float xm = __shfl_sync(0xffffffffu, x[cc], src0 + m);
-                x[cc] = fmaf(-f, xm, x[cc]);
-            }
-        }
+        for (int cc = 0; cc < 8; ++cc) x[cc] = lr[cc];
         __syncthreads();   // every warp is done with Ld, which X overwrites
         const int row = bs + r, c0 = bs + 8 * half;
         uint4* xs = reinterpret_cast<uint4*>(X + row * XS + c0);
