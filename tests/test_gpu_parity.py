@@ -55,7 +55,7 @@ def test_segmented_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", ["tiny_f32_k64_cp4", "cp4_small", "single_seg_small",
-                                  "slow_decay_h4_t1k_cp16", "bf16_k64_cp4"])
+                                  "slow_decay_h4_t1k_cp16", "bf16_k64_cp4", "uneven_pieces_cp4"])
 def test_decayed_read_matches_oracle(name):
     # the other reading of the token update (the read sees the decayed state): through the
     # WY tiles on the tensor-core path and the in-chain solve on the CUDA-core path
@@ -277,3 +277,43 @@ def test_full_size_sampled_heads(name):
         assert rel_err(np64(o[b:b + 1, :, h:h + 1]), o_ref) <= TOL_BF16, (b, h)
         assert rel_err(np64(hf[b:b + 1, h:h + 1]), hf_ref) <= TOL_BF16, (b, h)
         assert rel_err(np64(hin[:, b:b + 1, h:h + 1]), hin_ref) <= TOL_BF16, (b, h)
+
+
+def test_uneven_pieces_h_in_guard_bands_bf16_and_determinism():
+    # few chains on many SMs: the sequences are cut into unequal pieces whose starts are not
+    # segment starts, and the forward chains write H_in as they pass the segment starts. Each
+    # segment's slot is written exactly once (NaN guard bands around H_in stay NaN), repeated
+    # calls agree bit for bit, and bf16 output keeps its bar.
+    w = SMALL["uneven_pieces_cp4"]
+    x = synth.make_inputs(w)
+    o_ref, hf_ref, hin_ref = oracle_ref(x, w.seg_len)
+    d = upload(x, w)
+    B, T, H, K = d["k"].shape
+    o = torch.empty((B, T, H, w.V), dtype=torch.float32, device="cuda")
+    hf = torch.empty((B, H, K, w.V), dtype=torch.float32, device="cuda")
+    prob = gdn.problem(d["k"], d["v"], o)
+    P = gdn.segmented_pieces(prob, w.nseg)
+    assert P not in {w.nseg * m for m in (1, 2, 4, 8)}, P   # not an equal-piece plan
+    n_in = w.nseg * B * H * K * w.V
+    pad = 4096
+    hbuf = torch.full((n_in + 2 * pad,), float("nan"), device="cuda")
+    hin = hbuf[pad:pad + n_in].view(w.nseg, B, H, K, w.V)
+    ws = gdn.alloc_workspace(prob, w.nseg)
+    outs = []
+    for _ in range(3):
+        gdn.gdn_segmented_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf,
+                              w.nseg, ws, H_in=hin, prob=prob)
+        torch.cuda.synchronize()
+        st, detail = gdn.gdn_check_device_error(ws)
+        assert st == 0, (st, detail)
+        outs.append((o.clone(), hf.clone(), hin.clone()))
+    assert torch.isnan(hbuf[:pad]).all() and torch.isnan(hbuf[pad + n_in:]).all()
+    assert torch.isfinite(hin).all()
+    for a, b, c in outs[1:]:
+        assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1]) and torch.equal(c, outs[0][2])
+    assert rel_err(np64(o), o_ref) <= TOL_BF16
+    assert rel_err(np64(hf), hf_ref) <= TOL_BF16
+    assert rel_err(np64(hin), hin_ref) <= TOL_BF16
+    o16, hf16, _ = run_segmented(w, d, out_dtype=torch.bfloat16)
+    assert rel_err(np64(o16), o_ref) <= 3e-2
+    assert rel_err(np64(hf16), hf_ref) <= TOL_BF16
