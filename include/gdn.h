@@ -112,12 +112,15 @@ typedef struct {
 GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
 
 /* Pieces per sequence that gdn_segmented_fwd (and gdn_chunk_fwd, nseg = 1) cuts the tokens
- * into on the current device: a multiple of nseg, so segment starts are piece starts. The
- * forward of piece 0 runs from h0 beside the affine summaries of pieces 1..P-2 (RFC section
- * 2.2), an in-order scan gives the state entering every piece, and pieces 1..P-1 then run
- * their chunked forward from those states: each phase has B*H*(P-1) independent chains, so
- * the GPU stays busy when B*H alone would not fill it. Chosen to balance wave fill, chain
- * length and scan steps (nseg when no device is current). Returns 0 for an invalid problem. */
+ * into on the current device. The forward of piece 0 runs from h0 beside the affine summaries
+ * of pieces 1..P-2 (RFC section 2.2), an in-order scan gives the state entering every piece,
+ * and pieces 1..P-1 then run their chunked forward from those states: each phase has
+ * B*H*(P-1) independent chains, so the GPU stays busy when B*H alone would not fill it. The
+ * plan balances wave fill, chain length and scan steps: either P equal pieces with P a
+ * multiple of nseg (segment starts are piece starts), or -- on the tensor-core path, when
+ * each phase fits in one wave -- a piece 0 sized so that its forward ends with the summaries
+ * and P-1 equal pieces after it, whose starts need not be segment starts (nseg equal pieces
+ * when no device is current). Returns 0 for an invalid problem. */
 GDN_API int gdn_segmented_pieces(const gdn_problem* p, int nseg);
 
 /* Chunked forward over all T tokens from the initial state h0.
@@ -155,8 +158,8 @@ GDN_API gdn_status gdn_summary_scan(const gdn_problem* p, int nseg, const float*
  * gdn_segmented_pieces(p, nseg) pieces per sequence, piece 0's forward from h0 beside the
  * summaries of pieces 1..P-2, the in-order scan of those summaries from the state piece 0
  * ends in, then the chunked forward of pieces 1..P-1 from their scanned states. The state
- * entering segment s is the state entering piece s * P / nseg. o and h_final equal
- * gdn_chunk_fwd's up to rounding.
+ * entering segment s is written by the scan when it is a piece start, else by the forward of
+ * the piece that contains it. o and h_final equal gdn_chunk_fwd's up to rounding.
  *   H_in_out [nseg,B,H,K,V] fp32: if non-NULL receives the scanned states; if NULL they
  *   live in the workspace. Workspace: gdn_workspace_bytes(p, nseg). */
 GDN_API gdn_status gdn_segmented_fwd(const gdn_problem* p, int nseg, const void* q, const void* k,
