@@ -20,6 +20,7 @@ constexpr size_t kAlign = 256;
 constexpr int kMaxSub = 8;             // pieces per segment (segmented forward)
 constexpr int kMinPieceChunks = 8;     // shortest piece, in chunks
 constexpr int kMaxUnevenPieces = 16;   // unequal pieces (one wave per phase): at most this many
+constexpr unsigned kSelftestTag = 0x5E;   // detail word of the self-test's timeout
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -516,6 +517,17 @@ const char* gdn_status_string(gdn_status s) {
         case GDN_ERR_DEVICE: return "current device is not an sm_103 GPU";
     }
     return "unknown status";
+}
+
+gdn_status gdn_selftest_wait_timeout(void* workspace, long long limit_cycles, void* stream) {
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    if (limit_cycles < 1 || limit_cycles > (1LL << 32)) return GDN_ERR_INVALID_ARG;
+    if (misaligned(workspace)) return GDN_ERR_MISALIGNED;
+    gdn_status st = check_device();
+    if (st != GDN_OK) return st;
+    return from_cuda(gdn::launch_wait_selftest(reinterpret_cast<gdn::DeviceError*>(workspace),
+                                                limit_cycles, kSelftestTag,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_check_device_error(void* workspace, void* stream, unsigned* detail) {

@@ -95,6 +95,8 @@ cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, i
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);
 bool tc_runtime_ok();   // the driver entry point that encodes tensor maps is available
+// a bounded wait that runs out on purpose (see gdn_selftest_wait_timeout)
+cudaError_t launch_wait_selftest(DeviceError* err, long long limit, unsigned tag, cudaStream_t s);
 cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all chunks of every (b, h)
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);

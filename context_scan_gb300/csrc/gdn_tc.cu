@@ -1205,6 +1205,34 @@ bool tc_supported(const ChainParams& p) {
 
 bool tc_runtime_ok() { return encode_fn() != nullptr; }
 
+namespace {
+// One CTA waits, the way every chain kernel waits, on an mbarrier that nothing arrives at, with
+// a wait limit of `limit` SM cycles: the wait gives up, records GDN_ERR_TIMEOUT with `tag` in
+// the device error word and the kernel returns (a check of the failure path; the context
+// stays usable).
+__global__ void wait_selftest_kernel(DeviceError* err, long long limit, unsigned tag) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {   // one warp polls together, as the kernels' leader warps do
+        const bool ok = mbar_wait(b, 0, &abort_flag, limit, err, tag);
+        if (ok && threadIdx.x == 0) record_error(err, GDN_ERR_CUDA, tag);   // cannot happen
+    }
+    __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(DeviceError* err, long long limit, unsigned tag, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 64, 0, s>>>(err, limit, tag);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s) { return launch<false>(p, s); }
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s) { return launch<true>(p, s); }
 

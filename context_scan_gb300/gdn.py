@@ -21,7 +21,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
 EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
             "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
-            "gdn_status_string", "gdn_check_device_error")
+            "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
 
 
 class GdnError(RuntimeError):
@@ -69,9 +69,11 @@ def lib():
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
+        L.gdn_selftest_wait_timeout.argtypes = [_P, ctypes.c_longlong, _P]
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
-                   "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error"):
+                   "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error",
+                   "gdn_selftest_wait_timeout"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -232,6 +234,14 @@ def gdn_varlen_fwd_timed(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace
                                       _ptr(h_final), _ptr(workspace),
                                       workspace.numel() if workspace is not None else 0,
                                       _stream(stream), arr), "gdn_varlen_fwd_timed")
+
+
+def gdn_selftest_wait_timeout(workspace, limit_cycles, stream=None):
+    """Launches the bounded-wait self-test (a wait that runs out after limit_cycles SM cycles
+    and records GDN_ERR_TIMEOUT in the workspace's error word); read it with
+    gdn_check_device_error."""
+    _check(lib().gdn_selftest_wait_timeout(_ptr(workspace), int(limit_cycles), _stream(stream)),
+           "gdn_selftest_wait_timeout")
 
 
 def gdn_check_device_error(workspace, stream=None):

@@ -257,6 +257,14 @@ GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const in
                                         void* const* stage_events);
 
 /* Static, NUL-terminated description of a status code. */
+/* Self-test of the failure path every kernel wait takes: one CTA waits on a barrier that
+ * nothing arrives at, with a limit of limit_cycles SM clock cycles (1 .. 2^32), then records
+ * GDN_ERR_TIMEOUT (detail word 0x5E) in the workspace's device error word and returns, as a
+ * chain kernel does when a wait runs out; the context stays usable. Asynchronous on `stream`:
+ * read the result with gdn_check_device_error. workspace: any workspace of the calls above
+ * (only its first 8 bytes are touched). Returns GDN_ERR_INVALID_ARG for a limit out of range. */
+GDN_API gdn_status gdn_selftest_wait_timeout(void* workspace, long long limit_cycles, void* stream);
+
 GDN_API const char* gdn_status_string(gdn_status s);
 
 /* Synchronises `stream`, reads the workspace's device error word, clears it, and returns

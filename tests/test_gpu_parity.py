@@ -317,3 +317,25 @@ def test_uneven_pieces_h_in_guard_bands_bf16_and_determinism():
     o16, hf16, _ = run_segmented(w, d, out_dtype=torch.bfloat16)
     assert rel_err(np64(o16), o_ref) <= 3e-2
     assert rel_err(np64(hf16), hf_ref) <= TOL_BF16
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    # the failure path of every kernel wait, made to happen on the host's terms: one CTA waits
+    # on a barrier that nothing arrives at, with a ~1 ms limit. The wait gives up, the error word
+    # says GDN_ERR_TIMEOUT with the self-test's tag, reading it clears it, and the next call on
+    # the same context and workspace runs normally.
+    w = SMALL["cp4_small"]
+    x = synth.make_inputs(w)
+    d = upload(x, w)
+    prob = gdn.problem(d["k"], d["v"])
+    ws = gdn.alloc_workspace(prob, w.nseg)
+    gdn.gdn_selftest_wait_timeout(ws, 2_000_000)
+    st, detail = gdn.gdn_check_device_error(ws)
+    assert (st, detail) == (7, 0x5E)
+    assert gdn.gdn_check_device_error(ws) == (0, 0)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_selftest_wait_timeout(ws, 0)
+    o_ref, hf_ref, hin_ref = oracle_ref(x, w.seg_len)
+    o, hf, hin = run_segmented(w, d)
+    assert rel_err(np64(o), o_ref) <= tol_for(w)
+    assert rel_err(np64(hf), hf_ref) <= tol_for(w)
