@@ -23,6 +23,13 @@ What each function computes (pages cited by title and section):
                      Design", section 1.2): g is [B,T,H,K] and the state decays row by row,
                      diag(exp(g_t)); written apart from the scalar-gate functions, which
                      it must reproduce when every channel carries the same gate.
+  backward        -- the gradients of L = sum_t do_t . o_t + <dht, h_final> with respect to
+                     q, k, v, g, beta and h0 (RFC section 6.4.3, the reverse flow ending in
+                     dQ/dK/dV/dg/dbeta; "KDA Chunk Backward -- TPU/Pallas Kernel Design",
+                     section 1), token by token backwards over recomputed states.
+  state_grad_summary -- dS_local of each segment (RFC 6.4.3): the gradient reaching the
+                     state entering the segment from its own outputs, rank-1 per token.
+  state_grad_scan -- dH_in[s] = M[s]^T dH_in[s+1] + dS[s] from dH_in[nseg] = dht (RFC 6.4.3).
   chunked_fwd / chunked_summary -- the chunk equations of "Context Parallelism in ART",
                      section 08 "First parallelize within a GPU", restated for the RFC's
                      un-decayed read; used only to pin chunked == per-token.
@@ -71,11 +78,15 @@ def _load():
         lib.oracle_chunked_summary.argtypes = [_I] * 7 + [_P] * 6 + [_I, _I]
         lib.oracle_kda_recurrence.argtypes = [_I] * 6 + [_P] * 9 + [_I, _I, _I]
         lib.oracle_kda_summary.argtypes = [_I] * 6 + [_P] * 6 + [_I, _I]
+        lib.oracle_backward.argtypes = [_I] * 5 + [_P] * 14 + [_I, _I]
+        lib.oracle_state_grad_summary.argtypes = [_I] * 6 + [_P] * 7 + [_I, _I]
+        lib.oracle_state_grad_scan.argtypes = [_I] * 4 + [_P] * 4
         lib.oracle_num_threads.argtypes = [_I]
         lib.oracle_num_threads.restype = _I
         for fn in ("oracle_recurrence", "oracle_summary", "oracle_compose", "oracle_scan",
                    "oracle_chunked_fwd", "oracle_chunked_summary", "oracle_kda_recurrence",
-                   "oracle_kda_summary"):
+                   "oracle_kda_summary", "oracle_backward", "oracle_state_grad_summary",
+                   "oracle_state_grad_scan"):
             getattr(lib, fn).restype = None
         _lib = lib
     return _lib
@@ -232,3 +243,54 @@ def chunked_summary(k, v, g, beta, nseg: int, chunk: int = 64, nthreads: int = 0
     _load().oracle_chunked_summary(B, T, H, K, V, chunk, nseg, _ptr(k), _ptr(v), _ptr(g),
                                    _ptr(beta), _ptr(M), _ptr(S), nthreads, int(decay_first))
     return M, S
+
+
+def backward(q, k, v, g, beta, dO, h0=None, dht=None, nthreads: int = 0,
+             decay_first: bool = False):
+    """Gradients of L = sum_t do_t . o_t + <dht, h_final> (dht None = 0).
+
+    Returns (dq [B,T,H,K], dk [B,T,H,K], dv [B,T,H,V], dg [B,T,H], dbeta [B,T,H],
+    dh0 [B,H,K,V]), all fp64.
+    """
+    q, k, v, g, beta, h0, dO, dht = map(_f32, (q, k, v, g, beta, h0, dO, dht))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    dq = np.empty((B, T, H, K), np.float64)
+    dk = np.empty((B, T, H, K), np.float64)
+    dv = np.empty((B, T, H, V), np.float64)
+    dg = np.empty((B, T, H), np.float64)
+    db = np.empty((B, T, H), np.float64)
+    dh0 = np.empty((B, H, K, V), np.float64)
+    _load().oracle_backward(B, T, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                            _ptr(h0), _ptr(dO), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                            _ptr(dg), _ptr(db), _ptr(dh0), nthreads, int(decay_first))
+    return dq, dk, dv, dg, db, dh0
+
+
+def state_grad_summary(q, k, g, beta, dO, nseg: int, dH_end=None, nthreads: int = 0,
+                       decay_first: bool = False):
+    """dS [nseg,B,H,K,V]: the gradient on the state entering each segment from that
+    segment's outputs, plus dH_end[s] (the gradient on the state leaving it; None = 0)
+    carried back through the segment."""
+    q, k, g, beta, dO = map(_f32, (q, k, g, beta, dO))
+    dH_end = _f64(dH_end)
+    B, T, H, K = k.shape
+    V = dO.shape[-1]
+    assert T % nseg == 0
+    dS = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_state_grad_summary(B, T, H, K, V, nseg, _ptr(q), _ptr(k), _ptr(g),
+                                      _ptr(beta), _ptr(dO), _ptr(dH_end), _ptr(dS), nthreads,
+                                      int(decay_first))
+    return dS
+
+
+def state_grad_scan(M, dS, dht=None):
+    """Reverse scan: dH_in[s] = M[s]^T dH_in[s+1] + dS[s], dH_in[nseg] = dht (None = 0).
+
+    M [nseg,B,H,K,K], dS [nseg,B,H,K,V], dht [B,H,K,V]. Returns dH_in [nseg,B,H,K,V].
+    """
+    M, dS, dht = _f64(M), _f64(dS), _f64(dht)
+    nseg, B, H, K, V = dS.shape
+    dH_in = np.empty((nseg, B, H, K, V), np.float64)
+    _load().oracle_state_grad_scan(nseg, B * H, K, V, _ptr(M), _ptr(dS), _ptr(dht), _ptr(dH_in))
+    return dH_in

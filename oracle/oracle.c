@@ -658,3 +658,223 @@ void oracle_kda_summary(int B, int T, int H, int K, int V, int nseg, const float
     kda_sum_ctx c = {B, T, H, K, V, nseg, k, v, g, beta, M, S, decay_first};
     run_units(kda_sum_unit, &c, (long)B * H * nseg, nthreads);
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* 6. Backward of the per-token recurrence ([RFC] 6.4.3, the reverse flow that ends in   */
+/* dQ, dK, dV, dg, dbeta; [KDA] "KDA Chunk Backward -- TPU/Pallas Kernel Design" 1, the  */
+/* gradients it produces, dh0 included). The loss is                                      */
+/*   L = sum_t do_t . o_t + <dht, h_final>                                                */
+/* With P = H_{t-1}, a = exp(g_t), c = 1 (or a for the decayed read), one token is        */
+/*   x = P^T k,  r = beta (v - c x),  H_t = a P + k r^T,  o = H_t^T q.                    */
+/* Walking the tokens backwards with D = dL/dH_t from the later tokens:                   */
+/*   G  = D + q do^T                  dq = H_t do                                         */
+/*   dr = G^T k                       dk = G r + c P dx',  dx' = -beta dr                  */
+/*   dv = beta dr                     dbeta = dr . (v - c x)                              */
+/*   da = <G, P> (+ dx' . x when c = a)                 dg = a da                         */
+/*   D  <- a G + c k dx'^T            (the gradient on H_{t-1})                            */
+/* and dh0 is D after token 0. The states H_{t-1} are recomputed block by block from      */
+/* checkpoints taken every ~sqrt(T) tokens of a first forward walk. One unit = one head.  */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V;
+    const float *q, *k, *v, *g, *beta, *h0, *dO, *dht;
+    double *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    int decay_first;
+} bwd_ctx;
+
+/* one forward token on a K x V state X (in place) */
+static void fwd_token(int K, int V, double* X, const float* kt, const float* vt, double a,
+                      double bt, int decay_first, double* x) {
+    const double cr = decay_first ? a : 1.0;
+    for (int j = 0; j < V; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < K; ++i) acc += (double)kt[i] * X[(size_t)i * V + j];
+        x[j] = bt * ((double)vt[j] - cr * acc);   /* the residual r */
+    }
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < V; ++j)
+            X[(size_t)i * V + j] = a * X[(size_t)i * V + j] + (double)kt[i] * x[j];
+}
+
+static void bwd_unit(void* vctx, long unit) {
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T;
+    const int b = (int)(unit / H), h = (int)(unit % H);
+    const size_t KV = (size_t)K * V;
+    int blk = 1;
+    while (blk * blk < T) ++blk;
+    const int nblk = (T + blk - 1) / blk;
+    double* ck = (double*)malloc(sizeof(double) * KV * (size_t)nblk);      /* state entering block */
+    double* st = (double*)malloc(sizeof(double) * KV * (size_t)(blk + 1)); /* states inside a block */
+    double* D = (double*)malloc(sizeof(double) * KV);
+    double* G = (double*)malloc(sizeof(double) * KV);
+    double* x = (double*)malloc(sizeof(double) * (size_t)V);
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    double* dr = (double*)malloc(sizeof(double) * (size_t)V);
+    double* dxp = (double*)malloc(sizeof(double) * (size_t)V);
+    const size_t head = ((size_t)b * H + h) * KV;
+
+    /* forward walk: checkpoints */
+    for (size_t e = 0; e < KV; ++e) st[e] = c->h0 ? (double)c->h0[head + e] : 0.0;
+    for (int t = 0; t < T; ++t) {
+        if (t % blk == 0) memcpy(ck + (size_t)(t / blk) * KV, st, sizeof(double) * KV);
+        const size_t row = ((size_t)b * T + t) * H + h;
+        fwd_token(K, V, st, c->k + row * K, c->v + row * V, exp((double)c->g[row]),
+                  (double)c->beta[row], c->decay_first, x);
+    }
+    for (size_t e = 0; e < KV; ++e) D[e] = c->dht ? (double)c->dht[head + e] : 0.0;
+
+    for (int bi = nblk - 1; bi >= 0; --bi) {
+        const int t0 = bi * blk, n = (t0 + blk <= T) ? blk : T - t0;
+        memcpy(st, ck + (size_t)bi * KV, sizeof(double) * KV);
+        for (int i = 0; i < n; ++i) {
+            memcpy(st + (size_t)(i + 1) * KV, st + (size_t)i * KV, sizeof(double) * KV);
+            const size_t row = ((size_t)b * T + t0 + i) * H + h;
+            fwd_token(K, V, st + (size_t)(i + 1) * KV, c->k + row * K, c->v + row * V,
+                      exp((double)c->g[row]), (double)c->beta[row], c->decay_first, x);
+        }
+        for (int i = n - 1; i >= 0; --i) {
+            const int t = t0 + i;
+            const size_t row = ((size_t)b * T + t) * H + h;
+            const double* P = st + (size_t)i * KV;
+            const double* Ht = st + (size_t)(i + 1) * KV;
+            const float *qt = c->q + row * K, *kt = c->k + row * K, *vt = c->v + row * V;
+            const float* dot = c->dO + row * V;
+            const double a = exp((double)c->g[row]), bt = (double)c->beta[row];
+            const double cr = c->decay_first ? a : 1.0;
+            for (int kk = 0; kk < K; ++kk)
+                for (int j = 0; j < V; ++j)
+                    G[(size_t)kk * V + j] = D[(size_t)kk * V + j] + (double)qt[kk] * (double)dot[j];
+            for (int kk = 0; kk < K; ++kk) {   /* dq = H_t do */
+                double acc = 0.0;
+                for (int j = 0; j < V; ++j) acc += Ht[(size_t)kk * V + j] * (double)dot[j];
+                c->dq[row * K + kk] = acc;
+            }
+            double dbeta = 0.0;
+            for (int j = 0; j < V; ++j) {
+                double xa = 0.0, da_ = 0.0;
+                for (int kk = 0; kk < K; ++kk) {
+                    xa += (double)kt[kk] * P[(size_t)kk * V + j];
+                    da_ += G[(size_t)kk * V + j] * (double)kt[kk];
+                }
+                x[j] = xa;
+                r[j] = bt * ((double)vt[j] - cr * xa);
+                dr[j] = da_;
+                c->dv[row * V + j] = bt * da_;
+                dbeta += da_ * ((double)vt[j] - cr * xa);
+                dxp[j] = -bt * da_;
+            }
+            c->dbeta[row] = dbeta;
+            double da = 0.0;
+            for (size_t e = 0; e < KV; ++e) da += G[e] * P[e];
+            if (c->decay_first)
+                for (int j = 0; j < V; ++j) da += dxp[j] * x[j];
+            for (int kk = 0; kk < K; ++kk) {
+                double acc = 0.0;
+                for (int j = 0; j < V; ++j)
+                    acc += G[(size_t)kk * V + j] * r[j] + cr * P[(size_t)kk * V + j] * dxp[j];
+                c->dk[row * K + kk] = acc;
+            }
+            c->dg[row] = a * da;
+            for (int kk = 0; kk < K; ++kk)
+                for (int j = 0; j < V; ++j)
+                    D[(size_t)kk * V + j] = a * G[(size_t)kk * V + j] + cr * (double)kt[kk] * dxp[j];
+        }
+    }
+    if (c->dh0) memcpy(c->dh0 + head, D, sizeof(double) * KV);
+    free(ck); free(st); free(D); free(G); free(x); free(r); free(dr); free(dxp);
+}
+
+void oracle_backward(int B, int T, int H, int K, int V, const float* q, const float* k,
+                     const float* v, const float* g, const float* beta, const float* h0,
+                     const float* dO, const float* dht, double* dq, double* dk, double* dv,
+                     double* dg, double* dbeta, double* dh0, int nthreads, int decay_first) {
+    bwd_ctx c = {B, T, H, K, V, q, k, v, g, beta, h0, dO, dht,
+                 dq, dk, dv, dg, dbeta, dh0, decay_first};
+    run_units(bwd_unit, &c, (long)B * H, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 7. State-gradient summary of one segment ([RFC] 6.4.3: the summary step yields         */
+/* dS_local, the gradient reaching the state that enters the segment from the segment's  */
+/* own outputs). The gradient on the state obeys the transposed token transition; the     */
+/* transition exp(g) I - beta k k^T (or exp(g) (I - beta k k^T)) is symmetric, so one     */
+/* token backwards is, in rank-1 form,                                                    */
+/*   G = D + q do^T,   y = k^T G,   D <- exp(g) G - c beta k y^T   (c as in section 6)    */
+/* started at the segment's last token from dH_end[s] (zero when dH_end is NULL) and read */
+/* out after its first token. Needs neither v nor any forward state. One unit = one       */
+/* (b, h, segment). dS and dH_end are [nseg, B, H, K, V].                                 */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    int B, T, H, K, V, nseg;
+    const float *q, *k, *g, *beta, *dO;
+    const double* dH_end;
+    double* dS;
+    int decay_first;
+} sgs_ctx;
+
+static void sgs_unit(void* vctx, long unit) {
+    const sgs_ctx* c = (const sgs_ctx*)vctx;
+    const int K = c->K, V = c->V, H = c->H, T = c->T;
+    const int seg_len = T / c->nseg;
+    const int s = (int)(unit % c->nseg);
+    const long bh = unit / c->nseg;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    const size_t KV = (size_t)K * V;
+    double* D = c->dS + (((size_t)s * c->B + b) * H + h) * KV;
+    double* y = (double*)malloc(sizeof(double) * (size_t)V);
+    for (size_t e = 0; e < KV; ++e)
+        D[e] = c->dH_end ? c->dH_end[(((size_t)s * c->B + b) * H + h) * KV + e] : 0.0;
+    for (int t = (s + 1) * seg_len - 1; t >= s * seg_len; --t) {
+        const size_t row = ((size_t)b * T + t) * H + h;
+        const float *qt = c->q + row * K, *kt = c->k + row * K, *dot = c->dO + row * V;
+        const double a = exp((double)c->g[row]), bt = (double)c->beta[row];
+        const double cr = c->decay_first ? a : 1.0;
+        for (int i = 0; i < K; ++i)
+            for (int j = 0; j < V; ++j) D[(size_t)i * V + j] += (double)qt[i] * (double)dot[j];
+        for (int j = 0; j < V; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < K; ++i) acc += (double)kt[i] * D[(size_t)i * V + j];
+            y[j] = acc;
+        }
+        for (int i = 0; i < K; ++i)
+            for (int j = 0; j < V; ++j)
+                D[(size_t)i * V + j] = a * D[(size_t)i * V + j] - cr * bt * (double)kt[i] * y[j];
+    }
+    free(y);
+}
+
+void oracle_state_grad_summary(int B, int T, int H, int K, int V, int nseg, const float* q,
+                               const float* k, const float* g, const float* beta,
+                               const float* dO, const double* dH_end, double* dS, int nthreads,
+                               int decay_first) {
+    sgs_ctx c = {B, T, H, K, V, nseg, q, k, g, beta, dO, dH_end, dS, decay_first};
+    run_units(sgs_unit, &c, (long)B * H * nseg, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* 8. Reverse scan of the state gradients ([RFC] 6.4.3, "dH_in = M^T dH_out + dS_local"): */
+/* the state after the last segment carries dht (zero when NULL); going back over the     */
+/* segments, dH_in[s] = M[s]^T dH_in[s+1] + dS[s] with dH_in[nseg] = dht. dh0 is          */
+/* dH_in[0]. M [nseg,BH,K,K], dS / dH_in [nseg,BH,K,V], dht [BH,K,V].                       */
+/* ------------------------------------------------------------------------------------ */
+void oracle_state_grad_scan(int nseg, int BH, int K, int V, const double* M, const double* dS,
+                            const double* dht, double* dH_in) {
+    const size_t KV = (size_t)K * V, KK = (size_t)K * K;
+    double* cur = (double*)malloc(sizeof(double) * KV);
+    for (int bh = 0; bh < BH; ++bh) {
+        for (size_t e = 0; e < KV; ++e) cur[e] = dht ? dht[(size_t)bh * KV + e] : 0.0;
+        for (int s = nseg - 1; s >= 0; --s) {
+            const double* Ms = M + ((size_t)s * BH + bh) * KK;
+            double* out = dH_in + ((size_t)s * BH + bh) * KV;
+            for (int i = 0; i < K; ++i)
+                for (int j = 0; j < V; ++j) {
+                    double acc = dS[((size_t)s * BH + bh) * KV + (size_t)i * V + j];
+                    for (int m = 0; m < K; ++m) acc += Ms[(size_t)m * K + i] * cur[(size_t)m * V + j];
+                    out[(size_t)i * V + j] = acc;
+                }
+            memcpy(cur, out, sizeof(double) * KV);
+        }
+    }
+    free(cur);
+}
