@@ -33,6 +33,10 @@ sys.path.insert(0, ROOT)
 METRIC = "GDN segmented fwd tokens/s at H32 K=V=128 T=32K bf16; % of roofline"
 VARLEN_METRIC = "GDN packed-sequence fwd tokens/s (lengths 1800,1500,2000,1200,800) at H16 K=V=128 bf16"
 KDA_METRIC = "GDN per-channel-gate (KDA) fwd tokens/s at H16 K=V=128 T=8K bf16"
+STATE_GRAD_METRIC = ("GDN backward state-gradient path tokens/s (segment summaries M, dS_local, "
+                     "reverse M^T scan) at H32 K=V=128 T=32K bf16")
+# fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz maximum SM clock
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def metric_of(w) -> str:
@@ -454,6 +458,158 @@ def run_varlen(args):
         dist.destroy_process_group()
 
 
+def state_grad_algorithmic(w):
+    """Per launch of the state-gradient kernel over workload w: compulsory HBM bytes (read q, k,
+    g, beta in the input dtype and dO in fp32 once; write dS) and fp32 flops per chunk and head
+    counted once: K K^T and Q K^T (2 * 64*64*K*2), the 64 x 64 inverse (~0.17 M), dR = Kd D +
+    C^T dO (64*K*V*2 + 64*64*V*2), A^T dR (64*64*V), D update (2 * K*64*V*2)."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    nbytes = th * (2 * w.K * isz + 2 * isz + w.V * 4) + w.nseg * w.B * w.H * w.K * w.V * 4
+    c = 64
+    per_chunk = (2 * c * c * w.K * 2 + 0.17e6 + c * w.K * w.V * 2 + c * c * w.V * 2 +
+                 c * c * w.V + 2 * w.K * c * w.V * 2)
+    return {"bytes": nbytes, "flops": per_chunk * th / c}
+
+
+def run_state_grad(args):
+    """The backward's state-gradient path ("RFC: HyperParallel Linear Attention Context
+    Parallel", section 6.4.3) on the headline workload: one step is the segment summaries M
+    (gdn_segment_summary), the per-segment state gradients dS (gdn_state_grad_summary) and the
+    reverse scan to dH_in (gdn_state_grad_scan), each bracketed by events on the stream."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from context_scan_gb300 import gdn, synth
+
+    world, rank = init_dist("nccl" if args.gpus > 1 else "gloo")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w0 = synth.WORKLOADS[args.workload]
+    if w0.gate_k or w0.seq_lens is not None:
+        raise SystemExit("--path state_grad runs fixed-length scalar-gate workloads only")
+    w = synth.scaled(w0, seed=w0.seed + rank_seed_offset(rank))
+    if args.T:
+        w = synth.scaled(w, T=args.T)
+    x = synth.make_inputs(w)
+    gr = synth.make_grads(w, dht_sd=0.1)
+    dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    d = {n: torch.from_numpy(x[n]).to(dev).to(dt) for n in ("q", "k", "v", "g", "beta")}
+    dO = torch.from_numpy(gr["dO"]).to(dev)
+    dht = torch.from_numpy(gr["dht"]).to(dev)
+    B, H, K, V, nseg = w.B, w.H, w.K, w.V, w.nseg
+    M = torch.empty((nseg, B, H, K, K), dtype=torch.float32, device=dev)
+    S = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device=dev)
+    dS = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device=dev)
+    dH_in = torch.empty((nseg, B, H, K, V), dtype=torch.float32, device=dev)
+    prob = gdn.problem(d["k"], d["v"])
+    gprob = gdn.problem(d["k"], dO, dO)
+    ws = gdn.alloc_workspace(prob, 1, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev):
+        ev[0].record(stream)
+        gdn.gdn_segment_summary(d["k"], d["v"], d["g"], d["beta"], M, S, nseg, ws, prob=prob,
+                                stream=stream)
+        ev[1].record(stream)
+        gdn.gdn_state_grad_summary(d["q"], d["k"], d["g"], d["beta"], dO, dS, nseg, prob=gprob,
+                                   stream=stream)
+        ev[2].record(stream)
+        gdn.gdn_state_grad_scan(M, dS, dht, dH_in, stream=stream)
+        ev[3].record(stream)
+
+    def events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    for _ in range(args.warmup):
+        step(events())
+    torch.cuda.synchronize()
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
+    Ksteps = args.steps
+    ev = [events() for _ in range(Ksteps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dev)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(Ksteps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
+    total_s = t0.elapsed_time(t1) / 1e3
+    max_s = reduce_max(total_s, device=dev if world > 1 else "cpu")
+    barrier(dev)
+    avg = {name: sum(e[a].elapsed_time(e[a + 1]) for e in ev) / Ksteps
+           for a, name in enumerate(("summary_M", "state_grad", "scan"))}
+    alg = state_grad_algorithmic(w)
+    ach = alg["flops"] / (avg["state_grad"] * 1e-3) / 1e12
+    peaks, peaks_src = load_peaks()
+    ms_per_step = max_s / Ksteps * 1e3
+    value = aggregate(w.B * w.T, Ksteps, world, max_s)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+        done, secs = 0, 0.0
+        while done < len(heads) and secs < args.cpu_seconds:
+            b, h = heads[done]
+            xs = {n: np.ascontiguousarray(x[n][b:b + 1, :, h:h + 1])
+                  for n in ("q", "k", "v", "g", "beta")}
+            dOs = np.ascontiguousarray(gr["dO"][b:b + 1, :, h:h + 1])
+            t = time.perf_counter()
+            Ms, _ = oracle.summary(xs["k"], xs["v"], xs["g"], xs["beta"], nseg)
+            dSs = oracle.state_grad_summary(xs["q"], xs["k"], xs["g"], xs["beta"], dOs, nseg)
+            oracle.state_grad_scan(Ms, dSs, gr["dht"][b:b + 1, h:h + 1])
+            secs += time.perf_counter() - t
+            done += 1
+        cpu = {"value": round(B * w.T * done / len(heads) / secs, 1), "unit": "tokens/s",
+               "cores": oracle.num_threads(0), "kind": "oracle",
+               "sample": f"{done} of {len(heads)} (b,h) heads of {w.name}, all T={w.T} tokens: "
+                         f"fp64 segment summaries, per-segment state gradients and the reverse "
+                         f"scan; {secs:.1f} s; tokens/s scaled to the whole batch"}
+    if rank == 0:
+        line = {
+            "metric": STATE_GRAD_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": Ksteps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if w.in_dtype == "f32" else "bf16 in, f32 math",
+            "data": "synthetic",
+            "config": {"workload": w0.name, "path": "state_grad", "B": B, "H": H, "T": w.T,
+                       "K": K, "V": V, "nseg": nseg, "chunk": 64, "in_dtype": w.in_dtype,
+                       "dO_dtype": "f32", "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"weak: {world} rank(s) x one batch each"},
+            "roofline": {"bound": "alu", "achieved": round(ach, 3),
+                         "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
+                         "frac": round(ach / FP32_ALU_TFLOPS, 4), "traffic": None,
+                         "kernel": "state_grad_kernel", "kernel_ms": round(avg["state_grad"], 4),
+                         "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                         "peak_source": "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+            "stage_ms": {k: round(v, 4) for k, v in avg.items()},
+            "cpu_baseline": cpu,
+            "e2e": None,
+            # WY tiles + tensor-core summary (or one CUDA-core summary), state gradients, scan
+            "gpu_launches": (4 if w.in_dtype == "bf16" and K == 128 else 3) * Ksteps,
+            "clocks": clocks,
+            "peaks_source": peaks_src,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -741,6 +897,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", choices=["forward", "state_grad"], default="forward",
+                    help="forward: the segmented forward (the headline line); state_grad: the "
+                         "backward's state-gradient path on the same workload")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -753,6 +912,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "state_grad":
+        run_state_grad(args)
     else:
         run_ours(args)
 

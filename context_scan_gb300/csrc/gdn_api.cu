@@ -504,6 +504,52 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     return from_cuda(mark(stage_events, 2, s));
 }
 
+gdn_status gdn_state_grad_summary(const gdn_problem* p, int nseg, const void* q, const void* k,
+                                  const void* g, const void* beta, const void* dO,
+                                  const float* dH_end, float* dS, void* stream) {
+    gdn_status st = check_problem(p, nseg);
+    if (st != GDN_OK) return st;
+    if (p->gate_k) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!dS) return GDN_ERR_INVALID_ARG;
+    if (p->T > 0 && (!q || !k || !g || !beta || !dO)) return GDN_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, g, beta, dO, (const void*)dH_end, (const void*)dS})
+        if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
+    if ((st = check_device()) != GDN_OK) return st;
+    gdn::StateGradParams c{};
+    c.q = q;
+    c.k = k;
+    c.g = g;
+    c.beta = beta;
+    c.dO = dO;
+    c.dH_end = dH_end;
+    c.dS = dS;
+    c.B = p->B;
+    c.T = p->T;
+    c.H = p->H;
+    c.K = p->K;
+    c.V = p->V;
+    c.seg_len = p->T / nseg;
+    c.nseg = nseg;
+    c.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
+    c.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
+    c.decay_first = p->decay_first;
+    return from_cuda(gdn::launch_state_grad(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_state_grad_scan(const gdn_problem* p, int nseg, const float* M, const float* dS,
+                               const float* dht, float* dH_in, void* stream) {
+    if (!p || nseg < 1 || p->B < 1 || p->H < 1) return GDN_ERR_INVALID_ARG;
+    if (p->K != p->V || (p->K != 64 && p->K != 128)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!M || !dS || !dH_in) return GDN_ERR_INVALID_ARG;
+    if ((long long)p->B * p->H >= (1LL << 31)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    for (const void* ptr : {(const void*)M, (const void*)dS, (const void*)dht, (const void*)dH_in})
+        if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
+    gdn_status st = check_device();
+    if (st != GDN_OK) return st;
+    return from_cuda(gdn::launch_state_grad_scan(M, dS, dht, dH_in, nseg, p->B * p->H, p->K, p->V,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* gdn_status_string(gdn_status s) {
     switch (s) {
         case GDN_OK: return "ok";

@@ -92,6 +92,26 @@ cudaError_t launch_scan(const float* M, const float* S, const float* h_first, fl
 cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
                                DeviceError* err, cudaStream_t s);
 
+// State-gradient summaries (backward): chain (b, h, seg) walks segment seg's chunks from the
+// last to the first, starting from dH_end[seg] ([nseg][B][H][K][V], or zero when null), and
+// writes the gradient on the state entering the segment to dS[seg]. dO has the output dtype.
+struct StateGradParams {
+    const void* q;
+    const void* k;
+    const void* g;
+    const void* beta;
+    const void* dO;
+    const float* dH_end;
+    float* dS;
+    int B, T, H, K, V;
+    int seg_len, nseg;
+    int in_bf16, do_bf16, decay_first;
+};
+cudaError_t launch_state_grad(const StateGradParams& p, cudaStream_t s);
+// dH_in[s] = M[s]^T dH_in[s+1] + dS[s] for s = nseg-1 .. 0, dH_in[nseg] = dht (or zero)
+cudaError_t launch_state_grad_scan(const float* M, const float* dS, const float* dht,
+                                   float* dH_in, int nseg, int BH, int K, int V, cudaStream_t s);
+
 // tcgen05 tensor-core kernels (bf16 inputs, K == V == 128)
 bool tc_supported(const ChainParams& p);
 bool tc_runtime_ok();   // the driver entry point that encodes tensor maps is available

@@ -21,6 +21,7 @@ STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
 EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
             "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
+            "gdn_state_grad_summary", "gdn_state_grad_scan",
             "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
 
 
@@ -66,6 +67,8 @@ def lib():
         L.gdn_varlen_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 10 + [ctypes.c_size_t, _P]
         L.gdn_varlen_fwd_timed.argtypes = ([pp, ctypes.c_int] + [_P] * 10 +
                                            [ctypes.c_size_t, _P, _P])
+        L.gdn_state_grad_summary.argtypes = [pp, ctypes.c_int] + [_P] * 8
+        L.gdn_state_grad_scan.argtypes = [pp, ctypes.c_int] + [_P] * 5
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
@@ -73,7 +76,7 @@ def lib():
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
                    "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error",
-                   "gdn_selftest_wait_timeout"):
+                   "gdn_selftest_wait_timeout", "gdn_state_grad_summary", "gdn_state_grad_scan"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -234,6 +237,26 @@ def gdn_varlen_fwd_timed(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace
                                       _ptr(h_final), _ptr(workspace),
                                       workspace.numel() if workspace is not None else 0,
                                       _stream(stream), arr), "gdn_varlen_fwd_timed")
+
+
+def gdn_state_grad_summary(q, k, g, beta, dO, dS, nseg, dH_end=None, stream=None, prob=None):
+    """Per-segment state gradients: dS [nseg,B,H,K,V] fp32 receives the gradient on the state
+    entering each segment of its outputs' loss (sum dO . o) plus <dH_end[s], state leaving
+    it> (dH_end None = 0). dO carries the output dtype (fp32 or bf16)."""
+    prob = prob or problem(k, dO, dO)
+    if prob.gate_k:
+        raise GdnError(2, "gdn_state_grad_summary")
+    _check(lib().gdn_state_grad_summary(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(g),
+                                        _ptr(beta), _ptr(dO), _ptr(dH_end), _ptr(dS),
+                                        _stream(stream)), "gdn_state_grad_summary")
+
+
+def gdn_state_grad_scan(M, dS, dht, dH_in, stream=None, prob=None):
+    """Reverse scan: dH_in[s] = M[s]^T dH_in[s+1] + dS[s] with dH_in[nseg] = dht (None = 0)."""
+    nseg, B, H, K, V = dH_in.shape
+    prob = prob or Problem(B, 0, H, K, V, 64, GDN_DTYPE_F32, GDN_DTYPE_F32)
+    _check(lib().gdn_state_grad_scan(ctypes.byref(prob), nseg, _ptr(M), _ptr(dS), _ptr(dht),
+                                     _ptr(dH_in), _stream(stream)), "gdn_state_grad_scan")
 
 
 def gdn_selftest_wait_timeout(workspace, limit_cycles, stream=None):

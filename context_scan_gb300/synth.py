@@ -26,7 +26,7 @@ _SRC = os.path.join(_HERE, "csrc", "synth.c")
 _LIB_DIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIB_DIR, "libgdn_synth.so")
 
-TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "h0": 6}
+TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "h0": 6, "dO": 7, "dht": 8}
 KIND_NORMAL, KIND_UNIT, KIND_LOGSIGMOID, KIND_SIGMOID = 0, 1, 2, 3
 
 
@@ -186,3 +186,16 @@ def make_inputs(w: Workload, nthreads: int = 0) -> dict:
     if w.h0_sd is None:
         out["h0"] = None
     return out
+
+
+def make_grads(w: Workload, bf16_out: bool = False, dht_sd=None, nthreads: int = 0) -> dict:
+    """The backward's incoming gradients for workload w: dO [B,T,H,V] ~ N(0, 1) (rounded to
+    bf16 when the output is bf16) and, when dht_sd is given, dht [B,H,K,V] ~ N(0, dht_sd)
+    (fp32, like the state); drawn from the workload's seed with their own tensor ids."""
+    dO = fill(w.seed, "dO", (w.B, w.T, w.H, w.V), KIND_NORMAL, 0.0, 1.0, bf16=bf16_out,
+              nthreads=nthreads)
+    dht = None
+    if dht_sd is not None:
+        dht = fill(w.seed, "dht", (w.B, w.H, w.K, w.V), KIND_NORMAL, 0.0, dht_sd, bf16=False,
+                   nthreads=nthreads)
+    return {"dO": dO, "dht": dht}

@@ -211,6 +211,42 @@ GDN_API gdn_status gdn_segmented_fwd_noalloc(const gdn_problem* p, int nseg, con
                                              void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Backward: the state-gradient path (RFC section 6.4.3, reverse flow)
+ * ---------------------------------------------------------------------------------------
+ * The loss is L = sum_t dO_t . o_t + <dht, h_final>. The gradient on the state runs
+ * backwards through the transposed token transitions (exp(g_t) I - beta_t k_t k_t^T, or
+ * exp(g_t)(I - beta_t k_t k_t^T) with decay_first; both symmetric), so it needs q, k, g,
+ * beta and dO but neither v nor any forward state. The RFC's flow computes it per segment
+ * (dS_local), then applies the segment summaries backwards: dH_in = M^T dH_out + dS_local.
+ * Per-channel gates (gate_k) are not supported here (GDN_ERR_UNSUPPORTED_SHAPE). */
+
+/* Per-segment state-gradient summary (RFC 6.4.3 "backward_state_gradient_summary").
+ *   dS[s] = dL_s/dH_in[s]: the gradient on the state entering segment s of
+ *   L_s = sum over the segment's tokens of dO_t . o_t + <dH_end[s], state leaving s>,
+ *   computed chunk by chunk backwards (dR = Kd D + C^T dO; D <- exp(G_c) D + Qd^T dO - W^T dR).
+ *   Shapes and layouts as the forward: q, k [B,T,H,K] and g, beta [B,T,H] in in_dtype;
+ *   dO [B,T,H,V] in out_dtype (the output's dtype); dH_end [nseg,B,H,K,V] fp32 or NULL
+ *   (zero: the RFC's dS_local); dS [nseg,B,H,K,V] fp32, written. With nseg == 1 and
+ *   dH_end = dht, dS[0] is dh0, the initial-state gradient. T % (64*nseg) == 0, K = V in
+ *   {64, 128}; every pointer 16-byte aligned. fp32 arithmetic on CUDA cores; no workspace.
+ *   Asynchronous on `stream`. */
+GDN_API gdn_status gdn_state_grad_summary(const gdn_problem* p, int nseg, const void* q,
+                                          const void* k, const void* g, const void* beta,
+                                          const void* dO, const float* dH_end, float* dS,
+                                          void* stream);
+
+/* Reverse scan of the state gradients (RFC 6.4.3 "backward_summary_apply"):
+ *   dH_in[nseg] = dht (zeros if NULL),  dH_in[s] = M[s]^T dH_in[s+1] + dS[s]  (s = nseg-1..0).
+ *   M [nseg,B,H,K,K] from gdn_segment_summary, dS [nseg,B,H,K,V] from
+ *   gdn_state_grad_summary, dht [B,H,K,V], dH_in [nseg,B,H,K,V] out, all fp32. dH_in[s] is
+ *   the gradient of L on the state entering segment s; dH_in[0] is dh0, and dH_in[s+1] (dht
+ *   for the last segment) is what segment s's own backward starts from. Only p->B, p->H,
+ *   p->K, p->V are read from the problem. */
+GDN_API gdn_status gdn_state_grad_scan(const gdn_problem* p, int nseg, const float* M,
+                                       const float* dS, const float* dht, float* dH_in,
+                                       void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Packed variable-length sequences
  * ---------------------------------------------------------------------------------------
  * nseq sequences of different lengths share one token axis: sequence s holds tokens

@@ -59,7 +59,7 @@ def P(**kw):
     d = dict(B=1, T=128, H=2, K=128, V=128, chunk=64, in_dtype=1, out_dtype=0)
     d.update(kw)
     return gdn.Problem(**{k: d[k] for k in ("B", "T", "H", "K", "V", "chunk", "in_dtype",
-                                             "out_dtype")})
+                                             "out_dtype", "decay_first", "gate_k") if k in d})
 
 
 def test_workspace_bytes_and_status_strings(L):
@@ -135,3 +135,24 @@ def test_varlen_workspace_and_validation(L):
     assert L.gdn_varlen_fwd(ctypes.byref(P(B=2)), 1, *([None] * 10), 0, None) == 1
     assert L.gdn_varlen_fwd(ctypes.byref(P(B=1, chunk=32)), 1, *([None] * 10), 0, None) == 2
     assert L.gdn_varlen_fwd(ctypes.byref(P(B=1)), 1, *([None] * 10), 0, None) == 1   # no cu_seqlens
+
+
+def test_state_grad_validation(L):
+    # the backward's state-gradient entry points reject bad problems before any launch
+    S, C = L.gdn_state_grad_summary, L.gdn_state_grad_scan
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every case fails validation first
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    args = [fake] * 5 + [None, fake, None]
+    assert S(ctypes.byref(P(T=100)), 1, *args) == 2
+    assert S(ctypes.byref(P(T=128)), 4, *args) == 2               # T % (64 nseg)
+    assert S(ctypes.byref(P(K=96, V=96)), 1, *args) == 2
+    assert S(ctypes.byref(P(gate_k=1)), 1, *args) == 2            # per-channel gates
+    assert S(ctypes.byref(P(in_dtype=4)), 1, *args) == 3
+    assert S(ctypes.byref(P()), 0, *args) == 1
+    assert S(ctypes.byref(P()), 1, *([fake] * 5), None, None, None) == 1      # no dS
+    assert S(ctypes.byref(P()), 1, None, *([fake] * 4), None, fake, None) == 1   # no q
+    assert S(ctypes.byref(P()), 1, *([fake] * 4), odd, None, fake, None) == 4    # dO misaligned
+    assert C(ctypes.byref(P()), 2, None, fake, None, fake, None) == 1            # no M
+    assert C(ctypes.byref(P(K=64, V=128)), 2, fake, fake, None, fake, None) == 2
+    assert C(ctypes.byref(P()), 0, fake, fake, None, fake, None) == 1
+    assert C(ctypes.byref(P()), 2, fake, fake, odd, fake, None) == 4             # dht misaligned
