@@ -30,28 +30,40 @@ __device__ __forceinline__ float ld(const void* base, long long idx, int bf16) {
 
 template <int KD, int CT>
 struct BwdSmem {
-    static constexpr int KP = KD + 1;   // padded rows of k / q
-    static constexpr int LP = 65;       // padded rows of the 64 x 64 matrices
-    static constexpr int off_k = 0;
-    static constexpr int off_q = off_k + 64 * KP;
-    static constexpr int off_do = off_q + 64 * KP;
-    static constexpr int off_d = off_do + 64 * CT;
-    static constexpr int off_l = off_d + KD * CT;
-    static constexpr int off_a = off_l + 64 * LP;
-    static constexpr int off_c = off_a + 64 * LP;
-    static constexpr int off_z = off_c + 64 * LP;
-    static constexpr int off_r = off_z + 64 * CT;
-    static constexpr int off_s = off_r + 64 * CT;   // scalars: 6 x 64
+    static constexpr int TP = 68;       // padded rows of the transposed k / q ([l][i]) and of
+                                        // the 64 x 64 matrices (float4-aligned)
+    static constexpr int off_kr = 0;                    // k  [64][KD]  (row i = token)
+    static constexpr int off_qr = off_kr + 64 * KD;     // q  [64][KD]
+    static constexpr int off_kt = off_qr + 64 * KD;     // k^T [KD][TP]
+    static constexpr int off_qt = off_kt + KD * TP;     // q^T [KD][TP]
+    static constexpr int off_do = off_qt + KD * TP;     // dO tile [64][CT]
+    static constexpr int off_d = off_do + 64 * CT;      // D tile  [KD][CT]
+    static constexpr int off_l = off_d + KD * CT;       // L = diag(beta) P  [64][TP]
+    static constexpr int off_a = off_l + 64 * TP;       // A                 [64][TP]
+    static constexpr int off_c = off_a + 64 * TP;       // C                 [64][TP]
+    static constexpr int off_z = off_c + 64 * TP;       // Z tile [64][CT]
+    static constexpr int off_r = off_z + 64 * CT;       // dR tile [64][CT]
+    static constexpr int off_s = off_r + 64 * CT;       // scalars: 6 x 64
     static constexpr int total = off_s + 6 * 64;
     static constexpr size_t bytes = sizeof(float) * total;
 };
 
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+// Every large product below gives each thread a 4 x 4 (or 4 x 2) block of the result in
+// registers and reads its operands as float4 / float2 rows of shared memory, so the loop
+// does 8-16 FMAs per shared-memory load (a thread per output reads two operands per FMA).
 template <int KD, int CT>
 __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p) {
+    static_assert(CT == 32 && kThreads == 256, "thread blocking assumes 256 threads, CT = 32");
     using L = BwdSmem<KD, CT>;
-    extern __shared__ float sm[];
-    float* ks = sm + L::off_k;
-    float* qs = sm + L::off_q;
+    extern __shared__ float4 smv[];
+    float* sm = reinterpret_cast<float*>(smv);
+    float* kr = sm + L::off_kr;
+    float* qr = sm + L::off_qr;
+    float* kt = sm + L::off_kt;
+    float* qt = sm + L::off_qt;
     float* dos = sm + L::off_do;
     float* Ds = sm + L::off_d;
     float* Ls = sm + L::off_l;
@@ -65,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
     float* dk = bet + 64;         // exp(G_last - G_j)
     float* eq = dk + 64;          // exp(G_i)
     float* ekr = eq + 64;         // beta_i exp(Gx_i)
-    constexpr int KP = L::KP, LP = L::LP;
+    constexpr int TP = L::TP;
 
     const int tid = threadIdx.x;
     const int seg = blockIdx.x % p.nseg;
@@ -80,26 +92,60 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
         Ds[e] = p.dH_end ? p.dH_end[(head * KD + l) * V + c0 + c] : 0.f;
     }
 
+    // The next chunk's k, q, dO, g and beta are loaded into registers while the current
+    // chunk computes. Each thread owns NKQ (token quad, key channel) items of k and q -- the
+    // four tokens of a quad land in one float4 of the transposed copies, so those stores are
+    // free of bank conflicts -- and ND elements of the dO tile.
+    constexpr int NKQ = 16 * KD / kThreads, ND = 64 * CT / kThreads;
+    float pk[NKQ][4], pq[NKQ][4], pd[ND], pg = 0.f, pb = 0.f;
     const long long row0 = (long long)b * p.T + (long long)seg * p.seg_len;
-    for (int ch = p.seg_len / kChunk - 1; ch >= 0; --ch) {
+    auto prefetch = [&](int ch) {
         const long long r0 = row0 + (long long)ch * kChunk;
-        // ---- (1) load k, q, the dO tile, g, beta
-        for (int e = tid; e < 64 * KD; e += kThreads) {
-            const int i = e / KD, l = e % KD;
-            const long long row = (r0 + i) * H + h;
-            ks[i * KP + l] = ld(p.k, row * KD + l, p.in_bf16);
-            qs[i * KP + l] = ld(p.q, row * KD + l, p.in_bf16);
+#pragma unroll
+        for (int n = 0; n < NKQ; ++n) {
+            const int e = tid + n * kThreads, l = e % KD, i4 = (e / KD) * 4;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const long long idx = ((r0 + i4 + r) * H + h) * KD + l;
+                pk[n][r] = ld(p.k, idx, p.in_bf16);
+                pq[n][r] = ld(p.q, idx, p.in_bf16);
+            }
         }
-        for (int e = tid; e < 64 * CT; e += kThreads) {
-            const int i = e / CT, c = e % CT;
-            dos[e] = ld(p.dO, ((r0 + i) * H + h) * V + c0 + c, p.do_bf16);
+#pragma unroll
+        for (int n = 0; n < ND; ++n) {
+            const int e = tid + n * kThreads, i = e / CT, c = e % CT;
+            pd[n] = ld(p.dO, ((r0 + i) * H + h) * V + c0 + c, p.do_bf16);
         }
         if (tid < 64) {
             const long long row = (r0 + tid) * H + h;
-            gx[tid] = ld(p.g, row, p.in_bf16);   // raw gate until the cumsum
-            bet[tid] = ld(p.beta, row, p.in_bf16);
+            pg = ld(p.g, row, p.in_bf16);
+            pb = ld(p.beta, row, p.in_bf16);
+        }
+    };
+    const int n_chunks = p.seg_len / kChunk;
+    if (n_chunks > 0) prefetch(n_chunks - 1);
+    for (int ch = n_chunks - 1; ch >= 0; --ch) {
+        // ---- (1) the prefetched chunk into shared memory: k, q (row and transposed copies),
+        //      the dO tile, g, beta; then start loading the chunk before it
+#pragma unroll
+        for (int n = 0; n < NKQ; ++n) {
+            const int e = tid + n * kThreads, l = e % KD, i4 = (e / KD) * 4;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                kr[(i4 + r) * KD + l] = pk[n][r];
+                qr[(i4 + r) * KD + l] = pq[n][r];
+            }
+            st4(&kt[l * TP + i4], make_float4(pk[n][0], pk[n][1], pk[n][2], pk[n][3]));
+            st4(&qt[l * TP + i4], make_float4(pq[n][0], pq[n][1], pq[n][2], pq[n][3]));
+        }
+#pragma unroll
+        for (int n = 0; n < ND; ++n) dos[tid + n * kThreads] = pd[n];
+        if (tid < 64) {
+            gx[tid] = pg;   // raw gate until the cumsum
+            bet[tid] = pb;
         }
         __syncthreads();
+        if (ch > 0) prefetch(ch - 1);
         // ---- (2) inclusive / read-side cumulative gates (one warp, two tokens per lane)
         if (tid < 32) {
             const float a0 = gx[2 * tid], a1 = gx[2 * tid + 1];
@@ -121,24 +167,40 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             eq[tid] = expf(gam[tid]);
             ekr[tid] = bet[tid] * expf(gx[tid]);
         }
-        // ---- (3) L = diag(beta) P (j < i) and C (j <= i); clear A
-        for (int e = tid; e < 64 * 64; e += kThreads) {
-            const int i = e / 64, j = e % 64;
-            float lv = 0.f, cv = 0.f;
-            if (j <= i) {
-                float dkk = 0.f, dqk = 0.f;
-#pragma unroll 8
+        // ---- (3) L = diag(beta) P (j < i) and C (j <= i), one 4 x 4 block per thread; clear A
+        {
+            const int i0 = (tid / 16) * 4, j0 = (tid % 16) * 4;
+            float kk[4][4] = {}, qk[4][4] = {};
+            if (j0 <= i0 + 3) {   // blocks wholly above the diagonal stay zero
+#pragma unroll 4
                 for (int l = 0; l < KD; ++l) {
-                    const float kj = ks[j * KP + l];
-                    dkk = fmaf(ks[i * KP + l], kj, dkk);
-                    dqk = fmaf(qs[i * KP + l], kj, dqk);
+                    const float4 a = ld4(&kt[l * TP + i0]), qa = ld4(&qt[l * TP + i0]);
+                    const float4 bb = ld4(&kt[l * TP + j0]);
+                    const float av[4] = {a.x, a.y, a.z, a.w}, qv[4] = {qa.x, qa.y, qa.z, qa.w};
+                    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            kk[r][c] = fmaf(av[r], bv[c], kk[r][c]);
+                            qk[r][c] = fmaf(qv[r], bv[c], qk[r][c]);
+                        }
                 }
-                if (j < i) lv = bet[i] * expf(gx[i] - gam[j]) * dkk;
-                cv = expf(gam[i] - gam[j]) * dqk;
             }
-            Ls[i * LP + j] = lv;
-            Cs[i * LP + j] = cv;
-            As[i * LP + j] = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r;
+                float lv[4], cv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = j0 + c;
+                    lv[c] = (j < i) ? bet[i] * expf(gx[i] - gam[j]) * kk[r][c] : 0.f;
+                    cv[c] = (j <= i) ? expf(gam[i] - gam[j]) * qk[r][c] : 0.f;
+                }
+                st4(&Ls[i * TP + j0], make_float4(lv[0], lv[1], lv[2], lv[3]));
+                st4(&Cs[i * TP + j0], make_float4(cv[0], cv[1], cv[2], cv[3]));
+                st4(&As[i * TP + j0], make_float4(0.f, 0.f, 0.f, 0.f));
+            }
         }
         __syncthreads();
         // ---- (4a) inverses of the four 16 x 16 diagonal blocks of I + L (forward substitution)
@@ -151,11 +213,11 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             for (int r = 1; r < 16; ++r) {
                 float a = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) a = fmaf(Ls[(base + r) * LP + base + m], x[m], a);
+                for (int m = 0; m < r; ++m) a = fmaf(Ls[(base + r) * TP + base + m], x[m], a);
                 if (r > c) x[r] = -a;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) As[(base + r) * LP + base + c] = x[r];
+            for (int r = 0; r < 16; ++r) As[(base + r) * TP + base + c] = x[r];
         }
         __syncthreads();
         // ---- (4b) off-diagonal blocks: A_IJ = -inv(T_II) sum_{m=J}^{I-1} L_Im A_mJ
@@ -168,8 +230,8 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
                     for (int m = J; m < I; ++m) {
 #pragma unroll
                         for (int l = 0; l < 16; ++l)
-                            a = fmaf(Ls[(16 * I + r) * LP + 16 * m + l],
-                                     As[(16 * m + l) * LP + 16 * J + c], a);
+                            a = fmaf(Ls[(16 * I + r) * TP + 16 * m + l],
+                                     As[(16 * m + l) * TP + 16 * J + c], a);
                     }
                     Yb[J * 256 + r * 16 + c] = a;
                 }
@@ -178,40 +240,99 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
                     float a = 0.f;
 #pragma unroll
                     for (int l = 0; l < 16; ++l)
-                        a = fmaf(As[(16 * I + r) * LP + 16 * I + l], Yb[J * 256 + l * 16 + c], a);
-                    As[(16 * I + r) * LP + 16 * J + c] = -a;
+                        a = fmaf(As[(16 * I + r) * TP + 16 * I + l], Yb[J * 256 + l * 16 + c], a);
+                    As[(16 * I + r) * TP + 16 * J + c] = -a;
                 }
                 __syncthreads();
             }
         }
-        // ---- (5) dR = Kd D' + C^T dO
-        for (int e = tid; e < 64 * CT; e += kThreads) {
-            const int j = e / CT, c = e % CT;
-            float a = 0.f;
-#pragma unroll 8
-            for (int l = 0; l < KD; ++l) a = fmaf(ks[j * KP + l], Ds[l * CT + c], a);
-            float t = 0.f;
-            for (int i = j; i < 64; ++i) t = fmaf(Cs[i * LP + j], dos[i * CT + c], t);
-            Rs[e] = fmaf(dk[j], a, t);
+        // ---- (5) dR = Kd D' + C^T dO, one 4 x 2 block (rows j0.., columns cc..) per thread
+        const int j0 = (tid / 16) * 4, cc = (tid % 16) * 2;
+        {
+            float a[4][2] = {}, t[4][2] = {};
+#pragma unroll 4
+            for (int l = 0; l < KD; ++l) {
+                const float4 kv = ld4(&kt[l * TP + j0]);
+                const float2 dv = *reinterpret_cast<const float2*>(&Ds[l * CT + cc]);
+                const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    a[r][0] = fmaf(k4[r], dv.x, a[r][0]);
+                    a[r][1] = fmaf(k4[r], dv.y, a[r][1]);
+                }
+            }
+            for (int i = j0; i < 64; ++i) {   // C[i][j] = 0 for j > i
+                const float4 cv = ld4(&Cs[i * TP + j0]);
+                const float2 ov = *reinterpret_cast<const float2*>(&dos[i * CT + cc]);
+                const float c4[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    t[r][0] = fmaf(c4[r], ov.x, t[r][0]);
+                    t[r][1] = fmaf(c4[r], ov.y, t[r][1]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<float2*>(&Rs[(j0 + r) * CT + cc]) =
+                    make_float2(fmaf(dk[j0 + r], a[r][0], t[r][0]), fmaf(dk[j0 + r], a[r][1], t[r][1]));
         }
         __syncthreads();
-        // ---- (6) Z = diag(beta exp(Gx)) A^T dR
-        for (int e = tid; e < 64 * CT; e += kThreads) {
-            const int j = e / CT, c = e % CT;
-            float a = 0.f;
-            for (int i = j; i < 64; ++i) a = fmaf(As[i * LP + j], Rs[i * CT + c], a);
-            Zs[e] = ekr[j] * a;
+        // ---- (6) Z = diag(beta exp(Gx)) A^T dR (same blocking)
+        {
+            float a[4][2] = {};
+            for (int i = j0; i < 64; ++i) {   // A[i][j] = 0 for j > i
+                const float4 av = ld4(&As[i * TP + j0]);
+                const float2 rv = *reinterpret_cast<const float2*>(&Rs[i * CT + cc]);
+                const float a4[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    a[r][0] = fmaf(a4[r], rv.x, a[r][0]);
+                    a[r][1] = fmaf(a4[r], rv.y, a[r][1]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                *reinterpret_cast<float2*>(&Zs[(j0 + r) * CT + cc]) =
+                    make_float2(ekr[j0 + r] * a[r][0], ekr[j0 + r] * a[r][1]);
         }
         __syncthreads();
-        // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z
-        const float dlast = expf(glast);
-        for (int e = tid; e < KD * CT; e += kThreads) {
-            const int l = e / CT, c = e % CT;
-            float a = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < 64; ++i)
-                a = fmaf(eq[i] * qs[i * KP + l], dos[i * CT + c], fmaf(-ks[i * KP + l], Zs[i * CT + c], a));
-            Ds[e] = fmaf(dlast, Ds[e], a);
+        // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z, one 4 x CW block (rows l0..) per thread
+        {
+            constexpr int CW = KD * CT / (kThreads * 4);   // 4 columns at K = 128, 2 at K = 64
+            const int l0 = (tid / (CT / CW)) * 4, d0 = (tid % (CT / CW)) * CW;
+            float a[4][CW] = {};
+#pragma unroll 4
+            for (int i = 0; i < 64; ++i) {
+                const float e = eq[i];
+                const float4 qv = ld4(&qr[i * KD + l0]), kv = ld4(&kr[i * KD + l0]);
+                float o4[CW], z4[CW];
+                if constexpr (CW == 4) {
+                    const float4 ov = ld4(&dos[i * CT + d0]), zv = ld4(&Zs[i * CT + d0]);
+                    o4[0] = ov.x, o4[1] = ov.y, o4[2] = ov.z, o4[3] = ov.w;
+                    z4[0] = zv.x, z4[1] = zv.y, z4[2] = zv.z, z4[3] = zv.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < CW; ++c) {
+                        o4[c] = dos[i * CT + d0 + c];
+                        z4[c] = Zs[i * CT + d0 + c];
+                    }
+                }
+                const float q4[4] = {e * qv.x, e * qv.y, e * qv.z, e * qv.w};
+                const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < CW; ++c)
+                        a[r][c] = fmaf(q4[r], o4[c], fmaf(-k4[r], z4[c], a[r][c]));
+            }
+            const float dlast = expf(glast);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < CW; ++c) {
+                    float* dp = &Ds[(l0 + r) * CT + d0 + c];
+                    *dp = fmaf(dlast, *dp, a[r][c]);
+                }
         }
         __syncthreads();
     }
