@@ -592,7 +592,8 @@ def run_state_grad(args):
                        "parallelism": f"weak: {world} rank(s) x one batch each"},
             "roofline": {"bound": "alu", "achieved": round(ach, 3),
                          "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
-                         "frac": round(ach / FP32_ALU_TFLOPS, 4), "traffic": None,
+                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
+                         "traffic": None if args.T else recorded_traffic("state_grad_kernel", w0.name),
                          "kernel": "state_grad_kernel", "kernel_ms": round(avg["state_grad"], 4),
                          "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
                          "peak_source": "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
