@@ -510,6 +510,8 @@ gdn_status gdn_state_grad_summary(const gdn_problem* p, int nseg, const void* q,
     gdn_status st = check_problem(p, nseg);
     if (st != GDN_OK) return st;
     if (p->gate_k) return GDN_ERR_UNSUPPORTED_SHAPE;
+    // one CTA per (b, h, segment, 32-column tile) on a one-dimensional grid
+    if ((long long)p->B * p->H * nseg * (p->V / 32) >= (1LL << 31)) return GDN_ERR_UNSUPPORTED_SHAPE;
     if (!dS) return GDN_ERR_INVALID_ARG;
     if (p->T > 0 && (!q || !k || !g || !beta || !dO)) return GDN_ERR_INVALID_ARG;
     for (const void* ptr : {q, k, g, beta, dO, (const void*)dH_end, (const void*)dS})

@@ -79,11 +79,15 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
     float* ekr = eq + 64;         // beta_i exp(Gx_i)
     constexpr int TP = L::TP;
 
+    // one-dimensional grid, the column tile varying fastest: a chain's tiles are launched side
+    // by side and L2 serves the k, q, g, beta reads that they repeat
     const int tid = threadIdx.x;
-    const int seg = blockIdx.x % p.nseg;
-    const int bh = blockIdx.x / p.nseg;
+    const int ntiles = p.V / CT;
+    const int chain = blockIdx.x / ntiles;
+    const int seg = chain % p.nseg;
+    const int bh = chain / p.nseg;
     const int b = bh / p.H, h = bh % p.H;
-    const int c0 = blockIdx.y * CT;
+    const int c0 = (blockIdx.x % ntiles) * CT;
     const int V = p.V, H = p.H;
     const long long head = (long long)seg * p.B * H + bh;   // [seg][b][h] index
 
@@ -406,7 +410,7 @@ cudaError_t launch_state_grad_k(const StateGradParams& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L::bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.B * p.H * p.nseg), (unsigned)(p.V / CT));
+    dim3 grid((unsigned)(p.B * p.H * p.nseg * (p.V / CT)));
     kern<<<grid, kThreads, L::bytes, s>>>(p);
     return cudaGetLastError();
 }
