@@ -30,6 +30,9 @@ What each function computes (pages cited by title and section):
   state_grad_summary -- dS_local of each segment (RFC 6.4.3): the gradient reaching the
                      state entering the segment from its own outputs, rank-1 per token.
   state_grad_scan -- dH_in[s] = M[s]^T dH_in[s+1] + dS[s] from dH_in[nseg] = dht (RFC 6.4.3).
+  chunked_bwd.chunked_backward -- (module oracle/chunked_bwd.py, numpy) the same gradients in the
+                     chunk form a chunked GPU backward computes; used only to pin
+                     chunked == per-token and to expose the chunk intermediates.
   chunked_fwd / chunked_summary -- the chunk equations of "Context Parallelism in ART",
                      section 08 "First parallelize within a GPU", restated for the RFC's
                      un-decayed read; used only to pin chunked == per-token.
