@@ -79,6 +79,25 @@ def test_algorithmic_model_matches_hand_count():
     assert bench.launches_per_step(synth.WORKLOADS["single_seg_h16_t8k"], 1) == 2
 
 
+def test_state_grad_model_matches_hand_count():
+    # the backward state-gradient kernel, counted by hand per chunk of 64 tokens and head at
+    # K = V = 128: K K^T and Q K^T 2*(64*64*128*2) = 2.10 M, the inverse 0.17 M,
+    # dR = Kd D + C^T dO 64*128*128*2 + 64*64*128*2 = 3.15 M, A^T dR 64*64*128 = 0.52 M,
+    # the D update 2*(128*64*128*2) = 4.19 M: 10.13 M per chunk, 158 kFLOP per token-head
+    w = synth.WORKLOADS["cp4_b2_h32_t32k"]
+    tok_heads = 2 * 32768 * 32
+    alg = bench.state_grad_algorithmic(w)
+    per_chunk = 2 * 64 * 64 * 128 * 2 + 0.17e6 + 64 * 128 * 128 * 2 + 64 * 64 * 128 * 2 + \
+        64 * 64 * 128 + 2 * 128 * 64 * 128 * 2
+    assert abs(alg["flops"] - per_chunk * tok_heads / 64) < 1e3
+    assert 157e3 < alg["flops"] / tok_heads < 160e3
+    # q, k (2 x 128 bf16), g, beta (bf16) and dO (128 fp32) read once; dS (4 segments x 64
+    # heads x 64 KiB) written
+    assert alg["bytes"] == tok_heads * (512 + 4 + 512) + 4 * 64 * 128 * 128 * 4
+    # fp32 CUDA-core peak from unit counts and the maximum SM clock
+    assert abs(bench.FP32_ALU_TFLOPS - 80.55) < 0.01
+
+
 @pytest.mark.parametrize("steps", [3])
 def test_reference_arm_json_line(steps):
     env = dict(os.environ)
