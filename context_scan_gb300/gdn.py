@@ -243,9 +243,7 @@ def gdn_state_grad_summary(q, k, g, beta, dO, dS, nseg, dH_end=None, stream=None
     """Per-segment state gradients: dS [nseg,B,H,K,V] fp32 receives the gradient on the state
     entering each segment of its outputs' loss (sum dO . o) plus <dH_end[s], state leaving
     it> (dH_end None = 0). dO carries the output dtype (fp32 or bf16)."""
-    prob = prob or problem(k, dO, dO)
-    if prob.gate_k:
-        raise GdnError(2, "gdn_state_grad_summary")
+    prob = prob or problem(k, dO, dO, g=g)   # a [B,T,H,K] g sets gate_k: rejected below
     _check(lib().gdn_state_grad_summary(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(g),
                                         _ptr(beta), _ptr(dO), _ptr(dH_end), _ptr(dS),
                                         _stream(stream)), "gdn_state_grad_summary")

@@ -156,3 +156,18 @@ def test_state_grad_validation(L):
     assert C(ctypes.byref(P(K=64, V=128)), 2, fake, fake, None, fake, None) == 2
     assert C(ctypes.byref(P()), 0, fake, fake, None, fake, None) == 1
     assert C(ctypes.byref(P()), 2, fake, fake, odd, fake, None) == 4             # dht misaligned
+
+
+def test_state_grad_binding_rejects_per_channel_gates(L):
+    # the binding describes g's layout to the library: per-channel gates [B,T,H,K] are
+    # refused (GDN_ERR_UNSUPPORTED_SHAPE) before any pointer is used, never read as [B,T,H]
+    import torch
+    B, T, H, K = 1, 64, 2, 64
+    q = torch.zeros((B, T, H, K))
+    g4 = torch.zeros((B, T, H, K))
+    beta = torch.zeros((B, T, H))
+    dO = torch.zeros((B, T, H, K))
+    dS = torch.zeros((1, B, H, K, K))
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_state_grad_summary(q, q, g4, beta, dO, dS, 1, stream=0)
+    assert e.value.status == 2
