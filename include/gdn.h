@@ -228,8 +228,9 @@ GDN_API gdn_status gdn_segmented_fwd_noalloc(const gdn_problem* p, int nseg, con
  *   dO [B,T,H,V] in out_dtype (the output's dtype); dH_end [nseg,B,H,K,V] fp32 or NULL
  *   (zero: the RFC's dS_local); dS [nseg,B,H,K,V] fp32, written. With nseg == 1 and
  *   dH_end = dht, dS[0] is dh0, the initial-state gradient. T % (64*nseg) == 0, K = V in
- *   {64, 128}; every pointer 16-byte aligned. fp32 arithmetic on CUDA cores; no workspace.
- *   Asynchronous on `stream`. */
+ *   {64, 128}; every pointer 16-byte aligned; B*H*nseg*(V/32) < 2^31 (one CTA per 32-column
+ *   tile of every segment's state gradient). dS must not overlap any input (dH_end included).
+ *   fp32 arithmetic on CUDA cores; no workspace. Asynchronous on `stream`. */
 GDN_API gdn_status gdn_state_grad_summary(const gdn_problem* p, int nseg, const void* q,
                                           const void* k, const void* g, const void* beta,
                                           const void* dO, const float* dH_end, float* dS,
