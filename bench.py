@@ -96,11 +96,19 @@ def rank_seed_offset(rank: int) -> int:
 # ---------------------------------------------------------------------------------------
 # algorithmic model of the path (bytes and flops per launch)
 # ---------------------------------------------------------------------------------------
-def algorithmic(w, pieces=None, out_bytes: int = 4):
-    """Compulsory HBM bytes and dense-contraction flops of each stage for workload w, when the
-    library cuts every sequence into `pieces` pieces (default: one per segment), and of the
-    method itself (the pages' flow: summaries of nseg-1 segments, the scan, the forward)."""
-    P = pieces or w.nseg
+def algorithmic(w, plan=None, out_bytes: int = 4):
+    """Compulsory HBM bytes and dense-contraction flops of each stage for workload w under the
+    piece plan `plan` = (P, chunks of piece 0, chunks of each later piece) that the library
+    reports (default: one equal piece per segment), and of the method itself (the pages' flow:
+    summaries of the nseg-1 segments that feed a later one, the scan, the forward).
+
+    Intermediates (the WY factors, per-chunk states) count as zero: the method keeps them on
+    chip. The "wy" stage's bytes are this implementation's extra traffic, reported beside the
+    stages but not in the executed total."""
+    nch = w.T // 64
+    if plan is None:
+        plan = (w.nseg, nch // w.nseg, nch // w.nseg)
+    P, first, rest = plan
     isz = 2 if w.in_dtype == "bf16" else 4
     BH = w.B * w.H
     tok_heads = w.B * w.T * w.H
@@ -117,11 +125,13 @@ def algorithmic(w, pieces=None, out_bytes: int = 4):
                  + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
     # prep (K K^T, U, W) + augmented K x (K+V) state update, per chunk
     sum_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 2 * 64 * K * (K + V))
-    ps = max(P - 2, 0)   # pieces with a summary
+    ps = max(P - 2, 0)                  # pieces with a summary (1 .. P-2)
+    th_first = BH * first * 64          # token-heads of piece 0
+    th_rest = BH * rest * 64            # token-heads of each later piece
     stages = {
         # per-chunk WY factors (tensor-core path only): reads k, g, beta; writes two bf16
         # 64 x 64 tiles per chunk. An intermediate of this implementation, not of the method,
-        # so it is left out of the path total below.
+        # so it is left out of the executed total below.
         "wy": {
             "bytes": (tok_heads * (K * isz + 2 * isz) + chunks * 16384) if tc else 0,
             "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64) if tc else 0,
@@ -129,10 +139,12 @@ def algorithmic(w, pieces=None, out_bytes: int = 4):
         # piece 0's forward from h0 (handing its final state on) and the summaries of pieces
         # 1..P-2
         "phase1": {
-            "bytes": tok_heads // P * fwd_tok + 2 * kv_state
-            + tok_heads * ps // P * sum_tok + ps * (kk_state + kv_state),
-            "flops": chunks // P * fwd_flops + chunks * ps // P * sum_flops,
+            "bytes": th_first * fwd_tok + (2 if P > 1 else 1) * kv_state
+            + th_rest * ps * sum_tok + ps * (kk_state + kv_state),
+            "flops": th_first // 64 * fwd_flops + th_rest * ps // 64 * sum_flops,
         },
+        # reads the summaries and the state piece 0 ends in; writes the state entering every
+        # later piece and every segment
         "scan": {
             "bytes": (ps * (kk_state + kv_state) + kv_state + ps * kv_state + w.nseg * kv_state
                       if P > 1 else w.nseg * kv_state),
@@ -140,10 +152,12 @@ def algorithmic(w, pieces=None, out_bytes: int = 4):
         },
         # the forward of pieces 1..P-1 from their scanned states
         "phase2": {
-            "bytes": (tok_heads * (P - 1) // P * fwd_tok + P * kv_state) if P > 1 else 0,
-            "flops": chunks * (P - 1) // P * fwd_flops,
+            "bytes": (th_rest * (P - 1) * fwd_tok + P * kv_state) if P > 1 else 0,
+            "flops": th_rest * (P - 1) // 64 * fwd_flops,
         },
     }
+    executed = {"bytes": sum(stages[k]["bytes"] for k in ("phase1", "scan", "phase2")),
+                "flops": sum(stages[k]["flops"] for k in ("phase1", "scan", "phase2"))}
     nseg = w.nseg
     method = {
         "bytes": tok_heads * (nseg - 1) // nseg * sum_tok + (nseg - 1) * (kk_state + kv_state)
@@ -152,7 +166,39 @@ def algorithmic(w, pieces=None, out_bytes: int = 4):
         "flops": chunks * (nseg - 1) // nseg * sum_flops + (nseg - 1) * BH * 2 * K * K * V
         + chunks * fwd_flops,
     }
-    return stages, method
+    return stages, executed, method
+
+
+def literal_algorithmic(w, out_bytes: int = 4):
+    """The pages' literal flow as three public calls: every segment's summary (all nseg, as
+    every rank forms its own), the scan, every segment's forward from its H_in. Returns the
+    per-call bytes/flops (intermediates count as zero; "wy" is this implementation's extra
+    traffic, formed once per call that needs it) and the total."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    BH = w.B * w.H
+    tok_heads = w.B * w.T * w.H
+    chunks = tok_heads // 64
+    K, V = w.K, w.V
+    kv_state = BH * K * V * 4
+    kk_state = BH * K * K * 4
+    g_tok = (K if w.gate_k else 1) * isz
+    fwd_tok = (2 * K + V) * isz + g_tok + isz + V * out_bytes
+    sum_tok = (K + V) * isz + g_tok + isz
+    fwd_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 64 * K * V * 2
+                 + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
+    sum_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 2 * 64 * K * (K + V))
+    nseg = w.nseg
+    calls = {
+        "summary": {"bytes": tok_heads * sum_tok + nseg * (kk_state + kv_state),
+                    "flops": chunks * sum_flops},
+        "scan": {"bytes": (nseg - 1) * (kk_state + kv_state) + kv_state + nseg * kv_state,
+                 "flops": (nseg - 1) * BH * 2 * K * K * V},
+        "forward": {"bytes": tok_heads * fwd_tok + nseg * kv_state + kv_state,
+                    "flops": chunks * fwd_flops},
+    }
+    total = {"bytes": sum(c["bytes"] for c in calls.values()),
+             "flops": sum(c["flops"] for c in calls.values())}
+    return calls, total
 
 
 def launches_per_step(w, pieces=None):
@@ -172,26 +218,38 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
+# The translation units each recorded kernel is built from (and the headers they include):
+# a traffic record stays valid exactly as long as these files are unchanged.
+KERNEL_SOURCES = {
+    "gdn_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
+    "gdn_varlen_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
+    "gdn_wy": ("gdn_wy.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
+    "state_grad_kernel": ("gdn_bwd.cu", "gdn_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources the named kernel is built from (plus the public header)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "context_scan_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "gdn.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on this source."""
+    """dram bytes per launch from a committed ncu summary, if it was taken on the sources the
+    kernel is built from now."""
     p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
         return None
     kv = {}
     for line in open(p):
         if ":" in line:
             a, b = line.split(":", 1)
             kv[a.strip()] = b.strip()
-    if kv.get("kernel_source_hash") != kernel_source_hash():
+    if kv.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -461,14 +519,15 @@ def run_varlen(args):
 def state_grad_algorithmic(w):
     """Per launch of the state-gradient kernel over workload w: compulsory HBM bytes (read q, k,
     g, beta in the input dtype and dO in fp32 once; write dS) and fp32 flops per chunk and head
-    counted once: K K^T and Q K^T (2 * 64*64*K*2), the 64 x 64 inverse (~0.17 M), dR = Kd D +
-    C^T dO (64*K*V*2 + 64*64*V*2), A^T dR (64*64*V), D update (2 * K*64*V*2)."""
+    counted once, every product as a dense tile (the triangular C^T dO and A^T dR alike): K K^T
+    and Q K^T (2 * 64*64*K*2), the 64 x 64 inverse (~0.17 M), dR = Kd D + C^T dO (64*K*V*2 +
+    64*64*V*2), A^T dR (64*64*V*2), D update (2 * K*64*V*2)."""
     isz = 2 if w.in_dtype == "bf16" else 4
     th = w.B * w.T * w.H
     nbytes = th * (2 * w.K * isz + 2 * isz + w.V * 4) + w.nseg * w.B * w.H * w.K * w.V * 4
     c = 64
     per_chunk = (2 * c * c * w.K * 2 + 0.17e6 + c * w.K * w.V * 2 + c * c * w.V * 2 +
-                 c * c * w.V + 2 * w.K * c * w.V * 2)
+                 c * c * w.V * 2 + 2 * w.K * c * w.V * 2)
     return {"bytes": nbytes, "flops": per_chunk * th / c}
 
 
@@ -611,6 +670,16 @@ def run_state_grad(args):
         dist.destroy_process_group()
 
 
+def workload_metric(w0) -> str:
+    """The headline metric names its own workload; the other workloads carry their shape."""
+    if w0.name == DEFAULT_WORKLOAD:
+        return METRIC
+    if w0.gate_k:
+        return KDA_METRIC
+    return (f"GDN segmented fwd tokens/s at B{w0.B} H{w0.H} K=V={w0.K} T={w0.T} "
+            f"{w0.nseg} segments {w0.in_dtype}; % of roofline")
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -629,6 +698,7 @@ def run_ours(args):
                      per_sequence_seed=(None if w0.per_sequence_seed is None
                                         else w0.per_sequence_seed + rank_seed_offset(rank)),
                      **({} if args.T is None else {"T": args.T}))
+    literal = args.schedule == "literal"
     x = synth.make_inputs(w)
     dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
     names = ("q", "k", "v", "g", "beta")
@@ -640,19 +710,60 @@ def run_ours(args):
     prob = gdn.problem(d["k"], d["v"], o, g=d["g"])
     if prob.gate_k != int(w.gate_k):
         raise RuntimeError("the problem's gate layout does not match the workload")
-    pieces = gdn.segmented_pieces(prob, w.nseg)
-    ws = gdn.alloc_workspace(prob, w.nseg, device=dev)
     stream = torch.cuda.current_stream()
+    if literal:
+        # the pages' flow from three public calls: every segment's summary, the in-order
+        # apply, every segment's forward from its H_in
+        plan = (w.nseg, w.T // 64 // w.nseg, w.T // 64 // w.nseg)
+        ws = gdn.alloc_workspace(prob, 1, device=dev)
+        Mb = torch.empty((w.nseg, w.B, w.H, w.K, w.K), dtype=torch.float32, device=dev)
+        Sb = torch.empty((w.nseg, w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+        Hin = torch.empty((w.nseg, w.B, w.H, w.K, w.V), dtype=torch.float32, device=dev)
+        stage_names = ("summary", "scan", "forward")
+    else:
+        plan = gdn.segmented_plan(prob, w.nseg)
+        ws = gdn.alloc_workspace(prob, w.nseg, device=dev)
+        stage_names = ("wy", "phase1", "scan", "phase2")
+    pieces = plan[0]
+
+    def call(di, oi):
+        if literal:
+            gdn.gdn_segment_summary(di["k"], di["v"], di["g"], di["beta"], Mb, Sb, w.nseg, ws,
+                                    prob=prob, stream=stream)
+            gdn.gdn_summary_scan(Mb, Sb, di["h0"], Hin, stream=stream)
+            gdn.gdn_segment_fwd(di["q"], di["k"], di["v"], di["g"], di["beta"], Hin, oi[0],
+                                oi[1], w.nseg, ws, prob=prob, stream=stream)
+        else:
+            gdn.gdn_segmented_fwd(di["q"], di["k"], di["v"], di["g"], di["beta"], di["h0"],
+                                  oi[0], oi[1], w.nseg, ws, prob=prob, stream=stream)
 
     def step(events=None):
         if events is None:
-            gdn.gdn_segmented_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o, hf,
-                                  w.nseg, ws, prob=prob, stream=stream)
+            call(d, (o, hf))
+        elif literal:
+            events[0].record(stream)
+            gdn.gdn_segment_summary(d["k"], d["v"], d["g"], d["beta"], Mb, Sb, w.nseg, ws,
+                                    prob=prob, stream=stream)
+            events[1].record(stream)
+            gdn.gdn_summary_scan(Mb, Sb, d["h0"], Hin, stream=stream)
+            events[2].record(stream)
+            gdn.gdn_segment_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], Hin, o, hf, w.nseg,
+                                ws, prob=prob, stream=stream)
+            events[3].record(stream)
         else:
             gdn.gdn_segmented_fwd_timed(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], o,
                                         hf, w.nseg, ws, events, prob=prob, stream=stream)
 
+    # Inputs and output that fit in L2 twice over could be served from it in the next step:
+    # then a buffer larger than L2 is written between the timed steps, outside their events.
+    in_mb = total_input_mb(w)
+    touched = in_mb * 2**20 + w.B * w.T * w.H * w.V * 4
+    flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+             if touched < 2 * L2_BYTES else None)
+
     for _ in range(args.warmup):
+        if flush is not None:
+            flush.fill_(1.0)
         step()
     torch.cuda.synchronize()
     st, detail = gdn.gdn_check_device_error(ws)
@@ -660,7 +771,8 @@ def run_ours(args):
         raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    nev = len(stage_names) + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
     for e4 in ev:        # torch creates the CUDA event on first record; the library then
         for e in e4:     # re-records the same handles inside each step
             e.record(stream)
@@ -674,39 +786,63 @@ def run_ours(args):
         time.sleep(0.3)   # let the sampler start before the timed region
     t0.record(stream)
     for i in range(K):
+        if flush is not None:
+            flush.fill_(1.0)   # outside the step's own events
         step(ev[i])
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     barrier(dev)
-    elapsed = t0.elapsed_time(t1) / 1e3
+    if flush is None:
+        elapsed = t0.elapsed_time(t1) / 1e3
+    else:
+        elapsed = sum(e[0].elapsed_time(e[-1]) for e in ev) / 1e3
     max_elapsed = reduce_max(elapsed, device=dev if world > 1 else "cpu")
     st, detail = gdn.gdn_check_device_error(ws)
     if st != 0:
         raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
 
-    stage_ms = {"wy": [], "phase1": [], "scan": [], "phase2": []}
+    stage_ms = {n: [] for n in stage_names}
     for e in ev:
-        for i, name in enumerate(stage_ms):
+        for i, name in enumerate(stage_names):
             stage_ms[name].append(e[i].elapsed_time(e[i + 1]))
-    stages, total = algorithmic(w, pieces)
     avg = {k: sum(v) / len(v) for k, v in stage_ms.items()}
+    _, _, method = algorithmic(w, plan)
+    if literal:
+        stages, executed = literal_algorithmic(w)
+        kernel_name = {"summary": "gdn_summary_call", "scan": "gdn_scan",
+                       "forward": "gdn_segment_fwd"}
+    else:
+        stages, executed, _ = algorithmic(w, plan)
+        kernel_name = {"wy": "gdn_wy", "phase1": "gdn_phase1", "scan": "gdn_scan",
+                       "phase2": "gdn_forward"}
     dominant = max(avg, key=avg.get)
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    bf16_peak = float(peaks["bf16_tflops"])
     ach = stages[dominant]["bytes"] / (avg[dominant] * 1e-3) / 1e9
-    kernel_name = {"wy": "gdn_wy", "phase1": "gdn_phase1", "scan": "gdn_scan",
-                   "phase2": "gdn_forward"}[dominant]
     roofline = {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4), "traffic": recorded_traffic(kernel_name, w0.name),
-                "kernel": kernel_name, "kernel_ms": round(avg[dominant], 4),
+                "frac": round(ach / hbm, 4),
+                "traffic": recorded_traffic(kernel_name[dominant], w0.name),
+                "kernel": kernel_name[dominant], "kernel_ms": round(avg[dominant], 4),
                 "algorithmic_bytes": stages[dominant]["bytes"],
                 "peak_source": f"{peaks_src} hbm_gbs"}
-    t_roof = max(total["bytes"] / (hbm * 1e9),
-                 total["flops"] / (float(peaks["bf16_tflops"]) * 1e12))
     ms_per_step = max_elapsed / K * 1e3
     tokens = w.B * w.T
     value = aggregate(tokens, K, world, max_elapsed)
+
+    def path(total, what):
+        t_roof = max(total["bytes"] / (hbm * 1e9), total["flops"] / (bf16_peak * 1e12))
+        return {"t_roof_us": round(t_roof * 1e6, 1),
+                "frac": round(t_roof / (ms_per_step * 1e-3), 4),
+                "bytes": total["bytes"], "flops": total["flops"], "counts": what,
+                "peaks": f"{peaks_src}: hbm {hbm} GB/s, bf16 {peaks['bf16_tflops']} TF/s"}
+
+    path_roofline = path(executed, "the work this schedule runs: every pass it makes over the "
+                                   "inputs, summaries and states (intermediates such as the WY "
+                                   "tiles count as zero)")
+    method_roofline = path(method, f"the pages' method: summaries of the {w.nseg - 1} segments "
+                                   f"that feed a later one, the scan, the forward")
 
     # ---- end to end through the public API (pinned host -> device, call, device -> host)
     e2e = None
@@ -714,11 +850,6 @@ def run_ours(args):
         n_e2e = max(3, min(K, args.e2e_steps))
         h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
         d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
-
-        def call(di, oi):
-            gdn.gdn_segmented_fwd(di["q"], di["k"], di["v"], di["g"], di["beta"], di["h0"], oi[0],
-                                  oi[1], w.nseg, ws, prob=prob, stream=stream)
-
         barrier(dev)
         e_el = pipelined_e2e(torch, host, d, (o, hf), call, n_e2e, dev, stream)
         e_el = reduce_max(e_el, device=dev if world > 1 else "cpu")
@@ -734,27 +865,32 @@ def run_ours(args):
         cpu = cpu_baseline(w, x, budget_s=args.cpu_seconds)
 
     if rank == 0:
+        tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128 and not w.gate_k)
+        launches = (2 * tc + 3) if literal else launches_per_step(w, pieces)
+        l2 = (f"inputs larger than L2 ({in_mb:.0f} MB in + "
+              f"{w.B * w.T * w.H * w.V * 4 / 2**20:.0f} MB out > 129 MB); no flush"
+              if flush is None else
+              f"inputs fit in L2 ({in_mb:.0f} MB): a {2 * L2_BYTES / 2**20:.0f} MB buffer is "
+              f"written before every step, outside the step's events")
         line = {
-            "metric": metric_of(w), "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
+            "metric": workload_metric(w0), "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w0.name, "B": w.B, "H": w.H, "T": w.T, "K": w.K, "V": w.V,
-                       "nseg": w.nseg, "pieces": pieces, "chunk": 64, "in_dtype": w.in_dtype,
+                       "nseg": w.nseg, "schedule": args.schedule,
+                       "pieces": {"P": plan[0], "first_chunks": plan[1], "rest_chunks": plan[2]},
+                       "chunk": 64, "in_dtype": w.in_dtype,
                        "gates": "per key channel" if w.gate_k else "per token",
-                       "out_dtype": "f32", "state_dtype": "f32",
-                       "l2": f"inputs larger than L2 ({total_input_mb(w):.0f} MB in + "
-                             f"{w.B * w.T * w.H * w.V * 4 / 2**20:.0f} MB out > 129 MB); no flush",
+                       "out_dtype": "f32", "state_dtype": "f32", "l2": l2,
                        "parallelism": f"weak: {world} rank(s) x one batch each"},
             "roofline": roofline,
-            "path_roofline": {"t_roof_us": round(t_roof * 1e6, 1),
-                              "frac": round(t_roof / (ms_per_step * 1e-3), 4),
-                              "bytes": total["bytes"], "flops": total["flops"],
-                              "peaks": f"{peaks_src}: hbm {hbm} GB/s, bf16 {peaks['bf16_tflops']} TF/s"},
+            "path_roofline": path_roofline,
+            "method_roofline": method_roofline,
             "stage_ms": {k: round(v, 4) for k, v in avg.items()},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(w, pieces) * K,
+            "gpu_launches": launches * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -901,6 +1037,11 @@ def main(argv=None):
     ap.add_argument("--path", choices=["forward", "state_grad"], default="forward",
                     help="forward: the segmented forward (the headline line); state_grad: the "
                          "backward's state-gradient path on the same workload")
+    ap.add_argument("--schedule", choices=["pieces", "literal"], default="pieces",
+                    help="pieces: one gdn_segmented_fwd call (the library's piece plan; the "
+                         "headline line); literal: the pages' flow from three public calls -- "
+                         "gdn_segment_summary over every segment, gdn_summary_scan, "
+                         "gdn_segment_fwd")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

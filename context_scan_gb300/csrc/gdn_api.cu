@@ -374,6 +374,56 @@ gdn_status gdn_chunk_fwd(const gdn_problem* p, const void* q, const void* k, con
                          reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
+int gdn_segmented_plan(const gdn_problem* p, int nseg, int* first_chunks, int* rest_chunks) {
+    if (first_chunks) *first_chunks = 0;
+    if (rest_chunks) *rest_chunks = 0;
+    if (check_problem(p, nseg) != GDN_OK) return 0;
+    const PiecePlan plan = plan_pieces(*p, nseg);
+    if (first_chunks) *first_chunks = plan.first;
+    if (rest_chunks) *rest_chunks = plan.rest;
+    return plan.P;
+}
+
+gdn_status gdn_segment_fwd(const gdn_problem* p, int nseg, const void* q, const void* k,
+                           const void* v, const void* g, const void* beta, const float* H_in,
+                           void* o, float* h_final, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    gdn_status st = check_problem(p, nseg);
+    if (st != GDN_OK) return st;
+    if (p->T > 0 && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+    if ((st = check_workspace(p, 1, workspace, workspace_bytes)) != GDN_OK) return st;
+    for (const void* ptr : {q, k, v, g, beta, (const void*)H_in, (const void*)o,
+                            (const void*)h_final})
+        if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
+    if ((st = check_device()) != GDN_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = p->B * p->H;
+    if (p->T == 0) {
+        // no tokens: the state leaving the last segment is the state entering it
+        if (!h_final) return GDN_OK;
+        const float* last = H_in ? H_in + (long long)(nseg - 1) * BH * p->K * p->V : nullptr;
+        return from_cuda(gdn::launch_scan(nullptr, nullptr, last, nullptr, h_final, nullptr, 0, 1,
+                                          1, BH, p->K, p->V, s));
+    }
+    ChainParams c = base_params(p, workspace);
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.g = g;
+    c.beta = beta;
+    c.o = o;
+    c.h_start = H_in;
+    c.h_start_seg_stride = (long long)BH * p->K * p->V;
+    c.h_final = h_final;
+    c.seg_len = p->T / nseg;
+    c.seg_first = 0;
+    c.nseg_run = nseg;
+    c.nseg_total = nseg;
+    cudaError_t e = prepare(c, p, workspace, s);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    return from_cuda(run_forward(c, s));
+}
+
 gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const void* k, const void* v,
                                const void* g, const void* beta, float* M, float* S,
                                void* workspace, size_t workspace_bytes, void* stream) {

@@ -11,7 +11,10 @@
 // The array is a file-scope __device__ variable of GDN_NOALLOC_SCRATCH_BYTES bytes: every GPU
 // that loads this library holds it until the process exits. Host code cannot use the
 // array's name as a device address, so the first call on each device looks its address up
-// with cudaGetSymbolAddress (with that device current) and caches it.
+// with cudaGetSymbolAddress (with that device current) and caches it. The cache is keyed by
+// device number, which assumes the runtime's primary context: with another driver context
+// current, or after cudaDeviceReset, the cached address would belong to a context that is
+// gone, so those uses are documented as unsupported.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

@@ -18,8 +18,9 @@ GDN_DTYPE_F32, GDN_DTYPE_BF16 = 0, 1
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
           3: "GDN_ERR_UNSUPPORTED_DTYPE", 4: "GDN_ERR_MISALIGNED", 5: "GDN_ERR_WORKSPACE",
           6: "GDN_ERR_CUDA", 7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_DEVICE"}
-EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
-            "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
+EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_segmented_plan", "gdn_chunk_fwd",
+            "gdn_segment_summary", "gdn_summary_scan", "gdn_segment_fwd", "gdn_segmented_fwd",
+            "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
             "gdn_state_grad_summary", "gdn_state_grad_scan",
             "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
@@ -55,6 +56,10 @@ def lib():
         L.gdn_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_segmented_pieces.argtypes = [pp, ctypes.c_int]
         L.gdn_segmented_pieces.restype = ctypes.c_int
+        L.gdn_segmented_plan.argtypes = [pp, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int)]
+        L.gdn_segmented_plan.restype = ctypes.c_int
+        L.gdn_segment_fwd.argtypes = [pp, ctypes.c_int] + [_P] * 9 + [ctypes.c_size_t, _P]
         L.gdn_chunk_fwd.argtypes = [pp] + [_P] * 9 + [ctypes.c_size_t, _P]
         L.gdn_segment_summary.argtypes = [pp, ctypes.c_int] + [_P] * 7 + [ctypes.c_size_t, _P]
         L.gdn_summary_scan.argtypes = [pp, ctypes.c_int] + [_P] * 5
@@ -73,7 +78,7 @@ def lib():
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
         L.gdn_selftest_wait_timeout.argtypes = [_P, ctypes.c_longlong, _P]
-        for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan",
+        for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan", "gdn_segment_fwd",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
                    "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error",
                    "gdn_selftest_wait_timeout", "gdn_state_grad_summary", "gdn_state_grad_scan"):
@@ -126,6 +131,14 @@ def segmented_pieces(prob: Problem, nseg: int = 1) -> int:
     return int(lib().gdn_segmented_pieces(ctypes.byref(prob), nseg))
 
 
+def segmented_plan(prob: Problem, nseg: int = 1):
+    """(P, chunks of piece 0, chunks of each later piece) of the segmented forward's piece plan
+    on the current device ((0, 0, 0): invalid)."""
+    first, rest = ctypes.c_int(0), ctypes.c_int(0)
+    P = lib().gdn_segmented_plan(ctypes.byref(prob), nseg, ctypes.byref(first), ctypes.byref(rest))
+    return int(P), int(first.value), int(rest.value)
+
+
 def alloc_workspace(prob: Problem, nseg: int = 1, device="cuda"):
     """A zeroed workspace tensor of the size the library asks for (torch owns the memory)."""
     import torch
@@ -156,6 +169,17 @@ def gdn_summary_scan(M, S, h0, H_in, stream=None, prob=None):
     prob = prob or Problem(B, 0, H, K, V, 64, GDN_DTYPE_F32, GDN_DTYPE_F32)
     _check(lib().gdn_summary_scan(ctypes.byref(prob), nseg, _ptr(M), _ptr(S), _ptr(h0),
                                   _ptr(H_in), _stream(stream)), "gdn_summary_scan")
+
+
+def gdn_segment_fwd(q, k, v, g, beta, H_in, o, h_final, nseg, workspace, stream=None,
+                    prob=None):
+    """The chunked forward of each of nseg segments from H_in[s] (None: zero states);
+    workspace sized by workspace_bytes(prob, 1)."""
+    prob = prob or problem(k, v, o, g=g)
+    _check(lib().gdn_segment_fwd(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(H_in), _ptr(o), _ptr(h_final), _ptr(workspace),
+                                 workspace.numel() if workspace is not None else 0,
+                                 _stream(stream)), "gdn_segment_fwd")
 
 
 def gdn_segmented_fwd(q, k, v, g, beta, h0, o, h_final, nseg, workspace, H_in=None,

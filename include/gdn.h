@@ -40,7 +40,11 @@
  *
  * Ownership: the caller allocates every buffer (device memory) and keeps it alive until the
  * stream work completes. The library allocates nothing, keeps no state between calls and
- * never synchronises the stream, except gdn_check_device_error.
+ * never synchronises the stream, except gdn_check_device_error. One exception:
+ * gdn_segmented_fwd_noalloc takes its scratch from an array the library itself owns (held
+ * on every GPU that loads it), caches that array's address per device, and leaves the last
+ * call's contents in it; calls to it that overlap on the GPU must be serialised (see its
+ * description).
  *
  * Workspace: a caller-provided device buffer of at least gdn_workspace_bytes() bytes, whose
  * first 256 bytes must be zero before the first call that uses it (it holds the device
@@ -123,6 +127,13 @@ GDN_API size_t gdn_workspace_bytes(const gdn_problem* p, int nseg);
  * when no device is current). Returns 0 for an invalid problem. */
 GDN_API int gdn_segmented_pieces(const gdn_problem* p, int nseg);
 
+/* The piece plan behind gdn_segmented_pieces: returns P (0 for an invalid problem) and, when
+ * the pointers are non-NULL, the chunks of piece 0 (*first_chunks) and of each later piece
+ * (*rest_chunks); first == rest for an equal-piece plan. For accounting of the work a call
+ * does (which summaries run); same device dependence as gdn_segmented_pieces. */
+GDN_API int gdn_segmented_plan(const gdn_problem* p, int nseg, int* first_chunks,
+                               int* rest_chunks);
+
 /* Chunked forward over all T tokens from the initial state h0.
  *   RFC section 2.1 (recurrence); ART section 08 "First parallelize within a GPU" (chunks).
  *   Runs as gdn_segmented_fwd with one segment (cut into gdn_segmented_pieces(p, 1) pieces);
@@ -153,6 +164,24 @@ GDN_API gdn_status gdn_segment_summary(const gdn_problem* p, int nseg, const voi
  *   p->V are read from the problem. */
 GDN_API gdn_status gdn_summary_scan(const gdn_problem* p, int nseg, const float* M, const float* S,
                             const float* h0, float* H_in, void* stream);
+
+/* The chunked forward of every segment from the state given for its start -- the last two
+ * stages of the RFC's forward flow, "forward_apply_state" (per-chunk states) and
+ * "forward_output" (token output), section 6.4.2, run by every emulated rank at once once it
+ * has its H_in. Composed with gdn_segment_summary and gdn_summary_scan it is the pages'
+ * literal flow: every rank's summary, the in-order summary apply, then each rank's local
+ * forward (RFC sections 6.4.1 and 6.5).
+ *   H_in     [nseg,B,H,K,V] fp32: the state entering each segment (NULL: zero for every
+ *            segment); read only.
+ *   o        [B,T,H,V] out_dtype, written.
+ *   h_final  [B,H,K,V] fp32: the state after the last segment's last token; NULL skips it.
+ *   Workspace: gdn_workspace_bytes(p, 1). Segment s covers tokens [s*T/nseg, (s+1)*T/nseg)
+ *   and runs as one chain per (b, h, segment). T == 0 writes only h_final (= H_in[nseg-1],
+ *   or zeros). */
+GDN_API gdn_status gdn_segment_fwd(const gdn_problem* p, int nseg, const void* q, const void* k,
+                                   const void* v, const void* g, const void* beta,
+                                   const float* H_in, void* o, float* h_final, void* workspace,
+                                   size_t workspace_bytes, void* stream);
 
 /* The segmented forward (RFC section 6.4.1/6.4.2 forward flow on one GPU): with P =
  * gdn_segmented_pieces(p, nseg) pieces per sequence, piece 0's forward from h0 beside the
@@ -200,7 +229,10 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
  *   words that receive this call's device error word {code, detail} (see
  *   gdn_check_device_error for the codes) when the call's stream work completes.
  *   First call on a device: it looks up that device's copy of the array
- *   (cudaGetSymbolAddress) with the device current; make it before any stream capture.
+ *   (cudaGetSymbolAddress) with the device current and caches the address per device; make
+ *   it before any stream capture. The cache assumes the runtime's primary context of each
+ *   device: calls made with another driver context current, or after cudaDeviceReset, are
+ *   not supported (the cached address would belong to a context that is gone).
  *   All calls share the one array, which keeps the last call's contents (the call clears
  *   the error word itself): calls that overlap on the GPU -- on different streams, or from
  *   different host threads -- race on it and must be serialised by the caller. */
@@ -293,7 +325,6 @@ GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const in
                                         size_t workspace_bytes, void* stream,
                                         void* const* stage_events);
 
-/* Static, NUL-terminated description of a status code. */
 /* Self-test of the failure path every kernel wait takes: one CTA waits on a barrier that
  * nothing arrives at, with a limit of limit_cycles SM clock cycles (1 .. 2^32), then records
  * GDN_ERR_TIMEOUT (detail word 0x5E) in the workspace's device error word and returns, as a
@@ -302,6 +333,7 @@ GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const in
  * (only its first 8 bytes are touched). Returns GDN_ERR_INVALID_ARG for a limit out of range. */
 GDN_API gdn_status gdn_selftest_wait_timeout(void* workspace, long long limit_cycles, void* stream);
 
+/* Static, NUL-terminated description of a status code. */
 GDN_API const char* gdn_status_string(gdn_status s);
 
 /* Synchronises `stream`, reads the workspace's device error word, clears it, and returns

@@ -24,3 +24,23 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """With GDN_ERR_LOG set, list the largest recorded error of each (test, label): the
+    measured max|err| / RMS(ref) against the oracle, beside the bar the test applies."""
+    import json
+    path = os.environ.get("GDN_ERR_LOG")
+    if not path or not os.path.exists(path):
+        return
+    worst = {}
+    for line in open(path):
+        try:
+            r = json.loads(line)
+        except ValueError:
+            continue
+        key = (r["test"], r["label"] or "")
+        worst[key] = max(worst.get(key, 0.0), r["err"])
+    terminalreporter.write_sep("-", "recorded errors (max|err| / RMS(ref))")
+    for (test, label), e in sorted(worst.items()):
+        terminalreporter.write_line(f"{e:10.3e}  {test}  {label or ''}")

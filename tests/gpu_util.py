@@ -4,6 +4,9 @@ binding, run the oracle on the same inputs, and the tolerance metric.
 Tolerance metric (per tensor): max_i |x_gpu - x_ref| / sqrt(mean(x_ref^2)).
 Bars: 1e-4 for fp32 inputs; 2e-2 for bf16 inputs (fp32 outputs).
 """
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -14,13 +17,26 @@ TOL_F32 = 1e-4
 TOL_BF16 = 2e-2
 
 
-def rel_err(x, ref):
+# When GDN_ERR_LOG names a file, every measured error is appended to it as one JSON line
+# (the test, an optional label, the value), so a run records the margin to each bar.
+ERR_LOG = os.environ.get("GDN_ERR_LOG")
+
+
+def record(value, label=None):
+    if ERR_LOG:
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        with open(ERR_LOG, "a") as f:
+            f.write(json.dumps({"test": test, "label": label, "err": value}) + "\n")
+    return value
+
+
+def rel_err(x, ref, label=None):
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     scale = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
     if ref.size == 0:
         return 0.0
-    return float(np.max(np.abs(x - ref)) / max(scale, 1e-30))
+    return record(float(np.max(np.abs(x - ref)) / max(scale, 1e-30)), label)
 
 
 def tol_for(w):

@@ -58,7 +58,8 @@ def test_algorithmic_model_matches_hand_count():
     w = synth.WORKLOADS["cp4_b2_h32_t32k"]
     tok_heads = 2 * 32768 * 32
     for pieces in (4, 8):
-        stages, total = bench.algorithmic(w, pieces)
+        plan = (pieces, 512 // pieces, 512 // pieces)
+        stages, executed, method = bench.algorithmic(w, plan)
         # every token passes the forward once: piece 0 in phase 1, the rest in phase 2; q,k,v
         # bf16 (3*128*2) + g,beta bf16 (2*2) in, o fp32 (128*4) out
         fwd = stages["phase1"]["bytes"] + stages["phase2"]["bytes"]
@@ -66,12 +67,22 @@ def test_algorithmic_model_matches_hand_count():
         assert stages["phase2"]["bytes"] >= tok_heads * (pieces - 1) // pieces * (772 + 512)
         # the method's path total does not depend on how the library cuts the sequence:
         # summaries of 3 of the 4 segments (k, v, g, beta), the scan, the forward
-        t_roof = total["bytes"] / 6791.4e9
+        t_roof = method["bytes"] / 6791.4e9
         assert 520e-6 < t_roof < 540e-6
-        assert total["bytes"] >= tok_heads * 3 // 4 * 516 + tok_heads * (772 + 512)
+        assert method["bytes"] >= tok_heads * 3 // 4 * 516 + tok_heads * (772 + 512)
         # the WY stage: k, g, beta in, two 8 KiB tiles per chunk out
         assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 16384
-    assert bench.algorithmic(w, 8)[1] == bench.algorithmic(w, 4)[1]
+        assert executed["bytes"] == sum(stages[k]["bytes"] for k in ("phase1", "scan", "phase2"))
+    assert bench.algorithmic(w, (8, 64, 64))[2] == bench.algorithmic(w, (4, 128, 128))[2]
+    # the unequal plan the library takes on 152 SMs: piece 0 of 154 chunks, two of 179; only
+    # piece 1 is summarised, so the executed bytes are well below the method's (3/4 summarised)
+    stages, executed, method = bench.algorithmic(w, (3, 154, 179))
+    kv = 64 * 128 * 128 * 4
+    hand = (64 * 154 * 64 * 1284 + 2 * kv + 64 * 179 * 64 * 516 + 2 * kv      # phase 1
+            + 2 * kv + kv + kv + 4 * kv                                         # scan
+            + 2 * 64 * 179 * 64 * 1284 + 3 * kv)                                # phase 2
+    assert executed["bytes"] == hand
+    assert 3.12e9 < executed["bytes"] < 3.15e9 < method["bytes"]
     # WY, piece 0's forward, the summaries, the scan, the second forward
     assert bench.launches_per_step(w, 8) == 5
     # CUDA-core shapes have no WY launch; one piece is a single forward
@@ -79,18 +90,33 @@ def test_algorithmic_model_matches_hand_count():
     assert bench.launches_per_step(synth.WORKLOADS["single_seg_h16_t8k"], 1) == 2
 
 
+def test_literal_flow_model_matches_hand_count():
+    # every segment's summary (k, v, g, beta over all tokens; M and S written), the scan
+    # (3 summaries read, h0 read, 4 H_in written), the forward (every token; H_in read,
+    # h_final written)
+    w = synth.WORKLOADS["cp4_b2_h32_t32k"]
+    tok_heads = 2 * 32768 * 32
+    kv = 64 * 128 * 128 * 4
+    calls, total = bench.literal_algorithmic(w)
+    assert calls["summary"]["bytes"] == tok_heads * 516 + 4 * 2 * kv
+    assert calls["scan"]["bytes"] == 3 * 2 * kv + kv + 4 * kv
+    assert calls["forward"]["bytes"] == tok_heads * 1284 + 4 * kv + kv
+    assert total["bytes"] == sum(c["bytes"] for c in calls.values())
+
+
 def test_state_grad_model_matches_hand_count():
     # the backward state-gradient kernel, counted by hand per chunk of 64 tokens and head at
-    # K = V = 128: K K^T and Q K^T 2*(64*64*128*2) = 2.10 M, the inverse 0.17 M,
-    # dR = Kd D + C^T dO 64*128*128*2 + 64*64*128*2 = 3.15 M, A^T dR 64*64*128 = 0.52 M,
-    # the D update 2*(128*64*128*2) = 4.19 M: 10.13 M per chunk, 158 kFLOP per token-head
+    # K = V = 128, every product as a dense tile (the triangular C^T dO and A^T dR alike):
+    # K K^T and Q K^T 2*(64*64*128*2) = 2.10 M, the inverse 0.17 M,
+    # dR = Kd D + C^T dO 64*128*128*2 + 64*64*128*2 = 3.15 M, A^T dR 64*64*128*2 = 1.05 M,
+    # the D update 2*(128*64*128*2) = 4.19 M: 10.66 M per chunk, 167 kFLOP per token-head
     w = synth.WORKLOADS["cp4_b2_h32_t32k"]
     tok_heads = 2 * 32768 * 32
     alg = bench.state_grad_algorithmic(w)
     per_chunk = 2 * 64 * 64 * 128 * 2 + 0.17e6 + 64 * 128 * 128 * 2 + 64 * 64 * 128 * 2 + \
-        64 * 64 * 128 + 2 * 128 * 64 * 128 * 2
+        64 * 64 * 128 * 2 + 2 * 128 * 64 * 128 * 2
     assert abs(alg["flops"] - per_chunk * tok_heads / 64) < 1e3
-    assert 157e3 < alg["flops"] / tok_heads < 160e3
+    assert 166e3 < alg["flops"] / tok_heads < 168e3
     # q, k (2 x 128 bf16), g, beta (bf16) and dO (128 fp32) read once; dS (4 segments x 64
     # heads x 64 KiB) written
     assert alg["bytes"] == tok_heads * (512 + 4 + 512) + 4 * 64 * 128 * 128 * 4

@@ -10,8 +10,8 @@ import torch
 
 import oracle
 from context_scan_gb300 import gdn, synth
-from gpu_util import (TOL_BF16, TOL_F32, head_slice, np64, oracle_ref, rel_err, run_segmented,
-                      run_summary, tol_for, upload)
+from gpu_util import (TOL_BF16, TOL_F32, head_slice, np64, oracle_ref, record, rel_err,
+                      run_segmented, run_summary, tol_for, upload)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,9 @@ def test_segmented_matches_oracle(name):
     d = upload(x, w)
     o, hf, hin = run_segmented(w, d)
     tol = tol_for(w)
-    e_o, e_h, e_in = rel_err(np64(o), o_ref), rel_err(np64(hf), hf_ref), rel_err(np64(hin), hin_ref)
+    e_o = rel_err(np64(o), o_ref, label="o")
+    e_h = rel_err(np64(hf), hf_ref, label="h_final")
+    e_in = rel_err(np64(hin), hin_ref, label="H_in")
     assert e_o <= tol, (name, "o", e_o)
     assert e_h <= tol, (name, "h_final", e_h)
     assert e_in <= tol, (name, "H_in", e_in)
@@ -65,9 +67,12 @@ def test_decayed_read_matches_oracle(name):
     d = upload(x, w)
     o, hf, hin = run_segmented(w, d, decay_first=True)
     tol = tol_for(w)
-    assert rel_err(np64(o), o_ref) <= tol, ("o", rel_err(np64(o), o_ref))
-    assert rel_err(np64(hf), hf_ref) <= tol, ("h_final", rel_err(np64(hf), hf_ref))
-    assert rel_err(np64(hin), hin_ref) <= tol, ("H_in", rel_err(np64(hin), hin_ref))
+    e_o = rel_err(np64(o), o_ref, label="o")
+    e_h = rel_err(np64(hf), hf_ref, label="h_final")
+    e_in = rel_err(np64(hin), hin_ref, label="H_in")
+    assert e_o <= tol, ("o", e_o)
+    assert e_h <= tol, ("h_final", e_h)
+    assert e_in <= tol, ("H_in", e_in)
     # the flag is honoured: the result is much closer to this reading than to the default one
     o_def, _, _ = oracle_ref(x, w.seg_len)
     assert rel_err(np64(o), o_def) > 2 * rel_err(np64(o), o_ref)
@@ -94,9 +99,10 @@ def test_summary_matches_oracle(name):
     # Its error matters through M @ H_in (H_in, S are O(1)), so the scale has a floor of
     # 1e-12: an error below 1e-12 * tol in M is below 1e-10 of the state it feeds.
     m_scale = max(float(np.sqrt(np.mean(M_ref ** 2))), 1e-12)
-    m_err = float(np.max(np.abs(M - M_ref))) / m_scale
+    m_err = record(float(np.max(np.abs(M - M_ref))) / m_scale, "M")
     assert m_err <= tol, ("M", m_err)
-    assert rel_err(S, S_ref) <= tol, ("S", rel_err(S, S_ref))
+    s_err = rel_err(S, S_ref, label="S")
+    assert s_err <= tol, ("S", s_err)
 
 
 @pytest.mark.parametrize("name", ["tiny_f32_k64_cp4", "cp4_small"])
@@ -164,10 +170,21 @@ def test_continuation_through_h_final():
     o1, h1, _ = run_segmented(w, half)
     rest["h0"] = h1
     o2, h2, _ = run_segmented(w, rest)
+    # each half against the oracle: the first half from h0, the second from the oracle's own
+    # state after token 511 (so a GPU error in h1 is not carried into the second check)
+    xa = {n: (v[:, :512] if v is not None and n != "h0" else v) for n, v in x.items()}
+    oa_ref, ha_ref, _ = oracle_ref(xa, 0)
+    xb = {n: (v[:, 512:] if v is not None and n != "h0" else v) for n, v in x.items()}
+    xb["h0"] = ha_ref.astype(np.float32)
+    ob_ref, hb_ref, _ = oracle_ref(xb, 0)
+    assert rel_err(np64(o1), oa_ref, label="o first half") <= TOL_BF16
+    assert rel_err(np64(h1), ha_ref, label="h first half") <= TOL_BF16
+    assert rel_err(np64(o2), ob_ref, label="o second half") <= TOL_BF16
+    assert rel_err(np64(h2), hb_ref, label="h second half") <= TOL_BF16
     # The tensor-core chains keep the state as sigma * H_s with sigma a running product of
     # the chunk decays; a continuation restarts sigma at 1, so its tf32 operands round
-    # differently from the uninterrupted run's. Both stay within the parity tolerance of
-    # the oracle; between themselves they agree to rounding noise (~3e-3 of the RMS in o).
+    # differently from the uninterrupted run's. Between themselves the two runs agree to
+    # rounding noise (~3e-3 of the RMS in o).
     assert rel_err(np64(torch.cat([o1, o2], 1)), np64(o_all)) <= 1e-2
     assert rel_err(np64(h2), np64(hf_all)) <= 1e-3
 
@@ -274,9 +291,9 @@ def test_full_size_sampled_heads(name):
     for b, h in heads:
         xs = head_slice(x, b, h)
         o_ref, hf_ref, hin_ref = oracle_ref(xs, w.seg_len, col_block=16)
-        assert rel_err(np64(o[b:b + 1, :, h:h + 1]), o_ref) <= TOL_BF16, (b, h)
-        assert rel_err(np64(hf[b:b + 1, h:h + 1]), hf_ref) <= TOL_BF16, (b, h)
-        assert rel_err(np64(hin[:, b:b + 1, h:h + 1]), hin_ref) <= TOL_BF16, (b, h)
+        assert rel_err(np64(o[b:b + 1, :, h:h + 1]), o_ref, label=f"o {b},{h}") <= TOL_BF16, (b, h)
+        assert rel_err(np64(hf[b:b + 1, h:h + 1]), hf_ref, label=f"h_final {b},{h}") <= TOL_BF16, (b, h)
+        assert rel_err(np64(hin[:, b:b + 1, h:h + 1]), hin_ref, label=f"H_in {b},{h}") <= TOL_BF16, (b, h)
 
 
 def test_uneven_pieces_h_in_guard_bands_bf16_and_determinism():
@@ -339,3 +356,59 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     o, hf, hin = run_segmented(w, d)
     assert rel_err(np64(o), o_ref) <= tol_for(w)
     assert rel_err(np64(hf), hf_ref) <= tol_for(w)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32_k64_cp4", "cp4_small", "cp16_small", "bf16_k64_cp4",
+                                  "slow_decay_h4_t1k_cp16"])
+def test_literal_cp_flow_matches_oracle(name):
+    # The pages' flow composed from three public calls: every emulated rank's summary
+    # (gdn_segment_summary), the in-order apply (gdn_summary_scan), then every rank's local
+    # forward from its H_in (gdn_segment_fwd) -- RFC section 6.4.1 / 6.5
+    w = SMALL[name]
+    x = synth.make_inputs(w)
+    o_ref, hf_ref, hin_ref = oracle_ref(x, w.seg_len)
+    d = upload(x, w)
+    M, S = run_summary(w, d)
+    B, T, H, K = d["k"].shape
+    hin = torch.empty((w.nseg, B, H, K, w.V), device="cuda")
+    gdn.gdn_summary_scan(M, S, d["h0"], hin)
+    o = torch.empty((B, T, H, w.V), device="cuda")
+    hf = torch.empty((B, H, K, w.V), device="cuda")
+    prob = gdn.problem(d["k"], d["v"], o)
+    ws = gdn.alloc_workspace(prob, 1)
+    gdn.gdn_segment_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], hin, o, hf, w.nseg, ws,
+                        prob=prob)
+    torch.cuda.synchronize()
+    assert gdn.gdn_check_device_error(ws)[0] == 0
+    tol = tol_for(w)
+    assert rel_err(np64(hin), hin_ref, label="H_in") <= tol
+    assert rel_err(np64(o), o_ref, label="o") <= tol
+    assert rel_err(np64(hf), hf_ref, label="h_final") <= tol
+
+
+def test_segment_fwd_edge_cases():
+    # no H_in: every segment starts from zero (each segment equals a fresh gdn_chunk_fwd of
+    # its own tokens); T = 0: h_final is the last segment's H_in
+    w = synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=512, nseg=2, h0_sd=None)
+    x = synth.make_inputs(w)
+    d = upload(x, w)
+    o = torch.empty((1, 512, 2, 128), device="cuda")
+    hf = torch.empty((1, 2, 128, 128), device="cuda")
+    prob = gdn.problem(d["k"], d["v"], o)
+    ws = gdn.alloc_workspace(prob, 1)
+    gdn.gdn_segment_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, o, hf, 2, ws,
+                        prob=prob)
+    torch.cuda.synchronize()
+    xb = {n: (v[:, 256:] if v is not None else v) for n, v in x.items()}
+    ob_ref, hb_ref, _ = oracle_ref(xb, 0)
+    assert rel_err(np64(o[:, 256:]), ob_ref) <= TOL_BF16
+    assert rel_err(np64(hf), hb_ref) <= TOL_BF16
+    e = {n: torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device="cuda") for n in ("q", "k", "v")}
+    e["g"] = torch.empty((1, 0, 2), dtype=torch.bfloat16, device="cuda")
+    e["beta"] = torch.empty((1, 0, 2), dtype=torch.bfloat16, device="cuda")
+    hin = torch.randn((3, 1, 2, 128, 128), device="cuda")
+    p0 = gdn.problem(e["k"], e["v"], o)
+    gdn.gdn_segment_fwd(e["q"], e["k"], e["v"], e["g"], e["beta"], hin, o, hf, 3,
+                        gdn.alloc_workspace(p0, 1), prob=p0)
+    torch.cuda.synchronize()
+    assert torch.equal(hf, hin[2])

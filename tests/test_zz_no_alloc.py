@@ -2,9 +2,9 @@
 memory (a framework that owns all device memory through its own pool, a request path that
 must not pay an allocation's implicit synchronisation, a program holding only imported
 buffers). It takes its scratch from a fixed array inside the library instead of a caller
-workspace. Here it is called through the C ABI and compared with gdn_segmented_fwd, twice
-in a row (the array keeps the previous call's contents, so the second call must not be
-disturbed by the first).
+workspace. Here it is called through the C ABI and compared with gdn_segmented_fwd and with the
+fp64 oracle, twice in a row (the array keeps the previous call's contents, so the second call
+must not be disturbed by the first).
 
 This file is named so that pytest collects it last; it passes alone in a fresh process too.
 """
@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from context_scan_gb300 import gdn, synth
-from gpu_util import TOL_BF16, TOL_F32, np64, rel_err, upload
+from gpu_util import TOL_BF16, TOL_F32, np64, oracle_ref, rel_err, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,9 @@ def _alloc_out(d, w):
 @pytest.mark.parametrize("name", list(CASES))
 def test_noalloc_matches_workspace_entry_point_twice(name):
     w, tol = CASES[name]
-    d = upload(synth.make_inputs(w), w)
+    x = synth.make_inputs(w)
+    o_or, hf_or, _ = oracle_ref(x, w.seg_len)
+    d = upload(x, w)
     o_ref, hf_ref = _alloc_out(d, w)
     prob = gdn.problem(d["k"], d["v"], o_ref)
     ws = gdn.alloc_workspace(prob, w.nseg)
@@ -55,6 +57,8 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
         assert err_word.tolist() == [0, 0], (call, err_word.tolist())
         assert rel_err(np64(o), np64(o_ref)) <= tol, call
         assert rel_err(np64(hf), np64(hf_ref)) <= tol, call
+        assert rel_err(np64(o), o_or, label="o vs oracle") <= tol, call
+        assert rel_err(np64(hf), hf_or, label="h_final vs oracle") <= tol, call
 
 
 def test_noalloc_rejects_problems_beyond_the_array():
