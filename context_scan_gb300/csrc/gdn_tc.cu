@@ -67,6 +67,13 @@ constexpr int kD = 128;         // K == V
 constexpr int kC = 64;          // tokens per chunk
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRenorm = -64.f;   // log2 of the smallest sigma kept without folding
+// An fp32 value in tensor memory read as a tf32 MMA operand (H_s in S12, R^T in S3) loses its
+// low 13 bits: it is truncated toward zero by 2^-11 / m of its magnitude on average (m in
+// [1, 2) its mantissa), i.e. by 2^-11 / (2 ln 2) for mantissas spread log-uniformly. The B
+// operand of each of those products is scaled by the inverse, so that the products carry no
+// systematic bias; what remains is a zero-mean rounding error of at most 2^-11 of the operand.
+// (S4 reads the scaled R^T as a bf16 hi + lo pair, which is accurate to 2^-16.)
+constexpr float kTruncComp = 1.0f + 3.5222e-4f;
 
 // Warps and tensor memory (32-bit cells, 128 lanes); one CTA per SM. The forward has one
 // state warp group and two prep warp groups; a summary CTA carries both blocks of the
@@ -579,7 +586,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj) {
                                 const int j = 32 * grp + 16 * hh + jj;
-                                t[jj] = tf32_operand((j <= i) ? ex2(gi - gam[j]) * sv[jj] : 0.f);
+                                // (S3 reads R^T truncated: C carries kTruncComp)
+                                t[jj] = tf32_operand((j <= i) ? ex2(gi - gam[j]) * (sv[jj] * kTruncComp) : 0.f);
                             }
                             // columns 32 grp + 16 hh ..: tf32 block grp, 16-byte chunks 4 hh ..
 #pragma unroll
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
                                   TAG_QFULL, lane)) {
                         const int qt = (grp * 2 + (lq - 2)) * 32 + lane;
                         const int i = qt >> 1, kh = qt & 1;
-                        const float egi = sc[SC_EG * 64 + i];
+                        const float egi = sc[SC_EG * 64 + i] * kTruncComp;   // S12 reads H_s truncated
                         const uint8_t* src = sm + L::Q0 + qs * 16384 + kh * 8192;
 #pragma unroll 2
                         for (int cc = 0; cc < 8; ++cc) {
@@ -636,7 +644,7 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
             //      (the forward's Qd warps waited for that before the barrier above)
             {
                 if (SUMMARY && !pwait(bar0 + B_WFREE, (n - 1) & 1, TAG_WFREE, n >= 1)) break;
-                const float nsig = -sc[SC_MISC * 64 + 2];
+                const float nsig = -sc[SC_MISC * 64 + 2] * kTruncComp;   // S12 reads H_s truncated
                 // lane k of W^T's rows i: writes element (row i, feature k)
                 const int k = 32 * lq + lane;
                 uint8_t* col = sm + L::W + lq * L::WQ_KB + (k & 3) * 4;

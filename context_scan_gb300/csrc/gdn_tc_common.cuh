@@ -70,10 +70,13 @@ __device__ __forceinline__ void record_error(DeviceError* e, unsigned code, unsi
 
 // Bounded wait for the completion of the phase with the given parity. Gives up when the
 // CTA's abort flag is raised or after `limit` SM cycles (then records the timeout and
-// raises the flag). Returns false if it gave up.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       long long limit, DeviceError* err, unsigned tag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// raises the flag). Returns false if it gave up. The common case -- the phase has completed
+// -- is inlined at every call site; only the polling loop is a call. (With most of the SM's
+// shared memory in use, L1 is small and a call's stack traffic can go out to L2: in a kernel
+// whose warps hand work to each other every few hundred cycles, that was the largest cost
+// of a wait.)
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            long long limit, DeviceError* err, unsigned tag) {
     const long long t0 = clock64();
     for (;;) {
         // suspended in hardware (up to 20 us per try) rather than re-polling: a polling warp
@@ -86,6 +89,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit, DeviceError* err, unsigned tag) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, limit, err, tag);
 }
 
 // Bounded wait used only while shutting down after an abort: lets copies or MMAs this CTA

@@ -183,8 +183,9 @@ def test_continuation_through_h_final():
     assert rel_err(np64(h2), hb_ref, label="h second half") <= TOL_BF16
     # The tensor-core chains keep the state as sigma * H_s with sigma a running product of
     # the chunk decays; a continuation restarts sigma at 1, so its tf32 operands round
-    # differently from the uninterrupted run's. Between themselves the two runs agree to
-    # rounding noise (~3e-3 of the RMS in o).
+    # differently from the uninterrupted run's. Each run is within the parity bar of the
+    # oracle (checked above); between themselves they agree to rounding noise (~2e-3 of the
+    # RMS in o, ~2e-4 in the state).
     assert rel_err(np64(torch.cat([o1, o2], 1)), np64(o_all)) <= 1e-2
     assert rel_err(np64(h2), np64(hf_all)) <= 1e-3
 
