@@ -69,7 +69,7 @@ int sm_count() {
 //    forward and the summaries end together: max(L0, kSumRatio x) + x + 3 * (P - 2). The
 //    forward kernels then write the states entering the segments as they pass them.
 // Without a device to size the waves it stays at nseg equal pieces.
-constexpr double kSumRatio = 0.87;
+constexpr double kSumRatio = 1.0;
 
 PiecePlan plan_pieces(const gdn_problem& p, int nseg) {
     const int chunks = p.T / gdn::kChunk;   // a multiple of nseg (checked)
@@ -217,7 +217,10 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
                          void* const* events) {
     const WsLayout w = layout(*p, nseg);
     const int P = w.pieces, nsub = P / nseg;
-    const bool equal = w.plan.first == w.plan.rest;   // else the forwards write H_in_out
+    // equal pieces whose starts include every segment start: the scan writes H_in_out;
+    // otherwise (pieces of unequal length, or an unequal plan whose pieces came out equal but
+    // do not divide the segments) the forwards write it as they pass the segment starts
+    const bool equal = w.plan.first == w.plan.rest && P % nseg == 0;
     const int BH = p->B * p->H;
     char* wsb = reinterpret_cast<char*>(workspace);
     if (mark(events, 0, s) != cudaSuccess || mark(events, 1, s) != cudaSuccess ||

@@ -27,9 +27,10 @@ SMALL = {
     "slow_decay_h4_t1k_cp16": W["slow_decay_h4_t1k_cp16"],
     "bf16_k64_cp4": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=3, T=512, K=64, V=64),
     "one_chunk_segments": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=512, nseg=8),
-    # few chains on many SMs: unequal pieces whose starts are not segment starts, so the
-    # forwards write the states entering the segments as they pass them
-    "uneven_pieces_cp4": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=4096),
+    # few chains on many SMs: pieces whose starts are not segment starts (P = 6 pieces of 8
+    # chunks for 4 segments of 12 on 152 SMs), so the forwards write the states entering the
+    # segments as they pass them
+    "uneven_pieces_cp4": synth.scaled(W["cp4_b2_h32_t32k"], B=1, H=2, T=3072),
 }
 
 
@@ -302,7 +303,17 @@ def test_uneven_pieces_h_in_guard_bands_bf16_and_determinism():
     # segment starts, and the forward chains write H_in as they pass the segment starts. Each
     # segment's slot is written exactly once (NaN guard bands around H_in stay NaN), repeated
     # calls agree bit for bit, and bf16 output keeps its bar.
-    w = SMALL["uneven_pieces_cp4"]
+    # the first length whose plan has a first piece of its own length, P not a multiple of
+    # nseg (the plan depends on the device's SM count, so it is asked for, not assumed)
+    w = None
+    for T in (2816, 3328, 3840, 4352, 4096):
+        cand = synth.scaled(SMALL["uneven_pieces_cp4"], T=T)
+        pc = gdn.Problem(cand.B, T, cand.H, 128, 128, 64, gdn.GDN_DTYPE_BF16, gdn.GDN_DTYPE_F32)
+        P, first, rest = gdn.segmented_plan(pc, cand.nseg)
+        if first != rest and P % cand.nseg != 0:
+            w = cand
+            break
+    assert w is not None, "no length here gets an unequal piece plan"
     x = synth.make_inputs(w)
     o_ref, hf_ref, hin_ref = oracle_ref(x, w.seg_len)
     d = upload(x, w)
