@@ -1027,6 +1027,51 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def record_traffic(csv_path: str, kernel: str, workload: str, command: str, grid=None,
+                   scale_note: str = "", scale=None) -> str:
+    """Write profiles/traffic_<kernel>_<workload>.txt from an ncu CSV of one capture of the
+    kernel (metrics dram__bytes_read.sum and dram__bytes_write.sum; with several launches in
+    the CSV, the one whose grid is `grid`). The record carries the hash of the sources the
+    kernel is built from now, so bench.py trusts it exactly until one of them changes.
+    scale = (factor, fixed_bytes): per-launch bytes = (captured - fixed) * factor + fixed, for
+    a capture of a smaller case of the same kernel."""
+    units = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    launches = {}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rd = csv.DictReader(io.StringIO("".join(lines)))
+    for r in rd:
+        name = r.get("Metric Name", "")
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        key = (r.get("ID"), r.get("Kernel Name", ""), r.get("Grid Size", ""))
+        v = float(r["Metric Value"].replace(",", "")) * units.get(r.get("Metric Unit", "byte"), 1.0)
+        launches.setdefault(key, {})[name] = v
+    picked = [(k, v) for k, v in launches.items() if grid is None or k[2] == grid]
+    if len(picked) != 1:
+        raise SystemExit(f"expected one launch{' with grid ' + grid if grid else ''} in "
+                         f"{csv_path}, found {len(picked)}")
+    (lid, kname, kgrid), v = picked[0]
+    captured = v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"]
+    per_launch = captured
+    if scale is not None:
+        factor, fixed = scale
+        per_launch = (captured - fixed) * factor + fixed
+    out = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    with open(out, "w") as f:
+        f.write(f"kernel: {kname.split('(')[0].strip()} grid {kgrid} on {workload}\n")
+        f.write(f"kernel_source_hash: {kernel_source_hash(kernel)}\n")
+        f.write(f"dram_bytes_per_launch: {per_launch:.0f}\n")
+        f.write(f"captured: dram__bytes_read.sum {v['dram__bytes_read.sum']:.0f} + "
+                f"dram__bytes_write.sum {v['dram__bytes_write.sum']:.0f} = {captured:.0f}\n")
+        if scale is not None:
+            f.write(f"scaled: (captured - {scale[1]:.0f}) x {scale[0]:.4f} + {scale[1]:.0f}"
+                    f"{'; ' + scale_note if scale_note else ''}\n")
+        f.write(f"command: {command}\n")
+        f.write(f"hash covers: {', '.join(KERNEL_SOURCES[kernel])}, include/gdn.h\n")
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1049,7 +1094,17 @@ def main(argv=None):
     ap.add_argument("--T", type=int, default=None,
                     help="run the workload at this sequence length instead (a smaller case of "
                          "the same kernels for profiler captures; not a bench line)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV", default=None,
+                    help="write profiles/traffic_<--traffic-kernel>_<--workload>.txt from an ncu "
+                         "CSV of dram__bytes_read.sum and dram__bytes_write.sum (no GPU needed)")
+    ap.add_argument("--traffic-kernel", default="gdn_forward", choices=sorted(KERNEL_SOURCES))
+    ap.add_argument("--traffic-grid", default=None, help='the captured launch\'s grid, e.g. "(128, 1, 1)"')
+    ap.add_argument("--traffic-command", default="", help="the command line the CSV came from")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        print(record_traffic(args.record_traffic, args.traffic_kernel, args.workload,
+                             args.traffic_command, grid=args.traffic_grid))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
