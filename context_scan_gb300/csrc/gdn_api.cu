@@ -347,6 +347,40 @@ gdn_status check_varlen(const gdn_problem* p, int nseq) {
     return GDN_OK;
 }
 
+// ---- backward: [the forward's / summary's workspace (header first) | o scratch | Hc | Dc | M |
+//      S | dS | dH_in (nseg + 1 slots)], each region 256-byte aligned. Hc and Dc hold the state
+//      entering and the state gradient leaving every chunk ([T/64][B][H][K][V] fp32).
+struct BwdLayout {
+    size_t off_o, off_hc, off_dc, off_m, off_s, off_ds, off_dh, total;
+};
+
+BwdLayout bwd_layout(const gdn_problem& p, int nseg) {
+    BwdLayout w{};
+    const int nch = p.T / gdn::kChunk;
+    const size_t head = std::max(layout(p, nch > 0 ? nch : 1).total, layout(p, 1).total);
+    const size_t bh = (size_t)p.B * p.H, kv = (size_t)p.K * p.V, kk = (size_t)p.K * p.K;
+    const size_t osz = p.out_dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    w.off_o = round_up(head);
+    w.off_hc = w.off_o + round_up((size_t)p.B * p.T * p.H * p.V * osz);
+    w.off_dc = w.off_hc + round_up(sizeof(float) * nch * bh * kv);
+    w.off_m = w.off_dc + round_up(sizeof(float) * nch * bh * kv);
+    w.off_s = w.off_m + round_up(sizeof(float) * nseg * bh * kk);
+    w.off_ds = w.off_s + round_up(sizeof(float) * nseg * bh * kv);
+    w.off_dh = w.off_ds + round_up(sizeof(float) * nseg * bh * kv);
+    w.total = w.off_dh + round_up(sizeof(float) * (nseg + 1) * bh * kv);
+    return w;
+}
+
+gdn_status check_bwd(const gdn_problem* p, int nseg) {
+    gdn_status st = check_problem(p, nseg);
+    if (st != GDN_OK) return st;
+    if (p->gate_k) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)p->B * p->H * nseg * (p->V / 32) >= (1LL << 31) ||
+        (long long)p->B * p->H * (p->T / gdn::kChunk) >= (1LL << 31))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -603,6 +637,122 @@ gdn_status gdn_state_grad_scan(const gdn_problem* p, int nseg, const float* M, c
     if (st != GDN_OK) return st;
     return from_cuda(gdn::launch_state_grad_scan(M, dS, dht, dH_in, nseg, p->B * p->H, p->K, p->V,
                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gdn_chunk_bwd_workspace_bytes(const gdn_problem* p, int nseg) {
+    if (check_bwd(p, nseg) != GDN_OK) return 0;
+    return bwd_layout(*p, nseg).total;
+}
+
+gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const void* k,
+                         const void* v, const void* g, const void* beta, const float* h0,
+                         const void* dO, const float* dht, float* dq, float* dk, float* dv,
+                         float* dg, float* dbeta, float* dh0, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    gdn_status st = check_bwd(p, nseg);
+    if (st != GDN_OK) return st;
+    if (p->T > 0 && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
+        return GDN_ERR_INVALID_ARG;
+    const BwdLayout w = bwd_layout(*p, nseg);
+    if (!workspace || workspace_bytes < w.total) return GDN_ERR_WORKSPACE;
+    for (const void* ptr : {(const void*)workspace, q, k, v, g, beta, (const void*)h0, dO, (const void*)dht,
+                            (const void*)dq, (const void*)dk, (const void*)dv, (const void*)dg,
+                            (const void*)dbeta, (const void*)dh0})
+        if (misaligned(ptr)) return GDN_ERR_MISALIGNED;
+    if ((st = check_device()) != GDN_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int BH = p->B * p->H;
+    const long long kv = (long long)BH * p->K * p->V;
+    if (p->T == 0) {   // dh0 = dht (or zeros)
+        if (dh0 && gdn::launch_scan(nullptr, nullptr, dht, nullptr, dh0, nullptr, 0, 1, 1, BH,
+                                    p->K, p->V, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        return GDN_OK;
+    }
+    char* wsb = reinterpret_cast<char*>(workspace);
+    float* Hc = reinterpret_cast<float*>(wsb + w.off_hc);
+    float* Dc = reinterpret_cast<float*>(wsb + w.off_dc);
+    float* M = reinterpret_cast<float*>(wsb + w.off_m);
+    float* S = reinterpret_cast<float*>(wsb + w.off_s);
+    float* dS = reinterpret_cast<float*>(wsb + w.off_ds);
+    float* dH = reinterpret_cast<float*>(wsb + w.off_dh);   // [nseg + 1]: entering s; dht last
+    const int nch = p->T / gdn::kChunk;
+    // 1. the state entering every chunk: the forward with one segment per chunk (its output is
+    //    recomputed into scratch and not used)
+    st = run_segmented(p, nch, q, k, v, g, beta, h0, wsb + w.off_o, nullptr, Hc, workspace, s,
+                       nullptr);
+    if (st != GDN_OK) return st;
+    // 2. the segments' summaries M (their linear parts carry the state gradient backwards)
+    {
+        ChainParams c = base_params(p, workspace);
+        c.k = k;
+        c.v = v;
+        c.g = g;
+        c.beta = beta;
+        c.M = M;
+        c.S = S;
+        c.seg_len = p->T / nseg;
+        c.nseg_run = nseg;
+        c.nseg_total = nseg;
+        if (prepare(c, p, workspace, s) != cudaSuccess || run_summary(c, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
+    // 3. per-segment state gradients from the segments' own outputs (RFC 6.4.3 dS_local), and
+    //    the reverse scan to the gradient entering every segment; dH[nseg] = dht
+    gdn::StateGradParams sg{};
+    sg.q = q;
+    sg.k = k;
+    sg.g = g;
+    sg.beta = beta;
+    sg.dO = dO;
+    sg.B = p->B;
+    sg.T = p->T;
+    sg.H = p->H;
+    sg.K = p->K;
+    sg.V = p->V;
+    sg.seg_len = p->T / nseg;
+    sg.nseg = nseg;
+    sg.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
+    sg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
+    sg.decay_first = p->decay_first;
+    sg.dS = dS;
+    if (gdn::launch_state_grad(sg, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_scan(nullptr, nullptr, dht, nullptr, dH + nseg * kv, nullptr, 0, 1, 1, BH,
+                         p->K, p->V, s) != cudaSuccess ||
+        gdn::launch_state_grad_scan(M, dS, dht, dH, nseg, BH, p->K, p->V, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (dh0 && cudaMemcpyAsync(dh0, dH, sizeof(float) * kv, cudaMemcpyDeviceToDevice, s) !=
+                   cudaSuccess)
+        return GDN_ERR_CUDA;
+    // 4. each segment's chunks again from the gradient leaving it, recording the gradient on the
+    //    state leaving every chunk (RFC 6.4.3 backward_state)
+    sg.dH_end = dH + kv;
+    sg.D_chunks = Dc;
+    if (gdn::launch_state_grad(sg, s) != cudaSuccess) return GDN_ERR_CUDA;
+    // 5. every chunk's gradients (RFC 6.4.3 backward_finish)
+    gdn::ChunkGradParams cg{};
+    cg.q = q;
+    cg.k = k;
+    cg.v = v;
+    cg.g = g;
+    cg.beta = beta;
+    cg.dO = dO;
+    cg.Hc = Hc;
+    cg.Dc = Dc;
+    cg.dq = dq;
+    cg.dk = dk;
+    cg.dv = dv;
+    cg.dg = dg;
+    cg.dbeta = dbeta;
+    cg.B = p->B;
+    cg.T = p->T;
+    cg.H = p->H;
+    cg.K = p->K;
+    cg.V = p->V;
+    cg.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
+    cg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
+    cg.decay_first = p->decay_first;
+    return from_cuda(gdn::launch_chunk_grad(cg, s));
 }
 
 const char* gdn_status_string(gdn_status s) {

@@ -150,6 +150,15 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
         }
         __syncthreads();
         if (ch > 0) prefetch(ch - 1);
+        // the gradient on the state leaving this chunk (D' before the chunk's own update)
+        if (p.D_chunks) {
+            const long long cg = (long long)seg * (p.seg_len / kChunk) + ch;   // chunk index
+            float* dst = p.D_chunks + (cg * p.B * H + bh) * KD * V + c0;
+            for (int e = tid; e < KD * CT; e += kThreads) {
+                const int l = e / CT, c = e % CT;
+                dst[(long long)l * V + c] = Ds[e];
+            }
+        }
         // ---- (2) inclusive / read-side cumulative gates (one warp, two tokens per lane)
         if (tid < 32) {
             const float a0 = gx[2 * tid], a1 = gx[2 * tid + 1];

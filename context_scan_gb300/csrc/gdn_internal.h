@@ -103,11 +103,37 @@ struct StateGradParams {
     const void* dO;
     const float* dH_end;
     float* dS;
+    // when non-null, the gradient on the state leaving every chunk c (counted over the whole
+    // sequence) is written to D_chunks + c*B*H*K*V + (b*H + h)*K*V ([T/64][B][H][K][V])
+    float* D_chunks;
     int B, T, H, K, V;
     int seg_len, nseg;
     int in_bf16, do_bf16, decay_first;
 };
 cudaError_t launch_state_grad(const StateGradParams& p, cudaStream_t s);
+
+// Per-chunk gradients of the backward: every (b, h, chunk c) independently, from the chunk's
+// q, k, v, g, beta, dO, the state entering it (Hc[c]) and the gradient on the state leaving it
+// (Dc[c]), both [T/64][B][H][K][V] fp32: dq, dk [B,T,H,K], dv [B,T,H,V], dg, dbeta [B,T,H],
+// all fp32.
+struct ChunkGradParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    const void* dO;
+    const float* Hc;
+    const float* Dc;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dg;
+    float* dbeta;
+    int B, T, H, K, V;
+    int in_bf16, do_bf16, decay_first;
+};
+cudaError_t launch_chunk_grad(const ChunkGradParams& p, cudaStream_t s);
 // dH_in[s] = M[s]^T dH_in[s+1] + dS[s] for s = nseg-1 .. 0, dH_in[nseg] = dht (or zero)
 cudaError_t launch_state_grad_scan(const float* M, const float* dS, const float* dht,
                                    float* dH_in, int nseg, int BH, int K, int V, cudaStream_t s);

@@ -22,8 +22,8 @@ EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_segmented_plan",
             "gdn_segment_summary", "gdn_summary_scan", "gdn_segment_fwd", "gdn_segmented_fwd",
             "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
-            "gdn_state_grad_summary", "gdn_state_grad_scan",
-            "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
+            "gdn_state_grad_summary", "gdn_state_grad_scan", "gdn_chunk_bwd_workspace_bytes",
+            "gdn_chunk_bwd", "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
 
 
 class GdnError(RuntimeError):
@@ -74,6 +74,9 @@ def lib():
                                            [ctypes.c_size_t, _P, _P])
         L.gdn_state_grad_summary.argtypes = [pp, ctypes.c_int] + [_P] * 8
         L.gdn_state_grad_scan.argtypes = [pp, ctypes.c_int] + [_P] * 5
+        L.gdn_chunk_bwd_workspace_bytes.argtypes = [pp, ctypes.c_int]
+        L.gdn_chunk_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_chunk_bwd.argtypes = [pp, ctypes.c_int] + [_P] * 15 + [ctypes.c_size_t, _P]
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
@@ -81,7 +84,8 @@ def lib():
         for fn in ("gdn_chunk_fwd", "gdn_segment_summary", "gdn_summary_scan", "gdn_segment_fwd",
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
                    "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error",
-                   "gdn_selftest_wait_timeout", "gdn_state_grad_summary", "gdn_state_grad_scan"):
+                   "gdn_selftest_wait_timeout", "gdn_state_grad_summary", "gdn_state_grad_scan",
+                   "gdn_chunk_bwd"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -279,6 +283,32 @@ def gdn_state_grad_scan(M, dS, dht, dH_in, stream=None, prob=None):
     prob = prob or Problem(B, 0, H, K, V, 64, GDN_DTYPE_F32, GDN_DTYPE_F32)
     _check(lib().gdn_state_grad_scan(ctypes.byref(prob), nseg, _ptr(M), _ptr(dS), _ptr(dht),
                                      _ptr(dH_in), _stream(stream)), "gdn_state_grad_scan")
+
+
+def chunk_bwd_workspace_bytes(prob: Problem, nseg: int = 1) -> int:
+    return int(lib().gdn_chunk_bwd_workspace_bytes(ctypes.byref(prob), nseg))
+
+
+def alloc_bwd_workspace(prob: Problem, nseg: int = 1, device="cuda"):
+    """A zeroed workspace tensor for gdn_chunk_bwd (torch owns the memory)."""
+    import torch
+    n = chunk_bwd_workspace_bytes(prob, nseg)
+    if n == 0:
+        raise GdnError(2, "gdn_chunk_bwd_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, h0, dO, dht, dq, dk, dv, dg, dbeta, dh0, nseg, workspace,
+                  stream=None, prob=None):
+    """The backward: fp32 gradients dq, dk [B,T,H,K], dv [B,T,H,V], dg, dbeta [B,T,H] and dh0
+    [B,H,K,V] (None skips it) of sum(dO . o) + <dht, h_final>; dO has the output dtype, dht
+    (fp32, or None) the state's shape."""
+    prob = prob or problem(k, v, dO, g=g)
+    _check(lib().gdn_chunk_bwd(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(beta), _ptr(h0), _ptr(dO), _ptr(dht), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(workspace),
+                               workspace.numel() if workspace is not None else 0,
+                               _stream(stream)), "gdn_chunk_bwd")
 
 
 def gdn_selftest_wait_timeout(workspace, limit_cycles, stream=None):

@@ -279,6 +279,30 @@ GDN_API gdn_status gdn_state_grad_scan(const gdn_problem* p, int nseg, const flo
                                        const float* dS, const float* dht, float* dH_in,
                                        void* stream);
 
+/* The whole backward (RFC 6.4.3, the reverse flow through "backward_state" and
+ * "backward_finish"): the gradients of L = sum_t dO_t . o_t + <dht, h_final> with respect to
+ * every input, for the problem gdn_segmented_fwd computes.
+ *   Steps: the forward once more with one segment per chunk, which yields the state entering
+ *   every chunk; the segments' summaries M; the per-segment state gradients dS_local and the
+ *   reverse scan dH_in = M^T dH_out + dS_local (nseg segments, the emulated ranks); each
+ *   segment's chunks again from the gradient leaving it, which yields the gradient on the state
+ *   leaving every chunk; then every chunk's gradients at once, independently, from its inputs,
+ *   the state entering it and the gradient leaving it. The results do not depend on nseg.
+ *   Inputs as gdn_segmented_fwd (q, k, v, g, beta in in_dtype, h0 fp32 or NULL); dO
+ *   [B,T,H,V] in out_dtype; dht [B,H,K,V] fp32 or NULL (zero).
+ *   Outputs, fp32, written: dq, dk [B,T,H,K]; dv [B,T,H,V]; dg, dbeta [B,T,H]; dh0 [B,H,K,V]
+ *   (NULL skips it).
+ *   Per-chunk gradients are fp32 CUDA-core arithmetic; the forward's recomputation follows
+ *   gdn_segmented_fwd's paths. Per-channel gates (gate_k) are not supported
+ *   (GDN_ERR_UNSUPPORTED_SHAPE). Workspace: gdn_chunk_bwd_workspace_bytes(p, nseg), whose first
+ *   256 bytes must be zero before the first call (the device error word). */
+GDN_API size_t gdn_chunk_bwd_workspace_bytes(const gdn_problem* p, int nseg);
+GDN_API gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const void* k,
+                                 const void* v, const void* g, const void* beta, const float* h0,
+                                 const void* dO, const float* dht, float* dq, float* dk,
+                                 float* dv, float* dg, float* dbeta, float* dh0, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * Packed variable-length sequences
  * ---------------------------------------------------------------------------------------
