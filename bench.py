@@ -35,6 +35,8 @@ VARLEN_METRIC = "GDN packed-sequence fwd tokens/s (lengths 1800,1500,2000,1200,8
 KDA_METRIC = "GDN per-channel-gate (KDA) fwd tokens/s at H16 K=V=128 T=8K bf16"
 STATE_GRAD_METRIC = ("GDN backward state-gradient path tokens/s (segment summaries M, dS_local, "
                      "reverse M^T scan) at H32 K=V=128 T=32K bf16")
+BACKWARD_METRIC = ("GDN backward tokens/s (dq, dk, dv, dg, dbeta, dh0 from dO and dht) at H32 "
+                   "K=V=128 T=32K bf16")
 # fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz maximum SM clock
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
@@ -225,6 +227,7 @@ KERNEL_SOURCES = {
     "gdn_varlen_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
     "gdn_wy": ("gdn_wy.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
     "state_grad_kernel": ("gdn_bwd.cu", "gdn_internal.h"),
+    "chunk_grad_kernel": ("gdn_bwd_chunk.cu", "gdn_internal.h"),
 }
 
 
@@ -670,6 +673,202 @@ def run_state_grad(args):
         dist.destroy_process_group()
 
 
+def chunk_grad_algorithmic(w, out_bytes: int = 4):
+    """Per launch of the per-chunk gradient kernel over workload w. Bytes: read q, k, v, g, beta
+    (input dtype), dO (output dtype), the state entering and the gradient leaving every chunk
+    (fp32 K x V each); write dq, dk, dv, dg, dbeta (fp32). Flops per chunk and head, every
+    product counted once as a dense tile (triangular ones too, c = 64): K K^T and Q K^T
+    (2 c c K 2), the inverse (~0.17 M), W (c c K 2), R = A diag(beta) V - W H (c c V 2 + c K V 2),
+    dR = Kd D' + C^T dO (c K V 2 + c c V 2), dQd, dKd, dW (3 c V K 2), dC and dR V^T
+    (2 c c V 2), A^T dR (c c V 2), A^T dW and dW Kr^T (2 c c K 2), A^T dA and its product with
+    A^T (2 c c c 2), dq and dk from the score gradients (3 c c K 2)."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    c, K, V = 64, w.K, w.V
+    th = w.B * w.T * w.H
+    per_tok = (2 * K + V + 2) * isz + V * out_bytes + (2 * K + V + 2) * 4
+    nbytes = th * per_tok + (th // c) * 2 * K * V * 4
+    per_chunk = (2 * c * c * K * 2 + 0.17e6 + c * c * K * 2 + c * c * V * 2 + c * K * V * 2 +
+                 c * K * V * 2 + c * c * V * 2 + 3 * c * V * K * 2 + 2 * c * c * V * 2 +
+                 c * c * V * 2 + 2 * c * c * K * 2 + 2 * c * c * c * 2 + 3 * c * c * K * 2)
+    return {"bytes": nbytes, "flops": per_chunk * th / c}
+
+
+def backward_compulsory_bytes(w, out_bytes: int = 4):
+    """The backward's inputs read once (q, k, v, g, beta, dO, h0, dht) and its gradients
+    written once (dq, dk, dv, dg, dbeta fp32, dh0)."""
+    isz = 2 if w.in_dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    states = w.B * w.H * w.K * w.V * 4
+    return th * ((2 * w.K + w.V + 2) * isz + w.V * out_bytes + (2 * w.K + w.V + 2) * 4) + 3 * states
+
+
+def run_backward(args):
+    """The whole backward through gdn_chunk_bwd on one workload: one step is one call, its six
+    steps bracketed by events on the stream (forward recomputation, summaries M, per-segment
+    state gradients and their reverse scan, the second state-gradient pass, the per-chunk
+    gradients)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from context_scan_gb300 import gdn, synth
+
+    world, rank = init_dist("nccl" if args.gpus > 1 else "gloo")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    w0 = synth.WORKLOADS[args.workload]
+    if w0.gate_k or w0.seq_lens is not None:
+        raise SystemExit("--path backward runs fixed-length scalar-gate workloads only")
+    w = synth.scaled(w0, seed=w0.seed + rank_seed_offset(rank),
+                     **({} if args.T is None else {"T": args.T}))
+    x = synth.make_inputs(w)
+    gr = synth.make_grads(w, dht_sd=0.1)
+    dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
+    host = {n: torch.from_numpy(x[n]).to(dt).pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    host["h0"] = None if x["h0"] is None else torch.from_numpy(x["h0"]).pin_memory()
+    host["dO"] = torch.from_numpy(gr["dO"]).pin_memory()
+    host["dht"] = torch.from_numpy(gr["dht"]).pin_memory()
+    d = {n: (None if t is None else t.to(dev)) for n, t in host.items()}
+    B, T, H, K, V, nseg = w.B, w.T, w.H, w.K, w.V, w.nseg
+    outs = (torch.empty((B, T, H, K), device=dev), torch.empty((B, T, H, K), device=dev),
+            torch.empty((B, T, H, V), device=dev), torch.empty((B, T, H), device=dev),
+            torch.empty((B, T, H), device=dev), torch.empty((B, H, K, V), device=dev))
+    prob = gdn.problem(d["k"], d["v"], d["dO"], g=d["g"])
+    ws = gdn.alloc_bwd_workspace(prob, nseg, device=dev)
+    stream = torch.cuda.current_stream()
+    stage_names = ("forward", "summary_M", "state_grad_scan", "state_grad", "chunk_grad")
+
+    def call(di, oi, events=None):
+        args_ = (di["q"], di["k"], di["v"], di["g"], di["beta"], di["h0"], di["dO"], di["dht"],
+                 *oi, nseg, ws)
+        if events is None:
+            gdn.gdn_chunk_bwd(*args_, prob=prob, stream=stream)
+        else:
+            gdn.gdn_chunk_bwd_timed(*args_, events, prob=prob, stream=stream)
+
+    for _ in range(args.warmup):
+        call(d, outs)
+    torch.cuda.synchronize()
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
+    Ks = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Ks)]
+    for e6 in ev:
+        for e in e6:
+            e.record(stream)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dev)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(Ks):
+        call(d, outs, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    st, detail = gdn.gdn_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
+    total_s = t0.elapsed_time(t1) / 1e3
+    max_s = reduce_max(total_s, device=dev if world > 1 else "cpu")
+    barrier(dev)
+    avg = {name: sum(e[a].elapsed_time(e[a + 1]) for e in ev) / Ks
+           for a, name in enumerate(stage_names)}
+    alg = chunk_grad_algorithmic(w)
+    ach = alg["flops"] / (avg["chunk_grad"] * 1e-3) / 1e12
+    peaks, peaks_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ms_per_step = max_s / Ks * 1e3
+    tokens = B * T
+    value = aggregate(tokens, Ks, world, max_s)
+    comp = backward_compulsory_bytes(w)
+    t_comp = comp / (hbm * 1e9)
+
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = max(3, min(Ks, args.e2e_steps))
+        h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+        barrier(dev)
+        e_el = pipelined_e2e(torch, host, d, outs, call, n_e2e, dev, stream)
+        e_el = reduce_max(e_el, device=dev if world > 1 else "cpu")
+        st, detail = gdn.gdn_check_device_error(ws)
+        if st != 0:
+            raise RuntimeError(f"device error word {st} detail {detail} in the end-to-end run")
+        e2e = {"value": round(aggregate(tokens, n_e2e, world, e_el), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "pipelined": "two buffer sets; copies in and out on their own streams"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+        done, secs = 0, 0.0
+        nthreads = oracle.num_threads(0)
+        while done < len(heads) and secs < args.cpu_seconds:
+            b, h = heads[done]
+            xs = {n: np.ascontiguousarray(x[n][b:b + 1, :, h:h + 1])
+                  for n in ("q", "k", "v", "g", "beta")}
+            h0 = None if x["h0"] is None else np.ascontiguousarray(x["h0"][b:b + 1, h:h + 1])
+            t = time.perf_counter()
+            oracle.backward(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"],
+                            np.ascontiguousarray(gr["dO"][b:b + 1, :, h:h + 1]), h0,
+                            np.ascontiguousarray(gr["dht"][b:b + 1, h:h + 1]))
+            secs += time.perf_counter() - t
+            done += 1
+        cpu = {"value": round(tokens * done / len(heads) / secs, 1), "unit": "tokens/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"{done} of {len(heads)} (b,h) heads of {w.name}, all T={T} tokens: the "
+                         f"fp64 per-token backward (one head is one work unit, so one core of "
+                         f"the {nthreads} runs it); {secs:.1f} s; tokens/s scaled to the whole "
+                         f"batch"}
+    if rank == 0:
+        tc = int(w.in_dtype == "bf16" and K == 128 and V == 128)
+        fwd_plan = gdn.segmented_plan(prob, T // 64) if T else (1, 0, 0)
+        launches = launches_per_step(synth.scaled(w, nseg=T // 64 or 1), fwd_plan[0]) + \
+            (tc + 1) + 3 + 1 + 1
+        line = {
+            "metric": BACKWARD_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": Ks, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if w.in_dtype == "f32" else "bf16 in, f32 math",
+            "data": "synthetic",
+            "config": {"workload": w0.name, "path": "backward", "B": B, "H": H, "T": T, "K": K,
+                       "V": V, "nseg": nseg, "chunk": 64, "in_dtype": w.in_dtype,
+                       "dO_dtype": "f32", "grad_dtype": "f32",
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"weak: {world} rank(s) x one batch each"},
+            "roofline": {"bound": "alu", "achieved": round(ach, 3),
+                         "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
+                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
+                         "traffic": None if args.T else recorded_traffic("chunk_grad_kernel", w0.name),
+                         "kernel": "chunk_grad_kernel", "kernel_ms": round(avg["chunk_grad"], 4),
+                         "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                         "peak_source": "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+            "path_roofline": {"t_roof_us": round(t_comp * 1e6, 1),
+                              "frac": round(t_comp / (ms_per_step * 1e-3), 4),
+                              "bytes": comp,
+                              "counts": "compulsory HBM bytes only: inputs, dO and dht read "
+                                        "once, the gradients written once",
+                              "peaks": f"{peaks_src}: hbm {hbm} GB/s"},
+            "stage_ms": {k: round(v, 4) for k, v in avg.items()},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches * Ks,
+            "clocks": clocks,
+            "peaks_source": peaks_src,
+        }
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+
+
 def workload_metric(w0) -> str:
     """The headline metric names its own workload; the other workloads carry their shape."""
     if w0.name == DEFAULT_WORKLOAD:
@@ -1079,9 +1278,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--path", choices=["forward", "state_grad"], default="forward",
+    ap.add_argument("--path", choices=["forward", "state_grad", "backward"], default="forward",
                     help="forward: the segmented forward (the headline line); state_grad: the "
-                         "backward's state-gradient path on the same workload")
+                         "backward's state-gradient path on the same workload; backward: the "
+                         "whole backward (gdn_chunk_bwd)")
     ap.add_argument("--schedule", choices=["pieces", "literal"], default="pieces",
                     help="pieces: one gdn_segmented_fwd call (the library's piece plan; the "
                          "headline line); literal: the pages' flow from three public calls -- "
@@ -1111,6 +1311,8 @@ def main(argv=None):
         run_reference(args)
     elif args.path == "state_grad":
         run_state_grad(args)
+    elif args.path == "backward":
+        run_backward(args)
     else:
         run_ours(args)
 

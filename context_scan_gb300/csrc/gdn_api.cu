@@ -649,6 +649,16 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const vo
                          const void* dO, const float* dht, float* dq, float* dk, float* dv,
                          float* dg, float* dbeta, float* dh0, void* workspace,
                          size_t workspace_bytes, void* stream) {
+    return gdn_chunk_bwd_timed(p, nseg, q, k, v, g, beta, h0, dO, dht, dq, dk, dv, dg, dbeta,
+                               dh0, workspace, workspace_bytes, stream, nullptr);
+}
+
+gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q, const void* k,
+                               const void* v, const void* g, const void* beta, const float* h0,
+                               const void* dO, const float* dht, float* dq, float* dk, float* dv,
+                               float* dg, float* dbeta, float* dh0, void* workspace,
+                               size_t workspace_bytes, void* stream, void* const* stage_events) {
+    void* const* ev = stage_events;
     gdn_status st = check_bwd(p, nseg);
     if (st != GDN_OK) return st;
     if (p->T > 0 && (!q || !k || !v || !g || !beta || !dO || !dq || !dk || !dv || !dg || !dbeta))
@@ -679,9 +689,11 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const vo
     const int nch = p->T / gdn::kChunk;
     // 1. the state entering every chunk: the forward with one segment per chunk (its output is
     //    recomputed into scratch and not used)
+    if (mark(ev, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
     st = run_segmented(p, nch, q, k, v, g, beta, h0, wsb + w.off_o, nullptr, Hc, workspace, s,
                        nullptr);
     if (st != GDN_OK) return st;
+    if (mark(ev, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
     // 2. the segments' summaries M (their linear parts carry the state gradient backwards)
     {
         ChainParams c = base_params(p, workspace);
@@ -716,7 +728,8 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const vo
     sg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
     sg.decay_first = p->decay_first;
     sg.dS = dS;
-    if (gdn::launch_state_grad(sg, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (mark(ev, 2, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
     if (gdn::launch_scan(nullptr, nullptr, dht, nullptr, dH + nseg * kv, nullptr, 0, 1, 1, BH,
                          p->K, p->V, s) != cudaSuccess ||
         gdn::launch_state_grad_scan(M, dS, dht, dH, nseg, BH, p->K, p->V, s) != cudaSuccess)
@@ -728,7 +741,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const vo
     //    state leaving every chunk (RFC 6.4.3 backward_state)
     sg.dH_end = dH + kv;
     sg.D_chunks = Dc;
-    if (gdn::launch_state_grad(sg, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (mark(ev, 3, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess ||
+        mark(ev, 4, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
     // 5. every chunk's gradients (RFC 6.4.3 backward_finish)
     gdn::ChunkGradParams cg{};
     cg.q = q;
@@ -752,7 +767,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const vo
     cg.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
     cg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
     cg.decay_first = p->decay_first;
-    return from_cuda(gdn::launch_chunk_grad(cg, s));
+    if (gdn::launch_chunk_grad(cg, s) != cudaSuccess || mark(ev, 5, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
 const char* gdn_status_string(gdn_status s) {

@@ -40,6 +40,13 @@ __device__ __forceinline__ float ldv(const void* base, long long idx, int bf16) 
     return reinterpret_cast<const float*>(base)[idx];
 }
 __device__ __forceinline__ float4 l4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+// Sum over the 16 lanes of a half-warp, in a fixed order (every lane gets the sum). All sums of
+// the kernel are taken in a fixed order, so its results do not vary from run to run.
+__device__ __forceinline__ float half_sum(float x) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
 
 template <int KD>
 struct CgSmem {
@@ -264,6 +271,7 @@ __global__ void __launch_bounds__(kCgThreads) chunk_grad_kernel(ChunkGradParams 
     float* Dt = sm + L::t_d;   // D'^T tile [kCT][KP]
     float dQd[4][CW] = {}, dKd[4][CW] = {}, dW[4][CW] = {};
     float deg = 0.f;   // this thread's share of <D', H>
+    float xv = 0.f;    // this thread's share of rowsum(X . V) for row rr
     const int rr = tid >> 2, cc4 = (tid & 3) * 4;   // a 1 x 4 block of a 64 x 16 tile
     for (int c0 = 0; c0 < V; c0 += kCT) {
         for (int e = tid; e < 64 * kCT; e += kCgThreads) {
@@ -388,14 +396,18 @@ __global__ void __launch_bounds__(kCgThreads) chunk_grad_kernel(ChunkGradParams 
             const float4 v4 = l4(&vt[rr * CTP + cc4]);
             float* out = p.dv + ((row0 + rr) * H + h) * V + c0 + cc4;
             out[0] = be * x4[0], out[1] = be * x4[1], out[2] = be * x4[2], out[3] = be * x4[3];
-            atomicAdd(&dbs[rr], x4[0] * v4.x + x4[1] * v4.y + x4[2] * v4.z + x4[3] * v4.w);
+            xv += x4[0] * v4.x + x4[1] * v4.y + x4[2] * v4.z + x4[3] * v4.w;
         }
         __syncthreads();
     }
-    // <D', H> over the whole state: one value per block
+    // <D', H> over the whole state: one partial per warp (red[0..7]); rowsum(X . V) over the
+    // four threads of a row
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) deg += __shfl_xor_sync(0xffffffffu, deg, off);
-    if (lane == 0) atomicAdd(&red[0], deg);
+    if (lane == 0) red[tid >> 5] = deg;
+    xv += __shfl_xor_sync(0xffffffffu, xv, 1);
+    xv += __shfl_xor_sync(0xffffffffu, xv, 2);
+    if ((tid & 3) == 0) dbs[rr] += xv;
     // ---- (6) dW into shared memory (W is no longer needed)
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -433,8 +445,11 @@ __global__ void __launch_bounds__(kCgThreads) chunk_grad_kernel(ChunkGradParams 
                 dkacc[r][w] = ekr[j] * y[r][w];   // e^Gx beta Y = e^Gx dKr
             }
             // Y . Kr = e^Gx (Y . k); dKr . Kr = beta e^Gx (Y . k)
-            atomicAdd(&dbs[j], eGx[j] * s);
-            atomicAdd(&dGx[j], ekr[j] * s);
+            s = half_sum(s);
+            if ((tid & 15) == 0) {
+                dbs[j] += eGx[j] * s;
+                dGx[j] += ekr[j] * s;
+            }
         }
     }
     // ---- (8) dA += dW (diag(beta e^Gx) K)^T (4 x 4 blocks)
@@ -538,13 +553,26 @@ __global__ void __launch_bounds__(kCgThreads) chunk_grad_kernel(ChunkGradParams 
             }
             *reinterpret_cast<float4*>(&dCs[i * P64 + b0]) = make_float4(sv[0], sv[1], sv[2], sv[3]);
         }
+        // row sums over the 16 threads of a row block (one half-warp); column sums through
+        // shared memory (T1 is dead), one partial per row block
+        float* part = sm + L::t;   // [16][64]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            atomicAdd(&dbs[a0 + r], rsb[r]);
-            atomicAdd(&dGx[a0 + r], rsg[r]);
-            atomicAdd(&dG[a0 + r], rsc[r]);
-            atomicAdd(&dG[b0 + r], -csg[r] - csc[r]);
+            const float b = half_sum(rsb[r]), g = half_sum(rsg[r]), c = half_sum(rsc[r]);
+            if ((tid & 15) == 0) {
+                dbs[a0 + r] += b;
+                dGx[a0 + r] += g;
+                dG[a0 + r] += c;
+            }
+            part[(tid >> 4) * 64 + b0 + r] = -csg[r] - csc[r];
         }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        float a = 0.f;
+#pragma unroll
+        for (int g = 0; g < 16; ++g) a += sm[L::t + g * 64 + tid];
+        dG[tid] += a;
     }
     __syncthreads();
     // ---- (10) q back into the tile region (T1 is dead)
@@ -595,17 +623,26 @@ __global__ void __launch_bounds__(kCgThreads) chunk_grad_kernel(ChunkGradParams 
                 ok[w] = fmaf(f, dKd[r][w], dk[r][w]) + dkacc[r][w];
             }
         }
+        float tks = 0.f;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            atomicAdd(&dG[i0 + r], tg[r] - tk[r]);
-            atomicAdd(&red[1], tk[r]);   // sum of rowsum(dKd . Kd): part of dGn
+            const float t = half_sum(tg[r] - tk[r]);
+            tks += tk[r];
+            if ((tid & 15) == 0) dG[i0 + r] += t;
         }
+        tks = half_sum(tks);   // this row block's share of sum(dKd . Kd), part of dGn
+        if ((tid & 15) == 0) red[16 + (tid >> 4)] = tks;
     }
     __syncthreads();
     // ---- (12) dg = reverse cumulative sum of dG + dGx (+ dGn at the last token), minus dGx for
     //      the read before the decay; dbeta
     if (tid < 32) {
-        const float dGn = red[1] + expf(Gn) * red[0];
+        float tk = 0.f, hd = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) tk += red[16 + i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hd += red[i];
+        const float dGn = tk + expf(Gn) * hd;
         // lane owns tokens 2 lane, 2 lane + 1; reverse cumulative sum over 64 tokens
         float a0 = dG[2 * lane] + dGx[2 * lane];
         float a1 = dG[2 * lane + 1] + dGx[2 * lane + 1] + (lane == 31 ? dGn : 0.f);

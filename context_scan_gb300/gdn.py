@@ -23,7 +23,7 @@ EXPORTED = ("gdn_workspace_bytes", "gdn_segmented_pieces", "gdn_segmented_plan",
             "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
             "gdn_varlen_workspace_bytes", "gdn_varlen_fwd", "gdn_varlen_fwd_timed",
             "gdn_state_grad_summary", "gdn_state_grad_scan", "gdn_chunk_bwd_workspace_bytes",
-            "gdn_chunk_bwd", "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
+            "gdn_chunk_bwd", "gdn_chunk_bwd_timed", "gdn_status_string", "gdn_check_device_error", "gdn_selftest_wait_timeout")
 
 
 class GdnError(RuntimeError):
@@ -77,6 +77,7 @@ def lib():
         L.gdn_chunk_bwd_workspace_bytes.argtypes = [pp, ctypes.c_int]
         L.gdn_chunk_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_chunk_bwd.argtypes = [pp, ctypes.c_int] + [_P] * 15 + [ctypes.c_size_t, _P]
+        L.gdn_chunk_bwd_timed.argtypes = L.gdn_chunk_bwd.argtypes + [_P]
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_check_device_error.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint)]
@@ -85,7 +86,7 @@ def lib():
                    "gdn_segmented_fwd", "gdn_segmented_fwd_timed", "gdn_segmented_fwd_noalloc",
                    "gdn_varlen_fwd", "gdn_varlen_fwd_timed", "gdn_check_device_error",
                    "gdn_selftest_wait_timeout", "gdn_state_grad_summary", "gdn_state_grad_scan",
-                   "gdn_chunk_bwd"):
+                   "gdn_chunk_bwd", "gdn_chunk_bwd_timed"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -309,6 +310,21 @@ def gdn_chunk_bwd(q, k, v, g, beta, h0, dO, dht, dq, dk, dv, dg, dbeta, dh0, nse
                                _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(workspace),
                                workspace.numel() if workspace is not None else 0,
                                _stream(stream)), "gdn_chunk_bwd")
+
+
+def gdn_chunk_bwd_timed(q, k, v, g, beta, h0, dO, dht, dq, dk, dv, dg, dbeta, dh0, nseg,
+                        workspace, events, stream=None, prob=None):
+    """gdn_chunk_bwd with six torch.cuda.Event markers recorded between its steps."""
+    if len(events) != 6:
+        raise ValueError("gdn_chunk_bwd_timed takes six events")
+    prob = prob or problem(k, v, dO, g=g)
+    arr = (_P * 6)(*[e.cuda_event for e in events])
+    _check(lib().gdn_chunk_bwd_timed(ctypes.byref(prob), nseg, _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(g), _ptr(beta), _ptr(h0), _ptr(dO), _ptr(dht),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                                     _ptr(dh0), _ptr(workspace),
+                                     workspace.numel() if workspace is not None else 0,
+                                     _stream(stream), arr), "gdn_chunk_bwd_timed")
 
 
 def gdn_selftest_wait_timeout(workspace, limit_cycles, stream=None):

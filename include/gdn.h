@@ -303,6 +303,20 @@ GDN_API gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, 
                                  float* dv, float* dg, float* dbeta, float* dh0, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* gdn_chunk_bwd with stage markers, for timing each step from the caller. If stage_events is
+ * non-NULL it points to six cudaEvent_t recorded on `stream` before the forward's
+ * recomputation, before the segments' summaries M, before the per-segment state gradients
+ * (then the reverse scan), before the second pass of the state-gradient chains, before the
+ * per-chunk gradients and after them (none is recorded when T == 0). Same results as
+ * gdn_chunk_bwd. */
+GDN_API gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q,
+                                       const void* k, const void* v, const void* g,
+                                       const void* beta, const float* h0, const void* dO,
+                                       const float* dht, float* dq, float* dk, float* dv,
+                                       float* dg, float* dbeta, float* dh0, void* workspace,
+                                       size_t workspace_bytes, void* stream,
+                                       void* const* stage_events);
+
 /* ---------------------------------------------------------------------------------------
  * Packed variable-length sequences
  * ---------------------------------------------------------------------------------------

@@ -173,3 +173,25 @@ def test_backward_full_size_sampled_heads(name):
             o = out[n]
             got = o[b:b + 1, h:h + 1] if n == "dh0" else o[b:b + 1, :, h:h + 1]
             assert rel_err(np64(got), r, label=f"{n} {b},{h}") <= TOL["bf16"], (n, b, h)
+
+
+def test_timed_variant_matches_and_records_its_events():
+    w = SMALL["cp4_small"]
+    x = synth.make_inputs(w)
+    d = upload(x, w)
+    gr, dO, dht = grads(w)
+    ref = run_bwd(w, d, dO, dht)
+    B, T, H, K = d["k"].shape
+    out = [torch.empty_like(ref[n]) for n in NAMES]
+    prob = gdn.problem(d["k"], d["v"], dO, g=d["g"])
+    ws = gdn.alloc_bwd_workspace(prob, w.nseg)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in ev:
+        e.record()
+    gdn.gdn_chunk_bwd_timed(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], dO, dht, *out,
+                            w.nseg, ws, ev, prob=prob)
+    torch.cuda.synchronize()
+    for n, o in zip(NAMES, out):
+        assert torch.equal(o, ref[n]), n
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in times) and sum(times) > 0
