@@ -290,7 +290,8 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
     if (mark(events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (P >= 2)
         e = gdn::launch_scan(M, S, Hp + hstride, Hp, equal ? H_in_out : nullptr, h0, 1, P,
-                             equal ? nsub : 1, BH, p->K, p->V, s);
+                             equal ? nsub : 1, BH, p->K, p->V, s,
+                             reinterpret_cast<gdn::DeviceError*>(workspace));
     else if (H_in_out)
         e = gdn::launch_scan(nullptr, nullptr, h0, nullptr, H_in_out, nullptr, 0, 1, 1, BH, p->K, p->V, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;

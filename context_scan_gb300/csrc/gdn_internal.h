@@ -79,10 +79,17 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
 // M[p] H + S[p] (M, S indexed by piece, [piece][BH][K][K|V]). The state entering every piece
 // p > p_first is written to Hp[p] ([P][BH][K][V]) when Hp is non-null, and the state entering
 // every piece p with p % nsub == 0 to H_seg[p / nsub] ([P/nsub][BH][K][V]) when H_seg is
-// non-null; H_seg[0] is h_seg0 (or zero) when p_first > 0.
+// non-null; H_seg[0] is h_seg0 (or zero) when p_first > 0. With an error word (err non-null),
+// K == V == 128 and at least one product to form, the products run on the tensor cores
+// (launch_tc_scan), whose bounded waits report to err; otherwise on the CUDA cores.
 cudaError_t launch_scan(const float* M, const float* S, const float* h_first, float* Hp,
                         float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
-                        int K, int V, cudaStream_t s);
+                        int K, int V, cudaStream_t s, DeviceError* err = nullptr);
+// the same scan on tcgen05 (gdn_scan_tc.cu), when tc_scan_supported
+bool tc_scan_supported(const float* M, const float* S, int p_first, int P, int K, int V);
+cudaError_t launch_tc_scan(const float* M, const float* S, const float* h_first, float* Hp,
+                           float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
+                           DeviceError* err, cudaStream_t s);
 
 // varlen metadata: checks the caller's cu_seqlens [nseq+1] (0 first, T last, non-decreasing)
 // and writes a checked copy to cu_out and cu_chunks[s] = sum over sequences before s of

@@ -564,8 +564,10 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s) {
 
 cudaError_t launch_scan(const float* M, const float* S, const float* h_first, float* Hp,
                         float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
-                        int K, int V, cudaStream_t s) {
+                        int K, int V, cudaStream_t s, DeviceError* err) {
     if (nsub < 1 || p_first < 0 || P <= p_first) return cudaErrorInvalidValue;
+    if (err && tc_scan_supported(M, S, p_first, P, K, V))
+        return launch_tc_scan(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, err, s);
     if (K == 128) return launch_scan_k<128>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     if (K == 64) return launch_scan_k<64>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     return cudaErrorInvalidValue;
