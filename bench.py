@@ -39,6 +39,9 @@ BACKWARD_METRIC = ("GDN backward tokens/s (dq, dk, dv, dg, dbeta, dh0 from dO an
                    "K=V=128 T=32K bf16")
 # fp32 CUDA-core peak: 152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz maximum SM clock
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# dense tf32 against dense bf16 on the tensor cores, nominal (1.1 and 2.25 PFLOP/s per GPU): a
+# tf32 contraction's peak is the measured bf16 rate times this
+TF32_PER_BF16 = 1.1 / 2.25
 
 
 def metric_of(w) -> str:
@@ -616,8 +619,10 @@ def run_state_grad(args):
     avg = {name: sum(e[a].elapsed_time(e[a + 1]) for e in ev) / Ksteps
            for a, name in enumerate(("summary_M", "state_grad", "scan"))}
     alg = state_grad_algorithmic(w)
-    ach = alg["flops"] / (avg["state_grad"] * 1e-3) / 1e12
     peaks, peaks_src = load_peaks()
+    tensor = w.in_dtype == "bf16"   # bf16 inputs take the tensor-core (tf32) instance
+    roof = kernel_roofline(alg, avg["state_grad"], float(peaks["hbm_gbs"]),
+                           float(peaks["bf16_tflops"]) * TF32_PER_BF16 if tensor else None)
     ms_per_step = max_s / Ksteps * 1e3
     value = aggregate(w.B * w.T, Ksteps, world, max_s)
 
@@ -652,13 +657,13 @@ def run_state_grad(args):
                        "K": K, "V": V, "nseg": nseg, "chunk": 64, "in_dtype": w.in_dtype,
                        "dO_dtype": "f32", "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"weak: {world} rank(s) x one batch each"},
-            "roofline": {"bound": "alu", "achieved": round(ach, 3),
-                         "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
-                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
-                         "traffic": None if args.T else recorded_traffic("state_grad_kernel", w0.name),
-                         "kernel": "state_grad_kernel", "kernel_ms": round(avg["state_grad"], 4),
-                         "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
-                         "peak_source": "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+            "roofline": dict(roof, **{
+                "traffic": None if args.T else recorded_traffic("state_grad_kernel", w0.name),
+                "kernel": "state_grad_kernel", "kernel_ms": round(avg["state_grad"], 4),
+                "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                "peak_source": (f"{peaks_src} bf16_tflops x {TF32_PER_BF16:.4f} (tf32/bf16 nominal) "
+                                f"or hbm_gbs, whichever bounds" if tensor else
+                                "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz")}),
             "stage_ms": {k: round(v, 4) for k, v in avg.items()},
             "cpu_baseline": cpu,
             "e2e": None,
@@ -691,6 +696,23 @@ def chunk_grad_algorithmic(w, out_bytes: int = 4):
                  c * K * V * 2 + c * c * V * 2 + 3 * c * V * K * 2 + 2 * c * c * V * 2 +
                  c * c * V * 2 + 2 * c * c * K * 2 + 2 * c * c * c * 2 + 3 * c * c * K * 2)
     return {"bytes": nbytes, "flops": per_chunk * th / c}
+
+
+def kernel_roofline(alg, ms, hbm_gbs, tensor_tflops=None):
+    """The roofline object of one kernel from its algorithmic work per launch and its average
+    launch time: against the tensor-core rate or HBM, whichever bounds it (tensor_tflops given),
+    or against the fp32 CUDA-core peak (the CUDA-core instances)."""
+    if tensor_tflops is None:
+        ach = alg["flops"] / (ms * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": round(ach, 3), "peak": round(FP32_ALU_TFLOPS, 2),
+                "unit": "TFLOP/s", "frac": round(ach / FP32_ALU_TFLOPS, 4)}
+    if alg["flops"] / (tensor_tflops * 1e12) >= alg["bytes"] / (hbm_gbs * 1e9):
+        ach = alg["flops"] / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(tensor_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(ach / tensor_tflops, 4)}
+    ach = alg["bytes"] / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 2), "peak": hbm_gbs, "unit": "GB/s",
+            "frac": round(ach / hbm_gbs, 4)}
 
 
 def backward_compulsory_bytes(w, out_bytes: int = 4):
@@ -780,10 +802,21 @@ def run_backward(args):
     barrier(dev)
     avg = {name: sum(e[a].elapsed_time(e[a + 1]) for e in ev) / Ks
            for a, name in enumerate(stage_names)}
-    alg = chunk_grad_algorithmic(w)
-    ach = alg["flops"] / (avg["chunk_grad"] * 1e-3) / 1e12
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    # the dominant backward kernel: the second state-gradient pass or the per-chunk gradients
+    tensor = w.in_dtype == "bf16"   # bf16 inputs take the tensor-core (tf32) instances
+    cand = {"state_grad_kernel": (state_grad_algorithmic(w), avg["state_grad"]),
+            "chunk_grad_kernel": (chunk_grad_algorithmic(w), avg["chunk_grad"])}
+    kname = max(cand, key=lambda n: cand[n][1])
+    alg, kms = cand[kname]
+    roof = kernel_roofline(alg, kms, hbm, float(peaks["bf16_tflops"]) * TF32_PER_BF16 if tensor else None)
+    roof.update({"traffic": None if args.T else recorded_traffic(kname, w0.name), "kernel": kname,
+                 "kernel_ms": round(kms, 4), "algorithmic_flops": alg["flops"],
+                 "algorithmic_bytes": alg["bytes"],
+                 "peak_source": (f"{peaks_src} bf16_tflops x {TF32_PER_BF16:.4f} (tf32/bf16 nominal) "
+                                 f"or hbm_gbs, whichever bounds" if tensor else
+                                 "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz")})
     ms_per_step = max_s / Ks * 1e3
     tokens = B * T
     value = aggregate(tokens, Ks, world, max_s)
@@ -843,13 +876,7 @@ def run_backward(args):
                        "dO_dtype": "f32", "grad_dtype": "f32",
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"weak: {world} rank(s) x one batch each"},
-            "roofline": {"bound": "alu", "achieved": round(ach, 3),
-                         "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
-                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
-                         "traffic": None if args.T else recorded_traffic("chunk_grad_kernel", w0.name),
-                         "kernel": "chunk_grad_kernel", "kernel_ms": round(avg["chunk_grad"], 4),
-                         "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
-                         "peak_source": "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz"},
+            "roofline": roof,
             "path_roofline": {"t_roof_us": round(t_comp * 1e6, 1),
                               "frac": round(t_comp / (ms_per_step * 1e-3), 4),
                               "bytes": comp,

@@ -12,11 +12,15 @@
 // with W^T dR = K^T diag(beta exp(Gx)) (A^T dR), A = (I + diag(beta) P)^{-1}. The state
 // gradient's columns are independent, like the state's: each CTA owns one chain (b, h,
 // segment) and a tile of CT columns, walks the segment's chunks from the last to the first
-// and writes D at the segment's start. fp32 on the CUDA cores; exponents are differences of
-// cumulative gates, never exp(-G).
+// and writes D at the segment's start. Exponents are differences of cumulative gates, never
+// exp(-G). Two instances: fp32 on the CUDA cores (fp32 inputs), and with the products -- L, C,
+// dR, A^T dR and the update of D -- as warp-level tensor-core tiles (tf32 operands, fp32
+// accumulation; bf16 inputs), whose fragments are read from shared memory at row pitches that
+// keep them free of bank conflicts.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
+#include "gdn_warp_mma.cuh"
 
 namespace gdn {
 namespace {
@@ -28,24 +32,29 @@ __device__ __forceinline__ float ld(const void* base, long long idx, int bf16) {
     return reinterpret_cast<const float*>(base)[idx];
 }
 
-template <int KD, int CT>
+template <int KD, int CT, bool MMA>
 struct BwdSmem {
     static constexpr int TP = 68;       // padded rows of the transposed k / q ([l][i]) and of
                                         // the 64 x 64 matrices (float4-aligned)
+    // row pitch of the CT-column tiles: the tensor-core instance reads them as MMA fragments,
+    // which a pitch of 8 mod 32 words keeps free of bank conflicts
+    static constexpr int DP = MMA ? CT + 8 : CT;
+    static constexpr int KRQ = MMA ? 0 : 64 * KD;       // the row copies only the FFMA loops use
     static constexpr int off_kr = 0;                    // k  [64][KD]  (row i = token)
-    static constexpr int off_qr = off_kr + 64 * KD;     // q  [64][KD]
-    static constexpr int off_kt = off_qr + 64 * KD;     // k^T [KD][TP]
+    static constexpr int off_qr = off_kr + KRQ;         // q  [64][KD]
+    static constexpr int off_kt = off_qr + KRQ;         // k^T [KD][TP]
     static constexpr int off_qt = off_kt + KD * TP;     // q^T [KD][TP]
-    static constexpr int off_do = off_qt + KD * TP;     // dO tile [64][CT]
-    static constexpr int off_d = off_do + 64 * CT;      // D tile  [KD][CT]
-    static constexpr int off_l = off_d + KD * CT;       // L = diag(beta) P  [64][TP]
+    static constexpr int off_do = off_qt + KD * TP;     // dO tile [64][DP]
+    static constexpr int off_d = off_do + 64 * DP;      // D tile  [KD][DP]
+    static constexpr int off_l = off_d + KD * DP;       // L = diag(beta) P  [64][TP]
     static constexpr int off_a = off_l + 64 * TP;       // A                 [64][TP]
     static constexpr int off_c = off_a + 64 * TP;       // C                 [64][TP]
-    static constexpr int off_z = off_c + 64 * TP;       // Z tile [64][CT]
-    static constexpr int off_r = off_z + 64 * CT;       // dR tile [64][CT]
-    static constexpr int off_s = off_r + 64 * CT;       // scalars: 6 x 64
+    static constexpr int off_z = off_c + 64 * TP;       // Z tile [64][DP]
+    static constexpr int off_r = off_z + 64 * DP;       // dR tile [64][DP]
+    static constexpr int off_s = off_r + 64 * DP;       // scalars: 6 x 64
     static constexpr int total = off_s + 6 * 64;
     static constexpr size_t bytes = sizeof(float) * total;
+    static_assert(bytes <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
@@ -54,10 +63,11 @@ __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<floa
 // Every large product below gives each thread a 4 x 4 (or 4 x 2) block of the result in
 // registers and reads its operands as float4 / float2 rows of shared memory, so the loop
 // does 8-16 FMAs per shared-memory load (a thread per output reads two operands per FMA).
-template <int KD, int CT>
+template <int KD, int CT, bool MMA>
 __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p) {
     static_assert(CT == 32 && kThreads == 256, "thread blocking assumes 256 threads, CT = 32");
-    using L = BwdSmem<KD, CT>;
+    using L = BwdSmem<KD, CT, MMA>;
+    constexpr int DP = L::DP;
     extern __shared__ float4 smv[];
     float* sm = reinterpret_cast<float*>(smv);
     float* kr = sm + L::off_kr;
@@ -93,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
 
     for (int e = tid; e < KD * CT; e += kThreads) {
         const int l = e / CT, c = e % CT;
-        Ds[e] = p.dH_end ? p.dH_end[(head * KD + l) * V + c0 + c] : 0.f;
+        Ds[l * DP + c] = p.dH_end ? p.dH_end[(head * KD + l) * V + c0 + c] : 0.f;
     }
 
     // The next chunk's k, q, dO, g and beta are loaded into registers while the current
@@ -134,16 +144,21 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
 #pragma unroll
         for (int n = 0; n < NKQ; ++n) {
             const int e = tid + n * kThreads, l = e % KD, i4 = (e / KD) * 4;
+            if constexpr (!MMA) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                kr[(i4 + r) * KD + l] = pk[n][r];
-                qr[(i4 + r) * KD + l] = pq[n][r];
+                for (int r = 0; r < 4; ++r) {
+                    kr[(i4 + r) * KD + l] = pk[n][r];
+                    qr[(i4 + r) * KD + l] = pq[n][r];
+                }
             }
             st4(&kt[l * TP + i4], make_float4(pk[n][0], pk[n][1], pk[n][2], pk[n][3]));
             st4(&qt[l * TP + i4], make_float4(pq[n][0], pq[n][1], pq[n][2], pq[n][3]));
         }
 #pragma unroll
-        for (int n = 0; n < ND; ++n) dos[tid + n * kThreads] = pd[n];
+        for (int n = 0; n < ND; ++n) {
+            const int e = tid + n * kThreads;
+            dos[(e / CT) * DP + e % CT] = pd[n];
+        }
         if (tid < 64) {
             gx[tid] = pg;   // raw gate until the cumsum
             bet[tid] = pb;
@@ -156,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             float* dst = p.D_chunks + (cg * p.B * H + bh) * KD * V + c0;
             for (int e = tid; e < KD * CT; e += kThreads) {
                 const int l = e / CT, c = e % CT;
-                dst[(long long)l * V + c] = Ds[e];
+                dst[(long long)l * V + c] = Ds[l * DP + c];
             }
         }
         // ---- (2) inclusive / read-side cumulative gates (one warp, two tokens per lane)
@@ -180,8 +195,23 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             eq[tid] = expf(gam[tid]);
             ekr[tid] = bet[tid] * expf(gx[tid]);
         }
-        // ---- (3) L = diag(beta) P (j < i) and C (j <= i), one 4 x 4 block per thread; clear A
-        {
+        // ---- (3) L = diag(beta) P (j < i) and C (j <= i); clear A
+        if constexpr (MMA) {
+            const int warp = tid >> 5, lane = tid & 31;
+            const int m64 = 16 * (warp & 3), n64 = 32 * (warp >> 2);   // 16 x 32 per warp
+            float sq[1][4][4] = {}, sk[1][4][4] = {};
+            wtile<1, 4>(sq, m64, n64, KD, lane, [&](int i, int l) { return qt[l * TP + i]; },
+                        [&](int l, int j) { return kt[l * TP + j]; });
+            wtile<1, 4>(sk, m64, n64, KD, lane, [&](int i, int l) { return kt[l * TP + i]; },
+                        [&](int l, int j) { return kt[l * TP + j]; });
+            wtile_each<1, 4>(sk, m64, n64, lane, [&](int i, int j, float& v) {
+                Ls[i * TP + j] = (j < i) ? bet[i] * expf(gx[i] - gam[j]) * v : 0.f;
+                As[i * TP + j] = 0.f;
+            });
+            wtile_each<1, 4>(sq, m64, n64, lane, [&](int i, int j, float& v) {
+                Cs[i * TP + j] = (j <= i) ? expf(gam[i] - gam[j]) * v : 0.f;
+            });
+        } else {
             const int i0 = (tid / 16) * 4, j0 = (tid % 16) * 4;
             float kk[4][4] = {}, qk[4][4] = {};
             if (j0 <= i0 + 3) {   // blocks wholly above the diagonal stay zero
@@ -259,100 +289,138 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
                 __syncthreads();
             }
         }
-        // ---- (5) dR = Kd D' + C^T dO, one 4 x 2 block (rows j0.., columns cc..) per thread
-        const int j0 = (tid / 16) * 4, cc = (tid % 16) * 2;
-        {
-            float a[4][2] = {}, t[4][2] = {};
+        if constexpr (MMA) {
+            const int warp = tid >> 5, lane = tid & 31;
+            const int mr = 16 * (warp & 3), nr = 16 * (warp >> 2);   // 64 x 32: 16 x 16 per warp
+            // ---- (5) dR = Kd D' + C^T dO
+            {
+                float d[1][2][4] = {};
+                wtile<1, 2>(d, mr, nr, KD, lane, [&](int i, int l) { return dk[i] * kt[l * TP + i]; },
+                            [&](int l, int c) { return Ds[l * DP + c]; });
+                wtile<1, 2>(d, mr, nr, 64, lane, [&](int i, int j) { return Cs[j * TP + i]; },
+                            [&](int j, int c) { return dos[j * DP + c]; });
+                wtile_each<1, 2>(d, mr, nr, lane, [&](int i, int c, float& v) { Rs[i * DP + c] = v; });
+            }
+            __syncthreads();
+            // ---- (6) Z = diag(beta exp(Gx)) A^T dR
+            {
+                float z[1][2][4] = {};
+                wtile<1, 2>(z, mr, nr, 64, lane, [&](int j, int i) { return As[i * TP + j]; },
+                            [&](int i, int c) { return Rs[i * DP + c]; });
+                wtile_each<1, 2>(z, mr, nr, lane, [&](int j, int c, float& v) { Zs[j * DP + c] = ekr[j] * v; });
+            }
+            __syncthreads();
+            // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z: K x 32, (16 K / 64) x 16 per warp
+            {
+                constexpr int MT = KD / 64;
+                const int ml = 16 * MT * (warp & 3), nl = 16 * (warp >> 2);
+                float a[MT][2][4] = {};
+                wtile<MT, 2>(a, ml, nl, 64, lane, [&](int l, int i) { return eq[i] * qt[l * TP + i]; },
+                             [&](int i, int c) { return dos[i * DP + c]; });
+                wtile<MT, 2>(a, ml, nl, 64, lane, [&](int l, int i) { return -kt[l * TP + i]; },
+                             [&](int i, int c) { return Zs[i * DP + c]; });
+                const float dlast = expf(glast);
+                wtile_each<MT, 2>(a, ml, nl, lane, [&](int l, int c, float& v) {
+                    float* dp = &Ds[l * DP + c];
+                    *dp = fmaf(dlast, *dp, v);
+                });
+            }
+        } else {
+            // ---- (5) dR = Kd D' + C^T dO, one 4 x 2 block (rows j0.., columns cc..) per thread
+            const int j0 = (tid / 16) * 4, cc = (tid % 16) * 2;
+            {
+                float a[4][2] = {}, t[4][2] = {};
 #pragma unroll 4
-            for (int l = 0; l < KD; ++l) {
-                const float4 kv = ld4(&kt[l * TP + j0]);
-                const float2 dv = *reinterpret_cast<const float2*>(&Ds[l * CT + cc]);
-                const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
+                for (int l = 0; l < KD; ++l) {
+                    const float4 kv = ld4(&kt[l * TP + j0]);
+                    const float2 dv = *reinterpret_cast<const float2*>(&Ds[l * CT + cc]);
+                    const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    a[r][0] = fmaf(k4[r], dv.x, a[r][0]);
-                    a[r][1] = fmaf(k4[r], dv.y, a[r][1]);
-                }
-            }
-            for (int i = j0; i < 64; ++i) {   // C[i][j] = 0 for j > i
-                const float4 cv = ld4(&Cs[i * TP + j0]);
-                const float2 ov = *reinterpret_cast<const float2*>(&dos[i * CT + cc]);
-                const float c4[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    t[r][0] = fmaf(c4[r], ov.x, t[r][0]);
-                    t[r][1] = fmaf(c4[r], ov.y, t[r][1]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                *reinterpret_cast<float2*>(&Rs[(j0 + r) * CT + cc]) =
-                    make_float2(fmaf(dk[j0 + r], a[r][0], t[r][0]), fmaf(dk[j0 + r], a[r][1], t[r][1]));
-        }
-        __syncthreads();
-        // ---- (6) Z = diag(beta exp(Gx)) A^T dR (same blocking)
-        {
-            float a[4][2] = {};
-            for (int i = j0; i < 64; ++i) {   // A[i][j] = 0 for j > i
-                const float4 av = ld4(&As[i * TP + j0]);
-                const float2 rv = *reinterpret_cast<const float2*>(&Rs[i * CT + cc]);
-                const float a4[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    a[r][0] = fmaf(a4[r], rv.x, a[r][0]);
-                    a[r][1] = fmaf(a4[r], rv.y, a[r][1]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                *reinterpret_cast<float2*>(&Zs[(j0 + r) * CT + cc]) =
-                    make_float2(ekr[j0 + r] * a[r][0], ekr[j0 + r] * a[r][1]);
-        }
-        __syncthreads();
-        // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z, one 4 x CW block (rows l0..) per thread
-        {
-            constexpr int CW = KD * CT / (kThreads * 4);   // 4 columns at K = 128, 2 at K = 64
-            const int l0 = (tid / (CT / CW)) * 4, d0 = (tid % (CT / CW)) * CW;
-            float a[4][CW] = {};
-#pragma unroll 4
-            for (int i = 0; i < 64; ++i) {
-                const float e = eq[i];
-                const float4 qv = ld4(&qr[i * KD + l0]), kv = ld4(&kr[i * KD + l0]);
-                float o4[CW], z4[CW];
-                if constexpr (CW == 4) {
-                    const float4 ov = ld4(&dos[i * CT + d0]), zv = ld4(&Zs[i * CT + d0]);
-                    o4[0] = ov.x, o4[1] = ov.y, o4[2] = ov.z, o4[3] = ov.w;
-                    z4[0] = zv.x, z4[1] = zv.y, z4[2] = zv.z, z4[3] = zv.w;
-                } else {
-#pragma unroll
-                    for (int c = 0; c < CW; ++c) {
-                        o4[c] = dos[i * CT + d0 + c];
-                        z4[c] = Zs[i * CT + d0 + c];
+                    for (int r = 0; r < 4; ++r) {
+                        a[r][0] = fmaf(k4[r], dv.x, a[r][0]);
+                        a[r][1] = fmaf(k4[r], dv.y, a[r][1]);
                     }
                 }
-                const float q4[4] = {e * qv.x, e * qv.y, e * qv.z, e * qv.w};
-                const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
+                for (int i = j0; i < 64; ++i) {   // C[i][j] = 0 for j > i
+                    const float4 cv = ld4(&Cs[i * TP + j0]);
+                    const float2 ov = *reinterpret_cast<const float2*>(&dos[i * CT + cc]);
+                    const float c4[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        t[r][0] = fmaf(c4[r], ov.x, t[r][0]);
+                        t[r][1] = fmaf(c4[r], ov.y, t[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    *reinterpret_cast<float2*>(&Rs[(j0 + r) * CT + cc]) =
+                        make_float2(fmaf(dk[j0 + r], a[r][0], t[r][0]), fmaf(dk[j0 + r], a[r][1], t[r][1]));
+            }
+            __syncthreads();
+            // ---- (6) Z = diag(beta exp(Gx)) A^T dR (same blocking)
+            {
+                float a[4][2] = {};
+                for (int i = j0; i < 64; ++i) {   // A[i][j] = 0 for j > i
+                    const float4 av = ld4(&As[i * TP + j0]);
+                    const float2 rv = *reinterpret_cast<const float2*>(&Rs[i * CT + cc]);
+                    const float a4[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        a[r][0] = fmaf(a4[r], rv.x, a[r][0]);
+                        a[r][1] = fmaf(a4[r], rv.y, a[r][1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    *reinterpret_cast<float2*>(&Zs[(j0 + r) * CT + cc]) =
+                        make_float2(ekr[j0 + r] * a[r][0], ekr[j0 + r] * a[r][1]);
+            }
+            __syncthreads();
+            // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z, one 4 x CW block (rows l0..) per thread
+            {
+                constexpr int CW = KD * CT / (kThreads * 4);   // 4 columns at K = 128, 2 at K = 64
+                const int l0 = (tid / (CT / CW)) * 4, d0 = (tid % (CT / CW)) * CW;
+                float a[4][CW] = {};
+#pragma unroll 4
+                for (int i = 0; i < 64; ++i) {
+                    const float e = eq[i];
+                    const float4 qv = ld4(&qr[i * KD + l0]), kv = ld4(&kr[i * KD + l0]);
+                    float o4[CW], z4[CW];
+                    if constexpr (CW == 4) {
+                        const float4 ov = ld4(&dos[i * CT + d0]), zv = ld4(&Zs[i * CT + d0]);
+                        o4[0] = ov.x, o4[1] = ov.y, o4[2] = ov.z, o4[3] = ov.w;
+                        z4[0] = zv.x, z4[1] = zv.y, z4[2] = zv.z, z4[3] = zv.w;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < CW; ++c) {
+                            o4[c] = dos[i * CT + d0 + c];
+                            z4[c] = Zs[i * CT + d0 + c];
+                        }
+                    }
+                    const float q4[4] = {e * qv.x, e * qv.y, e * qv.z, e * qv.w};
+                    const float k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int c = 0; c < CW; ++c)
+                            a[r][c] = fmaf(q4[r], o4[c], fmaf(-k4[r], z4[c], a[r][c]));
+                }
+                const float dlast = expf(glast);
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
-                    for (int c = 0; c < CW; ++c)
-                        a[r][c] = fmaf(q4[r], o4[c], fmaf(-k4[r], z4[c], a[r][c]));
+                    for (int c = 0; c < CW; ++c) {
+                        float* dp = &Ds[(l0 + r) * CT + d0 + c];
+                        *dp = fmaf(dlast, *dp, a[r][c]);
+                    }
             }
-            const float dlast = expf(glast);
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < CW; ++c) {
-                    float* dp = &Ds[(l0 + r) * CT + d0 + c];
-                    *dp = fmaf(dlast, *dp, a[r][c]);
-                }
         }
         __syncthreads();
     }
 
     for (int e = tid; e < KD * CT; e += kThreads) {
         const int l = e / CT, c = e % CT;
-        p.dS[(head * KD + l) * V + c0 + c] = Ds[e];
+        p.dS[(head * KD + l) * V + c0 + c] = Ds[l * DP + c];
     }
 }
 
@@ -411,17 +479,25 @@ state_grad_scan_kernel(const float* __restrict__ M, const float* __restrict__ dS
     }
 }
 
-template <int KD>
-cudaError_t launch_state_grad_k(const StateGradParams& p, cudaStream_t s) {
-    constexpr int CT = 32;
-    using L = BwdSmem<KD, CT>;
-    auto kern = state_grad_kernel<KD, CT>;
+template <int KD, int CT, bool MMA>
+cudaError_t launch_state_grad_kv(const StateGradParams& p, cudaStream_t s) {
+    using L = BwdSmem<KD, CT, MMA>;
+    auto kern = state_grad_kernel<KD, CT, MMA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L::bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.B * p.H * p.nseg * (p.V / CT)));
     kern<<<grid, kThreads, L::bytes, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int KD>
+cudaError_t launch_state_grad_k(const StateGradParams& p, cudaStream_t s) {
+    constexpr int CT = 32;
+    // bf16 inputs: the tensor-core products (tf32 operands keep the bf16 bar); fp32 inputs keep
+    // fp32 products on the CUDA cores
+    if (p.in_bf16) return launch_state_grad_kv<KD, CT, true>(p, s);
+    return launch_state_grad_kv<KD, CT, false>(p, s);
 }
 
 template <int KD>

@@ -680,6 +680,9 @@ cudaError_t launch_chunk_grad_k(const ChunkGradParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_chunk_grad(const ChunkGradParams& p, cudaStream_t s) {
+    // bf16 inputs: the tensor-core products (tf32 operands keep the bf16 bar); fp32 inputs keep
+    // fp32 products on the CUDA cores
+    if (p.in_bf16) return launch_chunk_grad_mma(p, s);
     return p.K == 64 ? launch_chunk_grad_k<64>(p, s) : launch_chunk_grad_k<128>(p, s);
 }
 

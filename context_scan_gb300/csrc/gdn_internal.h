@@ -141,6 +141,8 @@ struct ChunkGradParams {
     int in_bf16, do_bf16, decay_first;
 };
 cudaError_t launch_chunk_grad(const ChunkGradParams& p, cudaStream_t s);
+// the same with the products on the warp-level tensor-core path (tf32 operands; bf16 inputs)
+cudaError_t launch_chunk_grad_mma(const ChunkGradParams& p, cudaStream_t s);
 // dH_in[s] = M[s]^T dH_in[s+1] + dS[s] for s = nseg-1 .. 0, dH_in[nseg] = dht (or zero)
 cudaError_t launch_state_grad_scan(const float* M, const float* dS, const float* dht,
                                    float* dH_in, int nseg, int BH, int K, int V, cudaStream_t s);

@@ -134,3 +134,19 @@ def test_reference_arm_json_line(steps):
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_kernel_roofline_picks_the_binding_limit():
+    # 1 TFLOP and 1 GB: at 100 TFLOP/s and 1000 GB/s the tensor rate binds (10 ms vs 1 ms)
+    alg = {"flops": 1e12, "bytes": 1e9}
+    r = bench.kernel_roofline(alg, 20.0, 1000.0, 100.0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 50.0) < 1e-6 and abs(r["frac"] - 0.5) < 1e-6
+    # at 10 000 TFLOP/s the bytes bind (1 ms vs 0.1 ms)
+    r = bench.kernel_roofline(alg, 2.0, 1000.0, 10000.0)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 500.0) < 1e-6 and abs(r["frac"] - 0.5) < 1e-6
+    # no tensor rate: the fp32 CUDA-core peak
+    r = bench.kernel_roofline(alg, 1000.0, 1000.0)
+    assert r["bound"] == "alu" and abs(r["achieved"] - 1.0) < 1e-9
+    assert abs(r["frac"] - 1.0 / bench.FP32_ALU_TFLOPS) < 1e-4   # frac is rounded to 4 places

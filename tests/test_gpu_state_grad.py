@@ -3,13 +3,16 @@ Context Parallel", section 6.4.3): per-segment state-gradient summaries dS and t
 scan dH_in[s] = M[s]^T dH_in[s+1] + dS[s], through the C ABI, against the fp64 oracle on
 the same seeded inputs and incoming gradients.
 
-Bars (per tensor, max|err| / RMS(ref)): 1e-4 for fp32 inputs and 1e-3 for bf16 inputs.
+Bars (per tensor, max|err| / RMS(ref)): 1e-4 for fp32 inputs and 1e-2 for bf16 inputs.
 Both sides read the same values (bf16 inputs arrive already rounded, dO is drawn in the
-dtype it is stored in), so the bar only has to cover the kernel's fp32 arithmetic: sums of
-at most 128-term products per chunk, carried through up to 128 chunks of decays that are
-all at most 1 (the bf16 bar is looser because bf16 workloads are the long ones). Where a
-result also passes through the segment summaries M computed on the GPU, it takes the
-forward's bar for bf16 inputs, 2e-2, which is the bar M itself is held to.
+dtype it is stored in). With fp32 inputs the kernel runs fp32 products on the CUDA cores, and
+the bar covers fp32 sums of at most 128-term products per chunk carried through up to 128
+chunks of decays that are all at most 1. With bf16 inputs the products run on the tensor
+cores with tf32 operands (rounded to nearest, 2^-11 of each operand at most): a chunk's
+contribution passes about five such roundings in series (dR, A^T dR, the update), measured at
+up to 4.1e-3 (wide gates; 2.7e-3 at full size); the bar is half the forward's bar for bf16
+inputs. Where a result also passes through the segment summaries M computed on the GPU, it
+takes the forward's bar for bf16 inputs, 2e-2, which is the bar M itself is held to.
 """
 import numpy as np
 import pytest
@@ -22,7 +25,7 @@ from gpu_util import head_slice, np64, rel_err, run_summary, upload
 pytestmark = pytest.mark.gpu
 
 W = synth.WORKLOADS
-TOL = {"f32": 1e-4, "bf16": 1e-3}
+TOL = {"f32": 1e-4, "bf16": 1e-2}
 TOL_WITH_M = {"f32": 1e-4, "bf16": 2e-2}
 
 SMALL = {
