@@ -698,6 +698,18 @@ def chunk_grad_algorithmic(w, out_bytes: int = 4):
     return {"bytes": nbytes, "flops": per_chunk * th / c}
 
 
+def bwd_pieces(w, sms: int) -> int:
+    """The piece count gdn_chunk_bwd gives its state-gradient chains (the library's rule,
+    restated to count its launches): 1 when B*H*column-tiles chains fill at most one wave,
+    else the largest power of two dividing the chunk count with that many chains per wave."""
+    tile = 64 if w.in_dtype == "bf16" else 32
+    chains = w.B * w.H * (w.V // tile)
+    nch, sms, P = w.T // 64, min(sms, 256), 1
+    while nch > 0 and nch % (2 * P) == 0 and chains * 2 * P <= sms:
+        P *= 2
+    return P
+
+
 def kernel_roofline(alg, ms, hbm_gbs, tensor_tflops=None):
     """The roofline object of one kernel from its algorithmic work per launch and its average
     launch time: against the tensor-core rate or HBM, whichever bounds it (tensor_tflops given),
@@ -759,7 +771,9 @@ def run_backward(args):
     prob = gdn.problem(d["k"], d["v"], d["dO"], g=d["g"])
     ws = gdn.alloc_bwd_workspace(prob, nseg, device=dev)
     stream = torch.cuda.current_stream()
-    stage_names = ("forward", "summary_M", "state_grad_scan", "state_grad", "chunk_grad")
+    # the state-gradient chains run one pass (one piece) or two around the summaries and the
+    # reverse scan (several pieces): see bwd_pieces
+    stage_names = ("forward", "summary_M", "state_grad_1", "state_grad_2", "chunk_grad")
 
     def call(di, oi, events=None):
         args_ = (di["q"], di["k"], di["v"], di["g"], di["beta"], di["h0"], di["dO"], di["dht"],
@@ -806,7 +820,9 @@ def run_backward(args):
     hbm = float(peaks["hbm_gbs"])
     # the dominant backward kernel: the second state-gradient pass or the per-chunk gradients
     tensor = w.in_dtype == "bf16"   # bf16 inputs take the tensor-core (tf32) instances
-    cand = {"state_grad_kernel": (state_grad_algorithmic(w), avg["state_grad"]),
+    pieces = bwd_pieces(w, torch.cuda.get_device_properties(dev).multi_processor_count)
+    cand = {"state_grad_kernel": (state_grad_algorithmic(synth.scaled(w, nseg=pieces)),
+                                  max(avg["state_grad_1"], avg["state_grad_2"])),
             "chunk_grad_kernel": (chunk_grad_algorithmic(w), avg["chunk_grad"])}
     kname = max(cand, key=lambda n: cand[n][1])
     alg, kms = cand[kname]
@@ -864,7 +880,7 @@ def run_backward(args):
         tc = int(w.in_dtype == "bf16" and K == 128 and V == 128)
         fwd_plan = gdn.segmented_plan(prob, T // 64) if T else (1, 0, 0)
         launches = launches_per_step(synth.scaled(w, nseg=T // 64 or 1), fwd_plan[0]) + \
-            (tc + 1) + 3 + 1 + 1
+            (1 + 1 if pieces == 1 else (tc + 1) + 3 + 1 + 1)
         line = {
             "metric": BACKWARD_METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": Ks, "warmup": args.warmup,
@@ -872,7 +888,8 @@ def run_backward(args):
             "vs_baseline": None, "dtype": "f32" if w.in_dtype == "f32" else "bf16 in, f32 math",
             "data": "synthetic",
             "config": {"workload": w0.name, "path": "backward", "B": B, "H": H, "T": T, "K": K,
-                       "V": V, "nseg": nseg, "chunk": 64, "in_dtype": w.in_dtype,
+                       "V": V, "nseg": nseg, "state_grad_pieces": pieces, "chunk": 64,
+                       "in_dtype": w.in_dtype,
                        "dO_dtype": "f32", "grad_dtype": "f32",
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"weak: {world} rank(s) x one batch each"},

@@ -349,13 +349,34 @@ gdn_status check_varlen(const gdn_problem* p, int nseq) {
 }
 
 // ---- backward: [the forward's / summary's workspace (header first) | o scratch | Hc | Dc | M |
-//      S | dS | dH_in (nseg + 1 slots)], each region 256-byte aligned. Hc and Dc hold the state
-//      entering and the state gradient leaving every chunk ([T/64][B][H][K][V] fp32).
+//      S | dS | dH_in (P + 1 slots)], each region 256-byte aligned, P the most pieces
+//      bwd_pieces gives on any device. Hc and Dc hold the state entering and the state gradient
+//      leaving every chunk ([T/64][B][H][K][V] fp32).
 struct BwdLayout {
     size_t off_o, off_hc, off_dc, off_m, off_s, off_ds, off_dh, total;
 };
 
-BwdLayout bwd_layout(const gdn_problem& p, int nseg) {
+// Pieces of the backward's state-gradient chains. Each (b, h, piece, column tile) is one chain
+// and runs one CTA per SM. When the chains of whole sequences fit in one wave, one pass from dht
+// gives the gradient leaving every chunk and dh0 (P = 1); otherwise P is the largest power of two
+// dividing the chunk count with B*H*tiles*P chains per wave: a first pass gives each piece's
+// dS_local, the reverse scan over the piece summaries the gradient leaving each piece, and a
+// second pass the gradient leaving every chunk. `sms` is the SM count (capped at
+// kBwdSmBound, which sizes the workspace for any device).
+constexpr int kBwdSmBound = 256;
+int bwd_pieces(const gdn_problem& p, int sms) {
+    const int nch = p.T / gdn::kChunk;
+    const long long chains =
+        (long long)p.B * p.H * (p.V / gdn::state_grad_tile(p.in_dtype == GDN_DTYPE_BF16));
+    sms = std::min(sms, kBwdSmBound);
+    int P = 1;
+    while (nch > 0 && nch % (2 * P) == 0 && chains * 2 * P <= sms) P *= 2;
+    return P;
+}
+
+BwdLayout bwd_layout(const gdn_problem& p, int nseg_api) {
+    (void)nseg_api;   // the backward's own piece count sizes the per-piece arrays
+    const int nseg = bwd_pieces(p, kBwdSmBound);
     BwdLayout w{};
     const int nch = p.T / gdn::kChunk;
     const size_t head = std::max(layout(p, nch > 0 ? nch : 1).total, layout(p, 1).total);
@@ -686,7 +707,7 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q, co
     float* M = reinterpret_cast<float*>(wsb + w.off_m);
     float* S = reinterpret_cast<float*>(wsb + w.off_s);
     float* dS = reinterpret_cast<float*>(wsb + w.off_ds);
-    float* dH = reinterpret_cast<float*>(wsb + w.off_dh);   // [nseg + 1]: entering s; dht last
+    float* dH = reinterpret_cast<float*>(wsb + w.off_dh);   // [P + 1]: entering piece s; dht last
     const int nch = p->T / gdn::kChunk;
     // 1. the state entering every chunk: the forward with one segment per chunk (its output is
     //    recomputed into scratch and not used)
@@ -695,23 +716,9 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q, co
                        nullptr);
     if (st != GDN_OK) return st;
     if (mark(ev, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
-    // 2. the segments' summaries M (their linear parts carry the state gradient backwards)
-    {
-        ChainParams c = base_params(p, workspace);
-        c.k = k;
-        c.v = v;
-        c.g = g;
-        c.beta = beta;
-        c.M = M;
-        c.S = S;
-        c.seg_len = p->T / nseg;
-        c.nseg_run = nseg;
-        c.nseg_total = nseg;
-        if (prepare(c, p, workspace, s) != cudaSuccess || run_summary(c, s) != cudaSuccess)
-            return GDN_ERR_CUDA;
-    }
-    // 3. per-segment state gradients from the segments' own outputs (RFC 6.4.3 dS_local), and
-    //    the reverse scan to the gradient entering every segment; dH[nseg] = dht
+    // 2-4. the gradient leaving every chunk (Dc) and dh0 (RFC 6.4.3: dS_local per piece, the
+    //      reverse scan dH_in = M^T dH_out + dS_local, then each piece's chunks again)
+    const int P = bwd_pieces(*p, sm_count());
     gdn::StateGradParams sg{};
     sg.q = q;
     sg.k = k;
@@ -723,28 +730,57 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q, co
     sg.H = p->H;
     sg.K = p->K;
     sg.V = p->V;
-    sg.seg_len = p->T / nseg;
-    sg.nseg = nseg;
     sg.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
     sg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
     sg.decay_first = p->decay_first;
-    sg.dS = dS;
-    if (mark(ev, 2, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (gdn::launch_scan(nullptr, nullptr, dht, nullptr, dH + nseg * kv, nullptr, 0, 1, 1, BH,
-                         p->K, p->V, s) != cudaSuccess ||
-        gdn::launch_state_grad_scan(M, dS, dht, dH, nseg, BH, p->K, p->V, s) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    if (dh0 && cudaMemcpyAsync(dh0, dH, sizeof(float) * kv, cudaMemcpyDeviceToDevice, s) !=
-                   cudaSuccess)
-        return GDN_ERR_CUDA;
-    // 4. each segment's chunks again from the gradient leaving it, recording the gradient on the
-    //    state leaving every chunk (RFC 6.4.3 backward_state)
-    sg.dH_end = dH + kv;
-    sg.D_chunks = Dc;
-    if (mark(ev, 3, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess ||
-        mark(ev, 4, s) != cudaSuccess)
-        return GDN_ERR_CUDA;
+    if (P == 1) {
+        // the chains of whole sequences fill at most one wave: one pass from dht (no summaries;
+        // the stage events of the summaries and of the second pass mark empty stages)
+        sg.seg_len = p->T;
+        sg.nseg = 1;
+        sg.dH_end = dht;
+        sg.dS = dh0 ? dh0 : dS;
+        sg.D_chunks = Dc;
+        if (mark(ev, 2, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess ||
+            mark(ev, 3, s) != cudaSuccess ||
+            mark(ev, 4, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    } else {
+        // the pieces' summaries M (their linear parts carry the state gradient backwards)
+        ChainParams c = base_params(p, workspace);
+        c.k = k;
+        c.v = v;
+        c.g = g;
+        c.beta = beta;
+        c.M = M;
+        c.S = S;
+        c.seg_len = p->T / P;
+        c.nseg_run = P;
+        c.nseg_total = P;
+        if (prepare(c, p, workspace, s) != cudaSuccess || run_summary(c, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        // dS_local of every piece, and the reverse scan to the gradient entering every piece;
+        // dH[P] = dht
+        sg.seg_len = p->T / P;
+        sg.nseg = P;
+        sg.dS = dS;
+        if (mark(ev, 2, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if (gdn::launch_scan(nullptr, nullptr, dht, nullptr, dH + P * kv, nullptr, 0, 1, 1, BH,
+                             p->K, p->V, s) != cudaSuccess ||
+            gdn::launch_state_grad_scan(M, dS, dht, dH, P, BH, p->K, p->V, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if (dh0 && cudaMemcpyAsync(dh0, dH, sizeof(float) * kv, cudaMemcpyDeviceToDevice, s) !=
+                       cudaSuccess)
+            return GDN_ERR_CUDA;
+        // each piece's chunks again from the gradient leaving it, recording the gradient on
+        // the state leaving every chunk (RFC 6.4.3 backward_state)
+        sg.dH_end = dH + kv;
+        sg.D_chunks = Dc;
+        if (mark(ev, 3, s) != cudaSuccess || gdn::launch_state_grad(sg, s) != cudaSuccess ||
+            mark(ev, 4, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
     // 5. every chunk's gradients (RFC 6.4.3 backward_finish)
     gdn::ChunkGradParams cg{};
     cg.q = q;

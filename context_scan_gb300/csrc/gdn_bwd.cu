@@ -65,7 +65,8 @@ __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<floa
 // does 8-16 FMAs per shared-memory load (a thread per output reads two operands per FMA).
 template <int KD, int CT, bool MMA>
 __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p) {
-    static_assert(CT == 32 && kThreads == 256, "thread blocking assumes 256 threads, CT = 32");
+    static_assert(kThreads == 256 && (CT == 32 || (MMA && CT == 64)),
+                  "thread blocking assumes 256 threads; CT = 32, or 64 for the tensor-core instance");
     using L = BwdSmem<KD, CT, MMA>;
     constexpr int DP = L::DP;
     extern __shared__ float4 smv[];
@@ -290,37 +291,39 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             }
         }
         if constexpr (MMA) {
+            // 8 warps: four row groups by two column halves of the CT-column tile
+            constexpr int NT = CT / 16;
             const int warp = tid >> 5, lane = tid & 31;
-            const int mr = 16 * (warp & 3), nr = 16 * (warp >> 2);   // 64 x 32: 16 x 16 per warp
+            const int mr = 16 * (warp & 3), nr = (CT / 2) * (warp >> 2);   // 64 x CT: 16 x CT/2 per warp
             // ---- (5) dR = Kd D' + C^T dO
             {
-                float d[1][2][4] = {};
-                wtile<1, 2>(d, mr, nr, KD, lane, [&](int i, int l) { return dk[i] * kt[l * TP + i]; },
-                            [&](int l, int c) { return Ds[l * DP + c]; });
-                wtile<1, 2>(d, mr, nr, 64, lane, [&](int i, int j) { return Cs[j * TP + i]; },
-                            [&](int j, int c) { return dos[j * DP + c]; });
-                wtile_each<1, 2>(d, mr, nr, lane, [&](int i, int c, float& v) { Rs[i * DP + c] = v; });
+                float d[1][NT][4] = {};
+                wtile<1, NT>(d, mr, nr, KD, lane, [&](int i, int l) { return dk[i] * kt[l * TP + i]; },
+                             [&](int l, int c) { return Ds[l * DP + c]; });
+                wtile<1, NT>(d, mr, nr, 64, lane, [&](int i, int j) { return Cs[j * TP + i]; },
+                             [&](int j, int c) { return dos[j * DP + c]; });
+                wtile_each<1, NT>(d, mr, nr, lane, [&](int i, int c, float& v) { Rs[i * DP + c] = v; });
             }
             __syncthreads();
             // ---- (6) Z = diag(beta exp(Gx)) A^T dR
             {
-                float z[1][2][4] = {};
-                wtile<1, 2>(z, mr, nr, 64, lane, [&](int j, int i) { return As[i * TP + j]; },
-                            [&](int i, int c) { return Rs[i * DP + c]; });
-                wtile_each<1, 2>(z, mr, nr, lane, [&](int j, int c, float& v) { Zs[j * DP + c] = ekr[j] * v; });
+                float z[1][NT][4] = {};
+                wtile<1, NT>(z, mr, nr, 64, lane, [&](int j, int i) { return As[i * TP + j]; },
+                             [&](int i, int c) { return Rs[i * DP + c]; });
+                wtile_each<1, NT>(z, mr, nr, lane, [&](int j, int c, float& v) { Zs[j * DP + c] = ekr[j] * v; });
             }
             __syncthreads();
-            // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z: K x 32, (16 K / 64) x 16 per warp
+            // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z: K x CT, (16 K / 64) x CT/2 per warp
             {
                 constexpr int MT = KD / 64;
-                const int ml = 16 * MT * (warp & 3), nl = 16 * (warp >> 2);
-                float a[MT][2][4] = {};
-                wtile<MT, 2>(a, ml, nl, 64, lane, [&](int l, int i) { return eq[i] * qt[l * TP + i]; },
-                             [&](int i, int c) { return dos[i * DP + c]; });
-                wtile<MT, 2>(a, ml, nl, 64, lane, [&](int l, int i) { return -kt[l * TP + i]; },
-                             [&](int i, int c) { return Zs[i * DP + c]; });
+                const int ml = 16 * MT * (warp & 3), nl = (CT / 2) * (warp >> 2);
+                float a[MT][NT][4] = {};
+                wtile<MT, NT>(a, ml, nl, 64, lane, [&](int l, int i) { return eq[i] * qt[l * TP + i]; },
+                              [&](int i, int c) { return dos[i * DP + c]; });
+                wtile<MT, NT>(a, ml, nl, 64, lane, [&](int l, int i) { return -kt[l * TP + i]; },
+                              [&](int i, int c) { return Zs[i * DP + c]; });
                 const float dlast = expf(glast);
-                wtile_each<MT, 2>(a, ml, nl, lane, [&](int l, int c, float& v) {
+                wtile_each<MT, NT>(a, ml, nl, lane, [&](int l, int c, float& v) {
                     float* dp = &Ds[l * DP + c];
                     *dp = fmaf(dlast, *dp, v);
                 });
@@ -493,11 +496,10 @@ cudaError_t launch_state_grad_kv(const StateGradParams& p, cudaStream_t s) {
 
 template <int KD>
 cudaError_t launch_state_grad_k(const StateGradParams& p, cudaStream_t s) {
-    constexpr int CT = 32;
-    // bf16 inputs: the tensor-core products (tf32 operands keep the bf16 bar); fp32 inputs keep
-    // fp32 products on the CUDA cores
-    if (p.in_bf16) return launch_state_grad_kv<KD, CT, true>(p, s);
-    return launch_state_grad_kv<KD, CT, false>(p, s);
+    // bf16 inputs: the tensor-core products (tf32 operands keep the bf16 bar) on 64-column
+    // tiles; fp32 inputs keep fp32 products on the CUDA cores, 32-column tiles
+    if (p.in_bf16) return launch_state_grad_kv<KD, state_grad_tile(1), true>(p, s);
+    return launch_state_grad_kv<KD, state_grad_tile(0), false>(p, s);
 }
 
 template <int KD>

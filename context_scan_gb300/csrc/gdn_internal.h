@@ -118,6 +118,9 @@ struct StateGradParams {
     int in_bf16, do_bf16, decay_first;
 };
 cudaError_t launch_state_grad(const StateGradParams& p, cudaStream_t s);
+// columns of the state gradient one CTA of launch_state_grad owns (its grid is
+// B*H*nseg*(V/tile) CTAs, one per SM)
+constexpr int state_grad_tile(int in_bf16) { return in_bf16 ? 64 : 32; }
 
 // Per-chunk gradients of the backward: every (b, h, chunk c) independently, from the chunk's
 // q, k, v, g, beta, dO, the state entering it (Hc[c]) and the gradient on the state leaving it

@@ -283,19 +283,25 @@ GDN_API gdn_status gdn_state_grad_scan(const gdn_problem* p, int nseg, const flo
  * "backward_finish"): the gradients of L = sum_t dO_t . o_t + <dht, h_final> with respect to
  * every input, for the problem gdn_segmented_fwd computes.
  *   Steps: the forward once more with one segment per chunk, which yields the state entering
- *   every chunk; the segments' summaries M; the per-segment state gradients dS_local and the
- *   reverse scan dH_in = M^T dH_out + dS_local (nseg segments, the emulated ranks); each
- *   segment's chunks again from the gradient leaving it, which yields the gradient on the state
- *   leaving every chunk; then every chunk's gradients at once, independently, from its inputs,
- *   the state entering it and the gradient leaving it. The results do not depend on nseg.
+ *   every chunk; then the gradient on the state leaving every chunk, by state-gradient chains
+ *   that run backwards over P pieces of each sequence. The library picks P for the GPU: when the
+ *   chains of whole sequences (B*H times the column tiles) fit in one wave, P = 1 and one pass
+ *   from dht gives every chunk's gradient and dh0; otherwise the pieces' summaries M, their
+ *   state gradients dS_local and the reverse scan dH_in = M^T dH_out + dS_local (the pieces
+ *   stand in for ranks), then each piece's chunks again from the gradient leaving it. Last,
+ *   every chunk's gradients at once, independently, from its inputs, the state entering it
+ *   and the gradient leaving it. nseg is validated as for gdn_segmented_fwd; the results do
+ *   not depend on it.
  *   Inputs as gdn_segmented_fwd (q, k, v, g, beta in in_dtype, h0 fp32 or NULL); dO
  *   [B,T,H,V] in out_dtype; dht [B,H,K,V] fp32 or NULL (zero).
  *   Outputs, fp32, written: dq, dk [B,T,H,K]; dv [B,T,H,V]; dg, dbeta [B,T,H]; dh0 [B,H,K,V]
  *   (NULL skips it).
- *   Per-chunk gradients are fp32 CUDA-core arithmetic; the forward's recomputation follows
- *   gdn_segmented_fwd's paths. Per-channel gates (gate_k) are not supported
- *   (GDN_ERR_UNSUPPORTED_SHAPE). Workspace: gdn_chunk_bwd_workspace_bytes(p, nseg), whose first
- *   256 bytes must be zero before the first call (the device error word). */
+ *   With bf16 inputs the products of the state-gradient chains and of the per-chunk gradients
+ *   run on the tensor cores with tf32 operands (fp32 accumulation); with fp32 inputs they are
+ *   fp32 CUDA-core arithmetic. The forward's recomputation follows gdn_segmented_fwd's paths.
+ *   Per-channel gates (gate_k) are not supported (GDN_ERR_UNSUPPORTED_SHAPE). Workspace:
+ *   gdn_chunk_bwd_workspace_bytes(p, nseg) (the same for every nseg), whose first 256 bytes
+ *   must be zero before the first call (the device error word). */
 GDN_API size_t gdn_chunk_bwd_workspace_bytes(const gdn_problem* p, int nseg);
 GDN_API gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, const void* k,
                                  const void* v, const void* g, const void* beta, const float* h0,
@@ -305,10 +311,10 @@ GDN_API gdn_status gdn_chunk_bwd(const gdn_problem* p, int nseg, const void* q, 
 
 /* gdn_chunk_bwd with stage markers, for timing each step from the caller. If stage_events is
  * non-NULL it points to six cudaEvent_t recorded on `stream` before the forward's
- * recomputation, before the segments' summaries M, before the per-segment state gradients
- * (then the reverse scan), before the second pass of the state-gradient chains, before the
- * per-chunk gradients and after them (none is recorded when T == 0). Same results as
- * gdn_chunk_bwd. */
+ * recomputation, before the pieces' summaries M, before the first pass of the state-gradient
+ * chains (then the reverse scan), before their second pass, before the per-chunk gradients and
+ * after them. With one piece the summaries and the second pass are empty stages and the first
+ * pass is the only one. None is recorded when T == 0. Same results as gdn_chunk_bwd. */
 GDN_API gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q,
                                        const void* k, const void* v, const void* g,
                                        const void* beta, const float* h0, const void* dO,

@@ -150,3 +150,14 @@ def test_kernel_roofline_picks_the_binding_limit():
     r = bench.kernel_roofline(alg, 1000.0, 1000.0)
     assert r["bound"] == "alu" and abs(r["achieved"] - 1.0) < 1e-9
     assert abs(r["frac"] - 1.0 / bench.FP32_ALU_TFLOPS) < 1e-4   # frac is rounded to 4 places
+
+
+def test_backward_piece_rule():
+    from context_scan_gb300 import synth
+    w = synth.WORKLOADS["cp4_b2_h32_t32k"]
+    assert bench.bwd_pieces(w, 152) == 1          # 64 heads x 2 tiles = 128 chains: one wave
+    small = synth.scaled(w, B=2, H=2, T=1024)     # 8 chains, 16 chunks
+    assert bench.bwd_pieces(small, 152) == 16
+    assert bench.bwd_pieces(synth.scaled(small, T=64 * 12), 152) == 4   # 12 chunks: 2-adic 4
+    f32 = synth.scaled(small, in_dtype="f32")     # 32-column tiles: 16 chains
+    assert bench.bwd_pieces(f32, 152) == 8
