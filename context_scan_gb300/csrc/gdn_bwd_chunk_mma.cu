@@ -33,11 +33,22 @@ __device__ __forceinline__ float ldin(const void* base, long long idx, int bf16)
     if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
     return reinterpret_cast<const float*>(base)[idx];
 }
+// 16-byte asynchronous copies global -> shared (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_prior() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 template <int KD>
 struct MgSmem {
     static constexpr int P64 = 68;          // row pitch of the 64 x 64 matrices
     static constexpr int KP = KD + 4;       // row pitch of the 64 x KD matrices and H^T tiles
-    static constexpr int CTP = kMT + 4;     // row pitch of the 64 x 16 tiles
+    static constexpr int CTP = kMT + 4;     // row pitch of the 64 x 16 fp32 tiles (R, dR, dO)
+    static constexpr int HP = kMT + 8;      // row pitch of the K x 16 tiles of H and D'
+    static constexpr int VPB = kMT + 8;     // row pitch (bf16 elements) of the 64 x 16 bf16 tiles
     static constexpr int k = 0;                          // k       [64][KP]
     static constexpr int a = k + 64 * KP;                // A       [64][P64]
     static constexpr int c = a + 64 * P64;               // C, then S'
@@ -45,11 +56,12 @@ struct MgSmem {
     static constexpr int da = p + 64 * P64;              // dA, then S
     static constexpr int w = da + 64 * P64;              // W, then dW  [64][KP]
     static constexpr int t = w + 64 * KP;                // tile region (see below)
-    // tile region: q before the tile loop (then the inverse's scratch); v, dO, R, dR
-    // [64][CTP] and H^T, D'^T [kMT][KP] during it; A^T dA [64][P64] after it, then q again
-    static constexpr int t_v = t, t_do = t_v + 64 * CTP, t_r = t_do + 64 * CTP,
-                         t_dr = t_r + 64 * CTP, t_h = t_dr + 64 * CTP, t_d = t_h + kMT * KP;
-    static constexpr int tile_end = t_d + kMT * KP;
+    // tile region: q before the tile loop (then the inverse's scratch); during it two buffers
+    // of the tile's inputs as copied -- H and D' [KD][HP] fp32, v [64][VPB] bf16, dO [64][CTP]
+    // fp32 or [64][VPB] bf16 -- and R, dR [64][CTP]; A^T dA [64][P64] after it, then q again
+    static constexpr int BUF = 2 * KD * HP + 64 * VPB / 2 + 64 * CTP;   // floats per buffer
+    static constexpr int t_buf = t, t_r = t_buf + 2 * BUF, t_dr = t_r + 64 * CTP;
+    static constexpr int tile_end = t_dr + 64 * CTP;
     static constexpr int s = (tile_end > t + 64 * KP ? tile_end : t + 64 * KP);
     enum { G = 0, GX, EG, EGX, DKF, BET, EKR, DG, DGX, DBETA, RED, NS };
     static constexpr int part = s + NS * 64;             // per-warp partial sums [12][64]
@@ -59,10 +71,10 @@ struct MgSmem {
     static_assert(bytes <= 232448, "shared memory budget");
 };
 
-template <int KD>
+template <int KD, bool DOB>   // DOB: dO in bf16 (the output dtype)
 __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGradParams p) {
     using L = MgSmem<KD>;
-    constexpr int KP = L::KP, P64 = L::P64, CTP = L::CTP;
+    constexpr int KP = L::KP, P64 = L::P64, CTP = L::CTP, HP = L::HP, VPB = L::VPB;
     // 64 x K warp tiles: 32 x 32 at K = 128 (column groups of 32: 4), 16 x 32 at K = 64 (2)
     constexpr int MTK = KD == 128 ? 2 : 1;
     constexpr int NCG = KD / 32;
@@ -212,61 +224,99 @@ __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGrad
     }
     __syncthreads();
 
-    // ---- (5) the V tiles
-    float* vt = sm + L::t_v;
-    float* dot = sm + L::t_do;
+    // ---- (5) the V tiles, each copied into shared memory while the one before it computes
     float* Rt = sm + L::t_r;
     float* dRt = sm + L::t_dr;
-    float* Ht = sm + L::t_h;   // H^T tile [kMT][KP]
-    float* Dt = sm + L::t_d;   // D'^T tile [kMT][KP]
+    auto buf_h = [&](int bb) { return sm + L::t_buf + bb * L::BUF; };            // H [KD][HP]
+    auto buf_d = [&](int bb) { return buf_h(bb) + KD * HP; };                     // D' [KD][HP]
+    auto buf_v = [&](int bb) {                                                    // v [64][VPB]
+        return reinterpret_cast<__nv_bfloat16*>(buf_h(bb) + 2 * KD * HP);
+    };
+    auto buf_o = [&](int bb) { return buf_h(bb) + 2 * KD * HP + 64 * VPB / 2; };  // dO
+    auto issue_tile = [&](int c0, int bb) {
+        float* hb = buf_h(bb);
+        float* db = buf_d(bb);
+        for (int e = tid; e < KD * (kMT / 4); e += kMgThreads) {
+            const int l = e / (kMT / 4), q4 = 4 * (e % (kMT / 4));
+            const long long g0 = st0 + (long long)l * V + c0 + q4;
+            cp16(hb + l * HP + q4, p.Hc + g0);
+            cp16(db + l * HP + q4, p.Dc + g0);
+        }
+        __nv_bfloat16* vb = buf_v(bb);
+        for (int e = tid; e < 64 * (kMT / 8); e += kMgThreads) {
+            const int j = e / (kMT / 8), q8 = 8 * (e % (kMT / 8));
+            cp16(vb + j * VPB + q8,
+                 reinterpret_cast<const __nv_bfloat16*>(p.v) + ((row0 + j) * H + h) * V + c0 + q8);
+        }
+        if (DOB) {
+            __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(buf_o(bb));
+            for (int e = tid; e < 64 * (kMT / 8); e += kMgThreads) {
+                const int j = e / (kMT / 8), q8 = 8 * (e % (kMT / 8));
+                cp16(ob + j * VPB + q8,
+                     reinterpret_cast<const __nv_bfloat16*>(p.dO) + ((row0 + j) * H + h) * V + c0 + q8);
+            }
+        } else {
+            float* ob = buf_o(bb);
+            for (int e = tid; e < 64 * (kMT / 4); e += kMgThreads) {
+                const int j = e / (kMT / 4), q4 = 4 * (e % (kMT / 4));
+                cp16(ob + j * CTP + q4,
+                     reinterpret_cast<const float*>(p.dO) + ((row0 + j) * H + h) * V + c0 + q4);
+            }
+        }
+        cp_commit();
+    };
     float dQd[MTK][4][4] = {}, dKd[MTK][4][4] = {}, dRH[MTK][4][4] = {};   // dW = -dR H^T
     float dCa[1][4][4] = {}, dAa[1][4][4] = {};
     float deg = 0.f;                  // this thread's share of <D', H>
     float xv0 = 0.f, xv1 = 0.f;       // rowsum(X . V) over this thread's columns, rows mV + g4, + 8
+    issue_tile(0, 0);
 #pragma unroll 1
     for (int c0 = 0; c0 < V; c0 += kMT) {
-        for (int e = tid; e < 64 * kMT; e += kMgThreads) {
-            const int i = e / kMT, cc = e % kMT;
-            const long long idx = ((row0 + i) * H + h) * V + c0 + cc;
-            vt[i * CTP + cc] = ldin(p.v, idx, p.in_bf16);
-            dot[i * CTP + cc] = ldin(p.dO, idx, p.do_bf16);
-        }
+        const int bb = (c0 / kMT) & 1;
+        if (c0 + kMT < V) issue_tile(c0 + kMT, bb ^ 1);
+        else cp_commit();   // an empty group keeps "all but the newest" meaning this tile
+        cp_wait_prior();
+        __syncthreads();
+        const float* Hn = buf_h(bb);
+        const float* Dn = buf_d(bb);
+        const __nv_bfloat16* vbt = buf_v(bb);
+        const float* obf = buf_o(bb);
+        const __nv_bfloat16* obh = reinterpret_cast<const __nv_bfloat16*>(buf_o(bb));
+        auto vt = [&](int j, int cc) { return __bfloat162float(vbt[j * VPB + cc]); };
+        auto dot = [&](int j, int cc) {
+            return DOB ? __bfloat162float(obh[j * VPB + cc]) : obf[j * CTP + cc];
+        };
         for (int e = tid; e < KD * kMT; e += kMgThreads) {
             const int l = e / kMT, cc = e % kMT;
-            const long long idx = st0 + (long long)l * V + c0 + cc;
-            const float hv = p.Hc[idx], dv = p.Dc[idx];
-            Ht[cc * KP + l] = hv;
-            Dt[cc * KP + l] = dv;
-            deg = fmaf(hv, dv, deg);
+            deg = fmaf(Hn[l * HP + cc], Dn[l * HP + cc], deg);
         }
-        __syncthreads();
         // R = A diag(beta) V - W H and dR = Kd D' + C^T dO on this tile's 16 columns
         {
             float r[1][1][4] = {}, d[1][1][4] = {};
             wtile<1, 1>(r, mV, nV, 64, lane, [&](int i, int j) { return As[i * P64 + j] * bet[j]; },
-                        [&](int j, int cc) { return vt[j * CTP + cc]; });
+                        [&](int j, int cc) { return vt(j, cc); });
             wtile<1, 1>(r, mV, nV, KD, lane, [&](int i, int l) { return -Ws[i * KP + l]; },
-                        [&](int l, int cc) { return Ht[cc * KP + l]; });
+                        [&](int l, int cc) { return Hn[l * HP + cc]; });
             wtile<1, 1>(d, mV, nV, KD, lane, [&](int i, int l) { return dkf[i] * ks[i * KP + l]; },
-                        [&](int l, int cc) { return Dt[cc * KP + l]; });
+                        [&](int l, int cc) { return Dn[l * HP + cc]; });
             wtile<1, 1>(d, mV, nV, 64, lane, [&](int i, int j) { return Cs[j * P64 + i]; },
-                        [&](int j, int cc) { return dot[j * CTP + cc]; });
+                        [&](int j, int cc) { return dot(j, cc); });
             wtile_each<1, 1>(r, mV, nV, lane, [&](int i, int cc, float& v) { Rt[i * CTP + cc] = v; });
             wtile_each<1, 1>(d, mV, nV, lane, [&](int i, int cc, float& v) { dRt[i * CTP + cc] = v; });
         }
         __syncthreads();
         // dQd += dO H^T, dKd += R D'^T, dR H^T (= -dW), contracting the tile's 16 columns
-        wtile<MTK, 4>(dQd, mK, nK, kMT, lane, [&](int i, int cc) { return dot[i * CTP + cc]; },
-                      [&](int cc, int l) { return Ht[cc * KP + l]; });
+        wtile<MTK, 4>(dQd, mK, nK, kMT, lane, [&](int i, int cc) { return dot(i, cc); },
+                      [&](int cc, int l) { return Hn[l * HP + cc]; });
         wtile<MTK, 4>(dKd, mK, nK, kMT, lane, [&](int i, int cc) { return Rt[i * CTP + cc]; },
-                      [&](int cc, int l) { return Dt[cc * KP + l]; });
+                      [&](int cc, int l) { return Dn[l * HP + cc]; });
         wtile<MTK, 4>(dRH, mK, nK, kMT, lane, [&](int i, int cc) { return dRt[i * CTP + cc]; },
-                      [&](int cc, int l) { return Ht[cc * KP + l]; });
+                      [&](int cc, int l) { return Hn[l * HP + cc]; });
         // dC += dO R^T and dA += dR (diag(beta) V)^T
-        wtile<1, 4>(dCa, m64, n64, kMT, lane, [&](int i, int cc) { return dot[i * CTP + cc]; },
+        wtile<1, 4>(dCa, m64, n64, kMT, lane, [&](int i, int cc) { return dot(i, cc); },
                     [&](int cc, int j) { return Rt[j * CTP + cc]; });
         wtile<1, 4>(dAa, m64, n64, kMT, lane, [&](int i, int cc) { return dRt[i * CTP + cc]; },
-                    [&](int cc, int j) { return bet[j] * vt[j * CTP + cc]; });
+                    [&](int cc, int j) { return bet[j] * vt(j, cc); });
         // X = A^T dR: dv = beta X, rowsum(X . V)
         {
             float x[1][1][4] = {};
@@ -278,8 +328,8 @@ __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGrad
                 make_float2(b0 * x[0][0][0], b0 * x[0][0][1]);
             *reinterpret_cast<float2*>(p.dv + ((row0 + j0 + 8) * H + h) * V + c0 + cc) =
                 make_float2(b1 * x[0][0][2], b1 * x[0][0][3]);
-            xv0 += x[0][0][0] * vt[j0 * CTP + cc] + x[0][0][1] * vt[j0 * CTP + cc + 1];
-            xv1 += x[0][0][2] * vt[(j0 + 8) * CTP + cc] + x[0][0][3] * vt[(j0 + 8) * CTP + cc + 1];
+            xv0 += x[0][0][0] * vt(j0, cc) + x[0][0][1] * vt(j0, cc + 1);
+            xv1 += x[0][0][2] * vt(j0 + 8, cc) + x[0][0][3] * vt(j0 + 8, cc + 1);
         }
         __syncthreads();
     }
@@ -490,10 +540,10 @@ __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGrad
     }
 }
 
-template <int KD>
+template <int KD, bool DOB>
 cudaError_t launch_k(const ChunkGradParams& p, cudaStream_t s) {
     using L = MgSmem<KD>;
-    auto kern = chunk_grad_mma_kernel<KD>;
+    auto kern = chunk_grad_mma_kernel<KD, DOB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L::bytes);
     if (e != cudaSuccess) return e;
@@ -506,7 +556,9 @@ cudaError_t launch_k(const ChunkGradParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_chunk_grad_mma(const ChunkGradParams& p, cudaStream_t s) {
-    return p.K == 64 ? launch_k<64>(p, s) : launch_k<128>(p, s);
+    if (!p.in_bf16) return cudaErrorInvalidValue;   // the v tiles are copied as bf16
+    if (p.K == 64) return p.do_bf16 ? launch_k<64, true>(p, s) : launch_k<64, false>(p, s);
+    return p.do_bf16 ? launch_k<128, true>(p, s) : launch_k<128, false>(p, s);
 }
 
 }  // namespace gdn
