@@ -74,6 +74,9 @@ struct ChainParams {
 // fp32 CUDA-core kernels (any supported K/V, fp32 or bf16 inputs)
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
+// per-channel gates (gate_k) with bf16 inputs: the chains by sub-block normalisation with their
+// products on the warp-level tensor cores (routed from the two launchers above)
+cudaError_t launch_kda_mma_chain(const ChainParams& p, bool summary, cudaStream_t s);
 // In-order scan over consecutive pieces p_first .. P-1 of every (b, h): the state entering
 // piece p_first is h_first ([BH][K][V], or zero when null); entering piece p+1 it is
 // M[p] H + S[p] (M, S indexed by piece, [piece][BH][K][K|V]). The state entering every piece

@@ -400,6 +400,9 @@ cudaError_t launch_chain_g(const ChainParams& p, cudaStream_t s) {
 
 template <int KD, bool SUMMARY>
 cudaError_t launch_chain(const ChainParams& p, cudaStream_t s) {
+    // per-channel gates at bf16 inputs: the sub-block normalised chains with their products on
+    // the tensor cores (gdn_kda_mma.cu)
+    if (p.gate_k && p.in_bf16) return launch_kda_mma_chain(p, SUMMARY, s);
     return p.gate_k ? launch_chain_g<KD, SUMMARY, true>(p, s) : launch_chain_g<KD, SUMMARY, false>(p, s);
 }
 

@@ -22,6 +22,12 @@ CASES = {
     "bf16_k128_single": synth.scaled(BASE, H=3, T=640, seed=0x6D6E0703),
     "f32_k64_fast_decay": synth.scaled(BASE, H=2, T=256, K=64, V=64, nseg=2, in_dtype="f32",
                                        g_mu=-1, g_sd=2, seed=0x6D6E0704),
+    # bf16 runs the sub-block normalised tensor-core chains: gates of about -6 per token spread
+    # every 16-token block past the factored form's limit (the blocks' exact path), and
+    # gates of N(-4, 1.5) before the log-sigmoid leave about half the blocks on each path
+    "bf16_k128_steep": synth.scaled(BASE, H=2, T=512, nseg=2, g_mu=-6, g_sd=1, seed=0x6D6E0705),
+    "bf16_k128_mixed": synth.scaled(BASE, H=2, T=512, nseg=2, g_mu=-4, g_sd=1.5, seed=0x6D6E0706),
+    "bf16_k64_cp2": synth.scaled(BASE, H=2, T=512, K=64, V=64, nseg=2, seed=0x6D6E0707),
 }
 
 
