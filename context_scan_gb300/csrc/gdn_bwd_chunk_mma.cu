@@ -116,14 +116,32 @@ __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGrad
     const int cgK = KD == 128 ? (warp >> 1) : (warp >> 2);
     const int mV = 16 * (warp & 3), nV = 8 * (warp >> 2);
 
-    // ---- (1) k, and q into the tile region; the gates and beta
+    // ---- (1) k, and q into the tile region (bf16, eight per 16-byte load, every load of a
+    //      thread in flight before the first store); the gates and beta
     float* qs = sm + L::t;
-    for (int e = tid; e < 64 * KD; e += kMgThreads) {
-        const int i = e / KD, l = e % KD;
-        const long long idx = ((row0 + i) * H + h) * KD + l;
-        ks[i * KP + l] = ldin(p.k, idx, p.in_bf16);
-        qs[i * KP + l] = ldin(p.q, idx, p.in_bf16);
-    }
+    constexpr int NKV = 64 * KD / 8 / kMgThreads;
+    auto load_rows = [&](const void* src, float* dst) {
+        uint4 u[NKV];
+#pragma unroll
+        for (int n = 0; n < NKV; ++n) {
+            const int e = tid + n * kMgThreads, i = e / (KD / 8), l8 = 8 * (e % (KD / 8));
+            u[n] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(src) +
+                                                    ((row0 + i) * H + h) * KD + l8);
+        }
+#pragma unroll
+        for (int n = 0; n < NKV; ++n) {
+            const int e = tid + n * kMgThreads, i = e / (KD / 8), l8 = 8 * (e % (KD / 8));
+            float* d = dst + i * KP + l8;
+            *reinterpret_cast<float4*>(d) =
+                make_float4(__uint_as_float(u[n].x << 16), __uint_as_float(u[n].x & 0xFFFF0000u),
+                            __uint_as_float(u[n].y << 16), __uint_as_float(u[n].y & 0xFFFF0000u));
+            *reinterpret_cast<float4*>(d + 4) =
+                make_float4(__uint_as_float(u[n].z << 16), __uint_as_float(u[n].z & 0xFFFF0000u),
+                            __uint_as_float(u[n].w << 16), __uint_as_float(u[n].w & 0xFFFF0000u));
+        }
+    };
+    load_rows(p.k, ks);
+    load_rows(p.q, qs);
     if (tid < 64) {
         const long long row = (row0 + tid) * H + h;
         Gx[tid] = ldin(p.g, row, p.in_bf16);   // raw gate until the cumsum
@@ -448,10 +466,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) chunk_grad_mma_kernel(ChunkGrad
     }
     __syncthreads();
     // ---- (10) q back into the tile region (T1 is dead)
-    for (int e = tid; e < 64 * KD; e += kMgThreads) {
-        const int i = e / KD, l = e % KD;
-        qs[i * KP + l] = ldin(p.q, ((row0 + i) * H + h) * KD + l, p.in_bf16);
-    }
+    load_rows(p.q, qs);
     __syncthreads();
     // ---- (11) dq = S' K + e^G dQd;  dk = S K + S^T K + S'^T Q + e^(Gn - G) dKd + e^Gx dKr;
     //      the gate terms of Qd and Kd
