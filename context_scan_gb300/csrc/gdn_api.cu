@@ -15,7 +15,11 @@ namespace {
 
 using gdn::ChainParams;
 
-constexpr size_t kHeaderBytes = 256;   // device error word lives here
+constexpr size_t kHeaderBytes = 256;   // device error word, then the WY queue counter
+constexpr size_t kQueueOffset = 64;    // the WY queue counter's offset in the header
+// the last piece's WY tiles are formed beside the first phase when they take at least this
+// many waves of the WY kernel's CTAs (six per SM) on the whole GPU
+constexpr int kTailMinWaves = 1;
 constexpr size_t kAlign = 256;
 constexpr int kMaxSub = 8;             // pieces per segment (segmented forward)
 constexpr int kMinPieceChunks = 8;     // shortest piece, in chunks
@@ -210,7 +214,8 @@ cudaError_t run_summary(const ChainParams& c, cudaStream_t s) {
 
 // The segmented forward on validated arguments (also gdn_chunk_fwd, nseg = 1): each sequence
 // is cut into P pieces (plan_pieces). Stage events: 0 before the WY tiles, 1 before the first
-// phase, 2 before the scan, 3 before the second phase, 4 at the end.
+// phase (which includes the last piece's WY tiles when they are formed beside it), 2 before the
+// scan, 3 before the second phase, 4 at the end.
 gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const void* k,
                          const void* v, const void* g, const void* beta, const float* h0, void* o,
                          float* h_final, float* H_in_out, void* workspace, cudaStream_t s,
@@ -258,14 +263,28 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
         }
         return c;
     };
-    // 0. the WY tiles of every chunk (tcgen05 path only)
+    // 0. the WY tiles (tcgen05 path only): of every chunk; or, when the first phase's chains
+    //    leave SMs free, of pieces 0..P-2 only -- the last piece's are formed on those SMs
+    //    beside the chains (a programmatic dependent of the first phase that hands its chunks
+    //    out from a counter), since only the second phase reads them
     if (mark(events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
     ChainParams cw = chain();
+    const int nchunks = p->T / gdn::kChunk;
+    const int last_lo = P >= 2 ? w.plan.first + (P - 2) * w.plan.rest : nchunks;
+    const int sms = sm_count();
+    const bool tail_beside = use_tc(cw) && P >= 2 && (long long)BH * (P - 1) < sms &&
+                             (long long)BH * (nchunks - last_lo) >= 6LL * kTailMinWaves * sms;
+    cw.wy_lo = 0;
+    cw.wy_cnt = tail_beside ? last_lo : 0;
+    unsigned* queue = reinterpret_cast<unsigned*>(wsb + kQueueOffset);
+    if (tail_beside && cudaMemsetAsync(queue, 0, sizeof(unsigned), s) != cudaSuccess)
+        return GDN_ERR_CUDA;
     cudaError_t e = prepare(cw, p, workspace, s);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     // 1. piece 0's forward from h0, which hands its final state to piece 1, beside the
-    //    summaries of pieces 1..P-2 (launched as its programmatic dependent, so they start
-    //    at once on the SMs it leaves free)
+    //    summaries of pieces 1..P-2 (one grid on the tensor-core path; otherwise the summaries
+    //    are launched as the forward's programmatic dependent, so they start at once on the
+    //    SMs it leaves free)
     if (mark(events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
     ChainParams f0 = chain();
     f0.wy = cw.wy;
@@ -275,7 +294,6 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
     f0.h_final = P == 1 ? h_final : nullptr;
     f0.h_out = P > 1 ? Hp : nullptr;
     f0.h_out_seg_stride = hstride;
-    if ((e = run_forward(f0, s)) != cudaSuccess) return GDN_ERR_CUDA;
     if (P >= 3) {
         ChainParams cs = chain();
         cs.wy = cw.wy;
@@ -283,8 +301,24 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
         cs.S = S;
         cs.seg_first = 1;
         cs.nseg_run = P - 2;
-        cs.launch_dependent = 1;
-        if ((e = run_summary(cs, s)) != cudaSuccess) return GDN_ERR_CUDA;
+        if (tail_beside) {
+            e = gdn::launch_tc_phase1(f0, cs, s);
+        } else {
+            cs.launch_dependent = 1;
+            e = run_forward(f0, s);
+            if (e == cudaSuccess) e = run_summary(cs, s);
+        }
+    } else {
+        e = run_forward(f0, s);
+    }
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    if (tail_beside) {
+        ChainParams ct = cw;
+        ct.wy_lo = last_lo;
+        ct.wy_cnt = nchunks - last_lo;
+        ct.wy_queue = queue;
+        ct.launch_dependent = 1;
+        if (gdn::launch_tc_wy(ct, s) != cudaSuccess) return GDN_ERR_CUDA;
     }
     // 2. the state entering every piece (and every segment)
     if (mark(events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;

@@ -68,6 +68,14 @@ struct ChainParams {
     // launch as the programmatic dependent of the preceding grid in the stream (the kernel
     // then finishes only after that grid has)
     int launch_dependent;
+    // WY tiles of the fixed-length batch: only chunks wy_lo .. wy_lo + wy_cnt - 1 of every
+    // (b, h) (wy_cnt = 0: wy_lo to the end)
+    int wy_lo, wy_cnt;
+    // WY tiles: when non-null, a grid of at most six CTAs per SM hands the chunks out one at
+    // a time from this counter (zeroed before the launch); with launch_dependent it is
+    // launched as the programmatic dependent of the preceding grid (and finishes only after
+    // that grid has)
+    unsigned* wy_queue;
     DeviceError* err;
 };
 
@@ -158,8 +166,11 @@ bool tc_supported(const ChainParams& p);
 bool tc_runtime_ok();   // the driver entry point that encodes tensor maps is available
 // a bounded wait that runs out on purpose (see gdn_selftest_wait_timeout)
 cudaError_t launch_wait_selftest(DeviceError* err, long long limit, unsigned tag, cudaStream_t s);
-cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // all chunks of every (b, h)
+cudaError_t launch_tc_wy(const ChainParams& p, cudaStream_t s);   // see wy_lo, wy_cnt, wy_queue
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s);
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s);
+// the first piece's forward (fwd) and the summaries beside it (sum) as one grid, whose CTAs let
+// a programmatic dependent start at once
+cudaError_t launch_tc_phase1(const ChainParams& fwd, const ChainParams& sum, cudaStream_t s);
 
 }  // namespace gdn

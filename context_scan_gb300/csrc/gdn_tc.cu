@@ -56,6 +56,7 @@
 // non-.aligned form: a group's leader warp diverges around its mbarrier poll. Every wait on
 // an mbarrier is bounded: on expiry the kernel records GDN_ERR_TIMEOUT in the device error
 // word, drains what it issued and frees tensor memory.
+#include <algorithm>
 #include <cstring>
 
 #include "gdn_tc_common.cuh"
@@ -203,7 +204,7 @@ __device__ __forceinline__ void pack_bar(int sg) {
 // VARLEN: the chains are the packed sequences of c.cu_seqlens (forward only); the
 // fixed-length instance has none of the end-of-sequence checks.
 template <bool SUMMARY, bool VARLEN, bool OUT_BF16>
-__global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant__ TcParams p) {
+__device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
     using L = Smem<SUMMARY>;
     using F = Cfg<SUMMARY>;
     constexpr int KST = L::KST, AST = L::AST, NUB = F::NUB, NSG = F::NSG;
@@ -222,7 +223,6 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 
     const ChainParams& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int chain = blockIdx.x;
     const int seg = c.seg_first + chain % c.nseg_run;
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
@@ -700,6 +700,8 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
 #undef warp_wait
 #undef pmma_wait
 #undef pwait
+    } else if (warp >= F::THREADS / 32) {
+        // warps of a wider launch (the forward's CTAs of the combined first-phase grid): idle
     } else if (SUMMARY && warp >= F::ISSUE_WARP0) {
         if constexpr (SUMMARY) {
         // ========================= state MMA issue (summary) =========================
@@ -1161,19 +1163,47 @@ __global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant_
     if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+template <bool SUMMARY, bool VARLEN, bool OUT_BF16>
+__global__ void __launch_bounds__(512, 1) tc_chain_kernel(const __grid_constant__ TcParams p) {
+    chain_body<SUMMARY, VARLEN, OUT_BF16>(p, blockIdx.x);
+}
+
+// The first phase of the segmented forward as one grid: CTAs 0 .. nf-1 run the first piece's
+// forward, the others the summaries of the pieces beside it. (The two kinds stay in contiguous
+// blocks of CTAs: alternated over the grid, they took twice as long, measured at the bench
+// workload.) Every CTA lets a programmatic dependent of the grid start at once (on the SMs the
+// chains leave free).
+struct TcPhase1Params {
+    TcParams f;
+    TcParams s;
+    int nf;
+};
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(512, 1) tc_phase1_kernel(const __grid_constant__ TcPhase1Params p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if ((int)blockIdx.x < p.nf) chain_body<false, false, OUT_BF16>(p.f, blockIdx.x);
+    else chain_body<true, false, false>(p.s, (int)blockIdx.x - p.nf);
+}
+
 // ------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------
 template <bool SUMMARY>
+bool make_params(const ChainParams& c, TcParams* tp) {
+    memset(tp, 0, sizeof(*tp));
+    tp->c = c;
+    tp->wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
+    if (!make_map(&tp->tm_k, c.k, c)) return false;
+    if (!SUMMARY && !make_map(&tp->tm_q, c.q, c)) return false;
+    return make_map(&tp->tm_v, c.v, c);
+}
+
+template <bool SUMMARY>
 cudaError_t launch(const ChainParams& c, cudaStream_t s) {
     if (!c.wy || (SUMMARY && c.cu_seqlens)) return cudaErrorInvalidValue;
     TcParams tp;
-    memset(&tp, 0, sizeof(tp));
-    tp.c = c;
-    tp.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
-    if (!make_map(&tp.tm_k, c.k, c)) return cudaErrorInvalidValue;
-    if (!SUMMARY && !make_map(&tp.tm_q, c.q, c)) return cudaErrorInvalidValue;
-    if (!make_map(&tp.tm_v, c.v, c)) return cudaErrorInvalidValue;
+    if (!make_params<SUMMARY>(c, &tp)) return cudaErrorInvalidValue;
     // one instance per output type and packing, so that each carries only its own store path
     void (*kern)(TcParams) = tc_chain_kernel<SUMMARY, false, false>;
     if constexpr (!SUMMARY) {
@@ -1202,6 +1232,24 @@ cudaError_t launch(const ChainParams& c, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tp);
+}
+
+cudaError_t launch_phase1(const ChainParams& f, const ChainParams& sm, cudaStream_t s) {
+    if (!f.wy || !sm.wy || f.cu_seqlens || sm.cu_seqlens) return cudaErrorInvalidValue;
+    TcPhase1Params pp;
+    if (!make_params<false>(f, &pp.f) || !make_params<true>(sm, &pp.s)) return cudaErrorInvalidValue;
+    const long long nf = (long long)f.B * f.H * f.nseg_run;
+    const long long ns = (long long)sm.B * sm.H * sm.nseg_run;
+    if (nf + ns >= (1LL << 31)) return cudaErrorInvalidValue;
+    pp.nf = (int)nf;
+    void (*kern)(TcPhase1Params) = f.out_bf16 ? tc_phase1_kernel<true> : tc_phase1_kernel<false>;
+    constexpr uint32_t bytes = std::max(Smem<false>::BYTES, Smem<true>::BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+    if (e != cudaSuccess) return e;
+    static_assert(Cfg<false>::THREADS <= Cfg<true>::THREADS, "the summary is the wider CTA");
+    kern<<<(unsigned)(nf + ns), Cfg<true>::THREADS, bytes, s>>>(pp);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -1243,5 +1291,8 @@ cudaError_t launch_wait_selftest(DeviceError* err, long long limit, unsigned tag
 
 cudaError_t launch_tc_forward(const ChainParams& p, cudaStream_t s) { return launch<false>(p, s); }
 cudaError_t launch_tc_summary(const ChainParams& p, cudaStream_t s) { return launch<true>(p, s); }
+cudaError_t launch_tc_phase1(const ChainParams& fwd, const ChainParams& sum, cudaStream_t s) {
+    return launch_phase1(fwd, sum, s);
+}
 
 }  // namespace gdn

@@ -25,6 +25,7 @@
 // of the inverse is scaled and written to global memory as bf16 as soon as it is final (blocks
 // above the diagonal as zeros). Six CTAs share an SM (64 tensor-memory columns each) and hide
 // each other's latencies; the two waits (the tile, K K^T) are bounded.
+#include <algorithm>
 #include <cstring>
 
 #include "gdn_tc_common.cuh"
@@ -70,6 +71,9 @@ struct WyParams {
     const int* cu_seqlens;   // varlen: packed sequences (null for the fixed-length batch)
     const int* cu_chunks;
     int nseq, total_chunks;   // varlen: total_chunks bounds the chunks (T/64 + nseq)
+    int wy_lo, wy_cnt;        // fixed length: chunks wy_lo .. wy_lo + wy_cnt - 1 of each (b, h)
+    unsigned* queue;          // wy_queue_kernel: the next chunk to hand out
+    unsigned items;           // chunks the launch covers
     DeviceError* err;
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
@@ -82,11 +86,64 @@ __device__ __forceinline__ uint4* out_chunk(uint8_t* tile, int row, int c) {
 // wait tags recorded in the device error word's detail field
 enum : unsigned { WTAG_TILE = 101, WTAG_KK = 102 };
 
-__global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant__ WyParams p) {
+// Per-CTA state of the WY kernels: shared-memory base, barriers and tensor memory.
+struct WyCta {
+    uint8_t* sm;
+    uint32_t base, bar_tile, bar_kk, tmem;
+    volatile int* abort_flag;
+};
+
+// Barriers and the 64 tensor-memory columns of a WY CTA (every thread calls this once).
+__device__ __forceinline__ WyCta wy_setup() {
     extern __shared__ uint8_t smem_raw[];
+    WyCta w;
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* sm = smem_raw + (base - raw);
+    w.base = (raw + 1023u) & ~1023u;
+    w.sm = smem_raw + (w.base - raw);
+    w.bar_tile = w.base + WY_BAR;
+    w.bar_kk = w.base + WY_BAR + 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(w.sm + WY_BAR + 16);
+    w.abort_flag = reinterpret_cast<volatile int*>(w.sm + WY_BAR + 20);
+    if (threadIdx.x == 0) {
+        mbar_init(w.bar_tile, 1);
+        mbar_init(w.bar_kk, 1);
+        *w.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (threadIdx.x < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         w.base + WY_BAR + 16),
+                     "r"(kWyTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    w.tmem = *tmem_slot;
+    return w;
+}
+
+__device__ __forceinline__ void wy_teardown(const WyCta& w) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(w.tmem),
+                     "r"(kWyTmemCols)
+                     : "memory");
+    }
+}
+
+// One chunk's pair of WY tiles. `ch` numbers the chunks the launch covers; `it` counts the
+// chunks this CTA has formed before (the barriers' phase). Every thread of the CTA calls it;
+// it ends with every thread past its last read of shared memory.
+__device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long long ch, uint32_t it) {
+    uint8_t* sm = w.sm;
+    const uint32_t base = w.base, bar_tile = w.bar_tile, bar_kk = w.bar_kk, tmem = w.tmem;
+    volatile int* abort_flag = w.abort_flag;
+    const uint32_t par = it & 1u;
     uint32_t* Lt = reinterpret_cast<uint32_t*>(sm + WY_LT);
     uint32_t* X = reinterpret_cast<uint32_t*>(sm + WY_X);
     float* Ld = reinterpret_cast<float*>(sm + WY_LD);
@@ -95,20 +152,19 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
     const float* G = sc + 64;
     const float* bet = sc + 128;
     const float* bekr = sc + 192;
-    const uint32_t bar_tile = base + WY_BAR, bar_kk = base + WY_BAR + 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + WY_BAR + 16);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + WY_BAR + 20);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long ch = blockIdx.x;   // (b*H + h) * (T/64) + n, or h * total_chunks + c (varlen)
     int h, valid = 64;                  // valid: tokens of the chunk inside its sequence
     long long row0;                     // flattened (b, t) of the chunk's first token
+    long long tile;                     // index of the chunk's tile pair in p.wy
     if (!p.cu_seqlens) {
+        // chunks wy_lo .. wy_lo + wy_cnt - 1 of every (b, h)
         const int nchunks = p.T / 64;
-        const int n = (int)(ch % nchunks);
-        const long long bh = ch / nchunks;
+        const long long bh = ch / p.wy_cnt;
+        const int n = p.wy_lo + (int)(ch % p.wy_cnt);
         h = (int)(bh % p.H);
         row0 = (bh / p.H) * p.T + (long long)n * 64;
+        tile = bh * nchunks + n;
     } else {
         h = (int)(ch / p.total_chunks);
         const int c = (int)(ch % p.total_chunks);
@@ -122,29 +178,17 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
         const int t0 = __ldg(p.cu_seqlens + lo) + 64 * n;
         row0 = t0;
         valid = min(64, __ldg(p.cu_seqlens + lo + 1) - t0);
+        tile = ch;
     }
-    uint8_t* out_b = p.wy + ch * 16384;   // A diag(beta)
-    uint8_t* out_g = out_b + 8192;        // A diag(beta 2^Gx)
+    uint8_t* out_b = p.wy + tile * 16384;   // A diag(beta)
+    uint8_t* out_g = out_b + 8192;          // A diag(beta 2^Gx)
 
-    // ---- the k tile (two 64-feature halves, 128-byte swizzle) by TMA; 64 columns of tensor
-    //      memory for K K^T
+    // ---- the k tile (two 64-feature halves, 128-byte swizzle) by TMA
     if (tid == 0) {
-        mbar_init(bar_tile, 1);
-        mbar_init(bar_kk, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        fence_proxy_async();
         mbar_arrive_expect_tx(bar_tile, 16384u);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
             tma_load_3d(base + WY_K + hf * 8192, &p.tm_k, bar_tile, hf * 64, h, (int)row0);
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         base + WY_BAR + 16),
-                     "r"(kWyTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     // ---- gates: cumulative sums in log2 units (two tokens per lane); tokens past the end of a
     //      varlen sequence get g = 0 and beta = 0, which makes them no-ops on the state
@@ -174,14 +218,13 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     // ---- K K^T (M = 128, N = 32 per group, bf16, fp32 accumulate): columns 0..31 with A
     //      starting at the tile (rows in lanes 0..63; lanes 64..127 unused), columns 32..63
     //      with A starting 64 rows before it (rows in lanes 64..127; lanes 0..63 unused), so
     //      each of the four warps reads its own quarter out of tensor memory
     bool issued = false;
-    if (tid == 0 && mbar_wait(bar_tile, 0, abort_flag, p.wait_limit, p.err, WTAG_TILE)) {
+    if (tid == 0 && mbar_wait(bar_tile, par, abort_flag, p.wait_limit, p.err, WTAG_TILE)) {
         tc_fence_after();
 #pragma unroll
         for (int k16 = 0; k16 < 8; ++k16) {
@@ -201,7 +244,7 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
     {
         const int i = 32 * (warp & 1) + lane, jb = 32 * (warp >> 1);
         const bool ok = __shfl_sync(0xffffffffu,
-                                    (int)mbar_wait(bar_kk, 0, abort_flag, p.wait_limit, p.err, WTAG_KK), 0) != 0;
+                                    (int)mbar_wait(bar_kk, par, abort_flag, p.wait_limit, p.err, WTAG_KK), 0) != 0;
         if (ok && warp != 2) {
             tc_fence_after();
             float kk[32];
@@ -233,19 +276,13 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
         tc_fence_before();
     }
     __syncthreads();
-    // tensor memory is read out: release it (after K K^T has retired, should a wait have given
-    // up) and let the tile's copy land before its memory is reused
-    if (tid == 0) {
-        if (issued) mbar_drain(bar_kk, 0, p.wait_limit);
-        if (*abort_flag) mbar_drain(bar_tile, 0, p.wait_limit);
+    // should a wait have given up, K K^T retires and the tile's copy lands before their memory
+    // is reused
+    if (tid == 0 && *abort_flag) {
+        if (issued) mbar_drain(bar_kk, par, p.wait_limit);
+        mbar_drain(bar_tile, par, p.wait_limit);
     }
     __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kWyTmemCols)
-                     : "memory");
-    }
 
     // ---- diagonal 16 x 16 blocks of (I + L)^-1 by forward substitution down the columns:
     //      warps 0 and 1 take two blocks each, lane (block, c) computes column c of its block,
@@ -352,6 +389,38 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
             *reinterpret_cast<uint32_t*>(out_g + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-xo[2] * e0, -xo[3] * e1);
         }
     }
+    // every warp is done with the tile, L and X before the next chunk's copy lands on them
+    fence_proxy_async();
+    __syncthreads();
+}
+
+// One CTA per chunk.
+__global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant__ WyParams p) {
+    const WyCta w = wy_setup();
+    wy_chunk(p, w, blockIdx.x, 0);
+    wy_teardown(w);
+}
+
+// Chunks handed out one at a time from p.queue (zeroed before the launch) to a grid of any
+// size: launched as the programmatic dependent of a chain grid, the CTAs that fit beside the
+// chains start at once and take chunks until none is left, and the rest start as the chains
+// finish. Every CTA then waits for the preceding grid, so that what follows in the stream sees
+// both grids complete.
+__global__ void __launch_bounds__(kWyThreads, 6) wy_queue_kernel(const __grid_constant__ WyParams p) {
+    const WyCta w = wy_setup();
+    volatile unsigned* slot = reinterpret_cast<volatile unsigned*>(w.sm + WY_BAR + 24);
+#pragma unroll 1
+    for (uint32_t it = 0;; ++it) {
+        if (threadIdx.x == 0) *slot = atomicAdd(p.queue, 1u);
+        __syncthreads();
+        const unsigned item = *slot;
+        const bool stop = item >= p.items || *w.abort_flag;
+        __syncthreads();   // every thread has read the slot (and the flag) before either changes
+        if (stop) break;
+        wy_chunk(p, w, item, it);
+    }
+    wy_teardown(w);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // varlen: chunk numbering of the packed sequences (a prefix sum over at most a few thousand
@@ -360,10 +429,13 @@ __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant
 
 cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     if (!c.wy) return cudaErrorInvalidValue;
-    const long long nblk = c.cu_seqlens ? (long long)c.H * c.total_chunks
-                                        : (long long)c.B * c.H * (c.T / kChunk);
+    const int nchunks = c.T / kChunk;
+    const int lo = c.cu_seqlens ? 0 : c.wy_lo;
+    const int cnt = c.cu_seqlens ? 0 : (c.wy_cnt > 0 ? c.wy_cnt : nchunks - lo);
+    if (!c.cu_seqlens && (lo < 0 || cnt < 0 || lo + cnt > nchunks)) return cudaErrorInvalidValue;
+    const long long nblk = c.cu_seqlens ? (long long)c.H * c.total_chunks : (long long)c.B * c.H * cnt;
     if (nblk == 0) return cudaSuccess;
-    if (nblk >= (1LL << 31)) return cudaErrorInvalidValue;
+    if (nblk >= (1LL << 31) || (c.wy_queue && c.cu_seqlens)) return cudaErrorInvalidValue;
     WyParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_k, c.k, c)) return cudaErrorInvalidValue;
@@ -377,13 +449,38 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     p.cu_chunks = c.cu_chunks;
     p.nseq = c.B;
     p.total_chunks = c.total_chunks;
+    p.wy_lo = lo;
+    p.wy_cnt = cnt;
+    p.queue = c.wy_queue;
+    p.items = (unsigned)nblk;
     p.err = c.err;
     p.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
-    cudaError_t e = cudaFuncSetAttribute(wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    void (*kern)(WyParams) = c.wy_queue ? wy_queue_kernel : wy_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kWySmem);
     if (e != cudaSuccess) return e;
-    wy_kernel<<<(unsigned)nblk, kWyThreads, kWySmem, s>>>(p);
-    return cudaGetLastError();
+    if (!c.wy_queue) {
+        wy_kernel<<<(unsigned)nblk, kWyThreads, kWySmem, s>>>(p);
+        return cudaGetLastError();
+    }
+    // as many CTAs as the whole GPU holds at once (six per SM), or fewer if there are fewer
+    // chunks; optionally launched as the programmatic dependent of the preceding grid
+    int sms = 0, dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const long long grid = std::min<long long>(nblk, 6LL * std::max(sms, 1));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kWyThreads);
+    cfg.dynamicSmemBytes = kWySmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c.launch_dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, wy_queue_kernel, p);
 }
 
 }  // namespace gdn
