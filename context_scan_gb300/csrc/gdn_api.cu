@@ -277,9 +277,9 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
     cw.wy_lo = 0;
     cw.wy_cnt = tail_beside ? last_lo : 0;
     unsigned* queue = reinterpret_cast<unsigned*>(wsb + kQueueOffset);
-    if (tail_beside && cudaMemsetAsync(queue, 0, sizeof(unsigned), s) != cudaSuccess)
-        return GDN_ERR_CUDA;
+    cw.wy_queue_reset = tail_beside ? queue : nullptr;   // zeroed by the first WY launch
     cudaError_t e = prepare(cw, p, workspace, s);
+    cw.wy_queue_reset = nullptr;
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     // 1. piece 0's forward from h0, which hands its final state to piece 1, beside the
     //    summaries of pieces 1..P-2 (one grid on the tensor-core path; otherwise the summaries

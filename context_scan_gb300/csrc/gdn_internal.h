@@ -76,6 +76,8 @@ struct ChainParams {
     // launched as the programmatic dependent of the preceding grid (and finishes only after
     // that grid has)
     unsigned* wy_queue;
+    // WY tiles, one CTA per chunk: a counter the launch zeroes for a later queue launch
+    unsigned* wy_queue_reset;
     DeviceError* err;
 };
 

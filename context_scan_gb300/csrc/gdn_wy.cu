@@ -73,6 +73,7 @@ struct WyParams {
     int nseq, total_chunks;   // varlen: total_chunks bounds the chunks (T/64 + nseq)
     int wy_lo, wy_cnt;        // fixed length: chunks wy_lo .. wy_lo + wy_cnt - 1 of each (b, h)
     unsigned* queue;          // wy_queue_kernel: the next chunk to hand out
+    unsigned* queue_reset;    // wy_kernel: a counter to zero for a later wy_queue_kernel launch
     unsigned items;           // chunks the launch covers
     DeviceError* err;
     long long wait_limit;   // SM clock cycles before a wait gives up
@@ -396,6 +397,7 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long
 
 // One CTA per chunk.
 __global__ void __launch_bounds__(kWyThreads, 6) wy_kernel(const __grid_constant__ WyParams p) {
+    if (p.queue_reset && blockIdx.x == 0 && threadIdx.x == 0) *p.queue_reset = 0u;
     const WyCta w = wy_setup();
     wy_chunk(p, w, blockIdx.x, 0);
     wy_teardown(w);
@@ -434,7 +436,9 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     const int cnt = c.cu_seqlens ? 0 : (c.wy_cnt > 0 ? c.wy_cnt : nchunks - lo);
     if (!c.cu_seqlens && (lo < 0 || cnt < 0 || lo + cnt > nchunks)) return cudaErrorInvalidValue;
     const long long nblk = c.cu_seqlens ? (long long)c.H * c.total_chunks : (long long)c.B * c.H * cnt;
-    if (nblk == 0) return cudaSuccess;
+    if (nblk == 0)
+        return c.wy_queue_reset ? cudaMemsetAsync(c.wy_queue_reset, 0, sizeof(unsigned), s)
+                                : cudaSuccess;
     if (nblk >= (1LL << 31) || (c.wy_queue && c.cu_seqlens)) return cudaErrorInvalidValue;
     WyParams p;
     memset(&p, 0, sizeof(p));
@@ -452,6 +456,7 @@ cudaError_t launch_tc_wy(const ChainParams& c, cudaStream_t s) {
     p.wy_lo = lo;
     p.wy_cnt = cnt;
     p.queue = c.wy_queue;
+    p.queue_reset = c.wy_queue_reset;
     p.items = (unsigned)nblk;
     p.err = c.err;
     p.wait_limit = 4000000000LL;   // ~2 s at GB300 clocks
