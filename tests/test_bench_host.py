@@ -90,6 +90,26 @@ def test_algorithmic_model_matches_hand_count():
     assert bench.launches_per_step(synth.WORKLOADS["single_seg_h16_t8k"], 1) == 2
 
 
+def test_wy_tail_rule_and_launch_count():
+    # the last piece's WY tiles go beside the first phase when that phase leaves SMs idle and
+    # the tiles fill at least one wave of WY CTAs (six per SM): the headline plan on 152 SMs
+    w = synth.WORKLOADS["cp4_b2_h32_t32k"]
+    plan = (3, 170, 171)
+    assert bench.wy_tail_beside(w, plan, 152)
+    # the first phase as one grid replaces its two launches, plus the WY grid for the tail
+    assert bench.launches_per_step(w, 3, plan, 152) == 5
+    # no idle SMs (128 chains on 128 SMs), or too few tiles (one 8K sequence of 16 heads)
+    assert not bench.wy_tail_beside(w, plan, 128)
+    w1 = synth.WORKLOADS["single_seg_h16_t8k"]
+    assert not bench.wy_tail_beside(w1, (8, 16, 16), 152)
+    # two pieces: the forward of piece 0 alone, then the tail's WY grid
+    w2 = synth.scaled(w, B=1, H=16)
+    assert bench.wy_tail_beside(w2, (2, 256, 256), 152)
+    assert bench.launches_per_step(w2, 2, (2, 256, 256), 152) == 5
+    # CUDA-core shapes never
+    assert not bench.wy_tail_beside(synth.WORKLOADS["tiny_f32_k64_cp4"], (4, 1, 1), 152)
+
+
 def test_literal_flow_model_matches_hand_count():
     # every segment's summary (k, v, g, beta over all tokens; M and S written), the scan
     # (3 summaries read, h0 read, 4 H_in written), the forward (every token; H_in read,
