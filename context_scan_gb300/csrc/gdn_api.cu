@@ -767,6 +767,9 @@ gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const void* q, co
     sg.in_bf16 = p->in_dtype == GDN_DTYPE_BF16;
     sg.do_bf16 = p->out_dtype == GDN_DTYPE_BF16;
     sg.decay_first = p->decay_first;
+    // on the tensor-core path the forward above left every chunk's WY tiles in the workspace:
+    // the state-gradient chains take A diag(beta exp(Gx)) from them instead of inverting
+    if (tc_shape(*p) && gdn::tc_runtime_ok()) sg.wy = wsb + layout(*p, 1).off_wy;
     if (P == 1) {
         // the chains of whole sequences fill at most one wave: one pass from dht (no summaries;
         // the stage events of the summaries and of the second pass mark empty stages)

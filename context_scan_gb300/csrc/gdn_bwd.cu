@@ -32,6 +32,17 @@ __device__ __forceinline__ float ld(const void* base, long long idx, int bf16) {
     return reinterpret_cast<const float*>(base)[idx];
 }
 
+// A prefetched element as loaded: fp32 bits, or the 16 bits of a bf16 in the high half -- the
+// conversion waits until the value is stored, so that the loads of the next chunk stay in
+// flight while the current one computes.
+__device__ __forceinline__ uint32_t ld_bits(const void* base, long long idx, int bf16) {
+    if (bf16) return (uint32_t)reinterpret_cast<const unsigned short*>(base)[idx];
+    return __float_as_uint(reinterpret_cast<const float*>(base)[idx]);
+}
+__device__ __forceinline__ float from_bits(uint32_t x, int bf16) {
+    return __uint_as_float(bf16 ? x << 16 : x);
+}
+
 template <int KD, int CT, bool MMA>
 struct BwdSmem {
     static constexpr int TP = 68;       // padded rows of the transposed k / q ([l][i]) and of
@@ -112,8 +123,14 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
     // four tokens of a quad land in one float4 of the transposed copies, so those stores are
     // free of bank conflicts -- and ND elements of the dO tile.
     constexpr int NKQ = 16 * KD / kThreads, ND = 64 * CT / kThreads;
-    float pk[NKQ][4], pq[NKQ][4], pd[ND], pg = 0.f, pb = 0.f;
+    uint32_t pk[NKQ][4], pq[NKQ][4], pd[ND], pg = 0u, pb = 0u;
+    uint4 pa[2];   // (with the WY tiles) this thread's two 16-byte pieces of A diag(beta 2^Gx)
     const long long row0 = (long long)b * p.T + (long long)seg * p.seg_len;
+    const bool use_wy = MMA && p.wy != nullptr;
+    const uint8_t* wy_head = use_wy ? reinterpret_cast<const uint8_t*>(p.wy) +
+                                          (((long long)bh * (p.T / kChunk) +
+                                            (long long)seg * (p.seg_len / kChunk)) << 14) + 8192
+                                    : nullptr;
     auto prefetch = [&](int ch) {
         const long long r0 = row0 + (long long)ch * kChunk;
 #pragma unroll
@@ -122,19 +139,24 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const long long idx = ((r0 + i4 + r) * H + h) * KD + l;
-                pk[n][r] = ld(p.k, idx, p.in_bf16);
-                pq[n][r] = ld(p.q, idx, p.in_bf16);
+                pk[n][r] = ld_bits(p.k, idx, p.in_bf16);
+                pq[n][r] = ld_bits(p.q, idx, p.in_bf16);
             }
         }
 #pragma unroll
         for (int n = 0; n < ND; ++n) {
             const int e = tid + n * kThreads, i = e / CT, c = e % CT;
-            pd[n] = ld(p.dO, ((r0 + i) * H + h) * V + c0 + c, p.do_bf16);
+            pd[n] = ld_bits(p.dO, ((r0 + i) * H + h) * V + c0 + c, p.do_bf16);
         }
         if (tid < 64) {
             const long long row = (r0 + tid) * H + h;
-            pg = ld(p.g, row, p.in_bf16);
-            pb = ld(p.beta, row, p.in_bf16);
+            pg = ld_bits(p.g, row, p.in_bf16);
+            pb = ld_bits(p.beta, row, p.in_bf16);
+        }
+        if (use_wy) {
+            const uint4* t = reinterpret_cast<const uint4*>(wy_head + ((long long)ch << 14));
+            pa[0] = t[tid];
+            pa[1] = t[tid + kThreads];
         }
     };
     const int n_chunks = p.seg_len / kChunk;
@@ -145,24 +167,44 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
 #pragma unroll
         for (int n = 0; n < NKQ; ++n) {
             const int e = tid + n * kThreads, l = e % KD, i4 = (e / KD) * 4;
+            float kv4[4], qv4[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                kv4[r] = from_bits(pk[n][r], p.in_bf16);
+                qv4[r] = from_bits(pq[n][r], p.in_bf16);
+            }
             if constexpr (!MMA) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    kr[(i4 + r) * KD + l] = pk[n][r];
-                    qr[(i4 + r) * KD + l] = pq[n][r];
+                    kr[(i4 + r) * KD + l] = kv4[r];
+                    qr[(i4 + r) * KD + l] = qv4[r];
                 }
             }
-            st4(&kt[l * TP + i4], make_float4(pk[n][0], pk[n][1], pk[n][2], pk[n][3]));
-            st4(&qt[l * TP + i4], make_float4(pq[n][0], pq[n][1], pq[n][2], pq[n][3]));
+            st4(&kt[l * TP + i4], make_float4(kv4[0], kv4[1], kv4[2], kv4[3]));
+            st4(&qt[l * TP + i4], make_float4(qv4[0], qv4[1], qv4[2], qv4[3]));
         }
 #pragma unroll
         for (int n = 0; n < ND; ++n) {
             const int e = tid + n * kThreads;
-            dos[(e / CT) * DP + e % CT] = pd[n];
+            dos[(e / CT) * DP + e % CT] = from_bits(pd[n], p.do_bf16);
         }
         if (tid < 64) {
-            gx[tid] = pg;   // raw gate until the cumsum
-            bet[tid] = pb;
+            gx[tid] = from_bits(pg, p.in_bf16);   // raw gate until the cumsum
+            bet[tid] = from_bits(pb, p.in_bf16);
+        }
+        if (use_wy) {
+            // A diag(beta 2^Gx) from its bf16 tile: 16-byte piece e of the tile is row e / 8,
+            // columns 8 ((e % 8) ^ (row % 8)) .. + 7 (the 128-byte swizzle)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int e = tid + r * kThreads, row = e >> 3, cb = 8 * ((e & 7) ^ (row & 7));
+                const uint32_t w4[4] = {pa[r].x, pa[r].y, pa[r].z, pa[r].w};
+                float* dst = As + row * TP + cb;
+                st4(dst, make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xFFFF0000u),
+                                     __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xFFFF0000u)));
+                st4(dst + 4, make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xFFFF0000u),
+                                         __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xFFFF0000u)));
+            }
         }
         __syncthreads();
         if (ch > 0) prefetch(ch - 1);
@@ -203,12 +245,14 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             float sq[1][4][4] = {}, sk[1][4][4] = {};
             wtile<1, 4>(sq, m64, n64, KD, lane, [&](int i, int l) { return qt[l * TP + i]; },
                         [&](int l, int j) { return kt[l * TP + j]; });
-            wtile<1, 4>(sk, m64, n64, KD, lane, [&](int i, int l) { return kt[l * TP + i]; },
-                        [&](int l, int j) { return kt[l * TP + j]; });
-            wtile_each<1, 4>(sk, m64, n64, lane, [&](int i, int j, float& v) {
-                Ls[i * TP + j] = (j < i) ? bet[i] * expf(gx[i] - gam[j]) * v : 0.f;
-                As[i * TP + j] = 0.f;
-            });
+            if (!use_wy) {
+                wtile<1, 4>(sk, m64, n64, KD, lane, [&](int i, int l) { return kt[l * TP + i]; },
+                            [&](int l, int j) { return kt[l * TP + j]; });
+                wtile_each<1, 4>(sk, m64, n64, lane, [&](int i, int j, float& v) {
+                    Ls[i * TP + j] = (j < i) ? bet[i] * expf(gx[i] - gam[j]) * v : 0.f;
+                    As[i * TP + j] = 0.f;
+                });
+            }
             wtile_each<1, 4>(sq, m64, n64, lane, [&](int i, int j, float& v) {
                 Cs[i * TP + j] = (j <= i) ? expf(gam[i] - gam[j]) * v : 0.f;
             });
@@ -248,7 +292,8 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
         }
         __syncthreads();
         // ---- (4a) inverses of the four 16 x 16 diagonal blocks of I + L (forward substitution)
-        if (tid < 64) {
+        //      (with the WY tiles, A diag(beta exp(Gx)) came with the chunk: steps 4a, 4b skipped)
+        if (!use_wy && tid < 64) {
             const int base = (tid / 16) * 16, c = tid % 16;
             float x[16];
 #pragma unroll
@@ -265,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
         }
         __syncthreads();
         // ---- (4b) off-diagonal blocks: A_IJ = -inv(T_II) sum_{m=J}^{I-1} L_Im A_mJ
-        {
+        if (!use_wy) {
             float* Yb = Zs;   // 3 blocks of 16 x 16 scratch (Zs is free until step 6)
             const int r = tid / 16, c = tid % 16;
             for (int I = 1; I < 4; ++I) {
@@ -310,7 +355,9 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
                 float z[1][NT][4] = {};
                 wtile<1, NT>(z, mr, nr, 64, lane, [&](int j, int i) { return As[i * TP + j]; },
                              [&](int i, int c) { return Rs[i * DP + c]; });
-                wtile_each<1, NT>(z, mr, nr, lane, [&](int j, int c, float& v) { Zs[j * DP + c] = ekr[j] * v; });
+                // (the WY tile is A diag(beta exp(Gx)) already)
+                wtile_each<1, NT>(z, mr, nr, lane,
+                                  [&](int j, int c, float& v) { Zs[j * DP + c] = (use_wy ? 1.f : ekr[j]) * v; });
             }
             __syncthreads();
             // ---- (7) D = exp(G_last) D' + Qd^T dO - K^T Z: K x CT, (16 K / 64) x CT/2 per warp

@@ -126,6 +126,10 @@ struct StateGradParams {
     // when non-null, the gradient on the state leaving every chunk c (counted over the whole
     // sequence) is written to D_chunks + c*B*H*K*V + (b*H + h)*K*V ([T/64][B][H][K][V])
     float* D_chunks;
+    // bf16 inputs with K == V == 128: when non-null, the forward's per-chunk WY tiles
+    // ([B*H][T/64][A diag(beta) | A diag(beta 2^Gx)], bf16 64 x 64 in the chain kernels'
+    // swizzled layout), whose second factor replaces the kernel's own inverse
+    const void* wy;
     int B, T, H, K, V;
     int seg_len, nseg;
     int in_bf16, do_bf16, decay_first;
