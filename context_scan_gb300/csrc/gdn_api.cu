@@ -45,6 +45,15 @@ bool tc_shape(const gdn_problem& p) {
     return p.in_dtype == GDN_DTYPE_BF16 && p.K == 128 && p.V == 128 && !p.gate_k;
 }
 
+// Per-channel gates at bf16 inputs: the chains read every chunk's A diag(beta) and C, formed
+// beforehand.
+bool kda_prep_shape(const gdn_problem& p) { return p.in_dtype == GDN_DTYPE_BF16 && p.gate_k; }
+
+// bytes of per-chunk factors the chains read, per chunk and head
+size_t chunk_factor_bytes(const gdn_problem& p) {
+    return tc_shape(p) ? 16384u : (kda_prep_shape(p) ? 2u * 64u * 64u * sizeof(float) : 0u);
+}
+
 // Device properties asked on every call, looked up once per device (a call on a short
 // problem would otherwise spend a visible part of its time in these queries).
 constexpr int kMaxDevices = 64;
@@ -121,7 +130,7 @@ WsLayout layout(const gdn_problem& p, int nseg) {
     w.plan = plan_pieces(p, nseg);
     w.pieces = w.plan.P;
     w.off_wy = kHeaderBytes;
-    const size_t wy_bytes = tc_shape(p) ? bh * (size_t)(p.T / gdn::kChunk) * 16384u : 0;
+    const size_t wy_bytes = bh * (size_t)(p.T / gdn::kChunk) * chunk_factor_bytes(p);
     w.off_M = w.off_wy + round_up(wy_bytes);
     const size_t P = (size_t)w.pieces;
     const size_t m_bytes = P >= 3 ? round_up(sizeof(float) * P * bh * p.K * p.K) : 0;
@@ -201,7 +210,9 @@ bool use_tc(const ChainParams& c) { return c.T > 0 && gdn::tc_supported(c); }
 // launch for all chunks of the problem). Nothing to do on the CUDA-core path.
 cudaError_t prepare(ChainParams& c, const gdn_problem* p, void* ws, cudaStream_t s) {
     c.wy = reinterpret_cast<char*>(ws) + layout(*p, 1).off_wy;
-    return use_tc(c) ? gdn::launch_tc_wy(c, s) : cudaSuccess;
+    if (use_tc(c)) return gdn::launch_tc_wy(c, s);
+    if (kda_prep_shape(*p) && p->T > 0) return gdn::launch_kda_prep(c, s);
+    return cudaSuccess;
 }
 
 cudaError_t run_forward(const ChainParams& c, cudaStream_t s) {
@@ -357,7 +368,7 @@ VarlenLayout varlen_layout(const gdn_problem& p, int nseq) {
     VarlenLayout w{};
     w.chunk_bound = p.T / gdn::kChunk + nseq;
     w.off_wy = kHeaderBytes;
-    const size_t wy_bytes = tc_shape(p) ? (size_t)p.H * (size_t)w.chunk_bound * 16384u : 0;
+    const size_t wy_bytes = (size_t)p.H * (size_t)w.chunk_bound * chunk_factor_bytes(p);
     w.off_cu = w.off_wy + round_up(wy_bytes);
     w.off_cc = w.off_cu + round_up(sizeof(int) * ((size_t)nseq + 1));
     w.total = w.off_cc + round_up(sizeof(int) * ((size_t)nseq + 1));
@@ -641,6 +652,8 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     c.wy = wsb + w.off_wy;
     const bool tc = use_tc(c) && p->T >= gdn::kChunk;   // (a tensor map box holds 64 tokens)
     if (tc && gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (kda_prep_shape(*p) && p->T > 0 && gdn::launch_kda_prep(c, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
     if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
     if ((tc ? gdn::launch_tc_forward(c, s) : gdn::launch_simt_forward(c, s)) != cudaSuccess)
         return GDN_ERR_CUDA;

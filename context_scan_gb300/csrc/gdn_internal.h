@@ -34,7 +34,8 @@ struct ChainParams {
     float* M;          // summary: [nseg_total,B,H,K,K]
     float* S;          // summary: [nseg_total,B,H,K,V]
     // tcgen05 path: per-chunk WY factors, [B*H][T/64][A diag(beta) | A diag(beta 2^Gx)], each
-    // a bf16 64 x 64 tile in the chain kernels' swizzled operand layout (8192 bytes)
+    // a bf16 64 x 64 tile in the chain kernels' swizzled operand layout (8192 bytes); per-channel
+    // gates at bf16 inputs: [B*H][T/64][A diag(beta) | C], fp32 64 x 64 row-major
     void* wy;
     int B, T, H, K, V;
     int seg_len;       // tokens per segment (multiple of 64)
@@ -87,6 +88,9 @@ cudaError_t launch_simt_summary(const ChainParams& p, cudaStream_t s);
 // per-channel gates (gate_k) with bf16 inputs: the chains by sub-block normalisation with their
 // products on the warp-level tensor cores (routed from the two launchers above)
 cudaError_t launch_kda_mma_chain(const ChainParams& p, bool summary, cudaStream_t s);
+// ... whose per-chunk factors A diag(beta) and C ([chunk][2][64][64] fp32 at p.wy, chunks
+// numbered as the WY tiles) this forms beforehand, one CTA per chunk
+cudaError_t launch_kda_prep(const ChainParams& p, cudaStream_t s);
 // In-order scan over consecutive pieces p_first .. P-1 of every (b, h): the state entering
 // piece p_first is h_first ([BH][K][V], or zero when null); entering piece p+1 it is
 // M[p] H + S[p] (M, S indexed by piece, [piece][BH][K][K|V]). The state entering every piece
