@@ -66,20 +66,23 @@ __device__ __forceinline__ void put8(float* dst, uint4 u) {
 // ---- the per-chunk factors: A diag(beta) and C -------------------------------------------
 template <int KD>
 struct PrepSmem {
-    static constexpr int KP = KD + 4;   // row pitch of k, q, G (4 mod 32 words)
+    static constexpr int KPB = KD + 8;  // row pitch (bf16 elements) of k and q: 4 mod 32 words
+    static constexpr int KP = KD + 4;   // row pitch of G (4 mod 32 words)
     static constexpr int LP = 68;       // row pitch of the 64 x 64 matrices
-    static constexpr int QSZ = 64 * KP > 64 * LP + 3 * 256 ? 64 * KP : 64 * LP + 3 * 256;
-    static constexpr int k = 0;                        // k [64][KP]
-    static constexpr int q = k + 64 * KP;              // q [64][KP]; then A [64][LP] and the
-                                                       // inverse's scratch (3 x 256)
-    static constexpr int gk = q + QSZ;                 // cumulative gates G [64][KP]
+    // k and q as bf16 (as loaded); once L and C are formed, A [64][LP] and the inverse's
+    // scratch (3 x 256) take their place
+    static constexpr int KQ = 64 * KPB;   // floats of the k and q rows together
+    static constexpr int KQSZ = KQ > 64 * LP + 3 * 256 ? KQ : 64 * LP + 3 * 256;
+    static constexpr int kq = 0;
+    static constexpr int gk = kq + KQSZ;               // cumulative gates G [64][KP]
     static constexpr int l = gk + 64 * KP;             // L [64][LP]
     static constexpr int c = l + 64 * LP;              // C [64][LP]
     static constexpr int bet = c + 64 * LP;            // beta [64]
     static constexpr int ref = bet + 64;               // block references [4][KD]
     static constexpr int total = ref + 4 * KD;
     static constexpr size_t bytes = sizeof(float) * total;
-    static_assert(bytes <= 232448, "shared memory budget");
+    // two CTAs per SM
+    static_assert(2 * (bytes + 1024) <= 233472, "shared memory budget: two CTAs per SM");
 };
 
 // One CTA per chunk: the chunk's per-channel cumulative gates, L and C by sub-block
@@ -89,18 +92,20 @@ struct PrepSmem {
 // h*total_chunks + cu_chunks[b] + n for packed sequences (tokens past a sequence's end load as
 // zeros with g = beta = 0).
 template <int KD>
-__global__ void __launch_bounds__(kKdaThreads, 1) kda_prep_kernel(ChainParams p, float* out) {
+__global__ void __launch_bounds__(kKdaThreads, 2) kda_prep_kernel(ChainParams p, float* out) {
     using L = PrepSmem<KD>;
-    constexpr int KP = L::KP, LP = L::LP;
+    constexpr int KP = L::KP, LP = L::LP, KPB = L::KPB;
     extern __shared__ float4 smv[];
     float* sm = reinterpret_cast<float*>(smv);
-    float* ks = sm + L::k;
-    float* qs = sm + L::q;
+    unsigned short* kb16 = reinterpret_cast<unsigned short*>(sm + L::kq);
+    unsigned short* qb16 = kb16 + 64 * KPB;
+    auto kf = [&](int i, int l) { return __uint_as_float((uint32_t)kb16[i * KPB + l] << 16); };
+    auto qf = [&](int i, int l) { return __uint_as_float((uint32_t)qb16[i * KPB + l] << 16); };
     float* Gk = sm + L::gk;
     float* Ls = sm + L::l;
     float* Cs = sm + L::c;
-    float* As = qs;                  // (once L and C are formed)
-    float* Yb = qs + 64 * LP;        // the inverse's scratch
+    float* As = sm + L::kq;          // (once L and C are formed)
+    float* Yb = As + 64 * LP;        // the inverse's scratch
     float* bet = sm + L::bet;
     float* ref = sm + L::ref;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -147,8 +152,8 @@ __global__ void __launch_bounds__(kKdaThreads, 1) kda_prep_kernel(ChainParams p,
 #pragma unroll
         for (int n = 0; n < NKV; ++n) {
             const int e = tid + n * kKdaThreads, i = e / (KD / 8), l8 = 8 * (e % (KD / 8));
-            put8(ks + i * KP + l8, uk[n]);
-            put8(qs + i * KP + l8, uq[n]);
+            *reinterpret_cast<uint4*>(kb16 + i * KPB + l8) = uk[n];
+            *reinterpret_cast<uint4*>(qb16 + i * KPB + l8) = uq[n];
             put8(Gk + i * KP + l8, ug[n]);
         }
         if (tid < 64) bet[tid] = bt;
@@ -183,14 +188,14 @@ __global__ void __launch_bounds__(kKdaThreads, 1) kda_prep_kernel(ChainParams p,
         const float* rf = ref + I * KD;
         float acc[1][8][4] = {};
         auto fb = [&](int l, int j) {   // the chunk's keys against reference I
-            return ks[j * KP + l] * __expf(fminf(rf[l] - Gk[j * KP + l], kSpreadMax));
+            return kf(j, l) * __expf(fminf(rf[l] - Gk[j * KP + l], kSpreadMax));
         };
         if (prod == 0)
             wtile<1, 8>(acc, 16 * I, 0, KD, lane,
-                        [&](int i, int l) { return ks[i * KP + l] * __expf(gread(i, l) - rf[l]); }, fb);
+                        [&](int i, int l) { return kf(i, l) * __expf(gread(i, l) - rf[l]); }, fb);
         else
             wtile<1, 8>(acc, 16 * I, 0, KD, lane,
-                        [&](int i, int l) { return qs[i * KP + l] * __expf(Gk[i * KP + l] - rf[l]); }, fb);
+                        [&](int i, int l) { return qf(i, l) * __expf(Gk[i * KP + l] - rf[l]); }, fb);
         if (prod == 0) {
             wtile_each<1, 8>(acc, 16 * I, 0, lane, [&](int i, int j, float& v) {
                 Ls[i * LP + j] = (j < i) ? bet[i] * v : 0.f;
@@ -213,12 +218,12 @@ __global__ void __launch_bounds__(kKdaThreads, 1) kda_prep_kernel(ChainParams p,
                 float lv = 0.f, cv = 0.f;
                 if (j < i) {
                     for (int l = 0; l < KD; ++l)
-                        lv = fmaf(ks[i * KP + l] * ks[j * KP + l], __expf(gread(i, l) - Gk[j * KP + l]), lv);
+                        lv = fmaf(kf(i, l) * kf(j, l), __expf(gread(i, l) - Gk[j * KP + l]), lv);
                     lv *= bet[i];
                 }
                 if (j <= i)
                     for (int l = 0; l < KD; ++l)
-                        cv = fmaf(qs[i * KP + l] * ks[j * KP + l], __expf(Gk[i * KP + l] - Gk[j * KP + l]), cv);
+                        cv = fmaf(qf(i, l) * kf(j, l), __expf(Gk[i * KP + l] - Gk[j * KP + l]), cv);
                 Ls[i * LP + j] = lv;
                 Cs[i * LP + j] = cv;
             }
