@@ -219,13 +219,15 @@ def wy_tail_beside(w, plan, sms):
 
 
 def launches_per_step(w, pieces=None, plan=None, sms=None):
-    """Kernels one gdn_segmented_fwd call launches: WY factors (tensor-core path), piece 0's
-    forward, the piece summaries (3 pieces or more), the scan and the second forward (2 pieces
-    or more). When the last piece's WY tiles are formed beside the first phase, that phase is
+    """Kernels one gdn_segmented_fwd call launches: WY factors (tensor-core path) or the
+    per-channel-gate pre-pass, piece 0's forward, the piece summaries (3 pieces or more), the
+    scan and the second forward (2 pieces or more). When the last piece's WY tiles are formed beside the first phase, that phase is
     one grid (forward and summaries) followed by the WY grid for the last piece."""
     P = pieces or w.nseg
     tc = int(w.in_dtype == "bf16" and w.K == 128 and w.V == 128 and not w.gate_k)
-    n = tc + 1 + (1 if P >= 3 else 0) + (2 if P >= 2 else 0)
+    # per-channel gates at bf16 inputs: the per-chunk factors' pre-pass, as the WY launch
+    prep = int(w.in_dtype == "bf16" and bool(w.gate_k))
+    n = tc + prep + 1 + (1 if P >= 3 else 0) + (2 if P >= 2 else 0)
     if plan is not None and wy_tail_beside(w, plan, sms):
         n += 0 if P >= 3 else 1
     return n

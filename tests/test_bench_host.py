@@ -108,6 +108,9 @@ def test_wy_tail_rule_and_launch_count():
     assert bench.launches_per_step(w2, 2, (2, 256, 256), 152) == 5
     # CUDA-core shapes never
     assert not bench.wy_tail_beside(synth.WORKLOADS["tiny_f32_k64_cp4"], (4, 1, 1), 152)
+    # per-channel gates at bf16 inputs: the pre-pass, piece 0's forward, the summaries, the scan
+    # and the second forward
+    assert bench.launches_per_step(synth.WORKLOADS["kda_h16_t8k"], 8) == 5
 
 
 def test_literal_flow_model_matches_hand_count():
