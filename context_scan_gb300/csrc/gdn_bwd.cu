@@ -249,12 +249,12 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
                 wtile<1, 4>(sk, m64, n64, KD, lane, [&](int i, int l) { return kt[l * TP + i]; },
                             [&](int l, int j) { return kt[l * TP + j]; });
                 wtile_each<1, 4>(sk, m64, n64, lane, [&](int i, int j, float& v) {
-                    Ls[i * TP + j] = (j < i) ? bet[i] * expf(gx[i] - gam[j]) * v : 0.f;
+                    Ls[i * TP + j] = (j < i) ? bet[i] * __expf(gx[i] - gam[j]) * v : 0.f;
                     As[i * TP + j] = 0.f;
                 });
             }
             wtile_each<1, 4>(sq, m64, n64, lane, [&](int i, int j, float& v) {
-                Cs[i * TP + j] = (j <= i) ? expf(gam[i] - gam[j]) * v : 0.f;
+                Cs[i * TP + j] = (j <= i) ? __expf(gam[i] - gam[j]) * v : 0.f;
             });
         } else {
             const int i0 = (tid / 16) * 4, j0 = (tid % 16) * 4;
