@@ -81,8 +81,10 @@ int sm_count() {
 //    chunks and pieces 1..P-1 of x chunks, x = chunks / (P - 1 + kSumRatio), so that piece 0's
 //    forward and the summaries end together: max(L0, kSumRatio x) + x + 3 * (P - 2). The
 //    forward kernels then write the states entering the segments as they pass them.
-// Without a device to size the waves it stays at nseg equal pieces.
-constexpr double kSumRatio = 1.0;
+// Without a device to size the waves it stays at nseg equal pieces. kSumRatio is the measured
+// per-chunk time of the first phase's summary chains over its forward chain (per-CTA clock
+// stamps at B2 H32 T32K: 2.46 against 2.51 us).
+constexpr double kSumRatio = 0.98;
 
 PiecePlan plan_pieces(const gdn_problem& p, int nseg) {
     const int chunks = p.T / gdn::kChunk;   // a multiple of nseg (checked)
