@@ -298,6 +298,32 @@ def test_full_size_sampled_heads(name):
         assert rel_err(np64(hin[:, b:b + 1, h:h + 1]), hin_ref, label=f"H_in {b},{h}") <= TOL_BF16, (b, h)
 
 
+def test_last_piece_wy_tiles_beside_the_first_phase():
+    # the schedule the headline runs, at a quarter of its length: the first phase leaves SMs
+    # idle, so the last piece's WY tiles are formed there by a grid that takes chunks from a
+    # counter while the chains run. Checked on sampled heads against the oracle, with the state
+    # entering every segment, and bit for bit from one call to the next (the order in which the
+    # chunks are taken varies; each tile does not)
+    import bench
+    w = synth.scaled(W["cp4_b2_h32_t32k"], T=8192)
+    pc = gdn.Problem(w.B, w.T, w.H, 128, 128, 64, gdn.GDN_DTYPE_BF16, gdn.GDN_DTYPE_F32)
+    plan = gdn.segmented_plan(pc, w.nseg)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert bench.wy_tail_beside(w, plan, sms), (plan, sms)
+    x = synth.make_inputs(w)
+    d = upload(x, w)
+    runs = [run_segmented(w, d) for _ in range(2)]
+    for a, b in zip(runs[0], runs[1]):
+        assert torch.equal(a, b)
+    o, hf, hin = runs[0]
+    for b, h in ((0, 0), (0, w.H - 1), (1, w.H // 2), (w.B - 1, w.H - 1)):
+        xs = head_slice(x, b, h)
+        o_ref, hf_ref, hin_ref = oracle_ref(xs, w.seg_len, col_block=16)
+        assert rel_err(np64(o[b:b + 1, :, h:h + 1]), o_ref, label=f"o {b},{h}") <= TOL_BF16, (b, h)
+        assert rel_err(np64(hf[b:b + 1, h:h + 1]), hf_ref, label=f"h_final {b},{h}") <= TOL_BF16, (b, h)
+        assert rel_err(np64(hin[:, b:b + 1, h:h + 1]), hin_ref, label=f"H_in {b},{h}") <= TOL_BF16, (b, h)
+
+
 def test_uneven_pieces_h_in_guard_bands_bf16_and_determinism():
     # few chains on many SMs: the sequences are cut into unequal pieces whose starts are not
     # segment starts, and the forward chains write H_in as they pass the segment starts. Each
