@@ -208,14 +208,17 @@ def literal_algorithmic(w, out_bytes: int = 4):
 
 def wy_tail_beside(w, plan, sms):
     """The library's rule: the last piece's WY tiles are formed beside the first phase when
-    that phase leaves SMs idle and those tiles take at least one wave of WY CTAs (six per SM)."""
+    that phase leaves at least 8 SMs idle in its last wave (its only one, if it fits one) and
+    those tiles take at least one wave of WY CTAs (six per SM)."""
     P, first, rest = plan
     tc = w.in_dtype == "bf16" and w.K == 128 and w.V == 128 and not w.gate_k
     if not tc or P < 2 or w.T == 0 or not sms:
         return False
     bh = w.B * w.H
     last_lo = first + (P - 2) * rest
-    return bh * (P - 1) < sms and bh * (w.T // 64 - last_lo) >= 6 * sms
+    chains1 = bh * (P - 1)
+    idle1 = sms - chains1 % sms if chains1 % sms else 0
+    return idle1 >= 8 and bh * (w.T // 64 - last_lo) >= 6 * sms
 
 
 def launches_per_step(w, pieces=None, plan=None, sms=None):

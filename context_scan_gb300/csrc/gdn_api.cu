@@ -18,8 +18,10 @@ using gdn::ChainParams;
 constexpr size_t kHeaderBytes = 256;   // device error word, then the WY queue counter
 constexpr size_t kQueueOffset = 64;    // the WY queue counter's offset in the header
 // the last piece's WY tiles are formed beside the first phase when they take at least this
-// many waves of the WY kernel's CTAs (six per SM) on the whole GPU
+// many waves of the WY kernel's CTAs (six per SM) on the whole GPU, and the first phase leaves
+// at least this many SMs idle in its last wave
 constexpr int kTailMinWaves = 1;
+constexpr int kTailMinIdle = 8;
 constexpr size_t kAlign = 256;
 constexpr int kMaxSub = 8;             // pieces per segment (segmented forward)
 constexpr int kMinPieceChunks = 8;     // shortest piece, in chunks
@@ -277,15 +279,19 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
         return c;
     };
     // 0. the WY tiles (tcgen05 path only): of every chunk; or, when the first phase's chains
-    //    leave SMs free, of pieces 0..P-2 only -- the last piece's are formed on those SMs
-    //    beside the chains (a programmatic dependent of the first phase that hands its chunks
-    //    out from a counter), since only the second phase reads them
+    //    leave SMs free (in its only wave, or in its last), of pieces 0..P-2 only -- the last
+    //    piece's are formed on those SMs beside the chains (a programmatic dependent of the
+    //    first phase that hands its chunks out from a counter), since only the second phase
+    //    reads them
     if (mark(events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
     ChainParams cw = chain();
     const int nchunks = p->T / gdn::kChunk;
     const int last_lo = P >= 2 ? w.plan.first + (P - 2) * w.plan.rest : nchunks;
     const int sms = sm_count();
-    const bool tail_beside = use_tc(cw) && P >= 2 && (long long)BH * (P - 1) < sms &&
+    // SMs the first phase leaves idle in its last wave (all of its chains when they fit one)
+    const long long chains1 = (long long)BH * (P - 1);
+    const long long idle1 = sms > 0 && chains1 % sms != 0 ? sms - chains1 % sms : 0;
+    const bool tail_beside = use_tc(cw) && P >= 2 && idle1 >= kTailMinIdle &&
                              (long long)BH * (nchunks - last_lo) >= 6LL * kTailMinWaves * sms;
     cw.wy_lo = 0;
     cw.wy_cnt = tail_beside ? last_lo : 0;

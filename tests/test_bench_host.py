@@ -100,6 +100,12 @@ def test_wy_tail_rule_and_launch_count():
     assert bench.launches_per_step(w, 3, plan, 152) == 5
     # no idle SMs (128 chains on 128 SMs), or too few tiles (one 8K sequence of 16 heads)
     assert not bench.wy_tail_beside(w, plan, 128)
+    # several waves, the last one partial: 512 chains on 152 SMs leave 96 idle in the fourth
+    w4 = synth.WORKLOADS["cp2_b16_h32_t4k"]
+    assert bench.wy_tail_beside(w4, (2, 32, 32), 152)
+    assert bench.launches_per_step(w4, 2, (2, 32, 32), 152) == 5
+    # ... but not when the last wave is all but full (4 idle)
+    assert not bench.wy_tail_beside(synth.scaled(w4, B=4, H=37), (2, 32, 32), 152)
     w1 = synth.WORKLOADS["single_seg_h16_t8k"]
     assert not bench.wy_tail_beside(w1, (8, 16, 16), 152)
     # two pieces: the forward of piece 0 alone, then the tail's WY grid
