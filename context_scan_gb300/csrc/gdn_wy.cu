@@ -16,15 +16,16 @@
 // layout; K K^T goes to tensor memory as two tcgen05 groups (bf16, fp32 accumulate) whose A
 // operand starts at the tile for columns 0..31 (rows in lanes 0..63) and 64 rows before it for
 // columns 32..63 (rows in lanes 64..127), so each warp reads out its own quarter and forms L;
-// then the four 16 x 16 diagonal blocks of the inverse by forward substitution (one block per
-// warp; rows in registers, shuffles), and block forward substitution on mma.sync (tf32), one
-// column of blocks per warp with no barrier between the block rows. The blocks of L that feed
-// the tensor cores and the inverse itself are kept as tf32 bit patterns in row-padded layouts
-// (68 and 72 words per row), so a fragment is two or four shared loads at constant offsets
-// without bank conflicts; the diagonal blocks of L stay fp32 for the substitution. Each block
-// of the inverse is scaled and written to global memory as bf16 as soon as it is final (blocks
-// above the diagonal as zeros). Six CTAs share an SM (64 tensor-memory columns each) and hide
-// each other's latencies; the two waits (the tile, K K^T) are bounded.
+// then the four 16 x 16 diagonal blocks of the inverse by forward substitution (warps 0 and 1,
+// a column per lane, L's rows as shared-memory broadcasts), then the blocks below the diagonal
+// by two levels of the block-triangular inverse on mma.sync (tf32): 16 -> 32 rows, then
+// 32 -> 64. The blocks of L that feed the tensor cores and the inverse itself are kept as tf32
+// bit patterns in row-padded layouts (68 and 72 words per row), so that fragments load with
+// ldmatrix or plain shared loads at constant offsets; the diagonal blocks of L stay fp32 for
+// the substitution. Each block of the inverse is scaled and written to global memory as bf16
+// as soon as it is final (blocks above the diagonal as zeros). Six CTAs share an SM (64
+// tensor-memory columns each) and hide each other's latencies; the two waits (the tile,
+// K K^T) are bounded.
 #include <algorithm>
 #include <cstring>
 
@@ -140,7 +141,7 @@ __device__ __forceinline__ void wy_teardown(const WyCta& w) {
 // One chunk's pair of WY tiles. `ch` numbers the chunks the launch covers; `it` counts the
 // chunks this CTA has formed before (the barriers' phase). Every thread of the CTA calls it;
 // it ends with every thread past its last read of shared memory.
-__device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long long ch, uint32_t it) {
+__device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsigned ch, uint32_t it) {
     uint8_t* sm = w.sm;
     const uint32_t base = w.base, bar_tile = w.bar_tile, bar_kk = w.bar_kk, tmem = w.tmem;
     volatile int* abort_flag = w.abort_flag;
@@ -158,17 +159,22 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long
     int h, valid = 64;                  // valid: tokens of the chunk inside its sequence
     long long row0;                     // flattened (b, t) of the chunk's first token
     long long tile;                     // index of the chunk's tile pair in p.wy
+    // (32-bit index arithmetic: a launch covers fewer than 2^31 chunks, and every thread
+    // computes these)
     if (!p.cu_seqlens) {
-        // chunks wy_lo .. wy_lo + wy_cnt - 1 of every (b, h)
-        const int nchunks = p.T / 64;
-        const long long bh = ch / p.wy_cnt;
-        const int n = p.wy_lo + (int)(ch % p.wy_cnt);
-        h = (int)(bh % p.H);
-        row0 = (bh / p.H) * p.T + (long long)n * 64;
-        tile = bh * nchunks + n;
+        // chunks wy_lo .. wy_lo + wy_cnt - 1 of every (b, h), the heads fastest: the CTAs of
+        // one chunk's heads run together and read neighbouring rows of k, g and beta
+        const unsigned nchunks = (unsigned)p.T / 64u;
+        const unsigned bn = ch / (unsigned)p.H;
+        h = (int)(ch - bn * (unsigned)p.H);
+        const unsigned b = bn / (unsigned)p.wy_cnt;
+        const int n = p.wy_lo + (int)(bn - b * (unsigned)p.wy_cnt);
+        row0 = (long long)b * p.T + (long long)n * 64;
+        tile = ((long long)b * p.H + h) * nchunks + n;
     } else {
-        h = (int)(ch / p.total_chunks);
-        const int c = (int)(ch % p.total_chunks);
+        // (the heads fastest here too)
+        const int c = (int)(ch / (unsigned)p.H);
+        h = (int)(ch - (unsigned)c * (unsigned)p.H);
         if (c >= __ldg(p.cu_chunks + p.nseq)) return;   // past the last chunk (the grid holds a bound)
         int lo = 0, hi = p.nseq;   // the sequence s with cu_chunks[s] <= c < cu_chunks[s+1]
         while (hi - lo > 1) {
@@ -179,7 +185,7 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long
         const int t0 = __ldg(p.cu_seqlens + lo) + 64 * n;
         row0 = t0;
         valid = min(64, __ldg(p.cu_seqlens + lo + 1) - t0);
-        tile = ch;
+        tile = (long long)h * p.total_chunks + c;
     }
     uint8_t* out_b = p.wy + tile * 16384;   // A diag(beta)
     uint8_t* out_g = out_b + 8192;          // A diag(beta 2^Gx)
@@ -338,57 +344,118 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, long
     }
     __syncthreads();
 
-    // ---- block forward substitution: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ. A column of
-    //      blocks depends only on itself above, the diagonal inverses and L, so each warp
-    //      walks one 8-wide half of block columns down on its own: warps 0, 1 column 0;
-    //      warps 2, 3 columns 1 and then 2. Each 16 x 8 tile goes back to X (tf32) and,
-    //      scaled, to the outputs (bf16 pairs).
-    float* Ys = reinterpret_cast<float*>(sm + WY_Y) + warp * 128;
+    // ---- the blocks below the diagonal, by two levels of the block-triangular inverse
+    //      [[A, 0], [C, D]]^-1 = [[A^-1, 0], [-D^-1 C A^-1, D^-1]]:
+    //      stage 1 (16 -> 32 rows): X_10 = -X_11 L_10 X_00 (warps 0, 1) and
+    //        X_32 = -X_33 L_32 X_22 (warps 2, 3), an 8-wide half of the block each;
+    //      stage 2 (32 -> 64 rows): the lower-left 32 x 32 block -X_[11] (L_[10] X_[00]) with
+    //        X_[00] = [[X_00, 0], [X_10, X_11]] and X_[11] = [[X_22, 0], [X_32, X_33]], one
+    //        8-wide column strip per warp (X_01 = 0 leaves warps 2, 3 half the sum).
+    //      Fragments of L and of the row-major X blocks by ldmatrix (four 8 x 4-word tiles);
+    //      the products Y go through a per-warp scratch to become B operands. Each finished
+    //      16 x 8 tile is scaled and written to the outputs as bf16 pairs; stage 1's tiles also
+    //      go back to X (tf32) for stage 2.
     const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll 1
-    for (int J = (warp < 2 ? 0 : 1); J < (warp < 2 ? 1 : 3); ++J) {
-        const int n0 = 16 * J + 8 * (warp & 1);
-#pragma unroll 1
-        for (int I = J + 1; I < 4; ++I) {
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int m = J; m < I; ++m)
+    const uint32_t lt_u = smem_u32(Lt), x_u = smem_u32(X);
+    // this lane's ldmatrix row address within a 16 x 8 tile at (r0, c0) of a row-major matrix
+    const int lm_r = (lane & 7) + 8 * ((lane >> 3) & 1), lm_c = 4 * (lane >> 4);
+    auto ldsm = [&](uint32_t (&a)[4], uint32_t m_u, int pitch, int r0, int c0) {
+        const uint32_t addr = m_u + (uint32_t)(((r0 + lm_r) * pitch + c0 + lm_c) * 4);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                     : "r"(addr)
+                     : "memory");
+    };
+    // B fragment: X rows k0 + tq (+4), column n0 + gq
+    auto ldx_b = [&](uint32_t (&bb)[2], int k0, int n0) {
+        const uint32_t* xb = X + (k0 + tq) * XS + n0 + gq;
+        bb[0] = xb[0];
+        bb[1] = xb[4 * XS];
+    };
+    // a 16 x 8 accumulator tile through row-major scratch Ys: B fragment rows 8 kk + tq (+4)
+    auto put_y = [&](float* Ys, const float (&y)[4]) {
+        Ys[gq * 8 + 2 * tq] = y[0];
+        Ys[gq * 8 + 2 * tq + 1] = y[1];
+        Ys[(gq + 8) * 8 + 2 * tq] = y[2];
+        Ys[(gq + 8) * 8 + 2 * tq + 1] = y[3];
+    };
+    auto get_y = [&](uint32_t (&bb)[2], const float* Ys, int kk) {
+        bb[0] = tf32_operand(Ys[(8 * kk + tq) * 8 + gq]);
+        bb[1] = tf32_operand(Ys[(8 * kk + tq + 4) * 8 + gq]);
+    };
+    // X = -z at rows r0, r0 + 8 (r0 = 16 I + gq), columns c0, c0 + 1 (c0 = n0 + 2 tq): both
+    // outputs as bf16 pairs (byte 4 tq of 16-byte chunk n0 / 8)
+    auto put_out = [&](const float (&z)[4], int r0, int n0) {
+        const int c0 = n0 + 2 * tq;
+        const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = bekr[c0], e1 = bekr[c0 + 1];
+        *reinterpret_cast<uint32_t*>(out_b + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-z[0] * b0, -z[1] * b1);
+        *reinterpret_cast<uint32_t*>(out_b + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-z[2] * b0, -z[3] * b1);
+        *reinterpret_cast<uint32_t*>(out_g + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-z[0] * e0, -z[1] * e1);
+        *reinterpret_cast<uint32_t*>(out_g + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-z[2] * e0, -z[3] * e1);
+    };
+    {
+        const int Ib = warp < 2 ? 1 : 3, Jb = Ib - 1;
+        const int n0 = 16 * Jb + 8 * (warp & 1);
+        float* Ys = reinterpret_cast<float*>(sm + WY_Y) + warp * 128;
+        float y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    // A = L rows 16I + g (+8), columns 16m + 8kk + t (+4); B = X rows
-                    // 16m + 8kk + t (+4), column n0 + g
-                    const uint32_t* la = Lt + (16 * I + gq) * LS + 16 * m + 8 * kk + tq;
-                    const uint32_t* xb = X + (16 * m + 8 * kk + tq) * XS + n0 + gq;
-                    const uint32_t a[4] = {la[0], la[8 * LS], la[4], la[8 * LS + 4]};
-                    const uint32_t bb[2] = {xb[0], xb[4 * XS]};
-                    mma_m16n8k8(y, a, bb);
-                }
-            Ys[gq * 8 + 2 * tq] = y[0];
-            Ys[gq * 8 + 2 * tq + 1] = y[1];
-            Ys[(gq + 8) * 8 + 2 * tq] = y[2];
-            Ys[(gq + 8) * 8 + 2 * tq + 1] = y[3];
-            __syncwarp();
-            float xo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const uint32_t* xa = X + (16 * I + gq) * XS + 16 * I + 8 * kk + tq;
-                const uint32_t a[4] = {xa[0], xa[8 * XS], xa[4], xa[8 * XS + 4]};
-                const uint32_t bb[2] = {tf32_operand(Ys[(8 * kk + tq) * 8 + gq]),
-                                        tf32_operand(Ys[(8 * kk + tq + 4) * 8 + gq])};
-                mma_m16n8k8(xo, a, bb);
-            }
-            const int r0 = 16 * I + gq, c0 = n0 + 2 * tq;
-            *reinterpret_cast<uint2*>(X + r0 * XS + c0) = make_uint2(tf32_operand(-xo[0]), tf32_operand(-xo[1]));
-            *reinterpret_cast<uint2*>(X + (r0 + 8) * XS + c0) =
-                make_uint2(tf32_operand(-xo[2]), tf32_operand(-xo[3]));
-            __syncwarp();   // the next block down reads this one (and Ys is reused)
-            // bf16 pairs (columns c0, c0 + 1) of rows r0 and r0 + 8: byte 4 tq of chunk n0 / 8
-            const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = bekr[c0], e1 = bekr[c0 + 1];
-            *reinterpret_cast<uint32_t*>(out_b + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-xo[0] * b0, -xo[1] * b1);
-            *reinterpret_cast<uint32_t*>(out_b + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-xo[2] * b0, -xo[3] * b1);
-            *reinterpret_cast<uint32_t*>(out_g + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-xo[0] * e0, -xo[1] * e1);
-            *reinterpret_cast<uint32_t*>(out_g + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-xo[2] * e0, -xo[3] * e1);
+        for (int kk = 0; kk < 2; ++kk) {   // Y = L_{Ib,Jb} X_{Jb,Jb}
+            ldsm(a, lt_u, LS, 16 * Ib, 16 * Jb + 8 * kk);
+            ldx_b(bb, 16 * Jb + 8 * kk, n0);
+            mma_m16n8k8(y, a, bb);
         }
+        put_y(Ys, y);
+        __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {   // Z = X_{Ib,Ib} Y
+            ldsm(a, x_u, XS, 16 * Ib, 16 * Ib + 8 * kk);
+            get_y(bb, Ys, kk);
+            mma_m16n8k8(z, a, bb);
+        }
+        const int r0 = 16 * Ib + gq, c0 = n0 + 2 * tq;
+        *reinterpret_cast<uint2*>(X + r0 * XS + c0) = make_uint2(tf32_operand(-z[0]), tf32_operand(-z[1]));
+        *reinterpret_cast<uint2*>(X + (r0 + 8) * XS + c0) = make_uint2(tf32_operand(-z[2]), tf32_operand(-z[3]));
+        put_out(z, r0, n0);
+    }
+    __syncthreads();   // X_10 and X_32 are in X; L_10 (rows 16..31 of L) is dead
+    {
+        const int Jw = warp >> 1, n0 = 8 * warp;
+        // scratch for Y_2, Y_3 in L's rows 16..31 (free after stage 1)
+        float* Y2 = reinterpret_cast<float*>(sm + WY_LT + 16 * LS * 4) + warp * 256;
+        float* Y3 = Y2 + 128;
+        float y2[4] = {0.f, 0.f, 0.f, 0.f}, y3[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t a[4], bb[2];
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {   // Y_I = sum_m L_{I,m} X_{m,Jw}, I = 2, 3
+            if (k8 >= 2 * Jw) {
+                ldx_b(bb, 8 * k8, n0);
+                ldsm(a, lt_u, LS, 32, 8 * k8);
+                mma_m16n8k8(y2, a, bb);
+                ldsm(a, lt_u, LS, 48, 8 * k8);
+                mma_m16n8k8(y3, a, bb);
+            }
+        }
+        put_y(Y2, y2);
+        put_y(Y3, y3);
+        __syncwarp();
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {   // Z_2 = X_22 Y_2
+            get_y(bb, Y2, kk);
+            ldsm(a, x_u, XS, 32, 32 + 8 * kk);
+            mma_m16n8k8(z, a, bb);
+        }
+        put_out(z, 32 + gq, n0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) z[e] = 0.f;
+#pragma unroll
+        for (int k8 = 0; k8 < 4; ++k8) {   // Z_3 = X_32 Y_2 + X_33 Y_3
+            get_y(bb, k8 < 2 ? Y2 : Y3, k8 & 1);
+            ldsm(a, x_u, XS, 48, 32 + 8 * k8);
+            mma_m16n8k8(z, a, bb);
+        }
+        put_out(z, 48 + gq, n0);
     }
     // every warp is done with the tile, L and X before the next chunk's copy lands on them
     fence_proxy_async();
