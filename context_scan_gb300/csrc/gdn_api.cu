@@ -53,7 +53,8 @@ bool kda_prep_shape(const gdn_problem& p) { return p.in_dtype == GDN_DTYPE_BF16 
 
 // bytes of per-chunk factors the chains read, per chunk and head
 size_t chunk_factor_bytes(const gdn_problem& p) {
-    return tc_shape(p) ? 16384u : (kda_prep_shape(p) ? 2u * 64u * 64u * sizeof(float) : 0u);
+    return tc_shape(p) ? (size_t)gdn::kWyPairBytes
+                       : (kda_prep_shape(p) ? 2u * 64u * 64u * sizeof(float) : 0u);
 }
 
 // Device properties asked on every call, looked up once per device (a call on a short

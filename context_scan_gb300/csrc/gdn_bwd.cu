@@ -124,13 +124,15 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
     // free of bank conflicts -- and ND elements of the dO tile.
     constexpr int NKQ = 16 * KD / kThreads, ND = 64 * CT / kThreads;
     uint32_t pk[NKQ][4], pq[NKQ][4], pd[ND], pg = 0u, pb = 0u;
-    uint4 pa[2];   // (with the WY tiles) this thread's two 16-byte pieces of A diag(beta 2^Gx)
+    uint4 pa[2];   // (with the WY tiles) this thread's 16-byte pieces of A diag(beta 2^Gx)
     const long long row0 = (long long)b * p.T + (long long)seg * p.seg_len;
     const bool use_wy = MMA && p.wy != nullptr;
     const uint8_t* wy_head = use_wy ? reinterpret_cast<const uint8_t*>(p.wy) +
-                                          (((long long)bh * (p.T / kChunk) +
-                                            (long long)seg * (p.seg_len / kChunk)) << 14) + 8192
+                                          ((long long)bh * (p.T / kChunk) +
+                                           (long long)seg * (p.seg_len / kChunk)) * kWyPairBytes +
+                                          kWyTileBytes
                                     : nullptr;
+
     auto prefetch = [&](int ch) {
         const long long r0 = row0 + (long long)ch * kChunk;
 #pragma unroll
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             pb = ld_bits(p.beta, row, p.in_bf16);
         }
         if (use_wy) {
-            const uint4* t = reinterpret_cast<const uint4*>(wy_head + ((long long)ch << 14));
+            const uint4* t = reinterpret_cast<const uint4*>(wy_head + (long long)ch * kWyPairBytes);
             pa[0] = t[tid];
             pa[1] = t[tid + kThreads];
         }
@@ -193,11 +195,12 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             bet[tid] = from_bits(pb, p.in_bf16);
         }
         if (use_wy) {
-            // A diag(beta 2^Gx) from its bf16 tile: 16-byte piece e of the tile is row e / 8,
-            // columns 8 ((e % 8) ^ (row % 8)) .. + 7 (the 128-byte swizzle)
+            // A diag(beta 2^Gx) from its bf16 tile: 16-byte piece e is row 8 (e / 64) + e % 8,
+            // columns 8 ((e / 8) % 8) .. + 7 (8 x 8 cores, K-major, no swizzle)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int e = tid + r * kThreads, row = e >> 3, cb = 8 * ((e & 7) ^ (row & 7));
+                const int e = tid + r * kThreads;
+                const int row = 8 * (e >> 6) + (e & 7), cb = 8 * ((e >> 3) & 7);
                 const uint32_t w4[4] = {pa[r].x, pa[r].y, pa[r].z, pa[r].w};
                 float* dst = As + row * TP + cb;
                 st4(dst, make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xFFFF0000u),

@@ -10,6 +10,19 @@ namespace gdn {
 
 constexpr int kChunk = 64;
 
+// WY tile pair of one chunk (tensor-core path): A diag(beta), then A diag(beta 2^Gx) (or
+// 2^G for the decayed read), each a bf16 64 x 64 tcgen05 operand image, K-major without
+// swizzle: 8 x 8 core matrices (8 rows of 16 bytes, 128 contiguous bytes), 128 bytes apart
+// along K and 1024 bytes apart from one 8-row group to the next. The factors are lower
+// triangular by 16 x 16 blocks: row group R has wy_ncore(R) nonzero cores, the rest are zero.
+constexpr int kWyTileBytes = 8192;
+constexpr int kWyPairBytes = 2 * kWyTileBytes;
+__host__ __device__ constexpr int wy_ncore(int R) { return 2 * (R >> 1) + 2; }
+// byte offset of the 16-byte piece holding row `row`, columns 8 kg .. 8 kg + 7 of one factor
+__host__ __device__ constexpr int wy_piece(int row, int kg) {
+    return (row >> 3) * 1024 + kg * 128 + (row & 7) * 16;
+}
+
 // Device error word, at the start of the caller's workspace. The first error a kernel
 // records sticks (atomicCAS from 0); gdn_check_device_error reads and clears it.
 struct DeviceError {
@@ -33,9 +46,9 @@ struct ChainParams {
     float* h_final;    // forward: written by chains whose segment is nseg_total-1 (nullable)
     float* M;          // summary: [nseg_total,B,H,K,K]
     float* S;          // summary: [nseg_total,B,H,K,V]
-    // tcgen05 path: per-chunk WY factors, [B*H][T/64][A diag(beta) | A diag(beta 2^Gx)], each
-    // a bf16 64 x 64 tile in the chain kernels' swizzled operand layout (8192 bytes); per-channel
-    // gates at bf16 inputs: [B*H][T/64][A diag(beta) | C], fp32 64 x 64 row-major
+    // tcgen05 path: per-chunk WY factors, [B*H][T/64] pairs of kWyPairBytes (the format at
+    // kWyTileBytes above); per-channel gates at bf16 inputs: [B*H][T/64][A diag(beta) | C],
+    // fp32 64 x 64 row-major
     void* wy;
     int B, T, H, K, V;
     int seg_len;       // tokens per segment (multiple of 64)
@@ -131,8 +144,8 @@ struct StateGradParams {
     // sequence) is written to D_chunks + c*B*H*K*V + (b*H + h)*K*V ([T/64][B][H][K][V])
     float* D_chunks;
     // bf16 inputs with K == V == 128: when non-null, the forward's per-chunk WY tiles
-    // ([B*H][T/64][A diag(beta) | A diag(beta 2^Gx)], bf16 64 x 64 in the chain kernels'
-    // swizzled layout), whose second factor replaces the kernel's own inverse
+    // ([B*H][T/64] pairs in the format at kWyTileBytes), whose second factor replaces the
+    // kernel's own inverse
     const void* wy;
     int B, T, H, K, V;
     int seg_len, nseg;

@@ -110,7 +110,8 @@ struct Cfg {
 
 // Shared-memory map (bytes from a 1024-aligned base). A k, q or v tile is two 64-feature
 // halves of 64 rows x 128 bytes (8 KB each, 128-byte swizzle); a WY stage is the tile pair
-// A diag(beta) | A diag(beta 2^Gx) (8 KB each).
+// A diag(beta) | A diag(beta 2^Gx) (8 KB each, K-major without swizzle: 8 x 8 cores 128
+// bytes apart along K, row groups 1024 bytes apart).
 template <bool SUMMARY>
 struct Smem {
     static constexpr int KST = SUMMARY ? 4 : 3;   // k ring stages
@@ -296,12 +297,12 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
         // The whole warp runs the loop (its lanes poll together and stay converged); lane 0
         // issues the copies, every lane loads two gates. The gates of chunk n+1 are loaded
         // into registers while chunk n's copies are in flight.
-        const uint32_t wy_bytes = need_v ? 16384u : 8192u;
-        const uint32_t wy_skip = 16384u - wy_bytes;
+        // (the M part of a summary needs only the second factor)
+        const uint32_t wy_bytes = need_v ? (uint32_t)kWyPairBytes : (uint32_t)kWyTileBytes;
         const uint8_t* wy_chain = reinterpret_cast<const uint8_t*>(c.wy) +
-                                  ((VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[b]
-                                                 : (long long)bh * (c.T / kC) + chunk0)
-                                   << 14);
+                                  (VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[b]
+                                          : (long long)bh * (c.T / kC) + chunk0) *
+                                      kWyPairBytes;
         int k_last[KST], q_last[2] = {-1, -1}, a_last[2] = {-1, -1}, v_last = -1;
 #pragma unroll
         for (int i = 0; i < KST; ++i) k_last[i] = -1;
@@ -357,9 +358,10 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
                     break;
                 if (lane == 0) {
                     const uint32_t full = bar0 + B_AFULL + 8 * as;
+                    const uint32_t skip = (uint32_t)kWyPairBytes - wy_bytes;
                     mbar_arrive_expect_tx(full, wy_bytes);
-                    bulk_load(base + L::A0 + as * 16384 + wy_skip,
-                              wy_chain + ((long long)n << 14) + wy_skip, wy_bytes, full);
+                    bulk_load(base + L::A0 + as * 16384 + skip,
+                              wy_chain + (long long)n * kWyPairBytes + skip, wy_bytes, full);
                 }
                 a_last[as] = n;
             }
@@ -417,11 +419,11 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
                     mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                   desc_k(ast + k16 * 32), k16 > 0);
+                                   desc_kn(ast + k16 * 256), k16 > 0);
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
                     mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
-                                   desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                                   desc_kn(ast + 8192 + k16 * 256), k16 > 0);
                 mma_commit(bar0 + B_VEMPTY);
                 mma_commit(bar0 + B_AEMPTY + 8 * as);
                 mma_commit(bar0 + B_BARP);
@@ -463,7 +465,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
                     mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                   desc_k(ast + k16 * 32), k16 > 0);
+                                   desc_kn(ast + k16 * 256), k16 > 0);
                 mma_commit(bar0 + B_VEMPTY);
                 // P3: W^T into the parity's O^T buffer once the prep group has stored chunk
                 // n-2's output rows from it (S12 of chunk n then accumulates O^T there)
@@ -472,7 +474,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
 #pragma unroll
                 for (int k16 = 0; k16 < 4; ++k16)
                     mma_ss<ID_P23>(tmem + TM_U + (n & 1) * 128 + 64, desc_mn(kst + k16 * 2048, 8192),
-                                   desc_k(ast + 8192 + k16 * 32), k16 > 0);
+                                   desc_kn(ast + 8192 + k16 * 256), k16 > 0);
                 mma_commit(bar0 + B_AEMPTY + 8 * as);
                 mma_commit(bar0 + B_BARP);   // covers P2 as well
             }

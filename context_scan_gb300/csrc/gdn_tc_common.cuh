@@ -187,6 +187,15 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 // K-major operand: rows of 128 bytes packed in 8-row groups of 1024 bytes
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return sdesc(saddr, 16, 1024); }
+// K-major operand without swizzle: 8-row x 16-byte core matrices 128 bytes apart along K,
+// 8-row groups 1024 bytes apart (the WY tiles)
+__device__ __forceinline__ uint64_t desc_kn(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
 // MN-major operand: 64-element blocks along M/N `mn_stride` bytes apart, 8-row groups along
 // K 1024 bytes apart
 __device__ __forceinline__ uint64_t desc_mn(uint32_t saddr, uint32_t mn_stride) {

@@ -7,10 +7,11 @@
 //   A_gam  = A diag(beta 2^Gx)     (so that W = A_gam K)
 // ("Context Parallelism in ART", section 08, the per-chunk WY representation; gates in log2
 // units, G the inclusive and Gx the exclusive cumulative sum of g within the chunk). The two
-// factors are written as bf16 64 x 64 tiles in exactly the byte image the chain kernels use
-// as tcgen05 operands: K-major rows of 128 bytes with the 128-byte swizzle. A chain then loads
-// a chunk's pair with one bulk copy instead of inverting on its critical path, and the
-// inverse is computed once per chunk rather than once per chain that walks the chunk.
+// factors are written as bf16 64 x 64 tcgen05 operand images of 8 x 8 core matrices (format
+// at kWyTileBytes in gdn_internal.h): a chain loads a chunk's pair with one bulk copy instead
+// of inverting on its critical path, and the inverse is computed once per chunk rather than
+// once per chain that walks the chunk. A core is 128 contiguous bytes, so every store of an
+// mma.sync fragment (a lane's two columns of rows g and g + 8) covers whole 128-byte lines.
 //
 // One CTA of four warps per chunk: the k tile arrives by TMA in the chain kernels' swizzled
 // layout; K K^T goes to tensor memory as two tcgen05 groups (bf16, fp32 accumulate) whose A
@@ -23,7 +24,8 @@
 // bit patterns in row-padded layouts (68 and 72 words per row), so that fragments load with
 // ldmatrix or plain shared loads at constant offsets; the diagonal blocks of L stay fp32 for
 // the substitution. Each block of the inverse is scaled and written to global memory as bf16
-// as soon as it is final (blocks above the diagonal as zeros). Six CTAs share an SM (64
+// as soon as it is final; the zero cores above the diagonal blocks are written by warps 2 and 3
+// during the substitution. Six CTAs share an SM (64
 // tensor-memory columns each) and hide each other's latencies; the two waits (the tile,
 // K K^T) are bounded.
 #include <algorithm>
@@ -37,9 +39,15 @@ namespace {
 constexpr int kWyThreads = 128;
 constexpr float kWyLog2e = 1.4426950408889634f;
 
-constexpr int LS = 68;   // row pitch (words) of the tf32 off-diagonal blocks of L
+constexpr int LS = 68;   // row pitch (words) of L (tf32 below the diagonal blocks)
 constexpr int XS = 72;   // row pitch (words) of the tf32 inverse X
-constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
+// The diagonal 16 x 16 blocks of L (fp32) live in L's rows above the diagonal, at the same
+// pitch: block b at rows ld_row(b).., columns ld_col(b).. (blocks 0, 1 in rows 16..31, columns
+// 16..47; blocks 2, 3 in rows 32..47, columns 32..63), so that two blocks read or written
+// together fall on different banks and X never overlaps them.
+__host__ __device__ constexpr int ld_row(int b) { return b < 2 ? 16 : 32; }
+__host__ __device__ constexpr int ld_col(int b) { return 16 + 16 * b - (b < 2 ? 0 : 16); }
+static_assert(ld_col(0) == 16 && ld_col(1) == 32 && ld_col(2) == 32 && ld_col(3) == 48, "diagonal block map");
 
 // shared-memory map (bytes from a 1024-aligned base). Rows 0..15 of L are never used (the
 // first block row has nothing below the diagonal), so the scratch, the scalars and the
@@ -50,7 +58,6 @@ constexpr int DS = 17;   // row pitch (words) of the fp32 diagonal blocks of L
 constexpr uint32_t WY_K = 8192;     // K tile bf16: [khalf 2][64 rows x 128 B], 128-byte swizzle
 constexpr uint32_t WY_LT = 0;       // then L (tf32, 64 x LS, rows 16..63) once K K^T is in TMEM
 constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
-constexpr uint32_t WY_LD = WY_X;    // diagonal blocks of L (fp32, 4 x 16 x DS), dead before X
 constexpr uint32_t WY_Y = 0;        // per-warp 16 x 8 fp32 scratch of the block rounds
 constexpr uint32_t WY_SC = 2048;    // Gx, G, beta, beta 2^Gx: [4][64] fp32
 constexpr uint32_t WY_BAR = 3072;   // mbarriers (tile, K K^T), tensor-memory address
@@ -66,7 +73,7 @@ struct WyParams {
     CUtensorMap tm_k;
     const void* g;
     const void* beta;
-    uint8_t* wy;        // [B*H][T/64][2][8192 B]
+    uint8_t* wy;        // [B*H][T/64] tile pairs of kWyPairBytes
     int T, H;
     int decay_first;   // read-side gate G (decayed read) instead of Gx
     const int* cu_seqlens;   // varlen: packed sequences (null for the fixed-length batch)
@@ -80,9 +87,9 @@ struct WyParams {
     long long wait_limit;   // SM clock cycles before a wait gives up
 };
 
-// 16-byte output chunk `c` (8 bf16 columns) of row `row` of one 64 x 64 output tile
+// 16-byte output piece of row `row`, columns 8 c .. 8 c + 7 of one factor's tile
 __device__ __forceinline__ uint4* out_chunk(uint8_t* tile, int row, int c) {
-    return reinterpret_cast<uint4*>(tile + sw128(row, c));
+    return reinterpret_cast<uint4*>(tile + wy_piece(row, c));
 }
 
 // wait tags recorded in the device error word's detail field
@@ -148,7 +155,7 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
     const uint32_t par = it & 1u;
     uint32_t* Lt = reinterpret_cast<uint32_t*>(sm + WY_LT);
     uint32_t* X = reinterpret_cast<uint32_t*>(sm + WY_X);
-    float* Ld = reinterpret_cast<float*>(sm + WY_LD);
+    float* Lf = reinterpret_cast<float*>(sm + WY_LT);   // L's words as fp32 (diagonal blocks)
     float* sc = reinterpret_cast<float*>(sm + WY_SC);
     const float* Gx = sc;
     const float* G = sc + 64;
@@ -187,8 +194,8 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
         valid = min(64, __ldg(p.cu_seqlens + lo + 1) - t0);
         tile = (long long)h * p.total_chunks + c;
     }
-    uint8_t* out_b = p.wy + tile * 16384;   // A diag(beta)
-    uint8_t* out_g = out_b + 8192;          // A diag(beta 2^Gx)
+    uint8_t* out_b = p.wy + tile * kWyPairBytes;   // A diag(beta)
+    uint8_t* out_g = out_b + kWyTileBytes;          // A diag(beta 2^Gx)
 
     // ---- the k tile (two 64-feature halves, 128-byte swizzle) by TMA
     if (tid == 0) {
@@ -272,11 +279,8 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
                     *reinterpret_cast<uint4*>(Lt + i * LS + j) =
                         make_uint4(tf32_operand(v[0]), tf32_operand(v[1]), tf32_operand(v[2]), tf32_operand(v[3]));
                 } else if ((j >> 4) == I) {
-                    float* ld = Ld + I * 16 * DS + (i & 15) * DS + (j & 15);
-                    ld[0] = v[0];
-                    ld[1] = v[1];
-                    ld[2] = v[2];
-                    ld[3] = v[3];
+                    *reinterpret_cast<float4*>(Lf + (ld_row(I) + (i & 15)) * LS + ld_col(I) + (j & 15)) =
+                        make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
         }
@@ -293,38 +297,61 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
 
     // ---- diagonal 16 x 16 blocks of (I + L)^-1 by forward substitution down the columns:
     //      warps 0 and 1 take two blocks each, lane (block, c) computes column c of its block,
-    //      X[i][c] = [i == c] - sum_{j<i} L[i][j] X[j][c] with the sum in increasing j, the
-    //      whole column in registers and L's rows read as broadcasts (no shuffles). The columns
-    //      go back over the block's L (fp32); every warp then reads its block row by row.
+    //      X[i][c] = [i == c] - sum_{j<i} L[i][j] X[j][c] (the sum as two interleaved partial
+    //      sums), the whole column in registers and L's rows read as broadcasts. The columns go
+    //      back over the block's L. Meanwhile warps 2 and 3 store the zero cores of both
+    //      outputs (row group R, cores wy_ncore(R) .. 7: 24 per factor, 3 pieces per thread).
     if (warp < 2) {
         const int blk = 2 * warp + (lane >> 4), c = lane & 15;
-        float* lb = Ld + blk * 16 * DS;
+        float* lb = Lf + ld_row(blk) * LS + ld_col(blk);
         float x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            float acc = (i == c) ? 1.f : 0.f;
+            float a0 = (i == c) ? 1.f : 0.f, a1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc = fmaf(-lb[i * DS + j], x[j], acc);
-            x[i] = acc;
+            for (int j4 = 0; j4 < i; j4 += 4) {
+                const float4 l4 = *reinterpret_cast<const float4*>(lb + i * LS + j4);
+                a0 = fmaf(-l4.x, x[j4], a0);
+                if (j4 + 1 < i) a1 = fmaf(-l4.y, x[j4 + 1], a1);
+                if (j4 + 2 < i) a0 = fmaf(-l4.z, x[j4 + 2], a0);
+                if (j4 + 3 < i) a1 = fmaf(-l4.w, x[j4 + 3], a1);
+            }
+            x[i] = a0 + a1;
         }
         __syncwarp();   // every lane of the warp has read its blocks of L
 #pragma unroll
-        for (int i = 0; i < 16; ++i) lb[i * DS + c] = x[i];
+        for (int i = 0; i < 16; ++i) lb[i * LS + c] = x[i];
+    } else {
+        // zero piece q = 0..191 of a factor: row group R = 2 m + (q / 8) % 2 of pair m (cores
+        // 2 m + 2 .. 7 above its diagonal blocks), core and row from the rest
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int q = (tid - 64) + 64 * k;              // 0..191
+            const int row8 = q & 7, rest = q >> 3;          // rest 0..23: (R, core)
+            // pairs m = 0, 1, 2 have 6, 4, 2 zero cores per row group: 12, 8, 4 per pair
+            const int m = rest < 12 ? 0 : (rest < 20 ? 1 : 2);
+            const int r2 = rest - (m == 0 ? 0 : (m == 1 ? 12 : 20));
+            const int nz = 6 - 2 * m;                       // zero cores per row group
+            const int R = 2 * m + r2 / nz, kg = 2 * m + 2 + r2 % nz;
+            const int off = R * 1024 + kg * 128 + row8 * 16;
+            *reinterpret_cast<uint4*>(out_b + off) = z;
+            *reinterpret_cast<uint4*>(out_g + off) = z;
+        }
     }
     __syncthreads();
     {
+        // every warp: its diagonal block, row r, columns 8 half .. +7 -> X (tf32) and both
+        // outputs (one 16-byte chunk per tile)
         const int bs = 16 * warp, r = lane & 15, half = lane >> 4;
-        const float* lr = Ld + warp * 16 * DS + r * DS + 8 * half;
-        float x[8];
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) x[cc] = lr[cc];
-        __syncthreads();   // every warp is done with Ld, which X overwrites
+        const float* lr = Lf + (ld_row(warp) + r) * LS + ld_col(warp) + 8 * half;
+        const float4 xa = *reinterpret_cast<const float4*>(lr);
+        const float4 xb = *reinterpret_cast<const float4*>(lr + 4);
+        const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
         const int row = bs + r, c0 = bs + 8 * half;
         uint4* xs = reinterpret_cast<uint4*>(X + row * XS + c0);
         xs[0] = make_uint4(tf32_operand(x[0]), tf32_operand(x[1]), tf32_operand(x[2]), tf32_operand(x[3]));
         xs[1] = make_uint4(tf32_operand(x[4]), tf32_operand(x[5]), tf32_operand(x[6]), tf32_operand(x[7]));
-        // output: this row's 8 columns of the diagonal block, scaled, as one 16-byte chunk per
-        // tile; and the row's chunks above the diagonal block as zeros (split between halves)
         *out_chunk(out_b, row, c0 >> 3) =
             make_uint4(pack_bf16(x[0] * bet[c0], x[1] * bet[c0 + 1]),
                        pack_bf16(x[2] * bet[c0 + 2], x[3] * bet[c0 + 3]),
@@ -335,12 +362,6 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
                        pack_bf16(x[2] * bekr[c0 + 2], x[3] * bekr[c0 + 3]),
                        pack_bf16(x[4] * bekr[c0 + 4], x[5] * bekr[c0 + 5]),
                        pack_bf16(x[6] * bekr[c0 + 6], x[7] * bekr[c0 + 7]));
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-        for (int cz = 2 * warp + 2 + half; cz < 8; cz += 2) {
-            *out_chunk(out_b, row, cz) = z;
-            *out_chunk(out_g, row, cz) = z;
-        }
     }
     __syncthreads();
 
@@ -384,14 +405,16 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
         bb[1] = tf32_operand(Ys[(8 * kk + tq + 4) * 8 + gq]);
     };
     // X = -z at rows r0, r0 + 8 (r0 = 16 I + gq), columns c0, c0 + 1 (c0 = n0 + 2 tq): both
-    // outputs as bf16 pairs (byte 4 tq of 16-byte chunk n0 / 8)
+    // outputs as bf16 pairs, byte 4 tq of the 16-byte piece (row, n0 / 8) -- across the warp
+    // one whole core per store
     auto put_out = [&](const float (&z)[4], int r0, int n0) {
         const int c0 = n0 + 2 * tq;
         const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = bekr[c0], e1 = bekr[c0 + 1];
-        *reinterpret_cast<uint32_t*>(out_b + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-z[0] * b0, -z[1] * b1);
-        *reinterpret_cast<uint32_t*>(out_b + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-z[2] * b0, -z[3] * b1);
-        *reinterpret_cast<uint32_t*>(out_g + sw128(r0, n0 >> 3) + 4 * tq) = pack_bf16(-z[0] * e0, -z[1] * e1);
-        *reinterpret_cast<uint32_t*>(out_g + sw128(r0 + 8, n0 >> 3) + 4 * tq) = pack_bf16(-z[2] * e0, -z[3] * e1);
+        const int o0 = wy_piece(r0, n0 >> 3) + 4 * tq, o1 = wy_piece(r0 + 8, n0 >> 3) + 4 * tq;
+        *reinterpret_cast<uint32_t*>(out_b + o0) = pack_bf16(-z[0] * b0, -z[1] * b1);
+        *reinterpret_cast<uint32_t*>(out_b + o1) = pack_bf16(-z[2] * b0, -z[3] * b1);
+        *reinterpret_cast<uint32_t*>(out_g + o0) = pack_bf16(-z[0] * e0, -z[1] * e1);
+        *reinterpret_cast<uint32_t*>(out_g + o1) = pack_bf16(-z[2] * e0, -z[3] * e1);
     };
     {
         const int Ib = warp < 2 ? 1 : 3, Jb = Ib - 1;
