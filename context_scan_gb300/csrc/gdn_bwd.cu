@@ -158,10 +158,15 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
         if (use_wy) {
             const uint4* t = reinterpret_cast<const uint4*>(wy_head + (long long)ch * kWyPairBytes);
             pa[0] = t[tid];
-            pa[1] = t[tid + kThreads];
+            if (tid + kThreads < kWyTileBytes / 16) pa[1] = t[tid + kThreads];
         }
     };
     const int n_chunks = p.seg_len / kChunk;
+    if (use_wy)   // A's entries above its diagonal blocks, which the tiles do not carry
+        for (int e = tid; e < 64 * 64; e += kThreads) {
+            const int i = e >> 6, j = e & 63;
+            if (j >= 16 * ((i >> 4) + 1)) As[i * TP + j] = 0.f;
+        }
     if (n_chunks > 0) prefetch(n_chunks - 1);
     for (int ch = n_chunks - 1; ch >= 0; --ch) {
         // ---- (1) the prefetched chunk into shared memory: k, q (row and transposed copies),
@@ -195,12 +200,21 @@ __global__ void __launch_bounds__(kThreads) state_grad_kernel(StateGradParams p)
             bet[tid] = from_bits(pb, p.in_bf16);
         }
         if (use_wy) {
-            // A diag(beta 2^Gx) from its bf16 tile: 16-byte piece e is row 8 (e / 64) + e % 8,
-            // columns 8 ((e / 8) % 8) .. + 7 (8 x 8 cores, K-major, no swizzle)
+            // A diag(beta 2^Gx) from its bf16 tile (its 320 nonzero 16-byte pieces): piece e
+            // lies in slab s, half hh, row group R, core row e % 8 -- row 8 R + e % 8, columns
+            // 8 (2 s + hh) .. + 7; the entries above the diagonal blocks were zeroed before the
+            // first chunk
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int e = tid + r * kThreads;
-                const int row = 8 * (e >> 6) + (e & 7), cb = 8 * ((e >> 3) & 7);
+                if (e >= kWyTileBytes / 16) break;
+                const int o = 16 * e;
+                int sl = 0;
+#pragma unroll
+                for (int q = 1; q < 4; ++q) sl += o >= wy_slab0(q);
+                const int o1 = o - wy_slab0(sl), hh = o1 >= wy_slab_lbo(sl) ? 1 : 0;
+                const int o2 = o1 - hh * wy_slab_lbo(sl);
+                const int row = 8 * (2 * sl + (o2 >> 7)) + (e & 7), cb = 8 * (2 * sl + hh);
                 const uint32_t w4[4] = {pa[r].x, pa[r].y, pa[r].z, pa[r].w};
                 float* dst = As + row * TP + cb;
                 st4(dst, make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xFFFF0000u),

@@ -11,17 +11,24 @@ namespace gdn {
 constexpr int kChunk = 64;
 
 // WY tile pair of one chunk (tensor-core path): A diag(beta), then A diag(beta 2^Gx) (or
-// 2^G for the decayed read), each a bf16 64 x 64 tcgen05 operand image, K-major without
-// swizzle: 8 x 8 core matrices (8 rows of 16 bytes, 128 contiguous bytes), 128 bytes apart
-// along K and 1024 bytes apart from one 8-row group to the next. The factors are lower
-// triangular by 16 x 16 blocks: row group R has wy_ncore(R) nonzero cores, the rest are zero.
-constexpr int kWyTileBytes = 8192;
+// 2^G for the decayed read). Each factor is lower triangular by 16 x 16 blocks and is stored,
+// bf16, as the B operands of the four tcgen05 MMAs that multiply by it (one per 16 columns
+// j): slab s holds rows 16 s .. 63 of columns 16 s .. 16 s + 15 as K-major 8 x 8 core matrices
+// without swizzle (8 rows of 16 bytes each), row groups 128 bytes apart, its two 8-column
+// halves wy_slab_lbo(s) bytes apart; the slabs follow one another from wy_slab0(s). No zeros
+// above the diagonal blocks are stored, and MMA s covers rows 16 s .. 63 only (N = 64 - 16 s).
+constexpr int kWyTileBytes = 5120;
 constexpr int kWyPairBytes = 2 * kWyTileBytes;
-__host__ __device__ constexpr int wy_ncore(int R) { return 2 * (R >> 1) + 2; }
+__host__ __device__ constexpr int wy_slab0(int s) { return 128 * (18 * s - 2 * s * s); }
+__host__ __device__ constexpr int wy_slab_lbo(int s) { return 128 * (8 - 2 * s); }
 // byte offset of the 16-byte piece holding row `row`, columns 8 kg .. 8 kg + 7 of one factor
+// (row >= 16 (kg / 2))
 __host__ __device__ constexpr int wy_piece(int row, int kg) {
-    return (row >> 3) * 1024 + kg * 128 + (row & 7) * 16;
+    return wy_slab0(kg >> 1) + (kg & 1) * wy_slab_lbo(kg >> 1) + ((row >> 3) - 2 * (kg >> 1)) * 128 +
+           (row & 7) * 16;
 }
+static_assert(wy_slab0(4) == kWyTileBytes && wy_piece(63, 7) + 16 == kWyTileBytes &&
+              wy_piece(16, 2) == wy_slab0(1), "WY tile format");
 
 // Device error word, at the start of the caller's workspace. The first error a kernel
 // records sticks (atomicCAS from 0); gdn_check_device_error reads and clears it.

@@ -109,9 +109,9 @@ struct Cfg {
 };
 
 // Shared-memory map (bytes from a 1024-aligned base). A k, q or v tile is two 64-feature
-// halves of 64 rows x 128 bytes (8 KB each, 128-byte swizzle); a WY stage is the tile pair
-// A diag(beta) | A diag(beta 2^Gx) (8 KB each, K-major without swizzle: 8 x 8 cores 128
-// bytes apart along K, row groups 1024 bytes apart).
+// halves of 64 rows x 128 bytes (8 KB each, 128-byte swizzle); a WY stage holds the tile pair
+// A diag(beta) | A diag(beta 2^Gx) as stored (kWyTileBytes each: the four MMA slabs of each
+// factor, no zeros above the diagonal blocks).
 template <bool SUMMARY>
 struct Smem {
     static constexpr int KST = SUMMARY ? 4 : 3;   // k ring stages
@@ -416,14 +416,8 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
                     ok(bar0 + B_VFULL, n & 1, TAG_VFULL);
                 if (!run) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                   desc_kn(ast + k16 * 256), k16 > 0);
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(tmem + TM_S, desc_mn(kst + k16 * 2048, 8192),
-                                   desc_kn(ast + 8192 + k16 * 256), k16 > 0);
+                wy_mma(t_u, base + L::V, ast);
+                wy_mma(tmem + TM_S, kst, ast + kWyTileBytes);
                 mma_commit(bar0 + B_VEMPTY);
                 mma_commit(bar0 + B_AEMPTY + 8 * as);
                 mma_commit(bar0 + B_BARP);
@@ -462,19 +456,13 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
                       ok(bar0 + B_VFULL, n & 1, TAG_VFULL);
                 if (!run) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(t_u, desc_mn(base + L::V + k16 * 2048, 8192),
-                                   desc_kn(ast + k16 * 256), k16 > 0);
+                wy_mma(t_u, base + L::V, ast);
                 mma_commit(bar0 + B_VEMPTY);
                 // P3: W^T into the parity's O^T buffer once the prep group has stored chunk
                 // n-2's output rows from it (S12 of chunk n then accumulates O^T there)
                 if (!(run = ok(bar0 + B_EPIDONE, n & 1, TAG_EPIDONE))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    mma_ss<ID_P23>(tmem + TM_U + (n & 1) * 128 + 64, desc_mn(kst + k16 * 2048, 8192),
-                                   desc_kn(ast + 8192 + k16 * 256), k16 > 0);
+                wy_mma(tmem + TM_U + (n & 1) * 128 + 64, kst, ast + kWyTileBytes);
                 mma_commit(bar0 + B_AEMPTY + 8 * as);
                 mma_commit(bar0 + B_BARP);   // covers P2 as well
             }

@@ -187,12 +187,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 // K-major operand: rows of 128 bytes packed in 8-row groups of 1024 bytes
 __device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return sdesc(saddr, 16, 1024); }
-// K-major operand without swizzle: 8-row x 16-byte core matrices 128 bytes apart along K,
-// 8-row groups 1024 bytes apart (the WY tiles)
-__device__ __forceinline__ uint64_t desc_kn(uint32_t saddr) {
+// K-major operand without swizzle: 8-row x 16-byte core matrices `lbo` bytes apart along K,
+// 8-row groups `sbo` bytes apart
+__device__ __forceinline__ uint64_t desc_kn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((128u >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
     return d;
 }
@@ -209,6 +209,10 @@ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
 }
 constexpr uint32_t ID_P1 = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_P23 = idesc_bf16(128, 64, true, false);
+constexpr uint32_t ID_WY1 = idesc_bf16(128, 48, true, false);
+constexpr uint32_t ID_WY2 = idesc_bf16(128, 32, true, false);
+constexpr uint32_t ID_WY3 = idesc_bf16(128, 16, true, false);
+
 constexpr uint32_t ID_S4 = idesc_bf16(128, 128, false, true);   // A from tensor memory
 // kind::tf32, M = 128, N = 64, A from tensor memory, B K-major (S1, S2, S3)
 constexpr uint32_t ID_TF = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) |
@@ -228,6 +232,18 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "n"(ID), "r"(accumulate)
         : "memory");
+}
+
+// D^T = X^T F^T for a WY factor F (format at kWyTileBytes in gdn_internal.h) and a 64-row
+// operand X whose transpose is the MN-major A operand at `a` (two 64-feature halves 8192
+// bytes apart): four MMAs, the one for columns 16 s .. 16 s + 15 of F over F's rows
+// 16 s .. 63 only (N = 64 - 16 s, into accumulator columns 16 s ..); the first initialises
+// all 64 columns
+__device__ __forceinline__ void wy_mma(uint32_t d_tmem, uint32_t a, uint32_t tile) {
+    mma_ss<ID_P23>(d_tmem, desc_mn(a, 8192), desc_kn(tile + wy_slab0(0), wy_slab_lbo(0), 128), 0u);
+    mma_ss<ID_WY1>(d_tmem + 16, desc_mn(a + 2048, 8192), desc_kn(tile + wy_slab0(1), wy_slab_lbo(1), 128), 1u);
+    mma_ss<ID_WY2>(d_tmem + 32, desc_mn(a + 4096, 8192), desc_kn(tile + wy_slab0(2), wy_slab_lbo(2), 128), 1u);
+    mma_ss<ID_WY3>(d_tmem + 48, desc_mn(a + 6144, 8192), desc_kn(tile + wy_slab0(3), wy_slab_lbo(3), 128), 1u);
 }
 
 template <uint32_t ID>

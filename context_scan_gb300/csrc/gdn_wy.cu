@@ -7,11 +7,12 @@
 //   A_gam  = A diag(beta 2^Gx)     (so that W = A_gam K)
 // ("Context Parallelism in ART", section 08, the per-chunk WY representation; gates in log2
 // units, G the inclusive and Gx the exclusive cumulative sum of g within the chunk). The two
-// factors are written as bf16 64 x 64 tcgen05 operand images of 8 x 8 core matrices (format
-// at kWyTileBytes in gdn_internal.h): a chain loads a chunk's pair with one bulk copy instead
-// of inverting on its critical path, and the inverse is computed once per chunk rather than
-// once per chain that walks the chunk. A core is 128 contiguous bytes, so every store of an
-// mma.sync fragment (a lane's two columns of rows g and g + 8) covers whole 128-byte lines.
+// factors are written as bf16 tcgen05 operands of 8 x 8 core matrices without their zero
+// blocks above the diagonal (format at kWyTileBytes in gdn_internal.h): a chain loads a
+// chunk's pair with one bulk copy instead of inverting on its critical path, and the inverse
+// is computed once per chunk rather than once per chain that walks the chunk. A core is 128
+// contiguous bytes, so every store of an mma.sync fragment (a lane's two columns of rows g
+// and g + 8) covers whole 128-byte lines.
 //
 // One CTA of four warps per chunk: the k tile arrives by TMA in the chain kernels' swizzled
 // layout; K K^T goes to tensor memory as two tcgen05 groups (bf16, fp32 accumulate) whose A
@@ -24,8 +25,7 @@
 // bit patterns in row-padded layouts (68 and 72 words per row), so that fragments load with
 // ldmatrix or plain shared loads at constant offsets; the diagonal blocks of L stay fp32 for
 // the substitution. Each block of the inverse is scaled and written to global memory as bf16
-// as soon as it is final; the zero cores above the diagonal blocks are written by warps 2 and 3
-// during the substitution. Six CTAs share an SM (64
+// as soon as it is final. Six CTAs share an SM (64
 // tensor-memory columns each) and hide each other's latencies; the two waits (the tile,
 // K K^T) are bounded.
 #include <algorithm>
@@ -299,8 +299,7 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
     //      warps 0 and 1 take two blocks each, lane (block, c) computes column c of its block,
     //      X[i][c] = [i == c] - sum_{j<i} L[i][j] X[j][c] (the sum as two interleaved partial
     //      sums), the whole column in registers and L's rows read as broadcasts. The columns go
-    //      back over the block's L. Meanwhile warps 2 and 3 store the zero cores of both
-    //      outputs (row group R, cores wy_ncore(R) .. 7: 24 per factor, 3 pieces per thread).
+    //      back over the block's L.
     if (warp < 2) {
         const int blk = 2 * warp + (lane >> 4), c = lane & 15;
         float* lb = Lf + ld_row(blk) * LS + ld_col(blk);
@@ -321,23 +320,6 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
         __syncwarp();   // every lane of the warp has read its blocks of L
 #pragma unroll
         for (int i = 0; i < 16; ++i) lb[i * LS + c] = x[i];
-    } else {
-        // zero piece q = 0..191 of a factor: row group R = 2 m + (q / 8) % 2 of pair m (cores
-        // 2 m + 2 .. 7 above its diagonal blocks), core and row from the rest
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            const int q = (tid - 64) + 64 * k;              // 0..191
-            const int row8 = q & 7, rest = q >> 3;          // rest 0..23: (R, core)
-            // pairs m = 0, 1, 2 have 6, 4, 2 zero cores per row group: 12, 8, 4 per pair
-            const int m = rest < 12 ? 0 : (rest < 20 ? 1 : 2);
-            const int r2 = rest - (m == 0 ? 0 : (m == 1 ? 12 : 20));
-            const int nz = 6 - 2 * m;                       // zero cores per row group
-            const int R = 2 * m + r2 / nz, kg = 2 * m + 2 + r2 % nz;
-            const int off = R * 1024 + kg * 128 + row8 * 16;
-            *reinterpret_cast<uint4*>(out_b + off) = z;
-            *reinterpret_cast<uint4*>(out_g + off) = z;
-        }
     }
     __syncthreads();
     {

@@ -108,8 +108,9 @@ typedef struct {
  * (nseg = 1 for gdn_chunk_fwd and gdn_segment_summary). Returns 0 for an invalid problem.
  * It holds the error word; for the tensor-core shapes (bf16 in, K == V == 128) the
  * per-chunk WY factors A diag(beta) and A diag(beta exp-decay), A = (I + L)^-1, as two bf16
- * 64 x 64 tiles per chunk (16 KiB per chunk and head, formed by one launch before the
- * chains); and, with P = gdn_segmented_pieces(p, nseg) pieces per sequence, fp32 [P,B,H,K,K]
+ * 64 x 64 tiles per chunk without their zero blocks above the diagonal (10 KiB per chunk and
+ * head, formed by one launch before the chains); and, with P = gdn_segmented_pieces(p, nseg)
+ * pieces per sequence, fp32 [P,B,H,K,K]
  * and [P,B,H,K,V] arrays for the piece summaries (P >= 3) and one [P,B,H,K,V] for the state
  * entering each piece (P >= 2). P depends on the current device's SM count: size and run on
  * the same device. */
@@ -223,8 +224,8 @@ GDN_API gdn_status gdn_segmented_fwd_timed(const gdn_problem* p, int nseg, const
  *   loads the library holds it until the process exits. The call allocates nothing.
  *   Limit: problems with gdn_workspace_bytes(p, nseg) > GDN_NOALLOC_SCRATCH_BYTES are
  *   rejected with GDN_ERR_WORKSPACE (at bf16, K = V = 128 and P >= 3 pieces that is
- *   B*H*(T/64*16 KiB + P*192 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
- *   T = 2048 in 4 segments (4 pieces) take 40 MiB).
+ *   B*H*(T/64*10 KiB + P*192 KiB) + 256 bytes at most 64 MiB, e.g. B*H = 32 heads of
+ *   T = 2048 in 4 segments (4 pieces) take 34 MiB).
  *   device_error: optional (NULL to skip) 8-byte-aligned device pointer to two unsigned
  *   words that receive this call's device error word {code, detail} (see
  *   gdn_check_device_error for the codes) when the call's stream work completes.

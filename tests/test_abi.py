@@ -64,8 +64,9 @@ def P(**kw):
 
 def test_workspace_bytes_and_status_strings(L):
     p = P(B=2, T=32768, H=32)
-    # bf16, K = V = 128: the error word and two 8 KiB WY tiles per chunk of each head
-    wy = 64 * (32768 // 64) * 16384
+    # bf16, K = V = 128: the error word and a WY tile pair of 10 KiB per chunk of each head
+    # (the two 64 x 64 bf16 factors without their zero blocks above the diagonal)
+    wy = 64 * (32768 // 64) * 10240
     assert L.gdn_workspace_bytes(ctypes.byref(p), 1) == 256 + wy
     # without a current device the planner keeps one piece per segment
     assert L.gdn_segmented_pieces(ctypes.byref(p), 1) == 1
@@ -124,10 +125,10 @@ def test_varlen_workspace_and_validation(L):
     # packed sequences: B == 1, any T; the WY tiles of at most T/64 + nseq chunks per head,
     # then two int32 arrays of nseq + 1 (each region 256-byte aligned)
     p = P(B=1, T=7300, H=16)
-    wy = 16 * (7300 // 64 + 5) * 16384
+    wy = 16 * (7300 // 64 + 5) * 10240
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 5) == 256 + wy + 256 + 256
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=7300, H=16, in_dtype=0)), 5) == 768
-    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=0)), 1) == 256 + 2 * 16384 + 512
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=0)), 1) == 256 + 2 * 10240 + 512
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=2, T=7300)), 5) == 0   # B must be 1
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 0) == 0
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, K=96, V=96)), 1) == 0

@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
 
 
 def test_noalloc_rejects_problems_beyond_the_array():
-    # B*H = 512 heads of 256 tokens in 2 segments (2 pieces) need 512*(4*16 KiB) of WY tiles
+    # B*H = 512 heads of 256 tokens in 2 segments (2 pieces) need 512*(4*10 KiB) of WY tiles
     # and 2*512*64 KiB of piece states: more than the fixed array
     w = synth.scaled(synth.WORKLOADS["cp2_b16_h32_t4k"], T=256)
     d = {n: torch.zeros((w.B, w.T, w.H, w.K), dtype=torch.bfloat16, device="cuda")
