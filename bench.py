@@ -453,10 +453,18 @@ def run_varlen(args):
     if st != 0:
         raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # stage times from a pass of the timed entry point (its events sit between the launches);
+    # the timed region runs the plain call, each step between two events of its own
+    Ks = min(K, 100)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Ks)]
     for e3 in ev:
         for e in e3:
             e.record(stream)
+    for i in range(Ks):
+        flush.fill_(1.0)
+        step(ev[i])
+    torch.cuda.synchronize()
+    pe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler = ClockSampler(local) if rank == 0 else None
     barrier(dev)
     torch.cuda.synchronize()
@@ -465,7 +473,9 @@ def run_varlen(args):
         time.sleep(0.3)
     for i in range(K):
         flush.fill_(1.0)   # outside the step's own events
-        step(ev[i])
+        pe[i][0].record(stream)
+        step()
+        pe[i][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     st, detail = gdn.gdn_check_device_error(ws)
@@ -473,11 +483,11 @@ def run_varlen(args):
         raise RuntimeError(f"device error word {st} detail {detail} in the timed region")
     wy_ms = [e[0].elapsed_time(e[1]) for e in ev]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_s = sum(a + b for a, b in zip(wy_ms, fwd_ms)) / 1e3
+    step_s = sum(a.elapsed_time(b) for a, b in pe) / 1e3
     max_s = reduce_max(step_s, device=dev if world > 1 else "cpu")
     barrier(dev)
     stages = varlen_algorithmic(w)
-    avg = {"wy": sum(wy_ms) / K, "forward": sum(fwd_ms) / K}
+    avg = {"wy": sum(wy_ms) / Ks, "forward": sum(fwd_ms) / Ks}
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     ach = stages["forward"]["bytes"] / (avg["forward"] * 1e-3) / 1e9
@@ -810,11 +820,17 @@ def run_backward(args):
     st, detail = gdn.gdn_check_device_error(ws)
     if st != 0:
         raise RuntimeError(f"device error word {st} detail {detail} during warm-up")
-    Ks = args.steps
+    # stage times from a pass of the timed entry point (its events sit between the launches);
+    # the timed region runs the plain call
+    K = args.steps
+    Ks = min(K, 20)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Ks)]
     for e6 in ev:
         for e in e6:
             e.record(stream)
+    for i in range(Ks):
+        call(d, outs, ev[i])
+    torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 else None
     barrier(dev)
     torch.cuda.synchronize()
@@ -824,8 +840,8 @@ def run_backward(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(Ks):
-        call(d, outs, ev[i])
+    for i in range(K):
+        call(d, outs)
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
@@ -854,15 +870,15 @@ def run_backward(args):
                  "peak_source": (f"{peaks_src} bf16_tflops x {TF32_PER_BF16:.4f} (tf32/bf16 nominal) "
                                  f"or hbm_gbs, whichever bounds" if tensor else
                                  "fp32 CUDA-core peak: 152 SMs x 128 lanes x 2 x 2.07 GHz")})
-    ms_per_step = max_s / Ks * 1e3
+    ms_per_step = max_s / K * 1e3
     tokens = B * T
-    value = aggregate(tokens, Ks, world, max_s)
+    value = aggregate(tokens, K, world, max_s)
     comp = backward_compulsory_bytes(w)
     t_comp = comp / (hbm * 1e9)
 
     e2e = None
     if not args.no_e2e:
-        n_e2e = max(3, min(Ks, args.e2e_steps))
+        n_e2e = max(3, min(K, args.e2e_steps))
         h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
         d2h = sum(t.numel() * t.element_size() for t in outs)
         barrier(dev)
@@ -905,7 +921,7 @@ def run_backward(args):
             (1 + 1 if pieces == 1 else (tc + 1) + 3 + 1 + 1)
         line = {
             "metric": BACKWARD_METRIC, "value": round(value, 1), "unit": "tokens/s",
-            "n_gpus": world, "steps": Ks, "warmup": args.warmup,
+            "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if w.in_dtype == "f32" else "bf16 in, f32 math",
             "data": "synthetic",
@@ -925,7 +941,7 @@ def run_backward(args):
             "stage_ms": {k: round(v, 4) for k, v in avg.items()},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches * Ks,
+            "gpu_launches": launches * K,
             "clocks": clocks,
             "peaks_source": peaks_src,
         }
