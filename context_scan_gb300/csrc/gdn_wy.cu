@@ -61,12 +61,14 @@ constexpr uint32_t WY_X = 17408;    // X = (I + L)^-1 (tf32, 64 x XS)
 constexpr uint32_t WY_Y = 0;        // per-warp 16 x 8 fp32 scratch of the block rounds
 constexpr uint32_t WY_SC = 2048;    // Gx, G, beta, beta 2^Gx: [4][64] fp32
 constexpr uint32_t WY_BAR = 3072;   // mbarriers (tile, K K^T), tensor-memory address
+constexpr uint32_t WY_CF = 3200;    // column factors 2^(r_J - G_j) of L (fp32 [64])
 constexpr uint32_t WY_END = 35840;
 constexpr uint32_t kWySmem = WY_END + 1024;   // + alignment slack
 constexpr uint32_t kWyTmemCols = 64;
 constexpr uint32_t ID_KK = idesc_bf16(128, 32, false, false);   // K K^T, 32 columns per group
 static_assert(64 * LS * 4 <= WY_X - WY_LT && 64 * XS * 4 <= WY_END - WY_X, "layout");
-static_assert(WY_BAR + 64 <= 16 * LS * 4, "scratch, scalars and barriers fit in L's unused rows");
+static_assert(WY_BAR + 64 <= WY_CF && WY_CF + 256 <= 16 * LS * 4,
+              "scratch, scalars and barriers fit in L's unused rows");
 static_assert(WY_K + 3 * 8192 + 128 <= WY_END, "the K K^T operand windows stay inside the allocation");
 
 struct WyParams {
@@ -228,6 +230,12 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
         // beta 2^Gx (beta 2^G when the read sees the decayed state)
         sc[192 + 2 * lane] = b0 * ex2(p.decay_first ? excl + g0 : excl);
         sc[192 + 2 * lane + 1] = b1 * ex2(p.decay_first ? excl + g0 + g1 : excl + g0);
+        // column factors of L below the diagonal blocks: 2^(r_J - G_j), r_J = G at the end of
+        // j's 16-token block J (lane 8 J + 7 holds it as its second token); at most 1
+        const float rJ = __shfl_sync(0xffffffffu, excl + g0 + g1, 8 * (lane >> 3) + 7);
+        float* cf = reinterpret_cast<float*>(sm + WY_CF);
+        cf[2 * lane] = ex2(rJ - (excl + g0));
+        cf[2 * lane + 1] = ex2(rJ - (excl + g0 + g1));
     }
     tc_fence_before();
     __syncthreads();
@@ -268,19 +276,33 @@ __device__ __forceinline__ void wy_chunk(const WyParams& p, const WyCta& w, unsi
             tmem_wait_ld();
             const float bi = bet[i], gxi = p.decay_first ? G[i] : Gx[i];   // read-side gate
             const int I = i >> 4;
+            const float* cf = reinterpret_cast<const float*>(sm + WY_CF);
 #pragma unroll
-            for (int j4 = 0; j4 < 32; j4 += 4) {
-                const int j = jb + j4;
-                float v[4];
+            for (int hb = 0; hb < 2; ++hb) {   // the warp's two 16-column blocks J
+                const int J = (jb >> 4) + hb;
+                const float* kv = kk + 16 * hb;
+                if (J < I) {
+                    // below the diagonal blocks: 2^(gx_i - G_j) = 2^(gx_i - r_J) 2^(r_J - G_j),
+                    // both factors at most 1 (the gates only decay), so no exponential per entry
+                    const float rf = bi * ex2(gxi - G[16 * J + 15]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v[e] = (j + e < i) ? bi * ex2(gxi - G[j + e]) * kk[j4 + e] : 0.f;
-                if ((j >> 4) < I) {
-                    *reinterpret_cast<uint4*>(Lt + i * LS + j) =
-                        make_uint4(tf32_operand(v[0]), tf32_operand(v[1]), tf32_operand(v[2]), tf32_operand(v[3]));
-                } else if ((j >> 4) == I) {
-                    *reinterpret_cast<float4*>(Lf + (ld_row(I) + (i & 15)) * LS + ld_col(I) + (j & 15)) =
-                        make_float4(v[0], v[1], v[2], v[3]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 c4 = *reinterpret_cast<const float4*>(cf + 16 * J + 4 * q);
+                        *reinterpret_cast<uint4*>(Lt + i * LS + 16 * J + 4 * q) =
+                            make_uint4(tf32_operand(rf * c4.x * kv[4 * q]), tf32_operand(rf * c4.y * kv[4 * q + 1]),
+                                       tf32_operand(rf * c4.z * kv[4 * q + 2]), tf32_operand(rf * c4.w * kv[4 * q + 3]));
+                    }
+                } else if (J == I) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = 16 * J + 4 * q;
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            v[e] = (j + e < i) ? bi * ex2(gxi - G[j + e]) * kv[4 * q + e] : 0.f;
+                        *reinterpret_cast<float4*>(Lf + (ld_row(I) + (i & 15)) * LS + ld_col(I) + 4 * q) =
+                            make_float4(v[0], v[1], v[2], v[3]);
+                    }
                 }
             }
         }

@@ -7,7 +7,8 @@
  *   H_t        = exp(g_t) * H_{t-1} + outer(k_t, residual_t)
  *   o_t        = q_t @ H_t
  * -- "RFC: HyperParallel Linear Attention Context Parallel", section 2.1. The state reads
- * the un-decayed H_{t-1}; g is a natural-log decay; there is no query scale.
+ * the un-decayed H_{t-1}; g is a natural-log decay (g <= 0: the kernels rely on the state
+ * only decaying); there is no query scale.
  * Computed in chunks of 64 tokens (gate cumsum, chunk K K^T, lower-triangular solve, WY
  * form, inter-chunk state scan, output) -- "Context Parallelism in ART", section 08,
  * "First parallelize within a GPU".
