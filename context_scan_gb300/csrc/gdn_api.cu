@@ -366,11 +366,17 @@ gdn_status run_segmented(const gdn_problem* p, int nseg, const void* q, const vo
 
 
 // ---- varlen: [header | WY tiles (tcgen05 shapes), [H][T/64 + nseq] | checked cu_seqlens |
-//      cu_chunks], each region 256-byte aligned. T/64 + nseq bounds the chunks of any split of
-//      T tokens into nseq sequences, so the layout needs no host copy of the lengths.
+//      cu_chunks | (tcgen05 shapes) the piece plan: tab1f, tab1s, tab2, counts, seqinfo |
+//      piece states | piece summaries M, S], each region 256-byte aligned. T/64 + nseq bounds the
+//      chunks of any split of T tokens into nseq sequences, and e_max = kPieceSmBound / H the
+//      pieces past the first ones on any device, so the layout needs no host copy of the
+//      lengths.
+constexpr int kPieceSmBound = 256;
 struct VarlenLayout {
-    size_t off_wy, off_cu, off_cc, total;
-    int chunk_bound;
+    size_t off_wy, off_cu, off_cc, off_t1f, off_t1s, off_t2, off_cnt, off_si, off_st, off_m, off_s,
+        total;
+    int chunk_bound, e_max;
+    bool pieces;
 };
 
 VarlenLayout varlen_layout(const gdn_problem& p, int nseq) {
@@ -381,6 +387,21 @@ VarlenLayout varlen_layout(const gdn_problem& p, int nseq) {
     w.off_cu = w.off_wy + round_up(wy_bytes);
     w.off_cc = w.off_cu + round_up(sizeof(int) * ((size_t)nseq + 1));
     w.total = w.off_cc + round_up(sizeof(int) * ((size_t)nseq + 1));
+    w.pieces = tc_shape(p) && !p.gate_k;
+    if (w.pieces) {
+        const size_t ent = sizeof(int) * gdn::kPieceFields;
+        const size_t kv = (size_t)p.K * p.V, kk = (size_t)p.K * p.K;
+        w.e_max = std::max(1, kPieceSmBound / p.H);
+        w.off_t1f = w.total;
+        w.off_t1s = w.off_t1f + round_up(ent * (size_t)nseq);
+        w.off_t2 = w.off_t1s + round_up(ent * (size_t)w.e_max);
+        w.off_cnt = w.off_t2 + round_up(ent * (size_t)w.e_max);
+        w.off_si = w.off_cnt + round_up(sizeof(int) * 4);
+        w.off_st = w.off_si + round_up(sizeof(int) * 3 * (size_t)nseq);
+        w.off_m = w.off_st + round_up(sizeof(float) * (size_t)w.e_max * p.H * kv);
+        w.off_s = w.off_m + round_up(sizeof(float) * (size_t)w.e_max * p.H * kk);
+        w.total = w.off_s + round_up(sizeof(float) * (size_t)w.e_max * p.H * kv);
+    }
     return w;
 }
 
@@ -643,7 +664,7 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
                                 reinterpret_cast<gdn::DeviceError*>(workspace), s) != cudaSuccess)
         return GDN_ERR_CUDA;
     ChainParams c = base_params(p, workspace);
-    c.B = nseq;   // one chain per (sequence, head)
+    c.B = nseq;   // one chain per (sequence, head), or per piece below
     c.q = q;
     c.k = k;
     c.v = v;
@@ -663,10 +684,57 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     if (tc && gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (kda_prep_shape(*p) && p->T > 0 && gdn::launch_kda_prep(c, s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
-    if ((tc ? gdn::launch_tc_forward(c, s) : gdn::launch_simt_forward(c, s)) != cudaSuccess)
+    const int sms = std::min(sm_count(), kPieceSmBound);
+    if (!tc || !w.pieces || !gdn::pieces_possible(p->T, nseq, p->H, sms)) {
+        if (mark(stage_events, 1, s) != cudaSuccess || mark(stage_events, 2, s) != cudaSuccess ||
+            mark(stage_events, 3, s) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        if ((tc ? gdn::launch_tc_forward(c, s) : gdn::launch_simt_forward(c, s)) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        return from_cuda(mark(stage_events, 4, s));
+    }
+    // the tcgen05 chains: long sequences cut into pieces, planned on the device (gdn_varlen.cu)
+    gdn::PiecePlan pl;
+    pl.tab1f = reinterpret_cast<int*>(wsb + w.off_t1f);
+    pl.tab1s = reinterpret_cast<int*>(wsb + w.off_t1s);
+    pl.tab2 = reinterpret_cast<int*>(wsb + w.off_t2);
+    pl.counts = reinterpret_cast<int*>(wsb + w.off_cnt);
+    pl.seqinfo = reinterpret_cast<int*>(wsb + w.off_si);
+    float* states = reinterpret_cast<float*>(wsb + w.off_st);
+    float* Mp = reinterpret_cast<float*>(wsb + w.off_m);
+    float* Sp = reinterpret_cast<float*>(wsb + w.off_s);
+    if (gdn::launch_piece_plan(cc, nseq, p->H, sms, w.e_max, pl, s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    return from_cuda(mark(stage_events, 2, s));
+    c.piece_states = states;
+    // 1. piece 0 of every sequence (the whole sequence when it is not cut) beside the summaries
+    //    of the middle pieces, launched as its programmatic dependent
+    if (mark(stage_events, 1, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ChainParams f1 = c;
+    f1.piece_tab = pl.tab1f;
+    f1.piece_n = pl.counts;
+    ChainParams s1 = c;
+    s1.B = w.e_max;
+    s1.piece_tab = pl.tab1s;
+    s1.piece_n = pl.counts + 1;
+    s1.M = Mp;
+    s1.S = Sp;
+    s1.h_start = nullptr;
+    s1.h_final = nullptr;
+    s1.launch_dependent = 1;
+    if (gdn::launch_tc_forward(f1, s) != cudaSuccess || gdn::launch_tc_summary(s1, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    // 2. the states entering pieces 2 .. k-1 of every cut sequence
+    if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_piece_scan(pl.seqinfo, nseq, p->H, Mp, Sp, states, s) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    // 3. pieces 1 .. k-1 from their states
+    if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ChainParams f2 = c;
+    f2.B = w.e_max;
+    f2.piece_tab = pl.tab2;
+    f2.piece_n = pl.counts + 2;
+    if (gdn::launch_tc_forward(f2, s) != cudaSuccess) return GDN_ERR_CUDA;
+    return from_cuda(mark(stage_events, 4, s));
 }
 
 gdn_status gdn_state_grad_summary(const gdn_problem* p, int nseg, const void* q, const void* k,

@@ -9,6 +9,9 @@
 namespace gdn {
 
 constexpr int kChunk = 64;
+// packed-sequence pieces: ints per table entry (see ChainParams::piece_tab)
+constexpr int kPieceFields = 8;
+enum { PF_SEQ = 0, PF_CHUNK0, PF_NCHUNKS, PF_START, PF_END, PF_MS };
 
 // WY tile pair of one chunk (tensor-core path): A diag(beta), then A diag(beta 2^Gx) (or
 // 2^G for the decayed read). Each factor is lower triangular by 16 x 16 blocks and is stored,
@@ -82,6 +85,14 @@ struct ChainParams {
     const int* cu_seqlens;
     const int* cu_chunks;
     int total_chunks;
+    // packed sequences cut into pieces (tcgen05 path; null otherwise): chain (e, h) of this
+    // launch runs entry e < *piece_n of piece_tab (B bounds the entries) -- kPieceFields ints:
+    // sequence (-1: no chain), first chunk, chunks, start (-1: the sequence's h_start, else a slot of
+    // piece_states), end (-1: the sequence's h_final, -2: not kept, else a slot), summary slot
+    // (M, S at [slot][H][K][K|V]). Slots of piece_states are [slot][H][K][V] fp32.
+    const int* piece_tab;
+    const int* piece_n;
+    float* piece_states;
     int in_bf16;
     int out_bf16;
     int decay_first;   // the read sees the decayed state (inclusive gate on the read side)
@@ -127,6 +138,30 @@ bool tc_scan_supported(const float* M, const float* S, int p_first, int P, int K
 cudaError_t launch_tc_scan(const float* M, const float* S, const float* h_first, float* Hp,
                            float* H_seg, const float* h_seg0, int p_first, int P, int nsub, int BH,
                            DeviceError* err, cudaStream_t s);
+
+// Packed sequences cut into pieces (gdn_varlen.cu): the plan's tables, in the workspace. tab1f
+// [nseq] (piece 0 of every sequence, the first phase's forwards), tab1s [e_max] (the summaries
+// of the middle pieces), tab2 [e_max] (the second phase's forwards), kPieceFields ints each;
+// counts: the entries of the three tables and the piece length chosen; seqinfo [nseq][3]:
+// pieces, first state slot, first summary slot of each sequence.
+struct PiecePlan {
+    int* tab1f;
+    int* tab1s;
+    int* tab2;
+    int* counts;
+    int* seqinfo;
+};
+// whether any plan could cut a sequence (every sequence's chains in one wave, a sequence long
+// enough for two pieces); when not, the chains run as before without the plan's launches
+bool pieces_possible(int T, int nseq, int H, int sms);
+// the plan for nseq sequences (chunk offsets cu_chunks from launch_varlen_meta) and H heads on
+// `sms` SMs, with at most e_max pieces past the first ones (one CTA)
+cudaError_t launch_piece_plan(const int* cu_chunks, int nseq, int H, int sms, int e_max,
+                              const PiecePlan& pl, cudaStream_t s);
+// the scan over each sequence's piece summaries M, S ([slot][H][K][K|V], K = V = 128) into the
+// state slots ([slot][H][K][V]) of its pieces 2 .. k-1, from the state entering piece 1
+cudaError_t launch_piece_scan(const int* seqinfo, int nseq, int H, const float* M, const float* S,
+                              float* states, cudaStream_t s);
 
 // varlen metadata: checks the caller's cu_seqlens [nseq+1] (0 first, T last, non-decreasing)
 // and writes a checked copy to cu_out and cu_chunks[s] = sum over sequences before s of

@@ -227,20 +227,54 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
     const int seg = c.seg_first + chain % c.nseg_run;
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
-    // tokens of this chain: a segment of the fixed-length batch, or a whole varlen sequence
+    // packed sequences cut into pieces: entry b of the piece table (the grid bounds the entries:
+    // chains past this plan's count return at once -- in a summary grid, launched as a
+    // programmatic dependent, after waiting for its primary like its other chains)
+    const int* pent = nullptr;
+    if (VARLEN && c.piece_tab) {
+        if (b >= __ldg(c.piece_n) || __ldg(c.piece_tab + kPieceFields * b + PF_SEQ) < 0) {
+            if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
+            return;
+        }
+        pent = c.piece_tab + kPieceFields * b;
+    }
+    const int vseq = pent ? __ldg(pent + PF_SEQ) : b;         // the packed sequence
+    const int vchunk0 = pent ? __ldg(pent + PF_CHUNK0) : 0;   // the piece's first chunk in it
+    // tokens of this chain: a segment of the fixed-length batch, or a varlen sequence or piece
     // (whose last chunk may be partial: its padding tokens get g = 0 here and beta = 0 in the
     // WY tiles, which leaves the state untouched, and their outputs are not stored)
     // (fixed length: segment 0 may be longer or shorter than the others, see first_chunks)
     const int seg_chunks0 = c.first_chunks > 0 ? c.first_chunks : c.seg_len / kC;
     const int chunk0 = VARLEN || seg == 0 ? 0 : seg_chunks0 + (seg - 1) * (c.seg_len / kC);
     const int seq_tokens =
-        VARLEN ? c.cu_seqlens[b + 1] - c.cu_seqlens[b] : (seg == 0 ? seg_chunks0 * kC : c.seg_len);
+        VARLEN ? min(c.cu_seqlens[vseq + 1] - c.cu_seqlens[vseq] - vchunk0 * kC,
+                     pent ? __ldg(pent + PF_NCHUNKS) * kC : (1 << 30))
+               : (seg == 0 ? seg_chunks0 * kC : c.seg_len);
     const int nchunks = (seq_tokens + kC - 1) / kC;
     constexpr bool need_v = true;   // every CTA forms U (the forward, or the summary's S part)
     const long long limit = p.wait_limit;
     const long long tok_stride = (long long)c.H * kD;   // elements between two tokens of o
-    const long long row_seg = VARLEN ? (long long)c.cu_seqlens[b]   // flattened (b, t)
-                                           : (long long)b * c.T + (long long)chunk0 * kC;
+    const long long row_seg = VARLEN ? (long long)c.cu_seqlens[vseq] + (long long)vchunk0 * kC
+                                     : (long long)b * c.T + (long long)chunk0 * kC;   // flattened (b, t)
+    // the state the chain starts from and the one it ends in (null: zero, not kept), and where
+    // a summary's M and S go
+    const long long kv = (long long)kD * kD;
+    const float* hstart = c.h_start ? c.h_start + seg * c.h_start_seg_stride + bh * kv : nullptr;
+    float* hend = c.h_final && seg == c.nseg_total - 1 ? c.h_final + bh * kv : nullptr;
+    float* msum = SUMMARY ? c.M + ((long long)seg * c.B * c.H + bh) * kv : nullptr;
+    float* ssum = SUMMARY ? c.S + ((long long)seg * c.B * c.H + bh) * kv : nullptr;
+    if (pent) {
+        const int ps = __ldg(pent + PF_START), pe = __ldg(pent + PF_END), pm = __ldg(pent + PF_MS);
+        const long long sh = (long long)vseq * c.H + h;   // the sequence's (s, h)
+        hstart = ps >= 0 ? c.piece_states + ((long long)ps * c.H + h) * kv
+                         : (c.h_start ? c.h_start + sh * kv : nullptr);
+        hend = pe >= 0 ? c.piece_states + ((long long)pe * c.H + h) * kv
+                       : (pe == -1 && c.h_final ? c.h_final + sh * kv : nullptr);
+        if (SUMMARY) {
+            msum = c.M + ((long long)pm * c.H + h) * kv;
+            ssum = c.S + ((long long)pm * c.H + h) * kv;
+        }
+    }
 
     // A forward grid lets a grid launched after it as its programmatic dependent start right
     // away (the summaries that run beside the first piece's forward); a summary grid so
@@ -300,7 +334,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
         // (the M part of a summary needs only the second factor)
         const uint32_t wy_bytes = need_v ? (uint32_t)kWyPairBytes : (uint32_t)kWyTileBytes;
         const uint8_t* wy_chain = reinterpret_cast<const uint8_t*>(c.wy) +
-                                  (VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[b]
+                                  (VARLEN ? (long long)h * c.total_chunks + c.cu_chunks[vseq] + vchunk0
                                           : (long long)bh * (c.T / kC) + chunk0) *
                                       kWyPairBytes;
         int k_last[KST], q_last[2] = {-1, -1}, a_last[2] = {-1, -1}, v_last = -1;
@@ -788,8 +822,8 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
                 float v0 = 0.f;
                 if (SUMMARY)
                     v0 = (m_part && k == st) ? 1.f : 0.f;
-                else if (c.h_start)
-                    v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + st];
+                else if (hstart)
+                    v0 = hstart[(long long)k * kD + st];
                 x[j] = __float_as_uint(v0);
             }
             tmem_st16(t_row + tm_h + 16 * g, x);
@@ -880,13 +914,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
         } else {
             tc_fence_after();
             // ---- the chain's final state H = sigma H_s: thread v writes column v of H
-            float* dst = nullptr;
-            if (SUMMARY) {
-                const long long sb = ((long long)seg * c.B * c.H + bh) * kD * kD;
-                dst = (m_part ? c.M : c.S) + sb;
-            } else if (c.h_final && seg == c.nseg_total - 1) {
-                dst = c.h_final + bhoff;
-            }
+            float* dst = SUMMARY ? (m_part ? msum : ssum) : hend;
             // the forward may also hand its final state to the next segment
             float* dst2 = (!SUMMARY && c.h_out) ? c.h_out + (seg + 1) * c.h_out_seg_stride + bhoff : nullptr;
             if (dst || dst2) {
@@ -947,8 +975,8 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
                 float v0 = 0.f;
                 if (SUMMARY)
                     v0 = (m_part && k == st) ? 1.f : 0.f;
-                else if (c.h_start)
-                    v0 = c.h_start[seg * c.h_start_seg_stride + bhoff + (long long)k * kD + st];
+                else if (hstart)
+                    v0 = hstart[(long long)k * kD + st];
                 x[j] = __float_as_uint(v0);
             }
             tmem_st16(t_row + tm_h + 16 * g, x);
@@ -1111,13 +1139,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
         } else {
             tc_fence_after();
             // ---- the chain's final state H = sigma H_s: thread v writes column v of H
-            float* dst = nullptr;
-            if (SUMMARY) {
-                const long long sb = ((long long)seg * c.B * c.H + bh) * kD * kD;
-                dst = (m_part ? c.M : c.S) + sb;
-            } else if (c.h_final && seg == c.nseg_total - 1) {
-                dst = c.h_final + bhoff;
-            }
+            float* dst = SUMMARY ? (m_part ? msum : ssum) : hend;
             // the forward may also hand its final state to the next segment
             float* dst2 = (!SUMMARY && c.h_out) ? c.h_out + (seg + 1) * c.h_out_seg_stride + bhoff : nullptr;
             if (dst || dst2) {
@@ -1191,12 +1213,15 @@ bool make_params(const ChainParams& c, TcParams* tp) {
 
 template <bool SUMMARY>
 cudaError_t launch(const ChainParams& c, cudaStream_t s) {
-    if (!c.wy || (SUMMARY && c.cu_seqlens)) return cudaErrorInvalidValue;
+    // (a summary over packed sequences: their pieces, from a piece table)
+    if (!c.wy || (SUMMARY && c.cu_seqlens && !c.piece_tab)) return cudaErrorInvalidValue;
     TcParams tp;
     if (!make_params<SUMMARY>(c, &tp)) return cudaErrorInvalidValue;
     // one instance per output type and packing, so that each carries only its own store path
     void (*kern)(TcParams) = tc_chain_kernel<SUMMARY, false, false>;
-    if constexpr (!SUMMARY) {
+    if constexpr (SUMMARY) {
+        if (c.cu_seqlens) kern = tc_chain_kernel<true, true, false>;
+    } else {
         if (c.cu_seqlens)
             kern = c.out_bf16 ? tc_chain_kernel<false, true, true> : tc_chain_kernel<false, true, false>;
         else if (c.out_bf16)

@@ -254,12 +254,13 @@ def gdn_varlen_fwd(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, stre
 
 def gdn_varlen_fwd_timed(q, k, v, g, beta, h0, o, h_final, cu_seqlens, workspace, events,
                          stream=None, prob=None):
-    """gdn_varlen_fwd recording three torch.cuda.Event (enable_timing=True): before the length
-    check and the WY factors, before the chunked forward, after it."""
+    """gdn_varlen_fwd recording five torch.cuda.Event (enable_timing=True): before the length
+    check, the plan and the WY factors; before the first phase (the whole forward when no
+    sequence is cut); before the scan; before the second phase; after it."""
     prob = prob or problem(k, v, o, g=g)
-    if len(events) != 3:
-        raise ValueError("gdn_varlen_fwd_timed takes three events")
-    arr = (_P * 3)(*[e.cuda_event for e in events])
+    if len(events) != 5:
+        raise ValueError("gdn_varlen_fwd_timed takes five events")
+    arr = (_P * 5)(*[e.cuda_event for e in events])
     nseq = int(cu_seqlens.numel()) - 1
     _check(lib().gdn_varlen_fwd_timed(ctypes.byref(prob), nseq, _ptr(cu_seqlens), _ptr(q),
                                       _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),

@@ -134,6 +134,11 @@ WORKLOADS = {
                  g_mu=2, g_sd=1, beta_mu=0, beta_sd=1, h0_sd=0.1, seed=0x6D6E0006,
                  seq_lens=(1800, 1500, 2000, 1200, 800),
                  notes="five packed sequences of the lengths the KDA design page measures"),
+        Workload("varlen8_h16_t32k", B=1, H=16, T=32640, K=128, V=128, nseg=1, in_dtype="bf16",
+                 g_mu=2, g_sd=1, beta_mu=0, beta_sd=1, h0_sd=0.1, seed=0x6D6E0008,
+                 seq_lens=(16384, 8192, 4096, 2048, 1024, 512, 256, 128),
+                 notes="a packed batch whose longest sequence (16K) sets the time unless it is "
+                       "cut into pieces; halving lengths as in a length-bucketed batch"),
     ]
 }
 

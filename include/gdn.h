@@ -338,11 +338,17 @@ GDN_API gdn_status gdn_chunk_bwd_timed(const gdn_problem* p, int nseg, const voi
  * packed in memory: the alignment is in the chunk numbering, not a padded copy.
  * Supported set: p->B == 1, T >= 0 (any length), nseq >= 1, the K/V/dtype set above;
  * bf16 inputs with K == V == 128 and T >= 64 run the tcgen05 kernels, the rest the CUDA-core
- * kernels. */
+ * kernels. On the tcgen05 path, when every sequence's chains fit the SMs at once, a plan made
+ * on the device may cut long sequences into pieces as gdn_segmented_fwd cuts its sequences
+ * (RFC section 2.2): piece 0's forward beside the summaries of the middle pieces, their scan,
+ * then the forwards of the other pieces, so that a long sequence no longer sets the time
+ * alone. The results are those of the uncut recurrence within the bf16 tolerance. */
 
 /* Workspace bytes for gdn_varlen_fwd: the error word, the WY tiles of at most T/64 + nseq
- * chunks per head (tensor-core shapes) and two int arrays of nseq + 1. Depends on T, H, K,
- * V, the dtypes and nseq only, not on the lengths. Returns 0 for an invalid problem. */
+ * chunks per head (tensor-core shapes), two int arrays of nseq + 1 and (tensor-core shapes)
+ * the piece plan: its tables and, for at most 256 / H pieces past the first ones, their fp32
+ * states and summaries (about 48 MiB at K = V = 128). Depends on T, H, K, V, the dtypes and
+ * nseq only, not on the lengths. Returns 0 for an invalid problem. */
 GDN_API size_t gdn_varlen_workspace_bytes(const gdn_problem* p, int nseq);
 
 /* Chunked forward of every packed sequence (RFC section 2.1 per sequence).
@@ -361,9 +367,10 @@ GDN_API gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_
                                   const void* beta, const float* h0, void* o, float* h_final,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
-/* gdn_varlen_fwd with stage markers: if stage_events is non-NULL it points to three
- * cudaEvent_t recorded on `stream` before the length check and WY-factor launches, before
- * the chunked forward, and after it. Same results as gdn_varlen_fwd. */
+/* gdn_varlen_fwd with stage markers: if stage_events is non-NULL it points to five
+ * cudaEvent_t recorded on `stream` before the length check, the plan and the WY-factor
+ * launches; before the first phase (the whole forward when no sequence is cut); before the
+ * scan; before the second phase; and after it. Same results as gdn_varlen_fwd. */
 GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_seqlens,
                                         const void* q, const void* k, const void* v,
                                         const void* g, const void* beta, const float* h0,

@@ -126,9 +126,22 @@ def test_varlen_workspace_and_validation(L):
     # then two int32 arrays of nseq + 1 (each region 256-byte aligned)
     p = P(B=1, T=7300, H=16)
     wy = 16 * (7300 // 64 + 5) * 10240
-    assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 5) == 256 + wy + 256 + 256
+
+    def rup(n):
+        return (n + 255) // 256 * 256
+
+    def pieces(nseq, H):
+        # the piece plan (tcgen05 shapes): three tables of 8-int entries (nseq, e_max, e_max),
+        # four counts, three ints per sequence, then fp32 states, M and S for e_max = 256 / H
+        # pieces past the first ones
+        e = max(1, 256 // H)
+        return (rup(32 * nseq) + 2 * rup(32 * e) + rup(16) + rup(12 * nseq) +
+                3 * rup(4 * e * H * 128 * 128))
+
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 5) == 256 + wy + 256 + 256 + pieces(5, 16)
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=7300, H=16, in_dtype=0)), 5) == 768
-    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=0)), 1) == 256 + 2 * 10240 + 512
+    assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, T=0)), 1) == (256 + 2 * 10240 + 512 +
+                                                                          pieces(1, 2))
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=2, T=7300)), 5) == 0   # B must be 1
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 0) == 0
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(P(B=1, K=96, V=96)), 1) == 0

@@ -35,7 +35,13 @@ CASES = {
     "f32_k64": packed((70, 0, 129, 5), K=64, in_dtype="f32"),
     "bf16_k64": packed((70, 200, 1), K=64),
     "no_initial_state": packed((65, 190), h0=False),
+    # long enough for the device plan to cut them into pieces (gdn_varlen.cu): the first into
+    # eight of 8 chunks (six scan steps), a ragged last chunk in a cut sequence
+    "cut_long_first": packed((4096, 100, 300, 64), H=4),
+    "cut_ragged": packed((3000, 37, 700), H=2),
+    "cut_no_initial_state": packed((3200, 900), H=3, h0=False),
 }
+CUT = ("cut_long_first", "cut_ragged", "cut_no_initial_state")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -91,7 +97,7 @@ def test_varlen_matches_oracle(name):
             assert not hf[s].any(), s   # empty sequence from a zero state
 
 
-@pytest.mark.parametrize("name", ["five_scaled", "edge_lengths", "f32_k64"])
+@pytest.mark.parametrize("name", ["five_scaled", "edge_lengths", "f32_k64", "cut_long_first"])
 def test_varlen_decayed_read(name):
     w = CASES[name]
     x = synth.make_inputs(w)
@@ -103,8 +109,9 @@ def test_varlen_decayed_read(name):
     assert rel_err(np64(hf), hf_ref) <= tol
 
 
-def test_varlen_bf16_output():
-    w = CASES["five_scaled"]
+@pytest.mark.parametrize("name", ["five_scaled", "cut_ragged"])
+def test_varlen_bf16_output(name):
+    w = CASES[name]
     x = synth.make_inputs(w)
     o, hf, st, _ = run_varlen(w, x, out_dtype=torch.bfloat16)
     assert st == 0 and o.dtype == torch.bfloat16
@@ -138,8 +145,9 @@ def test_varlen_bad_lengths_are_reported(cu):
     assert st == 0 and torch.isfinite(o).all()
 
 
-def test_varlen_deterministic():
-    w = CASES["edge_lengths"]
+@pytest.mark.parametrize("name", ["edge_lengths", "cut_long_first"])
+def test_varlen_deterministic(name):
+    w = CASES[name]
     x = synth.make_inputs(w)
     o1, hf1, _, _ = run_varlen(w, x)
     o2, hf2, _, _ = run_varlen(w, x)
@@ -160,3 +168,45 @@ def test_varlen_full_size_sampled_heads():
                                                  cu, x["h0"][:, h:h + 1])
         assert rel_err(np64(o[:, :, h:h + 1]), o_ref) <= TOL_BF16, h
         assert rel_err(np64(hf[:, h:h + 1]), hf_ref) <= TOL_BF16, h
+
+
+def test_varlen_cut_timed_matches_plain():
+    # with the long sequence cut, the timed entry point (five stage events between the plan's
+    # launches) gives the plain call's results bit for bit
+    w = CASES["cut_long_first"]
+    x = synth.make_inputs(w)
+    o, hf, _, _ = run_varlen(w, x)
+    dt = torch.bfloat16
+    d = {n: torch.from_numpy(x[n]).cuda().to(dt).contiguous() for n in ("q", "k", "v", "g", "beta")}
+    h0 = torch.from_numpy(x["h0"]).cuda().contiguous()
+    cu = torch.from_numpy(synth.cu_seqlens(w)).cuda()
+    nseq = len(w.seq_lens)
+    o2 = torch.full_like(o, float("nan"))
+    hf2 = torch.full_like(hf, float("nan"))
+    prob = gdn.problem(d["k"], d["v"], o2)
+    ws = gdn.alloc_varlen_workspace(prob, nseq)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    gdn.gdn_varlen_fwd_timed(d["q"], d["k"], d["v"], d["g"], d["beta"], h0, o2, hf2, cu, ws, ev,
+                             prob=prob)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hf, hf2)
+    assert gdn.gdn_check_device_error(ws)[0] == 0
+
+
+def test_varlen_cut_full_size_sampled_heads():
+    # a packed batch whose 16K-token sequence is cut into pieces (H = 16, K = V = 128), checked
+    # on sampled heads against the oracle's per-sequence recurrence
+    w = synth.WORKLOADS["varlen8_h16_t32k"]
+    x = synth.make_inputs(w)
+    o, hf, st, _ = run_varlen(w, x)
+    assert st == 0
+    assert torch.isfinite(o).all() and torch.isfinite(hf).all()
+    cu = synth.cu_seqlens(w)
+    for h in (0, 9):
+        xs = {n: x[n][:, :, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+        o_ref, hf_ref = oracle.varlen_recurrence(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"],
+                                                 cu, x["h0"][:, h:h + 1])
+        assert rel_err(np64(o[:, :, h:h + 1]), o_ref, label=f"o {h}") <= TOL_BF16, h
+        assert rel_err(np64(hf[:, h:h + 1]), hf_ref, label=f"h_final {h}") <= TOL_BF16, h
+        a, b = int(cu[0]), int(cu[1])   # the cut sequence on its own scale
+        assert rel_err(np64(o[:, a:b, h:h + 1]), o_ref[:, a:b]) <= TOL_BF16, h
