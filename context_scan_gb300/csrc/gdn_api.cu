@@ -396,8 +396,8 @@ VarlenLayout varlen_layout(const gdn_problem& p, int nseq) {
         w.off_t1s = w.off_t1f + round_up(ent * (size_t)nseq);
         w.off_t2 = w.off_t1s + round_up(ent * (size_t)w.e_max);
         w.off_cnt = w.off_t2 + round_up(ent * (size_t)w.e_max);
-        w.off_si = w.off_cnt + round_up(sizeof(int) * 4);
-        w.off_st = w.off_si + round_up(sizeof(int) * 3 * (size_t)nseq);
+        w.off_si = w.off_cnt + round_up(sizeof(int) * 8);
+        w.off_st = w.off_si + round_up(sizeof(int) * 4 * (size_t)nseq);
         w.off_m = w.off_st + round_up(sizeof(float) * (size_t)w.e_max * p.H * kv);
         w.off_s = w.off_m + round_up(sizeof(float) * (size_t)w.e_max * p.H * kk);
         w.total = w.off_s + round_up(sizeof(float) * (size_t)w.e_max * p.H * kv);
@@ -658,11 +658,6 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     char* wsb = reinterpret_cast<char*>(workspace);
     int* cu = reinterpret_cast<int*>(wsb + w.off_cu);
     int* cc = reinterpret_cast<int*>(wsb + w.off_cc);
-    // the chains read the checked copy of the lengths, never the caller's array
-    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_varlen_meta(cu_seqlens, nseq, p->T, cu, cc,
-                                reinterpret_cast<gdn::DeviceError*>(workspace), s) != cudaSuccess)
-        return GDN_ERR_CUDA;
     ChainParams c = base_params(p, workspace);
     c.B = nseq;   // one chain per (sequence, head), or per piece below
     c.q = q;
@@ -681,11 +676,29 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     c.total_chunks = w.chunk_bound;
     c.wy = wsb + w.off_wy;
     const bool tc = use_tc(c) && p->T >= gdn::kChunk;   // (a tensor map box holds 64 tokens)
+    const int sms = std::min(sm_count(), kPieceSmBound);
+    const bool pieces = tc && w.pieces && gdn::pieces_possible(p->T, nseq, p->H, sms);
+    // long sequences cut into pieces for the tcgen05 chains (gdn_varlen.cu): the plan's tables
+    gdn::PiecePlan pl{};
+    if (pieces) {
+        pl.tab1f = reinterpret_cast<int*>(wsb + w.off_t1f);
+        pl.tab1s = reinterpret_cast<int*>(wsb + w.off_t1s);
+        pl.tab2 = reinterpret_cast<int*>(wsb + w.off_t2);
+        pl.counts = reinterpret_cast<int*>(wsb + w.off_cnt);
+        pl.seqinfo = reinterpret_cast<int*>(wsb + w.off_si);
+    }
+    // the chains read the checked copy of the lengths, never the caller's array; the plan, when
+    // a cut is possible, is made in the same block right after the check
+    if (mark(stage_events, 0, s) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::DeviceError* derr = reinterpret_cast<gdn::DeviceError*>(workspace);
+    if ((pieces ? gdn::launch_varlen_meta_plan(cu_seqlens, nseq, p->T, cu, cc, derr, p->H, sms,
+                                               w.e_max, pl, s)
+                : gdn::launch_varlen_meta(cu_seqlens, nseq, p->T, cu, cc, derr, s)) != cudaSuccess)
+        return GDN_ERR_CUDA;
     if (tc && gdn::launch_tc_wy(c, s) != cudaSuccess) return GDN_ERR_CUDA;
     if (kda_prep_shape(*p) && p->T > 0 && gdn::launch_kda_prep(c, s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    const int sms = std::min(sm_count(), kPieceSmBound);
-    if (!tc || !w.pieces || !gdn::pieces_possible(p->T, nseq, p->H, sms)) {
+    if (!pieces) {
         if (mark(stage_events, 1, s) != cudaSuccess || mark(stage_events, 2, s) != cudaSuccess ||
             mark(stage_events, 3, s) != cudaSuccess)
             return GDN_ERR_CUDA;
@@ -693,18 +706,9 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
             return GDN_ERR_CUDA;
         return from_cuda(mark(stage_events, 4, s));
     }
-    // the tcgen05 chains: long sequences cut into pieces, planned on the device (gdn_varlen.cu)
-    gdn::PiecePlan pl;
-    pl.tab1f = reinterpret_cast<int*>(wsb + w.off_t1f);
-    pl.tab1s = reinterpret_cast<int*>(wsb + w.off_t1s);
-    pl.tab2 = reinterpret_cast<int*>(wsb + w.off_t2);
-    pl.counts = reinterpret_cast<int*>(wsb + w.off_cnt);
-    pl.seqinfo = reinterpret_cast<int*>(wsb + w.off_si);
     float* states = reinterpret_cast<float*>(wsb + w.off_st);
     float* Mp = reinterpret_cast<float*>(wsb + w.off_m);
     float* Sp = reinterpret_cast<float*>(wsb + w.off_s);
-    if (gdn::launch_piece_plan(cc, nseq, p->H, sms, w.e_max, pl, s) != cudaSuccess)
-        return GDN_ERR_CUDA;
     c.piece_states = states;
     // 1. piece 0 of every sequence (the whole sequence when it is not cut) beside the summaries
     //    of the middle pieces, launched as its programmatic dependent
@@ -723,16 +727,19 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     s1.launch_dependent = 1;
     if (gdn::launch_tc_forward(f1, s) != cudaSuccess || gdn::launch_tc_summary(s1, s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    // 2. the states entering pieces 2 .. k-1 of every cut sequence
+    // 2. the states entering pieces 2 .. k-1 of every cut sequence (the summary grid's
+    //    programmatic dependent)
     if (mark(stage_events, 2, s) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_piece_scan(pl.seqinfo, nseq, p->H, Mp, Sp, states, s) != cudaSuccess)
+    if (gdn::launch_piece_scan(pl, nseq, p->H, w.e_max, sms, Mp, Sp, states, s) != cudaSuccess)
         return GDN_ERR_CUDA;
-    // 3. pieces 1 .. k-1 from their states
+    // 3. pieces 1 .. k-1 from their states (the scan's programmatic dependent: its chains set
+    //    up while the scan runs and wait for it before they read a state)
     if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
     ChainParams f2 = c;
     f2.B = w.e_max;
     f2.piece_tab = pl.tab2;
     f2.piece_n = pl.counts + 2;
+    f2.launch_dependent = 1;
     if (gdn::launch_tc_forward(f2, s) != cudaSuccess) return GDN_ERR_CUDA;
     return from_cuda(mark(stage_events, 4, s));
 }

@@ -142,8 +142,9 @@ cudaError_t launch_tc_scan(const float* M, const float* S, const float* h_first,
 // Packed sequences cut into pieces (gdn_varlen.cu): the plan's tables, in the workspace. tab1f
 // [nseq] (piece 0 of every sequence, the first phase's forwards), tab1s [e_max] (the summaries
 // of the middle pieces), tab2 [e_max] (the second phase's forwards), kPieceFields ints each;
-// counts: the entries of the three tables and the piece length chosen; seqinfo [nseq][3]:
-// pieces, first state slot, first summary slot of each sequence.
+// counts [8]: the entries of the three tables, the piece length chosen and the scan's jobs;
+// seqinfo [4 nseq]: pieces, first state slot and first summary slot of each sequence
+// ([nseq][3]), then the scan's jobs (the sequences cut into three pieces or more, in order).
 struct PiecePlan {
     int* tab1f;
     int* tab1s;
@@ -154,14 +155,12 @@ struct PiecePlan {
 // whether any plan could cut a sequence (every sequence's chains in one wave, a sequence long
 // enough for two pieces); when not, the chains run as before without the plan's launches
 bool pieces_possible(int T, int nseq, int H, int sms);
-// the plan for nseq sequences (chunk offsets cu_chunks from launch_varlen_meta) and H heads on
-// `sms` SMs, with at most e_max pieces past the first ones (one CTA)
-cudaError_t launch_piece_plan(const int* cu_chunks, int nseq, int H, int sms, int e_max,
-                              const PiecePlan& pl, cudaStream_t s);
-// the scan over each sequence's piece summaries M, S ([slot][H][K][K|V], K = V = 128) into the
-// state slots ([slot][H][K][V]) of its pieces 2 .. k-1, from the state entering piece 1
-cudaError_t launch_piece_scan(const int* seqinfo, int nseq, int H, const float* M, const float* S,
-                              float* states, cudaStream_t s);
+// the scan over each job's piece summaries M, S ([slot][H][K][K|V], K = V = 128) into the state
+// slots ([slot][H][K][V]) of its pieces 2 .. k-1, from the state entering piece 1, on at most
+// `sms` CTAs; launched as the programmatic dependent of the summary grid before it (and the
+// second phase as its own)
+cudaError_t launch_piece_scan(const PiecePlan& pl, int nseq, int H, int e_max, int sms,
+                              const float* M, const float* S, float* states, cudaStream_t s);
 
 // varlen metadata: checks the caller's cu_seqlens [nseq+1] (0 first, T last, non-decreasing)
 // and writes a checked copy to cu_out and cu_chunks[s] = sum over sequences before s of
@@ -170,6 +169,11 @@ cudaError_t launch_piece_scan(const int* seqinfo, int nseq, int H, const float* 
 // kernels that read them stay inside the buffers.
 cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
                                DeviceError* err, cudaStream_t s);
+// the same check followed, in the same block, by the plan for the nseq sequences and H heads on
+// `sms` SMs, with at most e_max pieces past the first ones (gdn_varlen.cu)
+cudaError_t launch_varlen_meta_plan(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
+                                    DeviceError* err, int H, int sms, int e_max,
+                                    const PiecePlan& pl, cudaStream_t s);
 
 // State-gradient summaries (backward): chain (b, h, seg) walks segment seg's chunks from the
 // last to the first, starting from dH_end[seg] ([nseg][B][H][K][V], or zero when null), and

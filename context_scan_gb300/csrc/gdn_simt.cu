@@ -514,47 +514,6 @@ cudaError_t launch_scan_k(const float* M, const float* S, const float* h_first, 
     return cudaGetLastError();
 }
 
-// Varlen metadata in one block: each thread checks and sums a contiguous run of sequences,
-// a block scan turns the per-thread chunk counts into the run's first chunk index.
-constexpr int kMetaThreads = 256;
-constexpr unsigned kTagVarlen = 201;   // detail word of a rejected cu_seqlens
-
-__global__ void __launch_bounds__(kMetaThreads) varlen_meta_kernel(
-    const int* __restrict__ cu_in, int nseq, int T, int* __restrict__ cu_out,
-    int* __restrict__ cu_chunks, DeviceError* err) {
-    __shared__ long long part[kMetaThreads];
-    const int t = threadIdx.x;
-    const int per = (nseq + kMetaThreads - 1) / kMetaThreads;
-    const int s0 = min(nseq, t * per), s1 = min(nseq, s0 + per);
-    bool bad = t == 0 && (cu_in[0] != 0 || cu_in[nseq] != T);
-    long long acc = 0;
-    for (int s = s0; s < s1; ++s) {
-        const long long len = (long long)cu_in[s + 1] - cu_in[s];
-        bad |= len < 0;
-        acc += (len + kChunk - 1) / kChunk;
-    }
-    bad = __syncthreads_or(bad);
-    part[t] = acc;
-    __syncthreads();
-    for (int off = 1; off < kMetaThreads; off <<= 1) {   // inclusive scan
-        const long long x = t >= off ? part[t - off] : 0;
-        __syncthreads();
-        part[t] += x;
-        __syncthreads();
-    }
-    long long run = part[t] - acc;
-    for (int s = s0; s < s1; ++s) {
-        cu_out[s] = bad ? 0 : cu_in[s];
-        cu_chunks[s] = bad ? 0 : (int)run;
-        run += ((long long)cu_in[s + 1] - cu_in[s] + kChunk - 1) / kChunk;
-    }
-    if (t == 0) {
-        cu_out[nseq] = bad ? 0 : T;
-        cu_chunks[nseq] = bad ? 0 : (int)part[kMetaThreads - 1];
-        if (bad && err && atomicCAS(&err->code, 0u, (unsigned)GDN_ERR_INVALID_ARG) == 0u)
-            atomicExch(&err->detail, kTagVarlen);
-    }
-}
 }  // namespace
 
 cudaError_t launch_simt_forward(const ChainParams& p, cudaStream_t s) {
@@ -574,13 +533,6 @@ cudaError_t launch_scan(const float* M, const float* S, const float* h_first, fl
     if (K == 128) return launch_scan_k<128>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     if (K == 64) return launch_scan_k<64>(M, S, h_first, Hp, H_seg, h_seg0, p_first, P, nsub, BH, V, s);
     return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
-                               DeviceError* err, cudaStream_t s) {
-    if (!cu_in || !cu_out || !cu_chunks || nseq < 1) return cudaErrorInvalidValue;
-    varlen_meta_kernel<<<1, kMetaThreads, 0, s>>>(cu_in, nseq, T, cu_out, cu_chunks, err);
-    return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -228,12 +228,12 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
     const int bh = chain / c.nseg_run;
     const int b = bh / c.H, h = bh % c.H;
     // packed sequences cut into pieces: entry b of the piece table (the grid bounds the entries:
-    // chains past this plan's count return at once -- in a summary grid, launched as a
-    // programmatic dependent, after waiting for its primary like its other chains)
+    // chains past this plan's count return at once -- in a grid launched as a programmatic
+    // dependent, after waiting for its primary like its other chains)
     const int* pent = nullptr;
     if (VARLEN && c.piece_tab) {
         if (b >= __ldg(c.piece_n) || __ldg(c.piece_tab + kPieceFields * b + PF_SEQ) < 0) {
-            if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (SUMMARY || c.launch_dependent) asm volatile("griddepcontrol.wait;" ::: "memory");
             return;
         }
         pent = c.piece_tab + kPieceFields * b;
@@ -812,7 +812,9 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
              : group_wait<4, 128>(warp == 4, lane == 0, (bar), (parity), true, go, abort_flag,   \
                                   limit, c.err, (tag)))
 
-        // ---- initial state: row `st` of H^T (= column st of H), sigma = 1
+        // ---- initial state: row `st` of H^T (= column st of H), sigma = 1 (a forward grid
+        // launched as a programmatic dependent reads it only once its primary has completed)
+        if (!SUMMARY && c.launch_dependent) asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
         for (int g = 0; g < 8; ++g) {
             uint32_t x[16];
@@ -965,7 +967,9 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
 #define smma_wait() \
     (swait(bar_s, bars_phase, TAG_BARS) ? (bars_phase ^= 1u, bars_pending = false, true) : false)
 
-        // ---- initial state: row `st` of H^T (= column st of H), sigma = 1
+        // ---- initial state: row `st` of H^T (= column st of H), sigma = 1 (a forward grid
+        // launched as a programmatic dependent reads it only once its primary has completed)
+        if (!SUMMARY && c.launch_dependent) asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
         for (int g = 0; g < 8; ++g) {
             uint32_t x[16];
@@ -1170,9 +1174,9 @@ __device__ __forceinline__ void chain_body(const TcParams& p, const int chain) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(F::TMEM_COLS)
                      : "memory");
-    // a summary grid launched as a programmatic dependent completes after its primary grid
-    // (a no-op otherwise), so the launches that follow it in the stream see both finished
-    if (SUMMARY) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // a grid launched as a programmatic dependent completes after its primary grid (a no-op
+    // otherwise), so the launches that follow it in the stream see both finished
+    if (SUMMARY || c.launch_dependent) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <bool SUMMARY, bool VARLEN, bool OUT_BF16>

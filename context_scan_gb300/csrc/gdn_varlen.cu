@@ -20,6 +20,7 @@
 // sequence runs whole (as before).
 // The pieces of a sequence are ceil(n_s / k_s) chunks each, the last one the rest; a sequence
 // left whole runs in the first phase while it has room, else in the second.
+#include <algorithm>
 #include <climits>
 
 #include "gdn_internal.h"
@@ -47,94 +48,65 @@ __device__ __forceinline__ void put_entry(int* tab, int e, int seq, int chunk0, 
     t[7] = 0;
 }
 
-// block-wide exclusive prefix sum (in thread order)
-__device__ long long block_excl(long long x, long long* buf) {
-    const int t = threadIdx.x;
-    __syncthreads();
-    buf[t] = x;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {
-        const long long y = t >= off ? buf[t - off] : 0;
-        __syncthreads();
-        buf[t] += y;
-        __syncthreads();
-    }
-    return buf[t] - x;
-}
-
-__device__ __forceinline__ long long warp_sum(long long x) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
-}
 __device__ __forceinline__ int warp_max(int x) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, off));
     return x;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) piece_plan_kernel(const int* __restrict__ cc, int nseq,
-                                                                  int H, int sms, int e_max,
-                                                                  PiecePlan pl) {
-    __shared__ long long buf[kPlanThreads];
-    __shared__ int nsh[kPlanThreads];              // the lengths, when a cut is possible
-    __shared__ long long best_cost[kPlanThreads / 32];
-    __shared__ int best_x[kPlanThreads / 32], wmax[kPlanThreads / 32];
+// The plan (one CTA of kPlanThreads, after the length check): cc = the checked chunk offsets,
+// written by this block, read through L2.
+__device__ void plan_body(const int* cc, int nseq, int H, int sms, int e_max, const PiecePlan& pl) {
+    __shared__ int nsh[kPlanThreads];   // the lengths in chunks, when a cut is possible
+    __shared__ unsigned long long wbest[kPlanThreads / 32];
+    __shared__ int wmax[kPlanThreads / 32];
+    __shared__ int wsum[4][kPlanThreads / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int cap = sms / H;   // chains of one phase, in (sequence or piece) entries of H chains
     // a cut needs every sequence's chains in one wave, so then there is a thread per sequence
     const bool may_cut = nseq <= cap && nseq <= kPlanThreads;
     int maxn = 0;
-    for (int s = t; s < nseq; s += kPlanThreads) maxn = max(maxn, cc[s + 1] - cc[s]);
+    for (int s = t; s < nseq; s += kPlanThreads) maxn = max(maxn, __ldcg(cc + s + 1) - __ldcg(cc + s));
     maxn = warp_max(maxn);
     if (lane == 0) wmax[warp] = maxn;
-    if (may_cut && t < nseq) nsh[t] = cc[t + 1] - cc[t];
+    if (may_cut && t < nseq) nsh[t] = __ldcg(cc + t + 1) - __ldcg(cc + t);
     __syncthreads();
     for (int w = 0; w < kPlanThreads / 32; ++w) maxn = max(maxn, wmax[w]);
-    // candidate piece lengths X = kMinPiece, growing by an eighth, below maxn; warp w costs
-    // every eighth of them: with k_s = ceil(n_s / X), A = the pieces past the first ones of the
-    // cut sequences (entries in each phase), U = the sequences left whole (one entry in either
-    // phase), both phases within `cap` entries; the time 2 X + the scan's steps (which run in
-    // sequence for each sequence) + the fixed cost of a cut, in chunk times
-    long long my_cost = maxn;   // the sequences run whole
-    int my_x = maxn;
+    // candidate piece lengths X_0 = kMinPiece, X_{i+1} = X_i + max(1, X_i / 8), below maxn (at
+    // most ~130 of them for any length that fits an int): thread t costs X_t. With
+    // k_s = ceil(n_s / X), A = the pieces past the first ones of the cut sequences (entries in
+    // each phase), U = the sequences left whole (one entry in either phase), both phases
+    // within `cap` entries; the time 2 X + the scan's steps (which run in sequence for each
+    // sequence) + the fixed cost of a cut, in chunk times. Key: (time, X), the smallest wins;
+    // running the sequences whole costs maxn.
+    unsigned long long best = ((unsigned long long)maxn << 32) | (unsigned)maxn;
     if (may_cut && maxn >= 2 * kMinPiece) {
-        int i = 0;
-        for (int x = kMinPiece; x < maxn; x += max(1, x / 8), ++i) {
-            if (i % (kPlanThreads / 32) != warp) continue;
+        int x = kMinPiece;
+        for (int i = 0; i < t && x < maxn; ++i) x += max(1, x / 8);
+        if (x < maxn) {
             long long A = 0, U = 0;
             int steps = 0;
-            for (int s = lane; s < nseq; s += 32) {
+            for (int s = 0; s < nseq; ++s) {
                 const int n = nsh[s];
                 const int k = n > 0 ? (n + x - 1) / x : 1;
-                A += k > 1 ? k - 1 : 0;
+                A += k - 1;
                 U += k == 1 ? 1 : 0;
                 steps = max(steps, k - 2);
             }
-            A = warp_sum(A);
-            U = warp_sum(U);
-            steps = warp_max(steps);
             const bool fits = A <= cap && 2 * A + U <= 2LL * cap && A <= e_max;
             const long long cost = 2LL * x + (long long)kStepChunks * steps + kCutChunks;
-            if (fits && cost < my_cost) {
-                my_cost = cost;
-                my_x = x;
-            }
+            if (fits && cost < maxn) best = ((unsigned long long)cost << 32) | (unsigned)x;
         }
     }
-    if (lane == 0) {
-        best_cost[warp] = my_cost;
-        best_x[warp] = my_x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o < best ? o : best;
     }
+    if (lane == 0) wbest[warp] = best;
     __syncthreads();
-    int X = maxn;
-    long long bc = maxn;
-    for (int w = 0; w < kPlanThreads / 32; ++w)
-        if (best_cost[w] < bc || (best_cost[w] == bc && best_x[w] < X)) {
-            bc = best_cost[w];
-            X = best_x[w];
-        }
-    if (X < 1) X = 1;
+    for (int w = 0; w < kPlanThreads / 32; ++w) best = wbest[w] < best ? wbest[w] : best;
+    const int X = max(1, (int)(best & 0xffffffffu));
     if (X >= maxn || !may_cut) {
         // nothing cut: every sequence whole, in the first phase
         for (int s = t; s < nseq; s += kPlanThreads) {
@@ -148,27 +120,44 @@ __global__ void __launch_bounds__(kPlanThreads) piece_plan_kernel(const int* __r
             pl.counts[1] = 0;
             pl.counts[2] = 0;
             pl.counts[3] = maxn;
+            pl.counts[4] = 0;
         }
         return;
     }
     // a thread per sequence: its pieces, the slots of their states and summaries, and, for a
-    // sequence left whole, the phase it runs in (the first while that has room)
+    // sequence left whole, the phase it runs in (the first while that has room). Four
+    // exclusive prefix sums in thread order (warp scans, then the warps' totals): the first
+    // state slot (and second-phase entry), the first summary slot, the rank among the whole
+    // sequences and the rank among the sequences the scan visits (k >= 3).
     const bool mine = t < nseq;
     const int n = mine ? nsh[t] : 0;
     const int k = mine ? (n > 0 ? (n + X - 1) / X : 1) : 0;
-    const long long sig = block_excl(k > 1 ? k - 1 : 0, buf);   // state slots (and phase-2 entries)
-    const long long mu = block_excl(k > 2 ? k - 2 : 0, buf);    // summary slots
-    const long long u = block_excl(mine && k == 1 ? 1 : 0, buf);   // rank among whole ones
-    // the totals: the last thread's exclusive sum plus its own
-    __shared__ long long tot[3];
-    if (t == kPlanThreads - 1) {
-        tot[0] = sig + (k > 1 ? k - 1 : 0);
-        tot[1] = mu + (k > 2 ? k - 2 : 0);
-        tot[2] = u + (mine && k == 1 ? 1 : 0);
+    int v[4] = {k > 1 ? k - 1 : 0, k > 2 ? k - 2 : 0, mine && k == 1 ? 1 : 0, k > 2 ? 1 : 0};
+    int in[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int y = __shfl_up_sync(0xffffffffu, in[q], off);
+            if (lane >= off) in[q] += y;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wsum[q][warp] = in[q];
     }
     __syncthreads();
-    const long long A = tot[0], U = tot[2];
-    const long long room1 = cap - A;   // whole sequences in the first phase
+    int tot[4] = {0, 0, 0, 0};
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (w == warp) in[q] += tot[q] - v[q];   // inclusive -> exclusive, plus the warps before
+            tot[q] += wsum[q][w];
+        }
+    }
+    const int sig = in[0], mu = in[1], u = in[2];
+    const int A = tot[0], NM = tot[1], U = tot[2];
+    const int room1 = cap - A;   // whole sequences in the first phase
     if (mine) {
         const int s = t;
         const int xs = k > 1 ? (n + k - 1) / k : n;   // chunks of each piece but the last
@@ -177,32 +166,84 @@ __global__ void __launch_bounds__(kPlanThreads) piece_plan_kernel(const int* __r
                 put_entry(pl.tab1f, s, s, 0, INT_MAX / kChunk, -1, -1, -1);
             } else {   // in the second phase, after the cut sequences' pieces
                 put_entry(pl.tab1f, s, -1, 0, 0, -2, -2, -1);   // (no chain here)
-                put_entry(pl.tab2, (int)(A + u - room1), s, 0, INT_MAX / kChunk, -1, -1, -1);
+                put_entry(pl.tab2, A + u - room1, s, 0, INT_MAX / kChunk, -1, -1, -1);
             }
         } else {
             // piece 0 from the sequence's initial state; it ends in the state entering piece 1
-            put_entry(pl.tab1f, s, s, 0, xs, -1, (int)sig, -1);
+            put_entry(pl.tab1f, s, s, 0, xs, -1, sig, -1);
             for (int p = 1; p <= k - 2; ++p)   // the summaries of the middle pieces
-                put_entry(pl.tab1s, (int)mu + p - 1, s, p * xs, xs, -2, -2, (int)mu + p - 1);
+                put_entry(pl.tab1s, mu + p - 1, s, p * xs, xs, -2, -2, mu + p - 1);
             for (int p = 1; p <= k - 1; ++p)   // the forwards of pieces 1 .. k-1 from their states
-                put_entry(pl.tab2, (int)sig + p - 1, s, p * xs, p == k - 1 ? n - p * xs : xs,
-                          (int)sig + p - 1, p == k - 1 ? -1 : -2, -1);
+                put_entry(pl.tab2, sig + p - 1, s, p * xs, p == k - 1 ? n - p * xs : xs,
+                          sig + p - 1, p == k - 1 ? -1 : -2, -1);
         }
         pl.seqinfo[3 * s] = k;
-        pl.seqinfo[3 * s + 1] = (int)sig;
-        pl.seqinfo[3 * s + 2] = (int)mu;
+        pl.seqinfo[3 * s + 1] = sig;
+        pl.seqinfo[3 * s + 2] = mu;
+        if (k > 2) pl.seqinfo[3 * nseq + in[3]] = s;   // the scan's job list
     }
     if (t == 0) {
         pl.counts[0] = nseq;
-        pl.counts[1] = (int)tot[1];
-        pl.counts[2] = (int)(A + (U > room1 ? U - room1 : 0));
+        pl.counts[1] = NM;
+        pl.counts[2] = A + (U > room1 ? U - room1 : 0);
         pl.counts[3] = X;
+        pl.counts[4] = tot[3];
     }
 }
 
-// The scan of one sequence's pieces on one 16-column tile of the state (one CTA per sequence,
-// head and tile; 512 threads): the state entering piece 1 (written by piece 0's forward), then
-// H_{p+1} = M_p H_p + S_p for p = 1 .. k-2, each written to its slot. fp32 CUDA cores. The
+// The length check in one block: each thread checks and sums a contiguous run of sequences, a
+// block scan turns the per-thread chunk counts into the run's first chunk index. With PLAN,
+// the plan follows in the same block.
+constexpr unsigned kTagVarlen = 201;   // detail word of a rejected cu_seqlens
+
+template <bool PLAN>
+__global__ void __launch_bounds__(kPlanThreads) varlen_meta_kernel(
+    const int* __restrict__ cu_in, int nseq, int T, int* cu_out, int* cu_chunks, DeviceError* err,
+    int H, int sms, int e_max, PiecePlan pl) {
+    __shared__ long long part[kPlanThreads];
+    const int t = threadIdx.x;
+    const int per = (nseq + kPlanThreads - 1) / kPlanThreads;
+    const int s0 = min(nseq, t * per), s1 = min(nseq, s0 + per);
+    bool bad = t == 0 && (cu_in[0] != 0 || cu_in[nseq] != T);
+    long long acc = 0;
+    for (int s = s0; s < s1; ++s) {
+        const long long len = (long long)cu_in[s + 1] - cu_in[s];
+        bad |= len < 0;
+        acc += (len + kChunk - 1) / kChunk;
+    }
+    bad = __syncthreads_or(bad);
+    part[t] = acc;
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {   // inclusive scan
+        const long long x = t >= off ? part[t - off] : 0;
+        __syncthreads();
+        part[t] += x;
+        __syncthreads();
+    }
+    long long run = part[t] - acc;
+    for (int s = s0; s < s1; ++s) {
+        cu_out[s] = bad ? 0 : cu_in[s];
+        cu_chunks[s] = bad ? 0 : (int)run;
+        run += ((long long)cu_in[s + 1] - cu_in[s] + kChunk - 1) / kChunk;
+    }
+    if (t == 0) {
+        cu_out[nseq] = bad ? 0 : T;
+        cu_chunks[nseq] = bad ? 0 : (int)part[kPlanThreads - 1];
+        if (bad && err && atomicCAS(&err->code, 0u, (unsigned)GDN_ERR_INVALID_ARG) == 0u)
+            atomicExch(&err->detail, kTagVarlen);
+    }
+    if constexpr (PLAN) {
+        __syncthreads();   // the chunk offsets are complete
+        plan_body(cu_chunks, nseq, H, sms, e_max, pl);
+    }
+}
+
+// The scan of one sequence's pieces on one 16-column tile of the state (a task: a tile, a head
+// and a job -- a sequence cut into three pieces or more, from the plan's job list; at most one
+// CTA of 512 threads per SM, each taking every gridDim.x-th task, so that the whole grid is
+// resident at once and its programmatic dependent launches right away): the state entering
+// piece 1 (written by piece 0's forward), then H_{p+1} = M_p H_p + S_p for p = 1 .. k-2, each
+// written to its slot. fp32 CUDA cores. The
 // product's inner dimension is split over four thread groups of 128 (a 4 x 4 register tile
 // each, rows 4 rb .., columns 4 cb ..), whose partial sums meet in shared memory; M_p sits in
 // shared memory whole (rows padded to 129 floats: the column reads are conflict-free) and the
@@ -214,12 +255,12 @@ constexpr int kRp = 20;    // row pitch of the partial sums (float4 stores witho
 constexpr int kScanSmem = (128 * kScanCols + 128 * kMp) * 4;
 static_assert(4 * 128 * kRp <= 128 * kMp, "the partial sums fit where M was staged");
 
-__global__ void __launch_bounds__(kScanThreads, 1) piece_scan_kernel(const int* __restrict__ seqinfo,
-                                                                     int H,
-                                                                     const float* __restrict__ M,
-                                                                     const float* __restrict__ S,
-                                                                     float* __restrict__ states) {
-    const int s = blockIdx.x, h = blockIdx.y, c0 = blockIdx.z * kScanCols;
+__device__ __forceinline__ void scan_task(const int* __restrict__ seqinfo, int nseq, int H,
+                                          const float* __restrict__ M, const float* __restrict__ S,
+                                          float* __restrict__ states, int task) {
+    constexpr int tiles = 128 / kScanCols;
+    const int c0 = (task % tiles) * kScanCols, h = (task / tiles) % H, job = task / (tiles * H);
+    const int s = seqinfo[3 * nseq + job];
     const int k = seqinfo[3 * s], sig = seqinfo[3 * s + 1], mu = seqinfo[3 * s + 2];
     if (k < 3) return;
     extern __shared__ __align__(16) float smem[];
@@ -298,27 +339,69 @@ __global__ void __launch_bounds__(kScanThreads, 1) piece_scan_kernel(const int* 
     }
 }
 
+__global__ void __launch_bounds__(kScanThreads, 1) piece_scan_kernel(const int* __restrict__ seqinfo,
+                                                                     const int* __restrict__ counts,
+                                                                     int nseq, int H,
+                                                                     const float* __restrict__ M,
+                                                                     const float* __restrict__ S,
+                                                                     float* __restrict__ states) {
+    // launched as the summary grid's programmatic dependent: every CTA waits for the first
+    // phase, so this grid completes after it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int tasks = counts[4] * H * (128 / kScanCols);
+    for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
+        scan_task(seqinfo, nseq, H, M, S, states, task);
+        __syncthreads();   // shared memory is free for the next task
+    }
+    // the second phase's chains may launch once every CTA is here (they wait for this grid
+    // before they read a state): they are placed on a GPU the scan has left, not on the SMs it
+    // leaves idle while it runs (placed there, a few of them ran ~10 % slower, measured)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace
 
 bool pieces_possible(int T, int nseq, int H, int sms) {
     return (long long)nseq * H <= sms && (long long)T >= 2LL * kMinPiece * kChunk;
 }
 
-cudaError_t launch_piece_plan(const int* cu_chunks, int nseq, int H, int sms, int e_max,
-                              const PiecePlan& pl, cudaStream_t s) {
-    piece_plan_kernel<<<1, kPlanThreads, 0, s>>>(cu_chunks, nseq, H, sms, e_max, pl);
+cudaError_t launch_varlen_meta(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
+                               DeviceError* err, cudaStream_t s) {
+    if (!cu_in || !cu_out || !cu_chunks || nseq < 1) return cudaErrorInvalidValue;
+    varlen_meta_kernel<false><<<1, kPlanThreads, 0, s>>>(cu_in, nseq, T, cu_out, cu_chunks, err, 1, 1,
+                                                         1, PiecePlan{});
     return cudaGetLastError();
 }
 
-cudaError_t launch_piece_scan(const int* seqinfo, int nseq, int H, const float* M, const float* S,
-                              float* states, cudaStream_t s) {
-    if (nseq < 1 || H < 1 || H > 65535) return cudaErrorInvalidValue;
+cudaError_t launch_varlen_meta_plan(const int* cu_in, int nseq, int T, int* cu_out, int* cu_chunks,
+                                    DeviceError* err, int H, int sms, int e_max,
+                                    const PiecePlan& pl, cudaStream_t s) {
+    if (!cu_in || !cu_out || !cu_chunks || nseq < 1 || H < 1) return cudaErrorInvalidValue;
+    varlen_meta_kernel<true><<<1, kPlanThreads, 0, s>>>(cu_in, nseq, T, cu_out, cu_chunks, err, H,
+                                                        sms, e_max, pl);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_piece_scan(const PiecePlan& pl, int nseq, int H, int e_max, int sms,
+                              const float* M, const float* S, float* states, cudaStream_t s) {
+    if (nseq < 1 || H < 1 || e_max < 1 || sms < 1) return cudaErrorInvalidValue;
+    // a sequence the scan visits has two entries or more among the e_max
+    const long long tasks = (long long)std::max(1, std::min(nseq, e_max / 2)) * H * (128 / kScanCols);
     const cudaError_t e =
         cudaFuncSetAttribute(piece_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
     if (e != cudaSuccess) return e;
-    piece_scan_kernel<<<dim3((unsigned)nseq, (unsigned)H, 128 / kScanCols), kScanThreads, kScanSmem,
-                        s>>>(seqinfo, H, M, S, states);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)std::min<long long>(tasks, sms));
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.dynamicSmemBytes = kScanSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, piece_scan_kernel, (const int*)pl.seqinfo,
+                              (const int*)pl.counts, nseq, H, M, S, states);
 }
 
 }  // namespace gdn

@@ -132,10 +132,10 @@ def test_varlen_workspace_and_validation(L):
 
     def pieces(nseq, H):
         # the piece plan (tcgen05 shapes): three tables of 8-int entries (nseq, e_max, e_max),
-        # four counts, three ints per sequence, then fp32 states, M and S for e_max = 256 / H
+        # eight counts, four ints per sequence, then fp32 states, M and S for e_max = 256 / H
         # pieces past the first ones
         e = max(1, 256 // H)
-        return (rup(32 * nseq) + 2 * rup(32 * e) + rup(16) + rup(12 * nseq) +
+        return (rup(32 * nseq) + 2 * rup(32 * e) + rup(32) + rup(16 * nseq) +
                 3 * rup(4 * e * H * 128 * 128))
 
     assert L.gdn_varlen_workspace_bytes(ctypes.byref(p), 5) == 256 + wy + 256 + 256 + pieces(5, 16)
