@@ -134,11 +134,12 @@ def algorithmic(w, plan=None, out_bytes: int = 4):
     th_first = BH * first * 64          # token-heads of piece 0
     th_rest = BH * rest * 64            # token-heads of each later piece
     stages = {
-        # per-chunk WY factors (tensor-core path only): reads k, g, beta; writes two bf16
-        # 64 x 64 tiles per chunk. An intermediate of this implementation, not of the method,
-        # so it is left out of the executed total below.
+        # per-chunk WY factors (tensor-core path only): reads k, g, beta; writes the two bf16
+        # 64 x 64 factors without their zero blocks above the diagonal, 10 KiB per chunk. An
+        # intermediate of this implementation, not of the method, so it is left out of the
+        # executed total below.
         "wy": {
-            "bytes": (tok_heads * (K * isz + 2 * isz) + chunks * 16384) if tc else 0,
+            "bytes": (tok_heads * (K * isz + 2 * isz) + chunks * 10240) if tc else 0,
             "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64) if tc else 0,
         },
         # piece 0's forward from h0 (handing its final state on) and the summaries of pieces
@@ -248,7 +249,7 @@ def load_peaks():
 # a traffic record stays valid exactly as long as these files are unchanged.
 KERNEL_SOURCES = {
     "gdn_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
-    "gdn_varlen_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
+    "gdn_varlen_forward": ("gdn_tc.cu", "gdn_tc_common.cuh", "gdn_internal.h", "gdn_varlen.cu"),
     "gdn_wy": ("gdn_wy.cu", "gdn_tc_common.cuh", "gdn_internal.h"),
     "state_grad_kernel": ("gdn_bwd.cu", "gdn_internal.h"),
     "chunk_grad_kernel": ("gdn_bwd_chunk.cu", "gdn_internal.h"),
@@ -352,7 +353,7 @@ def varlen_algorithmic(w, out_bytes: int = 4):
     fwd_flops = (2 * 64 * 64 * K + 2 * 64 * 64 * V + 2 * 64 * 64 * K + 2 * 64 * K * V * 2
                  + 2 * 64 * 64 * K + 2 * 64 * K * V + 2 * 64 * 64 * V)
     return {
-        "wy": {"bytes": tok_heads * (K * isz + 2 * isz) + chunks * 16384,
+        "wy": {"bytes": tok_heads * (K * isz + 2 * isz) + chunks * 10240,
                "flops": chunks * (2 * 64 * 64 * K + 2 * 64 * 64 * 64)},
         "forward": {"bytes": tok_heads * fwd_tok + 2 * states, "flops": chunks * fwd_flops},
     }
@@ -1343,11 +1344,13 @@ def run_reference(args):
 
 
 def record_traffic(csv_path: str, kernel: str, workload: str, command: str, grid=None,
-                   scale_note: str = "", scale=None) -> str:
+                   scale_note: str = "", scale=None, out_dir=None) -> str:
     """Write profiles/traffic_<kernel>_<workload>.txt from an ncu CSV of one capture of the
     kernel (metrics dram__bytes_read.sum and dram__bytes_write.sum; with several launches in
-    the CSV, the one whose grid is `grid`). The record carries the hash of the sources the
-    kernel is built from now, so bench.py trusts it exactly until one of them changes.
+    the CSV, the one whose grid is `grid`, or with grid "sum" the sum over every launch in it:
+    the launches of one call of a stage that runs several). The record carries the hash of the
+    sources the kernel is built from now, so bench.py trusts it exactly until one of them
+    changes.
     scale = (factor, fixed_bytes): per-launch bytes = (captured - fixed) * factor + fixed, for
     a capture of a smaller case of the same kernel."""
     units = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
@@ -1362,19 +1365,28 @@ def record_traffic(csv_path: str, kernel: str, workload: str, command: str, grid
         key = (r.get("ID"), r.get("Kernel Name", ""), r.get("Grid Size", ""))
         v = float(r["Metric Value"].replace(",", "")) * units.get(r.get("Metric Unit", "byte"), 1.0)
         launches.setdefault(key, {})[name] = v
-    picked = [(k, v) for k, v in launches.items() if grid is None or k[2] == grid]
-    if len(picked) != 1:
-        raise SystemExit(f"expected one launch{' with grid ' + grid if grid else ''} in "
-                         f"{csv_path}, found {len(picked)}")
-    (lid, kname, kgrid), v = picked[0]
+    if grid == "sum":
+        if not launches:
+            raise SystemExit(f"no launch in {csv_path}")
+        v = {m: sum(x.get(m, 0.0) for x in launches.values())
+             for m in ("dram__bytes_read.sum", "dram__bytes_write.sum")}
+        kname = " + ".join(f"{k[1].split('(')[0].strip()} grid {k[2]}" for k in launches)
+        kname, kgrid = f"{len(launches)} launches: {kname}", "(one call)"
+    else:
+        picked = [(k, v) for k, v in launches.items() if grid is None or k[2] == grid]
+        if len(picked) != 1:
+            raise SystemExit(f"expected one launch{' with grid ' + grid if grid else ''} in "
+                             f"{csv_path}, found {len(picked)}")
+        (lid, kname, kgrid), v = picked[0]
     captured = v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"]
     per_launch = captured
     if scale is not None:
         factor, fixed = scale
         per_launch = (captured - fixed) * factor + fixed
-    out = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    out = os.path.join(out_dir or os.path.join(ROOT, "profiles"), f"traffic_{kernel}_{workload}.txt")
     with open(out, "w") as f:
-        f.write(f"kernel: {kname.split('(')[0].strip()} grid {kgrid} on {workload}\n")
+        name = kname if grid == "sum" else kname.split('(')[0].strip()
+        f.write(f"kernel: {name} grid {kgrid} on {workload}\n")
         f.write(f"kernel_source_hash: {kernel_source_hash(kernel)}\n")
         f.write(f"dram_bytes_per_launch: {per_launch:.0f}\n")
         f.write(f"captured: dram__bytes_read.sum {v['dram__bytes_read.sum']:.0f} + "
@@ -1414,7 +1426,9 @@ def main(argv=None):
                     help="write profiles/traffic_<--traffic-kernel>_<--workload>.txt from an ncu "
                          "CSV of dram__bytes_read.sum and dram__bytes_write.sum (no GPU needed)")
     ap.add_argument("--traffic-kernel", default="gdn_forward", choices=sorted(KERNEL_SOURCES))
-    ap.add_argument("--traffic-grid", default=None, help='the captured launch\'s grid, e.g. "(128, 1, 1)"')
+    ap.add_argument("--traffic-grid", default=None,
+                    help='the captured launch\'s grid, e.g. "(128, 1, 1)", or "sum": every '
+                         'launch in the CSV (one call of a stage that runs several)')
     ap.add_argument("--traffic-command", default="", help="the command line the CSV came from")
     args = ap.parse_args(argv)
     if args.record_traffic:

@@ -716,8 +716,11 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     ChainParams f1 = c;
     f1.piece_tab = pl.tab1f;
     f1.piece_n = pl.counts;
+    // (the plan keeps each phase within sms / H entries: the summaries and the second phase's
+    // entries are at most that many)
+    const int phase_entries = std::max(1, std::min(w.e_max, sms / p->H));
     ChainParams s1 = c;
-    s1.B = w.e_max;
+    s1.B = phase_entries;
     s1.piece_tab = pl.tab1s;
     s1.piece_n = pl.counts + 1;
     s1.M = Mp;
@@ -736,7 +739,7 @@ gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_se
     //    up while the scan runs and wait for it before they read a state)
     if (mark(stage_events, 3, s) != cudaSuccess) return GDN_ERR_CUDA;
     ChainParams f2 = c;
-    f2.B = w.e_max;
+    f2.B = phase_entries;
     f2.piece_tab = pl.tab2;
     f2.piece_n = pl.counts + 2;
     f2.launch_dependent = 1;

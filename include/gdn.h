@@ -368,9 +368,10 @@ GDN_API gdn_status gdn_varlen_fwd(const gdn_problem* p, int nseq, const int* cu_
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* gdn_varlen_fwd with stage markers: if stage_events is non-NULL it points to five
- * cudaEvent_t recorded on `stream` before the length check, the plan and the WY-factor
- * launches; before the first phase (the whole forward when no sequence is cut); before the
- * scan; before the second phase; and after it. Same results as gdn_varlen_fwd. */
+ * cudaEvent_t recorded on `stream` before the length check (which also makes the plan, when a
+ * cut is possible) and the WY-factor launch; before the first phase (the whole forward when
+ * no sequence is cut); before the scan; before the second phase; and after it. Same results
+ * as gdn_varlen_fwd. */
 GDN_API gdn_status gdn_varlen_fwd_timed(const gdn_problem* p, int nseq, const int* cu_seqlens,
                                         const void* q, const void* k, const void* v,
                                         const void* g, const void* beta, const float* h0,

@@ -70,8 +70,11 @@ def test_algorithmic_model_matches_hand_count():
         t_roof = method["bytes"] / 6791.4e9
         assert 520e-6 < t_roof < 540e-6
         assert method["bytes"] >= tok_heads * 3 // 4 * 516 + tok_heads * (772 + 512)
-        # the WY stage: k, g, beta in, two 8 KiB tiles per chunk out
-        assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 16384
+        # the WY stage: k, g, beta in; per chunk out, two bf16 factors, each 64 x 64 but for
+        # its zero blocks above the diagonal: 16-column slabs of 64, 48, 32 and 16 rows
+        factor = sum(64 - 16 * j for j in range(4)) * 16 * 2
+        assert factor == 5120
+        assert stages["wy"]["bytes"] == tok_heads * 260 + tok_heads // 64 * 2 * factor
         assert executed["bytes"] == sum(stages[k]["bytes"] for k in ("phase1", "scan", "phase2"))
     assert bench.algorithmic(w, (8, 64, 64))[2] == bench.algorithmic(w, (4, 128, 128))[2]
     # the unequal plan the library takes on 152 SMs: piece 0 of 154 chunks, two of 179; only
@@ -190,3 +193,30 @@ def test_backward_piece_rule():
     assert bench.bwd_pieces(synth.scaled(small, T=64 * 12), 152) == 4   # 12 chunks: 2-adic 4
     f32 = synth.scaled(small, in_dtype="f32")     # 32-column tiles: 16 chains
     assert bench.bwd_pieces(f32, 152) == 8
+
+
+def test_record_traffic_one_launch_and_sum(tmp_path):
+    # an ncu CSV of two launches, DRAM read and write bytes of each in the units ncu prints
+    rows = [
+        '"ID","Kernel Name","Grid Size","Metric Name","Metric Unit","Metric Value"',
+        '"0","void k1(P)","(128, 1, 1)","dram__bytes_read.sum","Mbyte","10.5"',
+        '"0","void k1(P)","(128, 1, 1)","dram__bytes_write.sum","byte","2,000"',
+        '"1","void k2(P)","(144, 1, 1)","dram__bytes_read.sum","Kbyte","3"',
+        '"1","void k2(P)","(144, 1, 1)","dram__bytes_write.sum","Gbyte","0.001"',
+    ]
+    csv_path = tmp_path / "t.csv"
+    csv_path.write_text("==PROF== a line ncu prints\n" + "\n".join(rows) + "\n")
+
+    def per_launch(path):
+        return float([ln for ln in open(path) if ln.startswith("dram_bytes_per_launch:")][0]
+                     .split(":")[1])
+
+    one = bench.record_traffic(str(csv_path), "gdn_forward", "w", "cmd", grid="(144, 1, 1)",
+                               out_dir=str(tmp_path))
+    assert per_launch(one) == 3e3 + 1e6
+    both = bench.record_traffic(str(csv_path), "gdn_varlen_forward", "w", "cmd", grid="sum",
+                                out_dir=str(tmp_path))
+    assert per_launch(both) == 10.5e6 + 2000 + 3e3 + 1e6
+    assert "2 launches" in open(both).read()
+    with pytest.raises(SystemExit):   # two launches and no grid: ambiguous
+        bench.record_traffic(str(csv_path), "gdn_forward", "w", "cmd", out_dir=str(tmp_path))
