@@ -31,7 +31,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN segmented fwd tokens/s at H32 K=V=128 T=32K bf16; % of roofline"
-VARLEN_METRIC = "GDN packed-sequence fwd tokens/s (lengths 1800,1500,2000,1200,800) at H16 K=V=128 bf16"
+def varlen_metric(w) -> str:
+    """The packed-sequence line's metric: tokens/s of the forward over these lengths and shapes."""
+    return (f"GDN packed-sequence fwd tokens/s (lengths {','.join(str(n) for n in w.seq_lens)}) "
+            f"at H{w.H} K={w.K} V={w.V} {w.in_dtype}").replace("K=128 V=128", "K=V=128")
 KDA_METRIC = "GDN per-channel-gate (KDA) fwd tokens/s at H16 K=V=128 T=8K bf16"
 STATE_GRAD_METRIC = ("GDN backward state-gradient path tokens/s (segment summaries M, dS_local, "
                      "reverse M^T scan) at H32 K=V=128 T=32K bf16")
@@ -527,7 +530,7 @@ def run_varlen(args):
         cpu = cpu_baseline_varlen(w, x, budget_s=args.cpu_seconds)
     if rank == 0:
         line = {
-            "metric": VARLEN_METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "metric": varlen_metric(w), "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -1291,7 +1294,7 @@ def run_reference_varlen(args, w, x):
     secs = sum(head((args.warmup + i) % w.H) for i in range(args.steps))
     value = w.T * args.steps / w.H / secs   # one step = one head of the packed batch
     line = {
-        "impl": "reference", "metric": VARLEN_METRIC, "value": round(value, 1),
+        "impl": "reference", "metric": varlen_metric(w), "value": round(value, 1),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
