@@ -51,7 +51,7 @@ def _lib():
     gdn.lib()
 
 
-def run_varlen(w, x, decay_first=False, out_dtype=torch.float32, cu=None):
+def run_varlen(w, x, decay_first=False, out_dtype=torch.float32, cu=None, keep_ws=None):
     dt = torch.bfloat16 if w.in_dtype == "bf16" else torch.float32
     d = {n: torch.from_numpy(x[n]).cuda().to(dt).contiguous() for n in ("q", "k", "v", "g", "beta")}
     h0 = None if x["h0"] is None else torch.from_numpy(x["h0"]).cuda().contiguous()
@@ -66,6 +66,8 @@ def run_varlen(w, x, decay_first=False, out_dtype=torch.float32, cu=None):
     gdn.gdn_varlen_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], h0, o, hf, cu_d, ws, prob=prob)
     torch.cuda.synchronize()
     st, detail = gdn.gdn_check_device_error(ws)
+    if keep_ws is not None:
+        keep_ws.append(ws)
     return o, hf, st, detail
 
 
@@ -210,3 +212,70 @@ def test_varlen_cut_full_size_sampled_heads():
         assert rel_err(np64(hf[:, h:h + 1]), hf_ref, label=f"h_final {h}") <= TOL_BF16, h
         a, b = int(cu[0]), int(cu[1])   # the cut sequence on its own scale
         assert rel_err(np64(o[:, a:b, h:h + 1]), o_ref[:, a:b]) <= TOL_BF16, h
+
+
+def expected_plan(lens, H, sms):
+    """The piece plan restated from its rule (the library makes it on the device, in the
+    length-check block): piece lengths X = 8 chunks, then each an eighth longer, below the
+    longest sequence; both phases in one wave of sms // H entries of H chains (A = the pieces
+    past the first ones, one entry per phase each; U = the sequences left whole, one entry in
+    either phase), A at most 256 // H; time 2 X + the most scan steps + 14 chunk times, the
+    smallest (then the shortest X) taken when it beats the longest sequence run whole.
+    Returns the counts (entries of the first phase, summaries, second-phase entries, X, scan
+    jobs) and each sequence's piece count."""
+    n = [(ln + 63) // 64 for ln in lens]
+    cap, e_max, maxn = sms // H, max(1, 256 // H), max(n)
+
+    def pieces(x):
+        return [max(1, -(-m // x)) for m in n]
+
+    best = (maxn, maxn)
+    if len(n) <= cap and len(n) <= 256 and maxn >= 16:
+        x = 8
+        while x < maxn:
+            k = pieces(x)
+            A, U = sum(kk - 1 for kk in k), sum(kk == 1 for kk in k)
+            cost = 2 * x + max(0, max(kk - 2 for kk in k)) + 14
+            if A <= cap and 2 * A + U <= 2 * cap and A <= e_max and (cost, x) < best:
+                best = (cost, x)
+            x += max(1, x // 8)
+    X = best[1]
+    if X >= maxn:
+        return [len(n), 0, 0, maxn, 0], [1] * len(n)
+    k = pieces(X)
+    A, U = sum(kk - 1 for kk in k), sum(kk == 1 for kk in k)
+    room1 = cap - A
+    return [len(n), sum(max(0, kk - 2) for kk in k), A + max(0, U - room1), X,
+            sum(kk >= 3 for kk in k)], k
+
+
+@pytest.mark.parametrize("name", CUT + ("five_scaled",))
+def test_varlen_plan_in_workspace(name):
+    # the plan the call made, read from its workspace (the layout gdn_api.cu gives it: header,
+    # WY tiles, two int arrays of nseq + 1, then the tables of nseq, e_max and e_max 8-int
+    # entries, eight counts, four ints per sequence), against the rule restated above: the
+    # cut cases are cut as their comments say, and a batch too short to pay is not
+    w = CASES[name]
+    x = synth.make_inputs(w)
+    kept = []
+    _, _, st, _ = run_varlen(w, x, keep_ws=kept)
+    assert st == 0
+    ws = kept[0]
+    nseq, H = len(w.seq_lens), w.H
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 256)
+    e_max = max(1, 256 // H)
+
+    def rup(b):
+        return (b + 255) // 256 * 256
+
+    off = 256 + rup(H * (w.T // 64 + nseq) * 10240) + 2 * rup(4 * (nseq + 1))
+    off += rup(32 * nseq) + 2 * rup(32 * e_max)
+    words = ws[off:off + rup(32) + 16 * nseq].cpu().view(torch.int32).numpy()
+    counts, seqinfo = words[:5].tolist(), words[8:8 + 3 * nseq].reshape(nseq, 3)
+    want_counts, want_k = expected_plan(w.seq_lens, H, sms)
+    assert counts == want_counts, (counts, want_counts)
+    assert seqinfo[:, 0].tolist() == want_k
+    if name == "cut_long_first":
+        assert counts[3] == 8 and want_k[0] == 8   # eight pieces of 8 chunks: six scan steps
+    if name == "five_scaled":
+        assert counts[2] == 0 and counts[4] == 0   # nothing cut
