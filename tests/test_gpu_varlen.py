@@ -42,6 +42,9 @@ CASES = {
     "cut_no_initial_state": packed((3200, 900), H=3, h0=False),
 }
 CUT = ("cut_long_first", "cut_ragged", "cut_no_initial_state")
+# planned (T of two 8-chunk pieces or more, every chain in one wave) but too short for a cut to
+# pay: the longest is 18 chunks, the best cut that fits 31 chunk times
+PLANNED_UNCUT = packed((1100, 900, 1000))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -249,13 +252,14 @@ def expected_plan(lens, H, sms):
             sum(kk >= 3 for kk in k)], k
 
 
-@pytest.mark.parametrize("name", CUT + ("five_scaled",))
+@pytest.mark.parametrize("name", CUT + ("planned_uncut",))
 def test_varlen_plan_in_workspace(name):
     # the plan the call made, read from its workspace (the layout gdn_api.cu gives it: header,
     # WY tiles, two int arrays of nseq + 1, then the tables of nseq, e_max and e_max 8-int
-    # entries, eight counts, four ints per sequence), against the rule restated above: the
+    # entries, eight counts, four ints per sequence, each region 256-byte aligned), against
+    # the rule restated above: the
     # cut cases are cut as their comments say, and a batch too short to pay is not
-    w = CASES[name]
+    w = PLANNED_UNCUT if name == "planned_uncut" else CASES[name]
     x = synth.make_inputs(w)
     kept = []
     _, _, st, _ = run_varlen(w, x, keep_ws=kept)
@@ -271,11 +275,15 @@ def test_varlen_plan_in_workspace(name):
     off = 256 + rup(H * (w.T // 64 + nseq) * 10240) + 2 * rup(4 * (nseq + 1))
     off += rup(32 * nseq) + 2 * rup(32 * e_max)
     words = ws[off:off + rup(32) + 16 * nseq].cpu().view(torch.int32).numpy()
-    counts, seqinfo = words[:5].tolist(), words[8:8 + 3 * nseq].reshape(nseq, 3)
+    # (each region 256-byte aligned: the counts take 64 words)
+    counts, seqinfo = words[:5].tolist(), words[64:64 + 3 * nseq].reshape(nseq, 3)
     want_counts, want_k = expected_plan(w.seq_lens, H, sms)
     assert counts == want_counts, (counts, want_counts)
     assert seqinfo[:, 0].tolist() == want_k
     if name == "cut_long_first":
         assert counts[3] == 8 and want_k[0] == 8   # eight pieces of 8 chunks: six scan steps
-    if name == "five_scaled":
-        assert counts[2] == 0 and counts[4] == 0   # nothing cut
+    if name == "planned_uncut":
+        assert counts[2] == 0 and counts[4] == 0 and want_k == [1, 1, 1]   # nothing cut
+        o, hf, _, _ = run_varlen(w, x)   # and the whole sequences are right
+        o_ref, hf_ref = reference(w, x)
+        assert rel_err(np64(o), o_ref) <= TOL_BF16 and rel_err(np64(hf), hf_ref) <= TOL_BF16
