@@ -40,8 +40,12 @@ CASES = {
     "cut_long_first": packed((4096, 100, 300, 64), H=4),
     "cut_ragged": packed((3000, 37, 700), H=2),
     "cut_no_initial_state": packed((3200, 900), H=3, h0=False),
+    # at H = 16 (nine entries of 16 chains per phase on 152 SMs): the first sequence in five
+    # pieces, the next two in two (no summary), two whole ones moved to the second phase, an
+    # empty one last
+    "cut_moved_whole": packed((5000, 1200, 1100, 1000, 900, 800, 700, 0), H=16),
 }
-CUT = ("cut_long_first", "cut_ragged", "cut_no_initial_state")
+CUT = ("cut_long_first", "cut_ragged", "cut_no_initial_state", "cut_moved_whole")
 # planned (T of two 8-chunk pieces or more, every chain in one wave) but too short for a cut to
 # pay: the longest is 18 chunks, the best cut that fits 31 chunk times
 PLANNED_UNCUT = packed((1100, 900, 1000))
@@ -282,6 +286,8 @@ def test_varlen_plan_in_workspace(name):
     assert seqinfo[:, 0].tolist() == want_k
     if name == "cut_long_first":
         assert counts[3] == 8 and want_k[0] == 8   # eight pieces of 8 chunks: six scan steps
+    if name == "cut_moved_whole" and sms == 152:
+        assert want_k == [5, 2, 2, 1, 1, 1, 1, 1] and counts[2] == 8   # 6 pieces + 2 whole
     if name == "planned_uncut":
         assert counts[2] == 0 and counts[4] == 0 and want_k == [1, 1, 1]   # nothing cut
         o, hf, _, _ = run_varlen(w, x)   # and the whole sequences are right
