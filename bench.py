@@ -497,7 +497,9 @@ def run_varlen(args):
     stages = varlen_algorithmic(w)
     sms = min(torch.cuda.get_device_properties(dev).multi_processor_count, 256)
     cut_possible = nseq * w.H <= sms and w.T >= 2 * 8 * 64   # gdn_varlen.cu: pieces_possible
-    launches = 7 if (cut_possible and w.in_dtype == "bf16" and w.K == 128 and not w.gate_k) else 3
+    # the length check (with the plan), the WY tiles, the first phase's forwards, the piece
+    # summaries, the scan and the second phase; without a possible cut: check, WY, forward
+    launches = 6 if (cut_possible and w.in_dtype == "bf16" and w.K == 128 and not w.gate_k) else 3
     peaks, peaks_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     ach = stages["forward"]["bytes"] / (avg["forward"] * 1e-3) / 1e9
