@@ -8,16 +8,16 @@
 // first phase runs piece 0's forward from the sequence's initial state beside the summaries
 // of pieces 1 .. k-2, the scan composes those from the state piece 0 ends in, and the second
 // phase runs the forwards of pieces 1 .. k-1 from the scanned states. The lengths live on the
-// device, so the plan is made there, by one CTA, before the chains run; the chain grids are
-// launched with a bound on their entries and the chains past the plan's count return at once.
+// device, so the plan is made there, by the block that checks them, right after the check and
+// before the WY tiles and the chains; the chain grids are launched with a bound on their
+// entries and the chains past the plan's count return at once.
 //
-// The plan: the smallest piece length X (at least kMinPiece chunks) at which both phases fit
-// in one wave -- with k_s = ceil(n_s / X), A = sum over the cut sequences of k_s - 1 entries in
-// each phase and one entry, in either phase, per sequence left whole; an entry is H chains --
-// and, among those X, the one with the shortest two phases and scan (2 X chunk times, plus the
-// scan's steps, which run in sequence for each sequence, and the fixed cost of a second phase
-// and the plan), taken when that beats the longest sequence run whole; otherwise every
-// sequence runs whole (as before).
+// The plan: among the piece lengths X (kMinPiece chunks, then each an eighth longer) at which
+// both phases fit in one wave -- with k_s = ceil(n_s / X), A = sum over the cut sequences of
+// k_s - 1 entries in each phase and one entry, in either phase, per sequence left whole; an
+// entry is H chains -- the one with the shortest two phases and scan (2 X chunk times, plus
+// the scan's steps, which run in sequence for each sequence, and the fixed cost of a cut),
+// taken when that beats the longest sequence run whole; otherwise every sequence runs whole.
 // The pieces of a sequence are ceil(n_s / k_s) chunks each, the last one the rest; a sequence
 // left whole runs in the first phase while it has room, else in the second.
 #include <algorithm>
